@@ -1,0 +1,196 @@
+"""fp64 CPU oracle of the MegaMoE expert path -- TEST INFRASTRUCTURE ONLY.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and the cpu_baseline / reference
+legs of ``bench.py`` may import this package. The product library never loads
+it. It wraps ``moe_oracle.c`` (plain C, fp64, OpenMP over tokens) through
+ctypes; see that file for the definitions and the page sections they follow.
+
+Inputs are torch tensors or numpy arrays. bf16 tensors are passed by their bit
+patterns, so the oracle sees their exact values.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+from dataclasses import dataclass
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+SOURCE = os.path.join(_HERE, "moe_oracle.c")
+_LIB_PATH = os.path.join(_HERE, "liboracle.so")
+_lock = threading.Lock()
+_default = None
+
+
+def compile_source(src: str, out: str) -> str:
+    """gcc -O2 -fopenmp: compile one oracle C source into a shared library."""
+    tmp = out + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-O2", "-std=c99", "-fopenmp", "-fPIC", "-shared", src, "-o", tmp, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, out)
+    return out
+
+
+def build(force: bool = False) -> str:
+    """Compile moe_oracle.c into oracle/liboracle.so unless it is up to date."""
+    if (not force and os.path.exists(_LIB_PATH)
+            and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(SOURCE)):
+        return _LIB_PATH
+    return compile_source(SOURCE, _LIB_PATH)
+
+
+def _bind(lib):
+    i64, i32, f64 = ctypes.c_int64, ctypes.c_int32, ctypes.c_double
+    vp = ctypes.c_void_p
+    lib.oracle_router.argtypes = [i64, i64, i64, i32, vp, vp, vp, vp, i32, i32, f64,
+                                  i32, i32, i32, vp, vp, vp, vp, vp, vp]
+    lib.oracle_router.restype = ctypes.c_int
+    lib.oracle_routing_metadata.argtypes = [i64, i32, i64, vp, vp, vp, vp, vp]
+    lib.oracle_routing_metadata.restype = ctypes.c_int64
+    lib.oracle_expert_forward.argtypes = [i64, i64, i64, i64, i32, vp, vp, vp, vp, vp,
+                                          vp, vp, vp]
+    lib.oracle_expert_forward.restype = ctypes.c_int
+    lib.oracle_num_threads.argtypes = []
+    lib.oracle_num_threads.restype = ctypes.c_int
+    return lib
+
+
+def _np(a, dtype=None):
+    """Host numpy copy of a torch tensor / array; bf16 comes back as uint16 bits."""
+    try:
+        import torch
+        if isinstance(a, torch.Tensor):
+            a = a.detach().cpu().contiguous()
+            if a.dtype == torch.bfloat16:
+                a = a.view(torch.int16).numpy().view(np.uint16)
+            else:
+                a = a.numpy()
+    except ImportError:  # pragma: no cover
+        pass
+    a = np.ascontiguousarray(a)
+    if dtype is not None and a.dtype != dtype:
+        a = np.ascontiguousarray(a.astype(dtype))
+    return a
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+@dataclass
+class RouterResult:
+    topk_idx: np.ndarray    # int32 [T, k], best first
+    topk_w: np.ndarray      # float64 [T, k]
+    scores: np.ndarray      # float64 [T, E], softmax or sigmoid of the logits
+    sel_gap: np.ndarray     # float64 [T], k-th minus (k+1)-th selection score
+    group_gap: np.ndarray   # float64 [T], same for groups (+inf without groups)
+    aux: float
+
+
+@dataclass
+class Metadata:
+    counts: np.ndarray     # int32 [E]
+    offsets: np.ndarray    # int32 [E+1]
+    perm_slot: np.ndarray  # int32 [offsets[E]]
+    row_of: np.ndarray     # int32 [T*k], -1 for dropped slots
+    dropped: int
+
+
+class Oracle:
+    """One loaded oracle library (the shipped one, or a test's compiled variant)."""
+
+    def __init__(self, lib_path: str):
+        self.path = lib_path
+        self.lib = _bind(ctypes.CDLL(lib_path))
+
+    def num_threads(self) -> int:
+        return int(self.lib.oracle_num_threads())
+
+    def router(self, x, w_r, k, *, score="softmax", normalize=True, scale=1.0, n_group=1,
+               topk_group=1, group_topn=2, logit_offset=None, sel_bias=None) -> RouterResult:
+        """Scores, (group-limited) top-k, weights and aux for every token of x."""
+        xb = _np(x)
+        assert xb.dtype == np.uint16, "x must be bf16"
+        wr = _np(w_r, np.float32)
+        T, H = xb.shape
+        E = wr.shape[0]
+        off = None if logit_offset is None else _np(logit_offset, np.float32)
+        bias = None if sel_bias is None else _np(sel_bias, np.float32)
+        idx = np.empty((T, k), np.int32)
+        w = np.empty((T, k), np.float64)
+        s = np.empty((T, E), np.float64)
+        sg = np.empty((T,), np.float64)
+        gg = np.empty((T,), np.float64)
+        aux = np.zeros((1,), np.float64)
+        rc = self.lib.oracle_router(T, H, E, k, _ptr(xb), _ptr(wr), _ptr(off), _ptr(bias),
+                                    0 if score == "softmax" else 1, int(bool(normalize)),
+                                    float(scale), int(n_group), int(topk_group), int(group_topn),
+                                    _ptr(idx), _ptr(w), _ptr(s), _ptr(sg), _ptr(gg), _ptr(aux))
+        if rc != 0:
+            raise ValueError("oracle_router rejected its arguments")
+        return RouterResult(idx, w, s, sg, gg, float(aux[0]))
+
+    def routing_metadata(self, topk_idx, E) -> Metadata:
+        """Per-expert counts, offsets and the stable slot permutation."""
+        idx = _np(topk_idx, np.int32)
+        T, k = idx.shape
+        counts = np.empty((E,), np.int32)
+        offsets = np.empty((E + 1,), np.int32)
+        perm = np.empty((T * k,), np.int32)
+        row_of = np.empty((T * k,), np.int32)
+        dropped = self.lib.oracle_routing_metadata(T, k, E, _ptr(idx), _ptr(counts),
+                                                   _ptr(offsets), _ptr(perm), _ptr(row_of))
+        return Metadata(counts, offsets, perm[: offsets[E]].copy(), row_of, int(dropped))
+
+    def expert_forward(self, x, topk_idx, topk_w, w1, w2, *, want_a=False, want_o=False):
+        """y [T, H] float64 (and optionally a / o per slot) for the given routing."""
+        xb = _np(x)
+        w1b = _np(w1)
+        w2b = _np(w2)
+        assert xb.dtype == np.uint16 and w1b.dtype == np.uint16 and w2b.dtype == np.uint16
+        idx = _np(topk_idx, np.int32)
+        w = _np(topk_w, np.float64)
+        T, H = xb.shape
+        E, twoI, H1 = w1b.shape
+        I = twoI // 2
+        assert H1 == H and w2b.shape == (E, H, I)
+        assert idx.shape == w.shape and idx.shape[0] == T
+        k = idx.shape[1]
+        y = np.empty((T, H), np.float64)
+        a = np.empty((T * k, I), np.float64) if want_a else None
+        o = np.empty((T * k, H), np.float64) if want_o else None
+        rc = self.lib.oracle_expert_forward(T, H, I, E, k, _ptr(xb), _ptr(idx), _ptr(w),
+                                            _ptr(w1b), _ptr(w2b), _ptr(y), _ptr(a), _ptr(o))
+        if rc != 0:
+            raise ValueError("oracle_expert_forward rejected its arguments")
+        if want_a or want_o:
+            return y, a, o
+        return y
+
+
+def default() -> Oracle:
+    """The oracle built from moe_oracle.c (compiled on first use)."""
+    global _default
+    with _lock:
+        if _default is None:
+            _default = Oracle(build())
+    return _default
+
+
+def router(*args, **kwargs) -> RouterResult:
+    return default().router(*args, **kwargs)
+
+
+def routing_metadata(*args, **kwargs) -> Metadata:
+    return default().routing_metadata(*args, **kwargs)
+
+
+def expert_forward(*args, **kwargs):
+    return default().expert_forward(*args, **kwargs)
+
+
+def num_threads() -> int:
+    return default().num_threads()

@@ -1,0 +1,355 @@
+/*
+ * moe_oracle.c -- plain fp64 CPU oracle of the MegaMoE expert path.
+ *
+ * TEST INFRASTRUCTURE ONLY. The only code allowed to load or run this library
+ * is tests/, __graft_entry__.smoke() and the cpu_baseline / reference legs of
+ * bench.py. The product library (libmoe) never links, loads or calls it, and
+ * the two share no source: no headers, helpers, tables or constants.
+ *
+ * What it computes. The MegaMoE guide (opening section "MegaMoE") describes
+ * the expert path as a fused router (score function, group-limited top-k and
+ * an aux load-balance score) followed by dispatch -> L1 grouped GEMM ->
+ * SwiGLU -> L2 grouped GEMM -> top-k-weighted combine. Its section "Design:
+ * two stages + weight modules" fixes the weight shapes: w1 [g, 2I, H] holding
+ * the gate rows then the up rows, and w2 [g, H, I]. The SwiGLU is
+ * silu(gate) * up, the form named in the "GDN <-> FLA Parity in Primus" page,
+ * section B (Megatron-LM behavioural patches, the fla_swiglu row).
+ *
+ * With one device, dispatch and combine are a gather and a weighted sum, so
+ * the exact result has a plain per-token definition:
+ *
+ *     y_t = sum_{e in K_t} w_{t,e} * W2_e ( silu(W1g_e x_t) (.) (W1u_e x_t) )
+ *
+ * This file evaluates exactly that, token by token, in double, from the exact
+ * values of the bf16 / fp32 inputs. It uses no permutation, no tiling, no
+ * blocking and no reordering of the arithmetic beyond the definition.
+ *
+ * Readings where the pages are silent (each one is listed in the design notes):
+ *   - the gate is rows [0, I) of w1[e] and the up projection rows [I, 2I);
+ *   - top-k ties go to the lower expert index, group ties to the lower group;
+ *   - the selection bias (sel_bias) enters only the selection and the group
+ *     scores, never the weights;
+ *   - aux = E * sum_e f_e * P_e with f_e = c_e / (T k) and
+ *     P_e = (1/T) sum_t s_{t,e} over the full score vector.
+ *
+ * Parity status: every exported function is pinned by tests that do not call
+ * the function's own formula again (closed forms of hand-built examples, the
+ * even round-robin routing of the guide's force-load-balancing table, a dense
+ * SwiGLU MLP in an independent library, brute force and invariants). The aux
+ * value for sigmoid scoring has no pin beyond its definition: parity unpinned.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+/* Exact value of a bf16 bit pattern: the top 16 bits of an IEEE float. */
+static double bf16_value(uint16_t bits) {
+    uint32_t u = ((uint32_t)bits) << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return (double)f;
+}
+
+static double silu(double z) { return z / (1.0 + exp(-z)); }
+
+int oracle_num_threads(void) {
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
+
+/*
+ * Index of the largest v[i] among i in [0, n) with ok[i] != 0; on equal values
+ * the lower index wins (scan in ascending order with a strict comparison).
+ * Returns -1 when no index is eligible.
+ */
+static int64_t argmax_eligible(const double *v, const unsigned char *ok, int64_t n) {
+    int64_t best = -1;
+    for (int64_t i = 0; i < n; ++i) {
+        if (!ok[i]) continue;
+        if (best < 0 || v[i] > v[best]) best = i;
+    }
+    return best;
+}
+
+/*
+ * Router for one token (MegaMoE opening section: "score function +
+ * group-limited top-k + aux score").
+ *
+ *   l_e   = sum_h x_h * Wr[e,h]  (+ logit_offset[e] when given)
+ *   s     = softmax(l) (score_fn 0) or sigmoid(l) elementwise (score_fn 1)
+ *   sel_e = s_e + sel_bias[e]    (bias only steers the selection)
+ *   with n_group > 1: group g holds experts [g*E/n_group, (g+1)*E/n_group);
+ *     its score is the sum of its group_topn largest sel values; the
+ *     topk_group best groups stay eligible, the rest are masked out
+ *   K     = the k eligible experts with the largest sel, best first
+ *   w_j   = s_{K_j}, divided by sum_j s_{K_j} when normalize, times scale
+ *
+ * sel_gap is sel of the k-th choice minus sel of the best unchosen eligible
+ * expert (+inf when none is left); group_gap is the same for groups.
+ */
+static void route_one_token(int64_t H, int64_t E, int32_t k,
+                            const uint16_t *x_t, const float *w_r,
+                            const float *logit_offset, const float *sel_bias,
+                            int32_t score_fn, int32_t normalize, double scale,
+                            int32_t n_group, int32_t topk_group, int32_t group_topn,
+                            double *s, double *sel, double *gscore,
+                            unsigned char *ok, unsigned char *gok,
+                            int32_t *idx_out, double *w_out,
+                            double *sel_gap_out, double *group_gap_out) {
+    /* logits and scores */
+    for (int64_t e = 0; e < E; ++e) {
+        double l = 0.0;
+        for (int64_t h = 0; h < H; ++h) l += bf16_value(x_t[h]) * (double)w_r[e * H + h];
+        if (logit_offset) l += (double)logit_offset[e];
+        s[e] = l;
+    }
+    if (score_fn == 0) {
+        double m = s[0];
+        for (int64_t e = 1; e < E; ++e) if (s[e] > m) m = s[e];
+        double z = 0.0;
+        for (int64_t e = 0; e < E; ++e) { s[e] = exp(s[e] - m); z += s[e]; }
+        for (int64_t e = 0; e < E; ++e) s[e] /= z;
+    } else {
+        for (int64_t e = 0; e < E; ++e) s[e] = 1.0 / (1.0 + exp(-s[e]));
+    }
+    for (int64_t e = 0; e < E; ++e) sel[e] = s[e] + (sel_bias ? (double)sel_bias[e] : 0.0);
+
+    /* group limit */
+    for (int64_t e = 0; e < E; ++e) ok[e] = 1;
+    double group_gap = INFINITY;
+    if (n_group > 1) {
+        int64_t gs = E / n_group;
+        for (int32_t g = 0; g < n_group; ++g) {
+            /* sum of the group_topn largest sel values of group g */
+            unsigned char *left = ok + g * gs; /* reused as scratch, reset below */
+            double sum = 0.0;
+            for (int32_t n = 0; n < group_topn && n < gs; ++n) {
+                int64_t b = argmax_eligible(sel + g * gs, left, gs);
+                sum += sel[g * gs + b];
+                left[b] = 0;
+            }
+            for (int64_t i = 0; i < gs; ++i) left[i] = 1;
+            gscore[g] = sum;
+        }
+        for (int32_t g = 0; g < n_group; ++g) gok[g] = 1;
+        unsigned char kept[1024];
+        for (int32_t g = 0; g < n_group; ++g) kept[g] = 0;
+        for (int32_t n = 0; n < topk_group; ++n) {
+            int64_t b = argmax_eligible(gscore, gok, n_group);
+            kept[b] = 1;
+            gok[b] = 0;
+        }
+        int64_t nb = argmax_eligible(gscore, gok, n_group);
+        if (nb >= 0) {
+            double worst_kept = INFINITY;
+            for (int32_t g = 0; g < n_group; ++g)
+                if (kept[g] && gscore[g] < worst_kept) worst_kept = gscore[g];
+            group_gap = worst_kept - gscore[nb];
+        }
+        for (int64_t e = 0; e < E; ++e) ok[e] = kept[e / gs];
+    }
+
+    /* top-k of sel among the eligible experts */
+    double chosen_sum = 0.0;
+    for (int32_t j = 0; j < k; ++j) {
+        int64_t b = argmax_eligible(sel, ok, E);
+        idx_out[j] = (int32_t)b;
+        ok[b] = 0;
+        w_out[j] = s[b];
+        chosen_sum += s[b];
+    }
+    int64_t next = argmax_eligible(sel, ok, E);
+    double sel_gap = INFINITY;
+    if (next >= 0) sel_gap = sel[idx_out[k - 1]] - sel[next];
+    for (int32_t j = 0; j < k; ++j) {
+        if (normalize) w_out[j] /= chosen_sum;
+        w_out[j] *= scale;
+    }
+    if (sel_gap_out) *sel_gap_out = sel_gap;
+    if (group_gap_out) *group_gap_out = group_gap;
+}
+
+/*
+ * Router over T tokens, plus the aux load-balance value (MegaMoE opening
+ * section: the aux loss is computed internally and returned; section
+ * "Configuration": only the standard aux loss is supported).
+ *
+ *   aux = E * sum_e (c_e / (T k)) * ((1/T) sum_t s_{t,e})
+ *
+ * Returns 0, or -1 on an invalid argument.
+ */
+int oracle_router(int64_t T, int64_t H, int64_t E, int32_t k,
+                  const uint16_t *x, const float *w_r,
+                  const float *logit_offset, const float *sel_bias,
+                  int32_t score_fn, int32_t normalize, double scale,
+                  int32_t n_group, int32_t topk_group, int32_t group_topn,
+                  int32_t *topk_idx, double *topk_w,
+                  double *scores, double *sel_gap, double *group_gap,
+                  double *aux) {
+    if (T < 0 || H <= 0 || E <= 0 || k <= 0 || k > E || !x || !w_r || !topk_idx || !topk_w)
+        return -1;
+    if (n_group > 1 && (E % n_group != 0 || topk_group <= 0 || topk_group > n_group ||
+                        n_group > 1024 || group_topn <= 0))
+        return -1;
+    if (n_group > 1 && (int64_t)topk_group * (E / n_group) < k) return -1;
+
+    double *all_s = (double *)malloc(sizeof(double) * (size_t)(T > 0 ? T : 1) * (size_t)E);
+    if (!all_s) return -1;
+    int bad = 0;
+#pragma omp parallel
+    {
+        double *sel = (double *)malloc(sizeof(double) * (size_t)E);
+        double *gscore = (double *)malloc(sizeof(double) * 1024);
+        unsigned char *ok = (unsigned char *)malloc((size_t)E);
+        unsigned char *gok = (unsigned char *)malloc(1024);
+        if (!sel || !gscore || !ok || !gok) {
+#pragma omp atomic write
+            bad = 1;
+        } else {
+#pragma omp for schedule(dynamic, 4)
+            for (int64_t t = 0; t < T; ++t) {
+                route_one_token(H, E, k, x + t * H, w_r, logit_offset, sel_bias,
+                                score_fn, normalize, scale, n_group, topk_group, group_topn,
+                                all_s + t * E, sel, gscore, ok, gok,
+                                topk_idx + t * k, topk_w + t * k,
+                                sel_gap ? sel_gap + t : NULL, group_gap ? group_gap + t : NULL);
+            }
+        }
+        free(sel); free(gscore); free(ok); free(gok);
+    }
+    if (bad) { free(all_s); return -1; }
+
+    if (scores) memcpy(scores, all_s, sizeof(double) * (size_t)T * (size_t)E);
+    if (aux) {
+        double a = 0.0;
+        for (int64_t e = 0; e < E; ++e) {
+            int64_t c = 0;
+            for (int64_t i = 0; i < T * k; ++i) if (topk_idx[i] == e) ++c;
+            double p = 0.0;
+            for (int64_t t = 0; t < T; ++t) p += all_s[t * E + e];
+            double f = (T > 0) ? (double)c / ((double)T * (double)k) : 0.0;
+            double P = (T > 0) ? p / (double)T : 0.0;
+            a += f * P;
+        }
+        *aux = (double)E * a;
+    }
+    free(all_s);
+    return 0;
+}
+
+/*
+ * Routing metadata for one device (expert parallelism 1): the local stand-in
+ * for the dispatch all-to-all (MegaMoE opening section, dispatch_grouped_gemm).
+ *
+ *   counts[e]     number of slots (t, j) with topk_idx[t*k + j] == e
+ *   offsets[e]    exclusive prefix sum of counts; offsets[E] = routed rows
+ *   perm_slot[r]  flat slot index t*k + j of routed row r; rows of expert e
+ *                 are offsets[e] .. offsets[e+1]-1 in increasing slot order
+ *   row_of[s]     routed row of slot s, or -1 if its index is outside [0, E)
+ *
+ * Written as a direct scan per expert so that stability is evident.
+ * Returns the number of slots dropped for an out-of-range index.
+ */
+int64_t oracle_routing_metadata(int64_t T, int32_t k, int64_t E, const int32_t *topk_idx,
+                                int32_t *counts, int32_t *offsets,
+                                int32_t *perm_slot, int32_t *row_of) {
+    int64_t R = T * k;
+    int64_t dropped = 0;
+    for (int64_t e = 0; e < E; ++e) counts[e] = 0;
+    for (int64_t s = 0; s < R; ++s) {
+        int32_t e = topk_idx[s];
+        if (e >= 0 && e < E) counts[e] += 1; else ++dropped;
+        row_of[s] = -1;
+    }
+    offsets[0] = 0;
+    for (int64_t e = 0; e < E; ++e) offsets[e + 1] = offsets[e] + counts[e];
+    for (int64_t e = 0; e < E; ++e) {
+        int32_t r = offsets[e];
+        for (int64_t s = 0; s < R; ++s) {
+            if (topk_idx[s] != e) continue;
+            perm_slot[r] = (int32_t)s;
+            row_of[s] = r;
+            ++r;
+        }
+    }
+    return dropped;
+}
+
+/*
+ * Expert path forward, token by token (MegaMoE opening section:
+ * dispatch_grouped_gemm -> SwiGLU -> grouped_gemm_combine).
+ *
+ *   for each token t and choice j with e = topk_idx[t,j] in [0, E):
+ *     g_i = sum_h w1[e, i, h]     x[t, h]        i in [0, I)   (gate rows)
+ *     u_i = sum_h w1[e, I + i, h] x[t, h]                      (up rows)
+ *     a_i = silu(g_i) * u_i
+ *     o_h = sum_i w2[e, h, i] a_i
+ *     y[t, h] += topk_w[t, j] * o_h
+ *
+ * Slots with an index outside [0, E) contribute nothing. a_slot, when given,
+ * receives a for every slot in flat slot order [T*k, I] (zero for dropped
+ * slots); o_slot likewise receives the unweighted o rows [T*k, H].
+ */
+int oracle_expert_forward(int64_t T, int64_t H, int64_t I, int64_t E, int32_t k,
+                          const uint16_t *x, const int32_t *topk_idx, const double *topk_w,
+                          const uint16_t *w1, const uint16_t *w2,
+                          double *y, double *a_slot, double *o_slot) {
+    if (T < 0 || H <= 0 || I <= 0 || E <= 0 || k <= 0 || !x || !topk_idx || !topk_w ||
+        !w1 || !w2 || !y)
+        return -1;
+    int bad = 0;
+#pragma omp parallel
+    {
+        double *xt = (double *)malloc(sizeof(double) * (size_t)H);
+        double *a = (double *)malloc(sizeof(double) * (size_t)I);
+        double *o = (double *)malloc(sizeof(double) * (size_t)H);
+        if (!xt || !a || !o) {
+#pragma omp atomic write
+            bad = 1;
+        } else {
+#pragma omp for schedule(dynamic, 1)
+            for (int64_t t = 0; t < T; ++t) {
+                double *yt = y + t * H;
+                for (int64_t h = 0; h < H; ++h) { yt[h] = 0.0; xt[h] = bf16_value(x[t * H + h]); }
+                for (int32_t j = 0; j < k; ++j) {
+                    int64_t slot = t * k + j;
+                    int32_t e = topk_idx[slot];
+                    if (e < 0 || e >= E) {
+                        if (a_slot) for (int64_t i = 0; i < I; ++i) a_slot[slot * I + i] = 0.0;
+                        if (o_slot) for (int64_t h = 0; h < H; ++h) o_slot[slot * H + h] = 0.0;
+                        continue;
+                    }
+                    const uint16_t *W1 = w1 + (int64_t)e * 2 * I * H;
+                    const uint16_t *W2 = w2 + (int64_t)e * H * I;
+                    for (int64_t i = 0; i < I; ++i) {
+                        double g = 0.0, u = 0.0;
+                        for (int64_t h = 0; h < H; ++h) {
+                            g += bf16_value(W1[i * H + h]) * xt[h];
+                            u += bf16_value(W1[(I + i) * H + h]) * xt[h];
+                        }
+                        a[i] = silu(g) * u;
+                        if (a_slot) a_slot[slot * I + i] = a[i];
+                    }
+                    for (int64_t h = 0; h < H; ++h) {
+                        double acc = 0.0;
+                        for (int64_t i = 0; i < I; ++i) acc += bf16_value(W2[h * I + i]) * a[i];
+                        o[h] = acc;
+                        if (o_slot) o_slot[slot * H + h] = acc;
+                    }
+                    double w = topk_w[slot];
+                    for (int64_t h = 0; h < H; ++h) yt[h] += w * o[h];
+                }
+            }
+        }
+        free(xt); free(a); free(o);
+    }
+    return bad ? -1 : 0;
+}
