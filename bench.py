@@ -1,0 +1,417 @@
+"""Benchmark of the MoE expert path (router -> routing metadata -> stage 1 ->
+stage 2) through the C ABI of libmoe on one or more GPUs of one node.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+                    [--impl ours|reference] [--no-cpu-baseline]
+
+A step is one pass of the whole path over one batch of seeded synthetic
+inputs already resident in HBM. Each rank runs its own independent replica
+(the path has no exchange step at expert parallelism 1), so scaling is weak.
+Rank 0 prints one JSON line.
+
+--impl reference times the fp64 CPU oracle on the host cores instead (each
+step a bounded sample of the same workload); under torchrun only rank 0 runs it.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from moe_expert_router_gb300.workloads import CONFIGS, generate  # noqa: E402
+
+METRIC = "MoE expert-path TFLOP/s and tokens/s (1 GB300) and fraction of bf16/HBM roofline"
+L2_FLUSH_BYTES = 256 << 20
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return {"hbm_gbs": float(d["hbm_gbs"]), "bf16_tflops": float(d["bf16_tflops"]),
+                "bf16_tflops_sustained": float(d.get("bf16_tflops_sustained", d["bf16_tflops"])),
+                "source": "measured"}
+    except (OSError, KeyError, ValueError):
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+                "source": "fallback"}
+
+
+# ---------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples taken while the timed region runs."""
+
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self.t0 = self.t1 = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self._reader = threading.Thread(target=self._read, daemon=True)
+        self._reader.start()
+        time.sleep(0.3)
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def mark_begin(self):
+        self.t0 = time.time()
+
+    def mark_end(self):
+        self.t1 = time.time()
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"],
+                    "samples": 0}
+        time.sleep(0.12)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        for ts, line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 10:
+                continue
+            rows.append((ts, parts))
+        inside = [r for r in rows if self.t0 is not None and self.t0 - 0.06 <= r[0] <= self.t1 + 0.06]
+        use = inside if inside else rows[-3:]
+        sm = [float(p[2]) for _, p in use if p[2].replace(".", "").isdigit()]
+        mx = [float(p[3]) for _, p in use if p[3].replace(".", "").isdigit()]
+        reasons = set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for _, p in use:
+            for name, v in zip(names, p[6:10]):
+                if v.lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(inside),
+                "window": "timed region" if inside else "nearest samples (timed region shorter than the sampling period)"}
+
+
+# ---------------------------------------------------------------- our arm
+
+def bytes_and_flops(cfg, counts):
+    """Algorithmic flops and bytes per stage (bytes the kernels could avoid are not counted)."""
+    R, H, I, T, E = cfg.R, cfg.H, cfg.I, cfg.T, cfg.E
+    active = int((counts > 0).sum())
+    return {
+        "gemm1": {"flops": 4.0 * R * H * I,
+                  "bytes": 4.0 * H * I * active + 2.0 * T * H + 2.0 * R * I},
+        "gemm2": {"flops": 2.0 * R * H * I,
+                  "bytes": 2.0 * H * I * active + 2.0 * R * I + 2.0 * T * H},
+        "active_experts": active,
+    }
+
+
+def run_ours(args, cfg, rank, world, local_rank):
+    from moe_expert_router_gb300 import binding as B
+    from moe_expert_router_gb300 import build as moe_build
+
+    moe_build.build()
+    B.load()
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    inp = generate(cfg, seed=rank, device=dev)
+    shp = B.shape(cfg.T, cfg.H, cfg.I, cfg.E, cfg.k)
+    ws = B.new_workspace(shp, dev)
+    rcfg = B.router_cfg(cfg.score, cfg.normalize, cfg.scale, cfg.n_group, cfg.topk_group,
+                        cfg.group_topn)
+    idx = torch.empty((cfg.T, cfg.k), dtype=torch.int32, device=dev)
+    w = torch.empty((cfg.T, cfg.k), dtype=torch.float32, device=dev)
+    aux = torch.zeros((1,), dtype=torch.float32, device=dev)
+    a = torch.empty((cfg.R, cfg.I), dtype=torch.bfloat16, device=dev)
+    y = torch.empty((cfg.T, cfg.H), dtype=torch.bfloat16, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    x_dev = inp["x"]
+
+    names = ["router", "metadata", "gemm1", "gemm2_combine"]
+
+    def step(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        B.moe_router(x_dev, inp["w_r"], shp, rcfg, idx, w, ws, aux=aux,
+                     logit_offset=inp["logit_offset"], sel_bias=inp["sel_bias"])
+        if ev is not None:
+            ev[1].record(stream)
+        B.moe_routing_metadata(idx, shp, ws)
+        if ev is not None:
+            ev[2].record(stream)
+        B.moe_dispatch_gemm1(x_dev, inp["w1"], shp, a, ws)
+        if ev is not None:
+            ev[3].record(stream)
+        B.moe_swiglu_gemm2_combine(a, w, inp["w2"], shp, y, ws)
+        if ev is not None:
+            ev[4].record(stream)
+
+    for _ in range(args.warmup):
+        flush.fill_(1)
+        step()
+    torch.cuda.synchronize(dev)
+    err = B.moe_get_device_error(ws)
+    if err:
+        raise RuntimeError(f"device error word {err:#x} after warm-up")
+
+    events = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    sampler = ClockSampler(local_rank) if rank == 0 else None
+    if sampler:
+        sampler.start()
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize(dev)
+    launches0 = B.moe_kernel_launch_count()
+    if sampler:
+        sampler.mark_begin()
+    t_wall0 = time.perf_counter()
+    for i in range(args.steps):
+        flush.fill_(i & 0xFF)           # evict L2 between steps (outside the step's events)
+        step(events[i])
+    torch.cuda.synchronize(dev)
+    t_wall = time.perf_counter() - t_wall0
+    if sampler:
+        sampler.mark_end()
+    if world > 1:
+        torch.distributed.barrier()
+    launches = B.moe_kernel_launch_count() - launches0
+    clocks = sampler.stop() if sampler else None
+
+    stage_ms = {n: [] for n in names}
+    step_ms = []
+    for ev in events:
+        for j, n in enumerate(names):
+            stage_ms[n].append(ev[j].elapsed_time(ev[j + 1]))
+        step_ms.append(ev[0].elapsed_time(ev[4]))
+    total_ms = sum(step_ms)
+
+    # metadata for the algorithmic byte counts
+    L = B.moe_workspace_layout(shp)
+    counts = ws[L.counts:L.counts + 4 * cfg.E].view(torch.int32).cpu()
+    bf = bytes_and_flops(cfg, counts)
+
+    # end to end: host x in, host y (+ aux) out, copies inside the timed region
+    x_host = inp["x"].cpu().pin_memory()
+    y_host = torch.empty((cfg.T, cfg.H), dtype=torch.bfloat16).pin_memory()
+    aux_host = torch.empty((1,), dtype=torch.float32).pin_memory()
+    x_e2e = torch.empty_like(x_dev)
+
+    def e2e_step():
+        x_e2e.copy_(x_host, non_blocking=True)
+        B.moe_router(x_e2e, inp["w_r"], shp, rcfg, idx, w, ws, aux=aux,
+                     logit_offset=inp["logit_offset"], sel_bias=inp["sel_bias"])
+        B.moe_routing_metadata(idx, shp, ws)
+        B.moe_dispatch_gemm1(x_e2e, inp["w1"], shp, a, ws)
+        B.moe_swiglu_gemm2_combine(a, w, inp["w2"], shp, y, ws)
+        y_host.copy_(y, non_blocking=True)
+        aux_host.copy_(aux, non_blocking=True)
+
+    for _ in range(max(1, args.warmup)):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    e2e_ms = []
+    for _ in range(args.steps):
+        flush.fill_(3)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        e2e_step()
+        e1.record(stream)
+        e1.synchronize()                 # the host reads the step's result
+        e2e_ms.append(e0.elapsed_time(e1))
+    h2d = x_host.numel() * x_host.element_size()
+    d2h = y_host.numel() * y_host.element_size() + 4
+    err = B.moe_get_device_error(ws)
+    if err:
+        raise RuntimeError(f"device error word {err:#x} after the timed region")
+
+    return {"total_ms": total_ms, "step_ms": step_ms, "stage_ms": stage_ms, "bf": bf,
+            "clocks": clocks, "launches": launches, "e2e_ms": sum(e2e_ms), "h2d": h2d, "d2h": d2h,
+            "wall_s": t_wall}
+
+
+# ---------------------------------------------------------------- oracle (CPU) arm
+
+def oracle_sample(cfg, n_tokens, seed=0, inputs=None):
+    """Run the oracle (router + expert path) on the first n_tokens tokens; return seconds."""
+    import oracle
+    inp = inputs if inputs is not None else cpu_inputs(cfg, seed)
+    x = inp["x"][:n_tokens]
+    t0 = time.perf_counter()
+    r = oracle.router(x, inp["w_r"], cfg.k, score=cfg.score, normalize=cfg.normalize,
+                      scale=cfg.scale, n_group=cfg.n_group, topk_group=cfg.topk_group,
+                      group_topn=cfg.group_topn, logit_offset=inp["logit_offset"],
+                      sel_bias=inp["sel_bias"])
+    oracle.expert_forward(x, r.topk_idx, r.topk_w, inp["w1"], inp["w2"])
+    return time.perf_counter() - t0
+
+
+_CPU_INPUTS = {}
+
+
+def cpu_inputs(cfg, seed=0):
+    key = (cfg.name, seed)
+    if key not in _CPU_INPUTS:
+        dev = "cuda" if torch.cuda.is_available() else "cpu"
+        inp = generate(cfg, seed=seed, device=dev)
+        _CPU_INPUTS[key] = {k: (v.cpu() if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
+    return _CPU_INPUTS[key]
+
+
+def cpu_baseline(cfg, budget_s=15.0):
+    """Oracle timed on the host cores on a bounded token sample (~budget_s of work)."""
+    import oracle
+    oracle.build()
+    inp = cpu_inputs(cfg)
+    n_cal = min(cfg.T, 8)
+    t_cal = oracle_sample(cfg, n_cal, inputs=inp)
+    n = int(max(1, min(cfg.T, n_cal * budget_s / max(t_cal, 1e-6))))
+    t = oracle_sample(cfg, n, inputs=inp) if n != n_cal else t_cal
+    flops = 6.0 * n * cfg.k * cfg.H * cfg.I
+    return {"value": flops / t / 1e12, "unit": "TFLOP/s", "cores": oracle.num_threads(),
+            "kind": "oracle", "tokens_per_s": n / t,
+            "sample": f"first {n} of {cfg.T} tokens of the '{cfg.name}' workload: fp64 router + "
+                      f"expert path, {t:.2f} s"}
+
+
+def run_reference(args, cfg):
+    import oracle
+    oracle.build()
+    inp = cpu_inputs(cfg)
+    n_cal = min(cfg.T, 8)
+    t_cal = oracle_sample(cfg, n_cal, inputs=inp)
+    per_step_budget = min(20.0, 150.0 / max(1, args.steps + args.warmup))
+    n = int(max(1, min(cfg.T, n_cal * per_step_budget / max(t_cal, 1e-6))))
+    for _ in range(args.warmup):
+        oracle_sample(cfg, n, inputs=inp)
+    times = [oracle_sample(cfg, n, inputs=inp) for _ in range(args.steps)]
+    tot = sum(times)
+    flops = 6.0 * n * cfg.k * cfg.H * cfg.I * args.steps
+    value = flops / tot / 1e12
+    return {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * tot / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "tokens_per_s": n * args.steps / tot,
+        "config": config_dict(cfg, args),
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": oracle.num_threads(),
+                         "kind": "oracle",
+                         "sample": f"each step: first {n} of {cfg.T} tokens, fp64 router + expert path"},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def config_dict(cfg, args):
+    return {"workload": cfg.name, "description": cfg.description, "T": cfg.T, "H": cfg.H,
+            "I": cfg.I, "E": cfg.E, "k": cfg.k, "score": cfg.score, "n_group": cfg.n_group,
+            "topk_group": cfg.topk_group, "zipf_s": cfg.zipf_s, "parallelism": f"replicas x{args.gpus}",
+            "l2": f"flushed between steps ({L2_FLUSH_BYTES >> 20} MiB write outside the step events); "
+                  "weights exceed L2"}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default="mid", choices=sorted(CONFIGS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    cfg = CONFIGS[args.workload]
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args, cfg)), flush=True)
+        return
+
+    if world > 1:
+        torch.distributed.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    res = run_ours(args, cfg, rank, world, local_rank)
+    total_ms = res["total_ms"]
+    e2e_ms = res["e2e_ms"]
+    if world > 1:
+        t = torch.tensor([total_ms, e2e_ms], dtype=torch.float64, device="cuda")
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_ms, e2e_ms = float(t[0]), float(t[1])
+
+    if rank == 0:
+        peaks = measured_peaks()
+        flops_step = cfg.expert_flops()
+        value = flops_step * args.steps * world / (total_ms / 1e3) / 1e12
+        tokens_per_s = cfg.T * args.steps * world / (total_ms / 1e3)
+        # dominant kernel of the step and its roofline
+        stage_avg = {n: sum(v) / len(v) for n, v in res["stage_ms"].items()}
+        bf = res["bf"]
+        dom = max(("gemm1", "gemm2"), key=lambda n: stage_avg["gemm1" if n == "gemm1" else "gemm2_combine"])
+        dom_ms = stage_avg["gemm1"] if dom == "gemm1" else stage_avg["gemm2_combine"]
+        f, b = bf[dom]["flops"], bf[dom]["bytes"]
+        t_tc = f / (peaks["bf16_tflops"] * 1e12)
+        t_hbm = b / (peaks["hbm_gbs"] * 1e9)
+        if t_tc >= t_hbm:
+            roof = {"bound": "tensor", "achieved": f / (dom_ms / 1e3) / 1e12,
+                    "peak": peaks["bf16_tflops"], "unit": "TFLOP/s"}
+        else:
+            roof = {"bound": "hbm", "achieved": b / (dom_ms / 1e3) / 1e9, "peak": peaks["hbm_gbs"],
+                    "unit": "GB/s"}
+        roof["frac"] = roof["achieved"] / roof["peak"]
+        roof["traffic"] = None
+        roof["kernel"] = ("grouped_gemm_kernel<true> (stage 1: gather + GEMM1 + SwiGLU)" if dom == "gemm1"
+                          else "grouped_gemm_kernel<false> + combine_kernel (stage 2)")
+        roof["peak_kind"] = f"{peaks['source']} burst"
+        roof["kernel_ms"] = dom_ms
+        out = {
+            "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": total_ms / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic", "config": config_dict(cfg, args),
+            "tokens_per_s": tokens_per_s,
+            "stage_ms": {n: round(v, 5) for n, v in stage_avg.items()},
+            "active_experts": bf["active_experts"],
+            "roofline": roof,
+            "e2e": {"value": flops_step * args.steps * world / (e2e_ms / 1e3) / 1e12, "unit": "TFLOP/s",
+                    "h2d_bytes_per_step": res["h2d"], "d2h_bytes_per_step": res["d2h"]},
+            "gpu_launches": res["launches"],
+            "clocks": res["clocks"],
+        }
+        if not args.no_cpu_baseline:
+            out["cpu_baseline"] = cpu_baseline(cfg)
+        print(json.dumps(out), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

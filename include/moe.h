@@ -1,0 +1,189 @@
+/*
+ * moe.h -- C ABI of the GB300 (sm_103a) MegaMoE expert path, expert parallelism 1.
+ *
+ * The MegaMoE guide (Primus technical guide "MegaMoE") describes the layer as a
+ * fused router (score function + group-limited top-k + aux score) followed by
+ * dispatch_grouped_gemm -> SwiGLU -> grouped_gemm_combine, with weights
+ * w1 [g, 2I, H] (gate rows, then up rows) and w2 [g, H, I] (section "Design:
+ * two stages + weight modules"), and names the one-shot op
+ * fused_mega_moe(x, topk_idx, topk_weights, w1, w2, group). On one GPU the
+ * dispatch / combine all-to-all becomes a local row gather and a weighted sum,
+ * and g = E (all experts are local).
+ *
+ * Conventions for every entry point:
+ *   - Pointers named x, w_r, ..., y and ws are DEVICE pointers owned by the
+ *     caller; the library never allocates, frees or keeps them. Tensors are
+ *     dense row-major and 16-byte aligned. bf16 means IEEE bfloat16 storage.
+ *   - `stream` is a cudaStream_t (NULL = legacy default stream). Calls only
+ *     enqueue work on it and return; they never synchronise the device, except
+ *     moe_get_device_error, which waits for `stream`.
+ *   - Argument errors are reported synchronously by the return value, before
+ *     anything is enqueued. Data errors found on the device (an expert index
+ *     outside [0, E), a wait that ran out of time) set bits in the error word
+ *     of the workspace; read them with moe_get_device_error.
+ *   - Limits: H and I multiples of 8; 1 <= k <= 32; k <= E <= 1024; T*k < 2^31.
+ *     Outside them a call returns MOE_ERR_UNSUPPORTED. The device must be an
+ *     sm_103 GPU.
+ *   - The workspace `ws` (moe_workspace_size bytes, 256-byte aligned) holds the
+ *     routing metadata and intermediates. Zero its first 256 bytes once before
+ *     first use (moe_workspace_init). Calls that share a workspace must be
+ *     ordered on one stream; stages read what earlier stages left there.
+ */
+#ifndef MOE_GB300_MOE_H
+#define MOE_GB300_MOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum moe_status {
+    MOE_OK = 0,
+    MOE_ERR_INVALID_ARG = 1,      /* null / misaligned pointer, bad size or config */
+    MOE_ERR_UNSUPPORTED = 2,      /* outside the limits above, or not an sm_103 device */
+    MOE_ERR_CUDA = 3,             /* a CUDA runtime call failed */
+    MOE_ERR_WORKSPACE = 4,        /* ws_bytes smaller than moe_workspace_size */
+    MOE_ERR_DEVICE_FLAGGED = 5    /* moe_get_device_error found a non-zero error word */
+} moe_status_t;
+
+/* Bits of the device error word. */
+#define MOE_DEVERR_BAD_EXPERT_INDEX 0x1  /* a topk_idx entry outside [0, E): that slot was dropped */
+#define MOE_DEVERR_WAIT_TIMEOUT     0x2  /* a pipeline wait ran out of time: outputs are invalid */
+
+typedef struct moe_shape {
+    int64_t T;   /* tokens */
+    int64_t H;   /* hidden size */
+    int64_t I;   /* expert intermediate size (w1 has 2I rows per expert) */
+    int64_t E;   /* experts */
+    int32_t k;   /* experts per token */
+    int32_t reserved;  /* must be 0 */
+} moe_shape_t;
+
+#define MOE_SCORE_SOFTMAX 0
+#define MOE_SCORE_SIGMOID 1
+
+typedef struct moe_router_cfg {
+    int32_t score_fn;    /* MOE_SCORE_SOFTMAX or MOE_SCORE_SIGMOID */
+    int32_t normalize;   /* 1: divide the k weights by their score sum */
+    float scale;         /* multiply the k weights (1.0 for none) */
+    int32_t n_group;     /* 1: no group limit; else E % n_group == 0 and n_group <= 32 */
+    int32_t topk_group;  /* groups kept per token (1 <= topk_group <= n_group) */
+    int32_t group_topn;  /* largest selection scores summed per group score (>= 1) */
+} moe_router_cfg_t;
+
+/* Byte offsets of the regions inside the workspace (for inspection and tests). */
+typedef struct moe_ws_layout {
+    size_t err;        /* int32 error word (first 4 bytes) */
+    size_t counts;     /* int32 [E]   rows routed to each expert */
+    size_t offsets;    /* int32 [E+1] exclusive prefix sum of counts */
+    size_t mt_prefix;  /* int32 [E+1] prefix sum of ceil(counts/128) (row tiles) */
+    size_t perm_slot;  /* int32 [T*k] flat slot t*k+j of each routed row */
+    size_t row_of;     /* int32 [T*k] routed row of each slot, -1 if dropped */
+    size_t router;     /* router scratch: float logits [T,E], float score sums [E], int32 counts [E] */
+    size_t a;          /* bf16 [T*k, I] SwiGLU activations (moe_forward only) */
+    size_t obuf;       /* bf16 [T*k, H] weighted expert outputs in slot order */
+    size_t total;      /* == moe_workspace_size */
+} moe_ws_layout_t;
+
+/* Bytes of workspace needed for `shape`. Host-only; touches no device. */
+moe_status_t moe_workspace_size(const moe_shape_t *shape, size_t *bytes);
+
+/* Region offsets of the workspace for `shape`. Host-only. */
+moe_status_t moe_workspace_layout(const moe_shape_t *shape, moe_ws_layout_t *layout);
+
+/* Zero the workspace header (error word and counters) on `stream`. */
+moe_status_t moe_workspace_init(void *ws, size_t ws_bytes, void *stream);
+
+/*
+ * Fused router (MegaMoE guide, opening section: score function + group-limited
+ * top-k + aux score; the aux load-balance value is computed and returned).
+ *
+ *   l[t,e]   = sum_h x[t,h] * w_r[e,h] (+ logit_offset[e]), fp32
+ *   s[t,:]   = softmax(l[t,:]) or sigmoid(l[t,:])
+ *   sel[t,e] = s[t,e] + sel_bias[e]          (selection only, never the weights)
+ *   groups   = (n_group > 1) keep the topk_group groups with the largest sum of
+ *              their group_topn best sel values; other experts are ineligible
+ *   topk_idx = the k eligible experts with the largest sel, best first; ties go
+ *              to the lower expert (and group) index
+ *   topk_w   = s of those experts, / their sum if normalize, * scale
+ *   aux      = E * sum_e (c_e / (T k)) * (1/T) sum_t s[t,e]   (c_e = rows of e)
+ *
+ * x bf16 [T,H]; w_r fp32 [E,H]; logit_offset, sel_bias fp32 [E] or NULL;
+ * topk_idx int32 [T,k], topk_w fp32 [T,k], aux fp32 [1] or NULL (outputs).
+ */
+moe_status_t moe_router(const void *x, const float *w_r, const float *logit_offset,
+                        const float *sel_bias, const moe_shape_t *shape,
+                        const moe_router_cfg_t *cfg, int32_t *topk_idx, float *topk_w,
+                        float *aux, void *ws, size_t ws_bytes, void *stream);
+
+/*
+ * Routing metadata: the local stand-in for the dispatch all-to-all (MegaMoE
+ * guide, opening section, dispatch_grouped_gemm; section "Router force load
+ * balancing": ragged per-expert counts absorbed without padding or host sync).
+ * From topk_idx int32 [T,k] it writes into ws the per-expert counts, their
+ * exclusive prefix sum, the row-tile prefix, and the stable permutation: rows
+ * of expert e are offsets[e] .. offsets[e+1]-1 in increasing flat slot order.
+ * Slots with an index outside [0, E) are dropped and flag the error word.
+ */
+moe_status_t moe_routing_metadata(const int32_t *topk_idx, const moe_shape_t *shape,
+                                  void *ws, size_t ws_bytes, void *stream);
+
+/*
+ * dispatch_grouped_gemm with the SwiGLU fused into its epilogue (MegaMoE
+ * guide, opening section and section "Design: two stages", stage 1):
+ *
+ *   for routed row r of expert e, token t = perm_slot[r] / k:
+ *     h = x[t,:] . w1[e]^T  (2I values, fp32 accumulate)
+ *     a[r, i] = silu(h[i]) * h[I + i],  i < I   (rounded to bf16)
+ *
+ * x bf16 [T,H]; w1 bf16 [E,2I,H]; a bf16 [T*k, I] (caller-owned, rows in the
+ * metadata's routed order; rows past offsets[E] are left untouched). Needs the
+ * metadata of moe_routing_metadata in ws.
+ */
+moe_status_t moe_dispatch_gemm1(const void *x, const void *w1, const moe_shape_t *shape,
+                                void *a, void *ws, size_t ws_bytes, void *stream);
+
+/*
+ * grouped_gemm_combine (MegaMoE guide, opening section and section "Design:
+ * two stages", stage 2). The SwiGLU already ran in stage 1's epilogue, so the
+ * input is a:
+ *
+ *   o[r,:] = a[r,:] . w2[e]^T   (H values, fp32 accumulate)
+ *   y[t,:] = sum_j topk_w[t,j] * o[row_of[t*k+j], :]   (fp32 sum, bf16 out)
+ *
+ * a bf16 [T*k, I] (routed order, from moe_dispatch_gemm1); topk_w fp32 [T,k];
+ * w2 bf16 [E,H,I]; y bf16 [T,H] is fully overwritten (tokens whose slots were
+ * all dropped get zeros). Needs the metadata of moe_routing_metadata in ws.
+ */
+moe_status_t moe_swiglu_gemm2_combine(const void *a, const float *topk_w, const void *w2,
+                                      const moe_shape_t *shape, void *y, void *ws,
+                                      size_t ws_bytes, void *stream);
+
+/*
+ * One-shot expert path, the single-device counterpart of the guide's
+ * fused_mega_moe(x, topk_idx, topk_weights, w1, w2, group) without the process
+ * group: routing metadata, then stage 1, then stage 2, with `a` kept in ws.
+ */
+moe_status_t moe_forward(const void *x, const int32_t *topk_idx, const float *topk_w,
+                         const void *w1, const void *w2, const moe_shape_t *shape, void *y,
+                         void *ws, size_t ws_bytes, void *stream);
+
+/*
+ * Wait for `stream`, then read and clear the workspace error word into *code.
+ * Returns MOE_ERR_DEVICE_FLAGGED when it was non-zero. Not for the hot path.
+ */
+moe_status_t moe_get_device_error(void *ws, int32_t *code, void *stream);
+
+/* Static description of a status code. */
+const char *moe_status_string(moe_status_t status);
+
+/* Number of kernels this library has launched in this process (statistics). */
+uint64_t moe_kernel_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_GB300_MOE_H */

@@ -1,0 +1,192 @@
+"""ctypes binding of libmoe.so: the same entry points as include/moe.h.
+
+Argument marshalling only -- every step of the expert path runs in the CUDA
+kernels of libmoe. There is no fallback: if the library is missing or cannot be
+loaded, every call raises.
+
+Tensors are torch CUDA tensors; the stream defaults to torch's current stream
+on the tensors' device.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+from .build import LIB_PATH
+
+MOE_OK = 0
+STATUS_NAMES = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED",
+                3: "MOE_ERR_CUDA", 4: "MOE_ERR_WORKSPACE", 5: "MOE_ERR_DEVICE_FLAGGED"}
+DEVERR_BAD_EXPERT_INDEX = 0x1
+DEVERR_WAIT_TIMEOUT = 0x2
+SCORE_SOFTMAX = 0
+SCORE_SIGMOID = 1
+
+
+class MoEError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        self.status = status
+        super().__init__(f"{fn} returned {STATUS_NAMES.get(status, status)}")
+
+
+class Shape(ctypes.Structure):
+    _fields_ = [("T", ctypes.c_int64), ("H", ctypes.c_int64), ("I", ctypes.c_int64),
+                ("E", ctypes.c_int64), ("k", ctypes.c_int32), ("reserved", ctypes.c_int32)]
+
+
+class RouterCfg(ctypes.Structure):
+    _fields_ = [("score_fn", ctypes.c_int32), ("normalize", ctypes.c_int32),
+                ("scale", ctypes.c_float), ("n_group", ctypes.c_int32),
+                ("topk_group", ctypes.c_int32), ("group_topn", ctypes.c_int32)]
+
+
+class WsLayout(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_size_t) for n in
+                ("err", "counts", "offsets", "mt_prefix", "perm_slot", "row_of", "router", "a",
+                 "obuf", "total")]
+
+
+# name -> argument types (all return moe_status_t unless listed in _RESTYPES)
+_P = ctypes.c_void_p
+_SIG = {
+    "moe_workspace_size": [ctypes.POINTER(Shape), ctypes.POINTER(ctypes.c_size_t)],
+    "moe_workspace_layout": [ctypes.POINTER(Shape), ctypes.POINTER(WsLayout)],
+    "moe_workspace_init": [_P, ctypes.c_size_t, _P],
+    "moe_router": [_P, _P, _P, _P, ctypes.POINTER(Shape), ctypes.POINTER(RouterCfg), _P, _P, _P,
+                   _P, ctypes.c_size_t, _P],
+    "moe_routing_metadata": [_P, ctypes.POINTER(Shape), _P, ctypes.c_size_t, _P],
+    "moe_dispatch_gemm1": [_P, _P, ctypes.POINTER(Shape), _P, _P, ctypes.c_size_t, _P],
+    "moe_swiglu_gemm2_combine": [_P, _P, _P, ctypes.POINTER(Shape), _P, _P, ctypes.c_size_t, _P],
+    "moe_forward": [_P, _P, _P, _P, _P, ctypes.POINTER(Shape), _P, _P, ctypes.c_size_t, _P],
+    "moe_get_device_error": [_P, ctypes.POINTER(ctypes.c_int32), _P],
+    "moe_status_string": [ctypes.c_int],
+    "moe_kernel_launch_count": [],
+}
+_RESTYPES = {"moe_status_string": ctypes.c_char_p, "moe_kernel_launch_count": ctypes.c_uint64}
+
+_lib = None
+
+
+def load(path: str = LIB_PATH):
+    """Load libmoe.so (built by moe_expert_router_gb300.build); raise if absent."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise RuntimeError(f"{path} is missing: build it first "
+                           "(python -c 'import __graft_entry__ as g; g.build()')")
+    lib = ctypes.CDLL(path)
+    for name, args in _SIG.items():
+        fn = getattr(lib, name)
+        fn.argtypes = args
+        fn.restype = _RESTYPES.get(name, ctypes.c_int)
+    _lib = lib
+    return lib
+
+
+def _check(fn: str, status: int):
+    if status != MOE_OK:
+        raise MoEError(fn, status)
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if not isinstance(t, torch.Tensor):
+        raise TypeError("expected a torch tensor")
+    if not t.is_cuda:
+        raise ValueError("libmoe takes CUDA tensors only")
+    if not t.is_contiguous():
+        raise ValueError("tensors must be contiguous")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream, like):
+    if stream is None:
+        stream = torch.cuda.current_stream(like.device)
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def shape(T, H, I, E, k) -> Shape:
+    return Shape(int(T), int(H), int(I), int(E), int(k), 0)
+
+
+def router_cfg(score="softmax", normalize=True, scale=1.0, n_group=1, topk_group=1,
+               group_topn=2) -> RouterCfg:
+    fn = SCORE_SOFTMAX if score == "softmax" else SCORE_SIGMOID
+    return RouterCfg(fn, int(bool(normalize)), float(scale), int(n_group), int(topk_group),
+                     int(group_topn))
+
+
+def moe_workspace_size(shp: Shape) -> int:
+    n = ctypes.c_size_t()
+    _check("moe_workspace_size", load().moe_workspace_size(ctypes.byref(shp), ctypes.byref(n)))
+    return int(n.value)
+
+
+def moe_workspace_layout(shp: Shape) -> WsLayout:
+    L = WsLayout()
+    _check("moe_workspace_layout", load().moe_workspace_layout(ctypes.byref(shp), ctypes.byref(L)))
+    return L
+
+
+def moe_workspace_init(ws, stream=None):
+    _check("moe_workspace_init",
+           load().moe_workspace_init(_ptr(ws), ws.numel() * ws.element_size(), _stream(stream, ws)))
+
+
+def moe_router(x, w_r, shp, cfg, topk_idx, topk_w, ws, aux=None, logit_offset=None,
+               sel_bias=None, stream=None):
+    _check("moe_router", load().moe_router(
+        _ptr(x), _ptr(w_r), _ptr(logit_offset), _ptr(sel_bias), ctypes.byref(shp),
+        ctypes.byref(cfg), _ptr(topk_idx), _ptr(topk_w), _ptr(aux), _ptr(ws),
+        ws.numel() * ws.element_size(), _stream(stream, x)))
+
+
+def moe_routing_metadata(topk_idx, shp, ws, stream=None):
+    _check("moe_routing_metadata", load().moe_routing_metadata(
+        _ptr(topk_idx), ctypes.byref(shp), _ptr(ws), ws.numel() * ws.element_size(),
+        _stream(stream, topk_idx)))
+
+
+def moe_dispatch_gemm1(x, w1, shp, a, ws, stream=None):
+    _check("moe_dispatch_gemm1", load().moe_dispatch_gemm1(
+        _ptr(x), _ptr(w1), ctypes.byref(shp), _ptr(a), _ptr(ws), ws.numel() * ws.element_size(),
+        _stream(stream, x)))
+
+
+def moe_swiglu_gemm2_combine(a, topk_w, w2, shp, y, ws, stream=None):
+    _check("moe_swiglu_gemm2_combine", load().moe_swiglu_gemm2_combine(
+        _ptr(a), _ptr(topk_w), _ptr(w2), ctypes.byref(shp), _ptr(y), _ptr(ws),
+        ws.numel() * ws.element_size(), _stream(stream, a)))
+
+
+def moe_forward(x, topk_idx, topk_w, w1, w2, shp, y, ws, stream=None):
+    _check("moe_forward", load().moe_forward(
+        _ptr(x), _ptr(topk_idx), _ptr(topk_w), _ptr(w1), _ptr(w2), ctypes.byref(shp), _ptr(y),
+        _ptr(ws), ws.numel() * ws.element_size(), _stream(stream, x)))
+
+
+def moe_get_device_error(ws, stream=None) -> int:
+    """Wait for the stream, return and clear the workspace error word (0 = none)."""
+    code = ctypes.c_int32()
+    st = load().moe_get_device_error(_ptr(ws), ctypes.byref(code), _stream(stream, ws))
+    if st not in (MOE_OK, 5):
+        raise MoEError("moe_get_device_error", st)
+    return int(code.value)
+
+
+def moe_kernel_launch_count() -> int:
+    return int(load().moe_kernel_launch_count())
+
+
+def new_workspace(shp: Shape, device=None) -> torch.Tensor:
+    """A 256-byte aligned uint8 workspace of the required size, header zeroed."""
+    n = moe_workspace_size(shp)
+    ws = torch.empty(n + 256, dtype=torch.uint8, device=device or "cuda")
+    off = (-ws.data_ptr()) % 256
+    ws = ws[off:off + n]
+    moe_workspace_init(ws)
+    return ws

@@ -1,0 +1,344 @@
+// router.cu -- the fused router of the MegaMoE layer (MegaMoE guide, opening
+// section: score function + group-limited top-k + aux score; the aux
+// load-balance value is computed on the device and returned).
+//
+//   logits kernel : l[t, e] = sum_h x[t, h] * w_r[e, h] (+ logit_offset[e]) in
+//                   fp32, 64x64 output tiles, 4x4 per thread. Block (0, 0)
+//                   also clears the aux accumulators of this call.
+//   top-k kernel  : one warp per token. Scores (softmax over the row, or
+//                   elementwise sigmoid), selection scores sel = s + sel_bias,
+//                   optional group limit (group score = sum of the group_topn
+//                   best sel; keep topk_group groups), k rounds of a warp
+//                   arg-max over (sel desc, expert index asc), weights s / sum
+//                   * scale. Per-block partial sums of s and of the chosen
+//                   experts go to global accumulators; the last block to
+//                   finish computes aux = E * sum_e (c_e / (T k)) * P_e.
+#include <math.h>
+
+#include "internal.cuh"
+#include "ptx.cuh"
+
+namespace moe {
+
+namespace {
+
+constexpr int LT = 64;        // logits tile: tokens
+constexpr int LE = 64;        // logits tile: experts
+constexpr int LK = 32;        // logits tile: reduction slice
+constexpr int kTopkWarps = 8;
+constexpr int kMaxE = 1024;
+
+__global__ void __launch_bounds__(256)
+router_logits_kernel(const __nv_bfloat16 *__restrict__ x, const float *__restrict__ w_r,
+                     const float *__restrict__ logit_offset, float *__restrict__ logits, int T,
+                     int H, int E, float *__restrict__ score_sum, int32_t *__restrict__ counts,
+                     int32_t *__restrict__ ticket) {
+    __shared__ float xs[LK][LT + 1];
+    __shared__ float wsm[LK][LE + 1];
+    if (blockIdx.x == 0 && blockIdx.y == 0) {
+        for (int e = threadIdx.x; e < E; e += blockDim.x) {
+            score_sum[e] = 0.0f;
+            counts[e] = 0;
+        }
+        if (threadIdx.x == 0) *ticket = 0;
+    }
+    const int t0 = blockIdx.y * LT;
+    const int e0 = blockIdx.x * LE;
+    const int tx = threadIdx.x & 15;   // expert quad
+    const int ty = threadIdx.x >> 4;   // token quad
+    float acc[4][4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) acc[i][j] = 0.0f;
+
+    for (int h0 = 0; h0 < H; h0 += LK) {
+        for (int i = threadIdx.x; i < LT * LK; i += blockDim.x) {
+            const int r = i / LK, c = i % LK;
+            const int t = t0 + r, h = h0 + c;
+            xs[c][r] = (t < T && h < H) ? __bfloat162float(x[static_cast<int64_t>(t) * H + h]) : 0.0f;
+            const int e = e0 + r;
+            wsm[c][r] = (e < E && h < H) ? w_r[static_cast<int64_t>(e) * H + h] : 0.0f;
+        }
+        __syncthreads();
+#pragma unroll 8
+        for (int c = 0; c < LK; ++c) {
+            float a[4], b[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                a[i] = xs[c][ty * 4 + i];
+                b[i] = wsm[c][tx * 4 + i];
+            }
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+#pragma unroll
+                for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
+        }
+        __syncthreads();
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int t = t0 + ty * 4 + i;
+        if (t >= T) continue;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int e = e0 + tx * 4 + j;
+            if (e < E) logits[static_cast<int64_t>(t) * E + e] = acc[i][j] + (logit_offset ? logit_offset[e] : 0.0f);
+        }
+    }
+}
+
+// Warp-wide arg-max in the order (value desc, index asc); every lane gets the winner.
+__device__ __forceinline__ void warp_argmax(float &v, int &i) {
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+        const float ov = __shfl_xor_sync(0xffffffffu, v, off);
+        const int oi = __shfl_xor_sync(0xffffffffu, i, off);
+        if (ov > v || (ov == v && oi < i)) {
+            v = ov;
+            i = oi;
+        }
+    }
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+    return v;
+}
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, off));
+    return v;
+}
+
+struct TopkArgs {
+    const float *logits;
+    const float *sel_bias;
+    int T, E, k, score_fn, normalize;
+    float scale;
+    int n_group, topk_group, group_topn;
+    int32_t *topk_idx;
+    float *topk_w;
+    float *score_sum;
+    int32_t *counts;
+    int32_t *ticket;
+    float *aux;
+};
+
+// V = experts per lane (lane l holds experts l, l+32, ..., l+32(V-1)).
+template <int V>
+__global__ void __launch_bounds__(kTopkWarps * 32)
+router_topk_kernel(const TopkArgs p) {
+    __shared__ float blk_sum[kMaxE];
+    __shared__ int blk_cnt[kMaxE];
+    __shared__ float sel_sh[kTopkWarps][kMaxE];
+    __shared__ int is_last;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    for (int e = threadIdx.x; e < p.E; e += blockDim.x) {
+        blk_sum[e] = 0.0f;
+        blk_cnt[e] = 0;
+    }
+    __syncthreads();
+
+    const int t = blockIdx.x * kTopkWarps + warp;
+    if (t < p.T) {
+        float s[V], sel[V];
+        bool elig[V];
+        const float *lrow = p.logits + static_cast<int64_t>(t) * p.E;
+#pragma unroll
+        for (int i = 0; i < V; ++i) {
+            const int e = lane + 32 * i;
+            s[i] = (e < p.E) ? lrow[e] : -INFINITY;
+        }
+        if (p.score_fn == MOE_SCORE_SOFTMAX) {
+            float m = -INFINITY;
+#pragma unroll
+            for (int i = 0; i < V; ++i) m = fmaxf(m, s[i]);
+            m = warp_max(m);
+            float z = 0.0f;
+#pragma unroll
+            for (int i = 0; i < V; ++i) {
+                const int e = lane + 32 * i;
+                s[i] = (e < p.E) ? expf(s[i] - m) : 0.0f;
+                z += s[i];
+            }
+            z = warp_sum(z);
+            const float inv = 1.0f / z;
+#pragma unroll
+            for (int i = 0; i < V; ++i) s[i] *= inv;
+        } else {
+#pragma unroll
+            for (int i = 0; i < V; ++i) {
+                const int e = lane + 32 * i;
+                s[i] = (e < p.E) ? 1.0f / (1.0f + expf(-s[i])) : 0.0f;
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < V; ++i) {
+            const int e = lane + 32 * i;
+            elig[i] = e < p.E;
+            sel[i] = elig[i] ? s[i] + (p.sel_bias ? p.sel_bias[e] : 0.0f) : -INFINITY;
+            if (elig[i]) atomicAdd(&blk_sum[e], s[i]);
+        }
+
+        if (p.n_group > 1) {
+            const int gs = p.E / p.n_group;
+            float *row = sel_sh[warp];
+#pragma unroll
+            for (int i = 0; i < V; ++i) {
+                const int e = lane + 32 * i;
+                if (e < p.E) row[e] = sel[i];
+            }
+            __syncwarp();
+            // lane g: sum of the group_topn best sel of group g, taken in the
+            // order (value desc, index asc) by repeatedly finding the best
+            // element ranked after the previous pick
+            float gscore = -INFINITY;
+            if (lane < p.n_group) {
+                float prev_v = INFINITY;
+                int prev_i = -1;
+                float sum = 0.0f;
+                for (int n = 0; n < p.group_topn && n < gs; ++n) {
+                    float bv = -INFINITY;
+                    int bi = -1;
+                    for (int i = 0; i < gs; ++i) {
+                        const float v = row[lane * gs + i];
+                        const bool after = (v < prev_v) || (v == prev_v && i > prev_i);
+                        if (after && (bi < 0 || v > bv)) {
+                            bv = v;
+                            bi = i;
+                        }
+                    }
+                    sum += bv;
+                    prev_v = bv;
+                    prev_i = bi;
+                }
+                gscore = sum;
+            }
+            unsigned kept = 0;
+            float gv = gscore;
+            for (int n = 0; n < p.topk_group; ++n) {
+                float v = gv;
+                int i = (lane < p.n_group) ? lane : 0x7fffffff;
+                warp_argmax(v, i);
+                kept |= 1u << i;
+                if (lane == i) gv = -INFINITY;
+            }
+#pragma unroll
+            for (int i = 0; i < V; ++i) {
+                const int e = lane + 32 * i;
+                if (e < p.E && !((kept >> (e / gs)) & 1u)) elig[i] = false;
+            }
+        }
+
+        int my_idx = 0;
+        float my_s = 0.0f, chosen_sum = 0.0f;
+        for (int j = 0; j < p.k; ++j) {
+            float v = -INFINITY;
+            int idx = 0x7fffffff;
+#pragma unroll
+            for (int i = 0; i < V; ++i) {
+                const int e = lane + 32 * i;
+                if (elig[i] && (idx == 0x7fffffff || sel[i] > v)) {
+                    v = sel[i];
+                    idx = e;
+                }
+            }
+            warp_argmax(v, idx);
+            float mine = 0.0f;
+#pragma unroll
+            for (int i = 0; i < V; ++i) {
+                if (lane + 32 * i == idx) {
+                    elig[i] = false;
+                    mine = s[i];
+                }
+            }
+            const float sc = __shfl_sync(0xffffffffu, mine, idx & 31);
+            chosen_sum += sc;
+            if (lane == j) {
+                my_idx = idx;
+                my_s = sc;
+            }
+            if (lane == 0) atomicAdd(&blk_cnt[idx], 1);
+        }
+        if (lane < p.k) {
+            float w = my_s;
+            if (p.normalize) w = w / chosen_sum;
+            w *= p.scale;
+            p.topk_idx[static_cast<int64_t>(t) * p.k + lane] = my_idx;
+            p.topk_w[static_cast<int64_t>(t) * p.k + lane] = w;
+        }
+    }
+    __syncthreads();
+    for (int e = threadIdx.x; e < p.E; e += blockDim.x) {
+        if (blk_sum[e] != 0.0f) atomicAdd(&p.score_sum[e], blk_sum[e]);
+        if (blk_cnt[e] != 0) atomicAdd(&p.counts[e], blk_cnt[e]);
+    }
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) is_last = (atomicAdd(p.ticket, 1) == static_cast<int>(gridDim.x) - 1);
+    __syncthreads();
+    if (is_last && p.aux != nullptr) {
+        __threadfence();
+        float part = 0.0f;
+        for (int e = threadIdx.x; e < p.E; e += blockDim.x)
+            part += static_cast<float>(__ldcg(&p.counts[e])) * __ldcg(&p.score_sum[e]);
+        part = warp_sum(part);
+        __shared__ float red[kTopkWarps];
+        if (lane == 0) red[warp] = part;
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            float tot = 0.0f;
+            for (int w = 0; w < kTopkWarps; ++w) tot += red[w];
+            const float Tf = static_cast<float>(p.T);
+            *p.aux = static_cast<float>(p.E) * tot / (Tf * static_cast<float>(p.k) * Tf);
+        }
+    }
+}
+
+template <int V>
+void launch_topk(const TopkArgs &a, int blocks, cudaStream_t st) {
+    router_topk_kernel<V><<<blocks, kTopkWarps * 32, 0, st>>>(a);
+}
+
+}  // namespace
+
+cudaError_t setup_router_kernels() { return cudaSuccess; }
+
+cudaError_t launch_router(const RouterLaunch &p, cudaStream_t st) {
+    dim3 lgrid((p.E + LE - 1) / LE, (p.T + LT - 1) / LT);
+    router_logits_kernel<<<lgrid, 256, 0, st>>>(p.x, p.w_r, p.logit_offset, p.scratch.logits, p.T, p.H,
+                                                 p.E, p.scratch.score_sum, p.scratch.counts,
+                                                 p.scratch.ticket);
+    TopkArgs a;
+    a.logits = p.scratch.logits;
+    a.sel_bias = p.sel_bias;
+    a.T = p.T;
+    a.E = p.E;
+    a.k = p.k;
+    a.score_fn = p.score_fn;
+    a.normalize = p.normalize;
+    a.scale = p.scale;
+    a.n_group = p.n_group;
+    a.topk_group = p.topk_group;
+    a.group_topn = p.group_topn;
+    a.topk_idx = p.topk_idx;
+    a.topk_w = p.topk_w;
+    a.score_sum = p.scratch.score_sum;
+    a.counts = p.scratch.counts;
+    a.ticket = p.scratch.ticket;
+    a.aux = p.aux;
+    const int blocks = (p.T + kTopkWarps - 1) / kTopkWarps;
+    const int v = (p.E + 31) / 32;
+    if (v <= 2) launch_topk<2>(a, blocks, st);
+    else if (v <= 4) launch_topk<4>(a, blocks, st);
+    else if (v <= 8) launch_topk<8>(a, blocks, st);
+    else if (v <= 16) launch_topk<16>(a, blocks, st);
+    else launch_topk<32>(a, blocks, st);
+    note_launches(2);
+    return cudaGetLastError();
+}
+
+}  // namespace moe

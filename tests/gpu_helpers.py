@@ -1,0 +1,125 @@
+"""Helpers for the GPU parity tests: run the C-ABI path, call the oracle, compare.
+
+Comparison rules (fixed by the benchmark spec for this path):
+  * routing indices and counts bit-exact, excluding tokens whose oracle gap
+    between the k-th and (k+1)-th selection score (and, with a group limit,
+    between the last kept and the best dropped group score) is below 1e-6;
+  * outputs within relative Frobenius error 1e-2 and max abs error
+    3e-2 * max|y_ref|.
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import oracle
+from moe_expert_router_gb300 import binding as B
+from moe_expert_router_gb300.workloads import MoEConfig
+
+GAP = 1e-6
+REL_FRO = 1e-2
+MAX_ABS_FRAC = 3e-2
+
+
+def assert_close_y(y_gpu, y_ref, what="y"):
+    """North-star output bound: rel-Frobenius <= 1e-2 and max-abs <= 3e-2 max|ref|."""
+    g = y_gpu.detach().float().cpu().double().numpy() if isinstance(y_gpu, torch.Tensor) else np.asarray(y_gpu, np.float64)
+    r = np.asarray(y_ref, np.float64)
+    assert g.shape == r.shape, (g.shape, r.shape)
+    assert np.isfinite(g).all(), f"{what}: non-finite values"
+    ref_norm = np.linalg.norm(r)
+    err = np.linalg.norm(g - r)
+    rel = err / ref_norm if ref_norm > 0 else err
+    mx = np.abs(r).max() if r.size else 0.0
+    max_abs = np.abs(g - r).max() if r.size else 0.0
+    assert rel <= REL_FRO, f"{what}: relative Frobenius error {rel:.3e} > {REL_FRO}"
+    assert max_abs <= MAX_ABS_FRAC * mx + 1e-30, f"{what}: max abs error {max_abs:.3e} > {MAX_ABS_FRAC} * {mx:.3e}"
+    return rel, max_abs
+
+
+def ws_view(ws, layout_off, count, dtype=torch.int32):
+    """A typed view of `count` elements of the workspace at byte offset `layout_off`."""
+    nbytes = count * torch.tensor([], dtype=dtype).element_size()
+    return ws[layout_off:layout_off + nbytes].view(dtype)
+
+
+def read_metadata(ws, shp):
+    L = B.moe_workspace_layout(shp)
+    E, R = shp.E, shp.T * shp.k
+    counts = ws_view(ws, L.counts, E).cpu().numpy()
+    offsets = ws_view(ws, L.offsets, E + 1).cpu().numpy()
+    mt_prefix = ws_view(ws, L.mt_prefix, E + 1).cpu().numpy()
+    perm = ws_view(ws, L.perm_slot, R).cpu().numpy()[: offsets[E]]
+    row_of = ws_view(ws, L.row_of, R).cpu().numpy()
+    return counts, offsets, mt_prefix, perm, row_of
+
+
+def router_cfg_of(cfg: MoEConfig):
+    return B.router_cfg(cfg.score, cfg.normalize, cfg.scale, cfg.n_group, cfg.topk_group,
+                        cfg.group_topn)
+
+
+def run_router(inp, cfg: MoEConfig, ws=None):
+    dev = inp["x"].device
+    shp = B.shape(cfg.T, cfg.H, cfg.I, cfg.E, cfg.k)
+    if ws is None:
+        ws = B.new_workspace(shp, dev)
+    idx = torch.empty((cfg.T, cfg.k), dtype=torch.int32, device=dev)
+    w = torch.empty((cfg.T, cfg.k), dtype=torch.float32, device=dev)
+    aux = torch.zeros((1,), dtype=torch.float32, device=dev)
+    B.moe_router(inp["x"], inp["w_r"], shp, router_cfg_of(cfg), idx, w, ws, aux=aux,
+                 logit_offset=inp.get("logit_offset"), sel_bias=inp.get("sel_bias"))
+    return idx, w, aux, ws
+
+
+def oracle_router(inp, cfg: MoEConfig, rows=None):
+    x = inp["x"] if rows is None else inp["x"][rows]
+    return oracle.router(x, inp["w_r"], cfg.k, score=cfg.score, normalize=cfg.normalize,
+                         scale=cfg.scale, n_group=cfg.n_group, topk_group=cfg.topk_group,
+                         group_topn=cfg.group_topn, logit_offset=inp.get("logit_offset"),
+                         sel_bias=inp.get("sel_bias"))
+
+
+def routing_mismatches(idx_gpu, ref, cfg: MoEConfig):
+    """(number of compared tokens, list of mismatching tokens, excluded mask)."""
+    g = idx_gpu.cpu().numpy() if isinstance(idx_gpu, torch.Tensor) else np.asarray(idx_gpu)
+    excluded = ref.sel_gap < GAP
+    if cfg.n_group > 1:
+        excluded |= ref.group_gap < GAP
+    bad = []
+    for t in np.nonzero(~excluded)[0]:
+        if sorted(g[t].tolist()) != sorted(ref.topk_idx[t].tolist()):
+            bad.append(int(t))
+    return int((~excluded).sum()), bad, excluded
+
+
+def run_forward(inp, idx, w, cfg: MoEConfig, ws=None, staged=False):
+    dev = inp["x"].device
+    shp = B.shape(cfg.T, cfg.H, cfg.I, cfg.E, cfg.k)
+    if ws is None:
+        ws = B.new_workspace(shp, dev)
+    y = torch.empty((cfg.T, cfg.H), dtype=torch.bfloat16, device=dev)
+    if staged:
+        a = torch.empty((cfg.T * cfg.k, cfg.I), dtype=torch.bfloat16, device=dev)
+        B.moe_routing_metadata(idx, shp, ws)
+        B.moe_dispatch_gemm1(inp["x"], inp["w1"], shp, a, ws)
+        B.moe_swiglu_gemm2_combine(a, w, inp["w2"], shp, y, ws)
+        return y, ws, a
+    B.moe_forward(inp["x"], idx, w, inp["w1"], inp["w2"], shp, y, ws)
+    return y, ws, None
+
+
+def oracle_y_for_tokens(inp, idx, w, tokens):
+    """Oracle y rows for `tokens` only: copies just the experts those tokens use."""
+    tokens = torch.as_tensor(tokens, dtype=torch.long)
+    idx_s = idx[tokens.to(idx.device)].cpu().long()
+    used = torch.unique(idx_s[(idx_s >= 0)])
+    remap = torch.full((int(inp["w1"].shape[0]) + 1,), -1, dtype=torch.long)
+    remap[used] = torch.arange(used.numel())
+    idx_r = torch.where(idx_s >= 0, remap[idx_s.clamp(min=0)], torch.full_like(idx_s, -1))
+    dev = inp["w1"].device
+    w1 = inp["w1"][used.to(dev)].cpu()
+    w2 = inp["w2"][used.to(dev)].cpu()
+    x = inp["x"][tokens.to(dev)].cpu()
+    ws_ = w[tokens.to(w.device)].cpu().double()
+    return oracle.expert_forward(x, idx_r.to(torch.int32), ws_, w1, w2)

@@ -1,0 +1,119 @@
+"""The C-ABI library on a host without a GPU: it builds, loads, exports every
+symbol include/moe.h declares, and its host-only entry points behave.
+
+No compute entry point is called here with valid arguments (that needs a GPU);
+argument errors are returned before any CUDA call, so they are checked.
+"""
+import ctypes
+import os
+import re
+
+import pytest
+
+from moe_expert_router_gb300 import binding as B
+from moe_expert_router_gb300 import build as moe_build
+from moe_expert_router_gb300.workloads import CONFIGS
+
+HEADER = os.path.join(moe_build.ROOT, "include", "moe.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    moe_build.build()
+    return B.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?[a-z_0-9]+\s*\*?\s*(moe_[a-z_0-9]+)\s*\(", text,
+                                 flags=re.M)))
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    for want in ("moe_router", "moe_routing_metadata", "moe_dispatch_gemm1",
+                 "moe_swiglu_gemm2_combine", "moe_forward", "moe_workspace_size",
+                 "moe_get_device_error"):
+        assert want in names, names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    names = declared_functions()
+    assert len(names) >= 10
+    for name in names:
+        assert hasattr(lib, name), f"libmoe.so does not export {name}"
+    assert set(names) == set(B._SIG), "binding and header disagree"
+
+
+def test_library_does_not_link_the_oracle():
+    data = open(moe_build.LIB_PATH, "rb").read()
+    assert b"oracle_" not in data and b"liboracle" not in data
+
+
+def test_workspace_size_and_layout(lib):
+    for cfg in CONFIGS.values():
+        shp = B.shape(cfg.T, cfg.H, cfg.I, cfg.E, cfg.k)
+        n = B.moe_workspace_size(shp)
+        L = B.moe_workspace_layout(shp)
+        R = cfg.T * cfg.k
+        assert L.total == n
+        offs = [L.counts, L.offsets, L.mt_prefix, L.perm_slot, L.row_of, L.router, L.a, L.obuf]
+        assert all(o % 256 == 0 for o in offs) and offs == sorted(offs) and L.err == 0
+        assert L.offsets - L.counts >= 4 * cfg.E
+        assert L.row_of - L.perm_slot >= 4 * R
+        assert L.a - L.router >= 4 * cfg.T * cfg.E + 8 * cfg.E
+        assert L.obuf - L.a >= 2 * R * cfg.I
+        assert n - L.obuf >= 2 * R * cfg.H
+
+
+@pytest.mark.parametrize("bad,status", [
+    ((4, 60, 64, 4, 2), 2),      # H % 8
+    ((4, 64, 36, 4, 2), 2),      # I % 8
+    ((4, 64, 64, 4, 5), 2),      # k > E
+    ((4, 64, 64, 2048, 2), 2),   # E > 1024
+    ((4, 64, 64, 64, 33), 2),    # k > 32
+    ((-1, 64, 64, 4, 2), 1),     # negative T
+    ((4, 0, 64, 4, 2), 1),       # H = 0
+])
+def test_shape_validation(lib, bad, status):
+    n = ctypes.c_size_t()
+    shp = B.shape(*bad)
+    assert lib.moe_workspace_size(ctypes.byref(shp), ctypes.byref(n)) == status
+
+
+def test_null_arguments_rejected_before_any_device_call(lib):
+    shp = B.shape(16, 64, 64, 4, 2)
+    cfg = B.router_cfg()
+    assert lib.moe_router(None, None, None, None, ctypes.byref(shp), ctypes.byref(cfg), None, None,
+                          None, None, 0, None) == 1
+    assert lib.moe_forward(None, None, None, None, None, ctypes.byref(shp), None, None, 0, None) == 1
+    assert lib.moe_routing_metadata(None, ctypes.byref(shp), None, 0, None) == 1
+    assert lib.moe_dispatch_gemm1(None, None, ctypes.byref(shp), None, None, 0, None) == 1
+    assert lib.moe_swiglu_gemm2_combine(None, None, None, ctypes.byref(shp), None, None, 0,
+                                        None) == 1
+    assert lib.moe_get_device_error(None, None, None) == 1
+    # misaligned workspace and a too-small workspace (host checks, no device touched)
+    x = ctypes.c_void_p(1 << 20)
+    assert lib.moe_routing_metadata(x, ctypes.byref(shp), ctypes.c_void_p((1 << 20) + 16), 1 << 30,
+                                    None) == 1
+    assert lib.moe_routing_metadata(x, ctypes.byref(shp), ctypes.c_void_p(1 << 20), 256, None) == 4
+
+
+def test_router_config_validation(lib):
+    shp = B.shape(16, 64, 64, 64, 8)
+    p = ctypes.c_void_p(1 << 20)
+    for cfg, want in [(B.router_cfg(n_group=7, topk_group=2), 1),     # E % n_group
+                      (B.router_cfg(n_group=8, topk_group=9), 1),     # topk_group > n_group
+                      (B.router_cfg(n_group=16, topk_group=1), 1),    # 1 group of 4 experts < k = 8
+                      (B.router_cfg(n_group=64, topk_group=4), 2),    # n_group > 32
+                      (B.RouterCfg(7, 1, 1.0, 1, 1, 2), 1)]:          # bad score function
+        st = lib.moe_router(p, p, None, None, ctypes.byref(shp), ctypes.byref(cfg), p, p, None, p,
+                            1 << 40, None)
+        assert st == want, (cfg.n_group, cfg.topk_group, st)
+
+
+def test_status_strings_and_counter(lib):
+    for s in range(6):
+        assert B.load().moe_status_string(s)
+    assert B.moe_kernel_launch_count() >= 0
