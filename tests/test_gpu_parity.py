@@ -315,7 +315,11 @@ def test_full_size_config(name):
     if not excluded.any():
         np.testing.assert_array_equal(counts, ref_counts)
     else:
-        touched = np.bincount(ref.topk_idx[excluded].reshape(-1), minlength=cfg.E)
+        # an excluded (near-tie) token may move one row between the expert the
+        # oracle chose and the one the GPU chose: credit both
+        gx = idx.cpu().numpy()[excluded]
+        touched = (np.bincount(ref.topk_idx[excluded].reshape(-1), minlength=cfg.E) +
+                   np.bincount(gx.reshape(-1), minlength=cfg.E))
         assert (np.abs(counts - ref_counts) <= touched).all()
     assert int(offsets[-1]) == cfg.T * cfg.k
     if cfg.score == "softmax":
