@@ -119,6 +119,33 @@ moe_status_t moe_router(const void *x, const float *w_r, const float *logit_offs
                         float *aux, void *ws, size_t ws_bytes, void *stream);
 
 /*
+ * moe_router_noalloc: the same router as moe_router, for callers that cannot
+ * allocate device memory. The pages have no counterpart to this entry point.
+ *
+ * Who needs it: a plug-in running inside a host runtime that owns all device
+ * memory (for example an inference engine with a fixed memory pool) must not
+ * call cudaMalloc, because the host accounts for every byte itself, and it may
+ * have no spare buffer to pass as a workspace. This call takes no workspace:
+ * the router's scratch (the fp32 logits and the aux accumulators) lives in a
+ * static array of about 4 MiB inside the library, which every GPU that loads
+ * the library keeps until the process exits. It allocates nothing.
+ *
+ * Limits: T * E <= 1048576 (the logits must fit the static array); larger
+ * shapes return MOE_ERR_UNSUPPORTED. All other arguments, limits and results
+ * are those of moe_router.
+ *
+ * The first call on each device looks up the array's device address (set-up
+ * once per device); make that first call before any stream capture. All calls
+ * on a device share the one array: calls whose kernels may run at the same
+ * time on the GPU (unordered streams) race on it and give wrong results.
+ * Each call clears the accumulators it needs before using them.
+ */
+moe_status_t moe_router_noalloc(const void *x, const float *w_r, const float *logit_offset,
+                                const float *sel_bias, const moe_shape_t *shape,
+                                const moe_router_cfg_t *cfg, int32_t *topk_idx, float *topk_w,
+                                float *aux, void *stream);
+
+/*
  * Routing metadata: the local stand-in for the dispatch all-to-all (MegaMoE
  * guide, opening section, dispatch_grouped_gemm; section "Router force load
  * balancing": ragged per-expert counts absorbed without padding or host sync).

@@ -56,6 +56,8 @@ _SIG = {
     "moe_workspace_init": [_P, ctypes.c_size_t, _P],
     "moe_router": [_P, _P, _P, _P, ctypes.POINTER(Shape), ctypes.POINTER(RouterCfg), _P, _P, _P,
                    _P, ctypes.c_size_t, _P],
+    "moe_router_noalloc": [_P, _P, _P, _P, ctypes.POINTER(Shape), ctypes.POINTER(RouterCfg), _P,
+                           _P, _P, _P],
     "moe_routing_metadata": [_P, ctypes.POINTER(Shape), _P, ctypes.c_size_t, _P],
     "moe_dispatch_gemm1": [_P, _P, ctypes.POINTER(Shape), _P, _P, ctypes.c_size_t, _P],
     "moe_swiglu_gemm2_combine": [_P, _P, _P, ctypes.POINTER(Shape), _P, _P, ctypes.c_size_t, _P],
@@ -143,6 +145,15 @@ def moe_router(x, w_r, shp, cfg, topk_idx, topk_w, ws, aux=None, logit_offset=No
         _ptr(x), _ptr(w_r), _ptr(logit_offset), _ptr(sel_bias), ctypes.byref(shp),
         ctypes.byref(cfg), _ptr(topk_idx), _ptr(topk_w), _ptr(aux), _ptr(ws),
         ws.numel() * ws.element_size(), _stream(stream, x)))
+
+
+def moe_router_noalloc(x, w_r, shp, cfg, topk_idx, topk_w, aux=None, logit_offset=None,
+                       sel_bias=None, stream=None):
+    """moe_router without a workspace: for callers that may not allocate device
+    memory (the scratch lives in a static array inside libmoe; T * E <= 2**20)."""
+    _check("moe_router_noalloc", load().moe_router_noalloc(
+        _ptr(x), _ptr(w_r), _ptr(logit_offset), _ptr(sel_bias), ctypes.byref(shp),
+        ctypes.byref(cfg), _ptr(topk_idx), _ptr(topk_w), _ptr(aux), _stream(stream, x)))
 
 
 def moe_routing_metadata(topk_idx, shp, ws, stream=None):

@@ -1,0 +1,136 @@
+// router_noalloc.cu -- moe_router_noalloc: the router for callers that cannot
+// allocate device memory and so cannot hand the library a workspace.
+//
+// Such callers are plug-ins hosted by a runtime that owns every byte of device
+// memory (an inference engine or serving process with a fixed pool that has
+// already been carved up): they are not allowed to call cudaMalloc, and their
+// host gives them no spare buffer for the router's intermediate logits. This
+// entry point therefore keeps that scratch in a fixed-size array that lives
+// inside the library image itself.
+//
+// It runs exactly the same kernels as moe_router; only the location of the
+// scratch differs.
+#include <mutex>
+
+#include "internal.cuh"
+
+namespace moe {
+
+namespace {
+
+// Capacity of the static scratch: logits for at most kMaxLogits = T * E
+// values, plus per-expert score sums and counts for up to 1024 experts, plus
+// the block ticket of the top-k kernel.
+constexpr size_t kMaxLogits = size_t(1) << 20;                 // 4 MiB of fp32 logits
+constexpr size_t kLogitsBytes = kMaxLogits * sizeof(float);
+constexpr size_t kSumsOffset = kLogitsBytes;
+constexpr size_t kCountsOffset = kSumsOffset + 1024 * sizeof(float);
+constexpr size_t kTicketOffset = kCountsOffset + 1024 * sizeof(int32_t);
+constexpr size_t kScratchBytes = kTicketOffset + 256;
+
+// Every GPU that loads this library holds this array until the process exits.
+// All calls on a device share it, so calls whose kernels overlap on the GPU
+// (different streams without ordering between them) race on it.
+static __device__ __align__(256) unsigned char g_router_scratch[kScratchBytes];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_mu;
+bool g_ready[kMaxDevices];
+moe_status_t g_status[kMaxDevices];
+unsigned char *g_scratch_ptr[kMaxDevices];
+
+// Once per device, with that device current: check the architecture and look
+// up the device address of the static array (a host-side use of its name is
+// only a stand-in, not a device pointer).
+moe_status_t scratch_for_current_device(unsigned char **out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
+    if (dev < 0 || dev >= kMaxDevices) return MOE_ERR_UNSUPPORTED;
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (!g_ready[dev]) {
+        g_ready[dev] = true;
+        int major = 0, minor = 0;
+        void *p = nullptr;
+        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess) {
+            g_status[dev] = MOE_ERR_CUDA;
+        } else if (major != 10 || minor != 3) {
+            g_status[dev] = MOE_ERR_UNSUPPORTED;
+        } else if (cudaGetSymbolAddress(&p, g_router_scratch) != cudaSuccess || p == nullptr) {
+            g_status[dev] = MOE_ERR_CUDA;
+        } else {
+            g_status[dev] = MOE_OK;
+            g_scratch_ptr[dev] = static_cast<unsigned char *>(p);
+        }
+        cudaGetLastError();
+    }
+    *out = g_scratch_ptr[dev];
+    return g_status[dev];
+}
+
+bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+}  // namespace
+
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" moe_status_t moe_router_noalloc(const void *x, const float *w_r,
+                                           const float *logit_offset, const float *sel_bias,
+                                           const moe_shape_t *shape, const moe_router_cfg_t *cfg,
+                                           int32_t *topk_idx, float *topk_w, float *aux,
+                                           void *stream) {
+    if (shape == nullptr || cfg == nullptr) return MOE_ERR_INVALID_ARG;
+    const moe_shape_t &s = *shape;
+    if (s.T < 0 || s.H <= 0 || s.I <= 0 || s.E <= 0 || s.k <= 0 || s.reserved != 0)
+        return MOE_ERR_INVALID_ARG;
+    if (s.k > 32 || s.k > s.E || s.E > 1024 || s.H % 8 != 0 || s.I % 8 != 0 ||
+        s.H >= (int64_t(1) << 31) || s.T * s.k >= (int64_t(1) << 31))
+        return MOE_ERR_UNSUPPORTED;
+    // the static scratch holds at most kMaxLogits router logits
+    if (s.T * s.E > static_cast<int64_t>(kMaxLogits)) return MOE_ERR_UNSUPPORTED;
+    if (s.T == 0) return MOE_OK;
+    if (x == nullptr || w_r == nullptr || topk_idx == nullptr || topk_w == nullptr)
+        return MOE_ERR_INVALID_ARG;
+    if (!aligned(x, 16) || !aligned(w_r, 16) || !aligned(topk_idx, 16) || !aligned(topk_w, 16) ||
+        !aligned(logit_offset, 4) || !aligned(sel_bias, 4) || !aligned(aux, 4))
+        return MOE_ERR_INVALID_ARG;
+    if (cfg->score_fn != MOE_SCORE_SOFTMAX && cfg->score_fn != MOE_SCORE_SIGMOID) return MOE_ERR_INVALID_ARG;
+    if (cfg->n_group < 1 || cfg->n_group > 32) return MOE_ERR_UNSUPPORTED;
+    if (cfg->n_group > 1) {
+        if (s.E % cfg->n_group != 0 || cfg->topk_group < 1 || cfg->topk_group > cfg->n_group ||
+            cfg->group_topn < 1 || cfg->group_topn > s.E / cfg->n_group ||
+            static_cast<int64_t>(cfg->topk_group) * (s.E / cfg->n_group) < s.k)
+            return MOE_ERR_INVALID_ARG;
+    }
+    unsigned char *scratch = nullptr;
+    moe_status_t r = scratch_for_current_device(&scratch);
+    if (r != MOE_OK) return r;
+
+    RouterLaunch p;
+    p.x = static_cast<const __nv_bfloat16 *>(x);
+    p.w_r = w_r;
+    p.logit_offset = logit_offset;
+    p.sel_bias = sel_bias;
+    p.T = static_cast<int>(s.T);
+    p.H = static_cast<int>(s.H);
+    p.E = static_cast<int>(s.E);
+    p.k = s.k;
+    p.score_fn = cfg->score_fn;
+    p.normalize = cfg->normalize;
+    p.scale = cfg->scale;
+    p.n_group = cfg->n_group;
+    p.topk_group = cfg->topk_group;
+    p.group_topn = cfg->group_topn;
+    p.topk_idx = topk_idx;
+    p.topk_w = topk_w;
+    p.aux = aux;
+    // the router's logits kernel clears the sums, counts and ticket at the start
+    // of every call, so nothing left in the array by an earlier call is read
+    p.scratch.logits = reinterpret_cast<float *>(scratch);
+    p.scratch.score_sum = reinterpret_cast<float *>(scratch + kSumsOffset);
+    p.scratch.counts = reinterpret_cast<int32_t *>(scratch + kCountsOffset);
+    p.scratch.ticket = reinterpret_cast<int32_t *>(scratch + kTicketOffset);
+    return launch_router(p, static_cast<cudaStream_t>(stream)) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}

@@ -1,0 +1,85 @@
+"""moe_router_noalloc against moe_router, through the C ABI.
+
+moe_router_noalloc serves callers that may not allocate device memory -- a
+plug-in inside a host runtime that owns every byte of device memory and gives
+it no workspace. It keeps the router's scratch in a static array inside the
+library instead of a caller-supplied workspace. This test checks that it gives
+the same routing as the workspace-based entry point on two calls in a row (the
+second call must not be disturbed by what the first left in the shared array),
+and that it refuses shapes whose logits do not fit that array.
+
+This file is named to be collected last.
+"""
+import numpy as np
+import pytest
+import torch
+
+from moe_expert_router_gb300 import binding as B
+from moe_expert_router_gb300.workloads import MoEConfig, generate
+
+pytestmark = pytest.mark.gpu
+
+CASES = [
+    MoEConfig("noalloc_softmax", T=4096, H=1024, I=64, E=64, k=6),
+    MoEConfig("noalloc_groups", T=2048, H=512, I=64, E=256, k=8, score="sigmoid", scale=2.5,
+              n_group=8, topk_group=4, group_topn=2, sel_bias=True),
+]
+
+
+def _cfg(c):
+    return B.router_cfg(c.score, c.normalize, c.scale, c.n_group, c.topk_group, c.group_topn)
+
+
+def _outputs(c):
+    return (torch.empty((c.T, c.k), dtype=torch.int32, device="cuda"),
+            torch.empty((c.T, c.k), dtype=torch.float32, device="cuda"),
+            torch.zeros((1,), dtype=torch.float32, device="cuda"))
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _device():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    B.load()
+
+
+def test_noalloc_router_matches_workspace_router_twice_in_a_row():
+    results = []
+    for c in CASES:                                   # two calls in a row, different shapes
+        inp = generate(c, seed=21, device="cuda")
+        shp = B.shape(c.T, c.H, c.I, c.E, c.k)
+        idx_n, w_n, aux_n = _outputs(c)
+        B.moe_router_noalloc(inp["x"], inp["w_r"], shp, _cfg(c), idx_n, w_n, aux=aux_n,
+                             logit_offset=inp["logit_offset"], sel_bias=inp["sel_bias"])
+        ws = B.new_workspace(shp)
+        idx_r, w_r, aux_r = _outputs(c)
+        B.moe_router(inp["x"], inp["w_r"], shp, _cfg(c), idx_r, w_r, ws, aux=aux_r,
+                     logit_offset=inp["logit_offset"], sel_bias=inp["sel_bias"])
+        torch.cuda.synchronize()
+        results.append((c, idx_n.cpu(), w_n.cpu(), aux_n.cpu(), idx_r.cpu(), w_r.cpu(), aux_r.cpu()))
+    for c, idx_n, w_n, aux_n, idx_r, w_r, aux_r in results:
+        # the same kernels run on the same inputs: routing identical, weights and
+        # aux within the tolerance the router parity tests use
+        assert torch.equal(idx_n, idx_r), c.name
+        np.testing.assert_allclose(w_n.numpy(), w_r.numpy(), rtol=1e-4, atol=1e-6)
+        np.testing.assert_allclose(aux_n.numpy(), aux_r.numpy(), rtol=1e-4)
+    # the first case again: the array now holds the second case's scratch
+    c = CASES[0]
+    inp = generate(c, seed=21, device="cuda")
+    shp = B.shape(c.T, c.H, c.I, c.E, c.k)
+    idx_n, w_n, aux_n = _outputs(c)
+    B.moe_router_noalloc(inp["x"], inp["w_r"], shp, _cfg(c), idx_n, w_n, aux=aux_n)
+    torch.cuda.synchronize()
+    assert torch.equal(idx_n.cpu(), results[0][4])
+    np.testing.assert_allclose(aux_n.cpu().numpy(), results[0][6].numpy(), rtol=1e-4)
+
+
+def test_noalloc_router_rejects_shapes_beyond_its_scratch():
+    c = MoEConfig("too_big", T=8193, H=64, I=64, E=128, k=2)      # T * E > 2**20
+    shp = B.shape(c.T, c.H, c.I, c.E, c.k)
+    x = torch.zeros((c.T, c.H), dtype=torch.bfloat16, device="cuda")
+    w_r = torch.zeros((c.E, c.H), dtype=torch.float32, device="cuda")
+    idx, w, aux = _outputs(c)
+    with pytest.raises(B.MoEError) as e:
+        B.moe_router_noalloc(x, w_r, shp, _cfg(c), idx, w, aux=aux)
+    assert e.value.status == 2   # MOE_ERR_UNSUPPORTED
