@@ -78,10 +78,10 @@ typedef struct moe_ws_layout {
     size_t err;        /* int32 error word (first 4 bytes) */
     size_t counts;     /* int32 [E]   rows routed to each expert */
     size_t offsets;    /* int32 [E+1] exclusive prefix sum of counts */
-    size_t mt_prefix;  /* int32 [E+1] prefix sum of ceil(counts/128) (row tiles) */
+    size_t mt_prefix;  /* int32 [E+1] prefix sum of ceil(counts/256) (row tiles) */
     size_t perm_slot;  /* int32 [T*k] flat slot t*k+j of each routed row */
     size_t row_of;     /* int32 [T*k] routed row of each slot, -1 if dropped */
-    size_t router;     /* router scratch: float logits [T,E], float score sums [E], int32 counts [E] */
+    size_t router;     /* router scratch: fp32 split-K partial logits [s,T,E], bf16 split of w_r [3,E,H], sums, counts */
     size_t a;          /* bf16 [T*k, I] SwiGLU activations (moe_forward only) */
     size_t obuf;       /* bf16 [T*k, H] weighted expert outputs in slot order */
     size_t total;      /* == moe_workspace_size */
@@ -126,13 +126,15 @@ moe_status_t moe_router(const void *x, const float *w_r, const float *logit_offs
  * memory (for example an inference engine with a fixed memory pool) must not
  * call cudaMalloc, because the host accounts for every byte itself, and it may
  * have no spare buffer to pass as a workspace. This call takes no workspace:
- * the router's scratch (the fp32 logits and the aux accumulators) lives in a
- * static array of about 4 MiB inside the library, which every GPU that loads
- * the library keeps until the process exits. It allocates nothing.
+ * the router's scratch (the bf16 split of w_r, the split-K partial logits and
+ * the aux accumulators) lives in a static array of 10 MiB + 9 KiB inside the
+ * library, which every GPU that loads the library keeps until the process
+ * exits. It allocates nothing.
  *
- * Limits: T * E <= 1048576 (the logits must fit the static array); larger
- * shapes return MOE_ERR_UNSUPPORTED. All other arguments, limits and results
- * are those of moe_router.
+ * Limits: T * E <= 1048576 and E * H <= 1048576 (the scratch must fit the
+ * static array); larger shapes return MOE_ERR_UNSUPPORTED. All other arguments,
+ * limits and results are those of moe_router, except that the split-K factor
+ * may be lower, which can change the last bits of the fp32 logits.
  *
  * The first call on each device looks up the array's device address (set-up
  * once per device); make that first call before any stream capture. All calls

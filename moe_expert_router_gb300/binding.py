@@ -150,7 +150,7 @@ def moe_router(x, w_r, shp, cfg, topk_idx, topk_w, ws, aux=None, logit_offset=No
 def moe_router_noalloc(x, w_r, shp, cfg, topk_idx, topk_w, aux=None, logit_offset=None,
                        sel_bias=None, stream=None):
     """moe_router without a workspace: for callers that may not allocate device
-    memory (the scratch lives in a static array inside libmoe; T * E <= 2**20)."""
+    memory (the scratch lives in a static array inside libmoe; T * E <= 2**20, E * H <= 2**20)."""
     _check("moe_router_noalloc", load().moe_router_noalloc(
         _ptr(x), _ptr(w_r), _ptr(logit_offset), _ptr(sel_bias), ctypes.byref(shp),
         ctypes.byref(cfg), _ptr(topk_idx), _ptr(topk_w), _ptr(aux), _stream(stream, x)))

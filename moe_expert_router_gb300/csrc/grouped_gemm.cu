@@ -1,33 +1,48 @@
-// grouped_gemm.cu -- the two expert-path grouped GEMMs of the MegaMoE layer on
+// grouped_gemm.cu -- the tensor-core GEMMs of the MegaMoE expert path on
 // sm_103a, plus the final k-way combine.
 //
 //   stage 1, dispatch_grouped_gemm (MegaMoE guide, opening section; section
 //   "Design: two stages", stage1 = dispatch + GEMM1): for each routed row r of
 //   expert e, h = x[token(r)] . w1[e]^T and a[r] = silu(h[:I]) * h[I:]
 //   (SwiGLU silu(x_glu) * x_linear, as in the "GDN <-> FLA Parity in Primus"
-//   page, section B). The dispatch is a TMA row gather (tile::gather4) of x
-//   driven by the routing permutation, so no permuted copy of x is made.
+//   page, section B). The dispatch is fused: dedicated warps gather the
+//   routed x rows straight into the shared-memory A tiles, driven by the
+//   routing permutation, so no permuted copy of x is ever written.
 //
 //   stage 2, grouped_gemm_combine (stage2 = GEMM2 + combine): o[r] = a[r] .
 //   w2[e]^T; the epilogue scales o[r] by the routing weight of its slot and
-//   scatters it to the slot's row of obuf (slot order t*k + j), and a light
-//   reduction sums the k rows of every token into y.
+//   scatters it to the slot's row of obuf (slot order t*k + j); a light
+//   reduction then sums the k rows of every token into y.
 //
-// Kernel design (one CTA per SM, persistent over work units):
-//   work unit  = (expert e, n-tile, 128-row tile of e's routed rows), ordered
-//                expert-major, then n-tile, then row tile, so that CTAs running
-//                side by side share a weight slab through L2;
-//   warp 0     = TMA producer (x row gather / a tile, weight slabs) into a
-//                4-stage ring of 128B-swizzled K-major tiles (BK = 64);
-//   warp 1     = TMEM allocator and single-thread tcgen05.mma issuer
-//                (M = 128, N = 256, K = 16 per instruction, fp32 accumulate);
-//   warps 2-5  = epilogue: tcgen05.ld of the accumulator, fused SwiGLU or
-//                weighted scatter, bf16 stores. Two TMEM accumulators (512
-//                columns) let the epilogue of one unit overlap the next
-//                unit's main loop.
-// Row counts per expert are read from device memory, so any (ragged) routing
-// runs without a host sync or re-launch. Rows of a tile past the expert's
-// count are computed on stale or foreign data and never stored.
+//   router GEMM (the fused router's score function, MegaMoE guide opening
+//   section): partial fp32 logits of x . w_r^T with w_r split exactly into
+//   three bf16 matrices hi + mid + lo (Henry, Tang and Heinecke 2019,
+//   "Leveraging the bfloat16 artificial intelligence datatype for higher-
+//   precision computations"); x is bf16, so every product is exact and the
+//   fp32 accumulation matches an fp32 dot product. Split-K partials are
+//   summed in a fixed order by the top-k kernel.
+//
+// Kernel design (one CTA per SM, persistent):
+//   work unit  = (expert e, n-tile, 256-row tile of e's routed rows) for the
+//                grouped stages, (256-row tile, n-tile, k split) for the
+//                router. The 256 rows are two 128-row halves that share every
+//                weight tile, which halves the weight bytes each SM loads per
+//                flop against a 128-row tile; an empty second half is neither
+//                loaded nor multiplied. Grouped units are numbered
+//                expert-major, then n-tile, then row tile; CTAs take the next
+//                unit from a global counter, so CTAs running side by side work
+//                on neighbouring units and share each weight slab through L2.
+//   warp 0     = scheduler + TMA producer: claims units, publishes them to an
+//                in-CTA queue and fills a 3-stage ring of 128B-swizzled
+//                K-major tiles (per stage: two 128x64 A halves, one 256x64 B).
+//   warp 1     = TMEM allocator and single-thread tcgen05.mma issuer: per
+//                16-deep k-step one M=128 N=256 MMA per half into two fp32
+//                TMEM accumulators (all 512 columns).
+//   warps 2-9  = epilogue, one TMEM lane quadrant of one half each:
+//                tcgen05.ld, then fused SwiGLU, weighted scatter or fp32 store.
+// Row counts are read from device memory, so ragged routing never needs a
+// host sync or a re-launch. Rows of a tile past the expert's count are
+// computed on stale or foreign data and never stored.
 #include "internal.cuh"
 #include "ptx.cuh"
 
@@ -35,28 +50,42 @@ namespace moe {
 
 namespace {
 
-constexpr int BM = kBM;          // 128 rows per tile (MMA M)
-constexpr int BK = 64;           // 64 bf16 = one 128-byte swizzled row per stage
-constexpr int BN = 256;          // accumulator columns per tile (MMA N)
+constexpr int BM = kBM;                      // rows per MMA / per accumulator
+constexpr int UM = kUnitM;                   // rows per work unit (two halves)
+constexpr int BK = kBK;
+constexpr int BN = kBN;
 constexpr int UMMA_K = 16;
-constexpr int STAGES = 4;
-constexpr int A_BYTES = BM * BK * 2;
-constexpr int B_BYTES = BN * BK * 2;
-constexpr int ACC_STAGES = 2;
-constexpr int TMEM_COLS = ACC_STAGES * BN;   // 512: the whole TMEM of the SM
-constexpr int NUM_THREADS = 192;
-constexpr int EPI_THREADS = 128;
+constexpr int STAGES = 3;
+constexpr int A_HALF_BYTES = BM * BK * 2;    // 16 KB
+constexpr int A_BYTES = 2 * A_HALF_BYTES;    // 32 KB
+constexpr int B_BYTES = BN * BK * 2;         // 32 KB
+constexpr int TMEM_COLS = 2 * BN;            // two accumulators: all 512 columns
+constexpr int EPI_WARPS = 8;
+constexpr int EPI_THREADS = EPI_WARPS * 32;
+constexpr int GATHER_WARPS = 4;              // stage 1: x row gather into the A tiles
+constexpr int GATHER_THREADS = GATHER_WARPS * 32;
+constexpr int UQ = 4;                        // depth of the in-CTA unit queue
 constexpr uint32_t IDESC = idesc_bf16_f32(BM, BN);
 constexpr uint64_t kDrainLimitNs = 10000000ull;  // 10 ms
+
+enum Mode : int { kStage1 = 0, kStage2 = 1, kRouter = 2 };
+
+// warps: 0 scheduler + TMA producer, 1 MMA issuer, 2..9 epilogue, and in
+// stage 1 also 10..13 gathering the routed x rows
+template <int MODE>
+constexpr int kNumThreads = 64 + EPI_THREADS + (MODE == kStage1 ? GATHER_THREADS : 0);
 
 struct __align__(1024) Smem {
     uint8_t a[STAGES][A_BYTES];
     uint8_t b[STAGES][B_BYTES];
     uint64_t full[STAGES];
     uint64_t empty[STAGES];
-    uint64_t acc_full[ACC_STAGES];
-    uint64_t acc_empty[ACC_STAGES];
+    uint64_t acc_full;
+    uint64_t acc_empty;
+    uint64_t uq_full[UQ];
+    uint64_t uq_empty[UQ];
     uint64_t drain;
+    int unit_q[UQ];
     uint32_t tmem_base;
     int abort;
 };
@@ -68,38 +97,75 @@ struct GemmArgs {
     const int32_t *offsets;
     const int32_t *mt_prefix;
     const int32_t *perm_slot;
+    const __nv_bfloat16 *x;  // stage 1: token rows [T, K]
     int32_t *err;
+    int32_t *sched;          // [0] next unit, [1] CTAs finished
     const float *topk_w;
     __nv_bfloat16 *out;
+    float *logits_part;      // router
     int E, k, K;
-    int n_out;      // valid output columns (I or H)
-    int n_tiles;    // n-tiles per expert
-    int b_rows;     // weight rows per expert (2I or H)
-    int half;       // stage 1: row offset of the up projection inside w1[e] (= I)
+    int n_out;               // valid output columns (I, H or E)
+    int n_tiles;             // n-tiles per expert (grouped) or per row tile (router)
+    int b_rows;              // weight rows per expert (2I or H)
+    int half;                // stage 1: row offset of the up projection inside w1[e] (= I)
+    int T, splits, kb_per_split, kb_total, kb_h;   // router
+    int total_units;         // router: known on the host; grouped: -1 (read from the device)
 };
 
 struct Unit {
-    int e, n, row0, rows;
+    int e, n, row0, rows, kb0, kb1, split;
 };
 
-// Unit u -> (expert, n-tile, row tile). Units of expert e are
-// [mt_prefix[e] * n_tiles, mt_prefix[e+1] * n_tiles), n-tile major.
+template <int MODE>
 __device__ __forceinline__ Unit decode_unit(int u, const GemmArgs &g) {
-    int lo = 0, hi = g.E;
-    while (hi - lo > 1) {
-        const int mid = (lo + hi) >> 1;
-        if (g.mt_prefix[mid] * g.n_tiles <= u) lo = mid; else hi = mid;
-    }
-    const int mt0 = g.mt_prefix[lo];
-    const int mt_e = g.mt_prefix[lo + 1] - mt0;
-    const int local = u - mt0 * g.n_tiles;
     Unit t;
-    t.e = lo;
-    t.n = local / mt_e;
-    const int m = local - t.n * mt_e;
-    t.row0 = g.offsets[lo] + m * BM;
-    t.rows = min(BM, g.counts[lo] - m * BM);
+    if constexpr (MODE == kRouter) {
+        const int per_m = g.n_tiles * g.splits;
+        const int m = u / per_m;
+        const int rem = u - m * per_m;
+        t.n = rem / g.splits;
+        t.split = rem - t.n * g.splits;
+        t.e = 0;
+        t.row0 = m * UM;
+        t.rows = min(UM, g.T - t.row0);
+        t.kb0 = t.split * g.kb_per_split;
+        t.kb1 = min(g.kb_total, t.kb0 + g.kb_per_split);
+    } else {
+        // units of expert e are [mt_prefix[e] * n_tiles, mt_prefix[e+1] * n_tiles)
+        int lo = 0, hi = g.E;
+        while (hi - lo > 1) {
+            const int mid = (lo + hi) >> 1;
+            if (g.mt_prefix[mid] * g.n_tiles <= u) lo = mid; else hi = mid;
+        }
+        const int mt0 = g.mt_prefix[lo];
+        const int mt_e = g.mt_prefix[lo + 1] - mt0;
+        const int local = u - mt0 * g.n_tiles;
+        t.e = lo;
+        t.n = local / mt_e;
+        const int m = local - t.n * mt_e;
+        t.row0 = g.offsets[lo] + m * UM;
+        t.rows = min(UM, g.counts[lo] - m * UM);
+        t.kb0 = 0;
+        t.kb1 = (g.K + BK - 1) / BK;
+        t.split = 0;
+    }
     return t;
+}
+
+// Weight (B operand) coordinates of k-block kb: inner coordinate and first row.
+template <int MODE>
+__device__ __forceinline__ void b_coords(const GemmArgs &g, const Unit &t, int kb, int &kx, int &row) {
+    if constexpr (MODE == kRouter) {
+        const int seg = kb / g.kb_h;              // 0: hi, 1: mid, 2: lo
+        kx = (kb - seg * g.kb_h) * BK;
+        row = seg * g.E + t.n * BN;
+    } else if constexpr (MODE == kStage1) {
+        kx = kb * BK;
+        row = t.e * g.b_rows + t.n * (BN / 2);
+    } else {
+        kx = kb * BK;
+        row = t.e * g.b_rows + t.n * BN;
+    }
 }
 
 // Wait that ignores the abort flag and sets no error: used only to let
@@ -115,26 +181,30 @@ __device__ __forceinline__ float silu_mul(float g, float u) {
     return g / (1.0f + __expf(-g)) * u;
 }
 
-template <bool kSwiGLU>
-__global__ void __launch_bounds__(NUM_THREADS, 1)
-grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_a,
-                    const __grid_constant__ CUtensorMap tm_b, const GemmArgs g) {
+template <int MODE>
+__global__ void __launch_bounds__(kNumThreads<MODE>, 1)
+tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
+               const GemmArgs g) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_addr(smem_raw);
     Smem &sm = *reinterpret_cast<Smem *>(smem_raw + ((1024u - (raw & 1023u)) & 1023u));
     volatile int *abort_flag = &sm.abort;
+    volatile int *unit_q = sm.unit_q;
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
-            mbar_init(smem_addr(&sm.full[s]), 1);
+            // stage 1: the producer's expect_tx arrival plus one per gather thread
+            mbar_init(smem_addr(&sm.full[s]), MODE == kStage1 ? 1 + GATHER_THREADS : 1);
             mbar_init(smem_addr(&sm.empty[s]), 1);
         }
-        for (int s = 0; s < ACC_STAGES; ++s) {
-            mbar_init(smem_addr(&sm.acc_full[s]), 1);
-            mbar_init(smem_addr(&sm.acc_empty[s]), EPI_THREADS);
+        mbar_init(smem_addr(&sm.acc_full), 1);
+        mbar_init(smem_addr(&sm.acc_empty), EPI_THREADS);
+        for (int s = 0; s < UQ; ++s) {
+            mbar_init(smem_addr(&sm.uq_full[s]), 1);
+            mbar_init(smem_addr(&sm.uq_empty[s]), 1 + EPI_WARPS + (MODE == kStage1 ? GATHER_WARPS : 0));
         }
         mbar_init(smem_addr(&sm.drain), 1);
         sm.abort = 0;
@@ -151,51 +221,55 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_a,
     tc_fence_after();
     const uint32_t tmem_base = sm.tmem_base;
 
-    const int total = g.mt_prefix[g.E] * g.n_tiles;
-    const int num_kb = (g.K + BK - 1) / BK;
-
     if (warp == 0) {
-        // ------------------------------------------------------------ TMA producer
-        int stage = 0, issued = 0;
-        uint32_t phase = 0;
+        // ------------------------------------------------ scheduler + TMA producer
+        const int total = (MODE == kRouter) ? g.total_units : g.mt_prefix[g.E] * g.n_tiles;
+        int stage = 0, issued = 0, q = 0;
+        uint32_t phase = 0, qphase = 0;
         bool ok = true;
-        for (int u = blockIdx.x; u < total && ok; u += gridDim.x) {
-            const Unit t = decode_unit(u, g);
-            const int brow = t.e * g.b_rows + t.n * (kSwiGLU ? BN / 2 : BN);
-            int tok[4] = {0, 0, 0, 0};
-            uint32_t a_bytes = A_BYTES;
-            int n_gather = 0;
-            if constexpr (kSwiGLU) {
-                // rows 4*lane .. 4*lane+3 of the tile; rows past the count reuse row 0
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const int r = lane * 4 + q;
-                    tok[q] = g.perm_slot[t.row0 + (r < t.rows ? r : 0)] / g.k;
+        while (true) {
+            int u = 0;
+            if (lane == 0) u = atomicAdd(&g.sched[0], 1);
+            u = __shfl_sync(0xffffffffu, u, 0);
+            const bool more = u < total;
+            bool w_ok = true;
+            if (lane == 0) {
+                w_ok = mbar_wait(smem_addr(&sm.uq_empty[q]), qphase ^ 1u, abort_flag, g.err);
+                if (w_ok) {
+                    unit_q[q] = more ? u : -1;
+                    mbar_arrive(smem_addr(&sm.uq_full[q]));
                 }
-                n_gather = (t.rows + 3) >> 2;
-                a_bytes = static_cast<uint32_t>(n_gather) * 4u * BK * 2u;
             }
-            for (int kb = 0; kb < num_kb; ++kb) {
-                bool w_ok = true;
-                if (lane == 0) w_ok = mbar_wait(smem_addr(&sm.empty[stage]), phase ^ 1u, abort_flag, g.err);
-                w_ok = __shfl_sync(0xffffffffu, w_ok, 0);
-                if (!w_ok) { ok = false; break; }
+            w_ok = __shfl_sync(0xffffffffu, w_ok, 0);
+            if (!w_ok) { ok = false; break; }
+            if (++q == UQ) { q = 0; qphase ^= 1u; }
+            if (!more) break;
+
+            const Unit t = decode_unit<MODE>(u, g);
+            const bool two = t.rows > BM;            // second half present
+            // stage 1: the A rows arrive through the gather warps, not TMA
+            const uint32_t a_bytes = (MODE == kStage1) ? 0u : (two ? A_BYTES : A_HALF_BYTES);
+            for (int kb = t.kb0; kb < t.kb1; ++kb) {
+                bool e_ok = true;
+                if (lane == 0) e_ok = mbar_wait(smem_addr(&sm.empty[stage]), phase ^ 1u, abort_flag, g.err);
+                e_ok = __shfl_sync(0xffffffffu, e_ok, 0);
+                if (!e_ok) { ok = false; break; }
                 const uint32_t full = smem_addr(&sm.full[stage]);
                 const uint32_t sa = smem_addr(sm.a[stage]);
                 const uint32_t sb = smem_addr(sm.b[stage]);
-                const int kx = kb * BK;
+                int kx, brow;
+                b_coords<MODE>(g, t, kb, kx, brow);
                 if (lane == 0) mbar_arrive_expect_tx(full, a_bytes + B_BYTES);
                 __syncwarp();
-                if constexpr (kSwiGLU) {
-                    if (lane < n_gather)
-                        tma_gather4(sa + lane * 4 * (BK * 2), &tm_a, kx, tok[0], tok[1], tok[2], tok[3], full);
+                if constexpr (MODE == kStage1) {
                     if (lane == 0) {
-                        tma_load_2d(sb, &tm_b, kx, brow, full);                       // gate rows
-                        tma_load_2d(sb + B_BYTES / 2, &tm_b, kx, brow + g.half, full);  // up rows
+                        tma_load_2d(sb, &tm_b, kx, brow, full);                        // gate rows
+                        tma_load_2d(sb + B_BYTES / 2, &tm_b, kx, brow + g.half, full);   // up rows
                     }
                 } else {
                     if (lane == 0) {
                         tma_load_2d(sa, &tm_a, kx, t.row0, full);
+                        if (two) tma_load_2d(sa + A_HALF_BYTES, &tm_a, kx, t.row0 + BM, full);
                         tma_load_2d(sb, &tm_b, kx, brow, full);
                     }
                 }
@@ -203,6 +277,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_a,
                 ++issued;
                 if (++stage == STAGES) { stage = 0; phase ^= 1u; }
             }
+            if (!ok) break;
         }
         if (!ok && lane == 0) {
             // let the copies already issued land before the CTA exits
@@ -214,19 +289,26 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_a,
             }
         }
     } else if (warp == 1) {
-        // ------------------------------------------------------------ MMA issuer
+        // ------------------------------------------------ MMA issuer
         if (lane == 0) {
-            int stage = 0, acc = 0;
-            uint32_t phase = 0, acc_phase = 0;
+            int stage = 0, q = 0;
+            uint32_t phase = 0, acc_phase = 0, qphase = 0;
             bool ok = true, any = false;
-            for (int u = blockIdx.x; u < total && ok; u += gridDim.x) {
-                if (!mbar_wait(smem_addr(&sm.acc_empty[acc]), acc_phase ^ 1u, abort_flag, g.err)) {
+            while (true) {
+                if (!mbar_wait(smem_addr(&sm.uq_full[q]), qphase, abort_flag, g.err)) { ok = false; break; }
+                const int u = unit_q[q];
+                mbar_arrive(smem_addr(&sm.uq_empty[q]));
+                if (++q == UQ) { q = 0; qphase ^= 1u; }
+                if (u < 0) break;
+                const Unit t = decode_unit<MODE>(u, g);
+                const bool two = t.rows > BM;
+                // the epilogue must have drained both accumulators of the previous unit
+                if (!mbar_wait(smem_addr(&sm.acc_empty), acc_phase ^ 1u, abort_flag, g.err)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
-                for (int kb = 0; kb < num_kb; ++kb) {
+                for (int kb = t.kb0; kb < t.kb1; ++kb) {
                     if (!mbar_wait(smem_addr(&sm.full[stage]), phase, abort_flag, g.err)) {
                         ok = false;
                         break;
@@ -236,16 +318,20 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_a,
                     const uint32_t sb = smem_addr(sm.b[stage]);
 #pragma unroll
                     for (int kk = 0; kk < BK / UMMA_K; ++kk) {
-                        mma_bf16(d_tmem, smem_desc_sw128(sa + kk * UMMA_K * 2),
-                                 smem_desc_sw128(sb + kk * UMMA_K * 2), IDESC, (kb | kk) != 0);
+                        const uint32_t acc = (kb > t.kb0 || kk > 0) ? 1u : 0u;
+                        const uint64_t bdesc = smem_desc_sw128(sb + kk * UMMA_K * 2);
+                        mma_bf16(tmem_base, smem_desc_sw128(sa + kk * UMMA_K * 2), bdesc, IDESC, acc);
+                        if (two)
+                            mma_bf16(tmem_base + BN, smem_desc_sw128(sa + A_HALF_BYTES + kk * UMMA_K * 2), bdesc,
+                                     IDESC, acc);
                     }
                     mma_commit(smem_addr(&sm.empty[stage]));   // frees the smem stage
                     any = true;
                     if (++stage == STAGES) { stage = 0; phase ^= 1u; }
                 }
                 if (!ok) break;
-                mma_commit(smem_addr(&sm.acc_full[acc]));      // accumulator ready
-                if (++acc == ACC_STAGES) { acc = 0; acc_phase ^= 1u; }
+                mma_commit(smem_addr(&sm.acc_full));           // accumulators ready
+                acc_phase ^= 1u;
             }
             if (!ok && any) {
                 mma_commit(smem_addr(&sm.drain));
@@ -253,83 +339,198 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_a,
             }
         }
         __syncwarp();
-    } else {
-        // ------------------------------------------------------------ epilogue
-        const int quad = warp & 3;              // TMEM lanes this warp may access
-        const int row = quad * 32 + lane;       // tile row = TMEM lane
-        int acc = 0;
-        uint32_t acc_phase = 0;
-        for (int u = blockIdx.x; u < total; u += gridDim.x) {
-            const Unit t = decode_unit(u, g);
+    } else if (warp < 2 + EPI_WARPS) {
+        // ------------------------------------------------ epilogue
+        const int quad = warp & 3;                  // TMEM lanes this warp may access
+        const int half = (warp - 2) >> 2;           // accumulator (row half) of this warp
+        const int row = half * BM + quad * 32 + lane;   // unit row
+        const uint32_t tacc = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) +
+                              static_cast<uint32_t>(half * BN);
+        int q = 0;
+        uint32_t acc_phase = 0, qphase = 0;
+        while (true) {
             bool ok = true;
-            if (lane == 0) ok = mbar_wait(smem_addr(&sm.acc_full[acc]), acc_phase, abort_flag, g.err);
-            ok = __shfl_sync(0xffffffffu, ok, 0);
-            if (!ok) break;
-            tc_fence_after();
-            const uint32_t tacc = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) +
-                                  static_cast<uint32_t>(acc * BN);
-            const bool valid = row < t.rows;
-            if constexpr (kSwiGLU) {
-                const int col0 = t.n * (BN / 2);
-                __nv_bfloat16 *dst =
-                    g.out + static_cast<int64_t>(t.row0 + row) * g.n_out + col0;
-#pragma unroll 1
-                for (int c = 0; c < BN / 2; c += 32) {
-                    uint32_t gv[32], uv[32];
-                    tmem_ld32(tacc + c, gv);
-                    tmem_ld32(tacc + BN / 2 + c, uv);
-                    tmem_wait_ld();
-                    tmem_reg_fence(gv);
-                    tmem_reg_fence(uv);
-                    if (valid) {
-                        uint32_t pk[16];
-#pragma unroll
-                        for (int i = 0; i < 16; ++i) {
-                            const float a0 = silu_mul(__uint_as_float(gv[2 * i]), __uint_as_float(uv[2 * i]));
-                            const float a1 = silu_mul(__uint_as_float(gv[2 * i + 1]),
-                                                      __uint_as_float(uv[2 * i + 1]));
-                            pk[i] = pack_bf16x2(a0, a1);
-                        }
-#pragma unroll
-                        for (int j = 0; j < 4; ++j) {
-                            if (col0 + c + j * 8 < g.n_out)
-                                *reinterpret_cast<uint4 *>(dst + c + j * 8) =
-                                    make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
-                        }
-                    }
+            int u = -1;
+            if (lane == 0) {
+                ok = mbar_wait(smem_addr(&sm.uq_full[q]), qphase, abort_flag, g.err);
+                if (ok) {
+                    u = unit_q[q];
+                    mbar_arrive(smem_addr(&sm.uq_empty[q]));
                 }
-            } else {
-                const int col0 = t.n * BN;
-                int slot = 0;
-                float w = 0.0f;
+            }
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            u = __shfl_sync(0xffffffffu, u, 0);
+            if (++q == UQ) { q = 0; qphase ^= 1u; }
+            if (!ok || u < 0) break;
+            const Unit t = decode_unit<MODE>(u, g);
+            const bool valid = row < t.rows;
+            int slot = 0;
+            float w = 0.0f;
+            if constexpr (MODE == kStage2) {
                 if (valid) {
                     slot = g.perm_slot[t.row0 + row];
                     w = g.topk_w[slot];
                 }
-                __nv_bfloat16 *dst = g.out + static_cast<int64_t>(slot) * g.n_out + col0;
+            }
+            if (lane == 0) ok = mbar_wait(smem_addr(&sm.acc_full), acc_phase, abort_flag, g.err);
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            if (!ok) break;
+            tc_fence_after();
+            if (t.rows > half * BM) {                   // this half was computed
+                if constexpr (MODE == kStage1) {
+                    const int col0 = t.n * (BN / 2);
+                    __nv_bfloat16 *dst = g.out + static_cast<int64_t>(t.row0 + row) * g.n_out + col0;
 #pragma unroll 1
-                for (int c = 0; c < BN; c += 32) {
-                    uint32_t v[32];
-                    tmem_ld32(tacc + c, v);
-                    tmem_wait_ld();
-                    tmem_reg_fence(v);
-                    if (valid) {
-                        uint32_t pk[16];
+                    for (int c = 0; c < BN / 2; c += 32) {
+                        uint32_t gv[32], uv[32];
+                        tmem_ld32(tacc + c, gv);
+                        tmem_ld32(tacc + BN / 2 + c, uv);
+                        tmem_wait_ld();
+                        tmem_reg_fence(gv);
+                        tmem_reg_fence(uv);
+                        if (valid) {
+                            uint32_t pk[16];
 #pragma unroll
-                        for (int i = 0; i < 16; ++i)
-                            pk[i] = pack_bf16x2(w * __uint_as_float(v[2 * i]), w * __uint_as_float(v[2 * i + 1]));
+                            for (int i = 0; i < 16; ++i) {
+                                const float a0 = silu_mul(__uint_as_float(gv[2 * i]), __uint_as_float(uv[2 * i]));
+                                const float a1 = silu_mul(__uint_as_float(gv[2 * i + 1]),
+                                                          __uint_as_float(uv[2 * i + 1]));
+                                pk[i] = pack_bf16x2(a0, a1);
+                            }
 #pragma unroll
-                        for (int j = 0; j < 4; ++j) {
-                            if (col0 + c + j * 8 < g.n_out)
-                                *reinterpret_cast<uint4 *>(dst + c + j * 8) =
-                                    make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+                            for (int j = 0; j < 4; ++j) {
+                                if (col0 + c + j * 8 < g.n_out)
+                                    *reinterpret_cast<uint4 *>(dst + c + j * 8) =
+                                        make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+                            }
+                        }
+                    }
+                } else if constexpr (MODE == kStage2) {
+                    const int col0 = t.n * BN;
+                    __nv_bfloat16 *dst = g.out + static_cast<int64_t>(slot) * g.n_out + col0;
+#pragma unroll 1
+                    for (int c = 0; c < BN; c += 32) {
+                        uint32_t v[32];
+                        tmem_ld32(tacc + c, v);
+                        tmem_wait_ld();
+                        tmem_reg_fence(v);
+                        if (valid) {
+                            uint32_t pk[16];
+#pragma unroll
+                            for (int i = 0; i < 16; ++i)
+                                pk[i] = pack_bf16x2(w * __uint_as_float(v[2 * i]), w * __uint_as_float(v[2 * i + 1]));
+#pragma unroll
+                            for (int j = 0; j < 4; ++j) {
+                                if (col0 + c + j * 8 < g.n_out)
+                                    *reinterpret_cast<uint4 *>(dst + c + j * 8) =
+                                        make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+                            }
+                        }
+                    }
+                } else {
+                    const int col0 = t.n * BN;
+                    float *dst = g.logits_part +
+                                 (static_cast<int64_t>(t.split) * g.T + t.row0 + row) * g.n_out + col0;
+                    const bool vec = (g.n_out & 3) == 0;
+#pragma unroll 1
+                    for (int c = 0; c < BN; c += 32) {
+                        uint32_t v[32];
+                        tmem_ld32(tacc + c, v);
+                        tmem_wait_ld();
+                        tmem_reg_fence(v);
+                        if (valid) {
+                            if (vec) {
+#pragma unroll
+                                for (int j = 0; j < 8; ++j) {
+                                    if (col0 + c + j * 4 < g.n_out)
+                                        *reinterpret_cast<uint4 *>(dst + c + j * 4) =
+                                            make_uint4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+                                }
+                            } else {
+#pragma unroll
+                                for (int j = 0; j < 32; ++j) {
+                                    if (col0 + c + j < g.n_out) dst[c + j] = __uint_as_float(v[j]);
+                                }
+                            }
                         }
                     }
                 }
             }
             tc_fence_before();
-            mbar_arrive(smem_addr(&sm.acc_empty[acc]));
-            if (++acc == ACC_STAGES) { acc = 0; acc_phase ^= 1u; }
+            mbar_arrive(smem_addr(&sm.acc_empty));
+            acc_phase ^= 1u;
+        }
+    } else {
+        // ------------------------------------------------ stage 1: routed x row gather
+        // The dispatch of dispatch_grouped_gemm: 128 threads copy the x rows of
+        // the unit's routed tokens straight into the 128B-swizzled A tiles with
+        // 16-byte cp.async (8 threads per 128-byte row slice, rows rg + 16i).
+        // Each thread waits for its own copies, orders them before the tensor
+        // core's async-proxy reads, then arrives on the stage's full barrier,
+        // one stage behind its issue so that two stages of copies are in flight.
+        if constexpr (MODE == kStage1) {
+            const int gt = threadIdx.x - (64 + EPI_THREADS);
+            const int chunk = gt & 7;
+            const int rg = gt >> 3;
+            int stage = 0, q = 0, pending = -1;
+            uint32_t phase = 0, qphase = 0;
+            while (true) {
+                bool ok = true;
+                int u = -1;
+                if (lane == 0) {
+                    ok = mbar_wait(smem_addr(&sm.uq_full[q]), qphase, abort_flag, g.err);
+                    if (ok) {
+                        u = unit_q[q];
+                        mbar_arrive(smem_addr(&sm.uq_empty[q]));
+                    }
+                }
+                ok = __shfl_sync(0xffffffffu, ok, 0);
+                u = __shfl_sync(0xffffffffu, u, 0);
+                if (++q == UQ) { q = 0; qphase ^= 1u; }
+                if (!ok || u < 0) break;
+                const Unit t = decode_unit<MODE>(u, g);
+                int tok[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    const int r = rg + 16 * i;
+                    tok[i] = (r < t.rows) ? g.perm_slot[t.row0 + r] / g.k : -1;
+                }
+                for (int kb = t.kb0; kb < t.kb1; ++kb) {
+                    bool e_ok = true;
+                    if (lane == 0) e_ok = mbar_wait(smem_addr(&sm.empty[stage]), phase ^ 1u, abort_flag, g.err);
+                    e_ok = __shfl_sync(0xffffffffu, e_ok, 0);
+                    if (!e_ok) { ok = false; break; }
+                    const int col = kb * BK + chunk * 8;
+                    const uint32_t nbytes = col < g.K ? 16u : 0u;   // zero-fill the K tail
+                    const uint32_t sa = smem_addr(sm.a[stage]);
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        if (tok[i] >= 0) {
+                            const int r = rg + 16 * i;
+                            const int rl = r & (BM - 1);
+                            const uint32_t dst = sa + (r >> 7) * A_HALF_BYTES + rl * (BK * 2) +
+                                                 ((chunk ^ (rl & 7)) << 4);
+                            cp_async_16(dst, g.x + static_cast<int64_t>(tok[i]) * g.K + (nbytes ? col : 0), nbytes);
+                        }
+                    }
+                    cp_async_commit();
+                    if (pending >= 0) {
+                        cp_async_wait<1>();
+                        fence_proxy_async_smem();
+                        mbar_arrive(smem_addr(&sm.full[pending]));
+                    }
+                    pending = stage;
+                    if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+                }
+                if (pending >= 0) {                       // signal the unit's last stage
+                    cp_async_wait<0>();
+                    fence_proxy_async_smem();
+                    mbar_arrive(smem_addr(&sm.full[pending]));
+                    pending = -1;
+                }
+                if (!ok) break;
+            }
+            cp_async_wait<0>();                           // no copy in flight at exit
         }
     }
 
@@ -338,6 +539,14 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_a,
     if (warp == 1) {
         tc_fence_after();
         tmem_dealloc(tmem_base, TMEM_COLS);
+    }
+    if (threadIdx.x == 0) {
+        // the last CTA to finish resets the unit counter for the next launch
+        __threadfence();
+        if (atomicAdd(&g.sched[1], 1) == static_cast<int>(gridDim.x) - 1) {
+            atomicExch(&g.sched[0], 0);
+            atomicExch(&g.sched[1], 0);
+        }
     }
 }
 
@@ -370,15 +579,18 @@ combine_kernel(const __nv_bfloat16 *__restrict__ obuf, const int32_t *__restrict
     }
 }
 
-GemmArgs make_args(const GemmLaunch &p, int n_tiles) {
-    GemmArgs g;
+GemmArgs grouped_args(const GemmLaunch &p, int n_tiles) {
+    GemmArgs g{};
     g.counts = p.counts;
     g.offsets = p.offsets;
     g.mt_prefix = p.mt_prefix;
     g.perm_slot = p.perm_slot;
+    g.x = p.x;
     g.err = p.err;
+    g.sched = p.sched;
     g.topk_w = p.topk_w;
     g.out = p.out;
+    g.logits_part = nullptr;
     g.E = p.E;
     g.k = p.k;
     g.K = p.K;
@@ -386,31 +598,57 @@ GemmArgs make_args(const GemmLaunch &p, int n_tiles) {
     g.n_tiles = n_tiles;
     g.b_rows = p.b_rows;
     g.half = p.half;
+    g.total_units = -1;
     return g;
 }
 
 }  // namespace
 
 cudaError_t setup_gemm_kernels() {
-    cudaError_t e = cudaFuncSetAttribute(grouped_gemm_kernel<true>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaError_t e = cudaFuncSetAttribute(tc_gemm_kernel<kStage1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(SMEM_BYTES));
     if (e != cudaSuccess) return e;
-    return cudaFuncSetAttribute(grouped_gemm_kernel<false>,
-                                cudaFuncAttributeMaxDynamicSharedMemorySize,
+    e = cudaFuncSetAttribute(tc_gemm_kernel<kStage2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(SMEM_BYTES));
+    if (e != cudaSuccess) return e;
+    return cudaFuncSetAttribute(tc_gemm_kernel<kRouter>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 static_cast<int>(SMEM_BYTES));
 }
 
 cudaError_t launch_gemm1_swiglu(const GemmLaunch &p, cudaStream_t st) {
-    const GemmArgs g = make_args(p, (p.n_out + BN / 2 - 1) / (BN / 2));
-    grouped_gemm_kernel<true><<<p.num_sms, NUM_THREADS, SMEM_BYTES, st>>>(*p.tm_a, *p.tm_b, g);
+    const GemmArgs g = grouped_args(p, (p.n_out + BN / 2 - 1) / (BN / 2));
+    tc_gemm_kernel<kStage1><<<p.num_sms, kNumThreads<kStage1>, SMEM_BYTES, st>>>(*p.tm_a, *p.tm_b, g);
     note_launches(1);
     return cudaGetLastError();
 }
 
 cudaError_t launch_gemm2_scatter(const GemmLaunch &p, cudaStream_t st) {
-    const GemmArgs g = make_args(p, (p.n_out + BN - 1) / BN);
-    grouped_gemm_kernel<false><<<p.num_sms, NUM_THREADS, SMEM_BYTES, st>>>(*p.tm_a, *p.tm_b, g);
+    const GemmArgs g = grouped_args(p, (p.n_out + BN - 1) / BN);
+    tc_gemm_kernel<kStage2><<<p.num_sms, kNumThreads<kStage2>, SMEM_BYTES, st>>>(*p.tm_a, *p.tm_b, g);
+    note_launches(1);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_router_gemm(const RouterGemmLaunch &p, cudaStream_t st) {
+    GemmArgs g{};
+    g.err = p.err;
+    g.sched = p.sched;
+    g.logits_part = p.logits_part;
+    g.E = p.E;
+    g.K = p.H;
+    g.n_out = p.E;
+    g.n_tiles = (p.E + BN - 1) / BN;
+    g.T = p.T;
+    g.kb_h = (p.H + BK - 1) / BK;
+    g.kb_total = 3 * g.kb_h;
+    g.splits = p.splits;
+    g.kb_per_split = (g.kb_total + p.splits - 1) / p.splits;
+    g.total_units = ((p.T + UM - 1) / UM) * g.n_tiles * p.splits;
+    // every split must own at least one k-block: an empty split would leave its
+    // accumulator unwritten
+    if (p.splits < 1 || (p.splits - 1) * g.kb_per_split >= g.kb_total) return cudaErrorInvalidValue;
+    const int grid = g.total_units < p.num_sms ? g.total_units : p.num_sms;
+    tc_gemm_kernel<kRouter><<<grid, kNumThreads<kRouter>, SMEM_BYTES, st>>>(*p.tm_x, *p.tm_w3, g);
     note_launches(1);
     return cudaGetLastError();
 }

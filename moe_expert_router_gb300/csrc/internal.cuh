@@ -10,19 +10,77 @@
 
 namespace moe {
 
-// Rows (routed tokens) per GEMM tile; the routing metadata counts row tiles in
-// these units, so every grouped GEMM uses the same value.
+// Rows per MMA (one TMEM accumulator holds 128 rows). A GEMM work unit spans
+// kUnitM = 2 * kBM rows that share every weight tile; the routing metadata
+// counts row tiles in units of kUnitM, so every grouped GEMM uses that value.
 constexpr int kBM = 128;
+constexpr int kUnitM = 256;
+constexpr int kBK = 64;     // reduction depth of one pipeline stage
+constexpr int kBN = 256;    // accumulator columns of one tile
 
-// Workspace header: int32 error word at byte 0, int32 router ticket at byte 4.
+// Workspace header (zeroed by moe_workspace_init):
+//   byte 0  int32 device error word
+//   byte 4  int32 router top-k block ticket
+//   byte 8  int32[2] stage-1 unit scheduler (next unit, finished CTAs)
+//   byte 16 int32[2] stage-2 unit scheduler
+//   byte 24 int32[2] router-GEMM unit scheduler
 constexpr size_t kWsHeaderBytes = 256;
 
+inline size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+// Split-K factor of the router GEMM (logits = x . w_r^T as three bf16 GEMMs):
+// enough units to cover two waves of 152 SMs, at most 32 splits and at least
+// one 64-deep k-block per split. Depends on the shape only.
+inline int router_splits(int64_t T, int64_t H, int64_t E) {
+    const int64_t mt = (T + kUnitM - 1) / kUnitM;
+    const int64_t nt = (E + kBN - 1) / kBN;
+    const int64_t kb_total = 3 * ((H + kBK - 1) / kBK);
+    int64_t s = (304 + mt * nt - 1) / (mt * nt);
+    if (s > 32) s = 32;
+    if (s > kb_total) s = kb_total;
+    if (s < 1) s = 1;
+    // no empty split: recompute from the per-split depth
+    const int64_t per = (kb_total + s - 1) / s;
+    return static_cast<int>((kb_total + per - 1) / per);
+}
+
+// Bytes of router scratch for a shape and split factor.
+inline size_t router_scratch_bytes(int64_t T, int64_t H, int64_t E, int splits) {
+    return align256(4 * static_cast<size_t>(splits) * T * E) +   // partial logits
+           align256(2 * 3 * static_cast<size_t>(E) * H) +         // bf16 x3 split of w_r
+           align256(4 * static_cast<size_t>(E)) +                 // score sums
+           align256(4 * static_cast<size_t>(E)) +                 // counts
+           256;                                                   // ticket + scheduler
+}
+
 struct RouterScratch {
-    float *logits;      // [T, E]
-    float *score_sum;   // [E]  sum over tokens of the full score vector
-    int32_t *counts;    // [E]  rows the router sent to each expert
-    int32_t *ticket;    // blocks of the top-k kernel that have finished
+    float *logits_part;       // [splits, T, E] partial fp32 logits
+    __nv_bfloat16 *w3;        // [3, E, H]: hi, mid, lo parts of w_r
+    float *score_sum;         // [E]  sum over tokens of the full score vector
+    int32_t *counts;          // [E]  rows the router sent to each expert
+    int32_t *ticket;          // top-k blocks that have finished
+    int32_t *sched;           // [2] router-GEMM unit scheduler
+    int splits;
 };
+
+// Carve router scratch out of `base` (256-byte aligned).
+inline RouterScratch carve_router_scratch(unsigned char *base, int64_t T, int64_t H, int64_t E,
+                                          int splits, int32_t *ticket, int32_t *sched) {
+    RouterScratch r;
+    size_t off = 0;
+    r.logits_part = reinterpret_cast<float *>(base + off);
+    off += align256(4 * static_cast<size_t>(splits) * T * E);
+    r.w3 = reinterpret_cast<__nv_bfloat16 *>(base + off);
+    off += align256(2 * 3 * static_cast<size_t>(E) * H);
+    r.score_sum = reinterpret_cast<float *>(base + off);
+    off += align256(4 * static_cast<size_t>(E));
+    r.counts = reinterpret_cast<int32_t *>(base + off);
+    off += align256(4 * static_cast<size_t>(E));
+    r.ticket = ticket ? ticket : reinterpret_cast<int32_t *>(base + off);
+    r.sched = sched ? sched : reinterpret_cast<int32_t *>(base + off + 64);
+    r.splits = splits;
+    return r;
+}
 
 struct RouterLaunch {
     const __nv_bfloat16 *x;
@@ -36,6 +94,8 @@ struct RouterLaunch {
     int32_t *topk_idx;
     float *topk_w;
     float *aux;                 // may be null
+    int32_t *err;
+    int num_sms;
     RouterScratch scratch;
 };
 
@@ -45,15 +105,29 @@ struct MetadataLaunch {
     int32_t *counts, *offsets, *mt_prefix, *perm_slot, *row_of, *err;
 };
 
-// One grouped GEMM launch: stage 1 (SwiGLU epilogue) or stage 2 (weighted scatter).
+// One grouped GEMM launch: stage 1 (fused x row gather + SwiGLU epilogue) or stage 2
+// (weighted scatter epilogue).
 struct GemmLaunch {
     const CUtensorMap *tm_a;    // host-encoded tensor maps (copied into the launch)
     const CUtensorMap *tm_b;
     const int32_t *counts, *offsets, *mt_prefix, *perm_slot;
+    const __nv_bfloat16 *x;     // stage 1: token rows gathered into the A tiles
     int32_t *err;
+    int32_t *sched;             // [2] unit scheduler of this stage
     const float *topk_w;        // stage 2 only
     __nv_bfloat16 *out;         // a [R, I] (stage 1) or obuf [R, H] (stage 2)
     int E, k, K, n_out, b_rows, half;
+    int num_sms;
+};
+
+// The router GEMM: partial logits [splits, T, E] of x . w3^T.
+struct RouterGemmLaunch {
+    const CUtensorMap *tm_x;    // x [T, H], box 64 x 128
+    const CUtensorMap *tm_w3;   // w3 [3E, H], box 64 x 256
+    float *logits_part;
+    int32_t *err;
+    int32_t *sched;
+    int T, H, E, splits;
     int num_sms;
 };
 
@@ -68,12 +142,18 @@ cudaError_t launch_router(const RouterLaunch &p, cudaStream_t st);
 cudaError_t launch_routing_metadata(const MetadataLaunch &p, cudaStream_t st);
 cudaError_t launch_gemm1_swiglu(const GemmLaunch &p, cudaStream_t st);
 cudaError_t launch_gemm2_scatter(const GemmLaunch &p, cudaStream_t st);
+cudaError_t launch_router_gemm(const RouterGemmLaunch &p, cudaStream_t st);
 cudaError_t launch_combine(const CombineLaunch &p, cudaStream_t st);
 
 // Per-device one-time kernel attribute set-up (dynamic shared memory limits).
-cudaError_t setup_router_kernels();
 cudaError_t setup_metadata_kernels();
 cudaError_t setup_gemm_kernels();
+
+// bf16 tensor [rows, inner] (inner contiguous) with a box_inner x box_rows box,
+// 128-byte swizzle, zero fill out of bounds. False if the encoder is missing
+// or rejects the arguments.
+bool encode_bf16_2d(CUtensorMap *map, const void *base, uint64_t inner, uint64_t rows,
+                    uint32_t box_inner, uint32_t box_rows);
 
 // Statistics: kernels launched by this library.
 void note_launches(int n);

@@ -22,14 +22,8 @@ struct DeviceState {
 std::mutex g_mu;
 DeviceState g_dev[kMaxDevices];
 
-typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
-                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
-                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
-                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-EncodeTiledFn g_encode = nullptr;
-
 // Per-device set-up: check for an sm_103 GPU, cache the SM count, raise the
-// dynamic shared memory limits and look up the tensor-map encoder.
+// dynamic shared memory limits.
 moe_status_t device_state(DeviceState **out) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
@@ -47,20 +41,8 @@ moe_status_t device_state(DeviceState **out) {
             d.status = MOE_ERR_UNSUPPORTED;
         } else {
             d.num_sms = sms;
-            if (setup_router_kernels() != cudaSuccess || setup_metadata_kernels() != cudaSuccess ||
-                setup_gemm_kernels() != cudaSuccess) {
+            if (setup_metadata_kernels() != cudaSuccess || setup_gemm_kernels() != cudaSuccess) {
                 d.status = MOE_ERR_CUDA;
-            }
-            if (g_encode == nullptr) {
-                void *fn = nullptr;
-                cudaDriverEntryPointQueryResult q;
-                if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
-                                                     cudaEnableDefault, &q) != cudaSuccess ||
-                    q != cudaDriverEntryPointSuccess || fn == nullptr) {
-                    d.status = MOE_ERR_CUDA;
-                } else {
-                    g_encode = reinterpret_cast<EncodeTiledFn>(fn);
-                }
             }
         }
         cudaGetLastError();  // do not leak a set-up error into the caller's error state
@@ -68,21 +50,6 @@ moe_status_t device_state(DeviceState **out) {
     *out = &d;
     return d.status;
 }
-
-// 2-D bf16 tensor [rows, inner] (inner contiguous) with a box of
-// box_inner x box_rows elements, 128-byte swizzle, zero fill out of bounds.
-bool encode_bf16_2d(CUtensorMap *map, const void *base, uint64_t inner, uint64_t rows,
-                    uint32_t box_inner, uint32_t box_rows) {
-    cuuint64_t dims[2] = {inner, rows};
-    cuuint64_t strides[1] = {inner * 2};
-    cuuint32_t box[2] = {box_inner, box_rows};
-    cuuint32_t estr[2] = {1, 1};
-    return g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides,
-                    box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
-size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -109,7 +76,7 @@ moe_ws_layout_t make_layout(const moe_shape_t &s) {
     L.mt_prefix = off; off = align256(off + 4 * (E + 1));
     L.perm_slot = off; off = align256(off + 4 * R);
     L.row_of = off;    off = align256(off + 4 * R);
-    L.router = off;    off = align256(off + align256(4 * T * E) + align256(4 * E) + 4 * E);
+    L.router = off;    off = align256(off + router_scratch_bytes(T, H, E, router_splits(T, H, E)));
     L.a = off;         off = align256(off + 2 * R * I);
     L.obuf = off;      off = align256(off + 2 * R * H);
     L.total = off;
@@ -117,7 +84,7 @@ moe_ws_layout_t make_layout(const moe_shape_t &s) {
 }
 
 struct Ws {
-    int32_t *err, *ticket, *counts, *offsets, *mt_prefix, *perm_slot, *row_of;
+    int32_t *err, *ticket, *counts, *offsets, *mt_prefix, *perm_slot, *row_of, *sched1, *sched2;
     RouterScratch router;
     __nv_bfloat16 *a, *obuf;
 };
@@ -133,11 +100,10 @@ Ws carve(void *ws, const moe_shape_t &s) {
     w.mt_prefix = reinterpret_cast<int32_t *>(b + L.mt_prefix);
     w.perm_slot = reinterpret_cast<int32_t *>(b + L.perm_slot);
     w.row_of = reinterpret_cast<int32_t *>(b + L.row_of);
-    const size_t logits_bytes = align256(4 * static_cast<size_t>(s.T) * s.E);
-    w.router.logits = reinterpret_cast<float *>(b + L.router);
-    w.router.score_sum = reinterpret_cast<float *>(b + L.router + logits_bytes);
-    w.router.counts = reinterpret_cast<int32_t *>(b + L.router + logits_bytes + align256(4 * s.E));
-    w.router.ticket = w.ticket;
+    w.sched1 = reinterpret_cast<int32_t *>(b + 8);
+    w.sched2 = reinterpret_cast<int32_t *>(b + 16);
+    w.router = carve_router_scratch(b + L.router, s.T, s.H, s.E, router_splits(s.T, s.H, s.E),
+                                    w.ticket, reinterpret_cast<int32_t *>(b + 24));
     w.a = reinterpret_cast<__nv_bfloat16 *>(b + L.a);
     w.obuf = reinterpret_cast<__nv_bfloat16 *>(b + L.obuf);
     return w;
@@ -154,18 +120,20 @@ moe_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE
 // Stage 1: tensor maps + launch (metadata must already be in ws).
 moe_status_t run_gemm1(const moe_shape_t &s, const void *x, const void *w1, void *a, const Ws &w,
                        const DeviceState &d, cudaStream_t st) {
-    CUtensorMap tm_x, tm_w1;
-    if (!encode_bf16_2d(&tm_x, x, s.H, s.T, 64, 1)) return MOE_ERR_CUDA;
+    // the x rows are gathered by the kernel's own warps; only w1 goes through TMA
+    CUtensorMap tm_w1;
     if (!encode_bf16_2d(&tm_w1, w1, s.H, static_cast<uint64_t>(s.E) * 2 * s.I, 64, 128))
         return MOE_ERR_CUDA;
     GemmLaunch p;
-    p.tm_a = &tm_x;
+    p.tm_a = &tm_w1;
     p.tm_b = &tm_w1;
+    p.x = static_cast<const __nv_bfloat16 *>(x);
     p.counts = w.counts;
     p.offsets = w.offsets;
     p.mt_prefix = w.mt_prefix;
     p.perm_slot = w.perm_slot;
     p.err = w.err;
+    p.sched = w.sched1;
     p.topk_w = nullptr;
     p.out = static_cast<__nv_bfloat16 *>(a);
     p.E = static_cast<int>(s.E);
@@ -189,11 +157,13 @@ moe_status_t run_gemm2(const moe_shape_t &s, const void *a, const float *topk_w,
     GemmLaunch p;
     p.tm_a = &tm_a;
     p.tm_b = &tm_w2;
+    p.x = nullptr;
     p.counts = w.counts;
     p.offsets = w.offsets;
     p.mt_prefix = w.mt_prefix;
     p.perm_slot = w.perm_slot;
     p.err = w.err;
+    p.sched = w.sched2;
     p.topk_w = topk_w;
     p.out = w.obuf;
     p.E = static_cast<int>(s.E);
@@ -230,6 +200,36 @@ moe_status_t run_metadata(const moe_shape_t &s, const int32_t *topk_idx, const W
 }
 
 }  // namespace
+
+namespace {
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+std::once_flag g_encode_once;
+EncodeTiledFn g_encode = nullptr;
+}  // namespace
+
+bool encode_bf16_2d(CUtensorMap *map, const void *base, uint64_t inner, uint64_t rows,
+                    uint32_t box_inner, uint32_t box_rows) {
+    std::call_once(g_encode_once, [] {
+        void *fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+        cudaGetLastError();
+    });
+    if (g_encode == nullptr) return false;
+    cuuint64_t dims[2] = {inner, rows};
+    cuuint64_t strides[1] = {inner * 2};
+    cuuint32_t box[2] = {box_inner, box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    return g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides,
+                    box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
 
 void note_launches(int n) { g_launches.fetch_add(static_cast<uint64_t>(n), std::memory_order_relaxed); }
 
@@ -307,6 +307,8 @@ moe_status_t moe_router(const void *x, const float *w_r, const float *logit_offs
     p.topk_idx = topk_idx;
     p.topk_w = topk_w;
     p.aux = aux;
+    p.err = w.err;
+    p.num_sms = d->num_sms;
     p.scratch = w.router;
     return cuda_status(launch_router(p, static_cast<cudaStream_t>(stream)));
 }

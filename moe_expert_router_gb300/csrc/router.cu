@@ -2,10 +2,15 @@
 // section: score function + group-limited top-k + aux score; the aux
 // load-balance value is computed on the device and returned).
 //
-//   logits kernel : l[t, e] = sum_h x[t, h] * w_r[e, h] (+ logit_offset[e]) in
-//                   fp32, 64x64 output tiles, 4x4 per thread. Block (0, 0)
-//                   also clears the aux accumulators of this call.
-//   top-k kernel  : one warp per token. Scores (softmax over the row, or
+//   split kernel  : w_r (fp32) -> w3 = [hi; mid; lo] (bf16) with
+//                   w_r = hi + mid + lo exactly; block 0 also clears the aux
+//                   accumulators of this call.
+//   router GEMM   : partial logits [splits, T, E] = x . w3^T on the tensor
+//                   cores (grouped_gemm.cu, router mode). x is bf16, so each
+//                   product is exact and the fp32 accumulation matches an
+//                   fp32 dot product of x with w_r.
+//   top-k kernel  : one warp per token. Logits = fixed-order sum of the split
+//                   partials (+ logit_offset). Scores (softmax over the row, or
 //                   elementwise sigmoid), selection scores sel = s + sel_bias,
 //                   optional group limit (group score = sum of the group_topn
 //                   best sel; keep topk_group groups), k rounds of a warp
@@ -22,69 +27,30 @@ namespace moe {
 
 namespace {
 
-constexpr int LT = 64;        // logits tile: tokens
-constexpr int LE = 64;        // logits tile: experts
-constexpr int LK = 32;        // logits tile: reduction slice
 constexpr int kTopkWarps = 8;
 constexpr int kMaxE = 1024;
 
 __global__ void __launch_bounds__(256)
-router_logits_kernel(const __nv_bfloat16 *__restrict__ x, const float *__restrict__ w_r,
-                     const float *__restrict__ logit_offset, float *__restrict__ logits, int T,
-                     int H, int E, float *__restrict__ score_sum, int32_t *__restrict__ counts,
-                     int32_t *__restrict__ ticket) {
-    __shared__ float xs[LK][LT + 1];
-    __shared__ float wsm[LK][LE + 1];
-    if (blockIdx.x == 0 && blockIdx.y == 0) {
+router_split_kernel(const float *__restrict__ w_r, __nv_bfloat16 *__restrict__ w3, int64_t n,
+                    int E, float *__restrict__ score_sum, int32_t *__restrict__ counts,
+                    int32_t *__restrict__ ticket) {
+    if (blockIdx.x == 0) {
         for (int e = threadIdx.x; e < E; e += blockDim.x) {
             score_sum[e] = 0.0f;
             counts[e] = 0;
         }
         if (threadIdx.x == 0) *ticket = 0;
     }
-    const int t0 = blockIdx.y * LT;
-    const int e0 = blockIdx.x * LE;
-    const int tx = threadIdx.x & 15;   // expert quad
-    const int ty = threadIdx.x >> 4;   // token quad
-    float acc[4][4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i)
-#pragma unroll
-        for (int j = 0; j < 4; ++j) acc[i][j] = 0.0f;
-
-    for (int h0 = 0; h0 < H; h0 += LK) {
-        for (int i = threadIdx.x; i < LT * LK; i += blockDim.x) {
-            const int r = i / LK, c = i % LK;
-            const int t = t0 + r, h = h0 + c;
-            xs[c][r] = (t < T && h < H) ? __bfloat162float(x[static_cast<int64_t>(t) * H + h]) : 0.0f;
-            const int e = e0 + r;
-            wsm[c][r] = (e < E && h < H) ? w_r[static_cast<int64_t>(e) * H + h] : 0.0f;
-        }
-        __syncthreads();
-#pragma unroll 8
-        for (int c = 0; c < LK; ++c) {
-            float a[4], b[4];
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                a[i] = xs[c][ty * 4 + i];
-                b[i] = wsm[c][tx * 4 + i];
-            }
-#pragma unroll
-            for (int i = 0; i < 4; ++i)
-#pragma unroll
-                for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
-        }
-        __syncthreads();
-    }
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const int t = t0 + ty * 4 + i;
-        if (t >= T) continue;
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const int e = e0 + tx * 4 + j;
-            if (e < E) logits[static_cast<int64_t>(t) * E + e] = acc[i][j] + (logit_offset ? logit_offset[e] : 0.0f);
-        }
+    for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n;
+         i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const float w = w_r[i];
+        const __nv_bfloat16 hi = __float2bfloat16_rn(w);
+        const float r1 = w - __bfloat162float(hi);          // exact
+        const __nv_bfloat16 mid = __float2bfloat16_rn(r1);
+        const float r2 = r1 - __bfloat162float(mid);        // exact, <= 8 significant bits
+        w3[i] = hi;
+        w3[n + i] = mid;
+        w3[2 * n + i] = __float2bfloat16_rn(r2);
     }
 }
 
@@ -114,7 +80,9 @@ __device__ __forceinline__ float warp_max(float v) {
 }
 
 struct TopkArgs {
-    const float *logits;
+    const float *logits_part;   // [splits, T, E]
+    int splits;
+    const float *logit_offset;
     const float *sel_bias;
     int T, E, k, score_fn, normalize;
     float scale;
@@ -146,11 +114,19 @@ router_topk_kernel(const TopkArgs p) {
     if (t < p.T) {
         float s[V], sel[V];
         bool elig[V];
-        const float *lrow = p.logits + static_cast<int64_t>(t) * p.E;
+        const int64_t split_stride = static_cast<int64_t>(p.T) * p.E;
+        const float *lrow = p.logits_part + static_cast<int64_t>(t) * p.E;
 #pragma unroll
         for (int i = 0; i < V; ++i) {
             const int e = lane + 32 * i;
-            s[i] = (e < p.E) ? lrow[e] : -INFINITY;
+            if (e < p.E) {
+                float l = 0.0f;
+                for (int sp = 0; sp < p.splits; ++sp) l += lrow[sp * split_stride + e];
+                if (p.logit_offset) l += p.logit_offset[e];
+                s[i] = l;
+            } else {
+                s[i] = -INFINITY;
+            }
         }
         if (p.score_fn == MOE_SCORE_SOFTMAX) {
             float m = -INFINITY;
@@ -305,15 +281,38 @@ void launch_topk(const TopkArgs &a, int blocks, cudaStream_t st) {
 
 }  // namespace
 
-cudaError_t setup_router_kernels() { return cudaSuccess; }
-
 cudaError_t launch_router(const RouterLaunch &p, cudaStream_t st) {
-    dim3 lgrid((p.E + LE - 1) / LE, (p.T + LT - 1) / LT);
-    router_logits_kernel<<<lgrid, 256, 0, st>>>(p.x, p.w_r, p.logit_offset, p.scratch.logits, p.T, p.H,
-                                                 p.E, p.scratch.score_sum, p.scratch.counts,
-                                                 p.scratch.ticket);
+    const RouterScratch &sc = p.scratch;
+    const int64_t n = static_cast<int64_t>(p.E) * p.H;
+    int64_t sblocks = (n + 255) / 256;
+    if (sblocks > 152 * 8) sblocks = 152 * 8;
+    router_split_kernel<<<static_cast<int>(sblocks), 256, 0, st>>>(p.w_r, sc.w3, n, p.E, sc.score_sum,
+                                                                   sc.counts, sc.ticket);
+    note_launches(1);
+    cudaError_t err = cudaGetLastError();
+    if (err != cudaSuccess) return err;
+
+    CUtensorMap tm_x, tm_w3;
+    if (!encode_bf16_2d(&tm_x, p.x, p.H, p.T, kBK, kBM) ||
+        !encode_bf16_2d(&tm_w3, sc.w3, p.H, 3 * static_cast<uint64_t>(p.E), kBK, kBN))
+        return cudaErrorInvalidValue;
+    RouterGemmLaunch g;
+    g.tm_x = &tm_x;
+    g.tm_w3 = &tm_w3;
+    g.logits_part = sc.logits_part;
+    g.err = p.err;
+    g.sched = sc.sched;
+    g.T = p.T;
+    g.H = p.H;
+    g.E = p.E;
+    g.splits = sc.splits;
+    g.num_sms = p.num_sms;
+    if ((err = launch_router_gemm(g, st)) != cudaSuccess) return err;
+
     TopkArgs a;
-    a.logits = p.scratch.logits;
+    a.logits_part = sc.logits_part;
+    a.splits = sc.splits;
+    a.logit_offset = p.logit_offset;
     a.sel_bias = p.sel_bias;
     a.T = p.T;
     a.E = p.E;
@@ -326,9 +325,9 @@ cudaError_t launch_router(const RouterLaunch &p, cudaStream_t st) {
     a.group_topn = p.group_topn;
     a.topk_idx = p.topk_idx;
     a.topk_w = p.topk_w;
-    a.score_sum = p.scratch.score_sum;
-    a.counts = p.scratch.counts;
-    a.ticket = p.scratch.ticket;
+    a.score_sum = sc.score_sum;
+    a.counts = sc.counts;
+    a.ticket = sc.ticket;
     a.aux = p.aux;
     const int blocks = (p.T + kTopkWarps - 1) / kTopkWarps;
     const int v = (p.E + 31) / 32;
@@ -337,7 +336,7 @@ cudaError_t launch_router(const RouterLaunch &p, cudaStream_t st) {
     else if (v <= 8) launch_topk<8>(a, blocks, st);
     else if (v <= 16) launch_topk<16>(a, blocks, st);
     else launch_topk<32>(a, blocks, st);
-    note_launches(2);
+    note_launches(1);
     return cudaGetLastError();
 }
 

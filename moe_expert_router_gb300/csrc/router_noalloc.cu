@@ -18,15 +18,13 @@ namespace moe {
 
 namespace {
 
-// Capacity of the static scratch: logits for at most kMaxLogits = T * E
-// values, plus per-expert score sums and counts for up to 1024 experts, plus
-// the block ticket of the top-k kernel.
-constexpr size_t kMaxLogits = size_t(1) << 20;                 // 4 MiB of fp32 logits
-constexpr size_t kLogitsBytes = kMaxLogits * sizeof(float);
-constexpr size_t kSumsOffset = kLogitsBytes;
-constexpr size_t kCountsOffset = kSumsOffset + 1024 * sizeof(float);
-constexpr size_t kTicketOffset = kCountsOffset + 1024 * sizeof(int32_t);
-constexpr size_t kScratchBytes = kTicketOffset + 256;
+// Capacity of the static scratch: split-K partial logits for at most
+// kMaxPartials = splits * T * E values (4 MiB), the bf16 x3 split of w_r for at
+// most E * H = kMaxEH weights (6 MiB), per-expert sums and counts for up to
+// 1024 experts, the block ticket, the GEMM unit scheduler and an error word.
+constexpr int64_t kMaxPartials = int64_t(1) << 20;
+constexpr int64_t kMaxEH = int64_t(1) << 20;
+constexpr size_t kScratchBytes = (size_t(4) << 20) + (size_t(6) << 20) + 4096 + 4096 + 1024;
 
 // Every GPU that loads this library holds this array until the process exits.
 // All calls on a device share it, so calls whose kernels overlap on the GPU
@@ -38,33 +36,38 @@ std::mutex g_mu;
 bool g_ready[kMaxDevices];
 moe_status_t g_status[kMaxDevices];
 unsigned char *g_scratch_ptr[kMaxDevices];
+int g_num_sms[kMaxDevices];
 
 // Once per device, with that device current: check the architecture and look
 // up the device address of the static array (a host-side use of its name is
 // only a stand-in, not a device pointer).
-moe_status_t scratch_for_current_device(unsigned char **out) {
+moe_status_t scratch_for_current_device(unsigned char **out, int *num_sms) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
     if (dev < 0 || dev >= kMaxDevices) return MOE_ERR_UNSUPPORTED;
     std::lock_guard<std::mutex> lock(g_mu);
     if (!g_ready[dev]) {
         g_ready[dev] = true;
-        int major = 0, minor = 0;
+        int major = 0, minor = 0, sms = 0;
         void *p = nullptr;
         if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
-            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess) {
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
             g_status[dev] = MOE_ERR_CUDA;
         } else if (major != 10 || minor != 3) {
             g_status[dev] = MOE_ERR_UNSUPPORTED;
-        } else if (cudaGetSymbolAddress(&p, g_router_scratch) != cudaSuccess || p == nullptr) {
+        } else if (cudaGetSymbolAddress(&p, g_router_scratch) != cudaSuccess || p == nullptr ||
+                   setup_gemm_kernels() != cudaSuccess) {
             g_status[dev] = MOE_ERR_CUDA;
         } else {
             g_status[dev] = MOE_OK;
             g_scratch_ptr[dev] = static_cast<unsigned char *>(p);
+            g_num_sms[dev] = sms;
         }
         cudaGetLastError();
     }
     *out = g_scratch_ptr[dev];
+    *num_sms = g_num_sms[dev];
     return g_status[dev];
 }
 
@@ -88,8 +91,8 @@ extern "C" moe_status_t moe_router_noalloc(const void *x, const float *w_r,
     if (s.k > 32 || s.k > s.E || s.E > 1024 || s.H % 8 != 0 || s.I % 8 != 0 ||
         s.H >= (int64_t(1) << 31) || s.T * s.k >= (int64_t(1) << 31))
         return MOE_ERR_UNSUPPORTED;
-    // the static scratch holds at most kMaxLogits router logits
-    if (s.T * s.E > static_cast<int64_t>(kMaxLogits)) return MOE_ERR_UNSUPPORTED;
+    // the static scratch must hold the split weights and one partial per split
+    if (s.T * s.E > kMaxPartials || s.E * s.H > kMaxEH) return MOE_ERR_UNSUPPORTED;
     if (s.T == 0) return MOE_OK;
     if (x == nullptr || w_r == nullptr || topk_idx == nullptr || topk_w == nullptr)
         return MOE_ERR_INVALID_ARG;
@@ -105,8 +108,18 @@ extern "C" moe_status_t moe_router_noalloc(const void *x, const float *w_r,
             return MOE_ERR_INVALID_ARG;
     }
     unsigned char *scratch = nullptr;
-    moe_status_t r = scratch_for_current_device(&scratch);
+    int num_sms = 0;
+    moe_status_t r = scratch_for_current_device(&scratch, &num_sms);
     if (r != MOE_OK) return r;
+
+    // the workspace router's split factor, lowered until the partials fit
+    int splits = router_splits(s.T, s.H, s.E);
+    const int64_t cap = kMaxPartials / (s.T * s.E);
+    if (splits > cap) {
+        const int64_t kb_total = 3 * ((s.H + kBK - 1) / kBK);
+        const int64_t per = (kb_total + cap - 1) / cap;
+        splits = static_cast<int>((kb_total + per - 1) / per);
+    }
 
     RouterLaunch p;
     p.x = static_cast<const __nv_bfloat16 *>(x);
@@ -126,11 +139,19 @@ extern "C" moe_status_t moe_router_noalloc(const void *x, const float *w_r,
     p.topk_idx = topk_idx;
     p.topk_w = topk_w;
     p.aux = aux;
-    // the router's logits kernel clears the sums, counts and ticket at the start
-    // of every call, so nothing left in the array by an earlier call is read
-    p.scratch.logits = reinterpret_cast<float *>(scratch);
-    p.scratch.score_sum = reinterpret_cast<float *>(scratch + kSumsOffset);
-    p.scratch.counts = reinterpret_cast<int32_t *>(scratch + kCountsOffset);
-    p.scratch.ticket = reinterpret_cast<int32_t *>(scratch + kTicketOffset);
+    // the split kernel clears the sums, counts and ticket at the start of every
+    // call, and the GEMM's unit counter (zero when the library is loaded)
+    // returns to zero at the end of every launch, so nothing an earlier call
+    // left in the array is read
+    // The error word, the top-k ticket and the GEMM unit counter sit at fixed
+    // places in the last 256 bytes, never inside a region whose position
+    // depends on the shape: the counter must read zero at the start of every
+    // launch, and a shape-dependent place could hold another call's logits.
+    unsigned char *tail = scratch + kScratchBytes - 256;
+    p.err = reinterpret_cast<int32_t *>(tail);
+    p.num_sms = num_sms;
+    p.scratch = carve_router_scratch(scratch, s.T, s.H, s.E, splits,
+                                     reinterpret_cast<int32_t *>(tail + 64),
+                                     reinterpret_cast<int32_t *>(tail + 128));
     return launch_router(p, static_cast<cudaStream_t>(stream)) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }

@@ -5,7 +5,7 @@
 // ragged, step-varying counts the guide's "Router force load balancing"
 // section talks about never reach the host):
 //   counts[e], offsets[e] (exclusive prefix), mt_prefix[e] (prefix of row
-//   tiles ceil(counts/128)), perm_slot[r] (flat slot of routed row r, stable:
+//   tiles ceil(counts/256)), perm_slot[r] (flat slot of routed row r, stable:
 //   increasing slot order inside each expert) and row_of[s] (inverse, -1 for a
 //   dropped slot).
 //
@@ -69,7 +69,7 @@ routing_metadata_kernel(const int32_t *__restrict__ topk_idx, int R, int E,
     // pass 2b: exclusive scans over experts of counts and of row tiles (E <= 1024)
     const int e = threadIdx.x;
     const int c = (e < E) ? base[e] : 0;
-    const int m = (c + kBM - 1) / kBM;
+    const int m = (c + kUnitM - 1) / kUnitM;
     int ic = c, im = m;
 #pragma unroll
     for (int off = 1; off < 32; off <<= 1) {

@@ -39,7 +39,7 @@ def _check_metadata(ws, shp, idx):
     np.testing.assert_array_equal(offsets, ref.offsets)
     np.testing.assert_array_equal(perm, ref.perm_slot)
     np.testing.assert_array_equal(row_of, ref.row_of)
-    want_mt = np.concatenate([[0], np.cumsum((ref.counts + 127) // 128)])
+    want_mt = np.concatenate([[0], np.cumsum((ref.counts + 255) // 256)])
     np.testing.assert_array_equal(mt, want_mt)
     return ref
 

@@ -6,7 +6,11 @@ it no workspace. It keeps the router's scratch in a static array inside the
 library instead of a caller-supplied workspace. This test checks that it gives
 the same routing as the workspace-based entry point on two calls in a row (the
 second call must not be disturbed by what the first left in the shared array),
-and that it refuses shapes whose logits do not fit that array.
+and that it refuses shapes whose scratch does not fit that array. Its split-K
+factor can be lower than the workspace router's (the array is smaller), which
+changes the fp32 summation order of the logits, so tokens whose top-k choice
+is a near-tie (oracle selection gap below 1e-6) are left out of the exact
+routing comparison, as in the other router tests.
 
 This file is named to be collected last.
 """
@@ -14,6 +18,7 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
 from moe_expert_router_gb300 import binding as B
 from moe_expert_router_gb300.workloads import MoEConfig, generate
 
@@ -58,10 +63,17 @@ def test_noalloc_router_matches_workspace_router_twice_in_a_row():
         torch.cuda.synchronize()
         results.append((c, idx_n.cpu(), w_n.cpu(), aux_n.cpu(), idx_r.cpu(), w_r.cpu(), aux_r.cpu()))
     for c, idx_n, w_n, aux_n, idx_r, w_r, aux_r in results:
-        # the same kernels run on the same inputs: routing identical, weights and
-        # aux within the tolerance the router parity tests use
-        assert torch.equal(idx_n, idx_r), c.name
-        np.testing.assert_allclose(w_n.numpy(), w_r.numpy(), rtol=1e-4, atol=1e-6)
+        inp = generate(c, seed=21, device="cuda")
+        ref = oracle.router(inp["x"], inp["w_r"], c.k, score=c.score, normalize=c.normalize,
+                            scale=c.scale, n_group=c.n_group, topk_group=c.topk_group,
+                            group_topn=c.group_topn, logit_offset=inp["logit_offset"],
+                            sel_bias=inp["sel_bias"])
+        keep = ref.sel_gap >= 1e-6
+        if c.n_group > 1:
+            keep &= ref.group_gap >= 1e-6
+        keep = torch.from_numpy(keep)
+        assert torch.equal(idx_n[keep], idx_r[keep]), c.name
+        np.testing.assert_allclose(w_n[keep].numpy(), w_r[keep].numpy(), rtol=1e-4, atol=1e-6)
         np.testing.assert_allclose(aux_n.numpy(), aux_r.numpy(), rtol=1e-4)
     # the first case again: the array now holds the second case's scratch
     c = CASES[0]
@@ -70,8 +82,8 @@ def test_noalloc_router_matches_workspace_router_twice_in_a_row():
     idx_n, w_n, aux_n = _outputs(c)
     B.moe_router_noalloc(inp["x"], inp["w_r"], shp, _cfg(c), idx_n, w_n, aux=aux_n)
     torch.cuda.synchronize()
-    assert torch.equal(idx_n.cpu(), results[0][4])
-    np.testing.assert_allclose(aux_n.cpu().numpy(), results[0][6].numpy(), rtol=1e-4)
+    assert torch.equal(idx_n.cpu(), results[0][1])     # same call, same result
+    np.testing.assert_allclose(aux_n.cpu().numpy(), results[0][3].numpy(), rtol=1e-6)
 
 
 def test_noalloc_router_rejects_shapes_beyond_its_scratch():
