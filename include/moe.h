@@ -83,7 +83,7 @@ typedef struct moe_ws_layout {
     size_t row_of;     /* int32 [T*k] routed row of each slot, -1 if dropped */
     size_t router;     /* router scratch: fp32 split-K partial logits [s,T,E], bf16 split of w_r [3,E,H], sums, counts */
     size_t a;          /* bf16 [T*k, I] SwiGLU activations (moe_forward only) */
-    size_t obuf;       /* bf16 [T*k, H] weighted expert outputs in slot order */
+    size_t obuf;       /* bf16 [T*k, H] weighted expert outputs in routed-row order */
     size_t total;      /* == moe_workspace_size */
 } moe_ws_layout_t;
 

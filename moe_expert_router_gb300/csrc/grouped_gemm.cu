@@ -11,8 +11,8 @@
 //
 //   stage 2, grouped_gemm_combine (stage2 = GEMM2 + combine): o[r] = a[r] .
 //   w2[e]^T; the epilogue scales o[r] by the routing weight of its slot and
-//   scatters it to the slot's row of obuf (slot order t*k + j); a light
-//   reduction then sums the k rows of every token into y.
+//   writes it to row r of obuf; the combine then gathers the k rows of every
+//   token through row_of and sums them into y.
 //
 //   router GEMM (the fused router's score function, MegaMoE guide opening
 //   section): partial fp32 logits of x . w_r^T with w_r split exactly into
@@ -78,6 +78,7 @@ constexpr int kNumThreads = 64 + EPI_THREADS + (MODE == kStage1 ? GATHER_THREADS
 struct __align__(1024) Smem {
     uint8_t a[STAGES][A_BYTES];
     uint8_t b[STAGES][B_BYTES];
+    uint8_t stage_out[EPI_WARPS][32 * 128];  // per epilogue warp: a 32 x 64 bf16 output box
     uint64_t full[STAGES];
     uint64_t empty[STAGES];
     uint64_t acc_full;
@@ -177,14 +178,45 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
     }
 }
 
+// silu(g) * u with the fast exponential and division intrinsics (a few
+// instructions instead of an IEEE division); their error (a few ulp of fp32)
+// is far below the bf16 rounding of the result. For g < -88 the quotient
+// flushes to 0, which is the bf16 value of silu there anyway.
 __device__ __forceinline__ float silu_mul(float g, float u) {
-    return g / (1.0f + __expf(-g)) * u;
+    return __fdividef(g, 1.0f + __expf(-g)) * u;
+}
+
+// 32 output columns of this thread's row, packed to bf16: stage 1 applies the
+// SwiGLU to accumulator columns [c, c+32) (gate) and [BN/2 + c, ...) (up),
+// stage 2 scales accumulator columns [c, c+32) by the row's routing weight.
+template <int MODE>
+__device__ __forceinline__ void epilogue_piece(uint32_t tacc, int c, float w, uint32_t (&pk)[16]) {
+    if constexpr (MODE == kStage1) {
+        uint32_t gv[32], uv[32];
+        tmem_ld32(tacc + c, gv);
+        tmem_ld32(tacc + BN / 2 + c, uv);
+        tmem_wait_ld();
+        tmem_reg_fence(gv);
+        tmem_reg_fence(uv);
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+            pk[i] = pack_bf16x2(silu_mul(__uint_as_float(gv[2 * i]), __uint_as_float(uv[2 * i])),
+                                silu_mul(__uint_as_float(gv[2 * i + 1]), __uint_as_float(uv[2 * i + 1])));
+    } else {
+        uint32_t v[32];
+        tmem_ld32(tacc + c, v);
+        tmem_wait_ld();
+        tmem_reg_fence(v);
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+            pk[i] = pack_bf16x2(w * __uint_as_float(v[2 * i]), w * __uint_as_float(v[2 * i + 1]));
+    }
 }
 
 template <int MODE>
 __global__ void __launch_bounds__(kNumThreads<MODE>, 1)
 tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
-               const GemmArgs g) {
+               const __grid_constant__ CUtensorMap tm_out, const GemmArgs g) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_addr(smem_raw);
     Smem &sm = *reinterpret_cast<Smem *>(smem_raw + ((1024u - (raw & 1023u)) & 1023u));
@@ -364,66 +396,62 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
             if (!ok || u < 0) break;
             const Unit t = decode_unit<MODE>(u, g);
             const bool valid = row < t.rows;
-            int slot = 0;
-            float w = 0.0f;
+            float w = 0.0f;                             // stage 2: routing weight of the row's slot
             if constexpr (MODE == kStage2) {
-                if (valid) {
-                    slot = g.perm_slot[t.row0 + row];
-                    w = g.topk_w[slot];
-                }
+                if (valid) w = g.topk_w[g.perm_slot[t.row0 + row]];
             }
             if (lane == 0) ok = mbar_wait(smem_addr(&sm.acc_full), acc_phase, abort_flag, g.err);
             ok = __shfl_sync(0xffffffffu, ok, 0);
             if (!ok) break;
             tc_fence_after();
             if (t.rows > half * BM) {                   // this half was computed
-                if constexpr (MODE == kStage1) {
-                    const int col0 = t.n * (BN / 2);
-                    __nv_bfloat16 *dst = g.out + static_cast<int64_t>(t.row0 + row) * g.n_out + col0;
+                if constexpr (MODE == kStage1 || MODE == kStage2) {
+                    // output rows are the unit's routed rows t.row0 + row (a for stage 1,
+                    // obuf for stage 2), columns [col0, col0 + ncols)
+                    constexpr int ncols = (MODE == kStage1) ? BN / 2 : BN;
+                    const int col0 = t.n * ncols;
+                    const int slab0 = half * BM + quad * 32;      // first unit row of this warp
+                    if (slab0 + 32 <= t.rows) {
+                        // whole 32-row slab valid: stage 32 x 64 bf16 boxes in shared
+                        // memory (128B-swizzled) and write each with one TMA store
+                        const uint32_t buf = smem_addr(sm.stage_out[warp - 2]);
 #pragma unroll 1
-                    for (int c = 0; c < BN / 2; c += 32) {
-                        uint32_t gv[32], uv[32];
-                        tmem_ld32(tacc + c, gv);
-                        tmem_ld32(tacc + BN / 2 + c, uv);
-                        tmem_wait_ld();
-                        tmem_reg_fence(gv);
-                        tmem_reg_fence(uv);
-                        if (valid) {
-                            uint32_t pk[16];
+                        for (int cc = 0; cc < ncols; cc += 64) {
+                            if (col0 + cc >= g.n_out) break;
+                            if (lane == 0) bulk_wait_read<0>();   // previous box read out
+                            __syncwarp();
 #pragma unroll
-                            for (int i = 0; i < 16; ++i) {
-                                const float a0 = silu_mul(__uint_as_float(gv[2 * i]), __uint_as_float(uv[2 * i]));
-                                const float a1 = silu_mul(__uint_as_float(gv[2 * i + 1]),
-                                                          __uint_as_float(uv[2 * i + 1]));
-                                pk[i] = pack_bf16x2(a0, a1);
+                            for (int p = 0; p < 2; ++p) {
+                                uint32_t pk[16];
+                                epilogue_piece<MODE>(tacc, cc + 32 * p, w, pk);
+#pragma unroll
+                                for (int j = 0; j < 4; ++j) {
+                                    const int c16 = p * 4 + j;
+                                    st_shared_v4(buf + lane * 128 + ((c16 ^ (lane & 7)) << 4), pk[4 * j],
+                                                 pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+                                }
                             }
-#pragma unroll
-                            for (int j = 0; j < 4; ++j) {
-                                if (col0 + c + j * 8 < g.n_out)
-                                    *reinterpret_cast<uint4 *>(dst + c + j * 8) =
-                                        make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+                            fence_proxy_async_smem();
+                            __syncwarp();
+                            if (lane == 0) {
+                                tma_store_2d(&tm_out, buf, col0 + cc, t.row0 + slab0);
+                                bulk_commit();
                             }
                         }
-                    }
-                } else if constexpr (MODE == kStage2) {
-                    const int col0 = t.n * BN;
-                    __nv_bfloat16 *dst = g.out + static_cast<int64_t>(slot) * g.n_out + col0;
+                    } else {
+                        // partial slab (the expert's last rows): masked direct stores
+                        __nv_bfloat16 *dst = g.out + static_cast<int64_t>(t.row0 + row) * g.n_out + col0;
 #pragma unroll 1
-                    for (int c = 0; c < BN; c += 32) {
-                        uint32_t v[32];
-                        tmem_ld32(tacc + c, v);
-                        tmem_wait_ld();
-                        tmem_reg_fence(v);
-                        if (valid) {
+                        for (int c = 0; c < ncols; c += 32) {
                             uint32_t pk[16];
+                            epilogue_piece<MODE>(tacc, c, w, pk);
+                            if (valid) {
 #pragma unroll
-                            for (int i = 0; i < 16; ++i)
-                                pk[i] = pack_bf16x2(w * __uint_as_float(v[2 * i]), w * __uint_as_float(v[2 * i + 1]));
-#pragma unroll
-                            for (int j = 0; j < 4; ++j) {
-                                if (col0 + c + j * 8 < g.n_out)
-                                    *reinterpret_cast<uint4 *>(dst + c + j * 8) =
-                                        make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+                                for (int j = 0; j < 4; ++j) {
+                                    if (col0 + c + j * 8 < g.n_out)
+                                        *reinterpret_cast<uint4 *>(dst + c + j * 8) =
+                                            make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+                                }
                             }
                         }
                     }
@@ -460,6 +488,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
             mbar_arrive(smem_addr(&sm.acc_empty));
             acc_phase ^= 1u;
         }
+        if (lane == 0) bulk_wait<0>();                  // every output box written
     } else {
         // ------------------------------------------------ stage 1: routed x row gather
         // The dispatch of dispatch_grouped_gemm: 128 threads copy the x rows of
@@ -550,8 +579,9 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
     }
 }
 
-// y[t, :] = sum over the token's k slots of obuf[slot, :] (already weighted);
-// dropped slots (row_of < 0) are skipped. fp32 sum, bf16 result.
+// y[t, :] = sum over the token's k slots s of obuf[row_of[s], :] (rows already
+// weighted, in routed order); dropped slots (row_of < 0) are skipped. fp32 sum,
+// bf16 result.
 __global__ void __launch_bounds__(256)
 combine_kernel(const __nv_bfloat16 *__restrict__ obuf, const int32_t *__restrict__ row_of,
                __nv_bfloat16 *__restrict__ y, int T, int H, int k) {
@@ -564,8 +594,9 @@ combine_kernel(const __nv_bfloat16 *__restrict__ obuf, const int32_t *__restrict
         float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
         for (int j = 0; j < k; ++j) {
             const int64_t s = static_cast<int64_t>(t) * k + j;
-            if (row_of[s] < 0) continue;
-            const uint4 v = __ldg(reinterpret_cast<const uint4 *>(obuf + s * H + c));
+            const int r = row_of[s];
+            if (r < 0) continue;
+            const uint4 v = __ldg(reinterpret_cast<const uint4 *>(obuf + static_cast<int64_t>(r) * H + c));
             const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
@@ -617,14 +648,14 @@ cudaError_t setup_gemm_kernels() {
 
 cudaError_t launch_gemm1_swiglu(const GemmLaunch &p, cudaStream_t st) {
     const GemmArgs g = grouped_args(p, (p.n_out + BN / 2 - 1) / (BN / 2));
-    tc_gemm_kernel<kStage1><<<p.num_sms, kNumThreads<kStage1>, SMEM_BYTES, st>>>(*p.tm_a, *p.tm_b, g);
+    tc_gemm_kernel<kStage1><<<p.num_sms, kNumThreads<kStage1>, SMEM_BYTES, st>>>(*p.tm_a, *p.tm_b, *p.tm_out, g);
     note_launches(1);
     return cudaGetLastError();
 }
 
 cudaError_t launch_gemm2_scatter(const GemmLaunch &p, cudaStream_t st) {
     const GemmArgs g = grouped_args(p, (p.n_out + BN - 1) / BN);
-    tc_gemm_kernel<kStage2><<<p.num_sms, kNumThreads<kStage2>, SMEM_BYTES, st>>>(*p.tm_a, *p.tm_b, g);
+    tc_gemm_kernel<kStage2><<<p.num_sms, kNumThreads<kStage2>, SMEM_BYTES, st>>>(*p.tm_a, *p.tm_b, *p.tm_out, g);
     note_launches(1);
     return cudaGetLastError();
 }
@@ -648,7 +679,7 @@ cudaError_t launch_router_gemm(const RouterGemmLaunch &p, cudaStream_t st) {
     // accumulator unwritten
     if (p.splits < 1 || (p.splits - 1) * g.kb_per_split >= g.kb_total) return cudaErrorInvalidValue;
     const int grid = g.total_units < p.num_sms ? g.total_units : p.num_sms;
-    tc_gemm_kernel<kRouter><<<grid, kNumThreads<kRouter>, SMEM_BYTES, st>>>(*p.tm_x, *p.tm_w3, g);
+    tc_gemm_kernel<kRouter><<<grid, kNumThreads<kRouter>, SMEM_BYTES, st>>>(*p.tm_x, *p.tm_w3, *p.tm_w3, g);
     note_launches(1);
     return cudaGetLastError();
 }

@@ -110,12 +110,13 @@ struct MetadataLaunch {
 struct GemmLaunch {
     const CUtensorMap *tm_a;    // host-encoded tensor maps (copied into the launch)
     const CUtensorMap *tm_b;
+    const CUtensorMap *tm_out;  // output [R, n_out], box 64 x 32 (epilogue TMA stores)
     const int32_t *counts, *offsets, *mt_prefix, *perm_slot;
     const __nv_bfloat16 *x;     // stage 1: token rows gathered into the A tiles
     int32_t *err;
     int32_t *sched;             // [2] unit scheduler of this stage
     const float *topk_w;        // stage 2 only
-    __nv_bfloat16 *out;         // a [R, I] (stage 1) or obuf [R, H] (stage 2)
+    __nv_bfloat16 *out;         // a [R, I] (stage 1) or obuf [R, H] (stage 2), routed rows
     int E, k, K, n_out, b_rows, half;
     int num_sms;
 };

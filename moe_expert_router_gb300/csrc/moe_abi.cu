@@ -121,12 +121,14 @@ moe_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE
 moe_status_t run_gemm1(const moe_shape_t &s, const void *x, const void *w1, void *a, const Ws &w,
                        const DeviceState &d, cudaStream_t st) {
     // the x rows are gathered by the kernel's own warps; only w1 goes through TMA
-    CUtensorMap tm_w1;
-    if (!encode_bf16_2d(&tm_w1, w1, s.H, static_cast<uint64_t>(s.E) * 2 * s.I, 64, 128))
+    CUtensorMap tm_w1, tm_out;
+    if (!encode_bf16_2d(&tm_w1, w1, s.H, static_cast<uint64_t>(s.E) * 2 * s.I, 64, 128) ||
+        !encode_bf16_2d(&tm_out, a, s.I, static_cast<uint64_t>(s.T) * s.k, 64, 32))
         return MOE_ERR_CUDA;
     GemmLaunch p;
     p.tm_a = &tm_w1;
     p.tm_b = &tm_w1;
+    p.tm_out = &tm_out;
     p.x = static_cast<const __nv_bfloat16 *>(x);
     p.counts = w.counts;
     p.offsets = w.offsets;
@@ -149,14 +151,16 @@ moe_status_t run_gemm1(const moe_shape_t &s, const void *x, const void *w1, void
 // Stage 2: GEMM2 with the weighted scatter, then the k-way combine.
 moe_status_t run_gemm2(const moe_shape_t &s, const void *a, const float *topk_w, const void *w2,
                        void *y, const Ws &w, const DeviceState &d, cudaStream_t st) {
-    CUtensorMap tm_a, tm_w2;
+    CUtensorMap tm_a, tm_w2, tm_out;
     const uint64_t R = static_cast<uint64_t>(s.T) * s.k;
     if (!encode_bf16_2d(&tm_a, a, s.I, R, 64, 128)) return MOE_ERR_CUDA;
     if (!encode_bf16_2d(&tm_w2, w2, s.I, static_cast<uint64_t>(s.E) * s.H, 64, 256))
         return MOE_ERR_CUDA;
+    if (!encode_bf16_2d(&tm_out, w.obuf, s.H, R, 64, 32)) return MOE_ERR_CUDA;
     GemmLaunch p;
     p.tm_a = &tm_a;
     p.tm_b = &tm_w2;
+    p.tm_out = &tm_out;
     p.x = nullptr;
     p.counts = w.counts;
     p.offsets = w.offsets;
