@@ -44,7 +44,7 @@ class RouterCfg(ctypes.Structure):
 
 class WsLayout(ctypes.Structure):
     _fields_ = [(n, ctypes.c_size_t) for n in
-                ("err", "counts", "offsets", "mt_prefix", "perm_slot", "row_of", "router", "a",
+                ("err", "counts", "offsets", "mt_prefix", "perm_slot", "row_of", "meta", "router", "a",
                  "obuf", "total")]
 
 

@@ -33,8 +33,9 @@
 //                unit from a global counter, so CTAs running side by side work
 //                on neighbouring units and share each weight slab through L2.
 //   warp 0     = scheduler + TMA producer: claims units, publishes them to an
-//                in-CTA queue and fills a 3-stage ring of 128B-swizzled
-//                K-major tiles (per stage: two 128x64 A halves, one 256x64 B).
+//                in-CTA queue and fills a ring of swizzled K-major tiles (per
+//                stage: two 128 x BK A halves and one 256 x BK B tile; six
+//                32 KB stages at BK = 32, three 64 KB stages at BK = 64).
 //   warp 1     = TMEM allocator and single-thread tcgen05.mma issuer: per
 //                16-deep k-step one M=128 N=256 MMA per half into two fp32
 //                TMEM accumulators (all 512 columns).
@@ -55,10 +56,11 @@ constexpr int UM = kUnitM;                   // rows per work unit (two halves)
 constexpr int BK = kBK;
 constexpr int BN = kBN;
 constexpr int UMMA_K = 16;
-constexpr int STAGES = 3;
-constexpr int A_HALF_BYTES = BM * BK * 2;    // 16 KB
+constexpr int ROW_BYTES = BK * 2;            // bytes of one K-major tile row per stage
+constexpr int STAGES = (BK == 64) ? 3 : 6;
+constexpr int A_HALF_BYTES = BM * BK * 2;    // 16 KB (BK 64) or 8 KB (BK 32)
 constexpr int A_BYTES = 2 * A_HALF_BYTES;    // 32 KB
-constexpr int B_BYTES = BN * BK * 2;         // 32 KB
+constexpr int B_BYTES = BN * BK * 2;         // 32 KB or 16 KB
 constexpr int TMEM_COLS = 2 * BN;            // two accumulators: all 512 columns
 constexpr int EPI_WARPS = 8;
 constexpr int EPI_THREADS = EPI_WARPS * 32;
@@ -351,10 +353,10 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
 #pragma unroll
                     for (int kk = 0; kk < BK / UMMA_K; ++kk) {
                         const uint32_t acc = (kb > t.kb0 || kk > 0) ? 1u : 0u;
-                        const uint64_t bdesc = smem_desc_sw128(sb + kk * UMMA_K * 2);
-                        mma_bf16(tmem_base, smem_desc_sw128(sa + kk * UMMA_K * 2), bdesc, IDESC, acc);
+                        const uint64_t bdesc = smem_desc_swizzled<ROW_BYTES>(sb + kk * UMMA_K * 2);
+                        mma_bf16(tmem_base, smem_desc_swizzled<ROW_BYTES>(sa + kk * UMMA_K * 2), bdesc, IDESC, acc);
                         if (two)
-                            mma_bf16(tmem_base + BN, smem_desc_sw128(sa + A_HALF_BYTES + kk * UMMA_K * 2), bdesc,
+                            mma_bf16(tmem_base + BN, smem_desc_swizzled<ROW_BYTES>(sa + A_HALF_BYTES + kk * UMMA_K * 2), bdesc,
                                      IDESC, acc);
                     }
                     mma_commit(smem_addr(&sm.empty[stage]));   // frees the smem stage
@@ -493,14 +495,17 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
         // ------------------------------------------------ stage 1: routed x row gather
         // The dispatch of dispatch_grouped_gemm: 128 threads copy the x rows of
         // the unit's routed tokens straight into the 128B-swizzled A tiles with
-        // 16-byte cp.async (8 threads per 128-byte row slice, rows rg + 16i).
+        // 16-byte cp.async (one thread per 16-byte chunk of a row slice).
         // Each thread waits for its own copies, orders them before the tensor
         // core's async-proxy reads, then arrives on the stage's full barrier,
         // one stage behind its issue so that two stages of copies are in flight.
         if constexpr (MODE == kStage1) {
             const int gt = threadIdx.x - (64 + EPI_THREADS);
-            const int chunk = gt & 7;
-            const int rg = gt >> 3;
+            constexpr int CHUNKS = ROW_BYTES / 16;                 // per row slice
+            constexpr int RSTEP = GATHER_THREADS / CHUNKS;         // rows per pass
+            constexpr int NROWS = UM / RSTEP;                      // rows per thread
+            const int chunk = gt % CHUNKS;
+            const int rg = gt / CHUNKS;                            // rows rg + RSTEP i
             int stage = 0, q = 0, pending = -1;
             uint32_t phase = 0, qphase = 0;
             while (true) {
@@ -518,10 +523,10 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
                 if (++q == UQ) { q = 0; qphase ^= 1u; }
                 if (!ok || u < 0) break;
                 const Unit t = decode_unit<MODE>(u, g);
-                int tok[16];
+                int tok[NROWS];
 #pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    const int r = rg + 16 * i;
+                for (int i = 0; i < NROWS; ++i) {
+                    const int r = rg + RSTEP * i;
                     tok[i] = (r < t.rows) ? g.perm_slot[t.row0 + r] / g.k : -1;
                 }
                 for (int kb = t.kb0; kb < t.kb1; ++kb) {
@@ -533,12 +538,11 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
                     const uint32_t nbytes = col < g.K ? 16u : 0u;   // zero-fill the K tail
                     const uint32_t sa = smem_addr(sm.a[stage]);
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) {
+                    for (int i = 0; i < NROWS; ++i) {
                         if (tok[i] >= 0) {
-                            const int r = rg + 16 * i;
-                            const int rl = r & (BM - 1);
-                            const uint32_t dst = sa + (r >> 7) * A_HALF_BYTES + rl * (BK * 2) +
-                                                 ((chunk ^ (rl & 7)) << 4);
+                            const int r = rg + RSTEP * i;
+                            const uint32_t dst = sa + (r >> 7) * A_HALF_BYTES +
+                                                 swizzled_chunk<ROW_BYTES>(r & (BM - 1), chunk);
                             cp_async_16(dst, g.x + static_cast<int64_t>(tok[i]) * g.K + (nbytes ? col : 0), nbytes);
                         }
                     }

@@ -15,7 +15,14 @@ namespace moe {
 // counts row tiles in units of kUnitM, so every grouped GEMM uses that value.
 constexpr int kBM = 128;
 constexpr int kUnitM = 256;
-constexpr int kBK = 64;     // reduction depth of one pipeline stage
+// Reduction depth of one pipeline stage: 32 bf16 = 64-byte rows with the 64-byte
+// swizzle (six 32 KB stages), or 64 = 128-byte rows with the 128-byte swizzle
+// (three 64 KB stages).
+#ifndef MOE_STAGE_BK
+#define MOE_STAGE_BK 64
+#endif
+constexpr int kBK = MOE_STAGE_BK;
+static_assert(kBK == 32 || kBK == 64, "stage depth must be 32 or 64");
 constexpr int kBN = 256;    // accumulator columns of one tile
 
 // Workspace header (zeroed by moe_workspace_init):
@@ -24,7 +31,11 @@ constexpr int kBN = 256;    // accumulator columns of one tile
 //   byte 8  int32[2] stage-1 unit scheduler (next unit, finished CTAs)
 //   byte 16 int32[2] stage-2 unit scheduler
 //   byte 24 int32[2] router-GEMM unit scheduler
+//   byte 32 int32    routing-metadata block ticket
 constexpr size_t kWsHeaderBytes = 256;
+
+// Slots per CTA of the routing-metadata kernels (one histogram row each).
+constexpr int kMetaChunk = 4096;
 
 inline size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
@@ -103,6 +114,8 @@ struct MetadataLaunch {
     const int32_t *topk_idx;
     int R, E;
     int32_t *counts, *offsets, *mt_prefix, *perm_slot, *row_of, *err;
+    int32_t *block_hist;        // [ceil(R / kMetaChunk), E]
+    int32_t *ticket;
 };
 
 // One grouped GEMM launch: stage 1 (fused x row gather + SwiGLU epilogue) or stage 2
@@ -151,7 +164,7 @@ cudaError_t setup_metadata_kernels();
 cudaError_t setup_gemm_kernels();
 
 // bf16 tensor [rows, inner] (inner contiguous) with a box_inner x box_rows box,
-// 128-byte swizzle, zero fill out of bounds. False if the encoder is missing
+// zero fill out of bounds; the swizzle span equals the box row (64 or 128 bytes). False if the encoder is missing
 // or rejects the arguments.
 bool encode_bf16_2d(CUtensorMap *map, const void *base, uint64_t inner, uint64_t rows,
                     uint32_t box_inner, uint32_t box_rows);

@@ -76,6 +76,7 @@ moe_ws_layout_t make_layout(const moe_shape_t &s) {
     L.mt_prefix = off; off = align256(off + 4 * (E + 1));
     L.perm_slot = off; off = align256(off + 4 * R);
     L.row_of = off;    off = align256(off + 4 * R);
+    L.meta = off;      off = align256(off + 4 * E * ((R + kMetaChunk - 1) / kMetaChunk));
     L.router = off;    off = align256(off + router_scratch_bytes(T, H, E, router_splits(T, H, E)));
     L.a = off;         off = align256(off + 2 * R * I);
     L.obuf = off;      off = align256(off + 2 * R * H);
@@ -85,6 +86,7 @@ moe_ws_layout_t make_layout(const moe_shape_t &s) {
 
 struct Ws {
     int32_t *err, *ticket, *counts, *offsets, *mt_prefix, *perm_slot, *row_of, *sched1, *sched2;
+    int32_t *meta, *meta_ticket;
     RouterScratch router;
     __nv_bfloat16 *a, *obuf;
 };
@@ -100,6 +102,8 @@ Ws carve(void *ws, const moe_shape_t &s) {
     w.mt_prefix = reinterpret_cast<int32_t *>(b + L.mt_prefix);
     w.perm_slot = reinterpret_cast<int32_t *>(b + L.perm_slot);
     w.row_of = reinterpret_cast<int32_t *>(b + L.row_of);
+    w.meta = reinterpret_cast<int32_t *>(b + L.meta);
+    w.meta_ticket = reinterpret_cast<int32_t *>(b + 32);
     w.sched1 = reinterpret_cast<int32_t *>(b + 8);
     w.sched2 = reinterpret_cast<int32_t *>(b + 16);
     w.router = carve_router_scratch(b + L.router, s.T, s.H, s.E, router_splits(s.T, s.H, s.E),
@@ -122,7 +126,7 @@ moe_status_t run_gemm1(const moe_shape_t &s, const void *x, const void *w1, void
                        const DeviceState &d, cudaStream_t st) {
     // the x rows are gathered by the kernel's own warps; only w1 goes through TMA
     CUtensorMap tm_w1, tm_out;
-    if (!encode_bf16_2d(&tm_w1, w1, s.H, static_cast<uint64_t>(s.E) * 2 * s.I, 64, 128) ||
+    if (!encode_bf16_2d(&tm_w1, w1, s.H, static_cast<uint64_t>(s.E) * 2 * s.I, kBK, 128) ||
         !encode_bf16_2d(&tm_out, a, s.I, static_cast<uint64_t>(s.T) * s.k, 64, 32))
         return MOE_ERR_CUDA;
     GemmLaunch p;
@@ -153,8 +157,8 @@ moe_status_t run_gemm2(const moe_shape_t &s, const void *a, const float *topk_w,
                        void *y, const Ws &w, const DeviceState &d, cudaStream_t st) {
     CUtensorMap tm_a, tm_w2, tm_out;
     const uint64_t R = static_cast<uint64_t>(s.T) * s.k;
-    if (!encode_bf16_2d(&tm_a, a, s.I, R, 64, 128)) return MOE_ERR_CUDA;
-    if (!encode_bf16_2d(&tm_w2, w2, s.I, static_cast<uint64_t>(s.E) * s.H, 64, 256))
+    if (!encode_bf16_2d(&tm_a, a, s.I, R, kBK, 128)) return MOE_ERR_CUDA;
+    if (!encode_bf16_2d(&tm_w2, w2, s.I, static_cast<uint64_t>(s.E) * s.H, kBK, 256))
         return MOE_ERR_CUDA;
     if (!encode_bf16_2d(&tm_out, w.obuf, s.H, R, 64, 32)) return MOE_ERR_CUDA;
     GemmLaunch p;
@@ -200,6 +204,8 @@ moe_status_t run_metadata(const moe_shape_t &s, const int32_t *topk_idx, const W
     m.perm_slot = w.perm_slot;
     m.row_of = w.row_of;
     m.err = w.err;
+    m.block_hist = w.meta;
+    m.ticket = w.meta_ticket;
     return cuda_status(launch_routing_metadata(m, st));
 }
 
@@ -226,12 +232,14 @@ bool encode_bf16_2d(CUtensorMap *map, const void *base, uint64_t inner, uint64_t
         cudaGetLastError();
     });
     if (g_encode == nullptr) return false;
+    if (box_inner * 2 != 128 && box_inner * 2 != 64) return false;
     cuuint64_t dims[2] = {inner, rows};
     cuuint64_t strides[1] = {inner * 2};
     cuuint32_t box[2] = {box_inner, box_rows};
     cuuint32_t estr[2] = {1, 1};
     return g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides,
-                    box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                    box_inner * 2 == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 

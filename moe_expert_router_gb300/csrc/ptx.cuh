@@ -204,18 +204,31 @@ __device__ __forceinline__ void mma_commit(uint32_t bar) {
         ::"r"(bar) : "memory");
 }
 
-// Shared-memory matrix descriptor for a K-major bf16 tile stored as 128-byte
-// rows with the 128-byte swizzle (what TMA writes with CU_TENSOR_MAP_SWIZZLE_128B):
-// 8-row groups are 1024 bytes apart (stride byte offset); the leading byte
-// offset is unused for this layout; version 1 (bits 46-47); layout 2 = 128B swizzle.
-__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr) {
+// Shared-memory matrix descriptor for a K-major bf16 tile stored as ROW_BYTES
+// rows with the matching swizzle (what TMA writes with the 128- or 64-byte
+// swizzle): 8-row groups are 8 * ROW_BYTES apart (stride byte offset); the
+// leading byte offset is unused for these layouts; version 1 (bits 46-47);
+// layout type 2 = 128-byte swizzle, 4 = 64-byte swizzle (bits 61-63).
+template <int ROW_BYTES>
+__device__ __forceinline__ uint64_t smem_desc_swizzled(uint32_t saddr) {
+    static_assert(ROW_BYTES == 128 || ROW_BYTES == 64, "128- or 64-byte swizzle");
     uint64_t d = 0;
     d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
     d |= static_cast<uint64_t>(1) << 16;
-    d |= static_cast<uint64_t>(1024 >> 4) << 32;
+    d |= static_cast<uint64_t>((8 * ROW_BYTES) >> 4) << 32;
     d |= static_cast<uint64_t>(1) << 46;
-    d |= static_cast<uint64_t>(2) << 61;
+    d |= static_cast<uint64_t>(ROW_BYTES == 128 ? 2 : 4) << 61;
     return d;
+}
+
+// Byte offset of 16-byte chunk c of row r inside a tile of ROW_BYTES rows laid
+// out with the matching TMA swizzle: the chunk index is XORed with address
+// bits 7.. of the row start (r mod 8 for 128-byte rows, (r / 2) mod 4 for
+// 64-byte rows).
+template <int ROW_BYTES>
+__device__ __forceinline__ uint32_t swizzled_chunk(int r, int c) {
+    if constexpr (ROW_BYTES == 128) return r * 128 + ((c ^ (r & 7)) << 4);
+    else return r * 64 + ((c ^ ((r >> 1) & 3)) << 4);
 }
 
 // Instruction descriptor of kind::f16 with bf16 A and B (both K-major) and an

@@ -9,137 +9,188 @@
 //   increasing slot order inside each expert) and row_of[s] (inverse, -1 for a
 //   dropped slot).
 //
-// One CTA of 32 warps. Warp w owns the contiguous slot range
-// [w*chunk, (w+1)*chunk): pass 1 counts per (warp, expert) with __match_any,
-// pass 2 turns those counts into per-warp starting ranks and the expert
-// offsets, pass 3 re-walks the range and places every slot. Walking the slots
-// in order inside each warp and the warps in order makes the permutation
-// stable without sorting.
+// Two kernels over chunks of kChunk consecutive slots (one CTA per chunk):
+//   count : per-chunk expert histogram (warp __match_any + shared atomics),
+//           stored as block_hist[chunk][e]. The last CTA to finish (ticket)
+//           turns the histograms into per-(chunk, expert) starting rows, the
+//           counts, offsets and the row-tile prefix.
+//   place : each warp of a chunk counts its own contiguous sub-range, the CTA
+//           turns those into per-warp starting ranks, and the warp walks its
+//           sub-range again in slot order, giving every slot its row.
+// Chunks, warps and lanes all walk slots in increasing order, so the
+// permutation is stable without a sort.
 #include "internal.cuh"
 
 namespace moe {
 
 namespace {
 
-constexpr int kMetaThreads = 1024;
-constexpr int kMetaWarps = kMetaThreads / 32;
+constexpr int kChunk = kMetaChunk;       // slots per CTA
+constexpr int kThreads = 256;
+constexpr int kWarps = kThreads / 32;
+constexpr int kWarpSlots = kChunk / kWarps;
 
-__global__ void __launch_bounds__(kMetaThreads, 1)
-routing_metadata_kernel(const int32_t *__restrict__ topk_idx, int R, int E,
-                        int32_t *__restrict__ counts, int32_t *__restrict__ offsets,
-                        int32_t *__restrict__ mt_prefix, int32_t *__restrict__ perm_slot,
-                        int32_t *__restrict__ row_of, int32_t *__restrict__ err) {
-    extern __shared__ int32_t sh[];
-    int32_t *hist = sh;                       // [kMetaWarps][E]: counts, then start ranks
-    int32_t *base = sh + kMetaWarps * E;      // [E]: expert offsets
-    __shared__ int32_t warp_tot_c[kMetaWarps], warp_tot_m[kMetaWarps];
-
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    for (int i = threadIdx.x; i < kMetaWarps * E; i += kMetaThreads) hist[i] = 0;
+__global__ void __launch_bounds__(kThreads)
+metadata_count_kernel(const int32_t *__restrict__ topk_idx, int R, int E, int n_chunks,
+                      int32_t *__restrict__ block_hist, int32_t *__restrict__ counts,
+                      int32_t *__restrict__ offsets, int32_t *__restrict__ mt_prefix,
+                      int32_t *__restrict__ ticket, int32_t *__restrict__ err) {
+    extern __shared__ int32_t hist[];    // [E]
+    __shared__ int is_last;
+    __shared__ int32_t warp_tot_c[32], warp_tot_m[32];
+    for (int e = threadIdx.x; e < E; e += kThreads) hist[e] = 0;
     __syncthreads();
-
-    const int chunk = (R + kMetaWarps - 1) / kMetaWarps;
-    const int beg = warp * chunk;
-    const int end = min(R, beg + chunk);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int beg = blockIdx.x * kChunk + warp * kWarpSlots;
+    const int end = min(R, beg + kWarpSlots);
     int bad = 0;
-
-    // pass 1: rows per (warp, expert)
     for (int s0 = beg; s0 < end; s0 += 32) {
         const int s = s0 + lane;
         const int e = (s < end) ? topk_idx[s] : -1;
         const bool valid = (s < end) && e >= 0 && e < E;
         bad |= (s < end) && !valid;
         const unsigned peers = __match_any_sync(0xffffffffu, valid ? e : -1);
-        if (valid && lane == __ffs(peers) - 1) hist[warp * E + e] += __popc(peers);
+        if (valid && lane == __ffs(peers) - 1) atomicAdd(&hist[e], __popc(peers));
     }
+    if (bad) atomicOr(err, MOE_DEVERR_BAD_EXPERT_INDEX);
     __syncthreads();
+    for (int e = threadIdx.x; e < E; e += kThreads) block_hist[static_cast<int64_t>(blockIdx.x) * E + e] = hist[e];
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) is_last = (atomicAdd(ticket, 1) == static_cast<int>(gridDim.x) - 1);
+    __syncthreads();
+    if (!is_last) return;
+    __threadfence();
 
-    // pass 2a: per expert, running total over warps -> each warp's starting rank
-    for (int e = threadIdx.x; e < E; e += kMetaThreads) {
+    // last CTA: per expert, running total over chunks (chunk order = slot order)
+    for (int e = threadIdx.x; e < E; e += kThreads) {
         int run = 0;
-        for (int w = 0; w < kMetaWarps; ++w) {
-            const int c = hist[w * E + e];
-            hist[w * E + e] = run;
+        for (int b = 0; b < n_chunks; ++b) {
+            const int64_t i = static_cast<int64_t>(b) * E + e;
+            const int c = __ldcg(&block_hist[i]);
+            block_hist[i] = run;
             run += c;
         }
-        base[e] = run;
+        hist[e] = run;                    // counts
     }
     __syncthreads();
-
-    // pass 2b: exclusive scans over experts of counts and of row tiles (E <= 1024)
-    const int e = threadIdx.x;
-    const int c = (e < E) ? base[e] : 0;
-    const int m = (c + kUnitM - 1) / kUnitM;
-    int ic = c, im = m;
-#pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-        const int yc = __shfl_up_sync(0xffffffffu, ic, off);
-        const int ym = __shfl_up_sync(0xffffffffu, im, off);
-        if (lane >= off) { ic += yc; im += ym; }
-    }
-    if (lane == 31) { warp_tot_c[warp] = ic; warp_tot_m[warp] = im; }
-    __syncthreads();
-    if (warp == 0) {
-        int vc = warp_tot_c[lane], vm = warp_tot_m[lane];
-        const int oc = vc, om = vm;
+    // exclusive scans over experts of counts and of 256-row tiles, kThreads per pass
+    int carry_c = 0, carry_m = 0;
+    for (int e0 = 0; e0 < E; e0 += kThreads) {
+        const int e = e0 + threadIdx.x;
+        const int c = (e < E) ? hist[e] : 0;
+        const int m = (c + kUnitM - 1) / kUnitM;
+        int ic = c, im = m;
 #pragma unroll
         for (int off = 1; off < 32; off <<= 1) {
-            const int yc = __shfl_up_sync(0xffffffffu, vc, off);
-            const int ym = __shfl_up_sync(0xffffffffu, vm, off);
-            if (lane >= off) { vc += yc; vm += ym; }
+            const int yc = __shfl_up_sync(0xffffffffu, ic, off);
+            const int ym = __shfl_up_sync(0xffffffffu, im, off);
+            if (lane >= off) { ic += yc; im += ym; }
         }
-        warp_tot_c[lane] = vc - oc;   // exclusive prefix of the warp totals
-        warp_tot_m[lane] = vm - om;
-    }
-    __syncthreads();
-    const int ex_c = ic - c + warp_tot_c[warp];
-    const int ex_m = im - m + warp_tot_m[warp];
-    if (e < E) {
-        counts[e] = c;
-        offsets[e] = ex_c;
-        mt_prefix[e] = ex_m;
-        base[e] = ex_c;
-        if (e == E - 1) {
-            offsets[E] = ex_c + c;
-            mt_prefix[E] = ex_m + m;
+        if (lane == 31) { warp_tot_c[warp] = ic; warp_tot_m[warp] = im; }
+        __syncthreads();
+        if (warp == 0) {
+            int vc = lane < kWarps ? warp_tot_c[lane] : 0, vm = lane < kWarps ? warp_tot_m[lane] : 0;
+            const int oc = vc, om = vm;
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const int yc = __shfl_up_sync(0xffffffffu, vc, off);
+                const int ym = __shfl_up_sync(0xffffffffu, vm, off);
+                if (lane >= off) { vc += yc; vm += ym; }
+            }
+            if (lane < kWarps) { warp_tot_c[lane] = vc - oc; warp_tot_m[lane] = vm - om; }
         }
+        __syncthreads();
+        const int ex_c = carry_c + ic - c + warp_tot_c[warp];
+        const int ex_m = carry_m + im - m + warp_tot_m[warp];
+        if (e < E) {
+            counts[e] = c;
+            offsets[e] = ex_c;
+            mt_prefix[e] = ex_m;
+            if (e == E - 1) {
+                offsets[E] = ex_c + c;
+                mt_prefix[E] = ex_m + m;
+            }
+        }
+        // carry the pass total to the next pass
+        __syncthreads();
+        if (threadIdx.x == kThreads - 1) { warp_tot_c[31] = ex_c + c; warp_tot_m[31] = ex_m + m; }
+        __syncthreads();
+        carry_c = warp_tot_c[31];
+        carry_m = warp_tot_m[31];
+        __syncthreads();
     }
-    __syncthreads();
+    if (threadIdx.x == 0) *ticket = 0;   // ready for the next launch
+}
 
-    // pass 3: place every slot
+__global__ void __launch_bounds__(kThreads)
+metadata_place_kernel(const int32_t *__restrict__ topk_idx, int R, int E,
+                      const int32_t *__restrict__ block_hist, const int32_t *__restrict__ offsets,
+                      int32_t *__restrict__ perm_slot, int32_t *__restrict__ row_of) {
+    extern __shared__ int32_t sh[];
+    int32_t *base = sh;                  // [E]: first row of this chunk in each expert
+    int32_t *whist = sh + E;             // [kWarps][E]: per-warp counts, then start ranks
+    for (int e = threadIdx.x; e < E; e += kThreads) {
+        base[e] = offsets[e] + block_hist[static_cast<int64_t>(blockIdx.x) * E + e];
+        for (int w = 0; w < kWarps; ++w) whist[w * E + e] = 0;
+    }
+    __syncthreads();
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int beg = blockIdx.x * kChunk + warp * kWarpSlots;
+    const int end = min(R, beg + kWarpSlots);
+    int32_t *mine = whist + warp * E;
     for (int s0 = beg; s0 < end; s0 += 32) {
         const int s = s0 + lane;
-        const int ee = (s < end) ? topk_idx[s] : -1;
-        const bool valid = (s < end) && ee >= 0 && ee < E;
-        const unsigned peers = __match_any_sync(0xffffffffu, valid ? ee : -1);
+        const int e = (s < end) ? topk_idx[s] : -1;
+        const bool valid = (s < end) && e >= 0 && e < E;
+        const unsigned peers = __match_any_sync(0xffffffffu, valid ? e : -1);
+        if (valid && lane == __ffs(peers) - 1) mine[e] += __popc(peers);
+    }
+    __syncthreads();
+    for (int e = threadIdx.x; e < E; e += kThreads) {
+        int run = base[e];
+        for (int w = 0; w < kWarps; ++w) {
+            const int c = whist[w * E + e];
+            whist[w * E + e] = run;
+            run += c;
+        }
+    }
+    __syncthreads();
+    for (int s0 = beg; s0 < end; s0 += 32) {
+        const int s = s0 + lane;
+        const int e = (s < end) ? topk_idx[s] : -1;
+        const bool valid = (s < end) && e >= 0 && e < E;
+        const unsigned peers = __match_any_sync(0xffffffffu, valid ? e : -1);
         if (valid) {
-            const int rank = __popc(peers & ((1u << lane) - 1u));
-            const int pos = base[ee] + hist[warp * E + ee] + rank;
+            const int pos = mine[e] + __popc(peers & ((1u << lane) - 1u));
             perm_slot[pos] = s;
             row_of[s] = pos;
         } else if (s < end) {
             row_of[s] = -1;
         }
         __syncwarp();
-        if (valid && lane == __ffs(peers) - 1) hist[warp * E + ee] += __popc(peers);
+        if (valid && lane == __ffs(peers) - 1) mine[e] += __popc(peers);
         __syncwarp();
     }
-    if (bad) atomicOr(err, MOE_DEVERR_BAD_EXPERT_INDEX);
 }
 
-size_t metadata_smem(int E) { return sizeof(int32_t) * static_cast<size_t>(kMetaWarps + 1) * E; }
+size_t place_smem(int E) { return sizeof(int32_t) * static_cast<size_t>(kWarps + 1) * E; }
 
 }  // namespace
 
 cudaError_t setup_metadata_kernels() {
-    return cudaFuncSetAttribute(routing_metadata_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                static_cast<int>(metadata_smem(1024)));
+    return cudaFuncSetAttribute(metadata_place_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                static_cast<int>(place_smem(1024)));
 }
 
 cudaError_t launch_routing_metadata(const MetadataLaunch &p, cudaStream_t st) {
-    routing_metadata_kernel<<<1, kMetaThreads, metadata_smem(p.E), st>>>(
-        p.topk_idx, p.R, p.E, p.counts, p.offsets, p.mt_prefix, p.perm_slot, p.row_of, p.err);
-    note_launches(1);
+    const int n_chunks = (p.R + kChunk - 1) / kChunk;
+    if (n_chunks == 0) return cudaSuccess;
+    metadata_count_kernel<<<n_chunks, kThreads, sizeof(int32_t) * p.E, st>>>(
+        p.topk_idx, p.R, p.E, n_chunks, p.block_hist, p.counts, p.offsets, p.mt_prefix, p.ticket, p.err);
+    metadata_place_kernel<<<n_chunks, kThreads, place_smem(p.E), st>>>(
+        p.topk_idx, p.R, p.E, p.block_hist, p.offsets, p.perm_slot, p.row_of);
+    note_launches(2);
     return cudaGetLastError();
 }
 

@@ -74,6 +74,14 @@ CONFIGS: dict[str, MoEConfig] = {
                              description="Zipf(1.2)-skewed routing, decode-like T=64"),
     "train": MoEConfig("train", T=8192, H=4096, I=1536, E=64, k=6, backward=True,
                        description="training step shapes (forward part)"),
+    # profiling size: the large_group geometry per expert (H, I, k, groups, about
+    # 256 routed rows per expert) with 32 experts, so that a full ncu capture
+    # holds about 3 GB on the device
+    "large_group_slice": MoEConfig("large_group_slice", T=1024, H=7168, I=2048, E=32, k=8,
+                                   score="sigmoid", scale=2.5, n_group=8, topk_group=4,
+                                   group_topn=2, sel_bias=True,
+                                   description="large_group per-expert geometry, 32 experts "
+                                               "(profiling size)"),
 }
 
 

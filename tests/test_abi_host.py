@@ -58,7 +58,7 @@ def test_workspace_size_and_layout(lib):
         L = B.moe_workspace_layout(shp)
         R = cfg.T * cfg.k
         assert L.total == n
-        offs = [L.counts, L.offsets, L.mt_prefix, L.perm_slot, L.row_of, L.router, L.a, L.obuf]
+        offs = [L.counts, L.offsets, L.mt_prefix, L.perm_slot, L.row_of, L.meta, L.router, L.a, L.obuf]
         assert all(o % 256 == 0 for o in offs) and offs == sorted(offs) and L.err == 0
         assert L.offsets - L.counts >= 4 * cfg.E
         assert L.row_of - L.perm_slot >= 4 * R
