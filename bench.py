@@ -34,6 +34,26 @@ from moe_expert_router_gb300.workloads import CONFIGS, generate  # noqa: E402
 METRIC = "MoE expert-path TFLOP/s and tokens/s (1 GB300) and fraction of bf16/HBM roofline"
 L2_FLUSH_BYTES = 256 << 20
 
+# DRAM bytes (read + write) per launch of the stage-1 kernel, from ncu captures
+# of `bench.py --workload <name> --steps 2 --warmup 1 --no-cpu-baseline`
+# (summaries under profiles/). Reported only while the kernel sources still
+# hash to the value recorded with the capture; otherwise traffic is null.
+KERNEL_SOURCES = ("moe_expert_router_gb300/csrc/grouped_gemm.cu", "moe_expert_router_gb300/csrc/ptx.cuh",
+                  "moe_expert_router_gb300/csrc/internal.cuh")
+STAGE1_TRAFFIC = {
+    # profiles/tc_gemm_mid_ncu.md: 804.77 MB read + 59.73 MB written
+    "mid": {"src": "a7f446c52efcace7", "bytes": 864.5e6},
+}
+
+
+def kernel_source_hash():
+    import hashlib
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
 
 def measured_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
@@ -387,9 +407,11 @@ def main():
             roof = {"bound": "hbm", "achieved": b / (dom_ms / 1e3) / 1e9, "peak": peaks["hbm_gbs"],
                     "unit": "GB/s"}
         roof["frac"] = roof["achieved"] / roof["peak"]
-        roof["traffic"] = None
-        roof["kernel"] = ("grouped_gemm_kernel<true> (stage 1: gather + GEMM1 + SwiGLU)" if dom == "gemm1"
-                          else "grouped_gemm_kernel<false> + combine_kernel (stage 2)")
+        rec = STAGE1_TRAFFIC.get(cfg.name)
+        roof["traffic"] = rec["bytes"] if (dom == "gemm1" and rec and rec["src"] == kernel_source_hash()) else None
+        roof["algorithmic_bytes"] = b
+        roof["kernel"] = ("tc_gemm_kernel<kStage1> (stage 1: fused x row gather + GEMM1 + SwiGLU)"
+                          if dom == "gemm1" else "tc_gemm_kernel<kStage2> + combine_kernel (stage 2)")
         roof["peak_kind"] = f"{peaks['source']} burst"
         roof["kernel_ms"] = dom_ms
         out = {
