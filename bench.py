@@ -349,6 +349,21 @@ def run_reference(args, cfg):
     }
 
 
+def max_over_ranks(values, world, device="cpu"):
+    """Element-wise maximum over the ranks of the job (the job is as slow as its
+    slowest replica); identity for a single process."""
+    if world <= 1:
+        return [float(v) for v in values]
+    t = torch.tensor(values, dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return [float(v) for v in t.tolist()]
+
+
+def whole_job_throughput(units_per_rank_step, steps, world, total_ms):
+    """Units processed by all ranks per second over the slowest rank's time."""
+    return units_per_rank_step * steps * world / (total_ms / 1e3)
+
+
 def config_dict(cfg, args):
     return {"workload": cfg.name, "description": cfg.description, "T": cfg.T, "H": cfg.H,
             "I": cfg.I, "E": cfg.E, "k": cfg.k, "score": cfg.score, "n_group": cfg.n_group,
@@ -380,18 +395,14 @@ def main():
     if world > 1:
         torch.distributed.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
     res = run_ours(args, cfg, rank, world, local_rank)
-    total_ms = res["total_ms"]
-    e2e_ms = res["e2e_ms"]
-    if world > 1:
-        t = torch.tensor([total_ms, e2e_ms], dtype=torch.float64, device="cuda")
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms, e2e_ms = float(t[0]), float(t[1])
+    total_ms, e2e_ms = max_over_ranks([res["total_ms"], res["e2e_ms"]], world,
+                                      device=torch.device("cuda", local_rank))
 
     if rank == 0:
         peaks = measured_peaks()
         flops_step = cfg.expert_flops()
-        value = flops_step * args.steps * world / (total_ms / 1e3) / 1e12
-        tokens_per_s = cfg.T * args.steps * world / (total_ms / 1e3)
+        value = whole_job_throughput(flops_step, args.steps, world, total_ms) / 1e12
+        tokens_per_s = whole_job_throughput(cfg.T, args.steps, world, total_ms)
         # dominant kernel of the step and its roofline
         stage_avg = {n: sum(v) / len(v) for n, v in res["stage_ms"].items()}
         bf = res["bf"]
