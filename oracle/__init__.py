@@ -55,6 +55,12 @@ def _bind(lib):
     lib.oracle_expert_forward.restype = ctypes.c_int
     lib.oracle_num_threads.argtypes = []
     lib.oracle_num_threads.restype = ctypes.c_int
+    lib.oracle_expert_backward.argtypes = [i64, i64, i64, i64, i32, vp, vp, vp, vp, vp, vp,
+                                           vp, vp, vp, vp]
+    lib.oracle_expert_backward.restype = ctypes.c_int
+    lib.oracle_router_backward.argtypes = [i64, i64, i64, i32, vp, vp, vp, i32, i32, f64,
+                                           vp, vp, vp, vp, vp, vp]
+    lib.oracle_router_backward.restype = ctypes.c_int
     return lib
 
 
@@ -170,6 +176,65 @@ class Oracle:
             return y, a, o
         return y
 
+    def expert_backward(self, x, topk_idx, topk_w, w1, w2, dy, *, want_dw=True) -> Backward:
+        """dX (expert path), dW1, dW2 and the routing-weight gradient for dY."""
+        xb, w1b, w2b, dyb = _np(x), _np(w1), _np(w2), _np(dy)
+        assert all(a.dtype == np.uint16 for a in (xb, w1b, w2b, dyb))
+        idx = _np(topk_idx, np.int32)
+        w = _np(topk_w, np.float64)
+        T, H = xb.shape
+        E, twoI, _ = w1b.shape
+        I = twoI // 2
+        k = idx.shape[1]
+        dx = np.empty((T, H), np.float64)
+        dw1 = np.empty((E, 2 * I, H), np.float64) if want_dw else None
+        dw2 = np.empty((E, H, I), np.float64) if want_dw else None
+        dtw = np.empty((T, k), np.float64)
+        rc = self.lib.oracle_expert_backward(T, H, I, E, k, _ptr(xb), _ptr(idx), _ptr(w), _ptr(w1b),
+                                             _ptr(w2b), _ptr(dyb), _ptr(dx), _ptr(dw1), _ptr(dw2),
+                                             _ptr(dtw))
+        if rc != 0:
+            raise ValueError("oracle_expert_backward rejected its arguments")
+        return Backward(dx, dw1, dw2, dtw)
+
+    def router_backward(self, x, w_r, topk_idx, topk_w, dtopk_w, *, score="softmax",
+                        normalize=True, scale=1.0, logit_offset=None) -> RouterBackward:
+        """Logit gradient from the routing-weight gradient, and its dX / dW_r."""
+        xb = _np(x)
+        wr = _np(w_r, np.float32)
+        idx = _np(topk_idx, np.int32)
+        w = _np(topk_w, np.float64)
+        dw = _np(dtopk_w, np.float64)
+        off = None if logit_offset is None else _np(logit_offset, np.float32)
+        T, H = xb.shape
+        E = wr.shape[0]
+        k = idx.shape[1]
+        dl = np.empty((T, E), np.float64)
+        dxa = np.zeros((T, H), np.float64)
+        dwr = np.empty((E, H), np.float64)
+        rc = self.lib.oracle_router_backward(T, H, E, k, _ptr(xb), _ptr(wr), _ptr(off),
+                                             0 if score == "softmax" else 1, int(bool(normalize)),
+                                             float(scale), _ptr(idx), _ptr(w), _ptr(dw), _ptr(dl),
+                                             _ptr(dxa), _ptr(dwr))
+        if rc != 0:
+            raise ValueError("oracle_router_backward rejected its arguments")
+        return RouterBackward(dl, dxa, dwr)
+
+
+@dataclass
+class Backward:
+    dx: np.ndarray          # float64 [T, H]  (expert path only, router part not added)
+    dw1: np.ndarray         # float64 [E, 2I, H] or None
+    dw2: np.ndarray         # float64 [E, H, I] or None
+    dtopk_w: np.ndarray     # float64 [T, k]
+
+
+@dataclass
+class RouterBackward:
+    dlogits: np.ndarray     # float64 [T, E]
+    dx_add: np.ndarray      # float64 [T, H] router contribution to dX
+    dw_r: np.ndarray        # float64 [E, H]
+
 
 def default() -> Oracle:
     """The oracle built from moe_oracle.c (compiled on first use)."""
@@ -194,3 +259,11 @@ def expert_forward(*args, **kwargs):
 
 def num_threads() -> int:
     return default().num_threads()
+
+
+def expert_backward(*args, **kwargs) -> Backward:
+    return default().expert_backward(*args, **kwargs)
+
+
+def router_backward(*args, **kwargs) -> RouterBackward:
+    return default().router_backward(*args, **kwargs)

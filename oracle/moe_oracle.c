@@ -33,10 +33,12 @@
  *     P_e = (1/T) sum_t s_{t,e} over the full score vector.
  *
  * Parity status: every exported function is pinned by tests that do not call
- * the function's own formula again (closed forms of hand-built examples, the
- * even round-robin routing of the guide's force-load-balancing table, a dense
- * SwiGLU MLP in an independent library, brute force and invariants). The aux
- * value for sigmoid scoring has no pin beyond its definition: parity unpinned.
+ * its own formula again: closed forms of hand-built examples, the even
+ * round-robin routing of the guide's force-load-balancing table, a dense
+ * SwiGLU MLP in an independent library, brute force and invariants for the
+ * forward; torch fp64 autograd through an independently written forward for
+ * the backward. The aux value for sigmoid scoring has no pin beyond its
+ * definition: parity unpinned.
  */
 #include <math.h>
 #include <stdint.h>
@@ -80,6 +82,29 @@ static int64_t argmax_eligible(const double *v, const unsigned char *ok, int64_t
 }
 
 /*
+ * Scores of one token: l_e = sum_h x_h Wr[e,h] (+ logit_offset[e]), then
+ * s = softmax(l) over all E experts (score_fn 0) or sigmoid(l) (score_fn 1).
+ */
+static void token_scores(int64_t H, int64_t E, const uint16_t *x_t, const float *w_r,
+                         const float *logit_offset, int32_t score_fn, double *s) {
+    for (int64_t e = 0; e < E; ++e) {
+        double l = 0.0;
+        for (int64_t h = 0; h < H; ++h) l += bf16_value(x_t[h]) * (double)w_r[e * H + h];
+        if (logit_offset) l += (double)logit_offset[e];
+        s[e] = l;
+    }
+    if (score_fn == 0) {
+        double m = s[0];
+        for (int64_t e = 1; e < E; ++e) if (s[e] > m) m = s[e];
+        double z = 0.0;
+        for (int64_t e = 0; e < E; ++e) { s[e] = exp(s[e] - m); z += s[e]; }
+        for (int64_t e = 0; e < E; ++e) s[e] /= z;
+    } else {
+        for (int64_t e = 0; e < E; ++e) s[e] = 1.0 / (1.0 + exp(-s[e]));
+    }
+}
+
+/*
  * Router for one token (MegaMoE opening section: "score function +
  * group-limited top-k + aux score").
  *
@@ -104,22 +129,7 @@ static void route_one_token(int64_t H, int64_t E, int32_t k,
                             unsigned char *ok, unsigned char *gok,
                             int32_t *idx_out, double *w_out,
                             double *sel_gap_out, double *group_gap_out) {
-    /* logits and scores */
-    for (int64_t e = 0; e < E; ++e) {
-        double l = 0.0;
-        for (int64_t h = 0; h < H; ++h) l += bf16_value(x_t[h]) * (double)w_r[e * H + h];
-        if (logit_offset) l += (double)logit_offset[e];
-        s[e] = l;
-    }
-    if (score_fn == 0) {
-        double m = s[0];
-        for (int64_t e = 1; e < E; ++e) if (s[e] > m) m = s[e];
-        double z = 0.0;
-        for (int64_t e = 0; e < E; ++e) { s[e] = exp(s[e] - m); z += s[e]; }
-        for (int64_t e = 0; e < E; ++e) s[e] /= z;
-    } else {
-        for (int64_t e = 0; e < E; ++e) s[e] = 1.0 / (1.0 + exp(-s[e]));
-    }
+    token_scores(H, E, x_t, w_r, logit_offset, score_fn, s);
     for (int64_t e = 0; e < E; ++e) sel[e] = s[e] + (sel_bias ? (double)sel_bias[e] : 0.0);
 
     /* group limit */
@@ -284,6 +294,35 @@ int64_t oracle_routing_metadata(int64_t T, int32_t k, int64_t E, const int32_t *
 }
 
 /*
+ * One slot of expert e, given the token's values xt [H]:
+ *   g_i = sum_h W1[i, h] x_h        (gate rows [0, I))
+ *   u_i = sum_h W1[I + i, h] x_h    (up rows [I, 2I))
+ *   a_i = silu(g_i) * u_i
+ */
+static void slot_hidden(int64_t H, int64_t I, const uint16_t *W1, const double *xt,
+                        double *g, double *u, double *a) {
+    for (int64_t i = 0; i < I; ++i) {
+        double gi = 0.0, ui = 0.0;
+        for (int64_t h = 0; h < H; ++h) {
+            gi += bf16_value(W1[i * H + h]) * xt[h];
+            ui += bf16_value(W1[(I + i) * H + h]) * xt[h];
+        }
+        g[i] = gi;
+        u[i] = ui;
+        a[i] = silu(gi) * ui;
+    }
+}
+
+/* o_h = sum_i W2[h, i] a_i for one slot. */
+static void slot_output(int64_t H, int64_t I, const uint16_t *W2, const double *a, double *o) {
+    for (int64_t h = 0; h < H; ++h) {
+        double acc = 0.0;
+        for (int64_t i = 0; i < I; ++i) acc += bf16_value(W2[h * I + i]) * a[i];
+        o[h] = acc;
+    }
+}
+
+/*
  * Expert path forward, token by token (MegaMoE opening section:
  * dispatch_grouped_gemm -> SwiGLU -> grouped_gemm_combine).
  *
@@ -309,9 +348,11 @@ int oracle_expert_forward(int64_t T, int64_t H, int64_t I, int64_t E, int32_t k,
 #pragma omp parallel
     {
         double *xt = (double *)malloc(sizeof(double) * (size_t)H);
+        double *g = (double *)malloc(sizeof(double) * (size_t)I);
+        double *u = (double *)malloc(sizeof(double) * (size_t)I);
         double *a = (double *)malloc(sizeof(double) * (size_t)I);
         double *o = (double *)malloc(sizeof(double) * (size_t)H);
-        if (!xt || !a || !o) {
+        if (!xt || !g || !u || !a || !o) {
 #pragma omp atomic write
             bad = 1;
         } else {
@@ -329,27 +370,236 @@ int oracle_expert_forward(int64_t T, int64_t H, int64_t I, int64_t E, int32_t k,
                     }
                     const uint16_t *W1 = w1 + (int64_t)e * 2 * I * H;
                     const uint16_t *W2 = w2 + (int64_t)e * H * I;
-                    for (int64_t i = 0; i < I; ++i) {
-                        double g = 0.0, u = 0.0;
-                        for (int64_t h = 0; h < H; ++h) {
-                            g += bf16_value(W1[i * H + h]) * xt[h];
-                            u += bf16_value(W1[(I + i) * H + h]) * xt[h];
-                        }
-                        a[i] = silu(g) * u;
-                        if (a_slot) a_slot[slot * I + i] = a[i];
-                    }
-                    for (int64_t h = 0; h < H; ++h) {
-                        double acc = 0.0;
-                        for (int64_t i = 0; i < I; ++i) acc += bf16_value(W2[h * I + i]) * a[i];
-                        o[h] = acc;
-                        if (o_slot) o_slot[slot * H + h] = acc;
-                    }
+                    slot_hidden(H, I, W1, xt, g, u, a);
+                    slot_output(H, I, W2, a, o);
+                    if (a_slot) for (int64_t i = 0; i < I; ++i) a_slot[slot * I + i] = a[i];
+                    if (o_slot) for (int64_t h = 0; h < H; ++h) o_slot[slot * H + h] = o[h];
                     double w = topk_w[slot];
                     for (int64_t h = 0; h < H; ++h) yt[h] += w * o[h];
                 }
             }
         }
-        free(xt); free(a); free(o);
+        free(xt); free(g); free(u); free(a); free(o);
     }
     return bad ? -1 : 0;
+}
+
+/*
+ * Expert path backward, from its plain chain rule (MegaMoE guide, section
+ * "Design: two stages": stage 2's backward yields dW2, stage 1's dW1). With
+ * dY the gradient of y, for each token t and choice j with e = topk_idx[t,j]:
+ *
+ *   forward values  g, u, a = silu(g) * u, o = W2_e a      (as in the forward)
+ *   dw[t,j]   = <dY_t, o>                  gradient of the routing weight
+ *   dO        = w[t,j] dY_t
+ *   dA_i      = sum_h W2_e[h,i] dO_h
+ *   dU_i      = dA_i silu(g_i)
+ *   dG_i      = dA_i u_i silu'(g_i),   silu'(z) = s(z) (1 + z (1 - s(z))), s = sigmoid
+ *   dX_t     += sum_i W1_e[i,:] dG_i + W1_e[I+i,:] dU_i
+ *   dW1_e[i,:]   += dG_i x_t ;  dW1_e[I+i,:] += dU_i x_t
+ *   dW2_e[:,i]   += dO a_i
+ *
+ * dw1 [E,2I,H], dw2 [E,H,I], dx [T,H] and dtopk_w [T,k] are outputs (any may
+ * be NULL except dx). The weight gradients are accumulated per expert over its
+ * slots in flat slot order. Slots with an index outside [0, E) contribute
+ * nothing (their dtopk_w is 0).
+ */
+int oracle_expert_backward(int64_t T, int64_t H, int64_t I, int64_t E, int32_t k,
+                           const uint16_t *x, const int32_t *topk_idx, const double *topk_w,
+                           const uint16_t *w1, const uint16_t *w2, const uint16_t *dy,
+                           double *dx, double *dw1, double *dw2, double *dtopk_w) {
+    if (T < 0 || H <= 0 || I <= 0 || E <= 0 || k <= 0 || !x || !topk_idx || !topk_w || !w1 ||
+        !w2 || !dy || !dx)
+        return -1;
+    const int64_t R = T * k;
+    /* per-slot values kept for the weight gradients: dG|dU [R, 2I], dO [R, H], a [R, I] */
+    double *dh_s = (dw1 || dw2) ? (double *)calloc((size_t)R * 2 * I, sizeof(double)) : NULL;
+    double *do_s = dw2 ? (double *)calloc((size_t)R * H, sizeof(double)) : NULL;
+    double *a_s = dw2 ? (double *)calloc((size_t)R * I, sizeof(double)) : NULL;
+    if (((dw1 || dw2) && !dh_s) || (dw2 && (!do_s || !a_s))) {
+        free(dh_s); free(do_s); free(a_s);
+        return -1;
+    }
+    int bad = 0;
+#pragma omp parallel
+    {
+        double *xt = (double *)malloc(sizeof(double) * (size_t)H);
+        double *dyt = (double *)malloc(sizeof(double) * (size_t)H);
+        double *g = (double *)malloc(sizeof(double) * (size_t)I);
+        double *u = (double *)malloc(sizeof(double) * (size_t)I);
+        double *a = (double *)malloc(sizeof(double) * (size_t)I);
+        double *o = (double *)malloc(sizeof(double) * (size_t)H);
+        double *dO = (double *)malloc(sizeof(double) * (size_t)H);
+        double *dA = (double *)malloc(sizeof(double) * (size_t)I);
+        if (!xt || !dyt || !g || !u || !a || !o || !dO || !dA) {
+#pragma omp atomic write
+            bad = 1;
+        } else {
+#pragma omp for schedule(dynamic, 1)
+            for (int64_t t = 0; t < T; ++t) {
+                double *dxt = dx + t * H;
+                for (int64_t h = 0; h < H; ++h) {
+                    dxt[h] = 0.0;
+                    xt[h] = bf16_value(x[t * H + h]);
+                    dyt[h] = bf16_value(dy[t * H + h]);
+                }
+                for (int32_t j = 0; j < k; ++j) {
+                    const int64_t slot = t * k + j;
+                    const int32_t e = topk_idx[slot];
+                    if (e < 0 || e >= E) {
+                        if (dtopk_w) dtopk_w[slot] = 0.0;
+                        continue;
+                    }
+                    const uint16_t *W1 = w1 + (int64_t)e * 2 * I * H;
+                    const uint16_t *W2 = w2 + (int64_t)e * H * I;
+                    slot_hidden(H, I, W1, xt, g, u, a);
+                    slot_output(H, I, W2, a, o);
+                    const double w = topk_w[slot];
+                    double dwt = 0.0;
+                    for (int64_t h = 0; h < H; ++h) {
+                        dwt += dyt[h] * o[h];
+                        dO[h] = w * dyt[h];
+                    }
+                    if (dtopk_w) dtopk_w[slot] = dwt;
+                    for (int64_t i = 0; i < I; ++i) {
+                        double acc = 0.0;
+                        for (int64_t h = 0; h < H; ++h) acc += bf16_value(W2[h * I + i]) * dO[h];
+                        dA[i] = acc;
+                    }
+                    for (int64_t i = 0; i < I; ++i) {
+                        const double sg = 1.0 / (1.0 + exp(-g[i]));
+                        const double dsilu = sg * (1.0 + g[i] * (1.0 - sg));
+                        const double dU = dA[i] * silu(g[i]);
+                        const double dG = dA[i] * u[i] * dsilu;
+                        for (int64_t h = 0; h < H; ++h)
+                            dxt[h] += bf16_value(W1[i * H + h]) * dG + bf16_value(W1[(I + i) * H + h]) * dU;
+                        if (dh_s) {
+                            dh_s[slot * 2 * I + i] = dG;
+                            dh_s[slot * 2 * I + I + i] = dU;
+                        }
+                    }
+                    if (do_s) {
+                        for (int64_t h = 0; h < H; ++h) do_s[slot * H + h] = dO[h];
+                        for (int64_t i = 0; i < I; ++i) a_s[slot * I + i] = a[i];
+                    }
+                }
+            }
+        }
+        free(xt); free(dyt); free(g); free(u); free(a); free(o); free(dO); free(dA);
+    }
+    if (!bad && (dw1 || dw2)) {
+#pragma omp parallel for schedule(dynamic, 1)
+        for (int64_t e = 0; e < E; ++e) {
+            double *DW1 = dw1 ? dw1 + e * 2 * I * H : NULL;
+            double *DW2 = dw2 ? dw2 + e * H * I : NULL;
+            if (DW1) for (int64_t q = 0; q < 2 * I * H; ++q) DW1[q] = 0.0;
+            if (DW2) for (int64_t q = 0; q < H * I; ++q) DW2[q] = 0.0;
+            for (int64_t slot = 0; slot < R; ++slot) {
+                if (topk_idx[slot] != e) continue;
+                const int64_t t = slot / k;
+                if (DW1) {
+                    for (int64_t jj = 0; jj < 2 * I; ++jj) {
+                        const double d = dh_s[slot * 2 * I + jj];
+                        for (int64_t h = 0; h < H; ++h) DW1[jj * H + h] += d * bf16_value(x[t * H + h]);
+                    }
+                }
+                if (DW2) {
+                    for (int64_t h = 0; h < H; ++h) {
+                        const double d = do_s[slot * H + h];
+                        for (int64_t i = 0; i < I; ++i) DW2[h * I + i] += d * a_s[slot * I + i];
+                    }
+                }
+            }
+        }
+    }
+    free(dh_s); free(do_s); free(a_s);
+    return bad ? -1 : 0;
+}
+
+/*
+ * Router backward: the gradient of the logits from the gradient of the
+ * routing weights, then dX and dW_r through l = x W_r^T (+ offset). The
+ * selection (top-k, groups, bias) is piecewise constant and passes no
+ * gradient; the aux value is reported, not differentiated. With K the chosen
+ * experts of a token and p = the score function:
+ *
+ *   softmax, normalised:   w_j = scale e^{l_j} / sum_K e^l
+ *                          dl_i = w_i dw_i - (w_i / scale) sum_K w_j dw_j   (i in K)
+ *   softmax, plain:        w_j = scale s_j,  s = softmax over all E
+ *                          dl_i = scale s_i ([i in K] dw_i - sum_K s_j dw_j)
+ *   sigmoid, normalised:   w_j = scale s_j / S,  S = sum_K s
+ *                          dl_i = (s_i (1 - s_i) / S) (scale dw_i - sum_K w_j dw_j)   (i in K)
+ *   sigmoid, plain:        dl_i = scale s_i (1 - s_i) dw_i   (i in K)
+ *
+ *   dX_t += sum_e dl_{t,e} W_r[e,:]      dW_r[e,:] = sum_t dl_{t,e} x_t
+ *
+ * dlogits [T,E] (zero outside K for the normalised cases), dx_add [T,H] (added
+ * to, not overwritten) and dw_r [E,H] are outputs; any may be NULL.
+ */
+int oracle_router_backward(int64_t T, int64_t H, int64_t E, int32_t k,
+                           const uint16_t *x, const float *w_r, const float *logit_offset,
+                           int32_t score_fn, int32_t normalize, double scale,
+                           const int32_t *topk_idx, const double *topk_w, const double *dtopk_w,
+                           double *dlogits, double *dx_add, double *dw_r) {
+    if (T < 0 || H <= 0 || E <= 0 || k <= 0 || !x || !w_r || !topk_idx || !topk_w || !dtopk_w)
+        return -1;
+    double *dl = (double *)calloc((size_t)(T > 0 ? T : 1) * (size_t)E, sizeof(double));
+    if (!dl) return -1;
+#pragma omp parallel for schedule(dynamic, 4)
+    for (int64_t t = 0; t < T; ++t) {
+        double *dlt = dl + t * E;
+        const int32_t *K = topk_idx + t * k;
+        const double *w = topk_w + t * k;
+        const double *dw = dtopk_w + t * k;
+        /* scores of the token (needed by the plain softmax and the sigmoid cases) */
+        double *s = (double *)malloc(sizeof(double) * (size_t)E);
+        if (!s) continue;
+        token_scores(H, E, x + t * H, w_r, logit_offset, score_fn, s);
+        double sum_wdw = 0.0, sum_sdw = 0.0, S = 0.0;
+        for (int32_t j = 0; j < k; ++j) {
+            if (K[j] < 0 || K[j] >= E) continue;
+            sum_wdw += w[j] * dw[j];
+            sum_sdw += s[K[j]] * dw[j];
+            S += s[K[j]];
+        }
+        if (score_fn == 0 && normalize) {
+            for (int32_t j = 0; j < k; ++j)
+                if (K[j] >= 0 && K[j] < E) dlt[K[j]] += w[j] * dw[j] - (w[j] / scale) * sum_wdw;
+        } else if (score_fn == 0) {
+            for (int64_t e = 0; e < E; ++e) dlt[e] = -scale * s[e] * sum_sdw;
+            for (int32_t j = 0; j < k; ++j)
+                if (K[j] >= 0 && K[j] < E) dlt[K[j]] += scale * s[K[j]] * dw[j];
+        } else if (normalize) {
+            for (int32_t j = 0; j < k; ++j) {
+                if (K[j] < 0 || K[j] >= E) continue;
+                const double si = s[K[j]];
+                dlt[K[j]] += si * (1.0 - si) / S * (scale * dw[j] - sum_wdw);
+            }
+        } else {
+            for (int32_t j = 0; j < k; ++j) {
+                if (K[j] < 0 || K[j] >= E) continue;
+                const double si = s[K[j]];
+                dlt[K[j]] += scale * si * (1.0 - si) * dw[j];
+            }
+        }
+        if (dx_add)
+            for (int64_t h = 0; h < H; ++h) {
+                double acc = 0.0;
+                for (int64_t e = 0; e < E; ++e) acc += dlt[e] * (double)w_r[e * H + h];
+                dx_add[t * H + h] += acc;
+            }
+        free(s);
+    }
+    if (dw_r) {
+#pragma omp parallel for schedule(static)
+        for (int64_t e = 0; e < E; ++e)
+            for (int64_t h = 0; h < H; ++h) {
+                double acc = 0.0;
+                for (int64_t t = 0; t < T; ++t) acc += dl[t * E + e] * bf16_value(x[t * H + h]);
+                dw_r[e * H + h] = acc;
+            }
+    }
+    if (dlogits) memcpy(dlogits, dl, sizeof(double) * (size_t)T * (size_t)E);
+    free(dl);
+    return 0;
 }

@@ -10,7 +10,10 @@ the oracle disagrees with something the pages or mathematics fix:
 * brute force by sorting (top-k, group-limited top-k, stable permutation);
 * a grouped (per-expert batched) re-formulation of the expert path;
 * invariants: weight sums, count sums, NaN-poisoned unused experts,
-  token-permutation equivariance, linearity in w2, dropped slots, aux limits.
+  token-permutation equivariance, linearity in w2, dropped slots, aux limits;
+* for the backward: torch fp64 autograd through a forward written here with
+  library ops, the forward oracle's own o rows, exact scaling in dY, zero
+  gradients for unused experts and dropped slots.
 
 tests/test_oracle_mutants.py compiles deliberately broken copies of the oracle
 and checks that every one of them fails at least one pin.
@@ -351,6 +354,205 @@ def pin_dropped_slots(orc):
     w0[3, 1] = 0.0
     ref = orc.expert_forward(x, idx, w0, w1, w2)
     np.testing.assert_allclose(y, ref, rtol=1e-13, atol=1e-13)
+
+
+# --------------------------------------------------------------------------- backward
+
+def _torch_expert_forward(x, idx, w, w1, w2):
+    """Grouped expert forward in torch fp64, differentiable in x, w, w1 and w2."""
+    T, H = x.shape
+    E, twoI, _ = w1.shape
+    I = twoI // 2
+    k = idx.shape[1]
+    flat = idx.reshape(-1).long()
+    y = torch.zeros((T, H), dtype=torch.float64)
+    for e in range(E):
+        slots = torch.nonzero(flat == e).flatten()
+        if slots.numel() == 0:
+            continue
+        toks = slots // k
+        he = x[toks] @ w1[e].T
+        ae = torch.nn.functional.silu(he[:, :I]) * he[:, I:]
+        oe = ae @ w2[e].T
+        y = y.index_add(0, toks, oe * w.reshape(-1)[slots].unsqueeze(1))
+    return y
+
+
+def _leaf(t):
+    return t.detach().double().clone().requires_grad_(True)
+
+
+def pin_backward_autograd_expert(orc):
+    """dX, dW1, dW2 and d(routing weight) equal torch autograd of <dY, y>."""
+    x, w1, w2, idx, w = _problem(20, E=7)
+    idx = idx % 6                                   # expert 6 unused
+    gen = torch.Generator().manual_seed(21)
+    dy = _rand_bf16(gen, x.shape)
+    xd, w1d, w2d, wd = _leaf(x), _leaf(w1), _leaf(w2), _leaf(w)
+    y = _torch_expert_forward(xd, idx, wd, w1d, w2d)
+    (y * dy.double()).sum().backward()
+    b = orc.expert_backward(x, idx, w, w1, w2, dy)
+    np.testing.assert_allclose(b.dx, xd.grad.numpy(), rtol=1e-10, atol=1e-12)
+    np.testing.assert_allclose(b.dw1, w1d.grad.numpy(), rtol=1e-10, atol=1e-12)
+    np.testing.assert_allclose(b.dw2, w2d.grad.numpy(), rtol=1e-10, atol=1e-12)
+    np.testing.assert_allclose(b.dtopk_w, wd.grad.numpy(), rtol=1e-10, atol=1e-12)
+    assert not b.dw1[6].any() and not b.dw2[6].any()
+
+
+def pin_backward_routing_weight_is_o_dot_dy(orc):
+    """y is linear in each routing weight: its gradient is <dY_t, o_slot> of the forward."""
+    x, w1, w2, idx, w = _problem(22)
+    dy = _rand_bf16(torch.Generator().manual_seed(23), x.shape)
+    _, _, o = orc.expert_forward(x, idx, w, w1, w2, want_o=True)
+    b = orc.expert_backward(x, idx, w, w1, w2, dy, want_dw=False)
+    T, k = idx.shape
+    want = np.einsum("tkh,th->tk", o.reshape(T, k, -1), dy.double().numpy())
+    np.testing.assert_allclose(b.dtopk_w, want, rtol=1e-10, atol=1e-12)
+
+
+def pin_backward_scaling_and_drops(orc):
+    """Doubling dY doubles every gradient exactly; dropped slots give nothing."""
+    x, w1, w2, idx, w = _problem(24)
+    dy = _rand_bf16(torch.Generator().manual_seed(25), x.shape)
+    b1 = orc.expert_backward(x, idx, w, w1, w2, dy)
+    b2 = orc.expert_backward(x, idx, w, w1, w2, dy * 2)
+    for f in ("dx", "dw1", "dw2", "dtopk_w"):
+        np.testing.assert_array_equal(getattr(b2, f), 2 * getattr(b1, f))
+    bad = idx.clone()
+    bad[1, 0] = -1
+    bad[5, 2] = w1.shape[0]
+    w0 = w.clone()
+    w0[1, 0] = 0.0
+    w0[5, 2] = 0.0
+    bd = orc.expert_backward(x, bad, w, w1, w2, dy)
+    b0 = orc.expert_backward(x, idx, w0, w1, w2, dy)
+    assert bd.dtopk_w[1, 0] == 0.0 and bd.dtopk_w[5, 2] == 0.0
+    for f in ("dx", "dw1", "dw2"):
+        np.testing.assert_allclose(getattr(bd, f), getattr(b0, f), rtol=1e-13, atol=1e-13)
+
+
+def _torch_router_weights(xd, wrd, off, idx, score, normalize, scale):
+    logits = xd @ wrd.T
+    if off is not None:
+        logits = logits + torch.as_tensor(off, dtype=torch.float64)
+    logits.retain_grad()
+    s = torch.softmax(logits, dim=1) if score == "softmax" else torch.sigmoid(logits)
+    chosen = torch.gather(s, 1, idx.long())
+    if normalize:
+        chosen = chosen / chosen.sum(dim=1, keepdim=True)
+    return logits, chosen * scale
+
+
+def pin_backward_autograd_router(orc):
+    """Logit, dX and dW_r gradients of the routing weights equal torch autograd.
+
+    The selection is held fixed (it is piecewise constant); the selection bias
+    and the group limit steer it but must not enter the gradient.
+    """
+    gen = torch.Generator().manual_seed(26)
+    T, H, E, k = 20, 24, 16, 4
+    x = _rand_bf16(gen, (T, H))
+    w_r = torch.randn((E, H), generator=gen, dtype=torch.float32) * 0.3
+    off = (torch.randn((E,), generator=gen, dtype=torch.float32) * 0.5).numpy()
+    bias = (torch.randn((E,), generator=gen, dtype=torch.float32) * 0.05).numpy()
+    for score, normalize, scale in (("softmax", True, 2.5), ("softmax", False, 1.75),
+                                    ("sigmoid", True, 2.5), ("sigmoid", False, 1.75)):
+        r = orc.router(x, w_r, k, score=score, normalize=normalize, scale=scale, n_group=4,
+                       topk_group=2, group_topn=2, logit_offset=off, sel_bias=bias)
+        idx = torch.as_tensor(r.topk_idx)
+        dtw = torch.randn((T, k), generator=gen, dtype=torch.float64)
+        xd, wrd = _leaf(x), _leaf(w_r)
+        logits, wt = _torch_router_weights(xd, wrd, off, idx, score, normalize, scale)
+        np.testing.assert_allclose(r.topk_w, wt.detach().numpy(), rtol=1e-12, atol=1e-14)
+        (wt * dtw).sum().backward()
+        b = orc.router_backward(x, w_r, r.topk_idx, r.topk_w, dtw.numpy(), score=score,
+                                normalize=normalize, scale=scale, logit_offset=off)
+        np.testing.assert_allclose(b.dlogits, logits.grad.numpy(), rtol=1e-10, atol=1e-13)
+        np.testing.assert_allclose(b.dx_add, xd.grad.numpy(), rtol=1e-10, atol=1e-13)
+        np.testing.assert_allclose(b.dw_r, wrd.grad.numpy(), rtol=1e-10, atol=1e-13)
+
+
+def _grid_bf16(gen, shape, step=1.0 / 64, lim=1.5):
+    """bf16 values on a grid of ``step`` (exact in bf16, so v +- step is too)."""
+    v = torch.round(torch.randn(shape, generator=gen, dtype=torch.float64) * 0.6 / step) * step
+    return v.clamp(-lim, lim).to(torch.bfloat16)
+
+
+def pin_backward_finite_difference(orc):
+    """Central differences of the forward oracle match the backward's gradients.
+
+    Perturbations stay on the bf16 grid, so the forward sees them exactly; y is
+    linear in w2 and in the routing weights, quadratic-plus in x and w1.
+    """
+    gen = torch.Generator().manual_seed(27)
+    T, H, I, E, k = 3, 8, 4, 2, 2
+    x = _grid_bf16(gen, (T, H))
+    w1 = _grid_bf16(gen, (E, 2 * I, H))
+    w2 = _grid_bf16(gen, (E, H, I))
+    idx = torch.tensor([[0, 1], [1, 0], [1, 1]], dtype=torch.int32)
+    w = torch.rand((T, k), generator=gen, dtype=torch.float64) + 0.2
+    dy = _grid_bf16(gen, (T, H))
+    dyd = dy.double().numpy()
+    b = orc.expert_backward(x, idx, w, w1, w2, dy)
+    d = 1.0 / 64
+
+    def loss(xx=x, ww1=w1, ww2=w2, ww=w):
+        return float((orc.expert_forward(xx, idx, ww, ww1, ww2) * dyd).sum())
+
+    def central(name, tensor, pos, grad):
+        plus, minus = tensor.clone(), tensor.clone()
+        plus[pos] = float(tensor[pos]) + d
+        minus[pos] = float(tensor[pos]) - d
+        fd = (loss(**{name: plus}) - loss(**{name: minus})) / (2 * d)
+        assert abs(fd - grad) <= 2e-3 * max(1.0, abs(grad)), (name, pos, fd, grad)
+
+    for pos in [(0, 0), (1, 5), (2, 7)]:
+        central("xx", x, pos, b.dx[pos])
+    for pos in [(0, 0, 3), (1, 2, 0), (0, 5, 6), (1, 7, 7)]:
+        central("ww1", w1, pos, b.dw1[pos])
+    for pos in [(0, 0, 0), (1, 6, 3)]:
+        central("ww2", w2, pos, b.dw2[pos])
+    for pos in [(0, 1), (2, 0)]:
+        central("ww", w, pos, b.dtopk_w[pos])
+
+
+def pin_router_backward_finite_difference(orc):
+    """Central differences of the forward router in W_r and in the logit offsets.
+
+    fp32 steps of 2^-12 are exact on these inputs; the selection is checked to
+    stay the same on both sides of every step.
+    """
+    gen = torch.Generator().manual_seed(28)
+    T, H, E, k = 6, 8, 8, 3
+    x = _grid_bf16(gen, (T, H))
+    w_r = (torch.randn((E, H), generator=gen, dtype=torch.float32) * 0.5).numpy()
+    off = (torch.randn((E,), generator=gen, dtype=torch.float32) * 0.5).numpy()
+    dtw = torch.randn((T, k), generator=gen, dtype=torch.float64).numpy()
+    d = 2.0 ** -12
+    for score, normalize, scale in (("softmax", True, 2.0), ("sigmoid", True, 2.5),
+                                    ("softmax", False, 1.0), ("sigmoid", False, 1.5)):
+        kw = dict(score=score, normalize=normalize, scale=scale)
+        r = orc.router(x, w_r, k, logit_offset=off, **kw)
+        b = orc.router_backward(x, w_r, r.topk_idx, r.topk_w, dtw, logit_offset=off, **kw)
+
+        def loss(wr, of):
+            rr = orc.router(x, wr, k, logit_offset=of, **kw)
+            assert (rr.topk_idx == r.topk_idx).all(), "selection moved under the step"
+            return float((rr.topk_w * dtw).sum())
+
+        for e in range(E):
+            op, om = off.copy(), off.copy()
+            op[e] += d
+            om[e] -= d
+            fd = (loss(w_r, op) - loss(w_r, om)) / (2 * d)
+            want = b.dlogits[:, e].sum()
+            assert abs(fd - want) <= 1e-5 * max(1.0, abs(want)), (score, normalize, e, fd, want)
+        for e, h in [(0, 0), (3, 5), (7, 7)]:
+            wp, wm = w_r.copy(), w_r.copy()
+            wp[e, h] += d
+            wm[e, h] -= d
+            fd = (loss(wp, off) - loss(wm, off)) / (2 * d)
+            assert abs(fd - b.dw_r[e, h]) <= 1e-5 * max(1.0, abs(b.dw_r[e, h])), (e, h, fd)
 
 
 ALL_PINS = [v for n, v in sorted(globals().items()) if n.startswith("pin_") and callable(v)]

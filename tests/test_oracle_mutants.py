@@ -12,11 +12,13 @@ import oracle
 import oracle_pins
 
 MUTANTS = {
-    "silu_dropped": ("a[i] = silu(g) * u;", "a[i] = g * u;"),
-    "gate_up_swapped": ("a[i] = silu(g) * u;", "a[i] = silu(u) * g;"),
+    "silu_dropped": ("a[i] = silu(gi) * ui;", "a[i] = gi * ui;"),
+    "gate_up_swapped": ("a[i] = silu(gi) * ui;", "a[i] = silu(ui) * gi;"),
     "silu_sign": ("return z / (1.0 + exp(-z));", "return z / (1.0 + exp(z));"),
-    "w2_transposed": ("bf16_value(W2[h * I + i])", "bf16_value(W2[i * H + h])"),
-    "up_rows_offset": ("W1[(I + i) * H + h]", "W1[(I + i - 1 + (i == 0)) * H + h]"),
+    "w2_transposed": ("acc += bf16_value(W2[h * I + i]) * a[i];",
+                      "acc += bf16_value(W2[i * H + h]) * a[i];"),
+    "up_rows_offset": ("ui += bf16_value(W1[(I + i) * H + h]) * xt[h];",
+                       "ui += bf16_value(W1[(I + i - 1 + (i == 0)) * H + h]) * xt[h];"),
     "combine_unweighted": ("yt[h] += w * o[h];", "yt[h] += o[h];"),
     "normalize_dropped": ("if (normalize) w_out[j] /= chosen_sum;", ";"),
     "scale_dropped": ("w_out[j] *= scale;", ";"),
@@ -39,6 +41,30 @@ MUTANTS = {
                           "if (e < 0 || e >= E) { e = (e < 0) ? 0 : E - 1; } if (0) {\n                        if (a_slot)"),
     "router_weight_transposed": ("bf16_value(x_t[h]) * (double)w_r[e * H + h]",
                                  "bf16_value(x_t[h]) * (double)w_r[h * E + e]"),
+    # backward
+    "bwd_dsilu_as_sigmoid": ("const double dsilu = sg * (1.0 + g[i] * (1.0 - sg));",
+                             "const double dsilu = sg;"),
+    "bwd_dU_without_silu": ("const double dU = dA[i] * silu(g[i]);",
+                            "const double dU = dA[i] * g[i];"),
+    "bwd_dA_w2_transposed": ("acc += bf16_value(W2[h * I + i]) * dO[h];",
+                             "acc += bf16_value(W2[i * H + h]) * dO[h];"),
+    "bwd_dO_unweighted": ("dO[h] = w * dyt[h];", "dO[h] = dyt[h];"),
+    "bwd_dx_gate_up_swapped": (
+        "bf16_value(W1[i * H + h]) * dG + bf16_value(W1[(I + i) * H + h]) * dU",
+        "bf16_value(W1[i * H + h]) * dU + bf16_value(W1[(I + i) * H + h]) * dG"),
+    "bwd_dw2_a_reversed": ("DW2[h * I + i] += d * a_s[slot * I + i];",
+                           "DW2[h * I + i] += d * a_s[slot * I + (I - 1 - i)];"),
+    "bwd_dw1_wrong_token": ("const int64_t t = slot / k;", "const int64_t t = slot % T;"),
+    "bwd_dtopk_weighted": ("dwt += dyt[h] * o[h];", "dwt += w * dyt[h] * o[h];"),
+    "rbwd_softmax_norm_no_scale": ("(w[j] / scale) * sum_wdw", "w[j] * sum_wdw"),
+    "rbwd_sigmoid_deriv_dropped": ("si * (1.0 - si) / S", "si / S"),
+    "rbwd_softmax_plain_cross_dropped": ("dlt[e] = -scale * s[e] * sum_sdw;", "dlt[e] = 0.0;"),
+    "rbwd_sigmoid_plain_no_scale": ("dlt[K[j]] += scale * si * (1.0 - si) * dw[j];",
+                                    "dlt[K[j]] += si * (1.0 - si) * dw[j];"),
+    "rbwd_dx_wr_transposed": ("acc += dlt[e] * (double)w_r[e * H + h];",
+                              "acc += dlt[e] * (double)w_r[h * E + e];"),
+    "rbwd_dwr_wrong_token": ("acc += dl[t * E + e] * bf16_value(x[t * H + h]);",
+                             "acc += dl[t * E + e] * bf16_value(x[((t + 1) % T) * H + h]);"),
 }
 
 
