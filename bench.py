@@ -1,5 +1,7 @@
 """Benchmark of the MoE expert path (router -> routing metadata -> stage 1 ->
-stage 2) through the C ABI of libmoe on one or more GPUs of one node.
+stage 2, and for the training workload the backward: stage 2 data / weight,
+router, stage 1 data / weight) through the C ABI of libmoe on one or more GPUs
+of one node.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
                     [--impl ours|reference] [--no-cpu-baseline]
@@ -38,8 +40,8 @@ L2_FLUSH_BYTES = 256 << 20
 # of `bench.py --workload <name> --steps 2 --warmup 1 --no-cpu-baseline`
 # (summaries under profiles/). Reported only while the kernel sources still
 # hash to the value recorded with the capture; otherwise traffic is null.
-KERNEL_SOURCES = ("moe_expert_router_gb300/csrc/grouped_gemm.cu", "moe_expert_router_gb300/csrc/ptx.cuh",
-                  "moe_expert_router_gb300/csrc/internal.cuh")
+KERNEL_SOURCES = ("moe_expert_router_gb300/csrc/gemm_kernel.cuh", "moe_expert_router_gb300/csrc/grouped_gemm.cu",
+                  "moe_expert_router_gb300/csrc/ptx.cuh", "moe_expert_router_gb300/csrc/internal.cuh")
 STAGE1_TRAFFIC = {
     # profiles/tc_gemm_mid_ncu.md: 804.77 MB read + 59.73 MB written
     "mid": {"src": "a7f446c52efcace7", "bytes": 864.5e6},
@@ -141,16 +143,42 @@ class ClockSampler:
 # ---------------------------------------------------------------- our arm
 
 def bytes_and_flops(cfg, counts):
-    """Algorithmic flops and bytes per stage (bytes the kernels could avoid are not counted)."""
+    """Algorithmic flops and bytes of each GEMM stage (bytes the kernels could avoid
+    are not counted), keyed by the stage name used for the step's events."""
     R, H, I, T, E = cfg.R, cfg.H, cfg.I, cfg.T, cfg.E
     active = int((counts > 0).sum())
-    return {
+    st = {
         "gemm1": {"flops": 4.0 * R * H * I,
-                  "bytes": 4.0 * H * I * active + 2.0 * T * H + 2.0 * R * I},
-        "gemm2": {"flops": 2.0 * R * H * I,
-                  "bytes": 2.0 * H * I * active + 2.0 * R * I + 2.0 * T * H},
-        "active_experts": active,
+                  "bytes": 4.0 * H * I * active + 2.0 * T * H + 2.0 * R * I * (3 if cfg.backward else 1),
+                  "kernel": "tc_gemm_kernel<kStage1%s> (stage 1: fused x row gather + GEMM1 + SwiGLU)"
+                            % ("SaveH" if cfg.backward else "")},
+        "gemm2_combine": {"flops": 2.0 * R * H * I,
+                          "bytes": 2.0 * H * I * active + 2.0 * R * I + 2.0 * T * H,
+                          "kernel": "tc_gemm_kernel<kStage2> + combine_kernel (stage 2)"},
     }
+    if cfg.backward:
+        st["bwd_stage2_data"] = {
+            "flops": 2.0 * R * H * I,
+            "bytes": 2.0 * H * I * active + 2.0 * T * H + 4.0 * R * I + 4.0 * R * I + 2.0 * R * I,
+            "kernel": "tc_gemm_kernel<kBwdDA> (+ zero_tail_rows, dtw_reduce): dA + SwiGLU backward"}
+        st["bwd_stage2_weight"] = {
+            "flops": 2.0 * R * H * I,
+            "bytes": 2.0 * T * H + 2.0 * R * I + 2.0 * E * H * I,
+            "kernel": "tc_gemm_kernel<kBwdDW2>: dW2"}
+        st["bwd_stage1_data"] = {
+            "flops": 4.0 * R * H * I,
+            "bytes": 4.0 * R * I + 4.0 * H * I * active + 4.0 * R * H + 2.0 * T * H,
+            "kernel": "tc_gemm_kernel<kBwdDX> + combine_bwd_kernel: dX"}
+        st["bwd_stage1_weight"] = {
+            "flops": 4.0 * R * H * I,
+            "bytes": 4.0 * R * I + 2.0 * T * H + 4.0 * E * H * I,
+            "kernel": "tc_gemm_kernel<kBwdDW1>: dW1"}
+    return {"stages": st, "active_experts": active}
+
+
+def step_flops(cfg):
+    """Expert-path flops of one step: 6 R H I forward, + 12 R H I with the backward."""
+    return cfg.expert_flops() * (3.0 if cfg.backward else 1.0)
 
 
 def run_ours(args, cfg, rank, world, local_rank):
@@ -162,7 +190,8 @@ def run_ours(args, cfg, rank, world, local_rank):
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
     inp = generate(cfg, seed=rank, device=dev)
-    shp = B.shape(cfg.T, cfg.H, cfg.I, cfg.E, cfg.k)
+    train = cfg.backward
+    shp = B.shape(cfg.T, cfg.H, cfg.I, cfg.E, cfg.k, training=train)
     ws = B.new_workspace(shp, dev)
     rcfg = B.router_cfg(cfg.score, cfg.normalize, cfg.scale, cfg.n_group, cfg.topk_group,
                         cfg.group_topn)
@@ -174,25 +203,50 @@ def run_ours(args, cfg, rank, world, local_rank):
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
     x_dev = inp["x"]
+    if train:
+        logits = torch.empty((cfg.T, cfg.E), dtype=torch.float32, device=dev)
+        h = torch.empty((cfg.R, 2 * cfg.I), dtype=torch.bfloat16, device=dev)
+        dy_dev = inp["dy"]
+        dx = torch.empty((cfg.T, cfg.H), dtype=torch.bfloat16, device=dev)
+        dw1 = torch.empty_like(inp["w1"])
+        dw2 = torch.empty_like(inp["w2"])
+        dwr = torch.empty_like(inp["w_r"])
+        dtw = torch.empty((cfg.T, cfg.k), dtype=torch.float32, device=dev)
 
     names = ["router", "metadata", "gemm1", "gemm2_combine"]
+    if train:
+        names += ["bwd_stage2_data", "bwd_stage2_weight", "router_bwd", "bwd_stage1_data",
+                  "bwd_stage1_weight"]
+
+    def calls(x_in, dy_in):
+        """The step's C-ABI calls in order (one per event interval)."""
+        if train:
+            yield lambda: B.moe_router_train(x_in, inp["w_r"], shp, rcfg, idx, w, logits, ws, aux=aux,
+                                             logit_offset=inp["logit_offset"], sel_bias=inp["sel_bias"])
+        else:
+            yield lambda: B.moe_router(x_in, inp["w_r"], shp, rcfg, idx, w, ws, aux=aux,
+                                       logit_offset=inp["logit_offset"], sel_bias=inp["sel_bias"])
+        yield lambda: B.moe_routing_metadata(idx, shp, ws)
+        if train:
+            yield lambda: B.moe_dispatch_gemm1_train(x_in, inp["w1"], shp, a, h, ws)
+        else:
+            yield lambda: B.moe_dispatch_gemm1(x_in, inp["w1"], shp, a, ws)
+        yield lambda: B.moe_swiglu_gemm2_combine(a, w, inp["w2"], shp, y, ws)
+        if train:
+            yield lambda: B.moe_backward_stage2_data(dy_in, w, inp["w2"], h, shp, ws, dtopk_w=dtw)
+            yield lambda: B.moe_backward_stage2_weight(dy_in, shp, dw2, ws)
+            yield lambda: B.moe_router_backward(x_in, logits, idx, w, dtw, shp, rcfg, dwr, ws)
+            yield lambda: B.moe_backward_stage1_data(inp["w1"], shp, dx, ws, w_r=inp["w_r"], topk_idx=idx,
+                                                     cfg=rcfg)
+            yield lambda: B.moe_backward_stage1_weight(x_in, shp, dw1, ws)
 
     def step(ev=None):
+        for j, call in enumerate(calls(x_dev, inp["dy"] if train else None)):
+            if ev is not None:
+                ev[j].record(stream)
+            call()
         if ev is not None:
-            ev[0].record(stream)
-        B.moe_router(x_dev, inp["w_r"], shp, rcfg, idx, w, ws, aux=aux,
-                     logit_offset=inp["logit_offset"], sel_bias=inp["sel_bias"])
-        if ev is not None:
-            ev[1].record(stream)
-        B.moe_routing_metadata(idx, shp, ws)
-        if ev is not None:
-            ev[2].record(stream)
-        B.moe_dispatch_gemm1(x_dev, inp["w1"], shp, a, ws)
-        if ev is not None:
-            ev[3].record(stream)
-        B.moe_swiglu_gemm2_combine(a, w, inp["w2"], shp, y, ws)
-        if ev is not None:
-            ev[4].record(stream)
+            ev[len(names)].record(stream)
 
     for _ in range(args.warmup):
         flush.fill_(1)
@@ -202,7 +256,7 @@ def run_ours(args, cfg, rank, world, local_rank):
     if err:
         raise RuntimeError(f"device error word {err:#x} after warm-up")
 
-    events = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    events = [[torch.cuda.Event(enable_timing=True) for _ in range(len(names) + 1)] for _ in range(args.steps)]
     sampler = ClockSampler(local_rank) if rank == 0 else None
     if sampler:
         sampler.start()
@@ -230,7 +284,7 @@ def run_ours(args, cfg, rank, world, local_rank):
     for ev in events:
         for j, n in enumerate(names):
             stage_ms[n].append(ev[j].elapsed_time(ev[j + 1]))
-        step_ms.append(ev[0].elapsed_time(ev[4]))
+        step_ms.append(ev[0].elapsed_time(ev[len(names)]))
     total_ms = sum(step_ms)
 
     # metadata for the algorithmic byte counts
@@ -238,21 +292,27 @@ def run_ours(args, cfg, rank, world, local_rank):
     counts = ws[L.counts:L.counts + 4 * cfg.E].view(torch.int32).cpu()
     bf = bytes_and_flops(cfg, counts)
 
-    # end to end: host x in, host y (+ aux) out, copies inside the timed region
+    # end to end: host x (and dY) in, host y + aux (and dX) out, copies inside the
+    # timed region; weight gradients stay on the device for the optimizer
     x_host = inp["x"].cpu().pin_memory()
     y_host = torch.empty((cfg.T, cfg.H), dtype=torch.bfloat16).pin_memory()
     aux_host = torch.empty((1,), dtype=torch.float32).pin_memory()
     x_e2e = torch.empty_like(x_dev)
+    if train:
+        dy_host = inp["dy"].cpu().pin_memory()
+        dy_e2e = torch.empty_like(inp["dy"])
+        dx_host = torch.empty((cfg.T, cfg.H), dtype=torch.bfloat16).pin_memory()
 
     def e2e_step():
         x_e2e.copy_(x_host, non_blocking=True)
-        B.moe_router(x_e2e, inp["w_r"], shp, rcfg, idx, w, ws, aux=aux,
-                     logit_offset=inp["logit_offset"], sel_bias=inp["sel_bias"])
-        B.moe_routing_metadata(idx, shp, ws)
-        B.moe_dispatch_gemm1(x_e2e, inp["w1"], shp, a, ws)
-        B.moe_swiglu_gemm2_combine(a, w, inp["w2"], shp, y, ws)
+        if train:
+            dy_e2e.copy_(dy_host, non_blocking=True)
+        for call in calls(x_e2e, dy_e2e if train else None):
+            call()
         y_host.copy_(y, non_blocking=True)
         aux_host.copy_(aux, non_blocking=True)
+        if train:
+            dx_host.copy_(dx, non_blocking=True)
 
     for _ in range(max(1, args.warmup)):
         e2e_step()
@@ -267,8 +327,8 @@ def run_ours(args, cfg, rank, world, local_rank):
         e1.record(stream)
         e1.synchronize()                 # the host reads the step's result
         e2e_ms.append(e0.elapsed_time(e1))
-    h2d = x_host.numel() * x_host.element_size()
-    d2h = y_host.numel() * y_host.element_size() + 4
+    h2d = x_host.numel() * x_host.element_size() * (2 if train else 1)
+    d2h = y_host.numel() * y_host.element_size() * (2 if train else 1) + 4
     err = B.moe_get_device_error(ws)
     if err:
         raise RuntimeError(f"device error word {err:#x} after the timed region")
@@ -281,7 +341,8 @@ def run_ours(args, cfg, rank, world, local_rank):
 # ---------------------------------------------------------------- oracle (CPU) arm
 
 def oracle_sample(cfg, n_tokens, seed=0, inputs=None):
-    """Run the oracle (router + expert path) on the first n_tokens tokens; return seconds."""
+    """Run the oracle's step (router + expert path, and for a training workload the
+    expert and router backward) on the first n_tokens tokens; return seconds."""
     import oracle
     inp = inputs if inputs is not None else cpu_inputs(cfg, seed)
     x = inp["x"][:n_tokens]
@@ -291,7 +352,15 @@ def oracle_sample(cfg, n_tokens, seed=0, inputs=None):
                       group_topn=cfg.group_topn, logit_offset=inp["logit_offset"],
                       sel_bias=inp["sel_bias"])
     oracle.expert_forward(x, r.topk_idx, r.topk_w, inp["w1"], inp["w2"])
+    if cfg.backward:
+        b = oracle.expert_backward(x, r.topk_idx, r.topk_w, inp["w1"], inp["w2"], inp["dy"][:n_tokens])
+        oracle.router_backward(x, inp["w_r"], r.topk_idx, r.topk_w, b.dtopk_w, score=cfg.score,
+                               normalize=cfg.normalize, scale=cfg.scale, logit_offset=inp["logit_offset"])
     return time.perf_counter() - t0
+
+
+def sample_flops(cfg, n_tokens):
+    return step_flops(cfg) * n_tokens / cfg.T
 
 
 _CPU_INPUTS = {}
@@ -315,11 +384,11 @@ def cpu_baseline(cfg, budget_s=15.0):
     t_cal = oracle_sample(cfg, n_cal, inputs=inp)
     n = int(max(1, min(cfg.T, n_cal * budget_s / max(t_cal, 1e-6))))
     t = oracle_sample(cfg, n, inputs=inp) if n != n_cal else t_cal
-    flops = 6.0 * n * cfg.k * cfg.H * cfg.I
+    flops = sample_flops(cfg, n)
+    what = "forward and backward" if cfg.backward else "router + expert path"
     return {"value": flops / t / 1e12, "unit": "TFLOP/s", "cores": oracle.num_threads(),
             "kind": "oracle", "tokens_per_s": n / t,
-            "sample": f"first {n} of {cfg.T} tokens of the '{cfg.name}' workload: fp64 router + "
-                      f"expert path, {t:.2f} s"}
+            "sample": f"first {n} of {cfg.T} tokens of the '{cfg.name}' workload: fp64 {what}, {t:.2f} s"}
 
 
 def run_reference(args, cfg):
@@ -334,7 +403,7 @@ def run_reference(args, cfg):
         oracle_sample(cfg, n, inputs=inp)
     times = [oracle_sample(cfg, n, inputs=inp) for _ in range(args.steps)]
     tot = sum(times)
-    flops = 6.0 * n * cfg.k * cfg.H * cfg.I * args.steps
+    flops = sample_flops(cfg, n) * args.steps
     value = flops / tot / 1e12
     return {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": 1,
@@ -344,7 +413,8 @@ def run_reference(args, cfg):
         "config": config_dict(cfg, args),
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": oracle.num_threads(),
                          "kind": "oracle",
-                         "sample": f"each step: first {n} of {cfg.T} tokens, fp64 router + expert path"},
+                         "sample": f"each step: first {n} of {cfg.T} tokens, fp64 "
+                                   f"{'forward and backward' if cfg.backward else 'router + expert path'}"},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
 
@@ -400,15 +470,15 @@ def main():
 
     if rank == 0:
         peaks = measured_peaks()
-        flops_step = cfg.expert_flops()
+        flops_step = step_flops(cfg)
         value = whole_job_throughput(flops_step, args.steps, world, total_ms) / 1e12
         tokens_per_s = whole_job_throughput(cfg.T, args.steps, world, total_ms)
-        # dominant kernel of the step and its roofline
+        # dominant GEMM stage of the step and its roofline
         stage_avg = {n: sum(v) / len(v) for n, v in res["stage_ms"].items()}
         bf = res["bf"]
-        dom = max(("gemm1", "gemm2"), key=lambda n: stage_avg["gemm1" if n == "gemm1" else "gemm2_combine"])
-        dom_ms = stage_avg["gemm1"] if dom == "gemm1" else stage_avg["gemm2_combine"]
-        f, b = bf[dom]["flops"], bf[dom]["bytes"]
+        dom = max(bf["stages"], key=lambda n: stage_avg[n])
+        dom_ms = stage_avg[dom]
+        f, b = bf["stages"][dom]["flops"], bf["stages"][dom]["bytes"]
         t_tc = f / (peaks["bf16_tflops"] * 1e12)
         t_hbm = b / (peaks["hbm_gbs"] * 1e9)
         if t_tc >= t_hbm:
@@ -421,8 +491,8 @@ def main():
         rec = STAGE1_TRAFFIC.get(cfg.name)
         roof["traffic"] = rec["bytes"] if (dom == "gemm1" and rec and rec["src"] == kernel_source_hash()) else None
         roof["algorithmic_bytes"] = b
-        roof["kernel"] = ("tc_gemm_kernel<kStage1> (stage 1: fused x row gather + GEMM1 + SwiGLU)"
-                          if dom == "gemm1" else "tc_gemm_kernel<kStage2> + combine_kernel (stage 2)")
+        roof["kernel"] = bf["stages"][dom]["kernel"]
+        roof["stage"] = dom
         roof["peak_kind"] = f"{peaks['source']} burst"
         roof["kernel_ms"] = dom_ms
         out = {

@@ -28,6 +28,10 @@
  *     routing metadata and intermediates. Zero its first 256 bytes once before
  *     first use (moe_workspace_init). Calls that share a workspace must be
  *     ordered on one stream; stages read what earlier stages left there.
+ *   - Training: a shape with flags = MOE_SHAPE_TRAINING sizes the workspace
+ *     for the backward as well. The backward entry points read the routing
+ *     metadata the forward left in the workspace, so a training step runs its
+ *     forward and backward on one workspace, in order, on one stream.
  */
 #ifndef MOE_GB300_MOE_H
 #define MOE_GB300_MOE_H
@@ -58,8 +62,11 @@ typedef struct moe_shape {
     int64_t I;   /* expert intermediate size (w1 has 2I rows per expert) */
     int64_t E;   /* experts */
     int32_t k;   /* experts per token */
-    int32_t reserved;  /* must be 0 */
+    int32_t flags;  /* 0, or MOE_SHAPE_TRAINING */
 } moe_shape_t;
+
+/* moe_shape_t.flags: the workspace also holds the backward's intermediates. */
+#define MOE_SHAPE_TRAINING 0x1
 
 #define MOE_SCORE_SOFTMAX 0
 #define MOE_SCORE_SIGMOID 1
@@ -84,7 +91,13 @@ typedef struct moe_ws_layout {
     size_t meta;       /* int32 [ceil(T*k/4096), E] per-chunk expert histograms (scratch) */
     size_t router;     /* router scratch: fp32 split-K partial logits [s,T,E], bf16 split of w_r [3,E,H], sums, counts */
     size_t a;          /* bf16 [T*k, I] SwiGLU activations (moe_forward only) */
-    size_t obuf;       /* bf16 [T*k, H] weighted expert outputs in routed-row order */
+    size_t obuf;       /* bf16 [T*k, H] weighted expert outputs in routed-row order;
+                          the backward's dX rows (unweighted, routed order) reuse it */
+    /* training workspaces only (flags = MOE_SHAPE_TRAINING), else equal to total: */
+    size_t dh;         /* bf16 [T*k, 2I] gradient of h = [gate | up], routed order */
+    size_t aw;         /* bf16 [T*k, I] routing weight times a, routed order */
+    size_t dtw_part;   /* fp32 [ceil(I/256), T*k] partial routing-weight gradients */
+    size_t dlogits;    /* fp32 [T, E] gradient of the router logits */
     size_t total;      /* == moe_workspace_size */
 } moe_ws_layout_t;
 
@@ -199,6 +212,107 @@ moe_status_t moe_swiglu_gemm2_combine(const void *a, const float *topk_w, const 
 moe_status_t moe_forward(const void *x, const int32_t *topk_idx, const float *topk_w,
                          const void *w1, const void *w2, const moe_shape_t *shape, void *y,
                          void *ws, size_t ws_bytes, void *stream);
+
+/* ------------------------------------------------------------------ training
+ *
+ * The backward of the expert path and the router (MegaMoE guide, section
+ * "Design: two stages": stage 2's backward yields dW2, then stage 1's backward
+ * yields dW1). The loss gradient enters as dY bf16 [T,H]. All GEMMs accumulate
+ * in fp32; gradients of bf16 tensors are written in bf16. The selection (top-k,
+ * groups, selection bias) passes no gradient; the aux value is not
+ * differentiated. All calls below need a workspace sized with
+ * flags = MOE_SHAPE_TRAINING.
+ */
+
+/*
+ * moe_router with the fp32 logits l[t,e] (logit_offset included, selection
+ * bias not) also written to `logits` [T,E], for moe_router_backward.
+ */
+moe_status_t moe_router_train(const void *x, const float *w_r, const float *logit_offset,
+                              const float *sel_bias, const moe_shape_t *shape,
+                              const moe_router_cfg_t *cfg, int32_t *topk_idx, float *topk_w,
+                              float *aux, float *logits, void *ws, size_t ws_bytes, void *stream);
+
+/*
+ * moe_dispatch_gemm1 that also stores the pre-activation h [T*k, 2I] bf16 in
+ * routed order (columns [0,I) the gate, [I,2I) the up projection), which the
+ * backward's SwiGLU needs. h is caller-owned and must be kept until
+ * moe_backward_stage2_data has run.
+ */
+moe_status_t moe_dispatch_gemm1_train(const void *x, const void *w1, const moe_shape_t *shape,
+                                      void *a, void *h, void *ws, size_t ws_bytes, void *stream);
+
+/*
+ * Stage 2 backward, data part (grouped_gemm_combine and the SwiGLU):
+ *
+ *   for routed row r of expert e, token t, slot s, weight w = topk_w[s]:
+ *     dA_u[r,:] = dY[t,:] . w2[e]                      (I values)
+ *     dtopk_w[s] = sum_i dA_u[r,i] a[r,i]              (= <dY[t], o[r]>)
+ *     dA = w dA_u;  dU = dA silu(g);  dG = dA u silu'(g)   with [g | u] = h[r]
+ *
+ * dy bf16 [T,H]; topk_w fp32 [T,k]; w2 bf16 [E,H,I]; h from
+ * moe_dispatch_gemm1_train; dtopk_w fp32 [T,k] (output, 0 for dropped slots)
+ * or NULL. dH = [dG | dU] and w a stay in the workspace for the other
+ * backward calls.
+ */
+moe_status_t moe_backward_stage2_data(const void *dy, const float *topk_w, const void *w2, const void *h,
+                                      const moe_shape_t *shape, float *dtopk_w, void *ws, size_t ws_bytes,
+                                      void *stream);
+
+/*
+ * Stage 2 backward, weight part: dW2[e] = sum over e's rows of dY[t]^T (w a)[r]
+ * into dw2 bf16 [E,H,I] (every expert written; experts without rows get 0).
+ * Needs moe_backward_stage2_data on this workspace.
+ */
+moe_status_t moe_backward_stage2_weight(const void *dy, const moe_shape_t *shape, void *dw2, void *ws,
+                                        size_t ws_bytes, void *stream);
+
+/*
+ * Router backward: the logit gradient from dtopk_w (softmax or sigmoid,
+ * normalised over the chosen experts or not, times scale), kept in the
+ * workspace for moe_backward_stage1_data's dX term, and
+ *   dW_r[e,:] = sum_t dl[t,e] x[t,:]   (fp32 [E,H], output).
+ * logits from moe_router_train; topk_idx, topk_w from the same router call.
+ */
+moe_status_t moe_router_backward(const void *x, const float *logits, const int32_t *topk_idx,
+                                 const float *topk_w, const float *dtopk_w, const moe_shape_t *shape,
+                                 const moe_router_cfg_t *cfg, float *dw_r, void *ws, size_t ws_bytes,
+                                 void *stream);
+
+/*
+ * Stage 1 backward, data part (dispatch_grouped_gemm):
+ *
+ *   dX[t,:] = sum over t's slots of dH[r,:] . w1[e]  (+ sum_e dl[t,e] w_r[e,:]
+ *             when w_r is not NULL: the router's term, from moe_router_backward)
+ *
+ * w1 bf16 [E,2I,H]; w_r fp32 [E,H] or NULL; with w_r, topk_idx and cfg are
+ * those of the router call (they tell which logit gradients can be non-zero);
+ * dx bf16 [T,H] is the output: a sum of rows rounded to bf16 per slot plus the
+ * fp32 router term, rounded to bf16 once. Needs moe_backward_stage2_data (and,
+ * with w_r, moe_router_backward) on this workspace.
+ */
+moe_status_t moe_backward_stage1_data(const void *w1, const float *w_r, const int32_t *topk_idx,
+                                      const moe_router_cfg_t *cfg, const moe_shape_t *shape, void *dx,
+                                      void *ws, size_t ws_bytes, void *stream);
+
+/*
+ * Stage 1 backward, weight part: dW1[e] = sum over e's rows of dH[r]^T x[t]
+ * into dw1 bf16 [E,2I,H] (every expert written; experts without rows get 0).
+ * x bf16 [T,H]. Needs moe_backward_stage2_data on this workspace.
+ */
+moe_status_t moe_backward_stage1_weight(const void *x, const moe_shape_t *shape, void *dw1, void *ws,
+                                        size_t ws_bytes, void *stream);
+
+/*
+ * The whole backward, in the guide's order: stage 2 (data, weight), the router
+ * (skipped when w_r is NULL; then dw_r is not written and logits may be NULL),
+ * stage 1 (data, weight). dtopk_w may be NULL when w_r is NULL.
+ */
+moe_status_t moe_backward(const void *x, const float *w_r, const float *logits,
+                          const int32_t *topk_idx, const float *topk_w, const void *w1,
+                          const void *w2, const void *h, const void *dy, const moe_shape_t *shape,
+                          const moe_router_cfg_t *cfg, void *dx, void *dw1, void *dw2, float *dw_r,
+                          float *dtopk_w, void *ws, size_t ws_bytes, void *stream);
 
 /*
  * Wait for `stream`, then read and clear the workspace error word into *code.

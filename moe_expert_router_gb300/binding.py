@@ -23,6 +23,7 @@ DEVERR_BAD_EXPERT_INDEX = 0x1
 DEVERR_WAIT_TIMEOUT = 0x2
 SCORE_SOFTMAX = 0
 SCORE_SIGMOID = 1
+SHAPE_TRAINING = 0x1
 
 
 class MoEError(RuntimeError):
@@ -33,7 +34,7 @@ class MoEError(RuntimeError):
 
 class Shape(ctypes.Structure):
     _fields_ = [("T", ctypes.c_int64), ("H", ctypes.c_int64), ("I", ctypes.c_int64),
-                ("E", ctypes.c_int64), ("k", ctypes.c_int32), ("reserved", ctypes.c_int32)]
+                ("E", ctypes.c_int64), ("k", ctypes.c_int32), ("flags", ctypes.c_int32)]
 
 
 class RouterCfg(ctypes.Structure):
@@ -45,7 +46,7 @@ class RouterCfg(ctypes.Structure):
 class WsLayout(ctypes.Structure):
     _fields_ = [(n, ctypes.c_size_t) for n in
                 ("err", "counts", "offsets", "mt_prefix", "perm_slot", "row_of", "meta", "router", "a",
-                 "obuf", "total")]
+                 "obuf", "dh", "aw", "dtw_part", "dlogits", "total")]
 
 
 # name -> argument types (all return moe_status_t unless listed in _RESTYPES)
@@ -62,6 +63,18 @@ _SIG = {
     "moe_dispatch_gemm1": [_P, _P, ctypes.POINTER(Shape), _P, _P, ctypes.c_size_t, _P],
     "moe_swiglu_gemm2_combine": [_P, _P, _P, ctypes.POINTER(Shape), _P, _P, ctypes.c_size_t, _P],
     "moe_forward": [_P, _P, _P, _P, _P, ctypes.POINTER(Shape), _P, _P, ctypes.c_size_t, _P],
+    "moe_router_train": [_P, _P, _P, _P, ctypes.POINTER(Shape), ctypes.POINTER(RouterCfg), _P, _P,
+                         _P, _P, _P, ctypes.c_size_t, _P],
+    "moe_dispatch_gemm1_train": [_P, _P, ctypes.POINTER(Shape), _P, _P, _P, ctypes.c_size_t, _P],
+    "moe_backward_stage2_data": [_P, _P, _P, _P, ctypes.POINTER(Shape), _P, _P, ctypes.c_size_t, _P],
+    "moe_backward_stage2_weight": [_P, ctypes.POINTER(Shape), _P, _P, ctypes.c_size_t, _P],
+    "moe_router_backward": [_P, _P, _P, _P, _P, ctypes.POINTER(Shape), ctypes.POINTER(RouterCfg), _P,
+                            _P, ctypes.c_size_t, _P],
+    "moe_backward_stage1_data": [_P, _P, _P, ctypes.POINTER(RouterCfg), ctypes.POINTER(Shape), _P, _P,
+                                 ctypes.c_size_t, _P],
+    "moe_backward_stage1_weight": [_P, ctypes.POINTER(Shape), _P, _P, ctypes.c_size_t, _P],
+    "moe_backward": [_P, _P, _P, _P, _P, _P, _P, _P, _P, ctypes.POINTER(Shape),
+                     ctypes.POINTER(RouterCfg), _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P],
     "moe_get_device_error": [_P, ctypes.POINTER(ctypes.c_int32), _P],
     "moe_status_string": [ctypes.c_int],
     "moe_kernel_launch_count": [],
@@ -111,8 +124,8 @@ def _stream(stream, like):
     return ctypes.c_void_p(stream.cuda_stream)
 
 
-def shape(T, H, I, E, k) -> Shape:
-    return Shape(int(T), int(H), int(I), int(E), int(k), 0)
+def shape(T, H, I, E, k, training=False) -> Shape:
+    return Shape(int(T), int(H), int(I), int(E), int(k), SHAPE_TRAINING if training else 0)
 
 
 def router_cfg(score="softmax", normalize=True, scale=1.0, n_group=1, topk_group=1,
@@ -178,6 +191,66 @@ def moe_forward(x, topk_idx, topk_w, w1, w2, shp, y, ws, stream=None):
     _check("moe_forward", load().moe_forward(
         _ptr(x), _ptr(topk_idx), _ptr(topk_w), _ptr(w1), _ptr(w2), ctypes.byref(shp), _ptr(y),
         _ptr(ws), ws.numel() * ws.element_size(), _stream(stream, x)))
+
+
+def _cfg_ref(cfg):
+    return None if cfg is None else ctypes.byref(cfg)
+
+
+def _nbytes(ws):
+    return ws.numel() * ws.element_size()
+
+
+def moe_router_train(x, w_r, shp, cfg, topk_idx, topk_w, logits, ws, aux=None, logit_offset=None,
+                     sel_bias=None, stream=None):
+    """moe_router that also writes the fp32 logits [T, E] for moe_router_backward."""
+    _check("moe_router_train", load().moe_router_train(
+        _ptr(x), _ptr(w_r), _ptr(logit_offset), _ptr(sel_bias), ctypes.byref(shp),
+        ctypes.byref(cfg), _ptr(topk_idx), _ptr(topk_w), _ptr(aux), _ptr(logits), _ptr(ws),
+        _nbytes(ws), _stream(stream, x)))
+
+
+def moe_dispatch_gemm1_train(x, w1, shp, a, h, ws, stream=None):
+    """moe_dispatch_gemm1 that also stores the pre-activation h [T*k, 2I] (routed order)."""
+    _check("moe_dispatch_gemm1_train", load().moe_dispatch_gemm1_train(
+        _ptr(x), _ptr(w1), ctypes.byref(shp), _ptr(a), _ptr(h), _ptr(ws), _nbytes(ws),
+        _stream(stream, x)))
+
+
+def moe_backward_stage2_data(dy, topk_w, w2, h, shp, ws, dtopk_w=None, stream=None):
+    _check("moe_backward_stage2_data", load().moe_backward_stage2_data(
+        _ptr(dy), _ptr(topk_w), _ptr(w2), _ptr(h), ctypes.byref(shp), _ptr(dtopk_w), _ptr(ws),
+        _nbytes(ws), _stream(stream, ws)))
+
+
+def moe_backward_stage2_weight(dy, shp, dw2, ws, stream=None):
+    _check("moe_backward_stage2_weight", load().moe_backward_stage2_weight(
+        _ptr(dy), ctypes.byref(shp), _ptr(dw2), _ptr(ws), _nbytes(ws), _stream(stream, ws)))
+
+
+def moe_router_backward(x, logits, topk_idx, topk_w, dtopk_w, shp, cfg, dw_r, ws, stream=None):
+    _check("moe_router_backward", load().moe_router_backward(
+        _ptr(x), _ptr(logits), _ptr(topk_idx), _ptr(topk_w), _ptr(dtopk_w), ctypes.byref(shp),
+        ctypes.byref(cfg), _ptr(dw_r), _ptr(ws), _nbytes(ws), _stream(stream, ws)))
+
+
+def moe_backward_stage1_data(w1, shp, dx, ws, w_r=None, topk_idx=None, cfg=None, stream=None):
+    _check("moe_backward_stage1_data", load().moe_backward_stage1_data(
+        _ptr(w1), _ptr(w_r), _ptr(topk_idx), _cfg_ref(cfg), ctypes.byref(shp), _ptr(dx), _ptr(ws),
+        _nbytes(ws), _stream(stream, ws)))
+
+
+def moe_backward_stage1_weight(x, shp, dw1, ws, stream=None):
+    _check("moe_backward_stage1_weight", load().moe_backward_stage1_weight(
+        _ptr(x), ctypes.byref(shp), _ptr(dw1), _ptr(ws), _nbytes(ws), _stream(stream, ws)))
+
+
+def moe_backward(x, topk_idx, topk_w, w1, w2, h, dy, shp, dx, dw1, dw2, ws, w_r=None, logits=None,
+                 cfg=None, dw_r=None, dtopk_w=None, stream=None):
+    _check("moe_backward", load().moe_backward(
+        _ptr(x), _ptr(w_r), _ptr(logits), _ptr(topk_idx), _ptr(topk_w), _ptr(w1), _ptr(w2), _ptr(h),
+        _ptr(dy), ctypes.byref(shp), _cfg_ref(cfg), _ptr(dx), _ptr(dw1), _ptr(dw2), _ptr(dw_r),
+        _ptr(dtopk_w), _ptr(ws), _nbytes(ws), _stream(stream, ws)))
 
 
 def moe_get_device_error(ws, stream=None) -> int:

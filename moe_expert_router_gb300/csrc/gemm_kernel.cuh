@@ -1,0 +1,950 @@
+// gemm_kernel.cuh -- the persistent tcgen05 grouped-GEMM kernel template of the
+// MegaMoE expert path on sm_103a, shared by the forward (grouped_gemm.cu) and
+// the backward (grouped_gemm_bwd.cu) translation units.
+//
+// Forward modes (MegaMoE guide, opening section; section "Design: two stages"):
+//   kStage1  dispatch_grouped_gemm: for routed row r of expert e,
+//            h = x[token(r)] . w1[e]^T, a[r] = silu(h[:I]) * h[I:] (SwiGLU
+//            silu(x_glu) * x_linear, "GDN <-> FLA Parity in Primus" page,
+//            section B). Dedicated warps gather the routed x rows straight into
+//            the shared-memory A tiles. kStage1SaveH also stores h (gate and
+//            up halves, bf16) for the backward.
+//   kStage2  grouped_gemm_combine: o[r] = a[r] . w2[e]^T, scaled by the slot's
+//            routing weight and stored to row r of obuf (combined afterwards).
+//   kRouter  partial fp32 logits of x . w_r^T with w_r split exactly into three
+//            bf16 matrices (Henry, Tang and Heinecke 2019, "Leveraging the
+//            bfloat16 artificial intelligence datatype for higher-precision
+//            computations"); split-K partials are summed in a fixed order later.
+//
+// Backward modes (the guide's stage order: stage 2's backward yields dW2, then
+// stage 1's yields dW1; everything else is the chain rule of the forward):
+//   kBwdDA   dA_u[r] = dY[token(r)] . w2[e] (dY rows gathered like x in stage 1,
+//            w2[e] read MN-major). The epilogue applies the SwiGLU backward with
+//            the saved h: dA = w dA_u, dU = dA silu(g), dG = dA u silu'(g), and
+//            stores dH = [dG | dU], the weighted activations w a (for dW2) and
+//            per-tile partial sums of dA_u . a (the routing-weight gradient).
+//   kBwdDX   dXr[r] = dH[r] . w1[e] (w1[e] read MN-major), unweighted rows in
+//            routed order, summed per token afterwards.
+//   kBwdDW2  dW2[e] = sum over e's rows of dY[token(r)]^T (w a)[r]: M = H,
+//            N = I, K = the expert's rows; dY rows gathered MN-major.
+//   kBwdDW1  dW1[e] = sum over e's rows of dH[r]^T x[token(r)]: M = 2I, N = H,
+//            K = the expert's rows; x rows gathered MN-major.
+//
+// Kernel design (one CTA per SM, persistent):
+//   work unit  = (expert e, n-tile, 256-row tile of e's routed rows) for the
+//                row-grouped modes, (256-row tile, n-tile, k split) for the
+//                router, (expert e, 256-row m-tile, n-tile) for the weight
+//                gradients. The 256 rows are two 128-row halves that share every
+//                B tile; an empty second half is neither loaded nor multiplied.
+//                Units are numbered expert-major, so CTAs running side by side
+//                share each expert's operands through L2; CTAs take the next
+//                unit from a global counter.
+//   warp 0     = scheduler + TMA producer: claims units, publishes them to an
+//                in-CTA queue and fills a ring of swizzled tiles (per stage two
+//                128-row A halves and one 256-row B tile).
+//   warp 1     = TMEM allocator and single-thread tcgen05.mma issuer: per
+//                16-deep k-step one M=128 N=256 MMA per half into two fp32
+//                TMEM accumulators (all 512 columns).
+//   warps 2-9  = epilogue, one TMEM lane quadrant of one half each.
+//   warps 10-13 (gathering modes) = cp.async row gathers into the A or B tiles.
+// Operands are K-major (rows of K contiguous, 128- or 64-byte swizzle) or
+// MN-major (K rows of 64-element, 128-byte swizzled MN atoms; the atoms of one
+// tile are BK * 128 bytes apart, 8-row K groups 1024 bytes apart).
+// Row counts are read from device memory, so ragged routing never needs a
+// host sync or a re-launch.
+#pragma once
+
+#include "internal.cuh"
+#include "ptx.cuh"
+
+namespace moe {
+
+namespace {
+
+constexpr int BM = kBM;                      // rows per MMA / per accumulator
+constexpr int UM = kUnitM;                   // rows per work unit (two halves)
+constexpr int BK = kBK;
+constexpr int BN = kBN;
+constexpr int UMMA_K = 16;
+constexpr int ROW_BYTES = BK * 2;            // bytes of one K-major tile row per stage
+constexpr int STAGES = (BK == 64) ? 3 : 6;
+constexpr int A_HALF_BYTES = BM * BK * 2;    // 16 KB (BK 64) or 8 KB (BK 32)
+constexpr int A_BYTES = 2 * A_HALF_BYTES;    // 32 KB
+constexpr int B_BYTES = BN * BK * 2;         // 32 KB or 16 KB
+constexpr int MN_ATOM_BYTES = BK * 128;      // one 64-wide MN atom over the stage's BK rows
+constexpr int TMEM_COLS = 2 * BN;            // two accumulators: all 512 columns
+constexpr int EPI_WARPS = 8;
+constexpr int EPI_THREADS = EPI_WARPS * 32;
+constexpr int GATHER_WARPS = 4;
+constexpr int GATHER_THREADS = GATHER_WARPS * 32;
+constexpr int UQ = 4;                        // depth of the in-CTA unit queue
+constexpr uint64_t kDrainLimitNs = 10000000ull;  // 10 ms
+
+enum Mode : int {
+    kStage1 = 0, kStage2 = 1, kRouter = 2,
+    kBwdDA = 3, kBwdDX = 4, kBwdDW2 = 5, kBwdDW1 = 6,
+    kStage1SaveH = 7            // stage 1 that also stores h for the backward
+};
+
+template <int MODE> constexpr bool kIsStage1 = MODE == kStage1 || MODE == kStage1SaveH;
+// A is filled by the K-major row gather (token rows of x or dY)
+template <int MODE> constexpr bool kGatherK = kIsStage1<MODE> || MODE == kBwdDA;
+// the MN-major row gather fills A (dW2: dY rows) or B (dW1: x rows)
+template <int MODE> constexpr bool kGatherMnA = MODE == kBwdDW2;
+template <int MODE> constexpr bool kGatherMnB = MODE == kBwdDW1;
+template <int MODE> constexpr bool kGathers = kGatherK<MODE> || kGatherMnA<MODE> || kGatherMnB<MODE>;
+template <int MODE> constexpr bool kAMn = MODE == kBwdDW2 || MODE == kBwdDW1;
+template <int MODE> constexpr bool kBMn = MODE >= kBwdDA && MODE <= kBwdDW1;
+template <int MODE> constexpr bool kWeightGrad = MODE == kBwdDW2 || MODE == kBwdDW1;
+
+// warps: 0 scheduler + TMA producer, 1 MMA issuer, 2..9 epilogue, 10..13 gather
+template <int MODE>
+constexpr int kNumThreads = 64 + EPI_THREADS + (kGathers<MODE> ? GATHER_THREADS : 0);
+
+template <int MODE>
+constexpr uint32_t kIdesc = idesc_bf16_f32(BM, BN) | (kAMn<MODE> ? (1u << 15) : 0u) |
+                            (kBMn<MODE> ? (1u << 16) : 0u);
+
+struct __align__(1024) Smem {
+    uint8_t a[STAGES][A_BYTES];
+    uint8_t b[STAGES][B_BYTES];
+    uint8_t stage_out[EPI_WARPS][32 * 128];  // per epilogue warp: one 32 x 64 or two 32 x 32 bf16 boxes
+    uint64_t full[STAGES];
+    uint64_t empty[STAGES];
+    uint64_t acc_full;
+    uint64_t acc_empty;
+    uint64_t uq_full[UQ];
+    uint64_t uq_empty[UQ];
+    uint64_t drain;
+    int unit_q[UQ];
+    uint32_t tmem_base;
+    int abort;
+};
+
+constexpr size_t SMEM_BYTES = sizeof(Smem) + 1024;  // + slack to align the base to 1024
+
+// Tensor maps of one launch (unused ones are copies of a used one).
+struct GemmMaps {
+    CUtensorMap a;     // A operand (TMA-loaded modes)
+    CUtensorMap b;     // B operand
+    CUtensorMap out;   // primary output
+    CUtensorMap out2;  // kStage1SaveH: h gate half; dA: dH up half
+    CUtensorMap out3;  // kStage1SaveH: h up half;   dA: w a
+};
+
+struct GemmArgs {
+    const int32_t *counts;
+    const int32_t *offsets;
+    const int32_t *mt_prefix;
+    const int32_t *perm_slot;
+    const __nv_bfloat16 *src;   // gathered token rows [T, src_cols]: x or dY
+    const __nv_bfloat16 *h;     // dA: saved pre-activation [R, 2I]
+    int32_t *err;
+    int32_t *sched;             // [0] next unit, [1] CTAs finished
+    const float *topk_w;
+    __nv_bfloat16 *out;         // masked direct stores of partial row slabs
+    __nv_bfloat16 *out2, *out3; // kStage1SaveH: h gate / up halves; dA: dH up half, w a
+    float *logits_part;         // router
+    float *dtw_part;            // dA: [n_tiles, R] partial routing-weight gradients
+    int E, k, K;
+    int src_cols;               // valid columns of a gathered source row
+    int n_out;                  // valid output columns
+    int n_tiles;                // n-tiles per expert (grouped) or per row tile (router)
+    int m_total, m_tiles;       // weight gradients: output rows per expert, 256-row tiles
+    int b_rows;                 // weight rows per expert (stage 1: 2I)
+    int half;                   // stage 1: row offset of the up projection (= I); dA: I
+    int out_ld;                 // row stride (elements) of out / out2 / out3
+    int R;                      // routed rows
+    int T, splits, kb_per_split, kb_total, kb_h;   // router
+    int total_units;            // router / weight gradients: known on the host; else -1
+};
+
+struct Unit {
+    int e, n, row0, rows, kb0, kb1, split;
+    int koff, kcount;           // weight gradients: the expert's routed rows
+};
+
+template <int MODE>
+__device__ __forceinline__ Unit decode_unit(int u, const GemmArgs &g) {
+    Unit t;
+    t.koff = 0;
+    t.kcount = 0;
+    if constexpr (MODE == kRouter) {
+        const int per_m = g.n_tiles * g.splits;
+        const int m = u / per_m;
+        const int rem = u - m * per_m;
+        t.n = rem / g.splits;
+        t.split = rem - t.n * g.splits;
+        t.e = 0;
+        t.row0 = m * UM;
+        t.rows = min(UM, g.T - t.row0);
+        t.kb0 = t.split * g.kb_per_split;
+        t.kb1 = min(g.kb_total, t.kb0 + g.kb_per_split);
+    } else if constexpr (kWeightGrad<MODE>) {
+        const int per_e = g.m_tiles * g.n_tiles;
+        t.e = u / per_e;
+        const int rem = u - t.e * per_e;
+        const int m = rem / g.n_tiles;
+        t.n = rem - m * g.n_tiles;
+        t.row0 = m * UM;
+        t.rows = min(UM, g.m_total - t.row0);
+        t.koff = g.offsets[t.e];
+        t.kcount = g.counts[t.e];
+        t.kb0 = 0;
+        t.kb1 = (t.kcount + BK - 1) / BK;
+        t.split = 0;
+    } else {
+        // units of expert e are [mt_prefix[e] * n_tiles, mt_prefix[e+1] * n_tiles)
+        int lo = 0, hi = g.E;
+        while (hi - lo > 1) {
+            const int mid = (lo + hi) >> 1;
+            if (g.mt_prefix[mid] * g.n_tiles <= u) lo = mid; else hi = mid;
+        }
+        const int mt0 = g.mt_prefix[lo];
+        const int mt_e = g.mt_prefix[lo + 1] - mt0;
+        const int local = u - mt0 * g.n_tiles;
+        t.e = lo;
+        t.n = local / mt_e;
+        const int m = local - t.n * mt_e;
+        t.row0 = g.offsets[lo] + m * UM;
+        t.rows = min(UM, g.counts[lo] - m * UM);
+        t.kb0 = 0;
+        t.kb1 = (g.K + BK - 1) / BK;
+        t.split = 0;
+    }
+    return t;
+}
+
+// Descriptor of an MN-major bf16 operand: 64-element (128-byte) swizzled MN
+// atoms MN_ATOM_BYTES apart (leading byte offset), 8-row K groups 1024 bytes
+// apart (stride byte offset), version 1, 128-byte swizzle.
+__device__ __forceinline__ uint64_t smem_desc_mn(uint32_t saddr) {
+    uint64_t d = 0;
+    d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+    d |= static_cast<uint64_t>(MN_ATOM_BYTES >> 4) << 16;
+    d |= static_cast<uint64_t>(1024 >> 4) << 32;
+    d |= static_cast<uint64_t>(1) << 46;
+    d |= static_cast<uint64_t>(2) << 61;
+    return d;
+}
+
+template <bool MN>
+__device__ __forceinline__ uint64_t operand_desc(uint32_t base, int kk) {
+    if constexpr (MN) return smem_desc_mn(base + kk * UMMA_K * 128);
+    else return smem_desc_swizzled<ROW_BYTES>(base + kk * UMMA_K * 2);
+}
+
+// Wait that ignores the abort flag and sets no error: used only to let
+// in-flight copies or MMAs finish before an aborting CTA exits.
+__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
+    const uint64_t t0 = globaltimer_ns();
+    while (!mbar_try_wait(bar, parity)) {
+        if (globaltimer_ns() - t0 > kDrainLimitNs) return;
+    }
+}
+
+// silu(g) * u with the fast exponential and division intrinsics (a few
+// instructions instead of an IEEE division); their error (a few ulp of fp32)
+// is far below the bf16 rounding of the result. For g < -88 the quotient
+// flushes to 0, which is the bf16 value of silu there anyway.
+__device__ __forceinline__ float silu_mul(float g, float u) {
+    return __fdividef(g, 1.0f + __expf(-g)) * u;
+}
+
+__device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xffff0000u); }
+
+// Write 16 packed words (32 bf16 of one row) into a 32 x 32 box staged with the
+// 64-byte swizzle (what a TMA store of a 64-byte-wide box expects).
+__device__ __forceinline__ void stage_row32(uint32_t buf, int lane, const uint32_t (&pk)[16]) {
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+        st_shared_v4(buf + swizzled_chunk<64>(lane, j), pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+}
+
+// Masked direct store of 32 bf16 columns of one row (partial row slabs).
+__device__ __forceinline__ void store_row32(__nv_bfloat16 *dst, int cols_left, const uint32_t (&pk)[16]) {
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+        if (j * 8 < cols_left)
+            *reinterpret_cast<uint4 *>(dst + j * 8) = make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+}
+
+// ---------------------------------------------------------------- epilogue pieces
+
+// Stage 1: the SwiGLU of accumulator columns [c, c+32) (gate) and
+// [BN/2 + c, ...) (up), packed to bf16.
+__device__ __forceinline__ void swiglu_piece(uint32_t tacc, int c, uint32_t (&pk)[16]) {
+    uint32_t gv[32], uv[32];
+    tmem_ld32(tacc + c, gv);
+    tmem_ld32(tacc + BN / 2 + c, uv);
+    tmem_wait_ld();
+    tmem_reg_fence(gv);
+    tmem_reg_fence(uv);
+#pragma unroll
+    for (int i = 0; i < 16; ++i)
+        pk[i] = pack_bf16x2(silu_mul(__uint_as_float(gv[2 * i]), __uint_as_float(uv[2 * i])),
+                            silu_mul(__uint_as_float(gv[2 * i + 1]), __uint_as_float(uv[2 * i + 1])));
+}
+
+// 32 accumulator columns [c, c+32) scaled by w, packed to bf16.
+__device__ __forceinline__ void scaled_piece(uint32_t tacc, int c, float w, uint32_t (&pk)[16]) {
+    uint32_t v[32];
+    tmem_ld32(tacc + c, v);
+    tmem_wait_ld();
+    tmem_reg_fence(v);
+#pragma unroll
+    for (int i = 0; i < 16; ++i)
+        pk[i] = pack_bf16x2(w * __uint_as_float(v[2 * i]), w * __uint_as_float(v[2 * i + 1]));
+}
+
+// ---------------------------------------------------------------- the kernel
+
+template <int MODE>
+__global__ void __launch_bounds__(kNumThreads<MODE>, 1)
+tc_gemm_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs g) {
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_addr(smem_raw);
+    Smem &sm = *reinterpret_cast<Smem *>(smem_raw + ((1024u - (raw & 1023u)) & 1023u));
+    volatile int *abort_flag = &sm.abort;
+    volatile int *unit_q = sm.unit_q;
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            // gathering modes: the producer's expect_tx arrival plus one per gather thread
+            mbar_init(smem_addr(&sm.full[s]), kGathers<MODE> ? 1 + GATHER_THREADS : 1);
+            mbar_init(smem_addr(&sm.empty[s]), 1);
+        }
+        mbar_init(smem_addr(&sm.acc_full), 1);
+        mbar_init(smem_addr(&sm.acc_empty), EPI_THREADS);
+        for (int s = 0; s < UQ; ++s) {
+            mbar_init(smem_addr(&sm.uq_full[s]), 1);
+            mbar_init(smem_addr(&sm.uq_empty[s]), 1 + EPI_WARPS + (kGathers<MODE> ? GATHER_WARPS : 0));
+        }
+        mbar_init(smem_addr(&sm.drain), 1);
+        sm.abort = 0;
+        fence_mbar_init();
+        tma_prefetch_desc(&maps.a);
+        tma_prefetch_desc(&maps.b);
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_addr(&sm.tmem_base), TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = sm.tmem_base;
+
+    if (warp == 0) {
+        // ------------------------------------------------ scheduler + TMA producer
+        const int total = (MODE == kRouter || kWeightGrad<MODE>) ? g.total_units : g.mt_prefix[g.E] * g.n_tiles;
+        int stage = 0, issued = 0, q = 0;
+        uint32_t phase = 0, qphase = 0;
+        bool ok = true;
+        while (true) {
+            int u = 0;
+            if (lane == 0) u = atomicAdd(&g.sched[0], 1);
+            u = __shfl_sync(0xffffffffu, u, 0);
+            const bool more = u < total;
+            bool w_ok = true;
+            if (lane == 0) {
+                w_ok = mbar_wait(smem_addr(&sm.uq_empty[q]), qphase ^ 1u, abort_flag, g.err);
+                if (w_ok) {
+                    unit_q[q] = more ? u : -1;
+                    mbar_arrive(smem_addr(&sm.uq_full[q]));
+                }
+            }
+            w_ok = __shfl_sync(0xffffffffu, w_ok, 0);
+            if (!w_ok) { ok = false; break; }
+            if (++q == UQ) { q = 0; qphase ^= 1u; }
+            if (!more) break;
+
+            const Unit t = decode_unit<MODE>(u, g);
+            const bool two = t.rows > BM;            // second half present
+            uint32_t tx_bytes;
+            if constexpr (kGatherK<MODE> || kGatherMnA<MODE>) tx_bytes = B_BYTES;    // A gathered
+            else if constexpr (kGatherMnB<MODE>) tx_bytes = two ? A_BYTES : A_HALF_BYTES;  // B gathered
+            else tx_bytes = (two ? A_BYTES : A_HALF_BYTES) + B_BYTES;
+            for (int kb = t.kb0; kb < t.kb1; ++kb) {
+                bool e_ok = true;
+                if (lane == 0) e_ok = mbar_wait(smem_addr(&sm.empty[stage]), phase ^ 1u, abort_flag, g.err);
+                e_ok = __shfl_sync(0xffffffffu, e_ok, 0);
+                if (!e_ok) { ok = false; break; }
+                const uint32_t full = smem_addr(&sm.full[stage]);
+                const uint32_t sa = smem_addr(sm.a[stage]);
+                const uint32_t sb = smem_addr(sm.b[stage]);
+                if (lane == 0) {
+                    mbar_arrive_expect_tx(full, tx_bytes);
+                    if constexpr (kIsStage1<MODE>) {
+                        const int row = t.e * g.b_rows + t.n * (BN / 2);
+                        tma_load_2d(sb, &maps.b, kb * BK, row, full);                        // gate rows
+                        tma_load_2d(sb + B_BYTES / 2, &maps.b, kb * BK, row + g.half, full);  // up rows
+                    } else if constexpr (MODE == kStage2) {
+                        tma_load_2d(sa, &maps.a, kb * BK, t.row0, full);
+                        if (two) tma_load_2d(sa + A_HALF_BYTES, &maps.a, kb * BK, t.row0 + BM, full);
+                        tma_load_2d(sb, &maps.b, kb * BK, t.e * g.b_rows + t.n * BN, full);
+                    } else if constexpr (MODE == kRouter) {
+                        const int seg = kb / g.kb_h;              // 0: hi, 1: mid, 2: lo
+                        const int kx = (kb - seg * g.kb_h) * BK;
+                        tma_load_2d(sa, &maps.a, kx, t.row0, full);
+                        if (two) tma_load_2d(sa + A_HALF_BYTES, &maps.a, kx, t.row0 + BM, full);
+                        tma_load_2d(sb, &maps.b, kx, seg * g.E + t.n * BN, full);
+                    } else if constexpr (MODE == kBwdDA || MODE == kBwdDX) {
+                        if constexpr (MODE == kBwdDX) {
+                            tma_load_2d(sa, &maps.a, kb * BK, t.row0, full);
+                            if (two) tma_load_2d(sa + A_HALF_BYTES, &maps.a, kb * BK, t.row0 + BM, full);
+                        }
+                        // weight slab of expert e, MN-major: K rows kb*BK.., four 64-wide atoms
+#pragma unroll
+                        for (int j = 0; j < 4; ++j)
+                            tma_load_3d(sb + j * MN_ATOM_BYTES, &maps.b, t.n * BN + 64 * j, kb * BK, t.e, full);
+                    } else if constexpr (MODE == kBwdDW2) {
+#pragma unroll
+                        for (int j = 0; j < 4; ++j)
+                            tma_load_2d(sb + j * MN_ATOM_BYTES, &maps.b, t.n * BN + 64 * j, t.koff + kb * BK, full);
+                    } else {  // kBwdDW1: dH columns of the m-tile, MN-major
+                        const int na = two ? 4 : 2;
+                        for (int j = 0; j < na; ++j)
+                            tma_load_2d(sa + j * MN_ATOM_BYTES, &maps.a, t.row0 + 64 * j, t.koff + kb * BK, full);
+                    }
+                }
+                __syncwarp();
+                ++issued;
+                if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+            }
+            if (!ok) break;
+        }
+        if (!ok && lane == 0) {
+            // let the copies already issued land before the CTA exits
+            int s = stage;
+            uint32_t ph = phase;
+            for (int i = 0; i < min(issued, STAGES); ++i) {
+                if (--s < 0) { s = STAGES - 1; ph ^= 1u; }
+                drain_wait(smem_addr(&sm.full[s]), ph);
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            int stage = 0, q = 0;
+            uint32_t phase = 0, acc_phase = 0, qphase = 0;
+            bool ok = true, any = false;
+            while (true) {
+                if (!mbar_wait(smem_addr(&sm.uq_full[q]), qphase, abort_flag, g.err)) { ok = false; break; }
+                const int u = unit_q[q];
+                mbar_arrive(smem_addr(&sm.uq_empty[q]));
+                if (++q == UQ) { q = 0; qphase ^= 1u; }
+                if (u < 0) break;
+                const Unit t = decode_unit<MODE>(u, g);
+                const bool two = t.rows > BM;
+                // the epilogue must have drained both accumulators of the previous unit
+                if (!mbar_wait(smem_addr(&sm.acc_empty), acc_phase ^ 1u, abort_flag, g.err)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                for (int kb = t.kb0; kb < t.kb1; ++kb) {
+                    if (!mbar_wait(smem_addr(&sm.full[stage]), phase, abort_flag, g.err)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t sa = smem_addr(sm.a[stage]);
+                    const uint32_t sb = smem_addr(sm.b[stage]);
+#pragma unroll
+                    for (int kk = 0; kk < BK / UMMA_K; ++kk) {
+                        const uint32_t acc = (kb > t.kb0 || kk > 0) ? 1u : 0u;
+                        const uint64_t bdesc = operand_desc<kBMn<MODE>>(sb, kk);
+                        mma_bf16(tmem_base, operand_desc<kAMn<MODE>>(sa, kk), bdesc, kIdesc<MODE>, acc);
+                        if (two)
+                            mma_bf16(tmem_base + BN, operand_desc<kAMn<MODE>>(sa + A_HALF_BYTES, kk), bdesc,
+                                     kIdesc<MODE>, acc);
+                    }
+                    mma_commit(smem_addr(&sm.empty[stage]));   // frees the smem stage
+                    any = true;
+                    if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+                }
+                if (!ok) break;
+                // accumulators ready (with no k-block, at once: the epilogue then
+                // writes zeros without reading them)
+                mma_commit(smem_addr(&sm.acc_full));
+                acc_phase ^= 1u;
+            }
+            if (!ok && any) {
+                mma_commit(smem_addr(&sm.drain));
+                drain_wait(smem_addr(&sm.drain), 0);
+            }
+        }
+        __syncwarp();
+    } else if (warp < 2 + EPI_WARPS) {
+        // ------------------------------------------------ epilogue
+        const int quad = warp & 3;                  // TMEM lanes this warp may access
+        const int half = (warp - 2) >> 2;           // accumulator (row half) of this warp
+        const int row = half * BM + quad * 32 + lane;   // unit row
+        const uint32_t tacc = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) +
+                              static_cast<uint32_t>(half * BN);
+        const uint32_t buf = smem_addr(sm.stage_out[warp - 2]);
+        int q = 0;
+        uint32_t acc_phase = 0, qphase = 0;
+        while (true) {
+            bool ok = true;
+            int u = -1;
+            if (lane == 0) {
+                ok = mbar_wait(smem_addr(&sm.uq_full[q]), qphase, abort_flag, g.err);
+                if (ok) {
+                    u = unit_q[q];
+                    mbar_arrive(smem_addr(&sm.uq_empty[q]));
+                }
+            }
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            u = __shfl_sync(0xffffffffu, u, 0);
+            if (++q == UQ) { q = 0; qphase ^= 1u; }
+            if (!ok || u < 0) break;
+            const Unit t = decode_unit<MODE>(u, g);
+            const bool valid = row < t.rows;
+            float w = 1.0f;                             // routing weight of the row's slot
+            if constexpr (MODE == kStage2 || MODE == kBwdDA) {
+                w = valid ? g.topk_w[g.perm_slot[t.row0 + row]] : 0.0f;
+            }
+            if (lane == 0) ok = mbar_wait(smem_addr(&sm.acc_full), acc_phase, abort_flag, g.err);
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            if (!ok) break;
+            tc_fence_after();
+            const int slab0 = half * BM + quad * 32;    // first unit row of this warp
+            const bool full_slab = slab0 + 32 <= t.rows;
+            if (t.rows > half * BM) {                   // this half was computed
+                if constexpr (kIsStage1<MODE> || MODE == kStage2 || MODE == kBwdDX) {
+                    // row-grouped outputs: rows t.row0 + row, columns [col0, col0 + ncols)
+                    constexpr int ncols = kIsStage1<MODE> ? BN / 2 : BN;
+                    const int col0 = t.n * ncols;
+                    const int y = t.row0 + slab0;
+                    if constexpr (MODE == kStage1SaveH) {
+                        // a, h gate and h up in 32 x 32 boxes (two staging halves)
+                        const int64_t r = t.row0 + row;
+#pragma unroll 1
+                        for (int c = 0; c < ncols; c += 32) {
+                            if (col0 + c >= g.n_out) break;
+                            uint32_t gv[32], uv[32];
+                            tmem_ld32(tacc + c, gv);
+                            tmem_ld32(tacc + BN / 2 + c, uv);
+                            tmem_wait_ld();
+                            tmem_reg_fence(gv);
+                            tmem_reg_fence(uv);
+                            uint32_t pg[16], pu[16], pa[16];
+#pragma unroll
+                            for (int i = 0; i < 16; ++i) {
+                                pg[i] = pack_bf16x2(__uint_as_float(gv[2 * i]), __uint_as_float(gv[2 * i + 1]));
+                                pu[i] = pack_bf16x2(__uint_as_float(uv[2 * i]), __uint_as_float(uv[2 * i + 1]));
+                            }
+                            if (full_slab) {
+                                if (lane == 0) bulk_wait_read<0>();
+                                __syncwarp();
+                                stage_row32(buf, lane, pg);
+                                stage_row32(buf + 2048, lane, pu);
+                                fence_proxy_async_smem();
+                                __syncwarp();
+                                if (lane == 0) {
+                                    tma_store_2d(&maps.out2, buf, col0 + c, y);
+                                    tma_store_2d(&maps.out3, buf + 2048, col0 + c, y);
+                                    bulk_commit();
+                                }
+                            } else if (valid) {
+                                store_row32(g.out2 + r * g.out_ld + col0 + c, g.n_out - col0 - c, pg);
+                                store_row32(g.out3 + r * g.out_ld + col0 + c, g.n_out - col0 - c, pu);
+                            }
+#pragma unroll
+                            for (int i = 0; i < 16; ++i)
+                                pa[i] = pack_bf16x2(
+                                    silu_mul(__uint_as_float(gv[2 * i]), __uint_as_float(uv[2 * i])),
+                                    silu_mul(__uint_as_float(gv[2 * i + 1]), __uint_as_float(uv[2 * i + 1])));
+                            if (full_slab) {
+                                if (lane == 0) bulk_wait_read<0>();
+                                __syncwarp();
+                                stage_row32(buf, lane, pa);
+                                fence_proxy_async_smem();
+                                __syncwarp();
+                                if (lane == 0) {
+                                    tma_store_2d(&maps.out, buf, col0 + c, y);
+                                    bulk_commit();
+                                }
+                            } else if (valid) {
+                                store_row32(g.out + r * g.n_out + col0 + c, g.n_out - col0 - c, pa);
+                            }
+                        }
+                    } else if (full_slab) {
+                        // whole 32-row slab valid: stage 32 x 64 bf16 boxes in shared
+                        // memory (128B-swizzled) and write each with one TMA store
+#pragma unroll 1
+                        for (int cc = 0; cc < ncols; cc += 64) {
+                            if (col0 + cc >= g.n_out) break;
+                            if (lane == 0) bulk_wait_read<0>();   // previous box read out
+                            __syncwarp();
+#pragma unroll
+                            for (int p = 0; p < 2; ++p) {
+                                uint32_t pk[16];
+                                if constexpr (MODE == kStage1) swiglu_piece(tacc, cc + 32 * p, pk);
+                                else scaled_piece(tacc, cc + 32 * p, w, pk);
+#pragma unroll
+                                for (int j = 0; j < 4; ++j) {
+                                    const int c16 = p * 4 + j;
+                                    st_shared_v4(buf + lane * 128 + ((c16 ^ (lane & 7)) << 4), pk[4 * j],
+                                                 pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+                                }
+                            }
+                            fence_proxy_async_smem();
+                            __syncwarp();
+                            if (lane == 0) {
+                                tma_store_2d(&maps.out, buf, col0 + cc, y);
+                                bulk_commit();
+                            }
+                        }
+                    } else {
+                        // partial slab (the expert's last rows): masked direct stores
+                        __nv_bfloat16 *dst = g.out + static_cast<int64_t>(t.row0 + row) * g.n_out + col0;
+#pragma unroll 1
+                        for (int c = 0; c < ncols; c += 32) {
+                            if (col0 + c >= g.n_out) break;
+                            uint32_t pk[16];
+                            if constexpr (MODE == kStage1) swiglu_piece(tacc, c, pk);
+                            else scaled_piece(tacc, c, w, pk);
+                            if (valid) store_row32(dst + c, g.n_out - col0 - c, pk);
+                        }
+                    }
+                } else if constexpr (MODE == kBwdDA) {
+                    // SwiGLU backward: dG, dU (dH halves) and w a, plus sum_i dA_u a
+                    const int col0 = t.n * BN;
+                    const int y = t.row0 + slab0;
+                    const int64_t r = t.row0 + row;
+                    const __nv_bfloat16 *hrow = g.h + (valid ? r : 0) * (2 * static_cast<int64_t>(g.half));
+                    float dtw = 0.0f;
+#pragma unroll 1
+                    for (int c = 0; c < BN; c += 32) {
+                        const int col = col0 + c;
+                        if (col >= g.n_out) break;
+                        uint32_t v[32];
+                        tmem_ld32(tacc + c, v);
+                        uint32_t gw[16], uw[16];
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            uint4 gq = make_uint4(0u, 0u, 0u, 0u), uq = gq;
+                            if (valid && col + 8 * j < g.n_out) {
+                                gq = __ldg(reinterpret_cast<const uint4 *>(hrow + col + 8 * j));
+                                uq = __ldg(reinterpret_cast<const uint4 *>(hrow + g.half + col + 8 * j));
+                            }
+                            gw[4 * j] = gq.x; gw[4 * j + 1] = gq.y; gw[4 * j + 2] = gq.z; gw[4 * j + 3] = gq.w;
+                            uw[4 * j] = uq.x; uw[4 * j + 1] = uq.y; uw[4 * j + 2] = uq.z; uw[4 * j + 3] = uq.w;
+                        }
+                        tmem_wait_ld();
+                        tmem_reg_fence(v);
+                        uint32_t pdg[16], pdu[16], paw[16];
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) {
+                            float og[2], ou[2], oa[2];
+#pragma unroll
+                            for (int e2 = 0; e2 < 2; ++e2) {
+                                const float gv = e2 ? bf16_hi(gw[i]) : bf16_lo(gw[i]);
+                                const float uv = e2 ? bf16_hi(uw[i]) : bf16_lo(uw[i]);
+                                const float d = __uint_as_float(v[2 * i + e2]);
+                                const float sg = __fdividef(1.0f, 1.0f + __expf(-gv));
+                                const float silu = gv * sg;
+                                const float a = silu * uv;
+                                dtw = fmaf(d, a, dtw);
+                                const float dA = w * d;
+                                ou[e2] = dA * silu;
+                                og[e2] = dA * uv * sg * fmaf(gv, 1.0f - sg, 1.0f);
+                                oa[e2] = w * a;
+                            }
+                            pdg[i] = pack_bf16x2(og[0], og[1]);
+                            pdu[i] = pack_bf16x2(ou[0], ou[1]);
+                            paw[i] = pack_bf16x2(oa[0], oa[1]);
+                        }
+                        if (full_slab) {
+                            if (lane == 0) bulk_wait_read<0>();
+                            __syncwarp();
+                            stage_row32(buf, lane, pdg);
+                            stage_row32(buf + 2048, lane, pdu);
+                            fence_proxy_async_smem();
+                            __syncwarp();
+                            if (lane == 0) {
+                                tma_store_2d(&maps.out, buf, col, y);
+                                tma_store_2d(&maps.out2, buf + 2048, col, y);
+                                bulk_commit();
+                                bulk_wait_read<0>();
+                            }
+                            __syncwarp();
+                            stage_row32(buf, lane, paw);
+                            fence_proxy_async_smem();
+                            __syncwarp();
+                            if (lane == 0) {
+                                tma_store_2d(&maps.out3, buf, col, y);
+                                bulk_commit();
+                            }
+                        } else if (valid) {
+                            store_row32(g.out + r * g.out_ld + col, g.n_out - col, pdg);
+                            store_row32(g.out2 + r * g.out_ld + col, g.n_out - col, pdu);
+                            store_row32(g.out3 + r * g.n_out + col, g.n_out - col, paw);
+                        }
+                    }
+                    if (valid) g.dtw_part[static_cast<int64_t>(t.n) * g.R + r] = dtw;
+                } else if constexpr (kWeightGrad<MODE>) {
+                    // dW rows t.row0 + row of expert e, 32 x 64 boxes through a 3-D map
+                    // (rows past m_total and columns past n_out are clipped by the store)
+                    const int col0 = t.n * BN;
+                    const bool empty = t.kb1 == 0;      // expert without rows: zeros
+                    if (slab0 < t.rows) {
+#pragma unroll 1
+                        for (int cc = 0; cc < BN; cc += 64) {
+                            if (col0 + cc >= g.n_out) break;
+                            if (lane == 0) bulk_wait_read<0>();
+                            __syncwarp();
+#pragma unroll
+                            for (int p = 0; p < 2; ++p) {
+                                uint32_t pk[16];
+                                if (empty) {
+#pragma unroll
+                                    for (int i = 0; i < 16; ++i) pk[i] = 0u;
+                                } else {
+                                    scaled_piece(tacc, cc + 32 * p, 1.0f, pk);
+                                }
+#pragma unroll
+                                for (int j = 0; j < 4; ++j) {
+                                    const int c16 = p * 4 + j;
+                                    st_shared_v4(buf + lane * 128 + ((c16 ^ (lane & 7)) << 4), pk[4 * j],
+                                                 pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+                                }
+                            }
+                            fence_proxy_async_smem();
+                            __syncwarp();
+                            if (lane == 0) {
+                                tma_store_3d(&maps.out, buf, col0 + cc, t.row0 + slab0, t.e);
+                                bulk_commit();
+                            }
+                        }
+                    }
+                } else {
+                    const int col0 = t.n * BN;
+                    float *dst = g.logits_part +
+                                 (static_cast<int64_t>(t.split) * g.T + t.row0 + row) * g.n_out + col0;
+                    const bool vec = (g.n_out & 3) == 0;
+#pragma unroll 1
+                    for (int c = 0; c < BN; c += 32) {
+                        uint32_t v[32];
+                        tmem_ld32(tacc + c, v);
+                        tmem_wait_ld();
+                        tmem_reg_fence(v);
+                        if (valid) {
+                            if (vec) {
+#pragma unroll
+                                for (int j = 0; j < 8; ++j) {
+                                    if (col0 + c + j * 4 < g.n_out)
+                                        *reinterpret_cast<uint4 *>(dst + c + j * 4) =
+                                            make_uint4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+                                }
+                            } else {
+#pragma unroll
+                                for (int j = 0; j < 32; ++j) {
+                                    if (col0 + c + j < g.n_out) dst[c + j] = __uint_as_float(v[j]);
+                                }
+                            }
+                        }
+                    }
+                }
+            }
+            tc_fence_before();
+            mbar_arrive(smem_addr(&sm.acc_empty));
+            acc_phase ^= 1u;
+        }
+        if (lane == 0) bulk_wait<0>();                  // every output box written
+    } else {
+        // ------------------------------------------------ row gathers
+        // The dispatch of dispatch_grouped_gemm (and its backward twins): 128
+        // threads copy routed token rows straight into the 128B-swizzled tiles
+        // with 16-byte cp.async. Each thread waits for its own copies, orders them
+        // before the tensor core's async-proxy reads, then arrives on the stage's
+        // full barrier, one stage behind its issue so that two stages of copies
+        // are in flight.
+        const int gt = threadIdx.x - (64 + EPI_THREADS);
+        int stage = 0, q = 0, pending = -1;
+        uint32_t phase = 0, qphase = 0;
+        while (true) {
+            bool ok = true;
+            int u = -1;
+            if (lane == 0) {
+                ok = mbar_wait(smem_addr(&sm.uq_full[q]), qphase, abort_flag, g.err);
+                if (ok) {
+                    u = unit_q[q];
+                    mbar_arrive(smem_addr(&sm.uq_empty[q]));
+                }
+            }
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            u = __shfl_sync(0xffffffffu, u, 0);
+            if (++q == UQ) { q = 0; qphase ^= 1u; }
+            if (!ok || u < 0) break;
+            const Unit t = decode_unit<MODE>(u, g);
+            if constexpr (kGatherK<MODE>) {
+                // K-major A rows: one thread per 16-byte chunk of a row slice; rows past
+                // the unit's count are left as they are (never stored)
+                constexpr int CHUNKS = ROW_BYTES / 16;                 // per row slice
+                constexpr int RSTEP = GATHER_THREADS / CHUNKS;         // rows per pass
+                constexpr int NROWS = UM / RSTEP;                      // rows per thread
+                const int chunk = gt % CHUNKS;
+                const int rg = gt / CHUNKS;                            // rows rg + RSTEP i
+                int tok[NROWS];
+#pragma unroll
+                for (int i = 0; i < NROWS; ++i) {
+                    const int r = rg + RSTEP * i;
+                    tok[i] = (r < t.rows) ? g.perm_slot[t.row0 + r] / g.k : -1;
+                }
+                for (int kb = t.kb0; kb < t.kb1; ++kb) {
+                    bool e_ok = true;
+                    if (lane == 0) e_ok = mbar_wait(smem_addr(&sm.empty[stage]), phase ^ 1u, abort_flag, g.err);
+                    e_ok = __shfl_sync(0xffffffffu, e_ok, 0);
+                    if (!e_ok) { ok = false; break; }
+                    const int col = kb * BK + chunk * 8;
+                    const uint32_t nbytes = col < g.K ? 16u : 0u;   // zero-fill the K tail
+                    const uint32_t sa = smem_addr(sm.a[stage]);
+#pragma unroll
+                    for (int i = 0; i < NROWS; ++i) {
+                        if (tok[i] >= 0) {
+                            const int r = rg + RSTEP * i;
+                            const uint32_t dst = sa + (r >> 7) * A_HALF_BYTES +
+                                                 swizzled_chunk<ROW_BYTES>(r & (BM - 1), chunk);
+                            cp_async_16(dst, g.src + static_cast<int64_t>(tok[i]) * g.src_cols + (nbytes ? col : 0),
+                                        nbytes);
+                        }
+                    }
+                    cp_async_commit();
+                    if (pending >= 0) {
+                        cp_async_wait<1>();
+                        fence_proxy_async_smem();
+                        mbar_arrive(smem_addr(&sm.full[pending]));
+                    }
+                    pending = stage;
+                    if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+                }
+            } else if constexpr (kGatherMnA<MODE> || kGatherMnB<MODE>) {
+                // MN-major tile over the expert's routed rows (the reduction): warp w
+                // copies K rows w, w + 4, ...; lane c8 the 16-byte chunk c8 of the
+                // 256-column slice. K rows past the expert's count and columns past
+                // the source width are zero-filled, so they add nothing.
+                constexpr int NR = BK / GATHER_WARPS;
+                const int c8 = gt & 31;
+                const int kr0 = gt >> 5;
+                const int col = (kGatherMnA<MODE> ? t.row0 : t.n * BN) + c8 * 8;
+                const bool col_ok = col < g.src_cols;
+                const uint32_t chunk_off = static_cast<uint32_t>(c8 >> 3) * MN_ATOM_BYTES;
+                for (int kb = t.kb0; kb < t.kb1; ++kb) {
+                    bool e_ok = true;
+                    if (lane == 0) e_ok = mbar_wait(smem_addr(&sm.empty[stage]), phase ^ 1u, abort_flag, g.err);
+                    e_ok = __shfl_sync(0xffffffffu, e_ok, 0);
+                    if (!e_ok) { ok = false; break; }
+                    const uint32_t base = smem_addr(kGatherMnA<MODE> ? sm.a[stage] : sm.b[stage]) + chunk_off;
+#pragma unroll 4
+                    for (int i = 0; i < NR; ++i) {
+                        const int krow = kr0 + GATHER_WARPS * i;
+                        const int kk = kb * BK + krow;
+                        const bool ok_r = col_ok && kk < t.kcount;
+                        const int tok = ok_r ? g.perm_slot[t.koff + kk] / g.k : 0;
+                        cp_async_16(base + swizzled_chunk<128>(krow, c8 & 7),
+                                    g.src + static_cast<int64_t>(tok) * g.src_cols + (ok_r ? col : 0),
+                                    ok_r ? 16u : 0u);
+                    }
+                    cp_async_commit();
+                    if (pending >= 0) {
+                        cp_async_wait<1>();
+                        fence_proxy_async_smem();
+                        mbar_arrive(smem_addr(&sm.full[pending]));
+                    }
+                    pending = stage;
+                    if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+                }
+            }
+            if (pending >= 0) {                       // signal the unit's last stage
+                cp_async_wait<0>();
+                fence_proxy_async_smem();
+                mbar_arrive(smem_addr(&sm.full[pending]));
+                pending = -1;
+            }
+            if (!ok) break;
+        }
+        cp_async_wait<0>();                           // no copy in flight at exit
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, TMEM_COLS);
+    }
+    if (threadIdx.x == 0) {
+        // the last CTA to finish resets the unit counter for the next launch
+        __threadfence();
+        if (atomicAdd(&g.sched[1], 1) == static_cast<int>(gridDim.x) - 1) {
+            atomicExch(&g.sched[0], 0);
+            atomicExch(&g.sched[1], 0);
+        }
+    }
+}
+
+// Grouped-mode arguments shared by every launcher.
+inline GemmArgs grouped_args(const GemmLaunch &p) {
+    GemmArgs g{};
+    g.counts = p.counts;
+    g.offsets = p.offsets;
+    g.mt_prefix = p.mt_prefix;
+    g.perm_slot = p.perm_slot;
+    g.src = p.src;
+    g.h = p.h;
+    g.err = p.err;
+    g.sched = p.sched;
+    g.topk_w = p.topk_w;
+    g.out = p.out;
+    g.out2 = p.out2;
+    g.out3 = p.out3;
+    g.dtw_part = p.dtw_part;
+    g.E = p.E;
+    g.k = p.k;
+    g.K = p.K;
+    g.src_cols = p.src_cols;
+    g.n_out = p.n_out;
+    g.n_tiles = (p.n_out + p.n_tile - 1) / p.n_tile;
+    g.m_total = p.m_total;
+    g.m_tiles = (p.m_total + UM - 1) / UM;
+    g.b_rows = p.b_rows;
+    g.half = p.half;
+    g.out_ld = p.out_ld;
+    g.R = p.R;
+    g.total_units = -1;
+    return g;
+}
+
+inline GemmMaps maps_of(const GemmLaunch &p) {
+    GemmMaps m;
+    m.a = *(p.tm_a ? p.tm_a : p.tm_b);
+    m.b = *p.tm_b;
+    m.out = *p.tm_out;
+    m.out2 = *(p.tm_out2 ? p.tm_out2 : p.tm_out);
+    m.out3 = *(p.tm_out3 ? p.tm_out3 : p.tm_out);
+    return m;
+}
+
+template <int MODE>
+cudaError_t set_gemm_smem() {
+    return cudaFuncSetAttribute(tc_gemm_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                static_cast<int>(SMEM_BYTES));
+}
+
+template <int MODE>
+cudaError_t launch_tc_gemm(const GemmMaps &maps, const GemmArgs &g, int grid, cudaStream_t st) {
+    tc_gemm_kernel<MODE><<<grid, kNumThreads<MODE>, SMEM_BYTES, st>>>(maps, g);
+    note_launches(1);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+}  // namespace moe

@@ -105,6 +105,7 @@ struct RouterLaunch {
     int32_t *topk_idx;
     float *topk_w;
     float *aux;                 // may be null
+    float *logits;              // [T, E] saved fp32 logits for the backward, may be null
     int32_t *err;
     int num_sms;
     RouterScratch scratch;
@@ -118,19 +119,32 @@ struct MetadataLaunch {
     int32_t *ticket;
 };
 
-// One grouped GEMM launch: stage 1 (fused x row gather + SwiGLU epilogue) or stage 2
-// (weighted scatter epilogue).
+// One grouped GEMM launch (forward stages 1 and 2, backward dA / dX / dW2 / dW1).
 struct GemmLaunch {
-    const CUtensorMap *tm_a;    // host-encoded tensor maps (copied into the launch)
-    const CUtensorMap *tm_b;
-    const CUtensorMap *tm_out;  // output [R, n_out], box 64 x 32 (epilogue TMA stores)
+    const CUtensorMap *tm_a;    // host-encoded tensor maps (copied into the launch);
+    const CUtensorMap *tm_b;    // tm_a, tm_out2 and tm_out3 may be null when unused
+    const CUtensorMap *tm_out;
+    const CUtensorMap *tm_out2;
+    const CUtensorMap *tm_out3;
     const int32_t *counts, *offsets, *mt_prefix, *perm_slot;
-    const __nv_bfloat16 *x;     // stage 1: token rows gathered into the A tiles
+    const __nv_bfloat16 *src;   // token rows gathered by the kernel: x or dY [T, src_cols]
+    const __nv_bfloat16 *h;     // backward dA: saved pre-activation [R, 2I]
     int32_t *err;
-    int32_t *sched;             // [2] unit scheduler of this stage
-    const float *topk_w;        // stage 2 only
-    __nv_bfloat16 *out;         // a [R, I] (stage 1) or obuf [R, H] (stage 2), routed rows
-    int E, k, K, n_out, b_rows, half;
+    int32_t *sched;             // [2] unit scheduler of this launch
+    const float *topk_w;        // stage 2 and dA
+    __nv_bfloat16 *out;         // row-grouped output (masked stores of partial slabs)
+    __nv_bfloat16 *out2, *out3; // stage 1 with h: h gate / up halves; dA: dH up half, w a
+    float *dtw_part;            // dA: [ceil(I / 256), R]
+    int E, k;
+    int K;                      // reduction length of the row-grouped modes
+    int src_cols;               // columns of a gathered source row
+    int n_out;                  // output columns
+    int n_tile;                 // output columns per unit (128 for stage 1, else 256)
+    int m_total;                // weight gradients: output rows per expert
+    int b_rows, half;           // stage 1: 2I and I; dA: half = I
+    int out_ld;                 // row stride of out / out2 where it differs from n_out
+    int R;                      // routed rows (T * k)
+    int save_h;                 // stage 1: also store h
     int num_sms;
 };
 
@@ -159,6 +173,53 @@ cudaError_t launch_gemm2_scatter(const GemmLaunch &p, cudaStream_t st);
 cudaError_t launch_router_gemm(const RouterGemmLaunch &p, cudaStream_t st);
 cudaError_t launch_combine(const CombineLaunch &p, cudaStream_t st);
 
+// Routing-weight gradient: dtopk_w[s] = sum_n dtw_part[n, row_of[s]] (0 if dropped).
+struct DtwReduceLaunch {
+    const float *dtw_part;      // [n_part, R]
+    int n_part, R, T, k;
+    const int32_t *row_of;
+    float *dtopk_w;             // [T, k]
+};
+
+// Router backward: logit gradient, then dW_r (and the dX term in the combine).
+struct RouterBwdLaunch {
+    const float *logits;        // [T, E] fp32 logits of the forward (offset included)
+    const int32_t *topk_idx;
+    const float *topk_w, *dtopk_w;
+    int T, H, E, k, score_fn, normalize;
+    float scale;
+    float *dl;                  // [T, E] logit gradient (output)
+    const __nv_bfloat16 *x;     // [T, H]
+    const int32_t *offsets, *counts, *perm_slot;
+    float *dw_r;                // [E, H] (output)
+};
+
+// dX = sum over the token's slots of the dX rows (routed order) + dlogits . W_r.
+struct CombineBwdLaunch {
+    const __nv_bfloat16 *xbuf;  // [R, H]
+    const int32_t *row_of, *topk_idx;
+    const float *dl;            // [T, E] or null (no router term)
+    const float *w_r;           // [E, H] or null
+    int dense;                  // dl may be non-zero outside the chosen experts
+    __nv_bfloat16 *dx;
+    int T, H, E, k;
+};
+
+cudaError_t launch_dtw_reduce(const DtwReduceLaunch &p, cudaStream_t st);
+// Zero rows [*routed_rows, R) of dH [R, 2I] and w a [R, I] (rows of dropped slots).
+cudaError_t launch_zero_tail_rows(__nv_bfloat16 *dh, __nv_bfloat16 *aw, const int32_t *routed_rows, int R,
+                                  int I, cudaStream_t st);
+cudaError_t launch_router_dlogits(const RouterBwdLaunch &p, cudaStream_t st);
+cudaError_t launch_router_dwr(const RouterBwdLaunch &p, cudaStream_t st);
+cudaError_t launch_combine_bwd(const CombineBwdLaunch &p, cudaStream_t st);
+
+// Backward GEMMs (grouped_gemm_bwd.cu).
+cudaError_t launch_bwd_da(const GemmLaunch &p, cudaStream_t st);
+cudaError_t launch_bwd_dx(const GemmLaunch &p, cudaStream_t st);
+cudaError_t launch_bwd_dw2(const GemmLaunch &p, cudaStream_t st);
+cudaError_t launch_bwd_dw1(const GemmLaunch &p, cudaStream_t st);
+cudaError_t setup_bwd_gemm_kernels();
+
 // Per-device one-time kernel attribute set-up (dynamic shared memory limits).
 cudaError_t setup_metadata_kernels();
 cudaError_t setup_gemm_kernels();
@@ -168,6 +229,16 @@ cudaError_t setup_gemm_kernels();
 // or rejects the arguments.
 bool encode_bf16_2d(CUtensorMap *map, const void *base, uint64_t inner, uint64_t rows,
                     uint32_t box_inner, uint32_t box_rows);
+
+// bf16 tensor [depth, rows, inner] with a box_inner x box_rows x 1 box, zero
+// fill out of bounds, 128- or 64-byte swizzle as for encode_bf16_2d.
+bool encode_bf16_3d(CUtensorMap *map, const void *base, uint64_t inner, uint64_t rows, uint64_t depth,
+                    uint32_t box_inner, uint32_t box_rows);
+
+// bf16 2-D view with an explicit row stride (elements): a column slice of a
+// wider row-major tensor.
+bool encode_bf16_2d_strided(CUtensorMap *map, const void *base, uint64_t inner, uint64_t rows,
+                            uint64_t row_stride, uint32_t box_inner, uint32_t box_rows);
 
 // Statistics: kernels launched by this library.
 void note_launches(int n);

@@ -55,7 +55,8 @@ bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 moe_status_t check_shape(const moe_shape_t *s) {
     if (s == nullptr) return MOE_ERR_INVALID_ARG;
-    if (s->T < 0 || s->H <= 0 || s->I <= 0 || s->E <= 0 || s->k <= 0 || s->reserved != 0)
+    if (s->T < 0 || s->H <= 0 || s->I <= 0 || s->E <= 0 || s->k <= 0 ||
+        (s->flags & ~MOE_SHAPE_TRAINING) != 0)
         return MOE_ERR_INVALID_ARG;
     if (s->k > 32 || s->k > s->E || s->E > 1024) return MOE_ERR_UNSUPPORTED;
     if (s->H % 8 != 0 || s->I % 8 != 0) return MOE_ERR_UNSUPPORTED;
@@ -80,15 +81,30 @@ moe_ws_layout_t make_layout(const moe_shape_t &s) {
     L.router = off;    off = align256(off + router_scratch_bytes(T, H, E, router_splits(T, H, E)));
     L.a = off;         off = align256(off + 2 * R * I);
     L.obuf = off;      off = align256(off + 2 * R * H);
+    if (s.flags & MOE_SHAPE_TRAINING) {
+        L.dh = off;       off = align256(off + 2 * R * 2 * I);
+        L.aw = off;       off = align256(off + 2 * R * I);
+        L.dtw_part = off; off = align256(off + 4 * R * ((I + kBN - 1) / kBN));
+        L.dlogits = off;  off = align256(off + 4 * T * E);
+    } else {
+        L.dh = L.aw = L.dtw_part = L.dlogits = off;
+    }
     L.total = off;
     return L;
 }
 
+// Workspace header words (see internal.cuh for bytes 0-32).
+constexpr size_t kHdrSchedDA = 40, kHdrSchedDX = 48, kHdrSchedDW2 = 56, kHdrSchedDW1 = 64;
+
 struct Ws {
     int32_t *err, *ticket, *counts, *offsets, *mt_prefix, *perm_slot, *row_of, *sched1, *sched2;
     int32_t *meta, *meta_ticket;
+    int32_t *sched_da, *sched_dx, *sched_dw2, *sched_dw1;
     RouterScratch router;
     __nv_bfloat16 *a, *obuf;
+    __nv_bfloat16 *dh, *aw;     // training only
+    float *dtw_part, *dlogits;  // training only
+    bool training;
 };
 
 Ws carve(void *ws, const moe_shape_t &s) {
@@ -106,10 +122,19 @@ Ws carve(void *ws, const moe_shape_t &s) {
     w.meta_ticket = reinterpret_cast<int32_t *>(b + 32);
     w.sched1 = reinterpret_cast<int32_t *>(b + 8);
     w.sched2 = reinterpret_cast<int32_t *>(b + 16);
+    w.sched_da = reinterpret_cast<int32_t *>(b + kHdrSchedDA);
+    w.sched_dx = reinterpret_cast<int32_t *>(b + kHdrSchedDX);
+    w.sched_dw2 = reinterpret_cast<int32_t *>(b + kHdrSchedDW2);
+    w.sched_dw1 = reinterpret_cast<int32_t *>(b + kHdrSchedDW1);
     w.router = carve_router_scratch(b + L.router, s.T, s.H, s.E, router_splits(s.T, s.H, s.E),
                                     w.ticket, reinterpret_cast<int32_t *>(b + 24));
     w.a = reinterpret_cast<__nv_bfloat16 *>(b + L.a);
     w.obuf = reinterpret_cast<__nv_bfloat16 *>(b + L.obuf);
+    w.training = (s.flags & MOE_SHAPE_TRAINING) != 0;
+    w.dh = reinterpret_cast<__nv_bfloat16 *>(b + L.dh);
+    w.aw = reinterpret_cast<__nv_bfloat16 *>(b + L.aw);
+    w.dtw_part = reinterpret_cast<float *>(b + L.dtw_part);
+    w.dlogits = reinterpret_cast<float *>(b + L.dlogits);
     return w;
 }
 
@@ -121,34 +146,53 @@ moe_status_t check_ws(const moe_shape_t &s, const void *ws, size_t ws_bytes) {
 
 moe_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
 
-// Stage 1: tensor maps + launch (metadata must already be in ws).
-moe_status_t run_gemm1(const moe_shape_t &s, const void *x, const void *w1, void *a, const Ws &w,
-                       const DeviceState &d, cudaStream_t st) {
-    // the x rows are gathered by the kernel's own warps; only w1 goes through TMA
-    CUtensorMap tm_w1, tm_out;
-    if (!encode_bf16_2d(&tm_w1, w1, s.H, static_cast<uint64_t>(s.E) * 2 * s.I, kBK, 128) ||
-        !encode_bf16_2d(&tm_out, a, s.I, static_cast<uint64_t>(s.T) * s.k, 64, 32))
-        return MOE_ERR_CUDA;
-    GemmLaunch p;
-    p.tm_a = &tm_w1;
-    p.tm_b = &tm_w1;
-    p.tm_out = &tm_out;
-    p.x = static_cast<const __nv_bfloat16 *>(x);
+// A GemmLaunch with the metadata pointers of the workspace filled in.
+GemmLaunch base_launch(const moe_shape_t &s, const Ws &w, const DeviceState &d) {
+    GemmLaunch p{};
     p.counts = w.counts;
     p.offsets = w.offsets;
     p.mt_prefix = w.mt_prefix;
     p.perm_slot = w.perm_slot;
     p.err = w.err;
-    p.sched = w.sched1;
-    p.topk_w = nullptr;
-    p.out = static_cast<__nv_bfloat16 *>(a);
     p.E = static_cast<int>(s.E);
     p.k = s.k;
+    p.R = static_cast<int>(s.T * s.k);
+    p.num_sms = d.num_sms;
+    return p;
+}
+
+// Stage 1: tensor maps + launch (metadata must already be in ws). With h, the
+// pre-activation is stored too (a, h gate and h up in 32 x 32 boxes).
+moe_status_t run_gemm1(const moe_shape_t &s, const void *x, const void *w1, void *a, void *h, const Ws &w,
+                       const DeviceState &d, cudaStream_t st) {
+    // the x rows are gathered by the kernel's own warps; only w1 goes through TMA
+    const uint64_t R = static_cast<uint64_t>(s.T) * s.k;
+    CUtensorMap tm_w1, tm_out, tm_hg, tm_hu;
+    const uint32_t box = h ? 32 : 64;
+    if (!encode_bf16_2d(&tm_w1, w1, s.H, static_cast<uint64_t>(s.E) * 2 * s.I, kBK, 128) ||
+        !encode_bf16_2d(&tm_out, a, s.I, R, box, 32))
+        return MOE_ERR_CUDA;
+    if (h && (!encode_bf16_2d_strided(&tm_hg, h, s.I, R, 2 * s.I, 32, 32) ||
+              !encode_bf16_2d_strided(&tm_hu, static_cast<__nv_bfloat16 *>(h) + s.I, s.I, R, 2 * s.I, 32, 32)))
+        return MOE_ERR_CUDA;
+    GemmLaunch p = base_launch(s, w, d);
+    p.tm_b = &tm_w1;
+    p.tm_out = &tm_out;
+    p.tm_out2 = h ? &tm_hg : nullptr;
+    p.tm_out3 = h ? &tm_hu : nullptr;
+    p.src = static_cast<const __nv_bfloat16 *>(x);
+    p.sched = w.sched1;
+    p.out = static_cast<__nv_bfloat16 *>(a);
+    p.out2 = static_cast<__nv_bfloat16 *>(h);
+    p.out3 = h ? static_cast<__nv_bfloat16 *>(h) + s.I : nullptr;
     p.K = static_cast<int>(s.H);
+    p.src_cols = static_cast<int>(s.H);
     p.n_out = static_cast<int>(s.I);
+    p.n_tile = kBN / 2;
     p.b_rows = static_cast<int>(2 * s.I);
     p.half = static_cast<int>(s.I);
-    p.num_sms = d.num_sms;
+    p.out_ld = static_cast<int>(2 * s.I);
+    p.save_h = h != nullptr;
     return cuda_status(launch_gemm1_swiglu(p, st));
 }
 
@@ -161,26 +205,17 @@ moe_status_t run_gemm2(const moe_shape_t &s, const void *a, const float *topk_w,
     if (!encode_bf16_2d(&tm_w2, w2, s.I, static_cast<uint64_t>(s.E) * s.H, kBK, 256))
         return MOE_ERR_CUDA;
     if (!encode_bf16_2d(&tm_out, w.obuf, s.H, R, 64, 32)) return MOE_ERR_CUDA;
-    GemmLaunch p;
+    GemmLaunch p = base_launch(s, w, d);
     p.tm_a = &tm_a;
     p.tm_b = &tm_w2;
     p.tm_out = &tm_out;
-    p.x = nullptr;
-    p.counts = w.counts;
-    p.offsets = w.offsets;
-    p.mt_prefix = w.mt_prefix;
-    p.perm_slot = w.perm_slot;
-    p.err = w.err;
     p.sched = w.sched2;
     p.topk_w = topk_w;
     p.out = w.obuf;
-    p.E = static_cast<int>(s.E);
-    p.k = s.k;
     p.K = static_cast<int>(s.I);
     p.n_out = static_cast<int>(s.H);
+    p.n_tile = kBN;
     p.b_rows = static_cast<int>(s.H);
-    p.half = 0;
-    p.num_sms = d.num_sms;
     moe_status_t r = cuda_status(launch_gemm2_scatter(p, st));
     if (r != MOE_OK) return r;
     CombineLaunch c;
@@ -191,6 +226,160 @@ moe_status_t run_gemm2(const moe_shape_t &s, const void *a, const float *topk_w,
     c.H = static_cast<int>(s.H);
     c.k = s.k;
     return cuda_status(launch_combine(c, st));
+}
+
+// Stage 2 backward, data: rows of dropped slots zeroed, dA GEMM with the SwiGLU
+// backward epilogue, then the routing-weight gradient.
+moe_status_t run_bwd_stage2_data(const moe_shape_t &s, const void *dy, const float *topk_w, const void *w2,
+                                 const void *h, float *dtopk_w, const Ws &w, const DeviceState &d,
+                                 cudaStream_t st) {
+    const uint64_t R = static_cast<uint64_t>(s.T) * s.k;
+    CUtensorMap tm_w2, tm_dg, tm_du, tm_aw;
+    // w2 [E, H, I] read MN-major: K = H rows of expert e, N = I
+    if (!encode_bf16_3d(&tm_w2, w2, s.I, s.H, s.E, 64, kBK) ||
+        !encode_bf16_2d_strided(&tm_dg, w.dh, s.I, R, 2 * s.I, 32, 32) ||
+        !encode_bf16_2d_strided(&tm_du, w.dh + s.I, s.I, R, 2 * s.I, 32, 32) ||
+        !encode_bf16_2d(&tm_aw, w.aw, s.I, R, 32, 32))
+        return MOE_ERR_CUDA;
+    moe_status_t r = cuda_status(launch_zero_tail_rows(w.dh, w.aw, w.offsets + s.E, static_cast<int>(R),
+                                                      static_cast<int>(s.I), st));
+    if (r != MOE_OK) return r;
+    GemmLaunch p = base_launch(s, w, d);
+    p.tm_b = &tm_w2;
+    p.tm_out = &tm_dg;
+    p.tm_out2 = &tm_du;
+    p.tm_out3 = &tm_aw;
+    p.src = static_cast<const __nv_bfloat16 *>(dy);
+    p.h = static_cast<const __nv_bfloat16 *>(h);
+    p.sched = w.sched_da;
+    p.topk_w = topk_w;
+    p.out = w.dh;
+    p.out2 = w.dh + s.I;
+    p.out3 = w.aw;
+    p.dtw_part = w.dtw_part;
+    p.K = static_cast<int>(s.H);
+    p.src_cols = static_cast<int>(s.H);
+    p.n_out = static_cast<int>(s.I);
+    p.n_tile = kBN;
+    p.half = static_cast<int>(s.I);
+    p.out_ld = static_cast<int>(2 * s.I);
+    if ((r = cuda_status(launch_bwd_da(p, st))) != MOE_OK) return r;
+    if (dtopk_w == nullptr) return MOE_OK;
+    DtwReduceLaunch q;
+    q.dtw_part = w.dtw_part;
+    q.n_part = static_cast<int>((s.I + kBN - 1) / kBN);
+    q.R = static_cast<int>(R);
+    q.T = static_cast<int>(s.T);
+    q.k = s.k;
+    q.row_of = w.row_of;
+    q.dtopk_w = dtopk_w;
+    return cuda_status(launch_dtw_reduce(q, st));
+}
+
+// Stage 2 backward, weights: dW2[e] (M = H rows, N = I, K = e's rows): A = dY
+// rows gathered MN-major, B = w a rows through TMA.
+moe_status_t run_bwd_stage2_weight(const moe_shape_t &s, const void *dy, void *dw2, const Ws &w,
+                                   const DeviceState &d, cudaStream_t st) {
+    const uint64_t R = static_cast<uint64_t>(s.T) * s.k;
+    CUtensorMap tm_aw_mn, tm_dw2;
+    if (!encode_bf16_2d(&tm_aw_mn, w.aw, s.I, R, 64, kBK) ||
+        !encode_bf16_3d(&tm_dw2, dw2, s.I, s.H, s.E, 64, 32))
+        return MOE_ERR_CUDA;
+    GemmLaunch q = base_launch(s, w, d);
+    q.tm_b = &tm_aw_mn;
+    q.tm_out = &tm_dw2;
+    q.src = static_cast<const __nv_bfloat16 *>(dy);
+    q.sched = w.sched_dw2;
+    q.src_cols = static_cast<int>(s.H);
+    q.n_out = static_cast<int>(s.I);
+    q.n_tile = kBN;
+    q.m_total = static_cast<int>(s.H);
+    return cuda_status(launch_bwd_dw2(q, st));
+}
+
+// Router backward: logit gradient into the workspace, then dW_r.
+moe_status_t run_router_bwd(const moe_shape_t &s, const void *x, const float *logits, const int32_t *topk_idx,
+                            const float *topk_w, const float *dtopk_w, const moe_router_cfg_t &cfg, float *dw_r,
+                            const Ws &w, cudaStream_t st) {
+    RouterBwdLaunch p;
+    p.logits = logits;
+    p.topk_idx = topk_idx;
+    p.topk_w = topk_w;
+    p.dtopk_w = dtopk_w;
+    p.T = static_cast<int>(s.T);
+    p.H = static_cast<int>(s.H);
+    p.E = static_cast<int>(s.E);
+    p.k = s.k;
+    p.score_fn = cfg.score_fn;
+    p.normalize = cfg.normalize;
+    p.scale = cfg.scale;
+    p.dl = w.dlogits;
+    p.x = static_cast<const __nv_bfloat16 *>(x);
+    p.offsets = w.offsets;
+    p.counts = w.counts;
+    p.perm_slot = w.perm_slot;
+    p.dw_r = dw_r;
+    moe_status_t r = cuda_status(launch_router_dlogits(p, st));
+    if (r != MOE_OK) return r;
+    return cuda_status(launch_router_dwr(p, st));
+}
+
+// Stage 1 backward, data: dX rows GEMM, then the per-token sum (+ router term).
+moe_status_t run_bwd_stage1_data(const moe_shape_t &s, const void *w1, const float *w_r, const int32_t *topk_idx,
+                                 int dense_router, void *dx, const Ws &w, const DeviceState &d, cudaStream_t st) {
+    const uint64_t R = static_cast<uint64_t>(s.T) * s.k;
+    CUtensorMap tm_dh, tm_w1, tm_xr;
+    // w1 [E, 2I, H] read MN-major: K = 2I rows of expert e, N = H
+    if (!encode_bf16_2d(&tm_dh, w.dh, 2 * s.I, R, kBK, 128) ||
+        !encode_bf16_3d(&tm_w1, w1, s.H, 2 * s.I, s.E, 64, kBK) ||
+        !encode_bf16_2d(&tm_xr, w.obuf, s.H, R, 64, 32))
+        return MOE_ERR_CUDA;
+    GemmLaunch p = base_launch(s, w, d);
+    p.tm_a = &tm_dh;
+    p.tm_b = &tm_w1;
+    p.tm_out = &tm_xr;
+    p.sched = w.sched_dx;
+    p.out = w.obuf;
+    p.K = static_cast<int>(2 * s.I);
+    p.n_out = static_cast<int>(s.H);
+    p.n_tile = kBN;
+    moe_status_t r = cuda_status(launch_bwd_dx(p, st));
+    if (r != MOE_OK) return r;
+    CombineBwdLaunch c;
+    c.xbuf = w.obuf;
+    c.row_of = w.row_of;
+    c.topk_idx = topk_idx;
+    c.dl = w_r ? w.dlogits : nullptr;
+    c.w_r = w_r;
+    c.dense = dense_router;
+    c.dx = static_cast<__nv_bfloat16 *>(dx);
+    c.T = static_cast<int>(s.T);
+    c.H = static_cast<int>(s.H);
+    c.E = static_cast<int>(s.E);
+    c.k = s.k;
+    return cuda_status(launch_combine_bwd(c, st));
+}
+
+// Stage 1 backward, weights: dW1[e] (M = 2I rows, N = H, K = e's rows): A = dH
+// rows MN-major through TMA, B = x rows gathered MN-major.
+moe_status_t run_bwd_stage1_weight(const moe_shape_t &s, const void *x, void *dw1, const Ws &w,
+                                   const DeviceState &d, cudaStream_t st) {
+    const uint64_t R = static_cast<uint64_t>(s.T) * s.k;
+    CUtensorMap tm_dh_mn, tm_dw1;
+    if (!encode_bf16_2d(&tm_dh_mn, w.dh, 2 * s.I, R, 64, kBK) ||
+        !encode_bf16_3d(&tm_dw1, dw1, s.H, 2 * s.I, s.E, 64, 32))
+        return MOE_ERR_CUDA;
+    GemmLaunch q = base_launch(s, w, d);
+    q.tm_a = &tm_dh_mn;
+    q.tm_b = &tm_dh_mn;
+    q.tm_out = &tm_dw1;
+    q.src = static_cast<const __nv_bfloat16 *>(x);
+    q.sched = w.sched_dw1;
+    q.src_cols = static_cast<int>(s.H);
+    q.n_out = static_cast<int>(s.H);
+    q.n_tile = kBN;
+    q.m_total = static_cast<int>(2 * s.I);
+    return cuda_status(launch_bwd_dw1(q, st));
 }
 
 moe_status_t run_metadata(const moe_shape_t &s, const int32_t *topk_idx, const Ws &w, cudaStream_t st) {
@@ -220,8 +409,13 @@ std::once_flag g_encode_once;
 EncodeTiledFn g_encode = nullptr;
 }  // namespace
 
-bool encode_bf16_2d(CUtensorMap *map, const void *base, uint64_t inner, uint64_t rows,
-                    uint32_t box_inner, uint32_t box_rows) {
+namespace {
+
+// bf16 tensor of rank 2 or 3 (dims[0] contiguous, byte strides for the others)
+// with a box_inner x box_rows (x 1) box, zero fill out of bounds, and the
+// swizzle span equal to the box row (64 or 128 bytes).
+bool encode_bf16(CUtensorMap *map, const void *base, int rank, const cuuint64_t *dims,
+                 const cuuint64_t *byte_strides, uint32_t box_inner, uint32_t box_rows) {
     std::call_once(g_encode_once, [] {
         void *fn = nullptr;
         cudaDriverEntryPointQueryResult q;
@@ -233,14 +427,33 @@ bool encode_bf16_2d(CUtensorMap *map, const void *base, uint64_t inner, uint64_t
     });
     if (g_encode == nullptr) return false;
     if (box_inner * 2 != 128 && box_inner * 2 != 64) return false;
-    cuuint64_t dims[2] = {inner, rows};
-    cuuint64_t strides[1] = {inner * 2};
-    cuuint32_t box[2] = {box_inner, box_rows};
-    cuuint32_t estr[2] = {1, 1};
-    return g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides,
+    cuuint32_t box[3] = {box_inner, box_rows, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    return g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void *>(base), dims, byte_strides,
                     box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                     box_inner * 2 == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+bool encode_bf16_2d(CUtensorMap *map, const void *base, uint64_t inner, uint64_t rows,
+                    uint32_t box_inner, uint32_t box_rows) {
+    return encode_bf16_2d_strided(map, base, inner, rows, inner, box_inner, box_rows);
+}
+
+bool encode_bf16_2d_strided(CUtensorMap *map, const void *base, uint64_t inner, uint64_t rows,
+                            uint64_t row_stride, uint32_t box_inner, uint32_t box_rows) {
+    cuuint64_t dims[2] = {inner, rows};
+    cuuint64_t strides[1] = {row_stride * 2};
+    return encode_bf16(map, base, 2, dims, strides, box_inner, box_rows);
+}
+
+bool encode_bf16_3d(CUtensorMap *map, const void *base, uint64_t inner, uint64_t rows, uint64_t depth,
+                    uint32_t box_inner, uint32_t box_rows) {
+    cuuint64_t dims[3] = {inner, rows, depth};
+    cuuint64_t strides[2] = {inner * 2, inner * rows * 2};
+    return encode_bf16(map, base, 3, dims, strides, box_inner, box_rows);
 }
 
 void note_launches(int n) { g_launches.fetch_add(static_cast<uint64_t>(n), std::memory_order_relaxed); }
@@ -273,10 +486,26 @@ moe_status_t moe_workspace_init(void *ws, size_t ws_bytes, void *stream) {
     return cuda_status(cudaMemsetAsync(ws, 0, kWsHeaderBytes, static_cast<cudaStream_t>(stream)));
 }
 
-moe_status_t moe_router(const void *x, const float *w_r, const float *logit_offset,
-                        const float *sel_bias, const moe_shape_t *shape,
-                        const moe_router_cfg_t *cfg, int32_t *topk_idx, float *topk_w, float *aux,
-                        void *ws, size_t ws_bytes, void *stream) {
+}  // extern "C"
+
+namespace {
+
+moe_status_t check_router_cfg(const moe_shape_t *shape, const moe_router_cfg_t *cfg) {
+    if (cfg->score_fn != MOE_SCORE_SOFTMAX && cfg->score_fn != MOE_SCORE_SIGMOID) return MOE_ERR_INVALID_ARG;
+    if (cfg->n_group < 1 || cfg->n_group > 32) return MOE_ERR_UNSUPPORTED;
+    if (cfg->n_group > 1) {
+        if (shape->E % cfg->n_group != 0 || cfg->topk_group < 1 || cfg->topk_group > cfg->n_group ||
+            cfg->group_topn < 1 || cfg->group_topn > shape->E / cfg->n_group)
+            return MOE_ERR_INVALID_ARG;
+        if (static_cast<int64_t>(cfg->topk_group) * (shape->E / cfg->n_group) < shape->k)
+            return MOE_ERR_INVALID_ARG;
+    }
+    return MOE_OK;
+}
+
+moe_status_t router_impl(const void *x, const float *w_r, const float *logit_offset, const float *sel_bias,
+                         const moe_shape_t *shape, const moe_router_cfg_t *cfg, int32_t *topk_idx,
+                         float *topk_w, float *aux, float *logits, void *ws, size_t ws_bytes, void *stream) {
     moe_status_t r = check_shape(shape);
     if (r != MOE_OK) return r;
     if (shape->T == 0) return MOE_OK;  // nothing to route or compute
@@ -288,15 +517,8 @@ moe_status_t moe_router(const void *x, const float *w_r, const float *logit_offs
         (sel_bias && (reinterpret_cast<uintptr_t>(sel_bias) & 3u)) ||
         (aux && (reinterpret_cast<uintptr_t>(aux) & 3u)))
         return MOE_ERR_INVALID_ARG;
-    if (cfg->score_fn != MOE_SCORE_SOFTMAX && cfg->score_fn != MOE_SCORE_SIGMOID) return MOE_ERR_INVALID_ARG;
-    if (cfg->n_group < 1 || cfg->n_group > 32) return MOE_ERR_UNSUPPORTED;
-    if (cfg->n_group > 1) {
-        if (shape->E % cfg->n_group != 0 || cfg->topk_group < 1 || cfg->topk_group > cfg->n_group ||
-            cfg->group_topn < 1 || cfg->group_topn > shape->E / cfg->n_group)
-            return MOE_ERR_INVALID_ARG;
-        if (static_cast<int64_t>(cfg->topk_group) * (shape->E / cfg->n_group) < shape->k)
-            return MOE_ERR_INVALID_ARG;
-    }
+    if (logits != nullptr && !aligned16(logits)) return MOE_ERR_INVALID_ARG;
+    if ((r = check_router_cfg(shape, cfg)) != MOE_OK) return r;
     if ((r = check_ws(*shape, ws, ws_bytes)) != MOE_OK) return r;
     DeviceState *d = nullptr;
     if ((r = device_state(&d)) != MOE_OK) return r;
@@ -319,10 +541,43 @@ moe_status_t moe_router(const void *x, const float *w_r, const float *logit_offs
     p.topk_idx = topk_idx;
     p.topk_w = topk_w;
     p.aux = aux;
+    p.logits = logits;
     p.err = w.err;
     p.num_sms = d->num_sms;
     p.scratch = w.router;
     return cuda_status(launch_router(p, static_cast<cudaStream_t>(stream)));
+}
+
+// Common checks of the training entry points: a training workspace.
+moe_status_t check_training(const moe_shape_t *shape, const void *ws, size_t ws_bytes) {
+    moe_status_t r = check_ws(*shape, ws, ws_bytes);
+    if (r != MOE_OK) return r;
+    return (shape->flags & MOE_SHAPE_TRAINING) ? MOE_OK : MOE_ERR_INVALID_ARG;
+}
+
+bool dense_router_grad(const moe_router_cfg_t &cfg) {
+    return cfg.score_fn == MOE_SCORE_SOFTMAX && !cfg.normalize;
+}
+
+}  // namespace
+
+extern "C" {
+
+moe_status_t moe_router(const void *x, const float *w_r, const float *logit_offset,
+                        const float *sel_bias, const moe_shape_t *shape,
+                        const moe_router_cfg_t *cfg, int32_t *topk_idx, float *topk_w, float *aux,
+                        void *ws, size_t ws_bytes, void *stream) {
+    return router_impl(x, w_r, logit_offset, sel_bias, shape, cfg, topk_idx, topk_w, aux, nullptr, ws,
+                       ws_bytes, stream);
+}
+
+moe_status_t moe_router_train(const void *x, const float *w_r, const float *logit_offset,
+                              const float *sel_bias, const moe_shape_t *shape,
+                              const moe_router_cfg_t *cfg, int32_t *topk_idx, float *topk_w,
+                              float *aux, float *logits, void *ws, size_t ws_bytes, void *stream) {
+    if (shape != nullptr && shape->T > 0 && logits == nullptr) return MOE_ERR_INVALID_ARG;
+    return router_impl(x, w_r, logit_offset, sel_bias, shape, cfg, topk_idx, topk_w, aux, logits, ws,
+                       ws_bytes, stream);
 }
 
 moe_status_t moe_routing_metadata(const int32_t *topk_idx, const moe_shape_t *shape, void *ws,
@@ -347,7 +602,7 @@ moe_status_t moe_dispatch_gemm1(const void *x, const void *w1, const moe_shape_t
     if ((r = check_ws(*shape, ws, ws_bytes)) != MOE_OK) return r;
     DeviceState *d = nullptr;
     if ((r = device_state(&d)) != MOE_OK) return r;
-    return run_gemm1(*shape, x, w1, a, carve(ws, *shape), *d, static_cast<cudaStream_t>(stream));
+    return run_gemm1(*shape, x, w1, a, nullptr, carve(ws, *shape), *d, static_cast<cudaStream_t>(stream));
 }
 
 moe_status_t moe_swiglu_gemm2_combine(const void *a, const float *topk_w, const void *w2,
@@ -382,8 +637,127 @@ moe_status_t moe_forward(const void *x, const int32_t *topk_idx, const float *to
     const Ws w = carve(ws, *shape);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     if ((r = run_metadata(*shape, topk_idx, w, st)) != MOE_OK) return r;
-    if ((r = run_gemm1(*shape, x, w1, w.a, w, *d, st)) != MOE_OK) return r;
+    if ((r = run_gemm1(*shape, x, w1, w.a, nullptr, w, *d, st)) != MOE_OK) return r;
     return run_gemm2(*shape, w.a, topk_w, w2, y, w, *d, st);
+}
+
+moe_status_t moe_dispatch_gemm1_train(const void *x, const void *w1, const moe_shape_t *shape,
+                                      void *a, void *h, void *ws, size_t ws_bytes, void *stream) {
+    moe_status_t r = check_shape(shape);
+    if (r != MOE_OK) return r;
+    if (shape->T == 0) return MOE_OK;
+    if (x == nullptr || w1 == nullptr || a == nullptr || h == nullptr) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(w1) || !aligned16(a) || !aligned16(h)) return MOE_ERR_INVALID_ARG;
+    if ((r = check_training(shape, ws, ws_bytes)) != MOE_OK) return r;
+    DeviceState *d = nullptr;
+    if ((r = device_state(&d)) != MOE_OK) return r;
+    return run_gemm1(*shape, x, w1, a, h, carve(ws, *shape), *d, static_cast<cudaStream_t>(stream));
+}
+
+moe_status_t moe_backward_stage2_data(const void *dy, const float *topk_w, const void *w2, const void *h,
+                                      const moe_shape_t *shape, float *dtopk_w, void *ws, size_t ws_bytes,
+                                      void *stream) {
+    moe_status_t r = check_shape(shape);
+    if (r != MOE_OK) return r;
+    if (shape->T == 0) return MOE_OK;
+    if (dy == nullptr || topk_w == nullptr || w2 == nullptr || h == nullptr) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(dy) || !aligned16(topk_w) || !aligned16(w2) || !aligned16(h) ||
+        (dtopk_w && !aligned16(dtopk_w)))
+        return MOE_ERR_INVALID_ARG;
+    if ((r = check_training(shape, ws, ws_bytes)) != MOE_OK) return r;
+    DeviceState *d = nullptr;
+    if ((r = device_state(&d)) != MOE_OK) return r;
+    return run_bwd_stage2_data(*shape, dy, topk_w, w2, h, dtopk_w, carve(ws, *shape), *d,
+                               static_cast<cudaStream_t>(stream));
+}
+
+moe_status_t moe_backward_stage2_weight(const void *dy, const moe_shape_t *shape, void *dw2, void *ws,
+                                        size_t ws_bytes, void *stream) {
+    moe_status_t r = check_shape(shape);
+    if (r != MOE_OK) return r;
+    if (dw2 == nullptr || !aligned16(dw2)) return MOE_ERR_INVALID_ARG;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (shape->T == 0)  // no rows: every expert's weight gradient is zero
+        return cuda_status(cudaMemsetAsync(dw2, 0, 2 * static_cast<size_t>(shape->E) * shape->H * shape->I, st));
+    if (dy == nullptr || !aligned16(dy)) return MOE_ERR_INVALID_ARG;
+    if ((r = check_training(shape, ws, ws_bytes)) != MOE_OK) return r;
+    DeviceState *d = nullptr;
+    if ((r = device_state(&d)) != MOE_OK) return r;
+    return run_bwd_stage2_weight(*shape, dy, dw2, carve(ws, *shape), *d, st);
+}
+
+moe_status_t moe_router_backward(const void *x, const float *logits, const int32_t *topk_idx,
+                                 const float *topk_w, const float *dtopk_w, const moe_shape_t *shape,
+                                 const moe_router_cfg_t *cfg, float *dw_r, void *ws, size_t ws_bytes,
+                                 void *stream) {
+    moe_status_t r = check_shape(shape);
+    if (r != MOE_OK) return r;
+    if (cfg == nullptr || dw_r == nullptr || !aligned16(dw_r)) return MOE_ERR_INVALID_ARG;
+    if ((r = check_router_cfg(shape, cfg)) != MOE_OK) return r;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (shape->T == 0)
+        return cuda_status(cudaMemsetAsync(dw_r, 0, 4 * static_cast<size_t>(shape->E) * shape->H, st));
+    if (x == nullptr || logits == nullptr || topk_idx == nullptr || topk_w == nullptr || dtopk_w == nullptr)
+        return MOE_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(logits) || !aligned16(topk_idx) || !aligned16(topk_w) || !aligned16(dtopk_w))
+        return MOE_ERR_INVALID_ARG;
+    if ((r = check_training(shape, ws, ws_bytes)) != MOE_OK) return r;
+    DeviceState *d = nullptr;
+    if ((r = device_state(&d)) != MOE_OK) return r;
+    return run_router_bwd(*shape, x, logits, topk_idx, topk_w, dtopk_w, *cfg, dw_r, carve(ws, *shape), st);
+}
+
+moe_status_t moe_backward_stage1_data(const void *w1, const float *w_r, const int32_t *topk_idx,
+                                      const moe_router_cfg_t *cfg, const moe_shape_t *shape, void *dx,
+                                      void *ws, size_t ws_bytes, void *stream) {
+    moe_status_t r = check_shape(shape);
+    if (r != MOE_OK) return r;
+    if (w_r != nullptr && cfg == nullptr) return MOE_ERR_INVALID_ARG;
+    if (shape->T == 0) return MOE_OK;
+    if (w1 == nullptr || dx == nullptr || (w_r != nullptr && topk_idx == nullptr)) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(w1) || !aligned16(dx) || (w_r && !aligned16(w_r)) || (topk_idx && !aligned16(topk_idx)))
+        return MOE_ERR_INVALID_ARG;
+    if ((r = check_training(shape, ws, ws_bytes)) != MOE_OK) return r;
+    DeviceState *d = nullptr;
+    if ((r = device_state(&d)) != MOE_OK) return r;
+    return run_bwd_stage1_data(*shape, w1, w_r, topk_idx, w_r ? dense_router_grad(*cfg) : 0, dx,
+                               carve(ws, *shape), *d, static_cast<cudaStream_t>(stream));
+}
+
+moe_status_t moe_backward_stage1_weight(const void *x, const moe_shape_t *shape, void *dw1, void *ws,
+                                        size_t ws_bytes, void *stream) {
+    moe_status_t r = check_shape(shape);
+    if (r != MOE_OK) return r;
+    if (dw1 == nullptr || !aligned16(dw1)) return MOE_ERR_INVALID_ARG;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (shape->T == 0)
+        return cuda_status(cudaMemsetAsync(dw1, 0, 4 * static_cast<size_t>(shape->E) * shape->I * shape->H, st));
+    if (x == nullptr || !aligned16(x)) return MOE_ERR_INVALID_ARG;
+    if ((r = check_training(shape, ws, ws_bytes)) != MOE_OK) return r;
+    DeviceState *d = nullptr;
+    if ((r = device_state(&d)) != MOE_OK) return r;
+    return run_bwd_stage1_weight(*shape, x, dw1, carve(ws, *shape), *d, st);
+}
+
+moe_status_t moe_backward(const void *x, const float *w_r, const float *logits, const int32_t *topk_idx,
+                          const float *topk_w, const void *w1, const void *w2, const void *h, const void *dy,
+                          const moe_shape_t *shape, const moe_router_cfg_t *cfg, void *dx, void *dw1,
+                          void *dw2, float *dw_r, float *dtopk_w, void *ws, size_t ws_bytes, void *stream) {
+    moe_status_t r = check_shape(shape);
+    if (r != MOE_OK) return r;
+    if (w_r != nullptr && (logits == nullptr || cfg == nullptr || dw_r == nullptr || dtopk_w == nullptr ||
+                           topk_idx == nullptr))
+        return MOE_ERR_INVALID_ARG;
+    if ((r = moe_backward_stage2_data(dy, topk_w, w2, h, shape, dtopk_w, ws, ws_bytes, stream)) != MOE_OK ||
+        (r = moe_backward_stage2_weight(dy, shape, dw2, ws, ws_bytes, stream)) != MOE_OK)
+        return r;
+    if (w_r != nullptr &&
+        (r = moe_router_backward(x, logits, topk_idx, topk_w, dtopk_w, shape, cfg, dw_r, ws, ws_bytes, stream)) !=
+            MOE_OK)
+        return r;
+    if ((r = moe_backward_stage1_data(w1, w_r, topk_idx, cfg, shape, dx, ws, ws_bytes, stream)) != MOE_OK)
+        return r;
+    return moe_backward_stage1_weight(x, shape, dw1, ws, ws_bytes, stream);
 }
 
 moe_status_t moe_get_device_error(void *ws, int32_t *code, void *stream) {

@@ -93,6 +93,7 @@ struct TopkArgs {
     int32_t *counts;
     int32_t *ticket;
     float *aux;
+    float *logits_out;          // [T, E] fp32 logits (offset included) or null
 };
 
 // V = experts per lane (lane l holds experts l, l+32, ..., l+32(V-1)).
@@ -123,6 +124,7 @@ router_topk_kernel(const TopkArgs p) {
                 float l = 0.0f;
                 for (int sp = 0; sp < p.splits; ++sp) l += lrow[sp * split_stride + e];
                 if (p.logit_offset) l += p.logit_offset[e];
+                if (p.logits_out) p.logits_out[static_cast<int64_t>(t) * p.E + e] = l;
                 s[i] = l;
             } else {
                 s[i] = -INFINITY;
@@ -329,6 +331,7 @@ cudaError_t launch_router(const RouterLaunch &p, cudaStream_t st) {
     a.counts = sc.counts;
     a.ticket = sc.ticket;
     a.aux = p.aux;
+    a.logits_out = p.logits;
     const int blocks = (p.T + kTopkWarps - 1) / kTopkWarps;
     const int v = (p.E + 31) / 32;
     if (v <= 2) launch_topk<2>(a, blocks, st);

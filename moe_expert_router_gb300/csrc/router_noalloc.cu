@@ -86,7 +86,7 @@ extern "C" moe_status_t moe_router_noalloc(const void *x, const float *w_r,
                                            void *stream) {
     if (shape == nullptr || cfg == nullptr) return MOE_ERR_INVALID_ARG;
     const moe_shape_t &s = *shape;
-    if (s.T < 0 || s.H <= 0 || s.I <= 0 || s.E <= 0 || s.k <= 0 || s.reserved != 0)
+    if (s.T < 0 || s.H <= 0 || s.I <= 0 || s.E <= 0 || s.k <= 0 || (s.flags & ~MOE_SHAPE_TRAINING) != 0)
         return MOE_ERR_INVALID_ARG;
     if (s.k > 32 || s.k > s.E || s.E > 1024 || s.H % 8 != 0 || s.I % 8 != 0 ||
         s.H >= (int64_t(1) << 31) || s.T * s.k >= (int64_t(1) << 31))
@@ -139,6 +139,7 @@ extern "C" moe_status_t moe_router_noalloc(const void *x, const float *w_r,
     p.topk_idx = topk_idx;
     p.topk_w = topk_w;
     p.aux = aux;
+    p.logits = nullptr;
     // the split kernel clears the sums, counts and ticket at the start of every
     // call, and the GEMM's unit counter (zero when the library is loaded)
     // returns to zero at the end of every launch, so nothing an earlier call

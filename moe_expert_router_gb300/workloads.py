@@ -73,7 +73,7 @@ CONFIGS: dict[str, MoEConfig] = {
     "zipf_decode": MoEConfig("zipf_decode", T=64, H=4096, I=1536, E=128, k=8, zipf_s=1.2,
                              description="Zipf(1.2)-skewed routing, decode-like T=64"),
     "train": MoEConfig("train", T=8192, H=4096, I=1536, E=64, k=6, backward=True,
-                       description="training step shapes (forward part)"),
+                       description="training step: forward and backward (dX, dW1, dW2, router gradient)"),
     # profiling size: the large_group geometry per expert (H, I, k, groups, about
     # 256 routed rows per expert) with 32 experts, so that a full ncu capture
     # holds about 3 GB on the device

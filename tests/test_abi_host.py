@@ -117,3 +117,48 @@ def test_status_strings_and_counter(lib):
     for s in range(6):
         assert B.load().moe_status_string(s)
     assert B.moe_kernel_launch_count() >= 0
+
+
+def test_training_workspace_layout(lib):
+    for cfg in CONFIGS.values():
+        R = cfg.T * cfg.k
+        base = B.moe_workspace_layout(B.shape(cfg.T, cfg.H, cfg.I, cfg.E, cfg.k))
+        assert base.dh == base.aw == base.dtw_part == base.dlogits == base.total
+        L = B.moe_workspace_layout(B.shape(cfg.T, cfg.H, cfg.I, cfg.E, cfg.k, training=True))
+        offs = [L.obuf, L.dh, L.aw, L.dtw_part, L.dlogits, L.total]
+        assert offs == sorted(offs) and all(o % 256 == 0 for o in offs)
+        assert L.obuf == base.obuf                      # the forward regions do not move
+        assert L.aw - L.dh >= 2 * R * 2 * cfg.I
+        assert L.dtw_part - L.aw >= 2 * R * cfg.I
+        assert L.dlogits - L.dtw_part >= 4 * R * ((cfg.I + 255) // 256)
+        assert L.total - L.dlogits >= 4 * cfg.T * cfg.E
+
+
+def test_training_calls_need_a_training_workspace(lib):
+    p = ctypes.c_void_p(1 << 20)
+    cfg = B.router_cfg()
+    plain = B.shape(16, 64, 64, 4, 2)
+    train = B.shape(16, 64, 64, 4, 2, training=True)
+    big = 1 << 40
+    # a forward-only shape: rejected on the host before any device call
+    assert lib.moe_dispatch_gemm1_train(p, p, ctypes.byref(plain), p, p, p, big, None) == 1
+    assert lib.moe_backward_stage2_data(p, p, p, p, ctypes.byref(plain), p, p, big, None) == 1
+    assert lib.moe_backward_stage2_weight(p, ctypes.byref(plain), p, p, big, None) == 1
+    assert lib.moe_router_backward(p, p, p, p, p, ctypes.byref(plain), ctypes.byref(cfg), p, p, big,
+                                   None) == 1
+    assert lib.moe_backward_stage1_data(p, None, None, None, ctypes.byref(plain), p, p, big, None) == 1
+    assert lib.moe_backward_stage1_weight(p, ctypes.byref(plain), p, p, big, None) == 1
+    # missing outputs / inputs
+    assert lib.moe_router_train(p, p, None, None, ctypes.byref(train), ctypes.byref(cfg), p, p, None,
+                                None, p, big, None) == 1
+    assert lib.moe_dispatch_gemm1_train(p, p, ctypes.byref(train), p, None, p, big, None) == 1
+    assert lib.moe_backward_stage2_data(p, p, p, None, ctypes.byref(train), None, p, big, None) == 1
+    assert lib.moe_backward_stage2_weight(p, ctypes.byref(train), None, p, big, None) == 1
+    assert lib.moe_backward_stage1_data(p, p, None, ctypes.byref(cfg), ctypes.byref(train), p, p, big,
+                                        None) == 1     # w_r without topk_idx
+    assert lib.moe_backward(p, p, None, p, p, p, p, p, p, ctypes.byref(train), ctypes.byref(cfg), p, p, p,
+                            p, p, p, big, None) == 1   # w_r without logits
+    # unknown shape flags
+    bad = B.Shape(16, 64, 64, 4, 2, 2)
+    n = ctypes.c_size_t()
+    assert lib.moe_workspace_size(ctypes.byref(bad), ctypes.byref(n)) == 1

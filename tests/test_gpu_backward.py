@@ -1,0 +1,258 @@
+"""Backward of the expert path and the router (CUDA path through the C ABI)
+against the fp64 oracle's backward.
+
+Bars (the same relative-error bounds as the forward outputs): dX, dW1, dW2,
+dW_r and the routing-weight gradient within relative Frobenius error 1e-2 and
+max abs error 3e-2 * max|ref|. Routing is taken from the GPU router (its
+indices are checked against the oracle in the forward tests), so both sides
+differentiate the same selection.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from gpu_helpers import assert_close_y, router_cfg_of
+from moe_expert_router_gb300 import binding as B
+from moe_expert_router_gb300.workloads import CONFIGS, MoEConfig, generate, routing_with_counts
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _device():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    B.load()   # raises when libmoe.so is missing: there is no fallback
+
+
+def _cfg(T, H, I, E, k, **kw):
+    return MoEConfig("case", T=T, H=H, I=I, E=E, k=k, backward=True, **kw)
+
+
+def _inputs(cfg, seed=0):
+    inp = generate(cfg, seed=seed, device=DEV)
+    if inp["dy"] is None:
+        g = torch.Generator(device=DEV).manual_seed(seed + 100)
+        inp["dy"] = torch.randn((cfg.T, cfg.H), generator=g, device=DEV).to(torch.bfloat16)
+    return inp
+
+
+def train_step(inp, cfg, idx=None, w=None, staged=True, with_router=True):
+    """Forward (saving h and the logits) and backward through the C ABI."""
+    T, H, I, E, k = cfg.T, cfg.H, cfg.I, cfg.E, cfg.k
+    shp = B.shape(T, H, I, E, k, training=True)
+    ws = B.new_workspace(shp, DEV)
+    rc = router_cfg_of(cfg)
+    out = {"ws": ws, "shp": shp}
+    logits = None
+    if idx is None:
+        idx = torch.empty((T, k), dtype=torch.int32, device=DEV)
+        w = torch.empty((T, k), dtype=torch.float32, device=DEV)
+        logits = torch.empty((T, E), dtype=torch.float32, device=DEV)
+        B.moe_router_train(inp["x"], inp["w_r"], shp, rc, idx, w, logits, ws,
+                           logit_offset=inp.get("logit_offset"), sel_bias=inp.get("sel_bias"))
+    else:
+        with_router = False
+    a = torch.empty((T * k, I), dtype=torch.bfloat16, device=DEV)
+    h = torch.empty((T * k, 2 * I), dtype=torch.bfloat16, device=DEV)
+    y = torch.empty((T, H), dtype=torch.bfloat16, device=DEV)
+    B.moe_routing_metadata(idx, shp, ws)
+    B.moe_dispatch_gemm1_train(inp["x"], inp["w1"], shp, a, h, ws)
+    B.moe_swiglu_gemm2_combine(a, w, inp["w2"], shp, y, ws)
+    dx = torch.empty((T, H), dtype=torch.bfloat16, device=DEV)
+    dw1 = torch.full((E, 2 * I, H), float("nan"), dtype=torch.bfloat16, device=DEV)
+    dw2 = torch.full((E, H, I), float("nan"), dtype=torch.bfloat16, device=DEV)
+    dtw = torch.full((T, k), float("nan"), dtype=torch.float32, device=DEV)
+    dwr = torch.full((E, H), float("nan"), dtype=torch.float32, device=DEV) if with_router else None
+    w_r = inp["w_r"] if with_router else None
+    if staged:
+        B.moe_backward_stage2_data(inp["dy"], w, inp["w2"], h, shp, ws, dtopk_w=dtw)
+        B.moe_backward_stage2_weight(inp["dy"], shp, dw2, ws)
+        if with_router:
+            B.moe_router_backward(inp["x"], logits, idx, w, dtw, shp, rc, dwr, ws)
+        B.moe_backward_stage1_data(inp["w1"], shp, dx, ws, w_r=w_r, topk_idx=idx, cfg=rc)
+        B.moe_backward_stage1_weight(inp["x"], shp, dw1, ws)
+    else:
+        B.moe_backward(inp["x"], idx, w, inp["w1"], inp["w2"], h, inp["dy"], shp, dx, dw1, dw2, ws,
+                       w_r=w_r, logits=logits, cfg=rc, dw_r=dwr, dtopk_w=dtw)
+    err = B.moe_get_device_error(ws)
+    out.update(idx=idx, w=w, logits=logits, a=a, h=h, y=y, dx=dx, dw1=dw1, dw2=dw2, dtw=dtw, dwr=dwr,
+               err=err)
+    return out
+
+
+def oracle_grads(inp, cfg, idx, w, with_router=True):
+    cpu = {k_: (v.cpu() if isinstance(v, torch.Tensor) else v) for k_, v in inp.items()}
+    wd = w.cpu().double()
+    b = oracle.expert_backward(cpu["x"], idx.cpu(), wd, cpu["w1"], cpu["w2"], cpu["dy"])
+    res = {"dx": b.dx, "dw1": b.dw1, "dw2": b.dw2, "dtw": b.dtopk_w}
+    if with_router:
+        rb = oracle.router_backward(cpu["x"], cpu["w_r"], idx.cpu(), wd, b.dtopk_w, score=cfg.score,
+                                    normalize=cfg.normalize, scale=cfg.scale,
+                                    logit_offset=cpu.get("logit_offset"))
+        res["dx"] = res["dx"] + rb.dx_add
+        res["dwr"] = rb.dw_r
+        res["dlogits"] = rb.dlogits
+    return res
+
+
+def check_all(out, ref, with_router=True):
+    assert out["err"] == 0, f"device error word {out['err']:#x}"
+    assert_close_y(out["dtw"], ref["dtw"], "dtopk_w")
+    assert_close_y(out["dw2"], ref["dw2"], "dW2")
+    assert_close_y(out["dw1"], ref["dw1"], "dW1")
+    assert_close_y(out["dx"], ref["dx"], "dX")
+    if with_router:
+        assert_close_y(out["dwr"], ref["dwr"], "dW_r")
+
+
+CASES = {
+    "tiny": CONFIGS["tiny"],
+    "ragged_sigmoid_groups": _cfg(300, 192, 320, 16, 3, score="sigmoid", scale=2.5, n_group=4,
+                                  topk_group=2, sel_bias=True),
+    "two_units_per_expert": _cfg(1024, 512, 384, 4, 2),
+    "softmax_plain": _cfg(200, 256, 128, 8, 3, normalize=False, scale=1.5),
+    "sigmoid_plain": _cfg(200, 256, 128, 8, 3, score="sigmoid", normalize=False, scale=2.0),
+    "zipf_offsets": _cfg(512, 256, 192, 32, 4, zipf_s=1.2),
+    "h8_i8": _cfg(5, 8, 8, 3, 2),
+    "one_token": _cfg(1, 64, 64, 4, 2),
+}
+
+
+@pytest.mark.parametrize("name", sorted(CASES))
+def test_backward_matches_oracle(name):
+    cfg = CASES[name]
+    inp = _inputs(cfg, seed=3)
+    out = train_step(inp, cfg)
+    ref = oracle_grads(inp, cfg, out["idx"], out["w"])
+    check_all(out, ref)
+
+
+def test_one_shot_equals_staged():
+    cfg = CASES["ragged_sigmoid_groups"]
+    inp = _inputs(cfg, seed=4)
+    a = train_step(inp, cfg, staged=True)
+    b = train_step(inp, cfg, staged=False)
+    for key in ("dx", "dw1", "dw2", "dtw", "dwr"):
+        assert torch.equal(a[key], b[key]), key
+
+
+def test_saved_h_and_logits():
+    cfg = CASES["ragged_sigmoid_groups"]
+    inp = _inputs(cfg, seed=5)
+    out = train_step(inp, cfg)
+    # the stage-1 output a is unchanged by saving h, and h holds W1 x per routed row
+    shp_plain = B.shape(cfg.T, cfg.H, cfg.I, cfg.E, cfg.k)
+    ws = B.new_workspace(shp_plain, DEV)
+    a_plain = torch.empty_like(out["a"])
+    B.moe_routing_metadata(out["idx"], shp_plain, ws)
+    B.moe_dispatch_gemm1(inp["x"], inp["w1"], shp_plain, a_plain, ws)
+    R = int(out["idx"].numel())
+    assert torch.equal(a_plain[:R], out["a"][:R])
+    ref = oracle.routing_metadata(out["idx"].cpu(), cfg.E)
+    x = inp["x"].cpu().double()
+    h_ref = np.zeros((len(ref.perm_slot), 2 * cfg.I))
+    for e in range(cfg.E):
+        r0, r1 = int(ref.offsets[e]), int(ref.offsets[e + 1])
+        tok = torch.as_tensor(ref.perm_slot[r0:r1] // cfg.k, dtype=torch.long)
+        h_ref[r0:r1] = (x[tok] @ inp["w1"][e].cpu().double().T).numpy()
+    assert_close_y(out["h"][: len(ref.perm_slot)], h_ref, "h")
+    # logits: x W_r^T + offset in fp32
+    l_ref = inp["x"].cpu().double() @ inp["w_r"].cpu().double().T
+    assert_close_y(out["logits"], l_ref.numpy(), "logits")
+
+
+def test_empty_experts_and_nan_poison():
+    """Experts without rows get exactly zero weight gradients, whatever their weights hold."""
+    T, H, I, E, k = 96, 128, 64, 8, 2
+    cfg = _cfg(T, H, I, E, k)
+    inp = _inputs(cfg, seed=6)
+    counts = [40, 0, 60, 50, 0, 42, 0, 0]
+    idx, w = routing_with_counts(counts, T, k, seed=2, device=DEV)
+    for e, c in enumerate(counts):
+        if c == 0:
+            inp["w1"][e] = float("nan")
+            inp["w2"][e] = float("nan")
+    out = train_step(inp, cfg, idx=idx, w=w)
+    for e, c in enumerate(counts):
+        if c == 0:
+            assert not out["dw1"][e].float().abs().max().item()
+            assert not out["dw2"][e].float().abs().max().item()
+    ref = oracle_grads(inp, cfg, idx, w, with_router=False)
+    check_all(out, ref, with_router=False)
+
+
+def test_dropped_slots_have_zero_weight_gradient():
+    T, H, I, E, k = 64, 128, 64, 4, 2
+    cfg = _cfg(T, H, I, E, k)
+    inp = _inputs(cfg, seed=7)
+    idx, w = routing_with_counts([32, 32, 32, 32], T, k, seed=3, device=DEV)
+    idx[3, 1] = -1
+    idx[10, 0] = E
+    out = train_step(inp, cfg, idx=idx, w=w)
+    assert out["err"] & B.DEVERR_BAD_EXPERT_INDEX
+    out["err"] = 0
+    assert out["dtw"][3, 1].item() == 0.0 and out["dtw"][10, 0].item() == 0.0
+    ref = oracle_grads(inp, cfg, idx, w, with_router=False)
+    check_all(out, ref, with_router=False)
+
+
+def test_zero_tokens_zero_weight_gradients():
+    T, H, I, E, k = 0, 64, 64, 4, 2
+    shp = B.shape(T, H, I, E, k, training=True)
+    ws = B.new_workspace(shp, DEV)
+    dw1 = torch.full((E, 2 * I, H), 1.0, dtype=torch.bfloat16, device=DEV)
+    dw2 = torch.full((E, H, I), 1.0, dtype=torch.bfloat16, device=DEV)
+    dwr = torch.full((E, H), 1.0, dtype=torch.float32, device=DEV)
+    empty = torch.empty((0, H), dtype=torch.bfloat16, device=DEV)
+    B.moe_backward_stage2_data(empty, None, None, None, shp, ws)
+    B.moe_backward_stage2_weight(None, shp, dw2, ws)
+    B.moe_router_backward(None, None, None, None, None, shp, B.router_cfg(), dwr, ws)
+    B.moe_backward_stage1_data(None, shp, None, ws)
+    B.moe_backward_stage1_weight(None, shp, dw1, ws)
+    torch.cuda.synchronize()
+    assert not dw1.float().abs().max().item() and not dw2.float().abs().max().item()
+    assert not dwr.abs().max().item()
+
+
+@pytest.mark.slow
+def test_full_size_train_config_sampled():
+    """The training configuration at full size, in the bench's staged launch
+    sequence: dX and dtopk_w on sampled tokens, dW1 / dW2 of two experts, dW_r
+    given the GPU's own routing-weight gradient."""
+    cfg = CONFIGS["train"]
+    inp = _inputs(cfg, seed=0)
+    out = train_step(inp, cfg)
+    assert out["err"] == 0
+    idx, w = out["idx"], out["w"]
+    T, k, E = cfg.T, cfg.k, cfg.E
+    toks = [0, 1, T // 2, T - 1] + list(range(37, T, T // 12))[:12]
+    cpu = {k_: (v.cpu() if isinstance(v, torch.Tensor) else v) for k_, v in inp.items()}
+    tok_t = torch.as_tensor(toks)
+    b = oracle.expert_backward(cpu["x"][tok_t], idx.cpu()[tok_t], w.cpu()[tok_t].double(), cpu["w1"],
+                               cpu["w2"], cpu["dy"][tok_t], want_dw=False)
+    assert_close_y(out["dtw"].cpu()[tok_t], b.dtopk_w, "dtopk_w (sampled tokens)")
+    # dX adds the router term, which needs the token's logit gradient: from the oracle's
+    # router backward fed with the oracle's own routing-weight gradient of those tokens
+    rb = oracle.router_backward(cpu["x"][tok_t], cpu["w_r"], idx.cpu()[tok_t], w.cpu()[tok_t].double(),
+                                b.dtopk_w, score=cfg.score, normalize=cfg.normalize, scale=cfg.scale)
+    assert_close_y(out["dx"].cpu()[tok_t], b.dx + rb.dx_add, "dX (sampled tokens)")
+    # weight gradients of the most and the least loaded expert
+    flat = idx.cpu().reshape(-1).long()
+    counts = torch.bincount(flat, minlength=E)
+    for e in (int(counts.argmax()), int(counts.argmin())):
+        slots = torch.nonzero(flat == e).flatten()
+        tk = slots // k
+        one = torch.zeros((len(tk), 1), dtype=torch.int32)
+        be = oracle.expert_backward(cpu["x"][tk], one, w.cpu().reshape(-1)[slots].double().unsqueeze(1),
+                                    cpu["w1"][e:e + 1], cpu["w2"][e:e + 1], cpu["dy"][tk])
+        assert_close_y(out["dw2"][e], be.dw2[0], f"dW2[{e}]")
+        assert_close_y(out["dw1"][e], be.dw1[0], f"dW1[{e}]")
+    # dW_r from the GPU's own routing-weight gradient (the router backward stage alone)
+    rfull = oracle.router_backward(cpu["x"], cpu["w_r"], idx.cpu(), w.cpu().double(),
+                                   out["dtw"].cpu().double(), score=cfg.score, normalize=cfg.normalize,
+                                   scale=cfg.scale)
+    assert_close_y(out["dwr"], rfull.dw_r, "dW_r")
