@@ -99,35 +99,60 @@ __device__ __forceinline__ bool first_slot(const int32_t *__restrict__ idx_t, in
 
 // dW_r[e, c..c+8) per thread: block (e, 1024-column chunk). Sparse modes walk
 // the expert's routed rows; the dense mode (plain softmax) walks every token.
-__global__ void __launch_bounds__(128)
+// Rows go in batches of 128: each thread first resolves one row's token and
+// logit gradient into shared memory, then every thread accumulates the batch's
+// x rows for its 8 columns (independent loads, no dependent chain per row).
+constexpr int kDwrThreads = 128;
+
+__global__ void __launch_bounds__(kDwrThreads)
 router_dwr_kernel(const RouterBwdLaunch p, int chunks, int dense) {
+    __shared__ int tok_sh[kDwrThreads];
+    __shared__ float coef_sh[kDwrThreads];
     const int e = blockIdx.x / chunks;
-    const int c = ((blockIdx.x - e * chunks) * 128 + threadIdx.x) * 8;
-    if (c >= p.H) return;
+    const int c = ((blockIdx.x - e * chunks) * kDwrThreads + threadIdx.x) * 8;
     float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
     const int n = dense ? p.T : p.counts[e];
     const int r0 = dense ? 0 : p.offsets[e];
-    for (int i = 0; i < n; ++i) {
-        int t;
-        if (dense) {
-            t = i;
-        } else {
-            const int s = p.perm_slot[r0 + i];
-            t = s / p.k;
-            if (!first_slot(p.topk_idx + static_cast<int64_t>(t) * p.k, s - t * p.k, e)) continue;
+    for (int b0 = 0; b0 < n; b0 += kDwrThreads) {
+        const int i = b0 + threadIdx.x;
+        int t = -1;
+        float coef = 0.0f;
+        if (i < n) {
+            if (dense) {
+                t = i;
+            } else {
+                const int s = p.perm_slot[r0 + i];
+                t = s / p.k;
+                if (!first_slot(p.topk_idx + static_cast<int64_t>(t) * p.k, s - t * p.k, e)) t = -1;
+            }
+            if (t >= 0) coef = p.dl[static_cast<int64_t>(t) * p.E + e];
         }
-        const float coef = p.dl[static_cast<int64_t>(t) * p.E + e];
-        const uint4 v = __ldg(reinterpret_cast<const uint4 *>(p.x + static_cast<int64_t>(t) * p.H + c));
-        const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
+        __syncthreads();                    // the previous batch is consumed
+        tok_sh[threadIdx.x] = t;
+        coef_sh[threadIdx.x] = coef;
+        __syncthreads();
+        if (c < p.H) {
+            const int m = min(kDwrThreads, n - b0);
+#pragma unroll 4
+            for (int j = 0; j < m; ++j) {
+                const int tj = tok_sh[j];
+                if (tj < 0) continue;
+                const float cf = coef_sh[j];
+                const uint4 v = __ldg(reinterpret_cast<const uint4 *>(p.x + static_cast<int64_t>(tj) * p.H + c));
+                const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            acc[2 * q] = fmaf(coef, __uint_as_float(wv[q] << 16), acc[2 * q]);
-            acc[2 * q + 1] = fmaf(coef, __uint_as_float(wv[q] & 0xffff0000u), acc[2 * q + 1]);
+                for (int q = 0; q < 4; ++q) {
+                    acc[2 * q] = fmaf(cf, __uint_as_float(wv[q] << 16), acc[2 * q]);
+                    acc[2 * q + 1] = fmaf(cf, __uint_as_float(wv[q] & 0xffff0000u), acc[2 * q + 1]);
+                }
+            }
         }
     }
-    float4 *dst = reinterpret_cast<float4 *>(p.dw_r + static_cast<int64_t>(e) * p.H + c);
-    dst[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
-    dst[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+    if (c < p.H) {
+        float4 *dst = reinterpret_cast<float4 *>(p.dw_r + static_cast<int64_t>(e) * p.H + c);
+        dst[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+        dst[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+    }
 }
 
 __global__ void __launch_bounds__(256)
@@ -230,9 +255,9 @@ cudaError_t launch_router_dlogits(const RouterBwdLaunch &p, cudaStream_t st) {
 }
 
 cudaError_t launch_router_dwr(const RouterBwdLaunch &p, cudaStream_t st) {
-    const int chunks = (p.H + 1023) / 1024;
+    const int chunks = (p.H + 8 * kDwrThreads - 1) / (8 * kDwrThreads);
     const int dense = (p.score_fn == MOE_SCORE_SOFTMAX && !p.normalize) ? 1 : 0;
-    router_dwr_kernel<<<p.E * chunks, 128, 0, st>>>(p, chunks, dense);
+    router_dwr_kernel<<<p.E * chunks, kDwrThreads, 0, st>>>(p, chunks, dense);
     note_launches(1);
     return cudaGetLastError();
 }

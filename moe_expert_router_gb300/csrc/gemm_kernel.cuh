@@ -830,27 +830,35 @@ tc_gemm_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs g) {
                 // MN-major tile over the expert's routed rows (the reduction): warp w
                 // copies K rows w, w + 4, ...; lane c8 the 16-byte chunk c8 of the
                 // 256-column slice. K rows past the expert's count and columns past
-                // the source width are zero-filled, so they add nothing.
+                // the source width are zero-filled, so they add nothing. Lane l < NR
+                // looks up the token of the warp's l-th row one stage ahead; the
+                // copies take it by shuffle.
                 constexpr int NR = BK / GATHER_WARPS;
+                static_assert(NR <= 32, "one token per lane");
                 const int c8 = gt & 31;
                 const int kr0 = gt >> 5;
                 const int col = (kGatherMnA<MODE> ? t.row0 : t.n * BN) + c8 * 8;
                 const bool col_ok = col < g.src_cols;
                 const uint32_t chunk_off = static_cast<uint32_t>(c8 >> 3) * MN_ATOM_BYTES;
+                auto token_of = [&](int kb) {
+                    const int kk = kb * BK + kr0 + GATHER_WARPS * lane;
+                    return (lane < NR && kb < t.kb1 && kk < t.kcount) ? g.perm_slot[t.koff + kk] / g.k : -1;
+                };
+                int tok_next = token_of(t.kb0);
                 for (int kb = t.kb0; kb < t.kb1; ++kb) {
+                    const int tok_cur = tok_next;
+                    tok_next = token_of(kb + 1);
                     bool e_ok = true;
                     if (lane == 0) e_ok = mbar_wait(smem_addr(&sm.empty[stage]), phase ^ 1u, abort_flag, g.err);
                     e_ok = __shfl_sync(0xffffffffu, e_ok, 0);
                     if (!e_ok) { ok = false; break; }
                     const uint32_t base = smem_addr(kGatherMnA<MODE> ? sm.a[stage] : sm.b[stage]) + chunk_off;
-#pragma unroll 4
+#pragma unroll
                     for (int i = 0; i < NR; ++i) {
-                        const int krow = kr0 + GATHER_WARPS * i;
-                        const int kk = kb * BK + krow;
-                        const bool ok_r = col_ok && kk < t.kcount;
-                        const int tok = ok_r ? g.perm_slot[t.koff + kk] / g.k : 0;
-                        cp_async_16(base + swizzled_chunk<128>(krow, c8 & 7),
-                                    g.src + static_cast<int64_t>(tok) * g.src_cols + (ok_r ? col : 0),
+                        const int tok = __shfl_sync(0xffffffffu, tok_cur, i);
+                        const bool ok_r = col_ok && tok >= 0;
+                        cp_async_16(base + swizzled_chunk<128>(kr0 + GATHER_WARPS * i, c8 & 7),
+                                    g.src + static_cast<int64_t>(ok_r ? tok : 0) * g.src_cols + (ok_r ? col : 0),
                                     ok_r ? 16u : 0u);
                     }
                     cp_async_commit();

@@ -82,6 +82,10 @@ CONFIGS: dict[str, MoEConfig] = {
                                    group_topn=2, sel_bias=True,
                                    description="large_group per-expert geometry, 32 experts "
                                                "(profiling size)"),
+    # profiling size of the training step: the train geometry per expert (H, I, k,
+    # about 768 routed rows per expert) with 16 experts, about 1 GB on the device
+    "train_slice": MoEConfig("train_slice", T=2048, H=4096, I=1536, E=16, k=6, backward=True,
+                             description="train per-expert geometry, 16 experts (profiling size)"),
 }
 
 
