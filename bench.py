@@ -213,6 +213,15 @@ def run_ours(args, cfg, rank, world, local_rank):
         dwr = torch.empty_like(inp["w_r"])
         dtw = torch.empty((cfg.T, cfg.k), dtype=torch.float32, device=dev)
 
+    uniform = args.routing == "uniform"
+    if uniform:
+        # the guide's `uniform` force-balance mode: each step routes fresh N(0,1)
+        # logits (drawn before the timed region; a pool of 8 steps' worth is cycled)
+        gen = torch.Generator(device=dev)
+        gen.manual_seed(1000 + rank)
+        logit_pool = [torch.randn((cfg.T, cfg.E), generator=gen, device=dev) for _ in range(8)]
+    step_no = [0]
+
     names = ["router", "metadata", "gemm1", "gemm2_combine"]
     if train:
         names += ["bwd_stage2_data", "bwd_stage2_weight", "router_bwd", "bwd_stage1_data",
@@ -220,7 +229,12 @@ def run_ours(args, cfg, rank, world, local_rank):
 
     def calls(x_in, dy_in):
         """The step's C-ABI calls in order (one per event interval)."""
-        if train:
+        if uniform:
+            lg = logit_pool[step_no[0] % len(logit_pool)]
+            step_no[0] += 1
+            yield lambda: B.moe_route_logits(lg, shp, rcfg, idx, w, ws, aux=aux,
+                                             logit_offset=inp["logit_offset"], sel_bias=inp["sel_bias"])
+        elif train:
             yield lambda: B.moe_router_train(x_in, inp["w_r"], shp, rcfg, idx, w, logits, ws, aux=aux,
                                              logit_offset=inp["logit_offset"], sel_bias=inp["sel_bias"])
         else:
@@ -235,9 +249,13 @@ def run_ours(args, cfg, rank, world, local_rank):
         if train:
             yield lambda: B.moe_backward_stage2_data(dy_in, w, inp["w2"], h, shp, ws, dtopk_w=dtw)
             yield lambda: B.moe_backward_stage2_weight(dy_in, shp, dw2, ws)
-            yield lambda: B.moe_router_backward(x_in, logits, idx, w, dtw, shp, rcfg, dwr, ws)
-            yield lambda: B.moe_backward_stage1_data(inp["w1"], shp, dx, ws, w_r=inp["w_r"], topk_idx=idx,
-                                                     cfg=rcfg)
+            if uniform:         # random logits: no gradient reaches the router
+                yield lambda: None
+                yield lambda: B.moe_backward_stage1_data(inp["w1"], shp, dx, ws)
+            else:
+                yield lambda: B.moe_router_backward(x_in, logits, idx, w, dtw, shp, rcfg, dwr, ws)
+                yield lambda: B.moe_backward_stage1_data(inp["w1"], shp, dx, ws, w_r=inp["w_r"],
+                                                         topk_idx=idx, cfg=rcfg)
             yield lambda: B.moe_backward_stage1_weight(x_in, shp, dw1, ws)
 
     def step(ev=None):
@@ -340,19 +358,29 @@ def run_ours(args, cfg, rank, world, local_rank):
 
 # ---------------------------------------------------------------- oracle (CPU) arm
 
-def oracle_sample(cfg, n_tokens, seed=0, inputs=None):
+def oracle_sample(cfg, n_tokens, seed=0, inputs=None, routing="router"):
     """Run the oracle's step (router + expert path, and for a training workload the
-    expert and router backward) on the first n_tokens tokens; return seconds."""
+    expert and router backward) on the first n_tokens tokens; return seconds. With
+    uniform routing the oracle routes N(0,1) logits (its router on x = identity and
+    W_r = the logits transposed) and the router backward is skipped."""
     import oracle
     inp = inputs if inputs is not None else cpu_inputs(cfg, seed)
     x = inp["x"][:n_tokens]
+    if routing == "uniform":
+        g = torch.Generator().manual_seed(1000 + seed)
+        rx = torch.eye(n_tokens, dtype=torch.float32).to(torch.bfloat16)
+        rw = torch.randn((cfg.E, n_tokens), generator=g, dtype=torch.float32)
+    else:
+        rx, rw = x, inp["w_r"]
     t0 = time.perf_counter()
-    r = oracle.router(x, inp["w_r"], cfg.k, score=cfg.score, normalize=cfg.normalize,
+    r = oracle.router(rx, rw, cfg.k, score=cfg.score, normalize=cfg.normalize,
                       scale=cfg.scale, n_group=cfg.n_group, topk_group=cfg.topk_group,
                       group_topn=cfg.group_topn, logit_offset=inp["logit_offset"],
                       sel_bias=inp["sel_bias"])
     oracle.expert_forward(x, r.topk_idx, r.topk_w, inp["w1"], inp["w2"])
-    if cfg.backward:
+    if cfg.backward and routing == "uniform":
+        oracle.expert_backward(x, r.topk_idx, r.topk_w, inp["w1"], inp["w2"], inp["dy"][:n_tokens])
+    elif cfg.backward:
         b = oracle.expert_backward(x, r.topk_idx, r.topk_w, inp["w1"], inp["w2"], inp["dy"][:n_tokens])
         oracle.router_backward(x, inp["w_r"], r.topk_idx, r.topk_w, b.dtopk_w, score=cfg.score,
                                normalize=cfg.normalize, scale=cfg.scale, logit_offset=inp["logit_offset"])
@@ -375,15 +403,15 @@ def cpu_inputs(cfg, seed=0):
     return _CPU_INPUTS[key]
 
 
-def cpu_baseline(cfg, budget_s=15.0):
+def cpu_baseline(cfg, budget_s=15.0, routing="router"):
     """Oracle timed on the host cores on a bounded token sample (~budget_s of work)."""
     import oracle
     oracle.build()
     inp = cpu_inputs(cfg)
     n_cal = min(cfg.T, 8)
-    t_cal = oracle_sample(cfg, n_cal, inputs=inp)
+    t_cal = oracle_sample(cfg, n_cal, inputs=inp, routing=routing)
     n = int(max(1, min(cfg.T, n_cal * budget_s / max(t_cal, 1e-6))))
-    t = oracle_sample(cfg, n, inputs=inp) if n != n_cal else t_cal
+    t = oracle_sample(cfg, n, inputs=inp, routing=routing) if n != n_cal else t_cal
     flops = sample_flops(cfg, n)
     what = "forward and backward" if cfg.backward else "router + expert path"
     return {"value": flops / t / 1e12, "unit": "TFLOP/s", "cores": oracle.num_threads(),
@@ -396,12 +424,12 @@ def run_reference(args, cfg):
     oracle.build()
     inp = cpu_inputs(cfg)
     n_cal = min(cfg.T, 8)
-    t_cal = oracle_sample(cfg, n_cal, inputs=inp)
+    t_cal = oracle_sample(cfg, n_cal, inputs=inp, routing=args.routing)
     per_step_budget = min(20.0, 150.0 / max(1, args.steps + args.warmup))
     n = int(max(1, min(cfg.T, n_cal * per_step_budget / max(t_cal, 1e-6))))
     for _ in range(args.warmup):
-        oracle_sample(cfg, n, inputs=inp)
-    times = [oracle_sample(cfg, n, inputs=inp) for _ in range(args.steps)]
+        oracle_sample(cfg, n, inputs=inp, routing=args.routing)
+    times = [oracle_sample(cfg, n, inputs=inp, routing=args.routing) for _ in range(args.steps)]
     tot = sum(times)
     flops = sample_flops(cfg, n) * args.steps
     value = flops / tot / 1e12
@@ -435,7 +463,8 @@ def whole_job_throughput(units_per_rank_step, steps, world, total_ms):
 
 
 def config_dict(cfg, args):
-    return {"workload": cfg.name, "description": cfg.description, "T": cfg.T, "H": cfg.H,
+    return {"workload": cfg.name, "description": cfg.description, "routing": args.routing,
+            "T": cfg.T, "H": cfg.H,
             "I": cfg.I, "E": cfg.E, "k": cfg.k, "score": cfg.score, "n_group": cfg.n_group,
             "topk_group": cfg.topk_group, "zipf_s": cfg.zipf_s, "parallelism": f"replicas x{args.gpus}",
             "l2": f"flushed between steps ({L2_FLUSH_BYTES >> 20} MiB write outside the step events); "
@@ -450,6 +479,9 @@ def main():
     ap.add_argument("--workload", default="mid", choices=sorted(CONFIGS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--routing", default="router", choices=["router", "uniform"],
+                    help="router: the fused router on x; uniform: the guide's force-balance mode "
+                         "(fresh N(0,1) logits each step, routed by moe_route_logits)")
     args = ap.parse_args()
     cfg = CONFIGS[args.workload]
 
@@ -510,7 +542,7 @@ def main():
             "clocks": res["clocks"],
         }
         if not args.no_cpu_baseline:
-            out["cpu_baseline"] = cpu_baseline(cfg)
+            out["cpu_baseline"] = cpu_baseline(cfg, routing=args.routing)
         print(json.dumps(out), flush=True)
     if world > 1:
         torch.distributed.destroy_process_group()

@@ -133,6 +133,20 @@ moe_status_t moe_router(const void *x, const float *w_r, const float *logit_offs
                         float *aux, void *ws, size_t ws_bytes, void *stream);
 
 /*
+ * The router's selection from given fp32 logits l [T,E] instead of x . w_r^T:
+ * scores, selection bias, group limit, top-k, weights and aux exactly as in
+ * moe_router (logit_offset is added to l first). This is the guide's
+ * force-load-balancing mode `uniform` (section "Router force load
+ * balancing": the logits are replaced with random values before routing, so
+ * per-expert counts are balanced only statistically and vary from step to
+ * step) when the caller fills `logits` with random values; the random values
+ * are an input, drawn by the caller.
+ */
+moe_status_t moe_route_logits(const float *logits, const float *logit_offset, const float *sel_bias,
+                              const moe_shape_t *shape, const moe_router_cfg_t *cfg, int32_t *topk_idx,
+                              float *topk_w, float *aux, void *ws, size_t ws_bytes, void *stream);
+
+/*
  * moe_router_noalloc: the same router as moe_router, for callers that cannot
  * allocate device memory. The pages have no counterpart to this entry point.
  *

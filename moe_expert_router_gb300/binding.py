@@ -63,6 +63,8 @@ _SIG = {
     "moe_dispatch_gemm1": [_P, _P, ctypes.POINTER(Shape), _P, _P, ctypes.c_size_t, _P],
     "moe_swiglu_gemm2_combine": [_P, _P, _P, ctypes.POINTER(Shape), _P, _P, ctypes.c_size_t, _P],
     "moe_forward": [_P, _P, _P, _P, _P, ctypes.POINTER(Shape), _P, _P, ctypes.c_size_t, _P],
+    "moe_route_logits": [_P, _P, _P, ctypes.POINTER(Shape), ctypes.POINTER(RouterCfg), _P, _P, _P, _P,
+                         ctypes.c_size_t, _P],
     "moe_router_train": [_P, _P, _P, _P, ctypes.POINTER(Shape), ctypes.POINTER(RouterCfg), _P, _P,
                          _P, _P, _P, ctypes.c_size_t, _P],
     "moe_dispatch_gemm1_train": [_P, _P, ctypes.POINTER(Shape), _P, _P, _P, ctypes.c_size_t, _P],
@@ -199,6 +201,14 @@ def _cfg_ref(cfg):
 
 def _nbytes(ws):
     return ws.numel() * ws.element_size()
+
+
+def moe_route_logits(logits, shp, cfg, topk_idx, topk_w, ws, aux=None, logit_offset=None,
+                     sel_bias=None, stream=None):
+    """Routing from given fp32 logits [T, E] (random logits: the `uniform` force-balance mode)."""
+    _check("moe_route_logits", load().moe_route_logits(
+        _ptr(logits), _ptr(logit_offset), _ptr(sel_bias), ctypes.byref(shp), ctypes.byref(cfg),
+        _ptr(topk_idx), _ptr(topk_w), _ptr(aux), _ptr(ws), _nbytes(ws), _stream(stream, logits)))
 
 
 def moe_router_train(x, w_r, shp, cfg, topk_idx, topk_w, logits, ws, aux=None, logit_offset=None,

@@ -167,6 +167,9 @@ struct CombineLaunch {
 };
 
 cudaError_t launch_router(const RouterLaunch &p, cudaStream_t st);
+// The router's selection stage alone, from caller-given fp32 logits [T, E]
+// (p.x and p.w_r unused).
+cudaError_t launch_route_logits(const RouterLaunch &p, const float *logits, cudaStream_t st);
 cudaError_t launch_routing_metadata(const MetadataLaunch &p, cudaStream_t st);
 cudaError_t launch_gemm1_swiglu(const GemmLaunch &p, cudaStream_t st);
 cudaError_t launch_gemm2_scatter(const GemmLaunch &p, cudaStream_t st);

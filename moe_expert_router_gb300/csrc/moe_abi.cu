@@ -571,6 +571,46 @@ moe_status_t moe_router(const void *x, const float *w_r, const float *logit_offs
                        ws_bytes, stream);
 }
 
+moe_status_t moe_route_logits(const float *logits, const float *logit_offset, const float *sel_bias,
+                              const moe_shape_t *shape, const moe_router_cfg_t *cfg, int32_t *topk_idx,
+                              float *topk_w, float *aux, void *ws, size_t ws_bytes, void *stream) {
+    moe_status_t r = check_shape(shape);
+    if (r != MOE_OK) return r;
+    if (shape->T == 0) return MOE_OK;
+    if (cfg == nullptr || logits == nullptr || topk_idx == nullptr || topk_w == nullptr) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(logits) || !aligned16(topk_idx) || !aligned16(topk_w)) return MOE_ERR_INVALID_ARG;
+    if ((logit_offset && (reinterpret_cast<uintptr_t>(logit_offset) & 3u)) ||
+        (sel_bias && (reinterpret_cast<uintptr_t>(sel_bias) & 3u)) ||
+        (aux && (reinterpret_cast<uintptr_t>(aux) & 3u)))
+        return MOE_ERR_INVALID_ARG;
+    if ((r = check_router_cfg(shape, cfg)) != MOE_OK) return r;
+    if ((r = check_ws(*shape, ws, ws_bytes)) != MOE_OK) return r;
+    DeviceState *d = nullptr;
+    if ((r = device_state(&d)) != MOE_OK) return r;
+    const Ws w = carve(ws, *shape);
+    RouterLaunch p{};
+    p.logit_offset = logit_offset;
+    p.sel_bias = sel_bias;
+    p.T = static_cast<int>(shape->T);
+    p.H = static_cast<int>(shape->H);
+    p.E = static_cast<int>(shape->E);
+    p.k = shape->k;
+    p.score_fn = cfg->score_fn;
+    p.normalize = cfg->normalize;
+    p.scale = cfg->scale;
+    p.n_group = cfg->n_group;
+    p.topk_group = cfg->topk_group;
+    p.group_topn = cfg->group_topn;
+    p.topk_idx = topk_idx;
+    p.topk_w = topk_w;
+    p.aux = aux;
+    p.logits = nullptr;
+    p.err = w.err;
+    p.num_sms = d->num_sms;
+    p.scratch = w.router;
+    return cuda_status(launch_route_logits(p, logits, static_cast<cudaStream_t>(stream)));
+}
+
 moe_status_t moe_router_train(const void *x, const float *w_r, const float *logit_offset,
                               const float *sel_bias, const moe_shape_t *shape,
                               const moe_router_cfg_t *cfg, int32_t *topk_idx, float *topk_w,

@@ -283,37 +283,15 @@ void launch_topk(const TopkArgs &a, int blocks, cudaStream_t st) {
 
 }  // namespace
 
-cudaError_t launch_router(const RouterLaunch &p, cudaStream_t st) {
+namespace {
+
+// Selection, weights and aux from fp32 logits: `logits` holds `splits` partial
+// logit arrays [splits, T, E] that are summed in order.
+cudaError_t launch_selection(const RouterLaunch &p, const float *logits, int splits, cudaStream_t st) {
     const RouterScratch &sc = p.scratch;
-    const int64_t n = static_cast<int64_t>(p.E) * p.H;
-    int64_t sblocks = (n + 255) / 256;
-    if (sblocks > 152 * 8) sblocks = 152 * 8;
-    router_split_kernel<<<static_cast<int>(sblocks), 256, 0, st>>>(p.w_r, sc.w3, n, p.E, sc.score_sum,
-                                                                   sc.counts, sc.ticket);
-    note_launches(1);
-    cudaError_t err = cudaGetLastError();
-    if (err != cudaSuccess) return err;
-
-    CUtensorMap tm_x, tm_w3;
-    if (!encode_bf16_2d(&tm_x, p.x, p.H, p.T, kBK, kBM) ||
-        !encode_bf16_2d(&tm_w3, sc.w3, p.H, 3 * static_cast<uint64_t>(p.E), kBK, kBN))
-        return cudaErrorInvalidValue;
-    RouterGemmLaunch g;
-    g.tm_x = &tm_x;
-    g.tm_w3 = &tm_w3;
-    g.logits_part = sc.logits_part;
-    g.err = p.err;
-    g.sched = sc.sched;
-    g.T = p.T;
-    g.H = p.H;
-    g.E = p.E;
-    g.splits = sc.splits;
-    g.num_sms = p.num_sms;
-    if ((err = launch_router_gemm(g, st)) != cudaSuccess) return err;
-
     TopkArgs a;
-    a.logits_part = sc.logits_part;
-    a.splits = sc.splits;
+    a.logits_part = logits;
+    a.splits = splits;
     a.logit_offset = p.logit_offset;
     a.sel_bias = p.sel_bias;
     a.T = p.T;
@@ -341,6 +319,48 @@ cudaError_t launch_router(const RouterLaunch &p, cudaStream_t st) {
     else launch_topk<32>(a, blocks, st);
     note_launches(1);
     return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_router(const RouterLaunch &p, cudaStream_t st) {
+    const RouterScratch &sc = p.scratch;
+    const int64_t n = static_cast<int64_t>(p.E) * p.H;
+    int64_t sblocks = (n + 255) / 256;
+    if (sblocks > 152 * 8) sblocks = 152 * 8;
+    router_split_kernel<<<static_cast<int>(sblocks), 256, 0, st>>>(p.w_r, sc.w3, n, p.E, sc.score_sum,
+                                                                   sc.counts, sc.ticket);
+    note_launches(1);
+    cudaError_t err = cudaGetLastError();
+    if (err != cudaSuccess) return err;
+
+    CUtensorMap tm_x, tm_w3;
+    if (!encode_bf16_2d(&tm_x, p.x, p.H, p.T, kBK, kBM) ||
+        !encode_bf16_2d(&tm_w3, sc.w3, p.H, 3 * static_cast<uint64_t>(p.E), kBK, kBN))
+        return cudaErrorInvalidValue;
+    RouterGemmLaunch g;
+    g.tm_x = &tm_x;
+    g.tm_w3 = &tm_w3;
+    g.logits_part = sc.logits_part;
+    g.err = p.err;
+    g.sched = sc.sched;
+    g.T = p.T;
+    g.H = p.H;
+    g.E = p.E;
+    g.splits = sc.splits;
+    g.num_sms = p.num_sms;
+    if ((err = launch_router_gemm(g, st)) != cudaSuccess) return err;
+    return launch_selection(p, sc.logits_part, sc.splits, st);
+}
+
+cudaError_t launch_route_logits(const RouterLaunch &p, const float *logits, cudaStream_t st) {
+    const RouterScratch &sc = p.scratch;
+    // one block of the split kernel with nothing to split: it clears the aux accumulators
+    router_split_kernel<<<1, 256, 0, st>>>(nullptr, nullptr, 0, p.E, sc.score_sum, sc.counts, sc.ticket);
+    note_launches(1);
+    cudaError_t err = cudaGetLastError();
+    if (err != cudaSuccess) return err;
+    return launch_selection(p, logits, 1, st);
 }
 
 }  // namespace moe

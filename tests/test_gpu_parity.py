@@ -334,3 +334,51 @@ def test_full_size_config(name):
     assert_close_y(y[tokens], y_ref, what=f"{name} y[sampled tokens]")
     assert torch.isfinite(y.float()).all()
     assert B.moe_get_device_error(ws) == 0
+
+
+# ------------------------------------------------------------------ routing from given logits
+
+@pytest.mark.parametrize("case", [
+    dict(T=512, E=64, k=6),
+    dict(T=300, E=256, k=8, score="sigmoid", scale=2.5, n_group=8, topk_group=4, group_topn=2,
+         sel_bias=True),
+    dict(T=64, E=128, k=8, zipf_s=1.2),
+    dict(T=40, E=1024, k=32, normalize=False),
+])
+def test_route_logits_uniform_mode(case):
+    """The `uniform` force-balance mode: N(0,1) logits routed like the router's own
+    logits. Oracle: its router with x = identity (bf16) and W_r = logits^T, which
+    gives exactly those logits."""
+    case = dict(case)
+    T, E, k = case.pop("T"), case.pop("E"), case.pop("k")
+    zipf = case.pop("zipf_s", None)
+    cfg = _cfg(T, 64, 64, E, k, zipf_s=zipf, **case)
+    g = torch.Generator().manual_seed(T + E)
+    logits = torch.randn((T, E), generator=g, dtype=torch.float32)
+    inp = generate(cfg, seed=1)                        # selection bias / Zipf offsets only
+    shp = B.shape(T, 64, 64, E, k)
+    ws = B.new_workspace(shp)
+    idx = torch.empty((T, k), dtype=torch.int32, device=DEV)
+    w = torch.empty((T, k), dtype=torch.float32, device=DEV)
+    aux = torch.zeros((1,), dtype=torch.float32, device=DEV)
+    off = inp["logit_offset"].to(DEV) if inp["logit_offset"] is not None else None
+    bias = inp["sel_bias"].to(DEV) if inp["sel_bias"] is not None else None
+    B.moe_route_logits(logits.to(DEV), shp, B.router_cfg(cfg.score, cfg.normalize, cfg.scale, cfg.n_group,
+                                                          cfg.topk_group, cfg.group_topn),
+                       idx, w, ws, aux=aux, logit_offset=off, sel_bias=bias)
+    assert B.moe_get_device_error(ws) == 0
+    eye = torch.eye(T, dtype=torch.float32).to(torch.bfloat16)
+    ref = oracle.router(eye, logits.T.contiguous(), k, score=cfg.score, normalize=cfg.normalize,
+                        scale=cfg.scale, n_group=cfg.n_group, topk_group=cfg.topk_group,
+                        group_topn=cfg.group_topn, logit_offset=inp["logit_offset"],
+                        sel_bias=inp["sel_bias"])
+    n, bad, excluded = routing_mismatches(idx, ref, cfg)
+    assert not bad, f"{len(bad)} of {n} tokens routed differently"
+    keep = ~excluded
+    gi, gw = idx.cpu().numpy(), w.cpu().double().numpy()
+    for t in np.nonzero(keep)[0]:
+        order = np.argsort(gi[t])
+        ro = np.argsort(ref.topk_idx[t])
+        np.testing.assert_allclose(gw[t][order], ref.topk_w[t][ro], rtol=2e-5, atol=1e-7)
+    if keep.all():
+        assert abs(aux.item() - ref.aux) <= 1e-4 * max(1.0, abs(ref.aux))
