@@ -61,6 +61,12 @@ def _bind(lib):
     lib.oracle_router_backward.argtypes = [i64, i64, i64, i32, vp, vp, vp, i32, i32, f64,
                                            vp, vp, vp, vp, vp, vp]
     lib.oracle_router_backward.restype = ctypes.c_int
+    lib.oracle_mx_quantize_bf16.argtypes = [i64, i64, vp, vp, vp]
+    lib.oracle_mx_quantize_bf16.restype = ctypes.c_int
+    lib.oracle_mx_quantize_f64.argtypes = [i64, i64, vp, vp, vp]
+    lib.oracle_mx_quantize_f64.restype = ctypes.c_int
+    lib.oracle_expert_forward_mx.argtypes = [i64, i64, i64, i64, i32] + [vp] * 12
+    lib.oracle_expert_forward_mx.restype = ctypes.c_int
     return lib
 
 
@@ -197,6 +203,48 @@ class Oracle:
             raise ValueError("oracle_expert_backward rejected its arguments")
         return Backward(dx, dw1, dw2, dtw)
 
+    def mx_quantize(self, a):
+        """MXFP8 quantization along the last dimension: (codes uint8, scales uint8 [.., cols/32]).
+
+        `a` is bf16 (tensor) or float64 (array / tensor); any leading shape."""
+        arr = _np(a)
+        shape = arr.shape
+        cols = shape[-1]
+        rows = int(np.prod(shape[:-1])) if len(shape) > 1 else 1
+        codes = np.empty(shape, np.uint8)
+        scales = np.empty(shape[:-1] + (cols // 32,), np.uint8)
+        if arr.dtype == np.uint16:
+            rc = self.lib.oracle_mx_quantize_bf16(rows, cols, _ptr(arr), _ptr(codes), _ptr(scales))
+        else:
+            arr = np.ascontiguousarray(arr, np.float64)
+            rc = self.lib.oracle_mx_quantize_f64(rows, cols, _ptr(arr), _ptr(codes), _ptr(scales))
+        if rc != 0:
+            raise ValueError("oracle_mx_quantize rejected its arguments")
+        return codes, scales
+
+    def expert_forward_mx(self, xq, xs, topk_idx, topk_w, w1q, w1s, w2q, w2s, *, want_a=False):
+        """y [T, H] float64 of the MXFP8 expert path (optionally a before quantization and
+        its codes and scales per slot)."""
+        xq, xs = _np(xq, np.uint8), _np(xs, np.uint8)
+        w1q, w1s = _np(w1q, np.uint8), _np(w1s, np.uint8)
+        w2q, w2s = _np(w2q, np.uint8), _np(w2s, np.uint8)
+        idx = _np(topk_idx, np.int32)
+        w = _np(topk_w, np.float64)
+        T, H = xq.shape
+        E, twoI, _ = w1q.shape
+        I = twoI // 2
+        k = idx.shape[1]
+        y = np.empty((T, H), np.float64)
+        a = np.empty((T * k, I), np.float64) if want_a else None
+        ac = np.empty((T * k, I), np.uint8) if want_a else None
+        asc = np.empty((T * k, I // 32), np.uint8) if want_a else None
+        rc = self.lib.oracle_expert_forward_mx(T, H, I, E, k, _ptr(xq), _ptr(xs), _ptr(idx), _ptr(w),
+                                               _ptr(w1q), _ptr(w1s), _ptr(w2q), _ptr(w2s), _ptr(y),
+                                               _ptr(a), _ptr(ac), _ptr(asc))
+        if rc != 0:
+            raise ValueError("oracle_expert_forward_mx rejected its arguments")
+        return (y, a, ac, asc) if want_a else y
+
     def router_backward(self, x, w_r, topk_idx, topk_w, dtopk_w, *, score="softmax",
                         normalize=True, scale=1.0, logit_offset=None) -> RouterBackward:
         """Logit gradient from the routing-weight gradient, and its dX / dW_r."""
@@ -267,3 +315,34 @@ def expert_backward(*args, **kwargs) -> Backward:
 
 def router_backward(*args, **kwargs) -> RouterBackward:
     return default().router_backward(*args, **kwargs)
+
+
+def mx_quantize(*args, **kwargs):
+    return default().mx_quantize(*args, **kwargs)
+
+
+def expert_forward_mx(*args, **kwargs):
+    return default().expert_forward_mx(*args, **kwargs)
+
+
+def e4m3_values():
+    """float64 [256]: the value of every E4M3 code (NaN for 0x7F and 0xFF), from the
+    format's definition (sign, 4 exponent bits with bias 7, 3 mantissa bits)."""
+    v = np.empty(256, np.float64)
+    for c in range(256):
+        s, e, m = c >> 7, (c >> 3) & 15, c & 7
+        if e == 15 and m == 7:
+            v[c] = np.nan
+            continue
+        mag = m / 8.0 * 2.0 ** -6 if e == 0 else (1 + m / 8.0) * 2.0 ** (e - 7)
+        v[c] = -mag if s else mag
+    return v
+
+
+def mx_dequantize(codes, scales):
+    """Values of an MXFP8 matrix: code value times its block's 2^(scale - 127)."""
+    codes = np.asarray(codes)
+    scales = np.asarray(scales)
+    vals = e4m3_values()[codes]
+    blk = np.repeat(np.ldexp(1.0, scales.astype(np.int64) - 127), 32, axis=-1)
+    return vals * blk

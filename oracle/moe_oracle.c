@@ -603,3 +603,174 @@ int oracle_router_backward(int64_t T, int64_t H, int64_t E, int32_t k,
     free(dl);
     return 0;
 }
+
+/*
+ * ------------------------------------------------------------------ MXFP8
+ *
+ * The guide's second expert precision (section "Expert precision": mxfp8 runs
+ * the two expert stages in MXFP8). MXFP8 is the Open Compute Project
+ * Microscaling format (OCP MX v1.0): blocks of 32 consecutive elements along
+ * the reduction dimension share one power-of-two scale X stored as E8M0
+ * (biased exponent, bias 127); the elements are FP8 E4M3 (bias 7, no infinity,
+ * largest finite 448 = 1.75 * 2^8). Per the spec the shared exponent is
+ * floor(log2(max |v|)) - emax with emax = 8 for E4M3, and each element is
+ * v / X converted to E4M3, here with round-to-nearest-even and saturation to
+ * +-448. A block of zeros gets the smallest scale, 2^-127 (code 0).
+ */
+
+/* Value of an E4M3 code (finite codes only; 0x7F / 0xFF are NaN). */
+static double e4m3_value(uint8_t c) {
+    const int s = c >> 7, e = (c >> 3) & 15, m = c & 7;
+    const double v = (e == 0) ? ldexp((double)m, -9) : ldexp(1.0 + m / 8.0, e - 7);
+    return s ? -v : v;
+}
+
+/* E4M3 code of q, rounded to nearest (ties to even) and saturated. */
+static uint8_t e4m3_encode(double q) {
+    const uint8_t sign = (q < 0) ? 0x80 : 0x00;
+    double a = fabs(q);
+    if (a >= 448.0) return sign | 0x7E;
+    if (a < ldexp(1.0, -6)) {                 /* subnormals: m * 2^-9 */
+        const double m = rint(a * 512.0);     /* 8 -> the smallest normal, code 0x08 */
+        return sign | (uint8_t)m;
+    }
+    int p;
+    frexp(a, &p);                             /* a = f 2^p, f in [0.5, 1) */
+    p -= 1;                                   /* a in [2^p, 2^(p+1)) */
+    const double m = rint((ldexp(a, -p) - 1.0) * 8.0);   /* 0..8 */
+    int code = ((p + 7) << 3) + (int)m;       /* m = 8 carries into the exponent */
+    if (code > 0x7E) code = 0x7E;
+    return sign | (uint8_t)code;
+}
+
+/* E8M0 scale code of a block whose largest magnitude is amax. */
+static uint8_t mx_scale_code(double amax) {
+    if (amax == 0.0) return 0;
+    int p;
+    frexp(amax, &p);
+    int e = (p - 1) - 8;                      /* floor(log2 amax) - emax(E4M3) */
+    if (e < -127) e = -127;
+    if (e > 127) e = 127;
+    return (uint8_t)(e + 127);
+}
+
+static double e8m0_value(uint8_t s) { return ldexp(1.0, (int)s - 127); }
+
+/*
+ * Quantize a [rows, cols] matrix (cols a multiple of 32) to MXFP8 along its
+ * rows: codes [rows, cols], scales [rows, cols / 32]. Input as bf16 bit
+ * patterns (in_bf16) or doubles (in_f64); exactly one of them is non-NULL.
+ */
+static void mx_quantize_rows(int64_t rows, int64_t cols, const uint16_t *in_bf16, const double *in_f64,
+                             uint8_t *codes, uint8_t *scales) {
+#pragma omp parallel for schedule(static)
+    for (int64_t r = 0; r < rows; ++r) {
+        for (int64_t b = 0; b < cols / 32; ++b) {
+            double v[32], amax = 0.0;
+            for (int i = 0; i < 32; ++i) {
+                const int64_t j = r * cols + b * 32 + i;
+                v[i] = in_bf16 ? bf16_value(in_bf16[j]) : in_f64[j];
+                if (fabs(v[i]) > amax) amax = fabs(v[i]);
+            }
+            const uint8_t s = mx_scale_code(amax);
+            scales[r * (cols / 32) + b] = s;
+            for (int i = 0; i < 32; ++i)
+                codes[r * cols + b * 32 + i] = e4m3_encode(v[i] / e8m0_value(s));
+        }
+    }
+}
+
+int oracle_mx_quantize_bf16(int64_t rows, int64_t cols, const uint16_t *in, uint8_t *codes, uint8_t *scales) {
+    if (rows < 0 || cols <= 0 || cols % 32 != 0 || !in || !codes || !scales) return -1;
+    mx_quantize_rows(rows, cols, in, NULL, codes, scales);
+    return 0;
+}
+
+int oracle_mx_quantize_f64(int64_t rows, int64_t cols, const double *in, uint8_t *codes, uint8_t *scales) {
+    if (rows < 0 || cols <= 0 || cols % 32 != 0 || !in || !codes || !scales) return -1;
+    mx_quantize_rows(rows, cols, NULL, in, codes, scales);
+    return 0;
+}
+
+/* v = code value * scale value, for a quantized [rows, cols] matrix. */
+static double mx_value(const uint8_t *codes, const uint8_t *scales, int64_t cols, int64_t r, int64_t c) {
+    return e4m3_value(codes[r * cols + c]) * e8m0_value(scales[r * (cols / 32) + c / 32]);
+}
+
+/*
+ * Expert path forward in MXFP8 (the guide's mxfp8 expert precision): x, w1 and
+ * w2 are given quantized along their reduction dimension (x, w1 along H; w2
+ * along I). For each token t and choice j with e = topk_idx[t,j] in [0, E):
+ *
+ *   g_i, u_i = sum_h X(x)[t,h] X(w1)[e, i or I+i, h]       (exact, in double)
+ *   a_i      = silu(g_i) u_i
+ *   a_q      = MXFP8 quantization of a along I (blocks of 32)
+ *   o_h      = sum_i X(a_q)_i X(w2)[e,h,i]
+ *   y[t,:]  += topk_w[t,j] o
+ *
+ * X() is the dequantized value (code value times block scale). a_pre, when
+ * given, receives a before quantization per slot [T*k, I]; a_codes / a_scales
+ * its quantization [T*k, I] / [T*k, I/32] (zero for dropped slots).
+ */
+int oracle_expert_forward_mx(int64_t T, int64_t H, int64_t I, int64_t E, int32_t k,
+                             const uint8_t *x_codes, const uint8_t *x_scales,
+                             const int32_t *topk_idx, const double *topk_w,
+                             const uint8_t *w1_codes, const uint8_t *w1_scales,
+                             const uint8_t *w2_codes, const uint8_t *w2_scales,
+                             double *y, double *a_pre, uint8_t *a_codes, uint8_t *a_scales) {
+    if (T < 0 || H <= 0 || I <= 0 || E <= 0 || k <= 0 || H % 32 || I % 32 || !x_codes || !x_scales ||
+        !topk_idx || !topk_w || !w1_codes || !w1_scales || !w2_codes || !w2_scales || !y)
+        return -1;
+    int bad = 0;
+#pragma omp parallel
+    {
+        double *xt = (double *)malloc(sizeof(double) * (size_t)H);
+        double *a = (double *)malloc(sizeof(double) * (size_t)I);
+        double *aq = (double *)malloc(sizeof(double) * (size_t)I);
+        uint8_t *ac = (uint8_t *)malloc((size_t)I);
+        uint8_t *as = (uint8_t *)malloc((size_t)(I / 32));
+        if (!xt || !a || !aq || !ac || !as) {
+#pragma omp atomic write
+            bad = 1;
+        } else {
+#pragma omp for schedule(dynamic, 1)
+            for (int64_t t = 0; t < T; ++t) {
+                double *yt = y + t * H;
+                for (int64_t h = 0; h < H; ++h) { yt[h] = 0.0; xt[h] = mx_value(x_codes, x_scales, H, t, h); }
+                for (int32_t j = 0; j < k; ++j) {
+                    const int64_t slot = t * k + j;
+                    const int32_t e = topk_idx[slot];
+                    if (e < 0 || e >= E) {
+                        if (a_pre) for (int64_t i = 0; i < I; ++i) a_pre[slot * I + i] = 0.0;
+                        if (a_codes) memset(a_codes + slot * I, 0, (size_t)I);
+                        if (a_scales) memset(a_scales + slot * (I / 32), 0, (size_t)(I / 32));
+                        continue;
+                    }
+                    const int64_t r1 = (int64_t)e * 2 * I;      /* first w1 row of expert e */
+                    for (int64_t i = 0; i < I; ++i) {
+                        double g = 0.0, u = 0.0;
+                        for (int64_t h = 0; h < H; ++h) {
+                            g += mx_value(w1_codes, w1_scales, H, r1 + i, h) * xt[h];
+                            u += mx_value(w1_codes, w1_scales, H, r1 + I + i, h) * xt[h];
+                        }
+                        a[i] = silu(g) * u;
+                    }
+                    mx_quantize_rows(1, I, NULL, a, ac, as);
+                    for (int64_t i = 0; i < I; ++i) aq[i] = e4m3_value(ac[i]) * e8m0_value(as[i / 32]);
+                    if (a_pre) for (int64_t i = 0; i < I; ++i) a_pre[slot * I + i] = a[i];
+                    if (a_codes) memcpy(a_codes + slot * I, ac, (size_t)I);
+                    if (a_scales) memcpy(a_scales + slot * (I / 32), as, (size_t)(I / 32));
+                    const int64_t r2 = (int64_t)e * H;           /* first w2 row of expert e */
+                    const double w = topk_w[slot];
+                    for (int64_t h = 0; h < H; ++h) {
+                        double o = 0.0;
+                        for (int64_t i = 0; i < I; ++i) o += mx_value(w2_codes, w2_scales, I, r2 + h, i) * aq[i];
+                        yt[h] += w * o;
+                    }
+                }
+            }
+        }
+        free(xt); free(a); free(aq); free(ac); free(as);
+    }
+    return bad ? -1 : 0;
+}

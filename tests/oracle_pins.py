@@ -13,7 +13,12 @@ the oracle disagrees with something the pages or mathematics fix:
   token-permutation equivariance, linearity in w2, dropped slots, aux limits;
 * for the backward: torch fp64 autograd through a forward written here with
   library ops, the forward oracle's own o rows, exact scaling in dY, zero
-  gradients for unused experts and dropped slots.
+  gradients for unused experts and dropped slots;
+* for MXFP8: torch's float8_e4m3fn conversion (round to nearest even), the
+  round trip of every finite E4M3 code under several block scales, the
+  shared-exponent rule on chosen maxima, and the MX forward as a composition
+  of the bf16 oracle (on dequantized inputs), the quantizer and torch fp64
+  matmuls.
 
 tests/test_oracle_mutants.py compiles deliberately broken copies of the oracle
 and checks that every one of them fails at least one pin.
@@ -553,6 +558,89 @@ def pin_router_backward_finite_difference(orc):
             wm[e, h] -= d
             fd = (loss(wp, off) - loss(wm, off)) / (2 * d)
             assert abs(fd - b.dw_r[e, h]) <= 1e-5 * max(1.0, abs(b.dw_r[e, h])), (e, h, fd)
+
+
+# --------------------------------------------------------------------------- MXFP8
+
+def pin_mx_elements_match_torch_fp8(orc):
+    """With the block maximum in [256, 512) the scale is 2^0, so the codes are plain E4M3
+    conversions: they match torch's float8_e4m3fn cast (after clamping to +-448)."""
+    g = torch.Generator().manual_seed(30)
+    rows = 64
+    v = (torch.rand((rows, 32), generator=g, dtype=torch.float64) * 2 - 1) * 470.0
+    v[:, 0] = 300.0 + torch.rand((rows,), generator=g, dtype=torch.float64) * 150   # amax in [256, 512)
+    v[1] = torch.linspace(-0.03, 0.03, 32, dtype=torch.float64)                  # subnormal range
+    v[1, 0] = 260.0
+    vals = torch.tensor([0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 8.0, 16.0, 240.0, 416.0, 448.0], dtype=torch.float64)
+    mids = (vals[:-1] + vals[1:]) / 2
+    v[2, 1:1 + len(mids)] = mids                                                   # not all exact ties
+    v[3, 1:4] = torch.tensor([1.0625, 1.1875, 17.0], dtype=torch.float64)         # exact ties: to even
+    v[4, 1:4] = torch.tensor([460.0, 479.0, -500.0], dtype=torch.float64)         # saturation
+    codes, scales = orc.mx_quantize(v.numpy())
+    assert (scales == 127).all(), scales
+    want = v.clamp(-448.0, 448.0).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    np.testing.assert_array_equal(codes, want)
+
+
+def pin_mx_roundtrip_every_code(orc):
+    """A block holding code c's value times 2^s and an anchor 256 * 2^s quantizes back to
+    c with scale code s + 127, for every finite E4M3 code."""
+    import oracle as oracle_pkg
+    vals = oracle_pkg.e4m3_values()
+    finite = [c for c in range(256) if np.isfinite(vals[c]) and c != 0x80]
+    for sh in (-20, -3, 0, 5):
+        blk = np.zeros((len(finite), 32))
+        blk[:, 0] = [vals[c] * 2.0 ** sh for c in finite]
+        blk[:, 1] = 256.0 * 2.0 ** sh
+        codes, scales = orc.mx_quantize(blk)
+        assert (scales == sh + 127).all(), (sh, scales[:4])
+        assert codes[:, 0].tolist() == finite, sh
+
+
+def pin_mx_shared_exponent_rule(orc):
+    """Scale code = floor(log2 amax) - 8 + 127 (clamped at 0), zero blocks get code 0."""
+    amax = [2.0 ** -133, 2.0 ** -120, 0.75, 1.0, 1.999, 3.0, 2.0 ** 20 * 1.5, 2.0 ** 127]
+    blk = np.zeros((len(amax) + 1, 32))
+    for i, a in enumerate(amax):
+        blk[i, 5] = -a
+        blk[i, 6] = a / 3
+    codes, scales = orc.mx_quantize(blk)
+    for i, a in enumerate(amax):
+        e = int(np.floor(np.log2(a)))
+        assert scales[i, 0] == max(0, e - 8 + 127), (a, scales[i, 0])
+        assert codes[i, 5] & 0x80                      # sign kept
+    assert scales[-1, 0] == 0 and not codes[-1].any()
+
+
+def pin_mx_forward_composition(orc):
+    """MX forward = bf16 forward on dequantized inputs up to a, then the quantizer on a,
+    then a torch fp64 matmul per expert and the weighted sum."""
+    import oracle as oracle_pkg
+    T, H, I, E, k = 12, 64, 64, 4, 2
+    x, w1, w2, idx, w = _problem(31, T=T, H=H, I=I, E=E, k=k)
+    xq, xs = orc.mx_quantize(x)
+    w1q, w1s = orc.mx_quantize(w1)
+    w2q, w2s = orc.mx_quantize(w2)
+    y, a_pre, ac, asc = orc.expert_forward_mx(xq, xs, idx, w, w1q, w1s, w2q, w2s, want_a=True)
+    xd = oracle_pkg.mx_dequantize(xq, xs)
+    w1d = oracle_pkg.mx_dequantize(w1q, w1s)
+    w2d = oracle_pkg.mx_dequantize(w2q, w2s)
+    # dequantized values are exact in bf16 at these scales
+    bf = lambda a: torch.as_tensor(a).to(torch.bfloat16)
+    assert np.array_equal(bf(xd).double().numpy(), xd)
+    _, a_ref, _ = orc.expert_forward(bf(xd), idx, w, bf(w1d), bf(w2d), want_a=True)
+    np.testing.assert_allclose(a_pre, a_ref, rtol=1e-12, atol=1e-14)
+    c2, s2 = orc.mx_quantize(a_pre)
+    np.testing.assert_array_equal(ac, c2)
+    np.testing.assert_array_equal(asc, s2)
+    aq = torch.as_tensor(oracle_pkg.mx_dequantize(ac, asc))
+    y_ref = torch.zeros((T, H), dtype=torch.float64)
+    flat = idx.reshape(-1).long()
+    for slot in range(T * k):
+        e = int(flat[slot])
+        o = torch.as_tensor(w2d[e]) @ aq[slot]
+        y_ref[slot // k] += float(w.reshape(-1)[slot]) * o
+    np.testing.assert_allclose(y, y_ref.numpy(), rtol=1e-11, atol=1e-12)
 
 
 ALL_PINS = [v for n, v in sorted(globals().items()) if n.startswith("pin_") and callable(v)]

@@ -63,6 +63,19 @@ MUTANTS = {
                                     "dlt[K[j]] += si * (1.0 - si) * dw[j];"),
     "rbwd_dx_wr_transposed": ("acc += dlt[e] * (double)w_r[e * H + h];",
                               "acc += dlt[e] * (double)w_r[h * E + e];"),
+    # MXFP8
+    "mx_emax_7": ("int e = (p - 1) - 8;", "int e = (p - 1) - 7;"),
+    "mx_truncate": ("const double m = rint((ldexp(a, -p) - 1.0) * 8.0);",
+                    "const double m = floor((ldexp(a, -p) - 1.0) * 8.0);"),
+    "mx_subnormal_step": ("const double m = rint(a * 512.0);", "const double m = rint(a * 256.0);"),
+    "mx_amax_first_only": ("if (fabs(v[i]) > amax) amax = fabs(v[i]);", "if (i == 0) amax = fabs(v[i]);"),
+    "mx_dequant_unscaled": ("return e4m3_value(codes[r * cols + c]) * e8m0_value(scales[r * (cols / 32) + c / 32]);",
+                            "return e4m3_value(codes[r * cols + c]);"),
+    "mx_block_index_off": ("e8m0_value(scales[r * (cols / 32) + c / 32]);",
+                           "e8m0_value(scales[r * (cols / 32) + (c / 32 + 1) % (cols / 32)]);"),
+    "mx_a_not_requantized": ("for (int64_t i = 0; i < I; ++i) aq[i] = e4m3_value(ac[i]) * e8m0_value(as[i / 32]);",
+                             "for (int64_t i = 0; i < I; ++i) aq[i] = a[i];"),
+    "mx_overflow_to_nan": ("if (a >= 448.0) return sign | 0x7E;", "if (a >= 448.0) return sign | 0x7F;"),
     "rbwd_dwr_wrong_token": ("acc += dl[t * E + e] * bf16_value(x[t * H + h]);",
                              "acc += dl[t * E + e] * bf16_value(x[((t + 1) % T) * H + h]);"),
 }
