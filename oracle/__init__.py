@@ -335,7 +335,7 @@ def e4m3_values():
             v[c] = np.nan
             continue
         mag = m / 8.0 * 2.0 ** -6 if e == 0 else (1 + m / 8.0) * 2.0 ** (e - 7)
-        v[c] = -mag if s else mag
+        v[c] = -mag if s else mag           # code 0x80 is -0.0
     return v
 
 

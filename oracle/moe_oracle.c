@@ -615,7 +615,8 @@ int oracle_router_backward(int64_t T, int64_t H, int64_t E, int32_t k,
  * largest finite 448 = 1.75 * 2^8). Per the spec the shared exponent is
  * floor(log2(max |v|)) - emax with emax = 8 for E4M3, and each element is
  * v / X converted to E4M3, here with round-to-nearest-even and saturation to
- * +-448. A block of zeros gets the smallest scale, 2^-127 (code 0).
+ * +-448, keeping the sign of zero as IEEE-754 conversions do. A block of zeros
+ * gets the smallest scale, 2^-127 (code 0).
  */
 
 /* Value of an E4M3 code (finite codes only; 0x7F / 0xFF are NaN). */
@@ -627,7 +628,7 @@ static double e4m3_value(uint8_t c) {
 
 /* E4M3 code of q, rounded to nearest (ties to even) and saturated. */
 static uint8_t e4m3_encode(double q) {
-    const uint8_t sign = (q < 0) ? 0x80 : 0x00;
+    const uint8_t sign = signbit(q) ? 0x80 : 0x00;      /* -0 keeps its sign, as in IEEE conversions */
     double a = fabs(q);
     if (a >= 448.0) return sign | 0x7E;
     if (a < ldexp(1.0, -6)) {                 /* subnormals: m * 2^-9 */
