@@ -142,11 +142,22 @@ class ClockSampler:
 
 # ---------------------------------------------------------------- our arm
 
-def bytes_and_flops(cfg, counts):
+def bytes_and_flops(cfg, counts, precision="bf16"):
     """Algorithmic flops and bytes of each GEMM stage (bytes the kernels could avoid
     are not counted), keyed by the stage name used for the step's events."""
     R, H, I, T, E = cfg.R, cfg.H, cfg.I, cfg.T, cfg.E
     active = int((counts > 0).sum())
+    if precision == "mxfp8":
+        q = 1.0 + 1.0 / 32           # E4M3 byte + one E8M0 byte per 32 elements
+        return {"stages": {
+            "gemm1": {"flops": 4.0 * R * H * I,
+                      "bytes": 2.0 * H * I * q * active + R * H * q + R * I * q,
+                      "kernel": "tc_gemm_kernel<kStage1Mx> (stage 1 in MXFP8: dispatched E4M3 x rows, "
+                                "block-scaled MMA, SwiGLU + MXFP8 quantization of a)"},
+            "gemm2_combine": {"flops": 2.0 * R * H * I,
+                              "bytes": H * I * q * active + R * I * q + 2.0 * T * H,
+                              "kernel": "tc_gemm_kernel<kStage2Mx> + combine_kernel (stage 2 in MXFP8)"},
+        }, "active_experts": active}
     st = {
         "gemm1": {"flops": 4.0 * R * H * I,
                   "bytes": 4.0 * H * I * active + 2.0 * T * H + 2.0 * R * I * (3 if cfg.backward else 1),
@@ -214,6 +225,18 @@ def run_ours(args, cfg, rank, world, local_rank):
         dtw = torch.empty((cfg.T, cfg.k), dtype=torch.float32, device=dev)
 
     uniform = args.routing == "uniform"
+    mx = args.precision == "mxfp8"
+    if mx:
+        if train:
+            raise SystemExit("--precision mxfp8 covers the forward expert path; the train workload is bf16")
+        from moe_expert_router_gb300.mx_cache import MxWeightCache
+        shp = B.shape(cfg.T, cfg.H, cfg.I, cfg.E, cfg.k, mxfp8=True)
+        ws = B.new_workspace(shp, dev)
+        cache = MxWeightCache()           # weights quantized once, outside the timed region
+        w1q, w1s = cache.get(inp["w1"])
+        w2q, w2s = cache.get(inp["w2"])
+        aq = torch.empty((cfg.R, cfg.I), dtype=torch.uint8, device=dev)
+        as_ = torch.empty((cfg.R, cfg.I // 32), dtype=torch.uint8, device=dev)
     if uniform:
         # the guide's `uniform` force-balance mode: each step routes fresh N(0,1)
         # logits (drawn before the timed region; a pool of 8 steps' worth is cycled)
@@ -223,6 +246,8 @@ def run_ours(args, cfg, rank, world, local_rank):
     step_no = [0]
 
     names = ["router", "metadata", "gemm1", "gemm2_combine"]
+    if mx:
+        names = ["router", "metadata", "mx_dispatch", "gemm1", "gemm2_combine"]
     if train:
         names += ["bwd_stage2_data", "bwd_stage2_weight", "router_bwd", "bwd_stage1_data",
                   "bwd_stage1_weight"]
@@ -241,6 +266,11 @@ def run_ours(args, cfg, rank, world, local_rank):
             yield lambda: B.moe_router(x_in, inp["w_r"], shp, rcfg, idx, w, ws, aux=aux,
                                        logit_offset=inp["logit_offset"], sel_bias=inp["sel_bias"])
         yield lambda: B.moe_routing_metadata(idx, shp, ws)
+        if mx:
+            yield lambda: B.moe_mx_quantize_dispatch(x_in, shp, ws)
+            yield lambda: B.moe_dispatch_gemm1_mx(w1q, w1s, shp, aq, as_, ws)
+            yield lambda: B.moe_swiglu_gemm2_combine_mx(aq, as_, w, w2q, w2s, shp, y, ws)
+            return
         if train:
             yield lambda: B.moe_dispatch_gemm1_train(x_in, inp["w1"], shp, a, h, ws)
         else:
@@ -308,7 +338,7 @@ def run_ours(args, cfg, rank, world, local_rank):
     # metadata for the algorithmic byte counts
     L = B.moe_workspace_layout(shp)
     counts = ws[L.counts:L.counts + 4 * cfg.E].view(torch.int32).cpu()
-    bf = bytes_and_flops(cfg, counts)
+    bf = bytes_and_flops(cfg, counts, args.precision)
 
     # end to end: host x (and dY) in, host y + aux (and dX) out, copies inside the
     # timed region; weight gradients stay on the device for the optimizer
@@ -358,7 +388,10 @@ def run_ours(args, cfg, rank, world, local_rank):
 
 # ---------------------------------------------------------------- oracle (CPU) arm
 
-def oracle_sample(cfg, n_tokens, seed=0, inputs=None, routing="router"):
+_MX_WEIGHTS = {}
+
+
+def oracle_sample(cfg, n_tokens, seed=0, inputs=None, routing="router", precision="bf16"):
     """Run the oracle's step (router + expert path, and for a training workload the
     expert and router backward) on the first n_tokens tokens; return seconds. With
     uniform routing the oracle routes N(0,1) logits (its router on x = identity and
@@ -377,6 +410,16 @@ def oracle_sample(cfg, n_tokens, seed=0, inputs=None, routing="router"):
                       scale=cfg.scale, n_group=cfg.n_group, topk_group=cfg.topk_group,
                       group_topn=cfg.group_topn, logit_offset=inp["logit_offset"],
                       sel_bias=inp["sel_bias"])
+    if precision == "mxfp8":
+        # weights quantized once per workload (the cache), x per sample
+        if cfg.name not in _MX_WEIGHTS:
+            t1 = time.perf_counter()
+            _MX_WEIGHTS[cfg.name] = oracle.mx_quantize(inp["w1"]) + oracle.mx_quantize(inp["w2"])
+            t0 += time.perf_counter() - t1
+        w1q, w1s, w2q, w2s = _MX_WEIGHTS[cfg.name]
+        xq, xs = oracle.mx_quantize(x)
+        oracle.expert_forward_mx(xq, xs, r.topk_idx, r.topk_w, w1q, w1s, w2q, w2s)
+        return time.perf_counter() - t0
     oracle.expert_forward(x, r.topk_idx, r.topk_w, inp["w1"], inp["w2"])
     if cfg.backward and routing == "uniform":
         oracle.expert_backward(x, r.topk_idx, r.topk_w, inp["w1"], inp["w2"], inp["dy"][:n_tokens])
@@ -403,17 +446,19 @@ def cpu_inputs(cfg, seed=0):
     return _CPU_INPUTS[key]
 
 
-def cpu_baseline(cfg, budget_s=15.0, routing="router"):
+def cpu_baseline(cfg, budget_s=15.0, routing="router", precision="bf16"):
     """Oracle timed on the host cores on a bounded token sample (~budget_s of work)."""
     import oracle
     oracle.build()
     inp = cpu_inputs(cfg)
     n_cal = min(cfg.T, 8)
-    t_cal = oracle_sample(cfg, n_cal, inputs=inp, routing=routing)
+    t_cal = oracle_sample(cfg, n_cal, inputs=inp, routing=routing, precision=precision)
     n = int(max(1, min(cfg.T, n_cal * budget_s / max(t_cal, 1e-6))))
-    t = oracle_sample(cfg, n, inputs=inp, routing=routing) if n != n_cal else t_cal
+    t = oracle_sample(cfg, n, inputs=inp, routing=routing, precision=precision) if n != n_cal else t_cal
     flops = sample_flops(cfg, n)
     what = "forward and backward" if cfg.backward else "router + expert path"
+    if precision == "mxfp8":
+        what += " in MXFP8 (weights quantized once, outside the timing)"
     return {"value": flops / t / 1e12, "unit": "TFLOP/s", "cores": oracle.num_threads(),
             "kind": "oracle", "tokens_per_s": n / t,
             "sample": f"first {n} of {cfg.T} tokens of the '{cfg.name}' workload: fp64 {what}, {t:.2f} s"}
@@ -424,12 +469,13 @@ def run_reference(args, cfg):
     oracle.build()
     inp = cpu_inputs(cfg)
     n_cal = min(cfg.T, 8)
-    t_cal = oracle_sample(cfg, n_cal, inputs=inp, routing=args.routing)
+    kw = dict(inputs=inp, routing=args.routing, precision=args.precision)
+    t_cal = oracle_sample(cfg, n_cal, **kw)
     per_step_budget = min(20.0, 150.0 / max(1, args.steps + args.warmup))
     n = int(max(1, min(cfg.T, n_cal * per_step_budget / max(t_cal, 1e-6))))
     for _ in range(args.warmup):
-        oracle_sample(cfg, n, inputs=inp, routing=args.routing)
-    times = [oracle_sample(cfg, n, inputs=inp, routing=args.routing) for _ in range(args.steps)]
+        oracle_sample(cfg, n, **kw)
+    times = [oracle_sample(cfg, n, **kw) for _ in range(args.steps)]
     tot = sum(times)
     flops = sample_flops(cfg, n) * args.steps
     value = flops / tot / 1e12
@@ -464,6 +510,7 @@ def whole_job_throughput(units_per_rank_step, steps, world, total_ms):
 
 def config_dict(cfg, args):
     return {"workload": cfg.name, "description": cfg.description, "routing": args.routing,
+            "precision": args.precision,
             "T": cfg.T, "H": cfg.H,
             "I": cfg.I, "E": cfg.E, "k": cfg.k, "score": cfg.score, "n_group": cfg.n_group,
             "topk_group": cfg.topk_group, "zipf_s": cfg.zipf_s, "parallelism": f"replicas x{args.gpus}",
@@ -479,6 +526,8 @@ def main():
     ap.add_argument("--workload", default="mid", choices=sorted(CONFIGS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--precision", default="bf16", choices=["bf16", "mxfp8"],
+                    help="expert-path precision: bf16, or the guide's mxfp8 (E4M3 + E8M0 block scales)")
     ap.add_argument("--routing", default="router", choices=["router", "uniform"],
                     help="router: the fused router on x; uniform: the guide's force-balance mode "
                          "(fresh N(0,1) logits each step, routed by moe_route_logits)")
@@ -511,11 +560,14 @@ def main():
         dom = max(bf["stages"], key=lambda n: stage_avg[n])
         dom_ms = stage_avg[dom]
         f, b = bf["stages"][dom]["flops"], bf["stages"][dom]["bytes"]
-        t_tc = f / (peaks["bf16_tflops"] * 1e12)
+        # an MXFP8 contraction takes the fp8 peak: the measured bf16 peak times the
+        # nominal fp8 / bf16 ratio (4.5 / 2.25 PFLOP/s dense)
+        tc_peak = peaks["bf16_tflops"] * (2.0 if args.precision == "mxfp8" else 1.0)
+        t_tc = f / (tc_peak * 1e12)
         t_hbm = b / (peaks["hbm_gbs"] * 1e9)
         if t_tc >= t_hbm:
             roof = {"bound": "tensor", "achieved": f / (dom_ms / 1e3) / 1e12,
-                    "peak": peaks["bf16_tflops"], "unit": "TFLOP/s"}
+                    "peak": tc_peak, "unit": "TFLOP/s"}
         else:
             roof = {"bound": "hbm", "achieved": b / (dom_ms / 1e3) / 1e9, "peak": peaks["hbm_gbs"],
                     "unit": "GB/s"}
@@ -525,12 +577,15 @@ def main():
         roof["algorithmic_bytes"] = b
         roof["kernel"] = bf["stages"][dom]["kernel"]
         roof["stage"] = dom
-        roof["peak_kind"] = f"{peaks['source']} burst"
+        roof["peak_kind"] = (f"{peaks['source']} bf16 burst x 2 (nominal fp8/bf16 ratio)"
+                             if args.precision == "mxfp8" and roof["bound"] == "tensor"
+                             else f"{peaks['source']} burst")
         roof["kernel_ms"] = dom_ms
         out = {
             "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": total_ms / args.steps,
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "mxfp8 (e4m3 + e8m0 scales, fp32 accumulate)" if args.precision == "mxfp8" else "bf16",
             "data": "synthetic", "config": config_dict(cfg, args),
             "tokens_per_s": tokens_per_s,
             "stage_ms": {n: round(v, 5) for n, v in stage_avg.items()},
@@ -542,7 +597,7 @@ def main():
             "clocks": res["clocks"],
         }
         if not args.no_cpu_baseline:
-            out["cpu_baseline"] = cpu_baseline(cfg, routing=args.routing)
+            out["cpu_baseline"] = cpu_baseline(cfg, routing=args.routing, precision=args.precision)
         print(json.dumps(out), flush=True)
     if world > 1:
         torch.distributed.destroy_process_group()

@@ -62,11 +62,13 @@ typedef struct moe_shape {
     int64_t I;   /* expert intermediate size (w1 has 2I rows per expert) */
     int64_t E;   /* experts */
     int32_t k;   /* experts per token */
-    int32_t flags;  /* 0, or MOE_SHAPE_TRAINING */
+    int32_t flags;  /* 0, or an OR of MOE_SHAPE_TRAINING and MOE_SHAPE_MXFP8 */
 } moe_shape_t;
 
 /* moe_shape_t.flags: the workspace also holds the backward's intermediates. */
 #define MOE_SHAPE_TRAINING 0x1
+/* moe_shape_t.flags: the workspace also holds the MXFP8 path's quantized x and a. */
+#define MOE_SHAPE_MXFP8 0x2
 
 #define MOE_SCORE_SOFTMAX 0
 #define MOE_SCORE_SIGMOID 1
@@ -98,6 +100,11 @@ typedef struct moe_ws_layout {
     size_t aw;         /* bf16 [T*k, I] routing weight times a, routed order */
     size_t dtw_part;   /* fp32 [ceil(I/256), T*k] partial routing-weight gradients */
     size_t dlogits;    /* fp32 [T, E] gradient of the router logits */
+    /* MXFP8 workspaces only (flags & MOE_SHAPE_MXFP8), else equal to total: */
+    size_t x_codes;    /* E4M3 [T*k, H] quantized x rows in routed order (the MXFP8 dispatch) */
+    size_t x_scales;   /* E8M0 [T*k, H/32] */
+    size_t a_codes;    /* E4M3 [T*k, I] quantized SwiGLU output, routed order (moe_forward_mx) */
+    size_t a_scales;   /* E8M0 [T*k, I/32] */
     size_t total;      /* == moe_workspace_size */
 } moe_ws_layout_t;
 
@@ -327,6 +334,67 @@ moe_status_t moe_backward(const void *x, const float *w_r, const float *logits,
                           const void *w2, const void *h, const void *dy, const moe_shape_t *shape,
                           const moe_router_cfg_t *cfg, void *dx, void *dw1, void *dw2, float *dw_r,
                           float *dtopk_w, void *ws, size_t ws_bytes, void *stream);
+
+/* ------------------------------------------------------------------ MXFP8
+ *
+ * The guide's second expert precision (section "Expert precision": mxfp8 runs
+ * the two expert stages in MXFP8; parameters stay bf16). MXFP8 is the OCP
+ * Microscaling format: blocks of 32 consecutive elements along a GEMM's
+ * reduction dimension share a power-of-two scale 2^(floor(log2 max|v|) - 8),
+ * stored as E8M0 (one byte, bias 127); elements are FP8 E4M3 (one byte),
+ * rounded to nearest even and saturated to +-448. A matrix [rows, cols] is
+ * stored as codes [rows, cols] and scales [rows, cols/32], row-major.
+ * The MXFP8 calls need H and I multiples of 128 (else MOE_ERR_UNSUPPORTED).
+ */
+
+/*
+ * Quantize a bf16 [rows, cols] matrix (cols a multiple of 32) along its rows:
+ * codes uint8 [rows, cols] (E4M3) and scales uint8 [rows, cols/32] (E8M0).
+ * in and codes 16-byte aligned. For the weights, quantize w1 [E*2I, H] and
+ * w2 [E*H, I] once per weight update and keep the result (the guide's
+ * weight-quant cache); x is quantized every step (moe_forward_mx does it).
+ */
+moe_status_t moe_mx_quantize(const void *in, int64_t rows, int64_t cols, void *codes, void *scales,
+                             void *stream);
+
+/*
+ * The dispatch of the MXFP8 path, fused into the quantization of x: routed row
+ * r of the metadata (token t = perm_slot[r] / k) gets MXFP8 codes and scales of
+ * x[t,:] in the workspace (x_codes [T*k, H], x_scales [T*k, H/32], routed
+ * order), so stage 1 reads whole tiles. x bf16 [T,H]. Needs the metadata of
+ * moe_routing_metadata in ws and flags containing MOE_SHAPE_MXFP8.
+ */
+moe_status_t moe_mx_quantize_dispatch(const void *x, const moe_shape_t *shape, void *ws, size_t ws_bytes,
+                                      void *stream);
+
+/*
+ * Stage 1 in MXFP8 over the dispatched rows of moe_mx_quantize_dispatch: for
+ * routed row r of expert e,
+ *   h = X(x)[r,:] . X(w1)[e]^T (fp32 accumulate from E4M3 products scaled per block)
+ *   a[r, i] = silu(h[i]) * h[I + i], then quantized per 32 columns of i
+ * w1_codes / w1_scales [E,2I,H] / [E,2I,H/32]; a_codes / a_scales [T*k, I] /
+ * [T*k, I/32] (outputs, routed order).
+ */
+moe_status_t moe_dispatch_gemm1_mx(const void *w1_codes, const void *w1_scales, const moe_shape_t *shape,
+                                   void *a_codes, void *a_scales, void *ws, size_t ws_bytes, void *stream);
+
+/*
+ * Stage 2 in MXFP8: o[r,:] = X(a)[r,:] . X(w2)[e]^T, y[t,:] = sum_j topk_w[t,j] o[row_of[t*k+j],:]
+ * (bf16 y, fp32 sum). w2_codes / w2_scales [E,H,I] / [E,H,I/32].
+ */
+moe_status_t moe_swiglu_gemm2_combine_mx(const void *a_codes, const void *a_scales, const float *topk_w,
+                                         const void *w2_codes, const void *w2_scales,
+                                         const moe_shape_t *shape, void *y, void *ws, size_t ws_bytes,
+                                         void *stream);
+
+/*
+ * One-shot MXFP8 expert path: routing metadata, the quantizing dispatch of x,
+ * stage 1, stage 2. Needs a workspace sized with flags containing MOE_SHAPE_MXFP8.
+ */
+moe_status_t moe_forward_mx(const void *x, const int32_t *topk_idx, const float *topk_w,
+                            const void *w1_codes, const void *w1_scales, const void *w2_codes,
+                            const void *w2_scales, const moe_shape_t *shape, void *y, void *ws,
+                            size_t ws_bytes, void *stream);
 
 /*
  * Wait for `stream`, then read and clear the workspace error word into *code.

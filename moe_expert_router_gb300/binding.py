@@ -24,6 +24,7 @@ DEVERR_WAIT_TIMEOUT = 0x2
 SCORE_SOFTMAX = 0
 SCORE_SIGMOID = 1
 SHAPE_TRAINING = 0x1
+SHAPE_MXFP8 = 0x2
 
 
 class MoEError(RuntimeError):
@@ -46,7 +47,8 @@ class RouterCfg(ctypes.Structure):
 class WsLayout(ctypes.Structure):
     _fields_ = [(n, ctypes.c_size_t) for n in
                 ("err", "counts", "offsets", "mt_prefix", "perm_slot", "row_of", "meta", "router", "a",
-                 "obuf", "dh", "aw", "dtw_part", "dlogits", "total")]
+                 "obuf", "dh", "aw", "dtw_part", "dlogits", "x_codes", "x_scales", "a_codes", "a_scales",
+                 "total")]
 
 
 # name -> argument types (all return moe_status_t unless listed in _RESTYPES)
@@ -77,6 +79,11 @@ _SIG = {
     "moe_backward_stage1_weight": [_P, ctypes.POINTER(Shape), _P, _P, ctypes.c_size_t, _P],
     "moe_backward": [_P, _P, _P, _P, _P, _P, _P, _P, _P, ctypes.POINTER(Shape),
                      ctypes.POINTER(RouterCfg), _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P],
+    "moe_mx_quantize": [_P, ctypes.c_int64, ctypes.c_int64, _P, _P, _P],
+    "moe_mx_quantize_dispatch": [_P, ctypes.POINTER(Shape), _P, ctypes.c_size_t, _P],
+    "moe_dispatch_gemm1_mx": [_P, _P, ctypes.POINTER(Shape), _P, _P, _P, ctypes.c_size_t, _P],
+    "moe_swiglu_gemm2_combine_mx": [_P, _P, _P, _P, _P, ctypes.POINTER(Shape), _P, _P, ctypes.c_size_t, _P],
+    "moe_forward_mx": [_P, _P, _P, _P, _P, _P, _P, ctypes.POINTER(Shape), _P, _P, ctypes.c_size_t, _P],
     "moe_get_device_error": [_P, ctypes.POINTER(ctypes.c_int32), _P],
     "moe_status_string": [ctypes.c_int],
     "moe_kernel_launch_count": [],
@@ -126,8 +133,9 @@ def _stream(stream, like):
     return ctypes.c_void_p(stream.cuda_stream)
 
 
-def shape(T, H, I, E, k, training=False) -> Shape:
-    return Shape(int(T), int(H), int(I), int(E), int(k), SHAPE_TRAINING if training else 0)
+def shape(T, H, I, E, k, training=False, mxfp8=False) -> Shape:
+    flags = (SHAPE_TRAINING if training else 0) | (SHAPE_MXFP8 if mxfp8 else 0)
+    return Shape(int(T), int(H), int(I), int(E), int(k), flags)
 
 
 def router_cfg(score="softmax", normalize=True, scale=1.0, n_group=1, topk_group=1,
@@ -261,6 +269,39 @@ def moe_backward(x, topk_idx, topk_w, w1, w2, h, dy, shp, dx, dw1, dw2, ws, w_r=
         _ptr(x), _ptr(w_r), _ptr(logits), _ptr(topk_idx), _ptr(topk_w), _ptr(w1), _ptr(w2), _ptr(h),
         _ptr(dy), ctypes.byref(shp), _cfg_ref(cfg), _ptr(dx), _ptr(dw1), _ptr(dw2), _ptr(dw_r),
         _ptr(dtopk_w), _ptr(ws), _nbytes(ws), _stream(stream, ws)))
+
+
+def moe_mx_quantize(t, codes, scales, stream=None):
+    """MXFP8 quantization of a bf16 tensor along its last dimension (multiple of 32):
+    codes uint8 of the same shape, scales uint8 [..., cols / 32]."""
+    cols = t.shape[-1]
+    rows = t.numel() // cols if cols else 0
+    _check("moe_mx_quantize", load().moe_mx_quantize(_ptr(t), rows, cols, _ptr(codes), _ptr(scales),
+                                                     _stream(stream, t)))
+
+
+def moe_mx_quantize_dispatch(x, shp, ws, stream=None):
+    """The MXFP8 dispatch: x quantized into the workspace in routed-row order."""
+    _check("moe_mx_quantize_dispatch", load().moe_mx_quantize_dispatch(
+        _ptr(x), ctypes.byref(shp), _ptr(ws), _nbytes(ws), _stream(stream, ws)))
+
+
+def moe_dispatch_gemm1_mx(w1q, w1s, shp, aq, as_, ws, stream=None):
+    _check("moe_dispatch_gemm1_mx", load().moe_dispatch_gemm1_mx(
+        _ptr(w1q), _ptr(w1s), ctypes.byref(shp), _ptr(aq), _ptr(as_), _ptr(ws), _nbytes(ws),
+        _stream(stream, ws)))
+
+
+def moe_swiglu_gemm2_combine_mx(aq, as_, topk_w, w2q, w2s, shp, y, ws, stream=None):
+    _check("moe_swiglu_gemm2_combine_mx", load().moe_swiglu_gemm2_combine_mx(
+        _ptr(aq), _ptr(as_), _ptr(topk_w), _ptr(w2q), _ptr(w2s), ctypes.byref(shp), _ptr(y), _ptr(ws),
+        _nbytes(ws), _stream(stream, ws)))
+
+
+def moe_forward_mx(x, topk_idx, topk_w, w1q, w1s, w2q, w2s, shp, y, ws, stream=None):
+    _check("moe_forward_mx", load().moe_forward_mx(
+        _ptr(x), _ptr(topk_idx), _ptr(topk_w), _ptr(w1q), _ptr(w1s), _ptr(w2q), _ptr(w2s),
+        ctypes.byref(shp), _ptr(y), _ptr(ws), _nbytes(ws), _stream(stream, ws)))
 
 
 def moe_get_device_error(ws, stream=None) -> int:

@@ -55,6 +55,7 @@
 #pragma once
 
 #include "internal.cuh"
+#include "mx.cuh"
 #include "ptx.cuh"
 
 namespace moe {
@@ -83,12 +84,16 @@ constexpr uint64_t kDrainLimitNs = 10000000ull;  // 10 ms
 enum Mode : int {
     kStage1 = 0, kStage2 = 1, kRouter = 2,
     kBwdDA = 3, kBwdDX = 4, kBwdDW2 = 5, kBwdDW1 = 6,
-    kStage1SaveH = 7            // stage 1 that also stores h for the backward
+    kStage1SaveH = 7,           // stage 1 that also stores h for the backward
+    kStage1Mx = 8,              // stage 1 in MXFP8: E4M3 x and w1, a quantized in the epilogue
+    kStage2Mx = 9               // stage 2 in MXFP8: E4M3 a and w2
 };
 
-template <int MODE> constexpr bool kIsStage1 = MODE == kStage1 || MODE == kStage1SaveH;
-// A is filled by the K-major row gather (token rows of x or dY)
-template <int MODE> constexpr bool kGatherK = kIsStage1<MODE> || MODE == kBwdDA;
+template <int MODE> constexpr bool kIsMx = MODE == kStage1Mx || MODE == kStage2Mx;
+template <int MODE> constexpr bool kIsStage1 = MODE == kStage1 || MODE == kStage1SaveH || MODE == kStage1Mx;
+// A is filled by the K-major row gather (token rows of x or dY); stage 1 in
+// MXFP8 reads x rows already dispatched into routed order by its quantization
+template <int MODE> constexpr bool kGatherK = MODE == kStage1 || MODE == kStage1SaveH || MODE == kBwdDA;
 // the MN-major row gather fills A (dW2: dY rows) or B (dW1: x rows)
 template <int MODE> constexpr bool kGatherMnA = MODE == kBwdDW2;
 template <int MODE> constexpr bool kGatherMnB = MODE == kBwdDW1;
@@ -96,10 +101,25 @@ template <int MODE> constexpr bool kGathers = kGatherK<MODE> || kGatherMnA<MODE>
 template <int MODE> constexpr bool kAMn = MODE == kBwdDW2 || MODE == kBwdDW1;
 template <int MODE> constexpr bool kBMn = MODE >= kBwdDA && MODE <= kBwdDW1;
 template <int MODE> constexpr bool kWeightGrad = MODE == kBwdDW2 || MODE == kBwdDW1;
+// warps 10..13: row gathers, and in the MXFP8 modes the scale factors
+template <int MODE> constexpr bool kHelpers = kGathers<MODE> || kIsMx<MODE>;
+// accumulator columns of one 128-row half (a unit's output columns): 2 x 96
+// (gate, up) in stage 1 MXFP8, 224 in stage 2 MXFP8, else 256; the MXFP8 modes
+// keep the rest of tensor memory for per-stage scale factors
+template <int MODE> constexpr int kUnitN = MODE == kStage1Mx ? 192 : (MODE == kStage2Mx ? 224 : BN);
+// K elements per pipeline stage (128-byte rows either way)
+template <int MODE> constexpr int kStageK = kIsMx<MODE> ? 128 : BK;
+template <int MODE> constexpr int kElemBytes = kIsMx<MODE> ? 1 : 2;
+// scale factors of stage s: columns kSfBase + 16 s + [0, 4) A rows 0..127,
+// [4, 8) A rows 128..255, [8, 8 + N/32) B rows
+template <int MODE> constexpr int kSfBase = 2 * kUnitN<MODE>;
+constexpr int kSfStride = 16;
+static_assert(2 * 224 + STAGES * kSfStride <= 512, "MXFP8 scale factors must fit in tensor memory");
+static_assert(BK == 64, "the MXFP8 modes share the 128-byte stage rows of BK = 64");
 
-// warps: 0 scheduler + TMA producer, 1 MMA issuer, 2..9 epilogue, 10..13 gather
+// warps: 0 scheduler + TMA producer, 1 MMA issuer, 2..9 epilogue, 10..13 helpers
 template <int MODE>
-constexpr int kNumThreads = 64 + EPI_THREADS + (kGathers<MODE> ? GATHER_THREADS : 0);
+constexpr int kNumThreads = 64 + EPI_THREADS + (kHelpers<MODE> ? GATHER_THREADS : 0);
 
 template <int MODE>
 constexpr uint32_t kIdesc = idesc_bf16_f32(BM, BN) | (kAMn<MODE> ? (1u << 15) : 0u) |
@@ -146,6 +166,9 @@ struct GemmArgs {
     __nv_bfloat16 *out2, *out3; // kStage1SaveH: h gate / up halves; dA: dH up half, w a
     float *logits_part;         // router
     float *dtw_part;            // dA: [n_tiles, R] partial routing-weight gradients
+    const uint8_t *sfa;         // MXFP8: E8M0 scales of the A rows (x per token, or a per routed row)
+    const uint8_t *sfb;         // MXFP8: E8M0 scales of the weight rows
+    uint8_t *out_sf;            // stage 1 MXFP8: scales of a [R, I / 32]
     int E, k, K;
     int src_cols;               // valid columns of a gathered source row
     int n_out;                  // valid output columns
@@ -209,7 +232,7 @@ __device__ __forceinline__ Unit decode_unit(int u, const GemmArgs &g) {
         t.row0 = g.offsets[lo] + m * UM;
         t.rows = min(UM, g.counts[lo] - m * UM);
         t.kb0 = 0;
-        t.kb1 = (g.K + BK - 1) / BK;
+        t.kb1 = (g.K + kStageK<MODE> - 1) / kStageK<MODE>;
         t.split = 0;
     }
     return t;
@@ -298,6 +321,47 @@ __device__ __forceinline__ void scaled_piece(uint32_t tacc, int c, float w, uint
         pk[i] = pack_bf16x2(w * __uint_as_float(v[2 * i]), w * __uint_as_float(v[2 * i + 1]));
 }
 
+// MXFP8 scale factors of one stage, this thread's lane of the 16 scale
+// columns: column j < 8 = A row 32 j + lane (j >= 4: the second half), column
+// 8 + j = B row 32 j + lane. Each word holds the four E8M0 codes of the stage's
+// K steps. Offsets are byte offsets of a row's scales (-1: none). The words of
+// the next stage are loaded while the current one is consumed, so the global
+// latency stays off the pipeline's critical path.
+__device__ __forceinline__ void load_scales(const GemmArgs &g, int kb, bool any, const int64_t (&a_off)[8],
+                                            const int64_t (&b_off)[8], uint32_t (&r)[16]) {
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+        r[j] = (any && a_off[j] >= 0) ? __ldg(reinterpret_cast<const uint32_t *>(g.sfa + a_off[j]) + kb) : 0u;
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+        r[8 + j] = (any && b_off[j] >= 0) ? __ldg(reinterpret_cast<const uint32_t *>(g.sfb + b_off[j]) + kb) : 0u;
+}
+
+// Byte offsets of the scale rows a helper thread writes for unit t (see write_scales).
+template <int MODE>
+__device__ __forceinline__ void scale_rows(const GemmArgs &g, const Unit &t, int lane, int64_t (&a_off)[8],
+                                           int64_t (&b_off)[8]) {
+    const int64_t ld = g.K / 32;                      // scale bytes per row (A rows in routed order)
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        const int r = 32 * j + lane;
+        a_off[j] = (r < t.rows) ? static_cast<int64_t>(t.row0 + r) * ld : -1;
+    }
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        b_off[j] = -1;
+        if constexpr (MODE == kStage1Mx) {
+            // gate rows, then the matching up rows, of the unit's 96-column slice
+            const int c = t.n * 96 + 32 * (j % 3) + lane;
+            if (j < 6 && c < g.n_out)
+                b_off[j] = (static_cast<int64_t>(t.e) * g.b_rows + c + (j >= 3 ? g.half : 0)) * ld;
+        } else {
+            const int c = t.n * kUnitN<MODE> + 32 * j + lane;
+            if (j < 7 && c < g.n_out) b_off[j] = (static_cast<int64_t>(t.e) * g.b_rows + c) * ld;
+        }
+    }
+}
+
 // ---------------------------------------------------------------- the kernel
 
 template <int MODE>
@@ -315,14 +379,14 @@ tc_gemm_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs g) {
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
             // gathering modes: the producer's expect_tx arrival plus one per gather thread
-            mbar_init(smem_addr(&sm.full[s]), kGathers<MODE> ? 1 + GATHER_THREADS : 1);
+            mbar_init(smem_addr(&sm.full[s]), kHelpers<MODE> ? 1 + GATHER_THREADS : 1);
             mbar_init(smem_addr(&sm.empty[s]), 1);
         }
         mbar_init(smem_addr(&sm.acc_full), 1);
         mbar_init(smem_addr(&sm.acc_empty), EPI_THREADS);
         for (int s = 0; s < UQ; ++s) {
             mbar_init(smem_addr(&sm.uq_full[s]), 1);
-            mbar_init(smem_addr(&sm.uq_empty[s]), 1 + EPI_WARPS + (kGathers<MODE> ? GATHER_WARPS : 0));
+            mbar_init(smem_addr(&sm.uq_empty[s]), 1 + EPI_WARPS + (kHelpers<MODE> ? GATHER_WARPS : 0));
         }
         mbar_init(smem_addr(&sm.drain), 1);
         sm.abort = 0;
@@ -366,9 +430,9 @@ tc_gemm_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs g) {
             const Unit t = decode_unit<MODE>(u, g);
             const bool two = t.rows > BM;            // second half present
             uint32_t tx_bytes;
-            if constexpr (kGatherK<MODE> || kGatherMnA<MODE>) tx_bytes = B_BYTES;    // A gathered
+            if constexpr (kGatherK<MODE> || kGatherMnA<MODE>) tx_bytes = kUnitN<MODE> * 128;    // A gathered
             else if constexpr (kGatherMnB<MODE>) tx_bytes = two ? A_BYTES : A_HALF_BYTES;  // B gathered
-            else tx_bytes = (two ? A_BYTES : A_HALF_BYTES) + B_BYTES;
+            else tx_bytes = (two ? A_BYTES : A_HALF_BYTES) + kUnitN<MODE> * 128;
             for (int kb = t.kb0; kb < t.kb1; ++kb) {
                 bool e_ok = true;
                 if (lane == 0) e_ok = mbar_wait(smem_addr(&sm.empty[stage]), phase ^ 1u, abort_flag, g.err);
@@ -380,13 +444,20 @@ tc_gemm_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs g) {
                 if (lane == 0) {
                     mbar_arrive_expect_tx(full, tx_bytes);
                     if constexpr (kIsStage1<MODE>) {
-                        const int row = t.e * g.b_rows + t.n * (BN / 2);
-                        tma_load_2d(sb, &maps.b, kb * BK, row, full);                        // gate rows
-                        tma_load_2d(sb + B_BYTES / 2, &maps.b, kb * BK, row + g.half, full);  // up rows
-                    } else if constexpr (MODE == kStage2) {
-                        tma_load_2d(sa, &maps.a, kb * BK, t.row0, full);
-                        if (two) tma_load_2d(sa + A_HALF_BYTES, &maps.a, kb * BK, t.row0 + BM, full);
-                        tma_load_2d(sb, &maps.b, kb * BK, t.e * g.b_rows + t.n * BN, full);
+                        constexpr int hn = kUnitN<MODE> / 2;                                 // gate (= up) rows
+                        const int row = t.e * g.b_rows + t.n * hn;
+                        const int kx = kb * kStageK<MODE>;
+                        if constexpr (MODE == kStage1Mx) {                                  // dispatched x rows
+                            tma_load_2d(sa, &maps.a, kx, t.row0, full);
+                            if (two) tma_load_2d(sa + A_HALF_BYTES, &maps.a, kx, t.row0 + BM, full);
+                        }
+                        tma_load_2d(sb, &maps.b, kx, row, full);                            // gate rows
+                        tma_load_2d(sb + hn * 128, &maps.b, kx, row + g.half, full);        // up rows
+                    } else if constexpr (MODE == kStage2 || MODE == kStage2Mx) {
+                        const int kx = kb * kStageK<MODE>;
+                        tma_load_2d(sa, &maps.a, kx, t.row0, full);
+                        if (two) tma_load_2d(sa + A_HALF_BYTES, &maps.a, kx, t.row0 + BM, full);
+                        tma_load_2d(sb, &maps.b, kx, t.e * g.b_rows + t.n * kUnitN<MODE>, full);
                     } else if constexpr (MODE == kRouter) {
                         const int seg = kb / g.kb_h;              // 0: hi, 1: mid, 2: lo
                         const int kx = (kb - seg * g.kb_h) * BK;
@@ -455,14 +526,29 @@ tc_gemm_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs g) {
                     tc_fence_after();
                     const uint32_t sa = smem_addr(sm.a[stage]);
                     const uint32_t sb = smem_addr(sm.b[stage]);
+                    if constexpr (kIsMx<MODE>) {
+                        // four K = 32 steps; the scale words of this stage hold one byte per step
+                        const uint32_t sf = tmem_base + kSfBase<MODE> + stage * kSfStride;
 #pragma unroll
-                    for (int kk = 0; kk < BK / UMMA_K; ++kk) {
-                        const uint32_t acc = (kb > t.kb0 || kk > 0) ? 1u : 0u;
-                        const uint64_t bdesc = operand_desc<kBMn<MODE>>(sb, kk);
-                        mma_bf16(tmem_base, operand_desc<kAMn<MODE>>(sa, kk), bdesc, kIdesc<MODE>, acc);
-                        if (two)
-                            mma_bf16(tmem_base + BN, operand_desc<kAMn<MODE>>(sa + A_HALF_BYTES, kk), bdesc,
-                                     kIdesc<MODE>, acc);
+                        for (int kk = 0; kk < 4; ++kk) {
+                            const uint32_t acc = (kb > t.kb0 || kk > 0) ? 1u : 0u;
+                            const uint32_t idesc = idesc_mxf8(BM, kUnitN<MODE>, kk);
+                            const uint64_t bdesc = smem_desc_swizzled<128>(sb + kk * 32);
+                            mma_mxf8(tmem_base, smem_desc_swizzled<128>(sa + kk * 32), bdesc, idesc, sf, sf + 8, acc);
+                            if (two)
+                                mma_mxf8(tmem_base + kUnitN<MODE>, smem_desc_swizzled<128>(sa + A_HALF_BYTES + kk * 32),
+                                         bdesc, idesc, sf + 4, sf + 8, acc);
+                        }
+                    } else {
+#pragma unroll
+                        for (int kk = 0; kk < BK / UMMA_K; ++kk) {
+                            const uint32_t acc = (kb > t.kb0 || kk > 0) ? 1u : 0u;
+                            const uint64_t bdesc = operand_desc<kBMn<MODE>>(sb, kk);
+                            mma_bf16(tmem_base, operand_desc<kAMn<MODE>>(sa, kk), bdesc, kIdesc<MODE>, acc);
+                            if (two)
+                                mma_bf16(tmem_base + BN, operand_desc<kAMn<MODE>>(sa + A_HALF_BYTES, kk), bdesc,
+                                         kIdesc<MODE>, acc);
+                        }
                     }
                     mma_commit(smem_addr(&sm.empty[stage]));   // frees the smem stage
                     any = true;
@@ -486,8 +572,9 @@ tc_gemm_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs g) {
         const int half = (warp - 2) >> 2;           // accumulator (row half) of this warp
         const int row = half * BM + quad * 32 + lane;   // unit row
         const uint32_t tacc = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) +
-                              static_cast<uint32_t>(half * BN);
+                              static_cast<uint32_t>(half * kUnitN<MODE>);
         const uint32_t buf = smem_addr(sm.stage_out[warp - 2]);
+        uint32_t boxes = 0;                         // 32 x 32 boxes stored so far (ping-pong halves)
         int q = 0;
         uint32_t acc_phase = 0, qphase = 0;
         while (true) {
@@ -507,7 +594,7 @@ tc_gemm_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs g) {
             const Unit t = decode_unit<MODE>(u, g);
             const bool valid = row < t.rows;
             float w = 1.0f;                             // routing weight of the row's slot
-            if constexpr (MODE == kStage2 || MODE == kBwdDA) {
+            if constexpr (MODE == kStage2 || MODE == kBwdDA || MODE == kStage2Mx) {
                 w = valid ? g.topk_w[g.perm_slot[t.row0 + row]] : 0.0f;
             }
             if (lane == 0) ok = mbar_wait(smem_addr(&sm.acc_full), acc_phase, abort_flag, g.err);
@@ -517,7 +604,59 @@ tc_gemm_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs g) {
             const int slab0 = half * BM + quad * 32;    // first unit row of this warp
             const bool full_slab = slab0 + 32 <= t.rows;
             if (t.rows > half * BM) {                   // this half was computed
-                if constexpr (kIsStage1<MODE> || MODE == kStage2 || MODE == kBwdDX) {
+                if constexpr (MODE == kStage1Mx) {
+                    // SwiGLU of 32 gate / up columns, then the MXFP8 quantization of
+                    // that 32-column block of a: 32 E4M3 codes and one E8M0 scale
+                    const int col0 = t.n * (kUnitN<MODE> / 2);
+                    const int64_t r = t.row0 + row;
+#pragma unroll 1
+                    for (int c = 0; c < kUnitN<MODE> / 2; c += 32) {
+                        if (col0 + c >= g.n_out) break;
+                        uint32_t gv[32], uv[32];
+                        tmem_ld32(tacc + c, gv);
+                        tmem_ld32(tacc + kUnitN<MODE> / 2 + c, uv);
+                        tmem_wait_ld();
+                        tmem_reg_fence(gv);
+                        tmem_reg_fence(uv);
+                        float av[32];
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) av[i] = silu_mul(__uint_as_float(gv[i]), __uint_as_float(uv[i]));
+                        uint32_t q[8];
+                        const uint32_t sc = mx_quantize32(av, q);
+                        if (valid) {
+                            uint4 *dst = reinterpret_cast<uint4 *>(reinterpret_cast<uint8_t *>(g.out) + r * g.n_out + col0 + c);
+                            dst[0] = make_uint4(q[0], q[1], q[2], q[3]);
+                            dst[1] = make_uint4(q[4], q[5], q[6], q[7]);
+                            g.out_sf[r * (g.n_out / 32) + (col0 + c) / 32] = static_cast<uint8_t>(sc);
+                        }
+                    }
+                } else if constexpr (MODE == kStage2Mx) {
+                    // weighted rows into obuf, 32 x 32 boxes (the unit is 224 columns wide)
+                    const int col0 = t.n * kUnitN<MODE>;
+                    const int y = t.row0 + slab0;
+                    __nv_bfloat16 *dst = g.out + static_cast<int64_t>(t.row0 + row) * g.n_out;
+#pragma unroll 1
+                    for (int c = 0; c < kUnitN<MODE>; c += 32) {
+                        const int col = col0 + c;
+                        if (col >= g.n_out) break;
+                        uint32_t pk[16];
+                        scaled_piece(tacc, c, w, pk);
+                        if (full_slab) {
+                            if (lane == 0) bulk_wait_read<1>();   // the box two boxes ago is read out
+                            __syncwarp();
+                            const uint32_t b2 = buf + (boxes++ & 1u) * 2048;
+                            stage_row32(b2, lane, pk);
+                            fence_proxy_async_smem();
+                            __syncwarp();
+                            if (lane == 0) {
+                                tma_store_2d(&maps.out, b2, col, y);
+                                bulk_commit();
+                            }
+                        } else if (valid) {
+                            store_row32(dst + col, g.n_out - col, pk);
+                        }
+                    }
+                } else if constexpr (kIsStage1<MODE> || MODE == kStage2 || MODE == kBwdDX) {
                     // row-grouped outputs: rows t.row0 + row, columns [col0, col0 + ncols)
                     constexpr int ncols = kIsStage1<MODE> ? BN / 2 : BN;
                     const int col0 = t.n * ncols;
@@ -787,12 +926,14 @@ tc_gemm_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs g) {
             const Unit t = decode_unit<MODE>(u, g);
             if constexpr (kGatherK<MODE>) {
                 // K-major A rows: one thread per 16-byte chunk of a row slice; rows past
-                // the unit's count are left as they are (never stored)
+                // the unit's count are left as they are (never stored).
                 constexpr int CHUNKS = ROW_BYTES / 16;                 // per row slice
                 constexpr int RSTEP = GATHER_THREADS / CHUNKS;         // rows per pass
                 constexpr int NROWS = UM / RSTEP;                      // rows per thread
                 const int chunk = gt % CHUNKS;
                 const int rg = gt / CHUNKS;                            // rows rg + RSTEP i
+                const char *srcb = reinterpret_cast<const char *>(g.src);
+                const int64_t ldb = static_cast<int64_t>(g.src_cols) * kElemBytes<MODE>;
                 int tok[NROWS];
 #pragma unroll
                 for (int i = 0; i < NROWS; ++i) {
@@ -804,8 +945,8 @@ tc_gemm_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs g) {
                     if (lane == 0) e_ok = mbar_wait(smem_addr(&sm.empty[stage]), phase ^ 1u, abort_flag, g.err);
                     e_ok = __shfl_sync(0xffffffffu, e_ok, 0);
                     if (!e_ok) { ok = false; break; }
-                    const int col = kb * BK + chunk * 8;
-                    const uint32_t nbytes = col < g.K ? 16u : 0u;   // zero-fill the K tail
+                    const int colb = kb * ROW_BYTES + chunk * 16;
+                    const uint32_t nbytes = colb < g.K * kElemBytes<MODE> ? 16u : 0u;   // zero-fill the K tail
                     const uint32_t sa = smem_addr(sm.a[stage]);
 #pragma unroll
                     for (int i = 0; i < NROWS; ++i) {
@@ -813,8 +954,7 @@ tc_gemm_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs g) {
                             const int r = rg + RSTEP * i;
                             const uint32_t dst = sa + (r >> 7) * A_HALF_BYTES +
                                                  swizzled_chunk<ROW_BYTES>(r & (BM - 1), chunk);
-                            cp_async_16(dst, g.src + static_cast<int64_t>(tok[i]) * g.src_cols + (nbytes ? col : 0),
-                                        nbytes);
+                            cp_async_16(dst, srcb + static_cast<int64_t>(tok[i]) * ldb + (nbytes ? colb : 0), nbytes);
                         }
                     }
                     cp_async_commit();
@@ -870,6 +1010,26 @@ tc_gemm_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs g) {
                     pending = stage;
                     if (++stage == STAGES) { stage = 0; phase ^= 1u; }
                 }
+            } else if constexpr (kIsMx<MODE>) {
+                // A and B arrive through TMA; these warps only write the scale factors
+                int64_t a_off[8], b_off[8];
+                uint32_t sfw[16];
+                scale_rows<MODE>(g, t, lane, a_off, b_off);
+                load_scales(g, t.kb0, t.kb0 < t.kb1, a_off, b_off, sfw);
+                const uint32_t sf_lane = tmem_base + (static_cast<uint32_t>((warp & 3) * 32) << 16) + kSfBase<MODE>;
+                for (int kb = t.kb0; kb < t.kb1; ++kb) {
+                    bool e_ok = true;
+                    if (lane == 0) e_ok = mbar_wait(smem_addr(&sm.empty[stage]), phase ^ 1u, abort_flag, g.err);
+                    e_ok = __shfl_sync(0xffffffffu, e_ok, 0);
+                    if (!e_ok) { ok = false; break; }
+                    tc_fence_after();
+                    tmem_st16(sf_lane + stage * kSfStride, sfw);
+                    load_scales(g, kb + 1, kb + 1 < t.kb1, a_off, b_off, sfw);
+                    tmem_wait_st();
+                    tc_fence_before();
+                    mbar_arrive(smem_addr(&sm.full[stage]));
+                    if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+                }
             }
             if (pending >= 0) {                       // signal the unit's last stage
                 cp_async_wait<0>();
@@ -914,6 +1074,9 @@ inline GemmArgs grouped_args(const GemmLaunch &p) {
     g.out2 = p.out2;
     g.out3 = p.out3;
     g.dtw_part = p.dtw_part;
+    g.sfa = p.sfa;
+    g.sfb = p.sfb;
+    g.out_sf = p.out_sf;
     g.E = p.E;
     g.k = p.k;
     g.K = p.K;

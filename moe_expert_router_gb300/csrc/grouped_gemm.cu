@@ -48,6 +48,7 @@ cudaError_t setup_gemm_kernels() {
     if (e == cudaSuccess) e = set_gemm_smem<kStage2>();
     if (e == cudaSuccess) e = set_gemm_smem<kRouter>();
     if (e == cudaSuccess) e = setup_bwd_gemm_kernels();
+    if (e == cudaSuccess) e = setup_mx_gemm_kernels();
     return e;
 }
 

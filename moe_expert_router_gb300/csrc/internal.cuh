@@ -135,6 +135,8 @@ struct GemmLaunch {
     __nv_bfloat16 *out;         // row-grouped output (masked stores of partial slabs)
     __nv_bfloat16 *out2, *out3; // stage 1 with h: h gate / up halves; dA: dH up half, w a
     float *dtw_part;            // dA: [ceil(I / 256), R]
+    const uint8_t *sfa, *sfb;   // MXFP8: E8M0 scales of the A rows and of the weight rows
+    uint8_t *out_sf;            // stage 1 MXFP8: E8M0 scales of a [R, I / 32]
     int E, k;
     int K;                      // reduction length of the row-grouped modes
     int src_cols;               // columns of a gathered source row
@@ -215,6 +217,25 @@ cudaError_t launch_zero_tail_rows(__nv_bfloat16 *dh, __nv_bfloat16 *aw, const in
 cudaError_t launch_router_dlogits(const RouterBwdLaunch &p, cudaStream_t st);
 cudaError_t launch_router_dwr(const RouterBwdLaunch &p, cudaStream_t st);
 cudaError_t launch_combine_bwd(const CombineBwdLaunch &p, cudaStream_t st);
+
+// MXFP8 (grouped_gemm_mx.cu): quantization of a bf16 [rows, cols] matrix along its
+// rows (cols % 32 == 0) into E4M3 codes and E8M0 block scales; the two MXFP8
+// expert stages (stage 1: out = a codes, out_sf = a scales; stage 2 as kStage2).
+cudaError_t launch_mx_quantize(const __nv_bfloat16 *in, int64_t rows, int64_t cols, uint8_t *codes,
+                               uint8_t *scales, cudaStream_t st);
+// The MXFP8 dispatch: quantize the x rows of routed rows [0, *routed) (token
+// perm_slot[r] / k) into codes [R, cols] / scales [R, cols / 32], routed order.
+cudaError_t launch_mx_quantize_dispatch(const __nv_bfloat16 *x, const int32_t *perm_slot, const int32_t *routed,
+                                        int k, int64_t R, int64_t cols, uint8_t *codes, uint8_t *scales,
+                                        cudaStream_t st);
+cudaError_t launch_gemm1_mx(const GemmLaunch &p, cudaStream_t st);
+cudaError_t launch_gemm2_mx(const GemmLaunch &p, cudaStream_t st);
+cudaError_t setup_mx_gemm_kernels();
+
+// uint8 tensor [rows, inner] (e.g. E4M3 codes) with a box_inner x box_rows box,
+// 128-byte swizzle (box_inner = 128).
+bool encode_u8_2d(CUtensorMap *map, const void *base, uint64_t inner, uint64_t rows, uint32_t box_inner,
+                  uint32_t box_rows);
 
 // Backward GEMMs (grouped_gemm_bwd.cu).
 cudaError_t launch_bwd_da(const GemmLaunch &p, cudaStream_t st);

@@ -56,7 +56,7 @@ bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 moe_status_t check_shape(const moe_shape_t *s) {
     if (s == nullptr) return MOE_ERR_INVALID_ARG;
     if (s->T < 0 || s->H <= 0 || s->I <= 0 || s->E <= 0 || s->k <= 0 ||
-        (s->flags & ~MOE_SHAPE_TRAINING) != 0)
+        (s->flags & ~(MOE_SHAPE_TRAINING | MOE_SHAPE_MXFP8)) != 0)
         return MOE_ERR_INVALID_ARG;
     if (s->k > 32 || s->k > s->E || s->E > 1024) return MOE_ERR_UNSUPPORTED;
     if (s->H % 8 != 0 || s->I % 8 != 0) return MOE_ERR_UNSUPPORTED;
@@ -89,6 +89,14 @@ moe_ws_layout_t make_layout(const moe_shape_t &s) {
     } else {
         L.dh = L.aw = L.dtw_part = L.dlogits = off;
     }
+    if (s.flags & MOE_SHAPE_MXFP8) {
+        L.x_codes = off;  off = align256(off + R * H);
+        L.x_scales = off; off = align256(off + R * (H / 32));
+        L.a_codes = off;  off = align256(off + R * I);
+        L.a_scales = off; off = align256(off + R * (I / 32));
+    } else {
+        L.x_codes = L.x_scales = L.a_codes = L.a_scales = off;
+    }
     L.total = off;
     return L;
 }
@@ -104,7 +112,8 @@ struct Ws {
     __nv_bfloat16 *a, *obuf;
     __nv_bfloat16 *dh, *aw;     // training only
     float *dtw_part, *dlogits;  // training only
-    bool training;
+    uint8_t *x_codes, *x_scales, *a_codes, *a_scales;   // MXFP8 only
+    bool training, mxfp8;
 };
 
 Ws carve(void *ws, const moe_shape_t &s) {
@@ -135,6 +144,11 @@ Ws carve(void *ws, const moe_shape_t &s) {
     w.aw = reinterpret_cast<__nv_bfloat16 *>(b + L.aw);
     w.dtw_part = reinterpret_cast<float *>(b + L.dtw_part);
     w.dlogits = reinterpret_cast<float *>(b + L.dlogits);
+    w.mxfp8 = (s.flags & MOE_SHAPE_MXFP8) != 0;
+    w.x_codes = b + L.x_codes;
+    w.x_scales = b + L.x_scales;
+    w.a_codes = b + L.a_codes;
+    w.a_scales = b + L.a_scales;
     return w;
 }
 
@@ -217,6 +231,74 @@ moe_status_t run_gemm2(const moe_shape_t &s, const void *a, const float *topk_w,
     p.n_tile = kBN;
     p.b_rows = static_cast<int>(s.H);
     moe_status_t r = cuda_status(launch_gemm2_scatter(p, st));
+    if (r != MOE_OK) return r;
+    CombineLaunch c;
+    c.obuf = w.obuf;
+    c.row_of = w.row_of;
+    c.y = static_cast<__nv_bfloat16 *>(y);
+    c.T = static_cast<int>(s.T);
+    c.H = static_cast<int>(s.H);
+    c.k = s.k;
+    return cuda_status(launch_combine(c, st));
+}
+
+// Stage 1 in MXFP8: the dispatched E4M3 x rows (routed order, in ws) and E4M3
+// w1 through TMA, scales into tensor memory per stage; the epilogue quantizes a
+// per 32 columns.
+moe_status_t run_gemm1_mx(const moe_shape_t &s, const void *w1q, const void *w1s, void *aq, void *as, const Ws &w,
+                          const DeviceState &d, cudaStream_t st) {
+    const uint64_t R = static_cast<uint64_t>(s.T) * s.k;
+    CUtensorMap tm_x, tm_w1;
+    if (!encode_u8_2d(&tm_x, w.x_codes, s.H, R, 128, 128) ||
+        !encode_u8_2d(&tm_w1, w1q, s.H, static_cast<uint64_t>(s.E) * 2 * s.I, 128, 96))
+        return MOE_ERR_CUDA;
+    GemmLaunch p = base_launch(s, w, d);
+    p.tm_a = &tm_x;
+    p.tm_b = &tm_w1;
+    p.tm_out = &tm_w1;
+    p.sfa = w.x_scales;
+    p.sfb = static_cast<const uint8_t *>(w1s);
+    p.sched = w.sched1;
+    p.out = static_cast<__nv_bfloat16 *>(aq);             // E4M3 codes [R, I]
+    p.out_sf = static_cast<uint8_t *>(as);
+    p.K = static_cast<int>(s.H);
+    p.n_out = static_cast<int>(s.I);
+    p.n_tile = 96;
+    p.b_rows = static_cast<int>(2 * s.I);
+    p.half = static_cast<int>(s.I);
+    return cuda_status(launch_gemm1_mx(p, st));
+}
+
+// The MXFP8 dispatch: x quantized straight into routed order (needs the metadata).
+moe_status_t run_mx_dispatch(const moe_shape_t &s, const void *x, const Ws &w, cudaStream_t st) {
+    return cuda_status(launch_mx_quantize_dispatch(static_cast<const __nv_bfloat16 *>(x), w.perm_slot,
+                                                   w.offsets + s.E, s.k, s.T * s.k, s.H, w.x_codes, w.x_scales, st));
+}
+
+// Stage 2 in MXFP8: E4M3 a and w2 through TMA, weighted rows into obuf, then the k-way combine.
+moe_status_t run_gemm2_mx(const moe_shape_t &s, const void *aq, const void *as, const float *topk_w,
+                          const void *w2q, const void *w2s, void *y, const Ws &w, const DeviceState &d,
+                          cudaStream_t st) {
+    const uint64_t R = static_cast<uint64_t>(s.T) * s.k;
+    CUtensorMap tm_a, tm_w2, tm_out;
+    if (!encode_u8_2d(&tm_a, aq, s.I, R, 128, 128) ||
+        !encode_u8_2d(&tm_w2, w2q, s.I, static_cast<uint64_t>(s.E) * s.H, 128, 224) ||
+        !encode_bf16_2d(&tm_out, w.obuf, s.H, R, 32, 32))
+        return MOE_ERR_CUDA;
+    GemmLaunch p = base_launch(s, w, d);
+    p.tm_a = &tm_a;
+    p.tm_b = &tm_w2;
+    p.tm_out = &tm_out;
+    p.sfa = static_cast<const uint8_t *>(as);
+    p.sfb = static_cast<const uint8_t *>(w2s);
+    p.sched = w.sched2;
+    p.topk_w = topk_w;
+    p.out = w.obuf;
+    p.K = static_cast<int>(s.I);
+    p.n_out = static_cast<int>(s.H);
+    p.n_tile = 224;
+    p.b_rows = static_cast<int>(s.H);
+    moe_status_t r = cuda_status(launch_gemm2_mx(p, st));
     if (r != MOE_OK) return r;
     CombineLaunch c;
     c.obuf = w.obuf;
@@ -414,8 +496,8 @@ namespace {
 // bf16 tensor of rank 2 or 3 (dims[0] contiguous, byte strides for the others)
 // with a box_inner x box_rows (x 1) box, zero fill out of bounds, and the
 // swizzle span equal to the box row (64 or 128 bytes).
-bool encode_bf16(CUtensorMap *map, const void *base, int rank, const cuuint64_t *dims,
-                 const cuuint64_t *byte_strides, uint32_t box_inner, uint32_t box_rows) {
+// Looks up cuTensorMapEncodeTiled once; false when the driver lacks it.
+bool encode_ready() {
     std::call_once(g_encode_once, [] {
         void *fn = nullptr;
         cudaDriverEntryPointQueryResult q;
@@ -425,7 +507,12 @@ bool encode_bf16(CUtensorMap *map, const void *base, int rank, const cuuint64_t 
             g_encode = reinterpret_cast<EncodeTiledFn>(fn);
         cudaGetLastError();
     });
-    if (g_encode == nullptr) return false;
+    return g_encode != nullptr;
+}
+
+bool encode_bf16(CUtensorMap *map, const void *base, int rank, const cuuint64_t *dims,
+                 const cuuint64_t *byte_strides, uint32_t box_inner, uint32_t box_rows) {
+    if (!encode_ready()) return false;
     if (box_inner * 2 != 128 && box_inner * 2 != 64) return false;
     cuuint32_t box[3] = {box_inner, box_rows, 1};
     cuuint32_t estr[3] = {1, 1, 1};
@@ -440,6 +527,18 @@ bool encode_bf16(CUtensorMap *map, const void *base, int rank, const cuuint64_t 
 bool encode_bf16_2d(CUtensorMap *map, const void *base, uint64_t inner, uint64_t rows,
                     uint32_t box_inner, uint32_t box_rows) {
     return encode_bf16_2d_strided(map, base, inner, rows, inner, box_inner, box_rows);
+}
+
+bool encode_u8_2d(CUtensorMap *map, const void *base, uint64_t inner, uint64_t rows, uint32_t box_inner,
+                  uint32_t box_rows) {
+    if (!encode_ready() || box_inner != 128) return false;
+    cuuint64_t dims[2] = {inner, rows};
+    cuuint64_t strides[1] = {inner};
+    cuuint32_t box[2] = {box_inner, box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    return g_encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 bool encode_bf16_2d_strided(CUtensorMap *map, const void *base, uint64_t inner, uint64_t rows,
@@ -798,6 +897,95 @@ moe_status_t moe_backward(const void *x, const float *w_r, const float *logits, 
     if ((r = moe_backward_stage1_data(w1, w_r, topk_idx, cfg, shape, dx, ws, ws_bytes, stream)) != MOE_OK)
         return r;
     return moe_backward_stage1_weight(x, shape, dw1, ws, ws_bytes, stream);
+}
+
+moe_status_t moe_mx_quantize(const void *in, int64_t rows, int64_t cols, void *codes, void *scales,
+                             void *stream) {
+    if (rows < 0 || cols <= 0 || cols % 32 != 0) return MOE_ERR_INVALID_ARG;
+    if (rows == 0) return MOE_OK;
+    if (in == nullptr || codes == nullptr || scales == nullptr || !aligned16(in) || !aligned16(codes))
+        return MOE_ERR_INVALID_ARG;
+    DeviceState *d = nullptr;
+    moe_status_t r = device_state(&d);
+    if (r != MOE_OK) return r;
+    return cuda_status(launch_mx_quantize(static_cast<const __nv_bfloat16 *>(in), rows, cols,
+                                          static_cast<uint8_t *>(codes), static_cast<uint8_t *>(scales),
+                                          static_cast<cudaStream_t>(stream)));
+}
+
+moe_status_t moe_mx_quantize_dispatch(const void *x, const moe_shape_t *shape, void *ws, size_t ws_bytes,
+                                      void *stream) {
+    moe_status_t r = check_shape(shape);
+    if (r != MOE_OK) return r;
+    if (shape->H % 128 || shape->I % 128) return MOE_ERR_UNSUPPORTED;
+    if (shape->T == 0) return MOE_OK;
+    if (x == nullptr || !aligned16(x)) return MOE_ERR_INVALID_ARG;
+    if ((r = check_ws(*shape, ws, ws_bytes)) != MOE_OK) return r;
+    if (!(shape->flags & MOE_SHAPE_MXFP8)) return MOE_ERR_INVALID_ARG;
+    DeviceState *d = nullptr;
+    if ((r = device_state(&d)) != MOE_OK) return r;
+    return run_mx_dispatch(*shape, x, carve(ws, *shape), static_cast<cudaStream_t>(stream));
+}
+
+moe_status_t moe_dispatch_gemm1_mx(const void *w1_codes, const void *w1_scales, const moe_shape_t *shape,
+                                   void *a_codes, void *a_scales, void *ws, size_t ws_bytes, void *stream) {
+    moe_status_t r = check_shape(shape);
+    if (r != MOE_OK) return r;
+    if (shape->H % 128 || shape->I % 128) return MOE_ERR_UNSUPPORTED;
+    if (shape->T == 0) return MOE_OK;
+    if (!w1_codes || !w1_scales || !a_codes || !a_scales) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(w1_codes) || !aligned16(w1_scales) || !aligned16(a_codes) || !aligned16(a_scales))
+        return MOE_ERR_INVALID_ARG;
+    if ((r = check_ws(*shape, ws, ws_bytes)) != MOE_OK) return r;
+    if (!(shape->flags & MOE_SHAPE_MXFP8)) return MOE_ERR_INVALID_ARG;
+    DeviceState *d = nullptr;
+    if ((r = device_state(&d)) != MOE_OK) return r;
+    return run_gemm1_mx(*shape, w1_codes, w1_scales, a_codes, a_scales, carve(ws, *shape), *d,
+                        static_cast<cudaStream_t>(stream));
+}
+
+moe_status_t moe_swiglu_gemm2_combine_mx(const void *a_codes, const void *a_scales, const float *topk_w,
+                                         const void *w2_codes, const void *w2_scales,
+                                         const moe_shape_t *shape, void *y, void *ws, size_t ws_bytes,
+                                         void *stream) {
+    moe_status_t r = check_shape(shape);
+    if (r != MOE_OK) return r;
+    if (shape->H % 128 || shape->I % 128) return MOE_ERR_UNSUPPORTED;
+    if (shape->T == 0) return MOE_OK;
+    if (!a_codes || !a_scales || !topk_w || !w2_codes || !w2_scales || !y) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(a_codes) || !aligned16(a_scales) || !aligned16(topk_w) || !aligned16(w2_codes) ||
+        !aligned16(w2_scales) || !aligned16(y))
+        return MOE_ERR_INVALID_ARG;
+    if ((r = check_ws(*shape, ws, ws_bytes)) != MOE_OK) return r;
+    DeviceState *d = nullptr;
+    if ((r = device_state(&d)) != MOE_OK) return r;
+    return run_gemm2_mx(*shape, a_codes, a_scales, topk_w, w2_codes, w2_scales, y, carve(ws, *shape), *d,
+                        static_cast<cudaStream_t>(stream));
+}
+
+moe_status_t moe_forward_mx(const void *x, const int32_t *topk_idx, const float *topk_w,
+                            const void *w1_codes, const void *w1_scales, const void *w2_codes,
+                            const void *w2_scales, const moe_shape_t *shape, void *y, void *ws,
+                            size_t ws_bytes, void *stream) {
+    moe_status_t r = check_shape(shape);
+    if (r != MOE_OK) return r;
+    if (shape->H % 128 || shape->I % 128) return MOE_ERR_UNSUPPORTED;
+    if (shape->T == 0) return MOE_OK;
+    if (!x || !topk_idx || !topk_w || !w1_codes || !w1_scales || !w2_codes || !w2_scales || !y)
+        return MOE_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(topk_idx) || !aligned16(topk_w) || !aligned16(w1_codes) ||
+        !aligned16(w1_scales) || !aligned16(w2_codes) || !aligned16(w2_scales) || !aligned16(y))
+        return MOE_ERR_INVALID_ARG;
+    if ((r = check_ws(*shape, ws, ws_bytes)) != MOE_OK) return r;
+    if (!(shape->flags & MOE_SHAPE_MXFP8)) return MOE_ERR_INVALID_ARG;
+    DeviceState *d = nullptr;
+    if ((r = device_state(&d)) != MOE_OK) return r;
+    const Ws w = carve(ws, *shape);
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if ((r = run_metadata(*shape, topk_idx, w, st)) != MOE_OK) return r;
+    if ((r = run_mx_dispatch(*shape, x, w, st)) != MOE_OK) return r;
+    if ((r = run_gemm1_mx(*shape, w1_codes, w1_scales, w.a_codes, w.a_scales, w, *d, st)) != MOE_OK) return r;
+    return run_gemm2_mx(*shape, w.a_codes, w.a_scales, topk_w, w2_codes, w2_scales, y, w, *d, st);
 }
 
 moe_status_t moe_get_device_error(void *ws, int32_t *code, void *stream) {

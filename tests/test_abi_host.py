@@ -161,6 +161,35 @@ def test_training_calls_need_a_training_workspace(lib):
     assert lib.moe_backward(p, p, None, p, p, p, p, p, p, ctypes.byref(train), ctypes.byref(cfg), p, p, p,
                             p, p, p, big, None) == 1   # w_r without logits
     # unknown shape flags
-    bad = B.Shape(16, 64, 64, 4, 2, 2)
+    bad = B.Shape(16, 64, 64, 4, 2, 4)
     n = ctypes.c_size_t()
     assert lib.moe_workspace_size(ctypes.byref(bad), ctypes.byref(n)) == 1
+
+
+def test_mxfp8_layout_and_argument_checks(lib):
+    for cfg in CONFIGS.values():
+        if cfg.H % 128 or cfg.I % 128:
+            continue
+        R = cfg.T * cfg.k
+        base = B.moe_workspace_layout(B.shape(cfg.T, cfg.H, cfg.I, cfg.E, cfg.k))
+        assert base.x_codes == base.a_scales == base.total
+        L = B.moe_workspace_layout(B.shape(cfg.T, cfg.H, cfg.I, cfg.E, cfg.k, mxfp8=True))
+        offs = [L.dlogits, L.x_codes, L.x_scales, L.a_codes, L.a_scales, L.total]
+        assert offs == sorted(offs) and all(o % 256 == 0 for o in offs)
+        assert L.x_scales - L.x_codes >= R * cfg.H
+        assert L.a_codes - L.x_scales >= R * cfg.H // 32
+        assert L.a_scales - L.a_codes >= R * cfg.I
+        assert L.total - L.a_scales >= R * cfg.I // 32
+    p = ctypes.c_void_p(1 << 20)
+    big = 1 << 40
+    shp = B.shape(16, 256, 256, 4, 2, mxfp8=True)
+    odd = B.shape(16, 192, 256, 4, 2, mxfp8=True)           # H % 128 != 0
+    assert lib.moe_mx_quantize(p, 4, 48, p, p, None) == 1     # cols % 32
+    assert lib.moe_mx_quantize(None, 4, 64, p, p, None) == 1
+    assert lib.moe_dispatch_gemm1_mx(p, p, ctypes.byref(odd), p, p, p, big, None) == 2
+    assert lib.moe_dispatch_gemm1_mx(p, p, ctypes.byref(shp), p, None, p, big, None) == 1
+    assert lib.moe_mx_quantize_dispatch(p, ctypes.byref(odd), p, big, None) == 2
+    assert lib.moe_mx_quantize_dispatch(None, ctypes.byref(shp), p, big, None) == 1
+    assert lib.moe_swiglu_gemm2_combine_mx(p, p, p, p, p, ctypes.byref(odd), p, p, big, None) == 2
+    plain = B.shape(16, 256, 256, 4, 2)
+    assert lib.moe_forward_mx(p, p, p, p, p, p, p, ctypes.byref(plain), p, p, big, None) == 1

@@ -1,0 +1,202 @@
+"""MXFP8 expert precision (CUDA path through the C ABI) against the fp64 oracle.
+
+Bars: the quantizer's E4M3 codes and E8M0 scales bit-exact (integer output of
+exact inputs); the expert path's y within relative Frobenius error 1e-2 and max
+abs error 3e-2 * max|y_ref| of the oracle's MXFP8 forward fed the same codes.
+The SwiGLU output a is quantized from fp32 on the GPU and from fp64 in the
+oracle, so a few of its codes may sit one step apart at rounding boundaries;
+those are counted and bounded, not required equal.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from gpu_helpers import assert_close_y, read_metadata
+from moe_expert_router_gb300 import binding as B
+from moe_expert_router_gb300.workloads import CONFIGS, MoEConfig, generate, routing_with_counts
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _device():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    B.load()
+
+
+def gpu_quantize(t):
+    codes = torch.empty(t.shape, dtype=torch.uint8, device=DEV)
+    scales = torch.empty(t.shape[:-1] + (t.shape[-1] // 32,), dtype=torch.uint8, device=DEV)
+    B.moe_mx_quantize(t, codes, scales)
+    return codes, scales
+
+
+@pytest.mark.parametrize("kind", ["normal", "wide_range", "zeros_and_tiny", "saturating"])
+def test_quantizer_bit_exact(kind):
+    g = torch.Generator(device="cpu").manual_seed(hash(kind) % 1000)
+    x = torch.randn((97, 512), generator=g, dtype=torch.float32)
+    if kind == "wide_range":
+        x = x * torch.exp2(torch.randint(-40, 40, (97, 16), generator=g).float()).repeat_interleave(32, 1)
+    elif kind == "zeros_and_tiny":
+        x[::3] = 0.0
+        x[1::3] *= 2.0 ** -128                        # bf16 subnormal range
+        x[5, 64:96] = 0.0
+    elif kind == "saturating":
+        x *= 100.0
+        x[:, ::32] = 1.9 * 2.0 ** 8                   # block maxima with mantissa 1.9: scaled to 486 -> 448
+    xb = x.to(torch.bfloat16)
+    codes, scales = gpu_quantize(xb.to(DEV))
+    rc, rs = oracle.mx_quantize(xb)
+    np.testing.assert_array_equal(scales.cpu().numpy(), rs)
+    np.testing.assert_array_equal(codes.cpu().numpy(), rc)
+
+
+def _cfg(T, H, I, E, k, **kw):
+    return MoEConfig("case", T=T, H=H, I=I, E=E, k=k, **kw)
+
+
+def mx_inputs(cfg, seed=0, idx=None, w=None):
+    inp = generate(cfg, seed=seed, device=DEV)
+    if idx is None:
+        shp = B.shape(cfg.T, cfg.H, cfg.I, cfg.E, cfg.k)
+        ws = B.new_workspace(shp, DEV)
+        idx = torch.empty((cfg.T, cfg.k), dtype=torch.int32, device=DEV)
+        w = torch.empty((cfg.T, cfg.k), dtype=torch.float32, device=DEV)
+        B.moe_router(inp["x"], inp["w_r"], shp, B.router_cfg(cfg.score, cfg.normalize, cfg.scale, cfg.n_group,
+                                                             cfg.topk_group, cfg.group_topn),
+                     idx, w, ws, logit_offset=inp["logit_offset"], sel_bias=inp["sel_bias"])
+    E, I, H = cfg.E, cfg.I, cfg.H
+    w1q, w1s = gpu_quantize(inp["w1"].view(E * 2 * I, H))
+    w2q, w2s = gpu_quantize(inp["w2"].view(E * H, I))
+    return inp, idx, w, w1q.view(E, 2 * I, H), w1s.view(E, 2 * I, H // 32), w2q.view(E, H, I), w2s.view(E, H, I // 32)
+
+
+def run_mx(cfg, inp, idx, w, w1q, w1s, w2q, w2s, staged):
+    shp = B.shape(cfg.T, cfg.H, cfg.I, cfg.E, cfg.k, mxfp8=True)
+    ws = B.new_workspace(shp, DEV)
+    y = torch.empty((cfg.T, cfg.H), dtype=torch.bfloat16, device=DEV)
+    R = cfg.T * cfg.k
+    aq = torch.empty((R, cfg.I), dtype=torch.uint8, device=DEV)
+    as_ = torch.empty((R, cfg.I // 32), dtype=torch.uint8, device=DEV)
+    if staged:
+        B.moe_routing_metadata(idx, shp, ws)
+        B.moe_mx_quantize_dispatch(inp["x"], shp, ws)
+        B.moe_dispatch_gemm1_mx(w1q, w1s, shp, aq, as_, ws)
+        B.moe_swiglu_gemm2_combine_mx(aq, as_, w, w2q, w2s, shp, y, ws)
+    else:
+        B.moe_forward_mx(inp["x"], idx, w, w1q, w1s, w2q, w2s, shp, y, ws)
+        L = B.moe_workspace_layout(shp)
+        aq = ws[L.a_codes:L.a_codes + R * cfg.I].view(R, cfg.I)
+        as_ = ws[L.a_scales:L.a_scales + R * cfg.I // 32].view(R, cfg.I // 32)
+    err = B.moe_get_device_error(ws)
+    return y, aq, as_, ws, shp, err
+
+
+CASES = {
+    "small": _cfg(256, 256, 256, 8, 2),
+    "ragged": _cfg(300, 384, 384, 6, 3),
+    "tile_tails": _cfg(200, 512, 512, 4, 2),          # I / 96 and H / 224 leave partial tiles
+    "sigmoid_groups": _cfg(128, 256, 640, 16, 4, score="sigmoid", scale=2.5, n_group=4, topk_group=2,
+                           sel_bias=True),
+    "one_token": _cfg(1, 128, 128, 4, 2),
+}
+
+
+def test_quantizing_dispatch_is_the_quantizer_in_routed_order():
+    cfg = CASES["ragged"]
+    inp, idx, w, *_ = mx_inputs(cfg, seed=6)
+    shp = B.shape(cfg.T, cfg.H, cfg.I, cfg.E, cfg.k, mxfp8=True)
+    ws = B.new_workspace(shp, DEV)
+    B.moe_routing_metadata(idx, shp, ws)
+    B.moe_mx_quantize_dispatch(inp["x"], shp, ws)
+    L = B.moe_workspace_layout(shp)
+    R = cfg.T * cfg.k
+    codes = ws[L.x_codes:L.x_codes + R * cfg.H].view(R, cfg.H).cpu().numpy()
+    scales = ws[L.x_scales:L.x_scales + R * cfg.H // 32].view(R, cfg.H // 32).cpu().numpy()
+    _, _, _, perm, _ = read_metadata(ws, shp)
+    rc, rs = oracle.mx_quantize(inp["x"])
+    tok = perm // cfg.k
+    np.testing.assert_array_equal(codes[: len(perm)], rc[tok])
+    np.testing.assert_array_equal(scales[: len(perm)], rs[tok])
+
+
+@pytest.mark.parametrize("name", sorted(CASES))
+@pytest.mark.parametrize("staged", [True, False])
+def test_mx_forward_matches_oracle(name, staged):
+    cfg = CASES[name]
+    inp, idx, w, w1q, w1s, w2q, w2s = mx_inputs(cfg, seed=2)
+    y, aq, as_, ws, shp, err = run_mx(cfg, inp, idx, w, w1q, w1s, w2q, w2s, staged)
+    assert err == 0, f"device error word {err:#x}"
+    xq, xs = oracle.mx_quantize(inp["x"])
+    y_ref, _, ac_ref, as_ref = oracle.expert_forward_mx(xq, xs, idx.cpu(), w.cpu().double(), w1q.cpu(), w1s.cpu(),
+                                                        w2q.cpu(), w2s.cpu(), want_a=True)
+    assert_close_y(y, y_ref, "y (MXFP8)")
+    # a: codes in routed order on the GPU, in slot order in the oracle
+    _, _, _, perm, _ = read_metadata(ws, shp)
+    g_codes = aq.cpu().numpy()[: len(perm)]
+    r_codes = ac_ref[perm]
+    g_sc = as_.cpu().numpy()[: len(perm)]
+    r_sc = as_ref[perm]
+    assert (g_sc != r_sc).mean() <= 0.01, "block scales of a differ too often"
+    same = np.repeat(g_sc == r_sc, 32, axis=1)
+    vals = oracle.e4m3_values()
+    step = np.repeat(np.ldexp(1.0, r_sc.astype(np.int64) - 127 - 9), 32, axis=1)   # one subnormal step
+    g_val = vals[g_codes] * step * 512
+    r_val = vals[r_codes] * step * 512
+    differ = same & (g_codes != r_codes)
+    assert differ.mean() <= 0.01, f"{differ.mean():.3%} of a's codes differ"
+    # where the block scales agree, a differing code is the neighbouring E4M3 value
+    # (a value at a rounding boundary, computed in fp32 here and in fp64 there)
+    assert np.all(np.abs(g_val - r_val)[differ] <= np.maximum(0.13 * np.abs(r_val), step)[differ])
+
+
+def test_mx_unused_experts_with_nan_codes_are_never_read():
+    T, H, I, E, k = 96, 256, 256, 8, 2
+    cfg = _cfg(T, H, I, E, k)
+    counts = [40, 0, 60, 50, 0, 42, 0, 0]
+    idx, w = routing_with_counts(counts, T, k, seed=4, device=DEV)
+    inp, idx, w, w1q, w1s, w2q, w2s = mx_inputs(cfg, seed=3, idx=idx, w=w)
+    y0, *_ = run_mx(cfg, inp, idx, w, w1q, w1s, w2q, w2s, staged=True)
+    for e, c in enumerate(counts):
+        if c == 0:
+            w1q[e] = 0x7F      # E4M3 NaN
+            w2q[e] = 0x7F
+            w1s[e] = 0xFF      # E8M0 NaN
+            w2s[e] = 0xFF
+    y1, *_rest, err = run_mx(cfg, inp, idx, w, w1q, w1s, w2q, w2s, staged=True)
+    assert err == 0
+    assert torch.isfinite(y1.float()).all()
+    assert torch.equal(y0, y1)
+
+
+def test_mx_bf16_agreement_is_within_quantization_error():
+    """Sanity of the precision itself: MXFP8 y stays within a few percent of the bf16 path."""
+    cfg = CASES["ragged"]
+    inp, idx, w, w1q, w1s, w2q, w2s = mx_inputs(cfg, seed=5)
+    y_mx, *_ = run_mx(cfg, inp, idx, w, w1q, w1s, w2q, w2s, staged=True)
+    y_bf = oracle.expert_forward(inp["x"].cpu(), idx.cpu(), w.cpu().double(), inp["w1"].cpu(), inp["w2"].cpu())
+    rel = np.linalg.norm(y_mx.float().cpu().double().numpy() - y_bf) / np.linalg.norm(y_bf)
+    assert 1e-3 < rel < 0.08, rel
+
+
+@pytest.mark.slow
+def test_mx_full_size_mid_sampled():
+    """The mid configuration in MXFP8 at full size (one-shot call): y on sampled tokens."""
+    cfg = CONFIGS["mid"]
+    inp, idx, w, w1q, w1s, w2q, w2s = mx_inputs(cfg, seed=0)
+    y, aq, as_, ws, shp, err = run_mx(cfg, inp, idx, w, w1q, w1s, w2q, w2s, staged=False)
+    assert err == 0
+    toks = torch.as_tensor([0, 1, 2, cfg.T // 2, cfg.T - 1] + list(range(101, cfg.T, cfg.T // 10))[:10])
+    xq, xs = oracle.mx_quantize(inp["x"][toks.to(DEV)])
+    idx_s = idx.cpu()[toks].long()
+    used = torch.unique(idx_s)
+    remap = torch.full((cfg.E,), -1, dtype=torch.long)
+    remap[used] = torch.arange(used.numel())
+    u = used.to(DEV)
+    y_ref = oracle.expert_forward_mx(xq, xs, remap[idx_s].to(torch.int32), w.cpu()[toks].double(),
+                                     w1q[u].cpu(), w1s[u].cpu(), w2q[u].cpu(), w2s[u].cpu())
+    assert_close_y(y.cpu()[toks], y_ref, "y (MXFP8, sampled tokens)")

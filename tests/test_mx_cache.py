@@ -1,0 +1,46 @@
+"""The MXFP8 weight-quant cache's bookkeeping (host only; the quantizer is a fake)."""
+import torch
+
+from moe_expert_router_gb300.mx_cache import MxWeightCache
+
+
+def _fake_quantize(w):
+    return ("codes", w.clone()), ("scales", w.shape)
+
+
+def test_cache_hits_until_the_weight_changes():
+    c = MxWeightCache(quantize=_fake_quantize)
+    w = torch.zeros((2, 4, 64), dtype=torch.bfloat16)
+    q1 = c.get(w)
+    assert c.get(w) is q1 and c.quantizations == 1
+    w.add_(1.0)                              # in-place update bumps the version counter
+    q2 = c.get(w)
+    assert q2 is not q1 and c.quantizations == 2
+    assert torch.equal(q2[0][1], w)
+
+
+def test_invalidate_drops_entries_the_version_cannot_see():
+    c = MxWeightCache(quantize=_fake_quantize)
+    w = torch.zeros((2, 4, 64), dtype=torch.bfloat16)
+    c.get(w)
+    with torch.no_grad():
+        w.data.fill_(3.0)                    # a write through .data does not bump the version
+    assert c.get(w)[0][1].max().item() == 0.0     # stale, as in the guide's optimizer case
+    c.invalidate()
+    assert len(c) == 0
+    assert c.get(w)[0][1].max().item() == 3.0 and c.quantizations == 2
+
+
+def test_separate_tensors_have_separate_entries():
+    c = MxWeightCache(quantize=_fake_quantize)
+    w1 = torch.zeros((2, 4, 64), dtype=torch.bfloat16)
+    w2 = torch.ones((2, 8, 32), dtype=torch.bfloat16)
+    c.get(w1)
+    c.get(w2)
+    assert len(c) == 2 and c.quantizations == 2
+    try:
+        c.get(torch.zeros((2, 4, 48), dtype=torch.bfloat16))
+    except ValueError:
+        pass
+    else:
+        raise AssertionError("a last dimension that is not a multiple of 32 must be rejected")
