@@ -43,8 +43,8 @@ L2_FLUSH_BYTES = 256 << 20
 KERNEL_SOURCES = ("moe_expert_router_gb300/csrc/gemm_kernel.cuh", "moe_expert_router_gb300/csrc/grouped_gemm.cu",
                   "moe_expert_router_gb300/csrc/ptx.cuh", "moe_expert_router_gb300/csrc/internal.cuh")
 STAGE1_TRAFFIC = {
-    # profiles/tc_gemm_mid_ncu.md: 804.77 MB read + 59.73 MB written
-    "mid": {"src": "a7f446c52efcace7", "bytes": 864.5e6},
+    # profiles/launch_list_mid.md: 805.0 MB read + 61.1 MB written (mean of two launches)
+    "mid": {"src": "6415a91603391173", "bytes": 866.1e6},
 }
 
 
