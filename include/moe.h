@@ -234,6 +234,34 @@ moe_status_t moe_forward(const void *x, const int32_t *topk_idx, const float *to
                          const void *w1, const void *w2, const moe_shape_t *shape, void *y,
                          void *ws, size_t ws_bytes, void *stream);
 
+/* ------------------------------------------------------------------ expert parallelism
+ *
+ * Across devices the guide fuses the dispatch all-to-all into
+ * dispatch_grouped_gemm and the combine all-to-all into grouped_gemm_combine
+ * (opening section). These two calls are the device-side halves of that
+ * exchange when the caller moves the rows with its own collective: routed rows
+ * are expert-major, so the rows bound for the device that owns experts
+ * [e0, e1) are the contiguous rows offsets[e0] .. offsets[e1]-1.
+ */
+
+/*
+ * Dispatch send buffer: rows[r, :] = x[perm_slot[r] / k, :] for every routed row
+ * r < offsets[E] (rows of dropped slots are not written), and, when row_weight is
+ * not NULL, row_weight[r] = topk_w[perm_slot[r]]. x bf16 [T,H]; rows bf16
+ * [T*k, H]; topk_w fp32 [T,k]; row_weight fp32 [T*k]. Needs the metadata of
+ * moe_routing_metadata in ws.
+ */
+moe_status_t moe_dispatch_rows(const void *x, const float *topk_w, const moe_shape_t *shape, void *rows,
+                               float *row_weight, void *ws, size_t ws_bytes, void *stream);
+
+/*
+ * Combine of returned rows: y[t, :] = sum_j rows[row_of[t*k + j], :] (rows already
+ * weighted, in this device's routed order; dropped slots skipped; fp32 sum,
+ * bf16 y [T,H], fully written). Needs the metadata of moe_routing_metadata in ws.
+ */
+moe_status_t moe_combine_rows(const void *rows, const moe_shape_t *shape, void *y, void *ws, size_t ws_bytes,
+                              void *stream);
+
 /* ------------------------------------------------------------------ training
  *
  * The backward of the expert path and the router (MegaMoE guide, section

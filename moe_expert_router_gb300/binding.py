@@ -84,6 +84,8 @@ _SIG = {
     "moe_dispatch_gemm1_mx": [_P, _P, ctypes.POINTER(Shape), _P, _P, _P, ctypes.c_size_t, _P],
     "moe_swiglu_gemm2_combine_mx": [_P, _P, _P, _P, _P, ctypes.POINTER(Shape), _P, _P, ctypes.c_size_t, _P],
     "moe_forward_mx": [_P, _P, _P, _P, _P, _P, _P, ctypes.POINTER(Shape), _P, _P, ctypes.c_size_t, _P],
+    "moe_dispatch_rows": [_P, _P, ctypes.POINTER(Shape), _P, _P, _P, ctypes.c_size_t, _P],
+    "moe_combine_rows": [_P, ctypes.POINTER(Shape), _P, _P, ctypes.c_size_t, _P],
     "moe_get_device_error": [_P, ctypes.POINTER(ctypes.c_int32), _P],
     "moe_status_string": [ctypes.c_int],
     "moe_kernel_launch_count": [],
@@ -302,6 +304,20 @@ def moe_forward_mx(x, topk_idx, topk_w, w1q, w1s, w2q, w2s, shp, y, ws, stream=N
     _check("moe_forward_mx", load().moe_forward_mx(
         _ptr(x), _ptr(topk_idx), _ptr(topk_w), _ptr(w1q), _ptr(w1s), _ptr(w2q), _ptr(w2s),
         ctypes.byref(shp), _ptr(y), _ptr(ws), _nbytes(ws), _stream(stream, ws)))
+
+
+def moe_dispatch_rows(x, shp, rows, ws, topk_w=None, row_weight=None, stream=None):
+    """rows[r] = x[token of routed row r] (and row_weight[r] = its routing weight): the
+    send buffer of an expert-parallel dispatch."""
+    _check("moe_dispatch_rows", load().moe_dispatch_rows(
+        _ptr(x), _ptr(topk_w), ctypes.byref(shp), _ptr(rows), _ptr(row_weight), _ptr(ws), _nbytes(ws),
+        _stream(stream, ws)))
+
+
+def moe_combine_rows(rows, shp, y, ws, stream=None):
+    """y[t] = sum of the token's (already weighted) rows, in routed order."""
+    _check("moe_combine_rows", load().moe_combine_rows(
+        _ptr(rows), ctypes.byref(shp), _ptr(y), _ptr(ws), _nbytes(ws), _stream(stream, ws)))
 
 
 def moe_get_device_error(ws, stream=None) -> int:

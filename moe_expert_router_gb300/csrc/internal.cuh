@@ -177,6 +177,11 @@ cudaError_t launch_gemm1_swiglu(const GemmLaunch &p, cudaStream_t st);
 cudaError_t launch_gemm2_scatter(const GemmLaunch &p, cudaStream_t st);
 cudaError_t launch_router_gemm(const RouterGemmLaunch &p, cudaStream_t st);
 cudaError_t launch_combine(const CombineLaunch &p, cudaStream_t st);
+// rows[r, :] = x[perm_slot[r] / k, :] for routed rows r < *routed, and with row_w
+// row_w[r] = topk_w[perm_slot[r]] (rows.cu).
+cudaError_t launch_gather_rows(const __nv_bfloat16 *x, const int32_t *perm_slot, const int32_t *routed, int k,
+                               int64_t R, int64_t H, __nv_bfloat16 *rows, const float *topk_w, float *row_w,
+                               cudaStream_t st);
 
 // Routing-weight gradient: dtopk_w[s] = sum_n dtw_part[n, row_of[s]] (0 if dropped).
 struct DtwReduceLaunch {

@@ -988,6 +988,45 @@ moe_status_t moe_forward_mx(const void *x, const int32_t *topk_idx, const float 
     return run_gemm2_mx(*shape, w.a_codes, w.a_scales, topk_w, w2_codes, w2_scales, y, w, *d, st);
 }
 
+moe_status_t moe_dispatch_rows(const void *x, const float *topk_w, const moe_shape_t *shape, void *rows,
+                               float *row_weight, void *ws, size_t ws_bytes, void *stream) {
+    moe_status_t r = check_shape(shape);
+    if (r != MOE_OK) return r;
+    if (shape->T == 0) return MOE_OK;
+    if (x == nullptr || rows == nullptr || !aligned16(x) || !aligned16(rows)) return MOE_ERR_INVALID_ARG;
+    if (row_weight != nullptr && (topk_w == nullptr || (reinterpret_cast<uintptr_t>(row_weight) & 3u) ||
+                                  (reinterpret_cast<uintptr_t>(topk_w) & 3u)))
+        return MOE_ERR_INVALID_ARG;
+    if ((r = check_ws(*shape, ws, ws_bytes)) != MOE_OK) return r;
+    DeviceState *d = nullptr;
+    if ((r = device_state(&d)) != MOE_OK) return r;
+    const Ws w = carve(ws, *shape);
+    return cuda_status(launch_gather_rows(static_cast<const __nv_bfloat16 *>(x), w.perm_slot, w.offsets + shape->E,
+                                          shape->k, shape->T * shape->k, shape->H,
+                                          static_cast<__nv_bfloat16 *>(rows), topk_w, row_weight,
+                                          static_cast<cudaStream_t>(stream)));
+}
+
+moe_status_t moe_combine_rows(const void *rows, const moe_shape_t *shape, void *y, void *ws, size_t ws_bytes,
+                              void *stream) {
+    moe_status_t r = check_shape(shape);
+    if (r != MOE_OK) return r;
+    if (shape->T == 0) return MOE_OK;
+    if (rows == nullptr || y == nullptr || !aligned16(rows) || !aligned16(y)) return MOE_ERR_INVALID_ARG;
+    if ((r = check_ws(*shape, ws, ws_bytes)) != MOE_OK) return r;
+    DeviceState *d = nullptr;
+    if ((r = device_state(&d)) != MOE_OK) return r;
+    const Ws w = carve(ws, *shape);
+    CombineLaunch c;
+    c.obuf = static_cast<const __nv_bfloat16 *>(rows);
+    c.row_of = w.row_of;
+    c.y = static_cast<__nv_bfloat16 *>(y);
+    c.T = static_cast<int>(shape->T);
+    c.H = static_cast<int>(shape->H);
+    c.k = shape->k;
+    return cuda_status(launch_combine(c, static_cast<cudaStream_t>(stream)));
+}
+
 moe_status_t moe_get_device_error(void *ws, int32_t *code, void *stream) {
     if (ws == nullptr || code == nullptr) return MOE_ERR_INVALID_ARG;
     cudaStream_t st = static_cast<cudaStream_t>(stream);

@@ -95,6 +95,8 @@ def test_null_arguments_rejected_before_any_device_call(lib):
     assert lib.moe_get_device_error(None, None, None) == 1
     assert lib.moe_route_logits(None, None, None, ctypes.byref(shp), ctypes.byref(cfg), None, None, None,
                                 None, 0, None) == 1
+    assert lib.moe_dispatch_rows(None, None, ctypes.byref(shp), None, None, None, 0, None) == 1
+    assert lib.moe_combine_rows(None, ctypes.byref(shp), None, None, 0, None) == 1
     # misaligned workspace and a too-small workspace (host checks, no device touched)
     x = ctypes.c_void_p(1 << 20)
     assert lib.moe_routing_metadata(x, ctypes.byref(shp), ctypes.c_void_p((1 << 20) + 16), 1 << 30,
