@@ -161,7 +161,7 @@ def bytes_and_flops(cfg, counts, precision="bf16"):
     st = {
         "gemm1": {"flops": 4.0 * R * H * I,
                   "bytes": 4.0 * H * I * active + 2.0 * T * H + 2.0 * R * I * (3 if cfg.backward else 1),
-                  "kernel": "tc_gemm_kernel<kStage1%s> (stage 1: fused x row gather + GEMM1 + SwiGLU)"
+                  "kernel": "tc_gemm_kernel<kStage1%s> (stage 1: dispatch copy of x + GEMM1 + SwiGLU)"
                             % ("SaveH" if cfg.backward else "")},
         "gemm2_combine": {"flops": 2.0 * R * H * I,
                           "bytes": 2.0 * H * I * active + 2.0 * R * I + 2.0 * T * H,

@@ -94,12 +94,16 @@ typedef struct moe_ws_layout {
     size_t router;     /* router scratch: fp32 split-K partial logits [s,T,E], bf16 split of w_r [3,E,H], sums, counts */
     size_t a;          /* bf16 [T*k, I] SwiGLU activations (moe_forward only) */
     size_t obuf;       /* bf16 [T*k, H] weighted expert outputs in routed-row order;
-                          the backward's dX rows (unweighted, routed order) reuse it */
+                          before stage 2 writes them, stage 1 (outside training)
+                          holds x's rows dispatched into routed order here; the
+                          backward's dX rows (unweighted, routed order) reuse it */
     /* training workspaces only (flags = MOE_SHAPE_TRAINING), else equal to total: */
     size_t dh;         /* bf16 [T*k, 2I] gradient of h = [gate | up], routed order */
     size_t aw;         /* bf16 [T*k, I] routing weight times a, routed order */
     size_t dtw_part;   /* fp32 [ceil(I/256), T*k] partial routing-weight gradients */
     size_t dlogits;    /* fp32 [T, E] gradient of the router logits */
+    size_t xp;         /* bf16 [T*k, H] x rows in routed order (training stage 1's dispatch) */
+    size_t dyp;        /* bf16 [T*k, H] dY rows in routed order (the backward's dispatch) */
     /* MXFP8 workspaces only (flags & MOE_SHAPE_MXFP8), else equal to total: */
     size_t x_codes;    /* E4M3 [T*k, H] quantized x rows in routed order (the MXFP8 dispatch) */
     size_t x_scales;   /* E8M0 [T*k, H/32] */

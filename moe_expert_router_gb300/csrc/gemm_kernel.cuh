@@ -6,9 +6,10 @@
 //   kStage1  dispatch_grouped_gemm: for routed row r of expert e,
 //            h = x[token(r)] . w1[e]^T, a[r] = silu(h[:I]) * h[I:] (SwiGLU
 //            silu(x_glu) * x_linear, "GDN <-> FLA Parity in Primus" page,
-//            section B). Dedicated warps gather the routed x rows straight into
-//            the shared-memory A tiles. kStage1SaveH also stores h (gate and
-//            up halves, bf16) for the backward.
+//            section B). The routed x rows were dispatched into routed order
+//            beforehand (a copy kernel; the MXFP8 quantization in kStage1Mx), so
+//            the A tiles are plain TMA loads. kStage1SaveH also stores h (gate
+//            and up halves, bf16) for the backward.
 //   kStage2  grouped_gemm_combine: o[r] = a[r] . w2[e]^T, scaled by the slot's
 //            routing weight and stored to row r of obuf (combined afterwards).
 //   kRouter  partial fp32 logits of x . w_r^T with w_r split exactly into three
@@ -91,9 +92,9 @@ enum Mode : int {
 
 template <int MODE> constexpr bool kIsMx = MODE == kStage1Mx || MODE == kStage2Mx;
 template <int MODE> constexpr bool kIsStage1 = MODE == kStage1 || MODE == kStage1SaveH || MODE == kStage1Mx;
-// A is filled by the K-major row gather (token rows of x or dY); stage 1 in
-// MXFP8 reads x rows already dispatched into routed order by its quantization
-template <int MODE> constexpr bool kGatherK = MODE == kStage1 || MODE == kStage1SaveH || MODE == kBwdDA;
+// A is filled by the K-major row gather (token rows of dY); stage 1 reads x rows
+// already dispatched into routed order
+template <int MODE> constexpr bool kGatherK = MODE == kBwdDA;
 // the MN-major row gather fills A (dW2: dY rows) or B (dW1: x rows)
 template <int MODE> constexpr bool kGatherMnA = MODE == kBwdDW2;
 template <int MODE> constexpr bool kGatherMnB = MODE == kBwdDW1;
@@ -447,10 +448,8 @@ tc_gemm_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs g) {
                         constexpr int hn = kUnitN<MODE> / 2;                                 // gate (= up) rows
                         const int row = t.e * g.b_rows + t.n * hn;
                         const int kx = kb * kStageK<MODE>;
-                        if constexpr (MODE == kStage1Mx) {                                  // dispatched x rows
-                            tma_load_2d(sa, &maps.a, kx, t.row0, full);
-                            if (two) tma_load_2d(sa + A_HALF_BYTES, &maps.a, kx, t.row0 + BM, full);
-                        }
+                        tma_load_2d(sa, &maps.a, kx, t.row0, full);                         // dispatched x rows
+                        if (two) tma_load_2d(sa + A_HALF_BYTES, &maps.a, kx, t.row0 + BM, full);
                         tma_load_2d(sb, &maps.b, kx, row, full);                            // gate rows
                         tma_load_2d(sb + hn * 128, &maps.b, kx, row + g.half, full);        // up rows
                     } else if constexpr (MODE == kStage2 || MODE == kStage2Mx) {
@@ -900,8 +899,8 @@ tc_gemm_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs g) {
         if (lane == 0) bulk_wait<0>();                  // every output box written
     } else {
         // ------------------------------------------------ row gathers
-        // The dispatch of dispatch_grouped_gemm (and its backward twins): 128
-        // threads copy routed token rows straight into the 128B-swizzled tiles
+        // The row gathers of the backward (dY rows for dA and dW2, x rows for
+        // dW1): 128 threads copy routed token rows straight into the 128B-swizzled tiles
         // with 16-byte cp.async. Each thread waits for its own copies, orders them
         // before the tensor core's async-proxy reads, then arrives on the stage's
         // full barrier, one stage behind its issue so that two stages of copies

@@ -86,8 +86,10 @@ moe_ws_layout_t make_layout(const moe_shape_t &s) {
         L.aw = off;       off = align256(off + 2 * R * I);
         L.dtw_part = off; off = align256(off + 4 * R * ((I + kBN - 1) / kBN));
         L.dlogits = off;  off = align256(off + 4 * T * E);
+        L.xp = off;       off = align256(off + 2 * R * H);
+        L.dyp = off;      off = align256(off + 2 * R * H);
     } else {
-        L.dh = L.aw = L.dtw_part = L.dlogits = off;
+        L.dh = L.aw = L.dtw_part = L.dlogits = L.xp = L.dyp = off;
     }
     if (s.flags & MOE_SHAPE_MXFP8) {
         L.x_codes = off;  off = align256(off + R * H);
@@ -112,6 +114,7 @@ struct Ws {
     __nv_bfloat16 *a, *obuf;
     __nv_bfloat16 *dh, *aw;     // training only
     float *dtw_part, *dlogits;  // training only
+    __nv_bfloat16 *xp, *dyp;    // training only: x and dY rows in routed order
     uint8_t *x_codes, *x_scales, *a_codes, *a_scales;   // MXFP8 only
     bool training, mxfp8;
 };
@@ -144,6 +147,8 @@ Ws carve(void *ws, const moe_shape_t &s) {
     w.aw = reinterpret_cast<__nv_bfloat16 *>(b + L.aw);
     w.dtw_part = reinterpret_cast<float *>(b + L.dtw_part);
     w.dlogits = reinterpret_cast<float *>(b + L.dlogits);
+    w.xp = reinterpret_cast<__nv_bfloat16 *>(b + L.xp);
+    w.dyp = reinterpret_cast<__nv_bfloat16 *>(b + L.dyp);
     w.mxfp8 = (s.flags & MOE_SHAPE_MXFP8) != 0;
     w.x_codes = b + L.x_codes;
     w.x_scales = b + L.x_scales;
@@ -175,32 +180,38 @@ GemmLaunch base_launch(const moe_shape_t &s, const Ws &w, const DeviceState &d) 
     return p;
 }
 
-// Stage 1: tensor maps + launch (metadata must already be in ws). With h, the
-// pre-activation is stored too (a, h gate and h up in 32 x 32 boxes).
+// Stage 1: the dispatch (x rows copied into routed order), then tensor maps +
+// launch (metadata must already be in ws). The dispatched rows go to obuf, idle
+// until stage 2 writes its rows there, or with h (training) to xp, which the
+// backward reads again. With h, the pre-activation is stored too (a, h gate and
+// h up in 32 x 32 boxes).
 moe_status_t run_gemm1(const moe_shape_t &s, const void *x, const void *w1, void *a, void *h, const Ws &w,
                        const DeviceState &d, cudaStream_t st) {
-    // the x rows are gathered by the kernel's own warps; only w1 goes through TMA
     const uint64_t R = static_cast<uint64_t>(s.T) * s.k;
-    CUtensorMap tm_w1, tm_out, tm_hg, tm_hu;
+    __nv_bfloat16 *xp = h ? w.xp : w.obuf;
+    CUtensorMap tm_x, tm_w1, tm_out, tm_hg, tm_hu;
     const uint32_t box = h ? 32 : 64;
-    if (!encode_bf16_2d(&tm_w1, w1, s.H, static_cast<uint64_t>(s.E) * 2 * s.I, kBK, 128) ||
+    if (!encode_bf16_2d(&tm_x, xp, s.H, R, kBK, 128) ||
+        !encode_bf16_2d(&tm_w1, w1, s.H, static_cast<uint64_t>(s.E) * 2 * s.I, kBK, 128) ||
         !encode_bf16_2d(&tm_out, a, s.I, R, box, 32))
+        return MOE_ERR_CUDA;
+    if (launch_gather_rows(static_cast<const __nv_bfloat16 *>(x), w.perm_slot, w.offsets + s.E, s.k,
+                           static_cast<int64_t>(R), s.H, xp, nullptr, nullptr, st) != cudaSuccess)
         return MOE_ERR_CUDA;
     if (h && (!encode_bf16_2d_strided(&tm_hg, h, s.I, R, 2 * s.I, 32, 32) ||
               !encode_bf16_2d_strided(&tm_hu, static_cast<__nv_bfloat16 *>(h) + s.I, s.I, R, 2 * s.I, 32, 32)))
         return MOE_ERR_CUDA;
     GemmLaunch p = base_launch(s, w, d);
+    p.tm_a = &tm_x;
     p.tm_b = &tm_w1;
     p.tm_out = &tm_out;
     p.tm_out2 = h ? &tm_hg : nullptr;
     p.tm_out3 = h ? &tm_hu : nullptr;
-    p.src = static_cast<const __nv_bfloat16 *>(x);
     p.sched = w.sched1;
     p.out = static_cast<__nv_bfloat16 *>(a);
     p.out2 = static_cast<__nv_bfloat16 *>(h);
     p.out3 = h ? static_cast<__nv_bfloat16 *>(h) + s.I : nullptr;
     p.K = static_cast<int>(s.H);
-    p.src_cols = static_cast<int>(s.H);
     p.n_out = static_cast<int>(s.I);
     p.n_tile = kBN / 2;
     p.b_rows = static_cast<int>(2 * s.I);
