@@ -305,7 +305,8 @@ moe_status_t moe_dispatch_gemm1_train(const void *x, const void *w1, const moe_s
  *
  * dy bf16 [T,H]; topk_w fp32 [T,k]; w2 bf16 [E,H,I]; h from
  * moe_dispatch_gemm1_train; dtopk_w fp32 [T,k] (output, 0 for dropped slots)
- * or NULL. dH = [dG | dU] and w a stay in the workspace for the other
+ * or NULL. dY's rows are first copied into routed order (workspace region
+ * dyp); they, dH = [dG | dU] and w a stay in the workspace for the other
  * backward calls.
  */
 moe_status_t moe_backward_stage2_data(const void *dy, const float *topk_w, const void *w2, const void *h,
@@ -315,7 +316,9 @@ moe_status_t moe_backward_stage2_data(const void *dy, const float *topk_w, const
 /*
  * Stage 2 backward, weight part: dW2[e] = sum over e's rows of dY[t]^T (w a)[r]
  * into dw2 bf16 [E,H,I] (every expert written; experts without rows get 0).
- * Needs moe_backward_stage2_data on this workspace.
+ * Needs moe_backward_stage2_data on this workspace: the dY rows are read from
+ * the routed-order copy that call made, so dy must be the tensor given there
+ * (it is only checked for NULL and alignment).
  */
 moe_status_t moe_backward_stage2_weight(const void *dy, const moe_shape_t *shape, void *dw2, void *ws,
                                         size_t ws_bytes, void *stream);
@@ -351,7 +354,10 @@ moe_status_t moe_backward_stage1_data(const void *w1, const float *w_r, const in
 /*
  * Stage 1 backward, weight part: dW1[e] = sum over e's rows of dH[r]^T x[t]
  * into dw1 bf16 [E,2I,H] (every expert written; experts without rows get 0).
- * x bf16 [T,H]. Needs moe_backward_stage2_data on this workspace.
+ * x bf16 [T,H]. Needs moe_dispatch_gemm1_train and moe_backward_stage2_data on
+ * this workspace: the x rows are read from the routed-order copy that the
+ * training forward made, so x must be the tensor given there (it is only
+ * checked for NULL and alignment).
  */
 moe_status_t moe_backward_stage1_weight(const void *x, const moe_shape_t *shape, void *dw1, void *ws,
                                         size_t ws_bytes, void *stream);

@@ -19,17 +19,17 @@
 //
 // Backward modes (the guide's stage order: stage 2's backward yields dW2, then
 // stage 1's yields dW1; everything else is the chain rule of the forward):
-//   kBwdDA   dA_u[r] = dY[token(r)] . w2[e] (dY rows gathered like x in stage 1,
-//            w2[e] read MN-major). The epilogue applies the SwiGLU backward with
+//   kBwdDA   dA_u[r] = dY[token(r)] . w2[e] (dY rows dispatched into routed order
+//            like x in stage 1, w2[e] read MN-major). The epilogue applies the SwiGLU backward with
 //            the saved h: dA = w dA_u, dU = dA silu(g), dG = dA u silu'(g), and
 //            stores dH = [dG | dU], the weighted activations w a (for dW2) and
 //            per-tile partial sums of dA_u . a (the routing-weight gradient).
 //   kBwdDX   dXr[r] = dH[r] . w1[e] (w1[e] read MN-major), unweighted rows in
 //            routed order, summed per token afterwards.
 //   kBwdDW2  dW2[e] = sum over e's rows of dY[token(r)]^T (w a)[r]: M = H,
-//            N = I, K = the expert's rows; dY rows gathered MN-major.
+//            N = I, K = the expert's rows; dispatched dY rows read MN-major.
 //   kBwdDW1  dW1[e] = sum over e's rows of dH[r]^T x[token(r)]: M = 2I, N = H,
-//            K = the expert's rows; x rows gathered MN-major.
+//            K = the expert's rows; dispatched x rows read MN-major.
 //
 // Kernel design (one CTA per SM, persistent):
 //   work unit  = (expert e, n-tile, 256-row tile of e's routed rows) for the
@@ -47,7 +47,8 @@
 //                16-deep k-step one M=128 N=256 MMA per half into two fp32
 //                TMEM accumulators (all 512 columns).
 //   warps 2-9  = epilogue, one TMEM lane quadrant of one half each.
-//   warps 10-13 (gathering modes) = cp.async row gathers into the A or B tiles.
+//   warps 10-13 (weight gradients) = zero the K rows past the expert's count in
+//                the last k-block; (MXFP8) = the scale factors of every stage.
 // Operands are K-major (rows of K contiguous, 128- or 64-byte swizzle) or
 // MN-major (K rows of 64-element, 128-byte swizzled MN atoms; the atoms of one
 // tile are BK * 128 bytes apart, 8-row K groups 1024 bytes apart).
@@ -77,8 +78,8 @@ constexpr int MN_ATOM_BYTES = BK * 128;      // one 64-wide MN atom over the sta
 constexpr int TMEM_COLS = 2 * BN;            // two accumulators: all 512 columns
 constexpr int EPI_WARPS = 8;
 constexpr int EPI_THREADS = EPI_WARPS * 32;
-constexpr int GATHER_WARPS = 4;
-constexpr int GATHER_THREADS = GATHER_WARPS * 32;
+constexpr int HELPER_WARPS = 4;
+constexpr int HELPER_THREADS = HELPER_WARPS * 32;
 constexpr int UQ = 4;                        // depth of the in-CTA unit queue
 constexpr uint64_t kDrainLimitNs = 10000000ull;  // 10 ms
 
@@ -92,18 +93,12 @@ enum Mode : int {
 
 template <int MODE> constexpr bool kIsMx = MODE == kStage1Mx || MODE == kStage2Mx;
 template <int MODE> constexpr bool kIsStage1 = MODE == kStage1 || MODE == kStage1SaveH || MODE == kStage1Mx;
-// A is filled by the K-major row gather (token rows of dY); stage 1 reads x rows
-// already dispatched into routed order
-template <int MODE> constexpr bool kGatherK = MODE == kBwdDA;
-// the MN-major row gather fills A (dW2: dY rows) or B (dW1: x rows)
-template <int MODE> constexpr bool kGatherMnA = MODE == kBwdDW2;
-template <int MODE> constexpr bool kGatherMnB = MODE == kBwdDW1;
-template <int MODE> constexpr bool kGathers = kGatherK<MODE> || kGatherMnA<MODE> || kGatherMnB<MODE>;
 template <int MODE> constexpr bool kAMn = MODE == kBwdDW2 || MODE == kBwdDW1;
 template <int MODE> constexpr bool kBMn = MODE >= kBwdDA && MODE <= kBwdDW1;
 template <int MODE> constexpr bool kWeightGrad = MODE == kBwdDW2 || MODE == kBwdDW1;
-// warps 10..13: row gathers, and in the MXFP8 modes the scale factors
-template <int MODE> constexpr bool kHelpers = kGathers<MODE> || kIsMx<MODE>;
+// warps 10..13: the reduction-tail zeroing of the weight gradients, and in the
+// MXFP8 modes the scale factors
+template <int MODE> constexpr bool kHelpers = kWeightGrad<MODE> || kIsMx<MODE>;
 // accumulator columns of one 128-row half (a unit's output columns): 2 x 96
 // (gate, up) in stage 1 MXFP8, 224 in stage 2 MXFP8, else 256; the MXFP8 modes
 // keep the rest of tensor memory for per-stage scale factors
@@ -120,7 +115,7 @@ static_assert(BK == 64, "the MXFP8 modes share the 128-byte stage rows of BK = 6
 
 // warps: 0 scheduler + TMA producer, 1 MMA issuer, 2..9 epilogue, 10..13 helpers
 template <int MODE>
-constexpr int kNumThreads = 64 + EPI_THREADS + (kHelpers<MODE> ? GATHER_THREADS : 0);
+constexpr int kNumThreads = 64 + EPI_THREADS + (kHelpers<MODE> ? HELPER_THREADS : 0);
 
 template <int MODE>
 constexpr uint32_t kIdesc = idesc_bf16_f32(BM, BN) | (kAMn<MODE> ? (1u << 15) : 0u) |
@@ -137,6 +132,8 @@ struct __align__(1024) Smem {
     uint64_t uq_full[UQ];
     uint64_t uq_empty[UQ];
     uint64_t drain;
+    uint64_t tail_ready;                     // weight gradients: the MMA issuer saw a partial k-block land
+    uint64_t tail_fixed;                     // ... and the helpers zeroed its rows past the expert's count
     int unit_q[UQ];
     uint32_t tmem_base;
     int abort;
@@ -158,7 +155,6 @@ struct GemmArgs {
     const int32_t *offsets;
     const int32_t *mt_prefix;
     const int32_t *perm_slot;
-    const __nv_bfloat16 *src;   // gathered token rows [T, src_cols]: x or dY
     const __nv_bfloat16 *h;     // dA: saved pre-activation [R, 2I]
     int32_t *err;
     int32_t *sched;             // [0] next unit, [1] CTAs finished
@@ -171,7 +167,6 @@ struct GemmArgs {
     const uint8_t *sfb;         // MXFP8: E8M0 scales of the weight rows
     uint8_t *out_sf;            // stage 1 MXFP8: scales of a [R, I / 32]
     int E, k, K;
-    int src_cols;               // valid columns of a gathered source row
     int n_out;                  // valid output columns
     int n_tiles;                // n-tiles per expert (grouped) or per row tile (router)
     int m_total, m_tiles;       // weight gradients: output rows per expert, 256-row tiles
@@ -379,17 +374,19 @@ tc_gemm_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs g) {
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
-            // gathering modes: the producer's expect_tx arrival plus one per gather thread
-            mbar_init(smem_addr(&sm.full[s]), kHelpers<MODE> ? 1 + GATHER_THREADS : 1);
+            // MXFP8: the producer's expect_tx arrival plus one per scale-factor thread
+            mbar_init(smem_addr(&sm.full[s]), kIsMx<MODE> ? 1 + HELPER_THREADS : 1);
             mbar_init(smem_addr(&sm.empty[s]), 1);
         }
         mbar_init(smem_addr(&sm.acc_full), 1);
         mbar_init(smem_addr(&sm.acc_empty), EPI_THREADS);
         for (int s = 0; s < UQ; ++s) {
             mbar_init(smem_addr(&sm.uq_full[s]), 1);
-            mbar_init(smem_addr(&sm.uq_empty[s]), 1 + EPI_WARPS + (kHelpers<MODE> ? GATHER_WARPS : 0));
+            mbar_init(smem_addr(&sm.uq_empty[s]), 1 + EPI_WARPS + (kHelpers<MODE> ? HELPER_WARPS : 0));
         }
         mbar_init(smem_addr(&sm.drain), 1);
+        mbar_init(smem_addr(&sm.tail_ready), 1);
+        mbar_init(smem_addr(&sm.tail_fixed), HELPER_THREADS);
         sm.abort = 0;
         fence_mbar_init();
         tma_prefetch_desc(&maps.a);
@@ -430,10 +427,8 @@ tc_gemm_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs g) {
 
             const Unit t = decode_unit<MODE>(u, g);
             const bool two = t.rows > BM;            // second half present
-            uint32_t tx_bytes;
-            if constexpr (kGatherK<MODE> || kGatherMnA<MODE>) tx_bytes = kUnitN<MODE> * 128;    // A gathered
-            else if constexpr (kGatherMnB<MODE>) tx_bytes = two ? A_BYTES : A_HALF_BYTES;  // B gathered
-            else tx_bytes = (two ? A_BYTES : A_HALF_BYTES) + kUnitN<MODE> * 128;
+            // one or two 128-row halves of A (K-major rows or MN-major atoms) and the B tile
+            const uint32_t tx_bytes = (two ? A_BYTES : A_HALF_BYTES) + kUnitN<MODE> * 128;
             for (int kb = t.kb0; kb < t.kb1; ++kb) {
                 bool e_ok = true;
                 if (lane == 0) e_ok = mbar_wait(smem_addr(&sm.empty[stage]), phase ^ 1u, abort_flag, g.err);
@@ -464,22 +459,24 @@ tc_gemm_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs g) {
                         if (two) tma_load_2d(sa + A_HALF_BYTES, &maps.a, kx, t.row0 + BM, full);
                         tma_load_2d(sb, &maps.b, kx, seg * g.E + t.n * BN, full);
                     } else if constexpr (MODE == kBwdDA || MODE == kBwdDX) {
-                        if constexpr (MODE == kBwdDX) {
-                            tma_load_2d(sa, &maps.a, kb * BK, t.row0, full);
-                            if (two) tma_load_2d(sa + A_HALF_BYTES, &maps.a, kb * BK, t.row0 + BM, full);
-                        }
+                        // dA: dispatched dY rows; dX: dH rows
+                        tma_load_2d(sa, &maps.a, kb * BK, t.row0, full);
+                        if (two) tma_load_2d(sa + A_HALF_BYTES, &maps.a, kb * BK, t.row0 + BM, full);
                         // weight slab of expert e, MN-major: K rows kb*BK.., four 64-wide atoms
 #pragma unroll
                         for (int j = 0; j < 4; ++j)
                             tma_load_3d(sb + j * MN_ATOM_BYTES, &maps.b, t.n * BN + 64 * j, kb * BK, t.e, full);
-                    } else if constexpr (MODE == kBwdDW2) {
-#pragma unroll
-                        for (int j = 0; j < 4; ++j)
-                            tma_load_2d(sb + j * MN_ATOM_BYTES, &maps.b, t.n * BN + 64 * j, t.koff + kb * BK, full);
-                    } else {  // kBwdDW1: dH columns of the m-tile, MN-major
+                    } else {
+                        // weight gradients, MN-major over K = the expert's routed rows:
+                        // A = the m-tile's columns of the dispatched dY rows (dW2) or of
+                        // dH (dW1), B = the n-tile's columns of w a (dW2) or of the
+                        // dispatched x rows (dW1)
                         const int na = two ? 4 : 2;
                         for (int j = 0; j < na; ++j)
                             tma_load_2d(sa + j * MN_ATOM_BYTES, &maps.a, t.row0 + 64 * j, t.koff + kb * BK, full);
+#pragma unroll
+                        for (int j = 0; j < 4; ++j)
+                            tma_load_2d(sb + j * MN_ATOM_BYTES, &maps.b, t.n * BN + 64 * j, t.koff + kb * BK, full);
                     }
                 }
                 __syncwarp();
@@ -501,7 +498,7 @@ tc_gemm_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs g) {
         // ------------------------------------------------ MMA issuer
         if (lane == 0) {
             int stage = 0, q = 0;
-            uint32_t phase = 0, acc_phase = 0, qphase = 0;
+            uint32_t phase = 0, acc_phase = 0, qphase = 0, tail_phase = 0;
             bool ok = true, any = false;
             while (true) {
                 if (!mbar_wait(smem_addr(&sm.uq_full[q]), qphase, abort_flag, g.err)) { ok = false; break; }
@@ -523,6 +520,18 @@ tc_gemm_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs g) {
                         break;
                     }
                     tc_fence_after();
+                    if constexpr (kWeightGrad<MODE>) {
+                        if (kb == t.kb1 - 1 && t.kcount % BK != 0) {
+                            // the helpers zero this block's K rows past the expert's count first
+                            mbar_arrive(smem_addr(&sm.tail_ready));
+                            if (!mbar_wait(smem_addr(&sm.tail_fixed), tail_phase, abort_flag, g.err)) {
+                                ok = false;
+                                break;
+                            }
+                            tail_phase ^= 1u;
+                            tc_fence_after();
+                        }
+                    }
                     const uint32_t sa = smem_addr(sm.a[stage]);
                     const uint32_t sb = smem_addr(sm.b[stage]);
                     if constexpr (kIsMx<MODE>) {
@@ -898,18 +907,21 @@ tc_gemm_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs g) {
         }
         if (lane == 0) bulk_wait<0>();                  // every output box written
     } else {
-        // ------------------------------------------------ row gathers
-        // The row gathers of the backward (dY rows for dA and dW2, x rows for
-        // dW1): 128 threads copy routed token rows straight into the 128B-swizzled tiles
-        // with 16-byte cp.async. Each thread waits for its own copies, orders them
-        // before the tensor core's async-proxy reads, then arrives on the stage's
-        // full barrier, one stage behind its issue so that two stages of copies
-        // are in flight.
-        const int gt = threadIdx.x - (64 + EPI_THREADS);
-        int stage = 0, q = 0, pending = -1;
-        uint32_t phase = 0, qphase = 0;
-        while (true) {
-            bool ok = true;
+        // ------------------------------------------------ helpers
+        // Weight gradients: the reduction runs over the expert's routed rows, so
+        // the tiles of its last, partial k-block also hold rows past its count
+        // (the next expert's rows, or rows never written). When the MMA issuer
+        // has seen such a block land it signals tail_ready; these 128 threads
+        // then zero the block's K rows >= count in the dispatched operand (dY
+        // rows: dW2's A; x rows: dW1's B) and signal tail_fixed. The other
+        // operand's rows there are finite (dH and w a have their dropped-slot
+        // rows zeroed), so the padding adds nothing.
+        // MXFP8 modes: each stage's scale factors into tensor memory.
+        const int ht = threadIdx.x - (64 + EPI_THREADS);
+        int stage = 0, q = 0;
+        uint32_t phase = 0, qphase = 0, tail_phase = 0;
+        bool ok = true;
+        while (ok) {
             int u = -1;
             if (lane == 0) {
                 ok = mbar_wait(smem_addr(&sm.uq_full[q]), qphase, abort_flag, g.err);
@@ -923,92 +935,27 @@ tc_gemm_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs g) {
             if (++q == UQ) { q = 0; qphase ^= 1u; }
             if (!ok || u < 0) break;
             const Unit t = decode_unit<MODE>(u, g);
-            if constexpr (kGatherK<MODE>) {
-                // K-major A rows: one thread per 16-byte chunk of a row slice; rows past
-                // the unit's count are left as they are (never stored).
-                constexpr int CHUNKS = ROW_BYTES / 16;                 // per row slice
-                constexpr int RSTEP = GATHER_THREADS / CHUNKS;         // rows per pass
-                constexpr int NROWS = UM / RSTEP;                      // rows per thread
-                const int chunk = gt % CHUNKS;
-                const int rg = gt / CHUNKS;                            // rows rg + RSTEP i
-                const char *srcb = reinterpret_cast<const char *>(g.src);
-                const int64_t ldb = static_cast<int64_t>(g.src_cols) * kElemBytes<MODE>;
-                int tok[NROWS];
-#pragma unroll
-                for (int i = 0; i < NROWS; ++i) {
-                    const int r = rg + RSTEP * i;
-                    tok[i] = (r < t.rows) ? g.perm_slot[t.row0 + r] / g.k : -1;
+            if constexpr (kWeightGrad<MODE>) {
+                const int nkb = t.kb1 - t.kb0;
+                const int rem = t.kcount % BK;
+                if (nkb > 0 && rem != 0) {
+                    if (lane == 0) ok = mbar_wait(smem_addr(&sm.tail_ready), tail_phase, abort_flag, g.err);
+                    ok = __shfl_sync(0xffffffffu, ok, 0);
+                    if (!ok) break;
+                    tail_phase ^= 1u;
+                    const int tail = (stage + nkb - 1) % STAGES;
+                    const uint32_t base = smem_addr(MODE == kBwdDW2 ? sm.a[tail] : sm.b[tail]);
+                    const int atoms = (MODE == kBwdDW2 && t.rows <= BM) ? 2 : 4;
+                    const int per_atom = (BK - rem) * (128 / 16);          // 16-byte chunks of rows rem..BK-1
+                    for (int i = ht; i < atoms * per_atom; i += HELPER_THREADS) {
+                        const int at = i / per_atom;
+                        st_shared_v4(base + at * MN_ATOM_BYTES + rem * 128 + (i - at * per_atom) * 16, 0u, 0u, 0u,
+                                     0u);
+                    }
+                    fence_proxy_async_smem();
+                    mbar_arrive(smem_addr(&sm.tail_fixed));
                 }
-                for (int kb = t.kb0; kb < t.kb1; ++kb) {
-                    bool e_ok = true;
-                    if (lane == 0) e_ok = mbar_wait(smem_addr(&sm.empty[stage]), phase ^ 1u, abort_flag, g.err);
-                    e_ok = __shfl_sync(0xffffffffu, e_ok, 0);
-                    if (!e_ok) { ok = false; break; }
-                    const int colb = kb * ROW_BYTES + chunk * 16;
-                    const uint32_t nbytes = colb < g.K * kElemBytes<MODE> ? 16u : 0u;   // zero-fill the K tail
-                    const uint32_t sa = smem_addr(sm.a[stage]);
-#pragma unroll
-                    for (int i = 0; i < NROWS; ++i) {
-                        if (tok[i] >= 0) {
-                            const int r = rg + RSTEP * i;
-                            const uint32_t dst = sa + (r >> 7) * A_HALF_BYTES +
-                                                 swizzled_chunk<ROW_BYTES>(r & (BM - 1), chunk);
-                            cp_async_16(dst, srcb + static_cast<int64_t>(tok[i]) * ldb + (nbytes ? colb : 0), nbytes);
-                        }
-                    }
-                    cp_async_commit();
-                    if (pending >= 0) {
-                        cp_async_wait<1>();
-                        fence_proxy_async_smem();
-                        mbar_arrive(smem_addr(&sm.full[pending]));
-                    }
-                    pending = stage;
-                    if (++stage == STAGES) { stage = 0; phase ^= 1u; }
-                }
-            } else if constexpr (kGatherMnA<MODE> || kGatherMnB<MODE>) {
-                // MN-major tile over the expert's routed rows (the reduction): warp w
-                // copies K rows w, w + 4, ...; lane c8 the 16-byte chunk c8 of the
-                // 256-column slice. K rows past the expert's count and columns past
-                // the source width are zero-filled, so they add nothing. Lane l < NR
-                // looks up the token of the warp's l-th row one stage ahead; the
-                // copies take it by shuffle.
-                constexpr int NR = BK / GATHER_WARPS;
-                static_assert(NR <= 32, "one token per lane");
-                const int c8 = gt & 31;
-                const int kr0 = gt >> 5;
-                const int col = (kGatherMnA<MODE> ? t.row0 : t.n * BN) + c8 * 8;
-                const bool col_ok = col < g.src_cols;
-                const uint32_t chunk_off = static_cast<uint32_t>(c8 >> 3) * MN_ATOM_BYTES;
-                auto token_of = [&](int kb) {
-                    const int kk = kb * BK + kr0 + GATHER_WARPS * lane;
-                    return (lane < NR && kb < t.kb1 && kk < t.kcount) ? g.perm_slot[t.koff + kk] / g.k : -1;
-                };
-                int tok_next = token_of(t.kb0);
-                for (int kb = t.kb0; kb < t.kb1; ++kb) {
-                    const int tok_cur = tok_next;
-                    tok_next = token_of(kb + 1);
-                    bool e_ok = true;
-                    if (lane == 0) e_ok = mbar_wait(smem_addr(&sm.empty[stage]), phase ^ 1u, abort_flag, g.err);
-                    e_ok = __shfl_sync(0xffffffffu, e_ok, 0);
-                    if (!e_ok) { ok = false; break; }
-                    const uint32_t base = smem_addr(kGatherMnA<MODE> ? sm.a[stage] : sm.b[stage]) + chunk_off;
-#pragma unroll
-                    for (int i = 0; i < NR; ++i) {
-                        const int tok = __shfl_sync(0xffffffffu, tok_cur, i);
-                        const bool ok_r = col_ok && tok >= 0;
-                        cp_async_16(base + swizzled_chunk<128>(kr0 + GATHER_WARPS * i, c8 & 7),
-                                    g.src + static_cast<int64_t>(ok_r ? tok : 0) * g.src_cols + (ok_r ? col : 0),
-                                    ok_r ? 16u : 0u);
-                    }
-                    cp_async_commit();
-                    if (pending >= 0) {
-                        cp_async_wait<1>();
-                        fence_proxy_async_smem();
-                        mbar_arrive(smem_addr(&sm.full[pending]));
-                    }
-                    pending = stage;
-                    if (++stage == STAGES) { stage = 0; phase ^= 1u; }
-                }
+                stage = (stage + nkb) % STAGES;
             } else if constexpr (kIsMx<MODE>) {
                 // A and B arrive through TMA; these warps only write the scale factors
                 int64_t a_off[8], b_off[8];
@@ -1017,10 +964,9 @@ tc_gemm_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs g) {
                 load_scales(g, t.kb0, t.kb0 < t.kb1, a_off, b_off, sfw);
                 const uint32_t sf_lane = tmem_base + (static_cast<uint32_t>((warp & 3) * 32) << 16) + kSfBase<MODE>;
                 for (int kb = t.kb0; kb < t.kb1; ++kb) {
-                    bool e_ok = true;
-                    if (lane == 0) e_ok = mbar_wait(smem_addr(&sm.empty[stage]), phase ^ 1u, abort_flag, g.err);
-                    e_ok = __shfl_sync(0xffffffffu, e_ok, 0);
-                    if (!e_ok) { ok = false; break; }
+                    if (lane == 0) ok = mbar_wait(smem_addr(&sm.empty[stage]), phase ^ 1u, abort_flag, g.err);
+                    ok = __shfl_sync(0xffffffffu, ok, 0);
+                    if (!ok) break;
                     tc_fence_after();
                     tmem_st16(sf_lane + stage * kSfStride, sfw);
                     load_scales(g, kb + 1, kb + 1 < t.kb1, a_off, b_off, sfw);
@@ -1030,15 +976,7 @@ tc_gemm_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs g) {
                     if (++stage == STAGES) { stage = 0; phase ^= 1u; }
                 }
             }
-            if (pending >= 0) {                       // signal the unit's last stage
-                cp_async_wait<0>();
-                fence_proxy_async_smem();
-                mbar_arrive(smem_addr(&sm.full[pending]));
-                pending = -1;
-            }
-            if (!ok) break;
         }
-        cp_async_wait<0>();                           // no copy in flight at exit
     }
 
     tc_fence_before();
@@ -1064,7 +1002,6 @@ inline GemmArgs grouped_args(const GemmLaunch &p) {
     g.offsets = p.offsets;
     g.mt_prefix = p.mt_prefix;
     g.perm_slot = p.perm_slot;
-    g.src = p.src;
     g.h = p.h;
     g.err = p.err;
     g.sched = p.sched;
@@ -1079,7 +1016,6 @@ inline GemmArgs grouped_args(const GemmLaunch &p) {
     g.E = p.E;
     g.k = p.k;
     g.K = p.K;
-    g.src_cols = p.src_cols;
     g.n_out = p.n_out;
     g.n_tiles = (p.n_out + p.n_tile - 1) / p.n_tile;
     g.m_total = p.m_total;

@@ -127,7 +127,6 @@ struct GemmLaunch {
     const CUtensorMap *tm_out2;
     const CUtensorMap *tm_out3;
     const int32_t *counts, *offsets, *mt_prefix, *perm_slot;
-    const __nv_bfloat16 *src;   // token rows gathered by the kernel: x or dY [T, src_cols]
     const __nv_bfloat16 *h;     // backward dA: saved pre-activation [R, 2I]
     int32_t *err;
     int32_t *sched;             // [2] unit scheduler of this launch
@@ -139,7 +138,6 @@ struct GemmLaunch {
     uint8_t *out_sf;            // stage 1 MXFP8: E8M0 scales of a [R, I / 32]
     int E, k;
     int K;                      // reduction length of the row-grouped modes
-    int src_cols;               // columns of a gathered source row
     int n_out;                  // output columns
     int n_tile;                 // output columns per unit (128 for stage 1, else 256)
     int m_total;                // weight gradients: output rows per expert

@@ -321,28 +321,34 @@ moe_status_t run_gemm2_mx(const moe_shape_t &s, const void *aq, const void *as, 
     return cuda_status(launch_combine(c, st));
 }
 
-// Stage 2 backward, data: rows of dropped slots zeroed, dA GEMM with the SwiGLU
-// backward epilogue, then the routing-weight gradient.
+// Stage 2 backward, data: dY's rows dispatched into routed order (dyp, read
+// again by the weight part), rows of dropped slots zeroed, dA GEMM with the
+// SwiGLU backward epilogue, then the routing-weight gradient.
 moe_status_t run_bwd_stage2_data(const moe_shape_t &s, const void *dy, const float *topk_w, const void *w2,
                                  const void *h, float *dtopk_w, const Ws &w, const DeviceState &d,
                                  cudaStream_t st) {
     const uint64_t R = static_cast<uint64_t>(s.T) * s.k;
-    CUtensorMap tm_w2, tm_dg, tm_du, tm_aw;
+    CUtensorMap tm_dy, tm_w2, tm_dg, tm_du, tm_aw;
     // w2 [E, H, I] read MN-major: K = H rows of expert e, N = I
-    if (!encode_bf16_3d(&tm_w2, w2, s.I, s.H, s.E, 64, kBK) ||
+    if (!encode_bf16_2d(&tm_dy, w.dyp, s.H, R, kBK, 128) ||
+        !encode_bf16_3d(&tm_w2, w2, s.I, s.H, s.E, 64, kBK) ||
         !encode_bf16_2d_strided(&tm_dg, w.dh, s.I, R, 2 * s.I, 32, 32) ||
         !encode_bf16_2d_strided(&tm_du, w.dh + s.I, s.I, R, 2 * s.I, 32, 32) ||
         !encode_bf16_2d(&tm_aw, w.aw, s.I, R, 32, 32))
         return MOE_ERR_CUDA;
-    moe_status_t r = cuda_status(launch_zero_tail_rows(w.dh, w.aw, w.offsets + s.E, static_cast<int>(R),
-                                                      static_cast<int>(s.I), st));
+    moe_status_t r = cuda_status(launch_gather_rows(static_cast<const __nv_bfloat16 *>(dy), w.perm_slot,
+                                                    w.offsets + s.E, s.k, static_cast<int64_t>(R), s.H, w.dyp,
+                                                    nullptr, nullptr, st));
+    if (r != MOE_OK) return r;
+    r = cuda_status(launch_zero_tail_rows(w.dh, w.aw, w.offsets + s.E, static_cast<int>(R), static_cast<int>(s.I),
+                                          st));
     if (r != MOE_OK) return r;
     GemmLaunch p = base_launch(s, w, d);
+    p.tm_a = &tm_dy;
     p.tm_b = &tm_w2;
     p.tm_out = &tm_dg;
     p.tm_out2 = &tm_du;
     p.tm_out3 = &tm_aw;
-    p.src = static_cast<const __nv_bfloat16 *>(dy);
     p.h = static_cast<const __nv_bfloat16 *>(h);
     p.sched = w.sched_da;
     p.topk_w = topk_w;
@@ -351,7 +357,6 @@ moe_status_t run_bwd_stage2_data(const moe_shape_t &s, const void *dy, const flo
     p.out3 = w.aw;
     p.dtw_part = w.dtw_part;
     p.K = static_cast<int>(s.H);
-    p.src_cols = static_cast<int>(s.H);
     p.n_out = static_cast<int>(s.I);
     p.n_tile = kBN;
     p.half = static_cast<int>(s.I);
@@ -369,21 +374,21 @@ moe_status_t run_bwd_stage2_data(const moe_shape_t &s, const void *dy, const flo
     return cuda_status(launch_dtw_reduce(q, st));
 }
 
-// Stage 2 backward, weights: dW2[e] (M = H rows, N = I, K = e's rows): A = dY
-// rows gathered MN-major, B = w a rows through TMA.
-moe_status_t run_bwd_stage2_weight(const moe_shape_t &s, const void *dy, void *dw2, const Ws &w,
-                                   const DeviceState &d, cudaStream_t st) {
+// Stage 2 backward, weights: dW2[e] (M = H rows, N = I, K = e's rows): A = the
+// dY rows dispatched by the data part, B = w a rows, both MN-major through TMA.
+moe_status_t run_bwd_stage2_weight(const moe_shape_t &s, void *dw2, const Ws &w, const DeviceState &d,
+                                   cudaStream_t st) {
     const uint64_t R = static_cast<uint64_t>(s.T) * s.k;
-    CUtensorMap tm_aw_mn, tm_dw2;
-    if (!encode_bf16_2d(&tm_aw_mn, w.aw, s.I, R, 64, kBK) ||
+    CUtensorMap tm_dy_mn, tm_aw_mn, tm_dw2;
+    if (!encode_bf16_2d(&tm_dy_mn, w.dyp, s.H, R, 64, kBK) ||
+        !encode_bf16_2d(&tm_aw_mn, w.aw, s.I, R, 64, kBK) ||
         !encode_bf16_3d(&tm_dw2, dw2, s.I, s.H, s.E, 64, 32))
         return MOE_ERR_CUDA;
     GemmLaunch q = base_launch(s, w, d);
+    q.tm_a = &tm_dy_mn;
     q.tm_b = &tm_aw_mn;
     q.tm_out = &tm_dw2;
-    q.src = static_cast<const __nv_bfloat16 *>(dy);
     q.sched = w.sched_dw2;
-    q.src_cols = static_cast<int>(s.H);
     q.n_out = static_cast<int>(s.I);
     q.n_tile = kBN;
     q.m_total = static_cast<int>(s.H);
@@ -454,21 +459,21 @@ moe_status_t run_bwd_stage1_data(const moe_shape_t &s, const void *w1, const flo
 }
 
 // Stage 1 backward, weights: dW1[e] (M = 2I rows, N = H, K = e's rows): A = dH
-// rows MN-major through TMA, B = x rows gathered MN-major.
-moe_status_t run_bwd_stage1_weight(const moe_shape_t &s, const void *x, void *dw1, const Ws &w,
-                                   const DeviceState &d, cudaStream_t st) {
+// rows, B = the x rows dispatched by the training forward (xp), both MN-major
+// through TMA.
+moe_status_t run_bwd_stage1_weight(const moe_shape_t &s, void *dw1, const Ws &w, const DeviceState &d,
+                                   cudaStream_t st) {
     const uint64_t R = static_cast<uint64_t>(s.T) * s.k;
-    CUtensorMap tm_dh_mn, tm_dw1;
+    CUtensorMap tm_dh_mn, tm_x_mn, tm_dw1;
     if (!encode_bf16_2d(&tm_dh_mn, w.dh, 2 * s.I, R, 64, kBK) ||
+        !encode_bf16_2d(&tm_x_mn, w.xp, s.H, R, 64, kBK) ||
         !encode_bf16_3d(&tm_dw1, dw1, s.H, 2 * s.I, s.E, 64, 32))
         return MOE_ERR_CUDA;
     GemmLaunch q = base_launch(s, w, d);
     q.tm_a = &tm_dh_mn;
-    q.tm_b = &tm_dh_mn;
+    q.tm_b = &tm_x_mn;
     q.tm_out = &tm_dw1;
-    q.src = static_cast<const __nv_bfloat16 *>(x);
     q.sched = w.sched_dw1;
-    q.src_cols = static_cast<int>(s.H);
     q.n_out = static_cast<int>(s.H);
     q.n_tile = kBN;
     q.m_total = static_cast<int>(2 * s.I);
@@ -833,7 +838,7 @@ moe_status_t moe_backward_stage2_weight(const void *dy, const moe_shape_t *shape
     if ((r = check_training(shape, ws, ws_bytes)) != MOE_OK) return r;
     DeviceState *d = nullptr;
     if ((r = device_state(&d)) != MOE_OK) return r;
-    return run_bwd_stage2_weight(*shape, dy, dw2, carve(ws, *shape), *d, st);
+    return run_bwd_stage2_weight(*shape, dw2, carve(ws, *shape), *d, st);
 }
 
 moe_status_t moe_router_backward(const void *x, const float *logits, const int32_t *topk_idx,
@@ -886,7 +891,7 @@ moe_status_t moe_backward_stage1_weight(const void *x, const moe_shape_t *shape,
     if ((r = check_training(shape, ws, ws_bytes)) != MOE_OK) return r;
     DeviceState *d = nullptr;
     if ((r = device_state(&d)) != MOE_OK) return r;
-    return run_bwd_stage1_weight(*shape, x, dw1, carve(ws, *shape), *d, st);
+    return run_bwd_stage1_weight(*shape, dw1, carve(ws, *shape), *d, st);
 }
 
 moe_status_t moe_backward(const void *x, const float *w_r, const float *logits, const int32_t *topk_idx,
