@@ -90,7 +90,7 @@ typedef struct moe_ws_layout {
     size_t mt_prefix;  /* int32 [E+1] prefix sum of ceil(counts/256) (row tiles) */
     size_t perm_slot;  /* int32 [T*k] flat slot t*k+j of each routed row */
     size_t row_of;     /* int32 [T*k] routed row of each slot, -1 if dropped */
-    size_t meta;       /* int32 [ceil(T*k/4096), E] per-chunk expert histograms (scratch) */
+    size_t meta;       /* int32 [ceil(T*k/1024), E] per-chunk expert histograms (scratch) */
     size_t router;     /* router scratch: fp32 split-K partial logits [s,T,E], bf16 split of w_r [3,E,H], sums, counts */
     size_t a;          /* bf16 [T*k, I] SwiGLU activations (moe_forward only) */
     size_t obuf;       /* bf16 [T*k, H] weighted expert outputs in routed-row order;

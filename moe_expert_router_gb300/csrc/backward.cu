@@ -155,52 +155,84 @@ router_dwr_kernel(const RouterBwdLaunch p, int chunks, int dense) {
     }
 }
 
+// dX[t, :] = sum over t's slots of the dX rows (slot order), plus the router
+// term sum_e dl[t, e] w_r[e, :] (expert order for the dense form, slot order
+// over first occurrences otherwise). One warp per token (grid-stride): lane
+// j < k holds slot j's row and, for the sparse router term, its expert and
+// logit gradient; every lane then handles 8-column groups lane, lane + 32, ...
+// (all lanes run the same passes, so the shuffles see the whole warp).
 __global__ void __launch_bounds__(256)
 combine_bwd_kernel(const CombineBwdLaunch p) {
+    const int lane = threadIdx.x & 31;
     const int groups = p.H >> 3;
-    const int64_t total = static_cast<int64_t>(p.T) * groups;
-    for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
-         i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-        const int t = static_cast<int>(i / groups);
-        const int c = static_cast<int>(i - static_cast<int64_t>(t) * groups) * 8;
-        float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    const int warps = gridDim.x * (blockDim.x >> 5);
+    for (int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); t < p.T; t += warps) {
         const int32_t *idx_t = p.topk_idx + static_cast<int64_t>(t) * p.k;
-        for (int j = 0; j < p.k; ++j) {
-            const int r = p.row_of[static_cast<int64_t>(t) * p.k + j];
-            if (r < 0) continue;
-            const uint4 v = __ldg(reinterpret_cast<const uint4 *>(p.xbuf + static_cast<int64_t>(r) * p.H + c));
-            const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
+        const float *dl_t = p.dl != nullptr ? p.dl + static_cast<int64_t>(t) * p.E : nullptr;
+        const int my_row = lane < p.k ? __ldg(&p.row_of[static_cast<int64_t>(t) * p.k + lane]) : -1;
+        int my_e = -1;
+        float my_d = 0.0f;
+        if (dl_t != nullptr && !p.dense && lane < p.k) {
+            const int e = idx_t[lane];
+            if (e >= 0 && e < p.E && first_slot(idx_t, lane, e)) {
+                my_e = e;
+                my_d = dl_t[e];
+            }
+        }
+        for (int g0 = 0; g0 < groups; g0 += 32) {
+            const int g = g0 + lane;
+            const bool live = g < groups;
+            const int c = g * 8;
+            float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+            for (int j0 = 0; j0 < p.k; j0 += 8) {
+                uint4 v[8];
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                acc[2 * q] += __uint_as_float(wv[q] << 16);
-                acc[2 * q + 1] += __uint_as_float(wv[q] & 0xffff0000u);
-            }
-        }
-        if (p.dl != nullptr) {
-            const float *dl_t = p.dl + static_cast<int64_t>(t) * p.E;
-            const int n = p.dense ? p.E : p.k;
-            for (int j = 0; j < n; ++j) {
-                int e = j;
-                if (!p.dense) {
-                    e = idx_t[j];
-                    if (e < 0 || e >= p.E || !first_slot(idx_t, j, e)) continue;
+                for (int jj = 0; jj < 8; ++jj) {
+                    const int r = __shfl_sync(0xffffffffu, my_row, (j0 + jj) & 31);
+                    v[jj] = (live && j0 + jj < p.k && r >= 0)
+                                ? __ldg(reinterpret_cast<const uint4 *>(p.xbuf + static_cast<int64_t>(r) * p.H + c))
+                                : make_uint4(0u, 0u, 0u, 0u);
                 }
-                const float d = dl_t[e];
-                const float4 *wr = reinterpret_cast<const float4 *>(p.w_r + static_cast<int64_t>(e) * p.H + c);
-                const float4 a = __ldg(wr), b = __ldg(wr + 1);
-                acc[0] = fmaf(d, a.x, acc[0]);
-                acc[1] = fmaf(d, a.y, acc[1]);
-                acc[2] = fmaf(d, a.z, acc[2]);
-                acc[3] = fmaf(d, a.w, acc[3]);
-                acc[4] = fmaf(d, b.x, acc[4]);
-                acc[5] = fmaf(d, b.y, acc[5]);
-                acc[6] = fmaf(d, b.z, acc[6]);
-                acc[7] = fmaf(d, b.w, acc[7]);
+#pragma unroll
+                for (int jj = 0; jj < 8; ++jj) {
+                    const uint32_t wv[4] = {v[jj].x, v[jj].y, v[jj].z, v[jj].w};
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        acc[2 * q] += __uint_as_float(wv[q] << 16);
+                        acc[2 * q + 1] += __uint_as_float(wv[q] & 0xffff0000u);
+                    }
+                }
             }
+            if (dl_t != nullptr) {
+                const int n = p.dense ? p.E : p.k;
+                for (int j = 0; j < n; ++j) {
+                    int e = j;
+                    float d;
+                    if (p.dense) {
+                        d = dl_t[e];
+                    } else {
+                        e = __shfl_sync(0xffffffffu, my_e, j & 31);
+                        d = __shfl_sync(0xffffffffu, my_d, j & 31);
+                        if (e < 0) continue;
+                    }
+                    if (!live) continue;
+                    const float4 *wr = reinterpret_cast<const float4 *>(p.w_r + static_cast<int64_t>(e) * p.H + c);
+                    const float4 a = __ldg(wr), b = __ldg(wr + 1);
+                    acc[0] = fmaf(d, a.x, acc[0]);
+                    acc[1] = fmaf(d, a.y, acc[1]);
+                    acc[2] = fmaf(d, a.z, acc[2]);
+                    acc[3] = fmaf(d, a.w, acc[3]);
+                    acc[4] = fmaf(d, b.x, acc[4]);
+                    acc[5] = fmaf(d, b.y, acc[5]);
+                    acc[6] = fmaf(d, b.z, acc[6]);
+                    acc[7] = fmaf(d, b.w, acc[7]);
+                }
+            }
+            if (live)
+                *reinterpret_cast<uint4 *>(p.dx + static_cast<int64_t>(t) * p.H + c) =
+                    make_uint4(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]),
+                               pack_bf16x2(acc[4], acc[5]), pack_bf16x2(acc[6], acc[7]));
         }
-        *reinterpret_cast<uint4 *>(p.dx + static_cast<int64_t>(t) * p.H + c) =
-            make_uint4(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]),
-                       pack_bf16x2(acc[4], acc[5]), pack_bf16x2(acc[6], acc[7]));
     }
 }
 
@@ -263,9 +295,8 @@ cudaError_t launch_router_dwr(const RouterBwdLaunch &p, cudaStream_t st) {
 }
 
 cudaError_t launch_combine_bwd(const CombineBwdLaunch &p, cudaStream_t st) {
-    const int64_t total = static_cast<int64_t>(p.T) * (p.H / 8);
-    if (total == 0) return cudaSuccess;
-    combine_bwd_kernel<<<grid_for(total, 256), 256, 0, st>>>(p);
+    if (p.T == 0 || p.H == 0) return cudaSuccess;
+    combine_bwd_kernel<<<grid_for(p.T, 8), 256, 0, st>>>(p);      // eight tokens (warps) per block
     note_launches(1);
     return cudaGetLastError();
 }

@@ -175,6 +175,7 @@ struct GemmArgs {
     int out_ld;                 // row stride (elements) of out / out2 / out3
     int R;                      // routed rows
     int T, splits, kb_per_split, kb_total, kb_h;   // router
+    int n_mma;                  // router: N of its MMAs and rows of its weight tile (E rounded up to 32, <= 256)
     int total_units;            // router / weight gradients: known on the host; else -1
 };
 
@@ -428,7 +429,7 @@ tc_gemm_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs g) {
             const Unit t = decode_unit<MODE>(u, g);
             const bool two = t.rows > BM;            // second half present
             // one or two 128-row halves of A (K-major rows or MN-major atoms) and the B tile
-            const uint32_t tx_bytes = (two ? A_BYTES : A_HALF_BYTES) + kUnitN<MODE> * 128;
+            const uint32_t tx_bytes = (two ? A_BYTES : A_HALF_BYTES) + (MODE == kRouter ? g.n_mma : kUnitN<MODE>) * 128;
             for (int kb = t.kb0; kb < t.kb1; ++kb) {
                 bool e_ok = true;
                 if (lane == 0) e_ok = mbar_wait(smem_addr(&sm.empty[stage]), phase ^ 1u, abort_flag, g.err);
@@ -548,14 +549,16 @@ tc_gemm_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs g) {
                                          bdesc, idesc, sf + 4, sf + 8, acc);
                         }
                     } else {
+                        // the router's N follows E; the expert GEMMs use the full 256
+                        const uint32_t idesc = MODE == kRouter ? idesc_bf16_f32(BM, g.n_mma) : kIdesc<MODE>;
 #pragma unroll
                         for (int kk = 0; kk < BK / UMMA_K; ++kk) {
                             const uint32_t acc = (kb > t.kb0 || kk > 0) ? 1u : 0u;
                             const uint64_t bdesc = operand_desc<kBMn<MODE>>(sb, kk);
-                            mma_bf16(tmem_base, operand_desc<kAMn<MODE>>(sa, kk), bdesc, kIdesc<MODE>, acc);
+                            mma_bf16(tmem_base, operand_desc<kAMn<MODE>>(sa, kk), bdesc, idesc, acc);
                             if (two)
                                 mma_bf16(tmem_base + BN, operand_desc<kAMn<MODE>>(sa + A_HALF_BYTES, kk), bdesc,
-                                         kIdesc<MODE>, acc);
+                                         idesc, acc);
                         }
                     }
                     mma_commit(smem_addr(&sm.empty[stage]));   // frees the smem stage
@@ -878,7 +881,7 @@ tc_gemm_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs g) {
                                  (static_cast<int64_t>(t.split) * g.T + t.row0 + row) * g.n_out + col0;
                     const bool vec = (g.n_out & 3) == 0;
 #pragma unroll 1
-                    for (int c = 0; c < BN; c += 32) {
+                    for (int c = 0; c < g.n_mma; c += 32) {
                         uint32_t v[32];
                         tmem_ld32(tacc + c, v);
                         tmem_wait_ld();

@@ -10,33 +10,47 @@ namespace moe {
 namespace {
 
 // y[t, :] = sum over the token's k slots s of obuf[row_of[s], :] (rows already
-// weighted, in routed order); dropped slots (row_of < 0) are skipped. fp32 sum,
-// bf16 result.
+// weighted, in routed order); dropped slots (row_of < 0) are skipped. fp32 sum
+// in slot order, bf16 result. One warp per token (grid-stride over tokens):
+// lane j < k reads the token's row_of[j] once; every lane then sums 8-column
+// groups lane, lane + 32, ... with the k row loads of a group issued together
+// (all lanes run the same passes, so the shuffles see the whole warp).
 __global__ void __launch_bounds__(256)
 combine_kernel(const __nv_bfloat16 *__restrict__ obuf, const int32_t *__restrict__ row_of,
                __nv_bfloat16 *__restrict__ y, int T, int H, int k) {
+    const int lane = threadIdx.x & 31;
     const int groups = H >> 3;
-    const int64_t total = static_cast<int64_t>(T) * groups;
-    for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
-         i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-        const int t = static_cast<int>(i / groups);
-        const int c = static_cast<int>(i - static_cast<int64_t>(t) * groups) * 8;
-        float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-        for (int j = 0; j < k; ++j) {
-            const int64_t s = static_cast<int64_t>(t) * k + j;
-            const int r = row_of[s];
-            if (r < 0) continue;
-            const uint4 v = __ldg(reinterpret_cast<const uint4 *>(obuf + static_cast<int64_t>(r) * H + c));
-            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    const int warps = gridDim.x * (blockDim.x >> 5);
+    for (int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); t < T; t += warps) {
+        const int my_row = lane < k ? __ldg(&row_of[static_cast<int64_t>(t) * k + lane]) : -1;
+        for (int g0 = 0; g0 < groups; g0 += 32) {
+            const int g = g0 + lane;
+            const bool live = g < groups;
+            float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+            for (int j0 = 0; j0 < k; j0 += 8) {
+                uint4 v[8];
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                acc[2 * q] += bf16_lo(w[q]);
-                acc[2 * q + 1] += bf16_hi(w[q]);
+                for (int jj = 0; jj < 8; ++jj) {
+                    const int r = __shfl_sync(0xffffffffu, my_row, (j0 + jj) & 31);
+                    v[jj] = (live && j0 + jj < k && r >= 0)
+                                ? __ldg(reinterpret_cast<const uint4 *>(obuf + static_cast<int64_t>(r) * H) + g)
+                                : make_uint4(0u, 0u, 0u, 0u);
+                }
+#pragma unroll
+                for (int jj = 0; jj < 8; ++jj) {
+                    const uint32_t w[4] = {v[jj].x, v[jj].y, v[jj].z, v[jj].w};
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        acc[2 * q] += bf16_lo(w[q]);
+                        acc[2 * q + 1] += bf16_hi(w[q]);
+                    }
+                }
             }
+            if (live)
+                reinterpret_cast<uint4 *>(y + static_cast<int64_t>(t) * H)[g] =
+                    make_uint4(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]),
+                               pack_bf16x2(acc[4], acc[5]), pack_bf16x2(acc[6], acc[7]));
         }
-        *reinterpret_cast<uint4 *>(y + static_cast<int64_t>(t) * H + c) =
-            make_uint4(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]),
-                       pack_bf16x2(acc[4], acc[5]), pack_bf16x2(acc[6], acc[7]));
     }
 }
 
@@ -69,6 +83,7 @@ cudaError_t launch_router_gemm(const RouterGemmLaunch &p, cudaStream_t st) {
     g.E = p.E;
     g.K = p.H;
     g.n_out = p.E;
+    g.n_mma = router_n_mma(p.E);
     g.n_tiles = (p.E + BN - 1) / BN;
     g.T = p.T;
     g.kb_h = (p.H + BK - 1) / BK;
@@ -90,10 +105,9 @@ cudaError_t launch_router_gemm(const RouterGemmLaunch &p, cudaStream_t st) {
 }
 
 cudaError_t launch_combine(const CombineLaunch &p, cudaStream_t st) {
-    const int64_t total = static_cast<int64_t>(p.T) * (p.H / 8);
-    if (total == 0) return cudaSuccess;
-    int64_t blocks = (total + 255) / 256;
-    if (blocks > 152 * 16) blocks = 152 * 16;
+    if (p.T == 0 || p.H == 0) return cudaSuccess;
+    int64_t blocks = (static_cast<int64_t>(p.T) + 7) / 8;     // eight tokens (warps) per block
+    if (blocks > 152 * 8) blocks = 152 * 8;
     combine_kernel<<<static_cast<int>(blocks), 256, 0, st>>>(p.obuf, p.row_of, p.y, p.T, p.H, p.k);
     note_launches(1);
     return cudaGetLastError();

@@ -35,7 +35,7 @@ constexpr int kBN = 256;    // accumulator columns of one tile
 constexpr size_t kWsHeaderBytes = 256;
 
 // Slots per CTA of the routing-metadata kernels (one histogram row each).
-constexpr int kMetaChunk = 4096;
+constexpr int kMetaChunk = 1024;
 
 inline size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
@@ -54,6 +54,10 @@ inline int router_splits(int64_t T, int64_t H, int64_t E) {
     const int64_t per = (kb_total + s - 1) / s;
     return static_cast<int>((kb_total + per - 1) / per);
 }
+
+// N of the router GEMM's MMAs and rows of its weight tile: E rounded up to a
+// whole 32-column TMEM load, at most one 256-column tile.
+inline int router_n_mma(int64_t E) { return E >= kBN ? kBN : static_cast<int>((E + 31) / 32 * 32); }
 
 // Bytes of router scratch for a shape and split factor.
 inline size_t router_scratch_bytes(int64_t T, int64_t H, int64_t E, int splits) {
@@ -151,7 +155,7 @@ struct GemmLaunch {
 // The router GEMM: partial logits [splits, T, E] of x . w3^T.
 struct RouterGemmLaunch {
     const CUtensorMap *tm_x;    // x [T, H], box 64 x 128
-    const CUtensorMap *tm_w3;   // w3 [3E, H], box 64 x 256
+    const CUtensorMap *tm_w3;   // w3 [3E, H], box 64 x router_n_mma(E)
     float *logits_part;
     int32_t *err;
     int32_t *sched;

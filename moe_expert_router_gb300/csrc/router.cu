@@ -121,8 +121,17 @@ router_topk_kernel(const TopkArgs p) {
         for (int i = 0; i < V; ++i) {
             const int e = lane + 32 * i;
             if (e < p.E) {
+                // the split partials in a fixed order, eight loads in flight at a time
                 float l = 0.0f;
-                for (int sp = 0; sp < p.splits; ++sp) l += lrow[sp * split_stride + e];
+                for (int sp0 = 0; sp0 < p.splits; sp0 += 8) {
+                    float part[8];
+#pragma unroll
+                    for (int j = 0; j < 8; ++j)
+                        part[j] = (sp0 + j < p.splits) ? __ldcg(&lrow[(sp0 + j) * split_stride + e]) : 0.0f;
+#pragma unroll
+                    for (int j = 0; j < 8; ++j)
+                        if (sp0 + j < p.splits) l += part[j];
+                }
                 if (p.logit_offset) l += p.logit_offset[e];
                 if (p.logits_out) p.logits_out[static_cast<int64_t>(t) * p.E + e] = l;
                 s[i] = l;
@@ -336,7 +345,8 @@ cudaError_t launch_router(const RouterLaunch &p, cudaStream_t st) {
 
     CUtensorMap tm_x, tm_w3;
     if (!encode_bf16_2d(&tm_x, p.x, p.H, p.T, kBK, kBM) ||
-        !encode_bf16_2d(&tm_w3, sc.w3, p.H, 3 * static_cast<uint64_t>(p.E), kBK, kBN))
+        !encode_bf16_2d(&tm_w3, sc.w3, p.H, 3 * static_cast<uint64_t>(p.E), kBK,
+                        static_cast<uint32_t>(router_n_mma(p.E))))
         return cudaErrorInvalidValue;
     RouterGemmLaunch g;
     g.tm_x = &tm_x;

@@ -9,7 +9,9 @@
 //   increasing slot order inside each expert) and row_of[s] (inverse, -1 for a
 //   dropped slot).
 //
-// Two kernels over chunks of kChunk consecutive slots (one CTA per chunk):
+// Two kernels over chunks of kChunk consecutive slots (one CTA per chunk; each
+// lane loads its slots' expert indices up front, so a warp pays one memory
+// latency per kernel):
 //   count : per-chunk expert histogram (warp __match_any + shared atomics),
 //           stored as block_hist[chunk][e]. The last CTA to finish (ticket)
 //           turns the histograms into per-(chunk, expert) starting rows, the
@@ -29,6 +31,18 @@ constexpr int kChunk = kMetaChunk;       // slots per CTA
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
 constexpr int kWarpSlots = kChunk / kWarps;
+constexpr int kPerLane = kWarpSlots / 32;   // slots s = beg + 32 i + lane of a lane
+static_assert(kWarpSlots % 32 == 0, "whole warp passes");
+
+// The expert index of each of this lane's slots (-1 past the end).
+__device__ __forceinline__ void load_lane_slots(const int32_t *__restrict__ topk_idx, int beg, int end, int lane,
+                                                int (&ev)[kPerLane]) {
+#pragma unroll
+    for (int i = 0; i < kPerLane; ++i) {
+        const int s = beg + 32 * i + lane;
+        ev[i] = (s < end) ? __ldg(&topk_idx[s]) : -1;
+    }
+}
 
 __global__ void __launch_bounds__(kThreads)
 metadata_count_kernel(const int32_t *__restrict__ topk_idx, int R, int E, int n_chunks,
@@ -44,9 +58,12 @@ metadata_count_kernel(const int32_t *__restrict__ topk_idx, int R, int E, int n_
     const int beg = blockIdx.x * kChunk + warp * kWarpSlots;
     const int end = min(R, beg + kWarpSlots);
     int bad = 0;
-    for (int s0 = beg; s0 < end; s0 += 32) {
-        const int s = s0 + lane;
-        const int e = (s < end) ? topk_idx[s] : -1;
+    int ev[kPerLane];
+    load_lane_slots(topk_idx, beg, end, lane, ev);
+#pragma unroll
+    for (int i = 0; i < kPerLane; ++i) {
+        const int s = beg + 32 * i + lane;
+        const int e = ev[i];
         const bool valid = (s < end) && e >= 0 && e < E;
         bad |= (s < end) && !valid;
         const unsigned peers = __match_any_sync(0xffffffffu, valid ? e : -1);
@@ -62,14 +79,21 @@ metadata_count_kernel(const int32_t *__restrict__ topk_idx, int R, int E, int n_
     if (!is_last) return;
     __threadfence();
 
-    // last CTA: per expert, running total over chunks (chunk order = slot order)
+    // last CTA: per expert, running total over chunks (chunk order = slot order),
+    // eight chunks' histograms loaded before they are replaced by starting rows
+    constexpr int kBatch = 8;
     for (int e = threadIdx.x; e < E; e += kThreads) {
         int run = 0;
-        for (int b = 0; b < n_chunks; ++b) {
-            const int64_t i = static_cast<int64_t>(b) * E + e;
-            const int c = __ldcg(&block_hist[i]);
-            block_hist[i] = run;
-            run += c;
+        for (int b0 = 0; b0 < n_chunks; b0 += kBatch) {
+            int c[kBatch];
+#pragma unroll
+            for (int j = 0; j < kBatch; ++j)
+                c[j] = (b0 + j < n_chunks) ? __ldcg(&block_hist[static_cast<int64_t>(b0 + j) * E + e]) : 0;
+#pragma unroll
+            for (int j = 0; j < kBatch; ++j) {
+                if (b0 + j < n_chunks) block_hist[static_cast<int64_t>(b0 + j) * E + e] = run;
+                run += c[j];
+            }
         }
         hist[e] = run;                    // counts
     }
@@ -139,12 +163,16 @@ metadata_place_kernel(const int32_t *__restrict__ topk_idx, int R, int E,
     const int beg = blockIdx.x * kChunk + warp * kWarpSlots;
     const int end = min(R, beg + kWarpSlots);
     int32_t *mine = whist + warp * E;
-    for (int s0 = beg; s0 < end; s0 += 32) {
-        const int s = s0 + lane;
-        const int e = (s < end) ? topk_idx[s] : -1;
+    int ev[kPerLane];
+    load_lane_slots(topk_idx, beg, end, lane, ev);
+#pragma unroll
+    for (int i = 0; i < kPerLane; ++i) {
+        const int s = beg + 32 * i + lane;
+        const int e = ev[i];
         const bool valid = (s < end) && e >= 0 && e < E;
         const unsigned peers = __match_any_sync(0xffffffffu, valid ? e : -1);
         if (valid && lane == __ffs(peers) - 1) mine[e] += __popc(peers);
+        __syncwarp();
     }
     __syncthreads();
     for (int e = threadIdx.x; e < E; e += kThreads) {
@@ -156,9 +184,10 @@ metadata_place_kernel(const int32_t *__restrict__ topk_idx, int R, int E,
         }
     }
     __syncthreads();
-    for (int s0 = beg; s0 < end; s0 += 32) {
-        const int s = s0 + lane;
-        const int e = (s < end) ? topk_idx[s] : -1;
+#pragma unroll
+    for (int i = 0; i < kPerLane; ++i) {
+        const int s = beg + 32 * i + lane;
+        const int e = ev[i];
         const bool valid = (s < end) && e >= 0 && e < E;
         const unsigned peers = __match_any_sync(0xffffffffu, valid ? e : -1);
         if (valid) {

@@ -10,21 +10,32 @@ namespace moe {
 
 namespace {
 
-// rows[r, :] = x[perm_slot[r] / k, :] for r < *routed (16-byte chunks); with
-// row_w, also row_w[r] = topk_w[perm_slot[r]].
+// rows[r, :] = x[perm_slot[r] / k, :] for r < *routed; with row_w, also
+// row_w[r] = topk_w[perm_slot[r]]. One warp per row (grid-stride over rows),
+// 16-byte chunks, four loads in flight per lane.
 __global__ void __launch_bounds__(256)
 gather_rows_kernel(const __nv_bfloat16 *__restrict__ x, const int32_t *__restrict__ perm_slot,
                    const int32_t *__restrict__ routed, int k, int64_t H, __nv_bfloat16 *__restrict__ rows,
                    const float *__restrict__ topk_w, float *__restrict__ row_w) {
-    const int64_t per_row = H / 8;
-    const int64_t total = static_cast<int64_t>(*routed) * per_row;
-    for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
-         i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-        const int64_t r = i / per_row;
-        const int64_t c = (i - r * per_row) * 8;
-        const int64_t s = perm_slot[r];
-        *reinterpret_cast<uint4 *>(rows + r * H + c) = __ldg(reinterpret_cast<const uint4 *>(x + (s / k) * H + c));
-        if (row_w != nullptr && c == 0) row_w[r] = topk_w[s];
+    const int lane = threadIdx.x & 31;
+    const int64_t warps = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
+    const int n = *routed;
+    const int chunks = static_cast<int>(H / 8);
+    for (int64_t r = blockIdx.x * static_cast<int64_t>(blockDim.x >> 5) + (threadIdx.x >> 5); r < n; r += warps) {
+        const int s = __ldg(&perm_slot[r]);
+        const uint4 *src = reinterpret_cast<const uint4 *>(x + static_cast<int64_t>(s / k) * H);
+        uint4 *dst = reinterpret_cast<uint4 *>(rows + r * H);
+        int c = lane;
+        for (; c + 96 < chunks; c += 128) {
+            const uint4 v0 = __ldg(src + c), v1 = __ldg(src + c + 32), v2 = __ldg(src + c + 64),
+                        v3 = __ldg(src + c + 96);
+            dst[c] = v0;
+            dst[c + 32] = v1;
+            dst[c + 64] = v2;
+            dst[c + 96] = v3;
+        }
+        for (; c < chunks; c += 32) dst[c] = __ldg(src + c);
+        if (row_w != nullptr && lane == 0) row_w[r] = topk_w[s];
     }
 }
 
@@ -33,10 +44,9 @@ gather_rows_kernel(const __nv_bfloat16 *__restrict__ x, const int32_t *__restric
 cudaError_t launch_gather_rows(const __nv_bfloat16 *x, const int32_t *perm_slot, const int32_t *routed, int k,
                                int64_t R, int64_t H, __nv_bfloat16 *rows, const float *topk_w, float *row_w,
                                cudaStream_t st) {
-    const int64_t total = R * (H / 8);
-    if (total == 0) return cudaSuccess;
-    int64_t grid = (total + 255) / 256;
-    if (grid > 152 * 16) grid = 152 * 16;
+    if (R == 0 || H == 0) return cudaSuccess;
+    int64_t grid = (R + 7) / 8;                     // eight rows (warps) per block
+    if (grid > 152 * 8) grid = 152 * 8;
     gather_rows_kernel<<<static_cast<int>(grid), 256, 0, st>>>(x, perm_slot, routed, k, H, rows, topk_w, row_w);
     note_launches(1);
     return cudaGetLastError();
