@@ -612,6 +612,7 @@ tc_gemm_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs g) {
             ok = __shfl_sync(0xffffffffu, ok, 0);
             if (!ok) break;
             tc_fence_after();
+            bool released = false;                      // this thread's acc_empty arrival done
             const int slab0 = half * BM + quad * 32;    // first unit row of this warp
             const bool full_slab = slab0 + 32 <= t.rows;
             if (t.rows > half * BM) {                   // this half was computed
@@ -727,28 +728,48 @@ tc_gemm_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs g) {
                         }
                     } else if (full_slab) {
                         // whole 32-row slab valid: stage 32 x 64 bf16 boxes in shared
-                        // memory (128B-swizzled) and write each with one TMA store
-#pragma unroll 1
-                        for (int cc = 0; cc < ncols; cc += 64) {
-                            if (col0 + cc >= g.n_out) break;
-                            if (lane == 0) bulk_wait_read<0>();   // previous box read out
-                            __syncwarp();
+                        // memory (128B-swizzled) and write each with one TMA store. The
+                        // row's first box is staged at once and the rest is converted
+                        // into packed bf16 registers, so the accumulator is released
+                        // before the stores: their shared-memory waits overlap the
+                        // next unit's MMAs.
+                        constexpr int NPIECE = ncols / 32;
+                        uint32_t pk[NPIECE][16];
 #pragma unroll
-                            for (int p = 0; p < 2; ++p) {
-                                uint32_t pk[16];
-                                if constexpr (MODE == kStage1) swiglu_piece(tacc, cc + 32 * p, pk);
-                                else scaled_piece(tacc, cc + 32 * p, w, pk);
+                        for (int p = 0; p < NPIECE; ++p) {
+                            if constexpr (MODE == kStage1) swiglu_piece(tacc, 32 * p, pk[p]);
+                            else scaled_piece(tacc, 32 * p, w, pk[p]);
+                            if (p == 1) {                     // box 0 complete: stage it
+                                if (lane == 0) bulk_wait_read<0>();   // previous box read out
+                                __syncwarp();
 #pragma unroll
-                                for (int j = 0; j < 4; ++j) {
-                                    const int c16 = p * 4 + j;
-                                    st_shared_v4(buf + lane * 128 + ((c16 ^ (lane & 7)) << 4), pk[4 * j],
-                                                 pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+                                for (int j = 0; j < 8; ++j) {
+                                    const uint32_t *q = &pk[j >> 2][4 * (j & 3)];
+                                    st_shared_v4(buf + lane * 128 + ((j ^ (lane & 7)) << 4), q[0], q[1], q[2],
+                                                 q[3]);
+                                }
+                            }
+                        }
+                        tc_fence_before();
+                        mbar_arrive(smem_addr(&sm.acc_empty));
+                        released = true;
+#pragma unroll
+                        for (int b = 0; b < NPIECE / 2; ++b) {
+                            if (col0 + 64 * b >= g.n_out) break;
+                            if (b > 0) {
+                                if (lane == 0) bulk_wait_read<0>();   // previous box read out
+                                __syncwarp();
+#pragma unroll
+                                for (int j = 0; j < 8; ++j) {
+                                    const uint32_t *q = &pk[2 * b + (j >> 2)][4 * (j & 3)];
+                                    st_shared_v4(buf + lane * 128 + ((j ^ (lane & 7)) << 4), q[0], q[1], q[2],
+                                                 q[3]);
                                 }
                             }
                             fence_proxy_async_smem();
                             __syncwarp();
                             if (lane == 0) {
-                                tma_store_2d(&maps.out, buf, col0 + cc, y);
+                                tma_store_2d(&maps.out, buf, col0 + 64 * b, y);
                                 bulk_commit();
                             }
                         }
@@ -904,8 +925,10 @@ tc_gemm_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs g) {
                     }
                 }
             }
-            tc_fence_before();
-            mbar_arrive(smem_addr(&sm.acc_empty));
+            if (!released) {
+                tc_fence_before();
+                mbar_arrive(smem_addr(&sm.acc_empty));
+            }
             acc_phase ^= 1u;
         }
         if (lane == 0) bulk_wait<0>();                  // every output box written
