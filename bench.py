@@ -288,13 +288,17 @@ def run_ours(args, cfg, rank, world, local_rank):
                                                          topk_idx=idx, cfg=rcfg)
             yield lambda: B.moe_backward_stage1_weight(x_in, shp, dw1, ws)
 
-    def step(ev=None):
+    def step(ev=None, per_stage=False):
+        """One step. ev: [start, end] events, or with per_stage one event before every
+        call and one after the last (the breakdown pass: an event between two calls
+        keeps their kernels from overlapping, so the timed steps record only the two
+        ends)."""
         for j, call in enumerate(calls(x_dev, inp["dy"] if train else None)):
-            if ev is not None:
+            if ev is not None and (per_stage or j == 0):
                 ev[j].record(stream)
             call()
         if ev is not None:
-            ev[len(names)].record(stream)
+            ev[-1].record(stream)
 
     for _ in range(args.warmup):
         flush.fill_(1)
@@ -304,7 +308,7 @@ def run_ours(args, cfg, rank, world, local_rank):
     if err:
         raise RuntimeError(f"device error word {err:#x} after warm-up")
 
-    events = [[torch.cuda.Event(enable_timing=True) for _ in range(len(names) + 1)] for _ in range(args.steps)]
+    events = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
     sampler = ClockSampler(local_rank) if rank == 0 else None
     if sampler:
         sampler.start()
@@ -326,14 +330,20 @@ def run_ours(args, cfg, rank, world, local_rank):
         torch.distributed.barrier()
     launches = B.moe_kernel_launch_count() - launches0
     clocks = sampler.stop() if sampler else None
+    step_ms = [ev[0].elapsed_time(ev[1]) for ev in events]
+    total_ms = sum(step_ms)
 
+    # per-stage breakdown (not part of the timed region): events between the calls
+    n_bd = min(args.steps, 10)
+    bd_events = [[torch.cuda.Event(enable_timing=True) for _ in range(len(names) + 1)] for _ in range(n_bd)]
+    for i in range(n_bd):
+        flush.fill_(i & 0xFF)
+        step(bd_events[i], per_stage=True)
+    torch.cuda.synchronize(dev)
     stage_ms = {n: [] for n in names}
-    step_ms = []
-    for ev in events:
+    for ev in bd_events:
         for j, n in enumerate(names):
             stage_ms[n].append(ev[j].elapsed_time(ev[j + 1]))
-        step_ms.append(ev[0].elapsed_time(ev[len(names)]))
-    total_ms = sum(step_ms)
 
     # metadata for the algorithmic byte counts
     L = B.moe_workspace_layout(shp)

@@ -35,6 +35,7 @@ __device__ __forceinline__ float warp_max(float v) {
 __global__ void __launch_bounds__(256)
 dtw_reduce_kernel(const float *__restrict__ part, int n_part, int R, const int32_t *__restrict__ row_of,
                   float *__restrict__ dtopk_w, int64_t slots) {
+    griddep_wait();
     for (int64_t s = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; s < slots;
          s += static_cast<int64_t>(gridDim.x) * blockDim.x) {
         const int r = row_of[s];
@@ -48,6 +49,7 @@ dtw_reduce_kernel(const float *__restrict__ part, int n_part, int R, const int32
 // One warp per token; lane j < k owns slot j.
 __global__ void __launch_bounds__(256)
 router_dlogits_kernel(const RouterBwdLaunch p) {
+    griddep_wait();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int t = blockIdx.x * 8 + warp;
     if (t >= p.T) return;
@@ -106,6 +108,7 @@ constexpr int kDwrThreads = 128;
 
 __global__ void __launch_bounds__(kDwrThreads)
 router_dwr_kernel(const RouterBwdLaunch p, int chunks, int dense) {
+    griddep_wait();
     __shared__ int tok_sh[kDwrThreads];
     __shared__ float coef_sh[kDwrThreads];
     const int e = blockIdx.x / chunks;
@@ -163,6 +166,7 @@ router_dwr_kernel(const RouterBwdLaunch p, int chunks, int dense) {
 // (all lanes run the same passes, so the shuffles see the whole warp).
 __global__ void __launch_bounds__(256)
 combine_bwd_kernel(const CombineBwdLaunch p) {
+    griddep_wait();
     const int lane = threadIdx.x & 31;
     const int groups = p.H >> 3;
     const int warps = gridDim.x * (blockDim.x >> 5);
@@ -243,6 +247,7 @@ combine_bwd_kernel(const CombineBwdLaunch p) {
 __global__ void __launch_bounds__(256)
 zero_tail_rows_kernel(__nv_bfloat16 *__restrict__ dh, __nv_bfloat16 *__restrict__ aw,
                       const int32_t *__restrict__ routed_rows, int R, int I) {
+    griddep_wait();
     const int r0 = *routed_rows;
     const int64_t per_row = 3 * static_cast<int64_t>(I) / 8;   // 16-byte chunks: 2I of dH, I of w a
     const int64_t total = static_cast<int64_t>(R - r0) * per_row;
@@ -267,38 +272,40 @@ int grid_for(int64_t items, int per_block) {
 cudaError_t launch_dtw_reduce(const DtwReduceLaunch &p, cudaStream_t st) {
     const int64_t slots = static_cast<int64_t>(p.T) * p.k;
     if (slots == 0) return cudaSuccess;
-    dtw_reduce_kernel<<<grid_for(slots, 256), 256, 0, st>>>(p.dtw_part, p.n_part, p.R, p.row_of, p.dtopk_w, slots);
+    const cudaError_t e = launch_dep(dtw_reduce_kernel, dim3(grid_for(slots, 256)), dim3(256), 0, st, p.dtw_part,
+                                     p.n_part, p.R, p.row_of, p.dtopk_w, slots);
     note_launches(1);
-    return cudaGetLastError();
+    return e;
 }
 
 cudaError_t launch_zero_tail_rows(__nv_bfloat16 *dh, __nv_bfloat16 *aw, const int32_t *routed_rows, int R,
                                   int I, cudaStream_t st) {
-    zero_tail_rows_kernel<<<32, 256, 0, st>>>(dh, aw, routed_rows, R, I);
+    const cudaError_t e = launch_dep(zero_tail_rows_kernel, dim3(32), dim3(256), 0, st, dh, aw, routed_rows, R, I);
     note_launches(1);
-    return cudaGetLastError();
+    return e;
 }
 
 cudaError_t launch_router_dlogits(const RouterBwdLaunch &p, cudaStream_t st) {
     if (p.T == 0) return cudaSuccess;
-    router_dlogits_kernel<<<(p.T + 7) / 8, 256, 0, st>>>(p);
+    const cudaError_t e = launch_dep(router_dlogits_kernel, dim3((p.T + 7) / 8), dim3(256), 0, st, p);
     note_launches(1);
-    return cudaGetLastError();
+    return e;
 }
 
 cudaError_t launch_router_dwr(const RouterBwdLaunch &p, cudaStream_t st) {
     const int chunks = (p.H + 8 * kDwrThreads - 1) / (8 * kDwrThreads);
     const int dense = (p.score_fn == MOE_SCORE_SOFTMAX && !p.normalize) ? 1 : 0;
-    router_dwr_kernel<<<p.E * chunks, kDwrThreads, 0, st>>>(p, chunks, dense);
+    const cudaError_t e = launch_dep(router_dwr_kernel, dim3(p.E * chunks), dim3(kDwrThreads), 0, st, p, chunks, dense);
     note_launches(1);
-    return cudaGetLastError();
+    return e;
 }
 
 cudaError_t launch_combine_bwd(const CombineBwdLaunch &p, cudaStream_t st) {
     if (p.T == 0 || p.H == 0) return cudaSuccess;
-    combine_bwd_kernel<<<grid_for(p.T, 8), 256, 0, st>>>(p);      // eight tokens (warps) per block
+    // eight tokens (warps) per block
+    const cudaError_t e = launch_dep(combine_bwd_kernel, dim3(grid_for(p.T, 8)), dim3(256), 0, st, p);
     note_launches(1);
-    return cudaGetLastError();
+    return e;
 }
 
 }  // namespace moe

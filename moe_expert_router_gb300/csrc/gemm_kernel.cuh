@@ -307,6 +307,23 @@ __device__ __forceinline__ void swiglu_piece(uint32_t tacc, int c, uint32_t (&pk
                             silu_mul(__uint_as_float(gv[2 * i + 1]), __uint_as_float(uv[2 * i + 1])));
 }
 
+// 64 accumulator columns [c, c+64) scaled by w, packed to bf16: both loads in
+// flight before the one wait.
+__device__ __forceinline__ void scaled_piece2(uint32_t tacc, int c, float w, uint32_t (&pk0)[16],
+                                              uint32_t (&pk1)[16]) {
+    uint32_t v0[32], v1[32];
+    tmem_ld32(tacc + c, v0);
+    tmem_ld32(tacc + c + 32, v1);
+    tmem_wait_ld();
+    tmem_reg_fence(v0);
+    tmem_reg_fence(v1);
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        pk0[i] = pack_bf16x2(w * __uint_as_float(v0[2 * i]), w * __uint_as_float(v0[2 * i + 1]));
+        pk1[i] = pack_bf16x2(w * __uint_as_float(v1[2 * i]), w * __uint_as_float(v1[2 * i + 1]));
+    }
+}
+
 // 32 accumulator columns [c, c+32) scaled by w, packed to bf16.
 __device__ __forceinline__ void scaled_piece(uint32_t tacc, int c, float w, uint32_t (&pk)[16]) {
     uint32_t v[32];
@@ -364,6 +381,9 @@ __device__ __forceinline__ void scale_rows(const GemmArgs &g, const Unit &t, int
 template <int MODE>
 __global__ void __launch_bounds__(kNumThreads<MODE>, 1)
 tc_gemm_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs g) {
+    // every CTA is resident from the start (one per SM), so the next kernel may
+    // be scheduled right away; it waits for this grid in its own griddep_wait
+    griddep_launch_dependents();
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_addr(smem_raw);
     Smem &sm = *reinterpret_cast<Smem *>(smem_raw + ((1024u - (raw & 1023u)) & 1023u));
@@ -401,6 +421,7 @@ tc_gemm_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs g) {
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = sm.tmem_base;
+    griddep_wait();     // shared memory and tensor memory are set up; now the inputs
 
     if (warp == 0) {
         // ------------------------------------------------ scheduler + TMA producer
@@ -738,7 +759,7 @@ tc_gemm_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs g) {
 #pragma unroll
                         for (int p = 0; p < NPIECE; ++p) {
                             if constexpr (MODE == kStage1) swiglu_piece(tacc, 32 * p, pk[p]);
-                            else scaled_piece(tacc, 32 * p, w, pk[p]);
+                            else if (p % 2 == 0) scaled_piece2(tacc, 32 * p, w, pk[p], pk[p + 1]);
                             if (p == 1) {                     // box 0 complete: stage it
                                 if (lane == 0) bulk_wait_read<0>();   // previous box read out
                                 __syncwarp();
@@ -1072,9 +1093,9 @@ cudaError_t set_gemm_smem() {
 
 template <int MODE>
 cudaError_t launch_tc_gemm(const GemmMaps &maps, const GemmArgs &g, int grid, cudaStream_t st) {
-    tc_gemm_kernel<MODE><<<grid, kNumThreads<MODE>, SMEM_BYTES, st>>>(maps, g);
+    const cudaError_t e = launch_dep(tc_gemm_kernel<MODE>, dim3(grid), dim3(kNumThreads<MODE>), SMEM_BYTES, st, maps, g);
     note_launches(1);
-    return cudaGetLastError();
+    return e;
 }
 
 }  // namespace

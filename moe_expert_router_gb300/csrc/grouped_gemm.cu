@@ -18,6 +18,7 @@ namespace {
 __global__ void __launch_bounds__(256)
 combine_kernel(const __nv_bfloat16 *__restrict__ obuf, const int32_t *__restrict__ row_of,
                __nv_bfloat16 *__restrict__ y, int T, int H, int k) {
+    griddep_wait();
     const int lane = threadIdx.x & 31;
     const int groups = H >> 3;
     const int warps = gridDim.x * (blockDim.x >> 5);
@@ -108,9 +109,10 @@ cudaError_t launch_combine(const CombineLaunch &p, cudaStream_t st) {
     if (p.T == 0 || p.H == 0) return cudaSuccess;
     int64_t blocks = (static_cast<int64_t>(p.T) + 7) / 8;     // eight tokens (warps) per block
     if (blocks > 152 * 8) blocks = 152 * 8;
-    combine_kernel<<<static_cast<int>(blocks), 256, 0, st>>>(p.obuf, p.row_of, p.y, p.T, p.H, p.k);
+    const cudaError_t e = launch_dep(combine_kernel, dim3(static_cast<int>(blocks)), dim3(256), 0, st, p.obuf,
+                                     p.row_of, p.y, p.T, p.H, p.k);
     note_launches(1);
-    return cudaGetLastError();
+    return e;
 }
 
 }  // namespace moe

@@ -14,6 +14,7 @@ namespace {
 __global__ void __launch_bounds__(256)
 mx_quantize_kernel(const __nv_bfloat16 *__restrict__ in, int64_t blocks, uint8_t *__restrict__ codes,
                    uint8_t *__restrict__ scales) {
+    griddep_wait();
     for (int64_t b = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; b < blocks;
          b += static_cast<int64_t>(gridDim.x) * blockDim.x) {
         const uint4 *src = reinterpret_cast<const uint4 *>(in + b * 32);
@@ -45,6 +46,7 @@ __global__ void __launch_bounds__(256)
 mx_quantize_dispatch_kernel(const __nv_bfloat16 *__restrict__ x, const int32_t *__restrict__ perm_slot,
                             const int32_t *__restrict__ routed, int k, int64_t cols, uint8_t *__restrict__ codes,
                             uint8_t *__restrict__ scales) {
+    griddep_wait();
     const int64_t per_row = cols / 32;
     const int64_t blocks = static_cast<int64_t>(*routed) * per_row;
     for (int64_t b = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; b < blocks;
@@ -82,9 +84,10 @@ cudaError_t launch_mx_quantize_dispatch(const __nv_bfloat16 *x, const int32_t *p
     if (blocks == 0) return cudaSuccess;
     int64_t grid = (blocks + 255) / 256;
     if (grid > 152 * 16) grid = 152 * 16;
-    mx_quantize_dispatch_kernel<<<static_cast<int>(grid), 256, 0, st>>>(x, perm_slot, routed, k, cols, codes, scales);
+    const cudaError_t e = launch_dep(mx_quantize_dispatch_kernel, dim3(static_cast<int>(grid)), dim3(256), 0, st, x,
+                                     perm_slot, routed, k, cols, codes, scales);
     note_launches(1);
-    return cudaGetLastError();
+    return e;
 }
 
 cudaError_t setup_mx_gemm_kernels() {
@@ -99,9 +102,10 @@ cudaError_t launch_mx_quantize(const __nv_bfloat16 *in, int64_t rows, int64_t co
     if (blocks == 0) return cudaSuccess;
     int64_t grid = (blocks + 255) / 256;
     if (grid > 152 * 16) grid = 152 * 16;
-    mx_quantize_kernel<<<static_cast<int>(grid), 256, 0, st>>>(in, blocks, codes, scales);
+    const cudaError_t e = launch_dep(mx_quantize_kernel, dim3(static_cast<int>(grid)), dim3(256), 0, st, in, blocks,
+                                     codes, scales);
     note_launches(1);
-    return cudaGetLastError();
+    return e;
 }
 
 cudaError_t launch_gemm1_mx(const GemmLaunch &p, cudaStream_t st) {

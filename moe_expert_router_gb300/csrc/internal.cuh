@@ -6,6 +6,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include "moe.h"
 
 namespace moe {
@@ -273,5 +275,35 @@ bool encode_bf16_2d_strided(CUtensorMap *map, const void *base, uint64_t inner, 
 
 // Statistics: kernels launched by this library.
 void note_launches(int n);
+
+// Programmatic dependent launch. Every kernel of this library is launched with
+// launch_dep, which lets the stream schedule it while the preceding kernel is
+// still finishing (its prologue overlaps that kernel's tail), and every kernel
+// calls griddep_wait() before it reads or writes memory another kernel touches:
+// the wait returns once the preceding grid has completed and its writes are
+// visible (at once when there is no programmatic predecessor).
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+// Lets the next kernel in the stream be scheduled before this one finishes (it
+// still waits in griddep_wait); used by the persistent GEMM, whose CTAs are all
+// resident from the start.
+__device__ __forceinline__ void griddep_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_dep(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                       Args &&...args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 }  // namespace moe

@@ -34,6 +34,7 @@ __global__ void __launch_bounds__(256)
 router_split_kernel(const float *__restrict__ w_r, __nv_bfloat16 *__restrict__ w3, int64_t n,
                     int E, float *__restrict__ score_sum, int32_t *__restrict__ counts,
                     int32_t *__restrict__ ticket) {
+    griddep_wait();
     if (blockIdx.x == 0) {
         for (int e = threadIdx.x; e < E; e += blockDim.x) {
             score_sum[e] = 0.0f;
@@ -100,6 +101,7 @@ struct TopkArgs {
 template <int V>
 __global__ void __launch_bounds__(kTopkWarps * 32)
 router_topk_kernel(const TopkArgs p) {
+    griddep_wait();
     __shared__ float blk_sum[kMaxE];
     __shared__ int blk_cnt[kMaxE];
     __shared__ float sel_sh[kTopkWarps][kMaxE];
@@ -286,8 +288,8 @@ router_topk_kernel(const TopkArgs p) {
 }
 
 template <int V>
-void launch_topk(const TopkArgs &a, int blocks, cudaStream_t st) {
-    router_topk_kernel<V><<<blocks, kTopkWarps * 32, 0, st>>>(a);
+cudaError_t launch_topk(const TopkArgs &a, int blocks, cudaStream_t st) {
+    return launch_dep(router_topk_kernel<V>, dim3(blocks), dim3(kTopkWarps * 32), 0, st, a);
 }
 
 }  // namespace
@@ -321,13 +323,14 @@ cudaError_t launch_selection(const RouterLaunch &p, const float *logits, int spl
     a.logits_out = p.logits;
     const int blocks = (p.T + kTopkWarps - 1) / kTopkWarps;
     const int v = (p.E + 31) / 32;
-    if (v <= 2) launch_topk<2>(a, blocks, st);
-    else if (v <= 4) launch_topk<4>(a, blocks, st);
-    else if (v <= 8) launch_topk<8>(a, blocks, st);
-    else if (v <= 16) launch_topk<16>(a, blocks, st);
-    else launch_topk<32>(a, blocks, st);
+    cudaError_t e;
+    if (v <= 2) e = launch_topk<2>(a, blocks, st);
+    else if (v <= 4) e = launch_topk<4>(a, blocks, st);
+    else if (v <= 8) e = launch_topk<8>(a, blocks, st);
+    else if (v <= 16) e = launch_topk<16>(a, blocks, st);
+    else e = launch_topk<32>(a, blocks, st);
     note_launches(1);
-    return cudaGetLastError();
+    return e;
 }
 
 }  // namespace
@@ -337,10 +340,9 @@ cudaError_t launch_router(const RouterLaunch &p, cudaStream_t st) {
     const int64_t n = static_cast<int64_t>(p.E) * p.H;
     int64_t sblocks = (n + 255) / 256;
     if (sblocks > 152 * 8) sblocks = 152 * 8;
-    router_split_kernel<<<static_cast<int>(sblocks), 256, 0, st>>>(p.w_r, sc.w3, n, p.E, sc.score_sum,
-                                                                   sc.counts, sc.ticket);
+    cudaError_t err = launch_dep(router_split_kernel, dim3(static_cast<int>(sblocks)), dim3(256), 0, st, p.w_r, sc.w3,
+                                 n, p.E, sc.score_sum, sc.counts, sc.ticket);
     note_launches(1);
-    cudaError_t err = cudaGetLastError();
     if (err != cudaSuccess) return err;
 
     CUtensorMap tm_x, tm_w3;
@@ -366,9 +368,10 @@ cudaError_t launch_router(const RouterLaunch &p, cudaStream_t st) {
 cudaError_t launch_route_logits(const RouterLaunch &p, const float *logits, cudaStream_t st) {
     const RouterScratch &sc = p.scratch;
     // one block of the split kernel with nothing to split: it clears the aux accumulators
-    router_split_kernel<<<1, 256, 0, st>>>(nullptr, nullptr, 0, p.E, sc.score_sum, sc.counts, sc.ticket);
+    cudaError_t err = launch_dep(router_split_kernel, dim3(1), dim3(256), 0, st, static_cast<const float *>(nullptr),
+                                 static_cast<__nv_bfloat16 *>(nullptr), static_cast<int64_t>(0), p.E, sc.score_sum,
+                                 sc.counts, sc.ticket);
     note_launches(1);
-    cudaError_t err = cudaGetLastError();
     if (err != cudaSuccess) return err;
     return launch_selection(p, logits, 1, st);
 }

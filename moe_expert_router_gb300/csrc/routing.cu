@@ -49,6 +49,7 @@ metadata_count_kernel(const int32_t *__restrict__ topk_idx, int R, int E, int n_
                       int32_t *__restrict__ block_hist, int32_t *__restrict__ counts,
                       int32_t *__restrict__ offsets, int32_t *__restrict__ mt_prefix,
                       int32_t *__restrict__ ticket, int32_t *__restrict__ err) {
+    griddep_wait();
     extern __shared__ int32_t hist[];    // [E]
     __shared__ int is_last;
     __shared__ int32_t warp_tot_c[32], warp_tot_m[32];
@@ -151,6 +152,7 @@ __global__ void __launch_bounds__(kThreads)
 metadata_place_kernel(const int32_t *__restrict__ topk_idx, int R, int E,
                       const int32_t *__restrict__ block_hist, const int32_t *__restrict__ offsets,
                       int32_t *__restrict__ perm_slot, int32_t *__restrict__ row_of) {
+    griddep_wait();
     extern __shared__ int32_t sh[];
     int32_t *base = sh;                  // [E]: first row of this chunk in each expert
     int32_t *whist = sh + E;             // [kWarps][E]: per-warp counts, then start ranks
@@ -215,12 +217,14 @@ cudaError_t setup_metadata_kernels() {
 cudaError_t launch_routing_metadata(const MetadataLaunch &p, cudaStream_t st) {
     const int n_chunks = (p.R + kChunk - 1) / kChunk;
     if (n_chunks == 0) return cudaSuccess;
-    metadata_count_kernel<<<n_chunks, kThreads, sizeof(int32_t) * p.E, st>>>(
-        p.topk_idx, p.R, p.E, n_chunks, p.block_hist, p.counts, p.offsets, p.mt_prefix, p.ticket, p.err);
-    metadata_place_kernel<<<n_chunks, kThreads, place_smem(p.E), st>>>(
-        p.topk_idx, p.R, p.E, p.block_hist, p.offsets, p.perm_slot, p.row_of);
+    cudaError_t e = launch_dep(metadata_count_kernel, dim3(n_chunks), dim3(kThreads), sizeof(int32_t) * p.E, st,
+                               p.topk_idx, p.R, p.E, n_chunks, p.block_hist, p.counts, p.offsets, p.mt_prefix, p.ticket,
+                               p.err);
+    if (e == cudaSuccess)
+        e = launch_dep(metadata_place_kernel, dim3(n_chunks), dim3(kThreads), place_smem(p.E), st, p.topk_idx, p.R,
+                       p.E, p.block_hist, p.offsets, p.perm_slot, p.row_of);
     note_launches(2);
-    return cudaGetLastError();
+    return e;
 }
 
 }  // namespace moe

@@ -17,6 +17,7 @@ __global__ void __launch_bounds__(256)
 gather_rows_kernel(const __nv_bfloat16 *__restrict__ x, const int32_t *__restrict__ perm_slot,
                    const int32_t *__restrict__ routed, int k, int64_t H, __nv_bfloat16 *__restrict__ rows,
                    const float *__restrict__ topk_w, float *__restrict__ row_w) {
+    griddep_wait();
     const int lane = threadIdx.x & 31;
     const int64_t warps = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
     const int n = *routed;
@@ -47,9 +48,10 @@ cudaError_t launch_gather_rows(const __nv_bfloat16 *x, const int32_t *perm_slot,
     if (R == 0 || H == 0) return cudaSuccess;
     int64_t grid = (R + 7) / 8;                     // eight rows (warps) per block
     if (grid > 152 * 8) grid = 152 * 8;
-    gather_rows_kernel<<<static_cast<int>(grid), 256, 0, st>>>(x, perm_slot, routed, k, H, rows, topk_w, row_w);
+    const cudaError_t e = launch_dep(gather_rows_kernel, dim3(static_cast<int>(grid)), dim3(256), 0, st, x, perm_slot,
+                                     routed, k, H, rows, topk_w, row_w);
     note_launches(1);
-    return cudaGetLastError();
+    return e;
 }
 
 }  // namespace moe
