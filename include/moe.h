@@ -104,6 +104,7 @@ typedef struct moe_ws_layout {
     size_t dlogits;    /* fp32 [T, E] gradient of the router logits */
     size_t xp;         /* bf16 [T*k, H] x rows in routed order (training stage 1's dispatch) */
     size_t dyp;        /* bf16 [T*k, H] dY rows in routed order (the backward's dispatch) */
+    size_t dwr_part;   /* fp32 [8, E, H] partial sums of the router weight gradient */
     /* MXFP8 workspaces only (flags & MOE_SHAPE_MXFP8), else equal to total: */
     size_t x_codes;    /* E4M3 [T*k, H] quantized x rows in routed order (the MXFP8 dispatch) */
     size_t x_scales;   /* E8M0 [T*k, H/32] */

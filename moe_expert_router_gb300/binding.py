@@ -47,7 +47,7 @@ class RouterCfg(ctypes.Structure):
 class WsLayout(ctypes.Structure):
     _fields_ = [(n, ctypes.c_size_t) for n in
                 ("err", "counts", "offsets", "mt_prefix", "perm_slot", "row_of", "meta", "router", "a",
-                 "obuf", "dh", "aw", "dtw_part", "dlogits", "xp", "dyp", "x_codes", "x_scales", "a_codes", "a_scales",
+                 "obuf", "dh", "aw", "dtw_part", "dlogits", "xp", "dyp", "dwr_part", "x_codes", "x_scales", "a_codes", "a_scales",
                  "total")]
 
 

@@ -99,24 +99,26 @@ __device__ __forceinline__ bool first_slot(const int32_t *__restrict__ idx_t, in
     return true;
 }
 
-// dW_r[e, c..c+8) per thread: block (e, 1024-column chunk). Sparse modes walk
-// the expert's routed rows; the dense mode (plain softmax) walks every token.
-// Rows go in batches of 128: each thread first resolves one row's token and
-// logit gradient into shared memory, then every thread accumulates the batch's
-// x rows for its 8 columns (independent loads, no dependent chain per row).
+// Partial dW_r: block (e, 1024-column chunk, row segment) sums, for its thread's
+// 8 columns, the rows of the batches of 128 rows numbered segment, segment +
+// kDwrSegments, ... Sparse modes walk the expert's routed rows; the dense mode
+// (plain softmax) walks every token. Each thread first resolves one row's token
+// and logit gradient into shared memory; then every thread accumulates the
+// batch's x rows, eight row loads in flight at a time.
 constexpr int kDwrThreads = 128;
 
 __global__ void __launch_bounds__(kDwrThreads)
-router_dwr_kernel(const RouterBwdLaunch p, int chunks, int dense) {
+router_dwr_part_kernel(const RouterBwdLaunch p, int chunks, int dense) {
     griddep_wait();
     __shared__ int tok_sh[kDwrThreads];
     __shared__ float coef_sh[kDwrThreads];
     const int e = blockIdx.x / chunks;
+    const int seg = blockIdx.y;
     const int c = ((blockIdx.x - e * chunks) * kDwrThreads + threadIdx.x) * 8;
     float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
     const int n = dense ? p.T : p.counts[e];
     const int r0 = dense ? 0 : p.offsets[e];
-    for (int b0 = 0; b0 < n; b0 += kDwrThreads) {
+    for (int b0 = seg * kDwrThreads; b0 < n; b0 += kDwrSegments * kDwrThreads) {
         const int i = b0 + threadIdx.x;
         int t = -1;
         float coef = 0.0f;
@@ -136,25 +138,51 @@ router_dwr_kernel(const RouterBwdLaunch p, int chunks, int dense) {
         __syncthreads();
         if (c < p.H) {
             const int m = min(kDwrThreads, n - b0);
-#pragma unroll 4
-            for (int j = 0; j < m; ++j) {
-                const int tj = tok_sh[j];
-                if (tj < 0) continue;
-                const float cf = coef_sh[j];
-                const uint4 v = __ldg(reinterpret_cast<const uint4 *>(p.x + static_cast<int64_t>(tj) * p.H + c));
-                const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
+            for (int j0 = 0; j0 < m; j0 += 8) {
+                uint4 v[8];
+                float cf[8];
 #pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    acc[2 * q] = fmaf(cf, __uint_as_float(wv[q] << 16), acc[2 * q]);
-                    acc[2 * q + 1] = fmaf(cf, __uint_as_float(wv[q] & 0xffff0000u), acc[2 * q + 1]);
+                for (int jj = 0; jj < 8; ++jj) {
+                    const int tj = (j0 + jj < m) ? tok_sh[j0 + jj] : -1;
+                    cf[jj] = tj >= 0 ? coef_sh[j0 + jj] : 0.0f;
+                    v[jj] = tj >= 0 ? __ldg(reinterpret_cast<const uint4 *>(p.x + static_cast<int64_t>(tj) * p.H + c))
+                                    : make_uint4(0u, 0u, 0u, 0u);
+                }
+#pragma unroll
+                for (int jj = 0; jj < 8; ++jj) {
+                    const uint32_t wv[4] = {v[jj].x, v[jj].y, v[jj].z, v[jj].w};
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        acc[2 * q] = fmaf(cf[jj], __uint_as_float(wv[q] << 16), acc[2 * q]);
+                        acc[2 * q + 1] = fmaf(cf[jj], __uint_as_float(wv[q] & 0xffff0000u), acc[2 * q + 1]);
+                    }
                 }
             }
         }
     }
     if (c < p.H) {
-        float4 *dst = reinterpret_cast<float4 *>(p.dw_r + static_cast<int64_t>(e) * p.H + c);
+        float4 *dst = reinterpret_cast<float4 *>(p.dwr_part + (static_cast<int64_t>(seg) * p.E + e) * p.H + c);
         dst[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
         dst[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+    }
+}
+
+// dW_r[e, h] = sum over the segments, in segment order, of the partial sums.
+__global__ void __launch_bounds__(256)
+router_dwr_sum_kernel(const float *__restrict__ part, int64_t n4, float *__restrict__ dw_r) {
+    griddep_wait();
+    for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n4;
+         i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        float4 a = __ldcg(reinterpret_cast<const float4 *>(part) + i);
+#pragma unroll
+        for (int s = 1; s < kDwrSegments; ++s) {
+            const float4 b = __ldcg(reinterpret_cast<const float4 *>(part) + s * n4 + i);
+            a.x += b.x;
+            a.y += b.y;
+            a.z += b.z;
+            a.w += b.w;
+        }
+        reinterpret_cast<float4 *>(dw_r)[i] = a;
     }
 }
 
@@ -295,8 +323,13 @@ cudaError_t launch_router_dlogits(const RouterBwdLaunch &p, cudaStream_t st) {
 cudaError_t launch_router_dwr(const RouterBwdLaunch &p, cudaStream_t st) {
     const int chunks = (p.H + 8 * kDwrThreads - 1) / (8 * kDwrThreads);
     const int dense = (p.score_fn == MOE_SCORE_SOFTMAX && !p.normalize) ? 1 : 0;
-    const cudaError_t e = launch_dep(router_dwr_kernel, dim3(p.E * chunks), dim3(kDwrThreads), 0, st, p, chunks, dense);
-    note_launches(1);
+    cudaError_t e = launch_dep(router_dwr_part_kernel, dim3(p.E * chunks, kDwrSegments), dim3(kDwrThreads), 0, st, p,
+                               chunks, dense);
+    const int64_t n4 = static_cast<int64_t>(p.E) * p.H / 4;
+    if (e == cudaSuccess)
+        e = launch_dep(router_dwr_sum_kernel, dim3(grid_for(n4, 256)), dim3(256), 0, st,
+                       static_cast<const float *>(p.dwr_part), n4, p.dw_r);
+    note_launches(2);
     return e;
 }
 

@@ -206,7 +206,10 @@ struct RouterBwdLaunch {
     const __nv_bfloat16 *x;     // [T, H]
     const int32_t *offsets, *counts, *perm_slot;
     float *dw_r;                // [E, H] (output)
+    float *dwr_part;            // [kDwrSegments, E, H] partial sums (workspace)
 };
+// Row segments of the dW_r reduction (partial sums per segment, then a fixed-order sum).
+constexpr int kDwrSegments = 8;
 
 // dX = sum over the token's slots of the dX rows (routed order) + dlogits . W_r.
 struct CombineBwdLaunch {

@@ -88,8 +88,9 @@ moe_ws_layout_t make_layout(const moe_shape_t &s) {
         L.dlogits = off;  off = align256(off + 4 * T * E);
         L.xp = off;       off = align256(off + 2 * R * H);
         L.dyp = off;      off = align256(off + 2 * R * H);
+        L.dwr_part = off; off = align256(off + 4 * static_cast<size_t>(kDwrSegments) * E * H);
     } else {
-        L.dh = L.aw = L.dtw_part = L.dlogits = L.xp = L.dyp = off;
+        L.dh = L.aw = L.dtw_part = L.dlogits = L.xp = L.dyp = L.dwr_part = off;
     }
     if (s.flags & MOE_SHAPE_MXFP8) {
         L.x_codes = off;  off = align256(off + R * H);
@@ -115,6 +116,7 @@ struct Ws {
     __nv_bfloat16 *dh, *aw;     // training only
     float *dtw_part, *dlogits;  // training only
     __nv_bfloat16 *xp, *dyp;    // training only: x and dY rows in routed order
+    float *dwr_part;            // training only: partial sums of dW_r
     uint8_t *x_codes, *x_scales, *a_codes, *a_scales;   // MXFP8 only
     bool training, mxfp8;
 };
@@ -149,6 +151,7 @@ Ws carve(void *ws, const moe_shape_t &s) {
     w.dlogits = reinterpret_cast<float *>(b + L.dlogits);
     w.xp = reinterpret_cast<__nv_bfloat16 *>(b + L.xp);
     w.dyp = reinterpret_cast<__nv_bfloat16 *>(b + L.dyp);
+    w.dwr_part = reinterpret_cast<float *>(b + L.dwr_part);
     w.mxfp8 = (s.flags & MOE_SHAPE_MXFP8) != 0;
     w.x_codes = b + L.x_codes;
     w.x_scales = b + L.x_scales;
@@ -417,6 +420,7 @@ moe_status_t run_router_bwd(const moe_shape_t &s, const void *x, const float *lo
     p.counts = w.counts;
     p.perm_slot = w.perm_slot;
     p.dw_r = dw_r;
+    p.dwr_part = w.dwr_part;
     moe_status_t r = cuda_status(launch_router_dlogits(p, st));
     if (r != MOE_OK) return r;
     return cuda_status(launch_router_dwr(p, st));

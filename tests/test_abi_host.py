@@ -127,9 +127,9 @@ def test_training_workspace_layout(lib):
     for cfg in CONFIGS.values():
         R = cfg.T * cfg.k
         base = B.moe_workspace_layout(B.shape(cfg.T, cfg.H, cfg.I, cfg.E, cfg.k))
-        assert base.dh == base.aw == base.dtw_part == base.dlogits == base.xp == base.dyp == base.total
+        assert base.dh == base.aw == base.dtw_part == base.dlogits == base.xp == base.dyp == base.dwr_part == base.total
         L = B.moe_workspace_layout(B.shape(cfg.T, cfg.H, cfg.I, cfg.E, cfg.k, training=True))
-        offs = [L.obuf, L.dh, L.aw, L.dtw_part, L.dlogits, L.xp, L.dyp, L.total]
+        offs = [L.obuf, L.dh, L.aw, L.dtw_part, L.dlogits, L.xp, L.dyp, L.dwr_part, L.total]
         assert offs == sorted(offs) and all(o % 256 == 0 for o in offs)
         assert L.obuf == base.obuf                      # the forward regions do not move
         assert L.aw - L.dh >= 2 * R * 2 * cfg.I
@@ -137,7 +137,8 @@ def test_training_workspace_layout(lib):
         assert L.dlogits - L.dtw_part >= 4 * R * ((cfg.I + 255) // 256)
         assert L.xp - L.dlogits >= 4 * cfg.T * cfg.E
         assert L.dyp - L.xp >= 2 * R * cfg.H
-        assert L.total - L.dyp >= 2 * R * cfg.H
+        assert L.dwr_part - L.dyp >= 2 * R * cfg.H
+        assert L.total - L.dwr_part >= 4 * 8 * cfg.E * cfg.H
 
 
 def test_training_calls_need_a_training_workspace(lib):
