@@ -188,17 +188,22 @@ router_dwr_sum_kernel(const float *__restrict__ part, int64_t n4, float *__restr
 
 // dX[t, :] = sum over t's slots of the dX rows (slot order), plus the router
 // term sum_e dl[t, e] w_r[e, :] (expert order for the dense form, slot order
-// over first occurrences otherwise). One warp per token (grid-stride): lane
-// j < k holds slot j's row and, for the sparse router term, its expert and
-// logit gradient; every lane then handles 8-column groups lane, lane + 32, ...
-// (all lanes run the same passes, so the shuffles see the whole warp).
+// over first occurrences otherwise). Block (64-token group, 256-column slice):
+// each warp walks 8 of the group's tokens over the slice, lane l owning columns
+// 8 l .. 8 l + 7, so the w_r rows of the slice (E x 1 KB) are re-read from L1 by
+// the block's tokens rather than from L2 by every token. Lane j < k holds slot
+// j's row and, for the sparse router term, its expert and logit gradient.
+constexpr int kCbTokens = 64;                 // tokens per block (8 per warp)
+
 __global__ void __launch_bounds__(256)
 combine_bwd_kernel(const CombineBwdLaunch p) {
     griddep_wait();
-    const int lane = threadIdx.x & 31;
-    const int groups = p.H >> 3;
-    const int warps = gridDim.x * (blockDim.x >> 5);
-    for (int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); t < p.T; t += warps) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int g = blockIdx.y * 32 + lane;               // 8-column group of this lane
+    const bool live = g < (p.H >> 3);
+    const int c = g * 8;
+    const int t_end = min(p.T, (blockIdx.x + 1) * kCbTokens);
+    for (int t = blockIdx.x * kCbTokens + warp; t < t_end; t += 8) {
         const int32_t *idx_t = p.topk_idx + static_cast<int64_t>(t) * p.k;
         const float *dl_t = p.dl != nullptr ? p.dl + static_cast<int64_t>(t) * p.E : nullptr;
         const int my_row = lane < p.k ? __ldg(&p.row_of[static_cast<int64_t>(t) * p.k + lane]) : -1;
@@ -211,60 +216,55 @@ combine_bwd_kernel(const CombineBwdLaunch p) {
                 my_d = dl_t[e];
             }
         }
-        for (int g0 = 0; g0 < groups; g0 += 32) {
-            const int g = g0 + lane;
-            const bool live = g < groups;
-            const int c = g * 8;
-            float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-            for (int j0 = 0; j0 < p.k; j0 += 8) {
-                uint4 v[8];
+        float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        for (int j0 = 0; j0 < p.k; j0 += 8) {
+            uint4 v[8];
 #pragma unroll
-                for (int jj = 0; jj < 8; ++jj) {
-                    const int r = __shfl_sync(0xffffffffu, my_row, (j0 + jj) & 31);
-                    v[jj] = (live && j0 + jj < p.k && r >= 0)
-                                ? __ldg(reinterpret_cast<const uint4 *>(p.xbuf + static_cast<int64_t>(r) * p.H + c))
-                                : make_uint4(0u, 0u, 0u, 0u);
-                }
+            for (int jj = 0; jj < 8; ++jj) {
+                const int r = __shfl_sync(0xffffffffu, my_row, (j0 + jj) & 31);
+                v[jj] = (live && j0 + jj < p.k && r >= 0)
+                            ? __ldg(reinterpret_cast<const uint4 *>(p.xbuf + static_cast<int64_t>(r) * p.H + c))
+                            : make_uint4(0u, 0u, 0u, 0u);
+            }
 #pragma unroll
-                for (int jj = 0; jj < 8; ++jj) {
-                    const uint32_t wv[4] = {v[jj].x, v[jj].y, v[jj].z, v[jj].w};
+            for (int jj = 0; jj < 8; ++jj) {
+                const uint32_t wv[4] = {v[jj].x, v[jj].y, v[jj].z, v[jj].w};
 #pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        acc[2 * q] += __uint_as_float(wv[q] << 16);
-                        acc[2 * q + 1] += __uint_as_float(wv[q] & 0xffff0000u);
-                    }
+                for (int q = 0; q < 4; ++q) {
+                    acc[2 * q] += __uint_as_float(wv[q] << 16);
+                    acc[2 * q + 1] += __uint_as_float(wv[q] & 0xffff0000u);
                 }
             }
-            if (dl_t != nullptr) {
-                const int n = p.dense ? p.E : p.k;
-                for (int j = 0; j < n; ++j) {
-                    int e = j;
-                    float d;
-                    if (p.dense) {
-                        d = dl_t[e];
-                    } else {
-                        e = __shfl_sync(0xffffffffu, my_e, j & 31);
-                        d = __shfl_sync(0xffffffffu, my_d, j & 31);
-                        if (e < 0) continue;
-                    }
-                    if (!live) continue;
-                    const float4 *wr = reinterpret_cast<const float4 *>(p.w_r + static_cast<int64_t>(e) * p.H + c);
-                    const float4 a = __ldg(wr), b = __ldg(wr + 1);
-                    acc[0] = fmaf(d, a.x, acc[0]);
-                    acc[1] = fmaf(d, a.y, acc[1]);
-                    acc[2] = fmaf(d, a.z, acc[2]);
-                    acc[3] = fmaf(d, a.w, acc[3]);
-                    acc[4] = fmaf(d, b.x, acc[4]);
-                    acc[5] = fmaf(d, b.y, acc[5]);
-                    acc[6] = fmaf(d, b.z, acc[6]);
-                    acc[7] = fmaf(d, b.w, acc[7]);
-                }
-            }
-            if (live)
-                *reinterpret_cast<uint4 *>(p.dx + static_cast<int64_t>(t) * p.H + c) =
-                    make_uint4(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]),
-                               pack_bf16x2(acc[4], acc[5]), pack_bf16x2(acc[6], acc[7]));
         }
+        if (dl_t != nullptr) {
+            const int n = p.dense ? p.E : p.k;
+            for (int j = 0; j < n; ++j) {
+                int e = j;
+                float d;
+                if (p.dense) {
+                    d = dl_t[e];
+                } else {
+                    e = __shfl_sync(0xffffffffu, my_e, j & 31);
+                    d = __shfl_sync(0xffffffffu, my_d, j & 31);
+                    if (e < 0) continue;
+                }
+                if (!live) continue;
+                const float4 *wr = reinterpret_cast<const float4 *>(p.w_r + static_cast<int64_t>(e) * p.H + c);
+                const float4 a = __ldg(wr), b = __ldg(wr + 1);
+                acc[0] = fmaf(d, a.x, acc[0]);
+                acc[1] = fmaf(d, a.y, acc[1]);
+                acc[2] = fmaf(d, a.z, acc[2]);
+                acc[3] = fmaf(d, a.w, acc[3]);
+                acc[4] = fmaf(d, b.x, acc[4]);
+                acc[5] = fmaf(d, b.y, acc[5]);
+                acc[6] = fmaf(d, b.z, acc[6]);
+                acc[7] = fmaf(d, b.w, acc[7]);
+            }
+        }
+        if (live)
+            *reinterpret_cast<uint4 *>(p.dx + static_cast<int64_t>(t) * p.H + c) =
+                make_uint4(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]),
+                           pack_bf16x2(acc[4], acc[5]), pack_bf16x2(acc[6], acc[7]));
     }
 }
 
@@ -335,8 +335,9 @@ cudaError_t launch_router_dwr(const RouterBwdLaunch &p, cudaStream_t st) {
 
 cudaError_t launch_combine_bwd(const CombineBwdLaunch &p, cudaStream_t st) {
     if (p.T == 0 || p.H == 0) return cudaSuccess;
-    // eight tokens (warps) per block
-    const cudaError_t e = launch_dep(combine_bwd_kernel, dim3(grid_for(p.T, 8)), dim3(256), 0, st, p);
+    // 64-token groups x 256-column slices
+    const dim3 grid((p.T + kCbTokens - 1) / kCbTokens, (p.H / 8 + 31) / 32);
+    const cudaError_t e = launch_dep(combine_bwd_kernel, grid, dim3(256), 0, st, p);
     note_launches(1);
     return e;
 }

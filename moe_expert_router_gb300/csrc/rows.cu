@@ -12,7 +12,7 @@ namespace {
 
 // rows[r, :] = x[perm_slot[r] / k, :] for r < *routed; with row_w, also
 // row_w[r] = topk_w[perm_slot[r]]. One warp per row (grid-stride over rows),
-// 16-byte chunks, four loads in flight per lane.
+// 16-byte chunks, eight loads in flight per lane.
 __global__ void __launch_bounds__(256)
 gather_rows_kernel(const __nv_bfloat16 *__restrict__ x, const int32_t *__restrict__ perm_slot,
                    const int32_t *__restrict__ routed, int k, int64_t H, __nv_bfloat16 *__restrict__ rows,
@@ -27,13 +27,12 @@ gather_rows_kernel(const __nv_bfloat16 *__restrict__ x, const int32_t *__restric
         const uint4 *src = reinterpret_cast<const uint4 *>(x + static_cast<int64_t>(s / k) * H);
         uint4 *dst = reinterpret_cast<uint4 *>(rows + r * H);
         int c = lane;
-        for (; c + 96 < chunks; c += 128) {
-            const uint4 v0 = __ldg(src + c), v1 = __ldg(src + c + 32), v2 = __ldg(src + c + 64),
-                        v3 = __ldg(src + c + 96);
-            dst[c] = v0;
-            dst[c + 32] = v1;
-            dst[c + 64] = v2;
-            dst[c + 96] = v3;
+        for (; c + 224 < chunks; c += 256) {
+            uint4 v[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) v[j] = __ldg(src + c + 32 * j);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) dst[c + 32 * j] = v[j];
         }
         for (; c < chunks; c += 32) dst[c] = __ldg(src + c);
         if (row_w != nullptr && lane == 0) row_w[r] = topk_w[s];
