@@ -62,13 +62,18 @@ typedef struct moe_shape {
     int64_t I;   /* expert intermediate size (w1 has 2I rows per expert) */
     int64_t E;   /* experts */
     int32_t k;   /* experts per token */
-    int32_t flags;  /* 0, or an OR of MOE_SHAPE_TRAINING and MOE_SHAPE_MXFP8 */
+    int32_t flags;  /* 0, or an OR of the MOE_SHAPE_* flags below */
 } moe_shape_t;
 
 /* moe_shape_t.flags: the workspace also holds the backward's intermediates. */
 #define MOE_SHAPE_TRAINING 0x1
 /* moe_shape_t.flags: the workspace also holds the MXFP8 path's quantized x and a. */
 #define MOE_SHAPE_MXFP8 0x2
+/* moe_shape_t.flags: the w1 / w2 pointers given to moe_dispatch_gemm1,
+ * moe_swiglu_gemm2_combine and moe_forward are in the tile-packed layout of
+ * moe_pack_weights (bf16 forward only: not with MOE_SHAPE_TRAINING or
+ * MOE_SHAPE_MXFP8, which return MOE_ERR_UNSUPPORTED). */
+#define MOE_SHAPE_PACKED_WEIGHTS 0x4
 
 #define MOE_SCORE_SOFTMAX 0
 #define MOE_SCORE_SIGMOID 1
@@ -373,6 +378,36 @@ moe_status_t moe_backward(const void *x, const float *w_r, const float *logits,
                           const void *w2, const void *h, const void *dy, const moe_shape_t *shape,
                           const moe_router_cfg_t *cfg, void *dx, void *dw1, void *dw2, float *dw_r,
                           float *dtopk_w, void *ws, size_t ws_bytes, void *stream);
+
+/* ------------------------------------------------------------------ packed weights
+ *
+ * The forward GEMMs read one weight slab per pipeline stage: 256 rows x 64
+ * K-elements of one expert (stage 1: 128 gate rows and the matching 128 up
+ * rows; stage 2: 256 rows of w2[e]). Packed, each slab is one contiguous 32 KB
+ * block already in the 128-byte-swizzled shared-memory image, fetched with one
+ * bulk copy instead of 256 strided 128-byte pieces. Pack once per weight
+ * update (the layout is a pure permutation plus zero padding; the values are
+ * unchanged, so results are identical) and pass the packed buffers with
+ * flags |= MOE_SHAPE_PACKED_WEIGHTS.
+ *
+ *   w1p: 32 KB tiles (e, n, kb), n < ceil(I/128), kb < ceil(H/64), in that
+ *        order; tile row r < 128 = w1[e][128 n + r], row 128 + r =
+ *        w1[e][I + 128 n + r] (zero where 128 n + r >= I), columns
+ *        [64 kb, 64 kb + 64) (zero past H); 16-byte chunk c of row r at byte
+ *        128 r + 16 (c XOR (r mod 8)).
+ *   w2p: tiles (e, n, kb), n < ceil(H/256), kb < ceil(I/64); row r =
+ *        w2[e][256 n + r] (zero past H), columns [64 kb, 64 kb + 64) (zero
+ *        past I); same chunk order.
+ */
+
+/* Bytes of the packed w1 and w2 for `shape` (either pointer may be NULL). Host-only. */
+moe_status_t moe_packed_weights_size(const moe_shape_t *shape, size_t *w1p_bytes, size_t *w2p_bytes);
+
+/* Pack w1 [E,2I,H] into w1p and w2 [E,H,I] into w2p (bf16, 16-byte aligned,
+ * caller-owned; a pair of NULL src/dst pointers skips that tensor). Enqueued
+ * on `stream`. */
+moe_status_t moe_pack_weights(const void *w1, const void *w2, const moe_shape_t *shape, void *w1p, void *w2p,
+                              void *stream);
 
 /* ------------------------------------------------------------------ MXFP8
  *

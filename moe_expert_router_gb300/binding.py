@@ -25,6 +25,7 @@ SCORE_SOFTMAX = 0
 SCORE_SIGMOID = 1
 SHAPE_TRAINING = 0x1
 SHAPE_MXFP8 = 0x2
+SHAPE_PACKED_WEIGHTS = 0x4
 
 
 class MoEError(RuntimeError):
@@ -86,6 +87,9 @@ _SIG = {
     "moe_forward_mx": [_P, _P, _P, _P, _P, _P, _P, ctypes.POINTER(Shape), _P, _P, ctypes.c_size_t, _P],
     "moe_dispatch_rows": [_P, _P, ctypes.POINTER(Shape), _P, _P, _P, ctypes.c_size_t, _P],
     "moe_combine_rows": [_P, ctypes.POINTER(Shape), _P, _P, ctypes.c_size_t, _P],
+    "moe_packed_weights_size": [ctypes.POINTER(Shape), ctypes.POINTER(ctypes.c_size_t),
+                                ctypes.POINTER(ctypes.c_size_t)],
+    "moe_pack_weights": [_P, _P, ctypes.POINTER(Shape), _P, _P, _P],
     "moe_get_device_error": [_P, ctypes.POINTER(ctypes.c_int32), _P],
     "moe_status_string": [ctypes.c_int],
     "moe_kernel_launch_count": [],
@@ -135,8 +139,9 @@ def _stream(stream, like):
     return ctypes.c_void_p(stream.cuda_stream)
 
 
-def shape(T, H, I, E, k, training=False, mxfp8=False) -> Shape:
-    flags = (SHAPE_TRAINING if training else 0) | (SHAPE_MXFP8 if mxfp8 else 0)
+def shape(T, H, I, E, k, training=False, mxfp8=False, packed=False) -> Shape:
+    flags = ((SHAPE_TRAINING if training else 0) | (SHAPE_MXFP8 if mxfp8 else 0) |
+             (SHAPE_PACKED_WEIGHTS if packed else 0))
     return Shape(int(T), int(H), int(I), int(E), int(k), flags)
 
 
@@ -331,6 +336,30 @@ def moe_get_device_error(ws, stream=None) -> int:
 
 def moe_kernel_launch_count() -> int:
     return int(load().moe_kernel_launch_count())
+
+
+def moe_packed_weights_size(shp: Shape) -> tuple:
+    """Bytes of the tile-packed w1 and w2 for this shape."""
+    a, b = ctypes.c_size_t(0), ctypes.c_size_t(0)
+    _check("moe_packed_weights_size", load().moe_packed_weights_size(ctypes.byref(shp), ctypes.byref(a),
+                                                                     ctypes.byref(b)))
+    return a.value, b.value
+
+
+def moe_pack_weights(w1, w2, shp: Shape, w1p=None, w2p=None, stream=None):
+    """Tile-packed copies of w1 [E, 2I, H] and w2 [E, H, I] (uint8 tensors, allocated when
+    not given; either weight may be None to skip it). Pass them to the forward calls with a
+    shape made with packed=True."""
+    n1, n2 = moe_packed_weights_size(shp)
+    like = w1 if w1 is not None else w2
+    if w1 is not None and w1p is None:
+        w1p = torch.empty(n1, dtype=torch.uint8, device=like.device)
+    if w2 is not None and w2p is None:
+        w2p = torch.empty(n2, dtype=torch.uint8, device=like.device)
+    _check("moe_pack_weights", load().moe_pack_weights(
+        _ptr(w1) if w1 is not None else None, _ptr(w2) if w2 is not None else None, ctypes.byref(shp),
+        _ptr(w1p) if w1 is not None else None, _ptr(w2p) if w2 is not None else None, _stream(stream, like)))
+    return w1p, w2p
 
 
 def new_workspace(shp: Shape, device=None) -> torch.Tensor:

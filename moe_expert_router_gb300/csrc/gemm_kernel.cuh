@@ -176,6 +176,8 @@ struct GemmArgs {
     int R;                      // routed rows
     int T, splits, kb_per_split, kb_total, kb_h;   // router
     int n_mma;                  // router: N of its MMAs and rows of its weight tile (E rounded up to 32, <= 256)
+    const uint8_t *bpack;       // stage 1 / 2: the tile-packed weights (pack.cu), or null for the TMA views
+    int kb_tiles;               // K tiles per packed weight slab
     int total_units;            // router / weight gradients: known on the host; else -1
 };
 
@@ -467,13 +469,22 @@ tc_gemm_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs g) {
                         const int kx = kb * kStageK<MODE>;
                         tma_load_2d(sa, &maps.a, kx, t.row0, full);                         // dispatched x rows
                         if (two) tma_load_2d(sa + A_HALF_BYTES, &maps.a, kx, t.row0 + BM, full);
-                        tma_load_2d(sb, &maps.b, kx, row, full);                            // gate rows
-                        tma_load_2d(sb + hn * 128, &maps.b, kx, row + g.half, full);        // up rows
+                        if (MODE == kStage1 && g.bpack != nullptr) {                        // packed gate + up slab
+                            bulk_load(sb, g.bpack + ((static_cast<int64_t>(t.e) * g.n_tiles + t.n) * g.kb_tiles + kb) *
+                                                        B_BYTES, B_BYTES, full);
+                        } else {
+                            tma_load_2d(sb, &maps.b, kx, row, full);                        // gate rows
+                            tma_load_2d(sb + hn * 128, &maps.b, kx, row + g.half, full);    // up rows
+                        }
                     } else if constexpr (MODE == kStage2 || MODE == kStage2Mx) {
                         const int kx = kb * kStageK<MODE>;
                         tma_load_2d(sa, &maps.a, kx, t.row0, full);
                         if (two) tma_load_2d(sa + A_HALF_BYTES, &maps.a, kx, t.row0 + BM, full);
-                        tma_load_2d(sb, &maps.b, kx, t.e * g.b_rows + t.n * kUnitN<MODE>, full);
+                        if (MODE == kStage2 && g.bpack != nullptr)                          // packed slab
+                            bulk_load(sb, g.bpack + ((static_cast<int64_t>(t.e) * g.n_tiles + t.n) * g.kb_tiles + kb) *
+                                                        B_BYTES, B_BYTES, full);
+                        else
+                            tma_load_2d(sb, &maps.b, kx, t.e * g.b_rows + t.n * kUnitN<MODE>, full);
                     } else if constexpr (MODE == kRouter) {
                         const int seg = kb / g.kb_h;              // 0: hi, 1: mid, 2: lo
                         const int kx = (kb - seg * g.kb_h) * BK;
@@ -1060,6 +1071,8 @@ inline GemmArgs grouped_args(const GemmLaunch &p) {
     g.sfa = p.sfa;
     g.sfb = p.sfb;
     g.out_sf = p.out_sf;
+    g.bpack = p.bpack;
+    g.kb_tiles = (p.K + BK - 1) / BK;
     g.E = p.E;
     g.k = p.k;
     g.K = p.K;

@@ -127,6 +127,7 @@ struct MetadataLaunch {
 
 // One grouped GEMM launch (forward stages 1 and 2, backward dA / dX / dW2 / dW1).
 struct GemmLaunch {
+    const uint8_t *bpack;       // stage 1 / 2: tile-packed weights (pack.cu) instead of tm_b, or null
     const CUtensorMap *tm_a;    // host-encoded tensor maps (copied into the launch);
     const CUtensorMap *tm_b;    // tm_a, tm_out2 and tm_out3 may be null when unused
     const CUtensorMap *tm_out;
@@ -180,6 +181,11 @@ cudaError_t launch_routing_metadata(const MetadataLaunch &p, cudaStream_t st);
 cudaError_t launch_gemm1_swiglu(const GemmLaunch &p, cudaStream_t st);
 cudaError_t launch_gemm2_scatter(const GemmLaunch &p, cudaStream_t st);
 cudaError_t launch_router_gemm(const RouterGemmLaunch &p, cudaStream_t st);
+// Tile-packed forward weights (pack.cu): tile counts and the packing copies.
+int64_t packed_w1_tiles(int64_t E, int64_t H, int64_t I);
+int64_t packed_w2_tiles(int64_t E, int64_t H, int64_t I);
+cudaError_t launch_pack_w1(const __nv_bfloat16 *w1, int64_t E, int64_t H, int64_t I, void *w1p, cudaStream_t st);
+cudaError_t launch_pack_w2(const __nv_bfloat16 *w2, int64_t E, int64_t H, int64_t I, void *w2p, cudaStream_t st);
 cudaError_t launch_combine(const CombineLaunch &p, cudaStream_t st);
 // rows[r, :] = x[perm_slot[r] / k, :] for routed rows r < *routed, and with row_w
 // row_w[r] = topk_w[perm_slot[r]] (rows.cu).

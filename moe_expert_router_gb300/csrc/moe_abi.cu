@@ -56,8 +56,10 @@ bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 moe_status_t check_shape(const moe_shape_t *s) {
     if (s == nullptr) return MOE_ERR_INVALID_ARG;
     if (s->T < 0 || s->H <= 0 || s->I <= 0 || s->E <= 0 || s->k <= 0 ||
-        (s->flags & ~(MOE_SHAPE_TRAINING | MOE_SHAPE_MXFP8)) != 0)
+        (s->flags & ~(MOE_SHAPE_TRAINING | MOE_SHAPE_MXFP8 | MOE_SHAPE_PACKED_WEIGHTS)) != 0)
         return MOE_ERR_INVALID_ARG;
+    if ((s->flags & MOE_SHAPE_PACKED_WEIGHTS) && (s->flags & (MOE_SHAPE_TRAINING | MOE_SHAPE_MXFP8)))
+        return MOE_ERR_UNSUPPORTED;
     if (s->k > 32 || s->k > s->E || s->E > 1024) return MOE_ERR_UNSUPPORTED;
     if (s->H % 8 != 0 || s->I % 8 != 0) return MOE_ERR_UNSUPPORTED;
     if (s->T * s->k >= (int64_t(1) << 31)) return MOE_ERR_UNSUPPORTED;
@@ -207,6 +209,10 @@ moe_status_t run_gemm1(const moe_shape_t &s, const void *x, const void *w1, void
     GemmLaunch p = base_launch(s, w, d);
     p.tm_a = &tm_x;
     p.tm_b = &tm_w1;
+    if (s.flags & MOE_SHAPE_PACKED_WEIGHTS) {   // w1 is the packed tile array
+        p.bpack = static_cast<const uint8_t *>(w1);
+        p.tm_b = &tm_x;
+    }
     p.tm_out = &tm_out;
     p.tm_out2 = h ? &tm_hg : nullptr;
     p.tm_out3 = h ? &tm_hu : nullptr;
@@ -236,6 +242,10 @@ moe_status_t run_gemm2(const moe_shape_t &s, const void *a, const float *topk_w,
     GemmLaunch p = base_launch(s, w, d);
     p.tm_a = &tm_a;
     p.tm_b = &tm_w2;
+    if (s.flags & MOE_SHAPE_PACKED_WEIGHTS) {   // w2 is the packed tile array
+        p.bpack = static_cast<const uint8_t *>(w2);
+        p.tm_b = &tm_a;
+    }
     p.tm_out = &tm_out;
     p.sched = w.sched2;
     p.topk_w = topk_w;
@@ -776,6 +786,33 @@ moe_status_t moe_swiglu_gemm2_combine(const void *a, const float *topk_w, const 
     DeviceState *d = nullptr;
     if ((r = device_state(&d)) != MOE_OK) return r;
     return run_gemm2(*shape, a, topk_w, w2, y, carve(ws, *shape), *d, static_cast<cudaStream_t>(stream));
+}
+
+moe_status_t moe_packed_weights_size(const moe_shape_t *shape, size_t *w1p_bytes, size_t *w2p_bytes) {
+    moe_status_t r = check_shape(shape);
+    if (r != MOE_OK) return r;
+    constexpr size_t kTile = 32768;
+    if (w1p_bytes) *w1p_bytes = kTile * static_cast<size_t>(packed_w1_tiles(shape->E, shape->H, shape->I));
+    if (w2p_bytes) *w2p_bytes = kTile * static_cast<size_t>(packed_w2_tiles(shape->E, shape->H, shape->I));
+    return MOE_OK;
+}
+
+moe_status_t moe_pack_weights(const void *w1, const void *w2, const moe_shape_t *shape, void *w1p, void *w2p,
+                              void *stream) {
+    moe_status_t r = check_shape(shape);
+    if (r != MOE_OK) return r;
+    if ((w1 == nullptr) != (w1p == nullptr) || (w2 == nullptr) != (w2p == nullptr)) return MOE_ERR_INVALID_ARG;
+    if ((w1 && (!aligned16(w1) || !aligned16(w1p))) || (w2 && (!aligned16(w2) || !aligned16(w2p))))
+        return MOE_ERR_INVALID_ARG;
+    DeviceState *d = nullptr;
+    if ((r = device_state(&d)) != MOE_OK) return r;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (w1 && (r = cuda_status(launch_pack_w1(static_cast<const __nv_bfloat16 *>(w1), shape->E, shape->H, shape->I,
+                                              w1p, st))) != MOE_OK)
+        return r;
+    if (w2)
+        r = cuda_status(launch_pack_w2(static_cast<const __nv_bfloat16 *>(w2), shape->E, shape->H, shape->I, w2p, st));
+    return r;
 }
 
 moe_status_t moe_forward(const void *x, const int32_t *topk_idx, const float *topk_w, const void *w1,

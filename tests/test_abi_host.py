@@ -166,7 +166,7 @@ def test_training_calls_need_a_training_workspace(lib):
     assert lib.moe_backward(p, p, None, p, p, p, p, p, p, ctypes.byref(train), ctypes.byref(cfg), p, p, p,
                             p, p, p, big, None) == 1   # w_r without logits
     # unknown shape flags
-    bad = B.Shape(16, 64, 64, 4, 2, 4)
+    bad = B.Shape(16, 64, 64, 4, 2, 8)
     n = ctypes.c_size_t()
     assert lib.moe_workspace_size(ctypes.byref(bad), ctypes.byref(n)) == 1
 
@@ -198,3 +198,22 @@ def test_mxfp8_layout_and_argument_checks(lib):
     assert lib.moe_swiglu_gemm2_combine_mx(p, p, p, p, p, ctypes.byref(odd), p, p, big, None) == 2
     plain = B.shape(16, 256, 256, 4, 2)
     assert lib.moe_forward_mx(p, p, p, p, p, p, p, ctypes.byref(plain), p, p, big, None) == 1
+
+
+def test_packed_weight_sizes_and_flag_checks(lib):
+    for cfg in CONFIGS.values():
+        n1, n2 = B.moe_packed_weights_size(B.shape(cfg.T, cfg.H, cfg.I, cfg.E, cfg.k, packed=True))
+        assert n1 == 32768 * cfg.E * -(-cfg.I // 128) * -(-cfg.H // 64)
+        assert n2 == 32768 * cfg.E * -(-cfg.H // 256) * -(-cfg.I // 64)
+        assert n1 >= 2 * cfg.E * 2 * cfg.I * cfg.H and n2 >= 2 * cfg.E * cfg.H * cfg.I
+    size = ctypes.c_size_t(0)
+    for bad in (B.shape(16, 64, 64, 4, 2, training=True, packed=True),
+                B.shape(16, 128, 128, 4, 2, mxfp8=True, packed=True)):
+        assert lib.moe_workspace_size(ctypes.byref(bad), ctypes.byref(size)) == 2
+    shp = B.shape(16, 64, 64, 4, 2, packed=True)
+    p = ctypes.c_void_p(1 << 20)
+    # source and destination must come in pairs (checked before any device call)
+    assert lib.moe_pack_weights(p, None, ctypes.byref(shp), None, None, None) == 1
+    assert lib.moe_pack_weights(None, p, ctypes.byref(shp), None, None, None) == 1
+    misaligned = ctypes.c_void_p((1 << 20) + 8)
+    assert lib.moe_pack_weights(p, None, ctypes.byref(shp), misaligned, None, None) == 1
