@@ -82,6 +82,14 @@ constexpr int HELPER_WARPS = 4;
 constexpr int HELPER_THREADS = HELPER_WARPS * 32;
 constexpr int UQ = 4;                        // depth of the in-CTA unit queue
 constexpr uint64_t kDrainLimitNs = 10000000ull;  // 10 ms
+// Stages 1 and 2 hold their stages in a byte ring over the A and B arrays (192 KB)
+// with slots sized to the unit: 64 KB for a 256-row unit, 48 KB for a 128-row
+// one. A k-block's refill only starts once its slot has been consumed, so the
+// number of slots in flight sets how much load latency is covered: a 256-row
+// unit's three slots keep the tensor pipe fed, a 128-row unit gets four. At
+// most kRingSlots slots are in flight.
+constexpr int kRingSlots = 6;
+constexpr uint32_t kRingBytes = 3u * 64u * 1024u;
 
 enum Mode : int {
     kStage1 = 0, kStage2 = 1, kRouter = 2,
@@ -93,6 +101,7 @@ enum Mode : int {
 
 template <int MODE> constexpr bool kIsMx = MODE == kStage1Mx || MODE == kStage2Mx;
 template <int MODE> constexpr bool kIsStage1 = MODE == kStage1 || MODE == kStage1SaveH || MODE == kStage1Mx;
+template <int MODE> constexpr bool kRing = MODE == kStage1 || MODE == kStage2;
 template <int MODE> constexpr bool kAMn = MODE == kBwdDW2 || MODE == kBwdDW1;
 template <int MODE> constexpr bool kBMn = MODE >= kBwdDA && MODE <= kBwdDW1;
 template <int MODE> constexpr bool kWeightGrad = MODE == kBwdDW2 || MODE == kBwdDW1;
@@ -125,8 +134,8 @@ struct __align__(1024) Smem {
     uint8_t a[STAGES][A_BYTES];
     uint8_t b[STAGES][B_BYTES];
     uint8_t stage_out[EPI_WARPS][32 * 128];  // per epilogue warp: one 32 x 64 or two 32 x 32 bf16 boxes
-    uint64_t full[STAGES];
-    uint64_t empty[STAGES];
+    uint64_t full[STAGES > kRingSlots ? STAGES : kRingSlots];   // stages, or ring slots (stages 1 / 2)
+    uint64_t empty[STAGES > kRingSlots ? STAGES : kRingSlots];
     uint64_t acc_full;
     uint64_t acc_empty;
     uint64_t uq_full[UQ];
@@ -140,6 +149,8 @@ struct __align__(1024) Smem {
 };
 
 constexpr size_t SMEM_BYTES = sizeof(Smem) + 1024;  // + slack to align the base to 1024
+static_assert(STAGES * (A_BYTES + B_BYTES) == kRingBytes && offsetof(Smem, b) == STAGES * A_BYTES,
+              "the stage arrays must form one contiguous ring");
 
 // Tensor maps of one launch (unused ones are copies of a used one).
 struct GemmMaps {
@@ -276,6 +287,9 @@ __device__ __forceinline__ float silu_mul(float g, float u) {
 __device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xffff0000u); }
 
+// Bytes of A a stage of unit t holds: two 128-row halves or one.
+__device__ __forceinline__ uint32_t unit_a_bytes(const Unit &t) { return t.rows > BM ? A_BYTES : A_HALF_BYTES; }
+
 // Write 16 packed words (32 bf16 of one row) into a 32 x 32 box staged with the
 // 64-byte swizzle (what a TMA store of a 64-byte-wide box expects).
 __device__ __forceinline__ void stage_row32(uint32_t buf, int lane, const uint32_t (&pk)[16]) {
@@ -396,7 +410,7 @@ tc_gemm_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs g) {
     const int lane = threadIdx.x & 31;
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < STAGES; ++s) {
+        for (int s = 0; s < (STAGES > kRingSlots ? STAGES : kRingSlots); ++s) {
             // MXFP8: the producer's expect_tx arrival plus one per scale-factor thread
             mbar_init(smem_addr(&sm.full[s]), kIsMx<MODE> ? 1 + HELPER_THREADS : 1);
             mbar_init(smem_addr(&sm.empty[s]), 1);
@@ -431,6 +445,13 @@ tc_gemm_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs g) {
         int stage = 0, issued = 0, q = 0;
         uint32_t phase = 0, qphase = 0;
         bool ok = true;
+        // ring modes: slots rrel .. rj - 1 are in flight; slot m uses barrier pair
+        // m % kRingSlots and the bytes [rstart, rend) recorded under that index
+        const uint32_t ring0 = smem_addr(sm.a[0]);
+        uint32_t rhead = 0, rstart[kRingSlots], rend[kRingSlots];
+        int rj = 0, rrel = 0;
+#pragma unroll
+        for (int i = 0; i < kRingSlots; ++i) rstart[i] = rend[i] = 0;
         while (true) {
             int u = 0;
             if (lane == 0) u = atomicAdd(&g.sched[0], 1);
@@ -452,15 +473,50 @@ tc_gemm_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs g) {
             const Unit t = decode_unit<MODE>(u, g);
             const bool two = t.rows > BM;            // second half present
             // one or two 128-row halves of A (K-major rows or MN-major atoms) and the B tile
-            const uint32_t tx_bytes = (two ? A_BYTES : A_HALF_BYTES) + (MODE == kRouter ? g.n_mma : kUnitN<MODE>) * 128;
+            const uint32_t a_bytes = unit_a_bytes(t);
+            const uint32_t tx_bytes = a_bytes + (MODE == kRouter ? g.n_mma : kUnitN<MODE>) * 128;
             for (int kb = t.kb0; kb < t.kb1; ++kb) {
-                bool e_ok = true;
-                if (lane == 0) e_ok = mbar_wait(smem_addr(&sm.empty[stage]), phase ^ 1u, abort_flag, g.err);
-                e_ok = __shfl_sync(0xffffffffu, e_ok, 0);
-                if (!e_ok) { ok = false; break; }
-                const uint32_t full = smem_addr(&sm.full[stage]);
-                const uint32_t sa = smem_addr(sm.a[stage]);
-                const uint32_t sb = smem_addr(sm.b[stage]);
+                uint32_t full, sa, sb;
+                if constexpr (kRing<MODE>) {
+                    // a slot: the unit's A rows, then its B tile, contiguous; a slot that
+                    // would pass the end of the ring starts at its beginning
+                    const uint32_t bytes = a_bytes + B_BYTES;
+                    const uint32_t base = (rhead + bytes > kRingBytes) ? 0u : rhead;
+                    // the newest in-flight slot that must be consumed first: one whose
+                    // bytes the new slot reuses, or the one whose barrier pair it takes
+                    int need = rj - kRingSlots;
+#pragma unroll
+                    for (int i = 0; i < kRingSlots; ++i) {
+                        const int m = rj - kRingSlots + ((i - (rj - kRingSlots)) % kRingSlots + kRingSlots) % kRingSlots;
+                        if (m >= rrel && m >= 0 && rstart[i] < base + bytes && base < rend[i] && m > need) need = m;
+                    }
+                    if (need >= rrel) {
+                        bool e_ok = true;
+                        if (lane == 0)
+                            e_ok = mbar_wait(smem_addr(&sm.empty[need % kRingSlots]),
+                                             static_cast<uint32_t>(need / kRingSlots) & 1u, abort_flag, g.err);
+                        e_ok = __shfl_sync(0xffffffffu, e_ok, 0);
+                        if (!e_ok) { ok = false; break; }
+                        rrel = need + 1;
+                    }
+                    const int slot = rj % kRingSlots;
+#pragma unroll
+                    for (int i = 0; i < kRingSlots; ++i)
+                        if (i == slot) { rstart[i] = base; rend[i] = base + bytes; }
+                    rhead = base + bytes;
+                    full = smem_addr(&sm.full[slot]);
+                    sa = ring0 + base;
+                    sb = sa + a_bytes;
+                    ++rj;
+                } else {
+                    bool e_ok = true;
+                    if (lane == 0) e_ok = mbar_wait(smem_addr(&sm.empty[stage]), phase ^ 1u, abort_flag, g.err);
+                    e_ok = __shfl_sync(0xffffffffu, e_ok, 0);
+                    if (!e_ok) { ok = false; break; }
+                    full = smem_addr(&sm.full[stage]);
+                    sa = smem_addr(sm.a[stage]);
+                    sb = smem_addr(sm.b[stage]);
+                }
                 if (lane == 0) {
                     mbar_arrive_expect_tx(full, tx_bytes);
                     if constexpr (kIsStage1<MODE>) {
@@ -520,11 +576,16 @@ tc_gemm_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs g) {
         }
         if (!ok && lane == 0) {
             // let the copies already issued land before the CTA exits
-            int s = stage;
-            uint32_t ph = phase;
-            for (int i = 0; i < min(issued, STAGES); ++i) {
-                if (--s < 0) { s = STAGES - 1; ph ^= 1u; }
-                drain_wait(smem_addr(&sm.full[s]), ph);
+            if constexpr (kRing<MODE>) {
+                for (int m = rrel; m < rj; ++m)
+                    drain_wait(smem_addr(&sm.full[m % kRingSlots]), static_cast<uint32_t>(m / kRingSlots) & 1u);
+            } else {
+                int s = stage;
+                uint32_t ph = phase;
+                for (int i = 0; i < min(issued, STAGES); ++i) {
+                    if (--s < 0) { s = STAGES - 1; ph ^= 1u; }
+                    drain_wait(smem_addr(&sm.full[s]), ph);
+                }
             }
         }
     } else if (warp == 1) {
@@ -533,6 +594,9 @@ tc_gemm_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs g) {
             int stage = 0, q = 0;
             uint32_t phase = 0, acc_phase = 0, qphase = 0, tail_phase = 0;
             bool ok = true, any = false;
+            const uint32_t ring0 = smem_addr(sm.a[0]);
+            uint32_t mhead = 0;                 // ring modes: the producer's slot sequence, replayed
+            int mj = 0;
             while (true) {
                 if (!mbar_wait(smem_addr(&sm.uq_full[q]), qphase, abort_flag, g.err)) { ok = false; break; }
                 const int u = unit_q[q];
@@ -547,8 +611,24 @@ tc_gemm_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs g) {
                     break;
                 }
                 tc_fence_after();
+                const uint32_t a_bytes = unit_a_bytes(t);
                 for (int kb = t.kb0; kb < t.kb1; ++kb) {
-                    if (!mbar_wait(smem_addr(&sm.full[stage]), phase, abort_flag, g.err)) {
+                    uint32_t full_bar, empty_bar, fparity, ring_sa = 0;
+                    if constexpr (kRing<MODE>) {
+                        const uint32_t bytes = a_bytes + B_BYTES;
+                        const uint32_t base = (mhead + bytes > kRingBytes) ? 0u : mhead;
+                        mhead = base + bytes;
+                        full_bar = smem_addr(&sm.full[mj % kRingSlots]);
+                        empty_bar = smem_addr(&sm.empty[mj % kRingSlots]);
+                        fparity = static_cast<uint32_t>(mj / kRingSlots) & 1u;
+                        ring_sa = ring0 + base;
+                        ++mj;
+                    } else {
+                        full_bar = smem_addr(&sm.full[stage]);
+                        empty_bar = smem_addr(&sm.empty[stage]);
+                        fparity = phase;
+                    }
+                    if (!mbar_wait(full_bar, fparity, abort_flag, g.err)) {
                         ok = false;
                         break;
                     }
@@ -565,8 +645,8 @@ tc_gemm_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs g) {
                             tc_fence_after();
                         }
                     }
-                    const uint32_t sa = smem_addr(sm.a[stage]);
-                    const uint32_t sb = smem_addr(sm.b[stage]);
+                    const uint32_t sa = kRing<MODE> ? ring_sa : smem_addr(sm.a[stage]);
+                    const uint32_t sb = kRing<MODE> ? ring_sa + a_bytes : smem_addr(sm.b[stage]);
                     if constexpr (kIsMx<MODE>) {
                         // four K = 32 steps; the scale words of this stage hold one byte per step
                         const uint32_t sf = tmem_base + kSfBase<MODE> + stage * kSfStride;
@@ -593,7 +673,7 @@ tc_gemm_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs g) {
                                          idesc, acc);
                         }
                     }
-                    mma_commit(smem_addr(&sm.empty[stage]));   // frees the smem stage
+                    mma_commit(empty_bar);                     // frees the smem stage (or slot)
                     any = true;
                     if (++stage == STAGES) { stage = 0; phase ^= 1u; }
                 }
