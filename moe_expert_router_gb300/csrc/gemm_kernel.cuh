@@ -186,7 +186,10 @@ struct GemmArgs {
     int out_ld;                 // row stride (elements) of out / out2 / out3
     int R;                      // routed rows
     int T, splits, kb_per_split, kb_total, kb_h;   // router
-    int n_mma;                  // router: N of its MMAs and rows of its weight tile (E rounded up to 32, <= 256)
+    int n_mma;                  // router: N of its MMAs and rows of its weight tile (E rounded up to 32, <= 256;
+                                //   3 router_seg with the parts fused)
+    int router_seg;             // router: accumulator columns of each of the hi / mid / lo parts when one
+                                //   MMA covers all three (E <= 64), else 0
     const uint8_t *bpack;       // stage 1 / 2: the tile-packed weights (pack.cu), or null for the TMA views
     int kb_tiles;               // K tiles per packed weight slab
     int total_units;            // router / weight gradients: known on the host; else -1
@@ -542,11 +545,20 @@ tc_gemm_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs g) {
                         else
                             tma_load_2d(sb, &maps.b, kx, t.e * g.b_rows + t.n * kUnitN<MODE>, full);
                     } else if constexpr (MODE == kRouter) {
-                        const int seg = kb / g.kb_h;              // 0: hi, 1: mid, 2: lo
-                        const int kx = (kb - seg * g.kb_h) * BK;
-                        tma_load_2d(sa, &maps.a, kx, t.row0, full);
-                        if (two) tma_load_2d(sa + A_HALF_BYTES, &maps.a, kx, t.row0 + BM, full);
-                        tma_load_2d(sb, &maps.b, kx, seg * g.E + t.n * BN, full);
+                        if (g.router_seg) {
+                            // one x tile, then the hi, mid and lo rows of w_r, router_seg rows apart
+                            const int kx = kb * BK;
+                            tma_load_2d(sa, &maps.a, kx, t.row0, full);
+                            if (two) tma_load_2d(sa + A_HALF_BYTES, &maps.a, kx, t.row0 + BM, full);
+                            for (int part = 0; part < 3; ++part)
+                                tma_load_2d(sb + part * g.router_seg * ROW_BYTES, &maps.b, kx, part * g.E, full);
+                        } else {
+                            const int seg = kb / g.kb_h;              // 0: hi, 1: mid, 2: lo
+                            const int kx = (kb - seg * g.kb_h) * BK;
+                            tma_load_2d(sa, &maps.a, kx, t.row0, full);
+                            if (two) tma_load_2d(sa + A_HALF_BYTES, &maps.a, kx, t.row0 + BM, full);
+                            tma_load_2d(sb, &maps.b, kx, seg * g.E + t.n * BN, full);
+                        }
                     } else if constexpr (MODE == kBwdDA || MODE == kBwdDX) {
                         // dA: dispatched dY rows; dX: dH rows
                         tma_load_2d(sa, &maps.a, kb * BK, t.row0, full);
@@ -1013,10 +1025,25 @@ tc_gemm_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs g) {
                     float *dst = g.logits_part +
                                  (static_cast<int64_t>(t.split) * g.T + t.row0 + row) * g.n_out + col0;
                     const bool vec = (g.n_out & 3) == 0;
+                    const int ncols = g.router_seg ? g.router_seg : g.n_mma;
 #pragma unroll 1
-                    for (int c = 0; c < g.n_mma; c += 32) {
+                    for (int c = 0; c < ncols; c += 32) {
                         uint32_t v[32];
                         tmem_ld32(tacc + c, v);
+                        if (g.router_seg) {
+                            // logits = (hi + mid) + lo, each part's partial sum from its own columns
+                            uint32_t vm[32], vl[32];
+                            tmem_ld32(tacc + g.router_seg + c, vm);
+                            tmem_ld32(tacc + 2 * g.router_seg + c, vl);
+                            tmem_wait_ld();
+                            tmem_reg_fence(v);
+                            tmem_reg_fence(vm);
+                            tmem_reg_fence(vl);
+#pragma unroll
+                            for (int j = 0; j < 32; ++j)
+                                v[j] = __float_as_uint((__uint_as_float(v[j]) + __uint_as_float(vm[j])) +
+                                                       __uint_as_float(vl[j]));
+                        }
                         tmem_wait_ld();
                         tmem_reg_fence(v);
                         if (valid) {

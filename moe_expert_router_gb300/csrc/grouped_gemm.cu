@@ -84,11 +84,12 @@ cudaError_t launch_router_gemm(const RouterGemmLaunch &p, cudaStream_t st) {
     g.E = p.E;
     g.K = p.H;
     g.n_out = p.E;
-    g.n_mma = router_n_mma(p.E);
+    g.router_seg = router_seg(p.E);
+    g.n_mma = g.router_seg ? 3 * g.router_seg : router_n_mma(p.E);
     g.n_tiles = (p.E + BN - 1) / BN;
     g.T = p.T;
     g.kb_h = (p.H + BK - 1) / BK;
-    g.kb_total = 3 * g.kb_h;
+    g.kb_total = static_cast<int>(router_kb_total(p.H, p.E));
     g.splits = p.splits;
     g.kb_per_split = (g.kb_total + p.splits - 1) / p.splits;
     g.total_units = ((p.T + UM - 1) / UM) * g.n_tiles * p.splits;

@@ -44,11 +44,23 @@ inline size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255);
 // Split-K factor of the router GEMM (logits = x . w_r^T as three bf16 GEMMs):
 // enough units to cover two waves of 152 SMs, at most 32 splits and at least
 // one 64-deep k-block per split. Depends on the shape only.
+// Router GEMM layout. With E <= 64 one MMA of N = 3 * router_seg(E) multiplies
+// an x tile by the hi, mid and lo parts of w_r at once (each part's rows padded
+// to router_seg(E) accumulator columns), so x is loaded once per k-block;
+// otherwise the three parts are separate k-blocks of the reduction.
+inline int router_seg(int64_t E) { return E <= 32 ? 32 : (E <= 64 ? 64 : 0); }
+inline int64_t router_kb_total(int64_t H, int64_t E) {
+    const int64_t kb_h = (H + kBK - 1) / kBK;
+    return router_seg(E) ? kb_h : 3 * kb_h;
+}
+
 inline int router_splits(int64_t T, int64_t H, int64_t E) {
     const int64_t mt = (T + kUnitM - 1) / kUnitM;
     const int64_t nt = (E + kBN - 1) / kBN;
-    const int64_t kb_total = 3 * ((H + kBK - 1) / kBK);
-    int64_t s = (304 + mt * nt - 1) / (mt * nt);
+    const int64_t kb_total = router_kb_total(H, E);
+    // about two units per SM, or one with the parts fused (fewer partial logits to sum)
+    const int64_t target = router_seg(E) ? 152 : 304;
+    int64_t s = (target + mt * nt - 1) / (mt * nt);
     if (s > 32) s = 32;
     if (s > kb_total) s = kb_total;
     if (s < 1) s = 1;

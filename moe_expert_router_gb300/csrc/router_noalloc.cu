@@ -116,7 +116,7 @@ extern "C" moe_status_t moe_router_noalloc(const void *x, const float *w_r,
     int splits = router_splits(s.T, s.H, s.E);
     const int64_t cap = kMaxPartials / (s.T * s.E);
     if (splits > cap) {
-        const int64_t kb_total = 3 * ((s.H + kBK - 1) / kBK);
+        const int64_t kb_total = router_kb_total(s.H, s.E);
         const int64_t per = (kb_total + cap - 1) / cap;
         splits = static_cast<int>((kb_total + per - 1) / per);
     }
