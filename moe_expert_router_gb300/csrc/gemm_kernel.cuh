@@ -343,6 +343,23 @@ __device__ __forceinline__ void scaled_piece2(uint32_t tacc, int c, float w, uin
     }
 }
 
+// dA: the saved h of one row's columns [col, col+32): gate words into hg, the
+// matching up words (half columns further on) into hu; zeros past n_out or for
+// a row past the unit's count.
+__device__ __forceinline__ void load_h_piece(const __nv_bfloat16 *hrow, int half, int col, int n_out, bool valid,
+                                             uint32_t (&hg)[16], uint32_t (&hu)[16]) {
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        uint4 gq = make_uint4(0u, 0u, 0u, 0u), uq = gq;
+        if (valid && col + 8 * j < n_out) {
+            gq = __ldg(reinterpret_cast<const uint4 *>(hrow + col + 8 * j));
+            uq = __ldg(reinterpret_cast<const uint4 *>(hrow + half + col + 8 * j));
+        }
+        hg[4 * j] = gq.x; hg[4 * j + 1] = gq.y; hg[4 * j + 2] = gq.z; hg[4 * j + 3] = gq.w;
+        hu[4 * j] = uq.x; hu[4 * j + 1] = uq.y; hu[4 * j + 2] = uq.z; hu[4 * j + 3] = uq.w;
+    }
+}
+
 // 32 accumulator columns [c, c+32) scaled by w, packed to bf16.
 __device__ __forceinline__ void scaled_piece(uint32_t tacc, int c, float w, uint32_t (&pk)[16]) {
     uint32_t v[32];
@@ -732,6 +749,15 @@ tc_gemm_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs g) {
             if constexpr (MODE == kStage2 || MODE == kBwdDA || MODE == kStage2Mx) {
                 w = valid ? g.topk_w[g.perm_slot[t.row0 + row]] : 0.0f;
             }
+            // dA: the saved h (gate and up) of the row's first 32 columns, loaded while
+            // the unit's MMAs still run; each later piece's h is loaded before the
+            // previous piece's stores, so the epilogue rarely waits for global memory
+            uint32_t hg[16], hu[16];
+            const __nv_bfloat16 *hrow = nullptr;
+            if constexpr (MODE == kBwdDA) {
+                hrow = g.h + (valid ? static_cast<int64_t>(t.row0 + row) : 0) * (2 * static_cast<int64_t>(g.half));
+                load_h_piece(hrow, g.half, t.n * BN, g.n_out, valid, hg, hu);
+            }
             if (lane == 0) ok = mbar_wait(smem_addr(&sm.acc_full), acc_phase, abort_flag, g.err);
             ok = __shfl_sync(0xffffffffu, ok, 0);
             if (!ok) break;
@@ -914,7 +940,6 @@ tc_gemm_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs g) {
                     const int col0 = t.n * BN;
                     const int y = t.row0 + slab0;
                     const int64_t r = t.row0 + row;
-                    const __nv_bfloat16 *hrow = g.h + (valid ? r : 0) * (2 * static_cast<int64_t>(g.half));
                     float dtw = 0.0f;
 #pragma unroll 1
                     for (int c = 0; c < BN; c += 32) {
@@ -922,17 +947,6 @@ tc_gemm_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs g) {
                         if (col >= g.n_out) break;
                         uint32_t v[32];
                         tmem_ld32(tacc + c, v);
-                        uint32_t gw[16], uw[16];
-#pragma unroll
-                        for (int j = 0; j < 4; ++j) {
-                            uint4 gq = make_uint4(0u, 0u, 0u, 0u), uq = gq;
-                            if (valid && col + 8 * j < g.n_out) {
-                                gq = __ldg(reinterpret_cast<const uint4 *>(hrow + col + 8 * j));
-                                uq = __ldg(reinterpret_cast<const uint4 *>(hrow + g.half + col + 8 * j));
-                            }
-                            gw[4 * j] = gq.x; gw[4 * j + 1] = gq.y; gw[4 * j + 2] = gq.z; gw[4 * j + 3] = gq.w;
-                            uw[4 * j] = uq.x; uw[4 * j + 1] = uq.y; uw[4 * j + 2] = uq.z; uw[4 * j + 3] = uq.w;
-                        }
                         tmem_wait_ld();
                         tmem_reg_fence(v);
                         uint32_t pdg[16], pdu[16], paw[16];
@@ -941,8 +955,8 @@ tc_gemm_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs g) {
                             float og[2], ou[2], oa[2];
 #pragma unroll
                             for (int e2 = 0; e2 < 2; ++e2) {
-                                const float gv = e2 ? bf16_hi(gw[i]) : bf16_lo(gw[i]);
-                                const float uv = e2 ? bf16_hi(uw[i]) : bf16_lo(uw[i]);
+                                const float gv = e2 ? bf16_hi(hg[i]) : bf16_lo(hg[i]);
+                                const float uv = e2 ? bf16_hi(hu[i]) : bf16_lo(hu[i]);
                                 const float d = __uint_as_float(v[2 * i + e2]);
                                 const float sg = __fdividef(1.0f, 1.0f + __expf(-gv));
                                 const float silu = gv * sg;
@@ -957,6 +971,8 @@ tc_gemm_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs g) {
                             pdu[i] = pack_bf16x2(ou[0], ou[1]);
                             paw[i] = pack_bf16x2(oa[0], oa[1]);
                         }
+                        if (c + 32 < BN && col + 32 < g.n_out)          // the next piece's h
+                            load_h_piece(hrow, g.half, col + 32, g.n_out, valid, hg, hu);
                         if (full_slab) {
                             if (lane == 0) bulk_wait_read<0>();
                             __syncwarp();

@@ -121,8 +121,10 @@ SHAPES = [
     (37, 200, 136, 6, 3),      # K and N tails (H % 64 != 0, I % 128 != 0)
     (300, 328, 200, 5, 3),     # several row tiles per expert plus a ragged tail
     (1000, 512, 256, 16, 4),   # many units per CTA
-    (550, 1000, 328, 4, 2),    # 257-320 rows per expert: merged three-part units, partial n-tiles
-    (700, 520, 200, 4, 3),     # a full row tile before a merged unit, and experts without one
+    (550, 1000, 328, 4, 2),    # 257-320 rows per expert: a short last row tile, partial n-tiles
+    (700, 520, 200, 4, 3),     # a full row tile before a short one, and experts without one
+    (64, 64, 64, 1024, 32),    # the largest E and k: 2048 slots over 1024 experts
+    (300, 256, 192, 1, 1),     # one expert, k = 1: a dense SwiGLU MLP over two row tiles
     (64, 256, 128, 128, 8),    # more experts than rows: many empty experts
     (33, 8, 8, 3, 2),          # smallest dimensions
 ]
