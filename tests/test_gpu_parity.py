@@ -84,6 +84,21 @@ def test_metadata_large_zipf_like():
     _check_metadata(ws, shp, idx)
 
 
+@pytest.mark.parametrize("T,k,E", [
+    (8192, 8, 1024),    # 65,536 slots at the largest E
+    (8193, 8, 256),     # a partial last chunk of slots
+    (65536, 1, 3),      # few experts, 21,845 or more rows each
+])
+def test_metadata_many_slots(T, k, E):
+    g = torch.Generator().manual_seed(T + E)
+    idx = torch.randint(0, E, (T, k), generator=g, dtype=torch.int32).to(DEV)
+    shp = B.shape(T, 64, 64, E, k)
+    ws = B.new_workspace(shp)
+    B.moe_routing_metadata(idx, shp, ws)
+    _check_metadata(ws, shp, idx)
+    assert B.moe_get_device_error(ws) == 0
+
+
 def test_metadata_bad_index_flags_and_drops():
     T, k, E = 100, 3, 7
     g = torch.Generator().manual_seed(2)
