@@ -621,8 +621,12 @@ def main():
             roof = {"bound": "hbm", "achieved": b / (dom_ms / 1e3) / 1e9, "peak": peaks["hbm_gbs"],
                     "unit": "GB/s"}
         roof["frac"] = roof["achieved"] / roof["peak"]
+        # the capture is of the bf16 stage-1 kernel on row-major weights under the router's routing
         rec = STAGE1_TRAFFIC.get(cfg.name)
-        roof["traffic"] = rec["bytes"] if (dom == "gemm1" and rec and rec["src"] == kernel_source_hash()) else None
+        same_path = (args.precision == "bf16" and args.routing == "router" and
+                     getattr(args, "weights", "rowmajor") == "rowmajor")
+        roof["traffic"] = (rec["bytes"] if (dom == "gemm1" and same_path and rec and rec["src"] == kernel_source_hash())
+                           else None)
         roof["algorithmic_bytes"] = b
         roof["kernel"] = bf["stages"][dom]["kernel"]
         roof["stage"] = dom
