@@ -41,10 +41,7 @@ constexpr int kMetaChunk = 1024;
 
 inline size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
-// Split-K factor of the router GEMM (logits = x . w_r^T as three bf16 GEMMs):
-// enough units to cover two waves of 152 SMs, at most 32 splits and at least
-// one 64-deep k-block per split. Depends on the shape only.
-// Router GEMM layout. With E <= 64 one MMA of N = 3 * router_seg(E) multiplies
+// Router GEMM layout (logits = x . w_r^T with w_r split into three bf16 parts). With E <= 64 one MMA of N = 3 * router_seg(E) multiplies
 // an x tile by the hi, mid and lo parts of w_r at once (each part's rows padded
 // to router_seg(E) accumulator columns), so x is loaded once per k-block;
 // otherwise the three parts are separate k-blocks of the reduction.
@@ -55,18 +52,26 @@ inline int64_t router_kb_total(int64_t H, int64_t E) {
 }
 
 inline int router_splits(int64_t T, int64_t H, int64_t E) {
-    const int64_t mt = (T + kUnitM - 1) / kUnitM;
-    const int64_t nt = (E + kBN - 1) / kBN;
+    // Split-K count of the router GEMM: the one that minimises an estimated time,
+    // whole waves of units over the 152 SMs times the k-blocks of a unit (~0.6 us
+    // each), plus writing and re-reading one more [T, E] fp32 partial (~6 TB/s)
+    // per split. Every split owns at least one k-block.
+    const int64_t tiles = ((T + kUnitM - 1) / kUnitM) * ((E + kBN - 1) / kBN);
     const int64_t kb_total = router_kb_total(H, E);
-    // about two units per SM, or one with the parts fused (fewer partial logits to sum)
-    const int64_t target = router_seg(E) ? 152 : 304;
-    int64_t s = (target + mt * nt - 1) / (mt * nt);
-    if (s > 32) s = 32;
-    if (s > kb_total) s = kb_total;
-    if (s < 1) s = 1;
-    // no empty split: recompute from the per-split depth
-    const int64_t per = (kb_total + s - 1) / s;
-    return static_cast<int>((kb_total + per - 1) / per);
+    const int64_t smax = kb_total < 32 ? kb_total : 32;
+    int best = 1;
+    double best_cost = 0.0;
+    for (int64_t s = 1; s <= smax; ++s) {
+        const int64_t per = (kb_total + s - 1) / s;
+        const int64_t splits = (kb_total + per - 1) / per;
+        const int64_t waves = (tiles * splits + 151) / 152;
+        const double cost = 0.6 * static_cast<double>(waves * per) + 8.0 * static_cast<double>(splits * T * E) / 6.0e6;
+        if (s == 1 || cost < best_cost) {
+            best_cost = cost;
+            best = static_cast<int>(splits);
+        }
+    }
+    return best;
 }
 
 // N of the router GEMM's MMAs and rows of its weight tile: E rounded up to a
