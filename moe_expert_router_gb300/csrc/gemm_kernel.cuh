@@ -919,7 +919,12 @@ tc_gemm_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs g) {
                             fence_proxy_async_smem();
                             __syncwarp();
                             if (lane == 0) {
-                                tma_store_2d(&maps.out, buf, col0 + 64 * b, y);
+                                // stage 2's weighted rows are read again by the combine right
+                                // after this kernel: keep them in L2 ahead of the weight stream
+                                if constexpr (MODE == kStage2)
+                                    tma_store_2d_hint(&maps.out, buf, col0 + 64 * b, y, l2_policy_evict_last());
+                                else
+                                    tma_store_2d(&maps.out, buf, col0 + 64 * b, y);
                                 bulk_commit();
                             }
                         }
