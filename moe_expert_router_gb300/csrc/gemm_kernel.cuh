@@ -279,12 +279,19 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
     }
 }
 
-// silu(g) * u with the fast exponential and division intrinsics (a few
-// instructions instead of an IEEE division); their error (a few ulp of fp32)
-// is far below the bf16 rounding of the result. For g < -88 the quotient
-// flushes to 0, which is the bf16 value of silu there anyway.
+// silu(g) * u for the SwiGLU epilogues of stage 1, through the identity
+// silu(g) = g sigmoid(g) = h (1 + tanh(h)) with h = g / 2: one hardware tanh
+// approximation (tanh.approx.f32) and two FMA-pipe operations per element,
+// where 1 / (1 + exp(-g)) costs two special-function operations and more
+// instructions -- the epilogue holds the accumulator while this runs (mid
+// stage 1: 0.248 -> 0.243 ms). The approximation's error is a few times 1e-4
+// of |h|, below the bf16 rounding of a; the GPU tests bound a's relative error
+// against the fp64 oracle at 5e-3 (the general output bound is 1e-2).
 __device__ __forceinline__ float silu_mul(float g, float u) {
-    return __fdividef(g, 1.0f + __expf(-g)) * u;
+    const float h = 0.5f * g;
+    float t;
+    asm("tanh.approx.f32 %0, %1;" : "=f"(t) : "f"(h));
+    return fmaf(h, t, h) * u;
 }
 
 __device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }

@@ -145,6 +145,9 @@ SHAPES = [
 ]
 
 
+A_REL_FRO = 5e-3
+
+
 @pytest.mark.parametrize("shape", SHAPES, ids=lambda s: "x".join(map(str, s)))
 def test_stage1_a_rows(shape):
     T, H, I, E, k = shape
@@ -156,7 +159,10 @@ def test_stage1_a_rows(shape):
     _, a_ref, _ = oracle.expert_forward(inp["x"].cpu(), idx.cpu(), w.cpu().double(),
                                         inp["w1"].cpu(), inp["w2"].cpu(), want_a=True)
     n = int(ref_md.offsets[-1])
-    assert_close_y(a[:n], a_ref[ref_md.perm_slot], what="a (routed order)")
+    rel, _ = assert_close_y(a[:n], a_ref[ref_md.perm_slot], what="a (routed order)")
+    # a is one bf16 rounding (relative Frobenius ~1e-3) plus the SiLU's tanh
+    # approximation away from the fp64 value: a tighter bound than the outputs'
+    assert rel <= A_REL_FRO, f"a: relative Frobenius error {rel:.3e} > {A_REL_FRO}"
     assert B.moe_get_device_error(ws) == 0
 
 
