@@ -287,6 +287,13 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
 // stage 1: 0.248 -> 0.243 ms). The approximation's error is a few times 1e-4
 // of |h|, below the bf16 rounding of a; the GPU tests bound a's relative error
 // against the fp64 oracle at 5e-3 (the general output bound is 1e-2).
+__device__ __forceinline__ float sigmoid_tanh(float g) {
+    // sigmoid(g) = (1 + tanh(g / 2)) / 2, for the SwiGLU backward of dA
+    float t;
+    asm("tanh.approx.f32 %0, %1;" : "=f"(t) : "f"(0.5f * g));
+    return fmaf(0.5f, t, 0.5f);
+}
+
 __device__ __forceinline__ float silu_mul(float g, float u) {
     const float h = 0.5f * g;
     float t;
@@ -970,7 +977,7 @@ tc_gemm_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs g) {
                                 const float gv = e2 ? bf16_hi(hg[i]) : bf16_lo(hg[i]);
                                 const float uv = e2 ? bf16_hi(hu[i]) : bf16_lo(hu[i]);
                                 const float d = __uint_as_float(v[2 * i + e2]);
-                                const float sg = __fdividef(1.0f, 1.0f + __expf(-gv));
+                                const float sg = sigmoid_tanh(gv);
                                 const float silu = gv * sg;
                                 const float a = silu * uv;
                                 dtw = fmaf(d, a, dtw);
