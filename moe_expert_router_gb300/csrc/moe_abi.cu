@@ -200,7 +200,7 @@ moe_status_t run_gemm1(const moe_shape_t &s, const void *x, const void *w1, void
         !encode_bf16_2d(&tm_w1, w1, s.H, static_cast<uint64_t>(s.E) * 2 * s.I, kBK, 128) ||
         !encode_bf16_2d(&tm_out, a, s.I, R, box, 32))
         return MOE_ERR_CUDA;
-    if (launch_gather_rows(static_cast<const __nv_bfloat16 *>(x), w.row_of, s.T, s.k, s.H, xp, nullptr, nullptr,
+    if (launch_dispatch_rows(static_cast<const __nv_bfloat16 *>(x), w.row_of, s.T, s.k, s.H, xp, nullptr, nullptr,
                            st) != cudaSuccess)
         return MOE_ERR_CUDA;
     if (h && (!encode_bf16_2d_strided(&tm_hg, h, s.I, R, 2 * s.I, 32, 32) ||
@@ -349,7 +349,7 @@ moe_status_t run_bwd_stage2_data(const moe_shape_t &s, const void *dy, const flo
         !encode_bf16_2d_strided(&tm_du, w.dh + s.I, s.I, R, 2 * s.I, 32, 32) ||
         !encode_bf16_2d(&tm_aw, w.aw, s.I, R, 32, 32))
         return MOE_ERR_CUDA;
-    moe_status_t r = cuda_status(launch_gather_rows(static_cast<const __nv_bfloat16 *>(dy), w.row_of, s.T, s.k,
+    moe_status_t r = cuda_status(launch_dispatch_rows(static_cast<const __nv_bfloat16 *>(dy), w.row_of, s.T, s.k,
                                                     s.H, w.dyp, nullptr, nullptr, st));
     if (r != MOE_OK) return r;
     r = cuda_status(launch_zero_tail_rows(w.dh, w.aw, w.offsets + s.E, static_cast<int>(R), static_cast<int>(s.I),
@@ -1057,7 +1057,7 @@ moe_status_t moe_dispatch_rows(const void *x, const float *topk_w, const moe_sha
     DeviceState *d = nullptr;
     if ((r = device_state(&d)) != MOE_OK) return r;
     const Ws w = carve(ws, *shape);
-    return cuda_status(launch_gather_rows(static_cast<const __nv_bfloat16 *>(x), w.row_of, shape->T, shape->k,
+    return cuda_status(launch_dispatch_rows(static_cast<const __nv_bfloat16 *>(x), w.row_of, shape->T, shape->k,
                                           shape->H, static_cast<__nv_bfloat16 *>(rows), topk_w, row_weight,
                                           static_cast<cudaStream_t>(stream)));
 }
