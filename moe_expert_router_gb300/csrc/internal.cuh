@@ -207,7 +207,7 @@ cudaError_t launch_combine(const CombineLaunch &p, cudaStream_t st);
 // The dispatch copy: rows[row_of[s], :] = x[s / k, :] for every slot s with
 // row_of[s] >= 0, and with row_w row_w[row_of[s]] = topk_w[s] (rows.cu).
 cudaError_t launch_dispatch_rows(const __nv_bfloat16 *x, const int32_t *row_of, int64_t T, int k, int64_t H,
-                               __nv_bfloat16 *rows, const float *topk_w, float *row_w, cudaStream_t st);
+                                 __nv_bfloat16 *rows, const float *topk_w, float *row_w, cudaStream_t st);
 
 // Routing-weight gradient: dtopk_w[s] = sum_n dtw_part[n, row_of[s]] (0 if dropped).
 struct DtwReduceLaunch {

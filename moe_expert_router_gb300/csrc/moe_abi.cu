@@ -201,7 +201,7 @@ moe_status_t run_gemm1(const moe_shape_t &s, const void *x, const void *w1, void
         !encode_bf16_2d(&tm_out, a, s.I, R, box, 32))
         return MOE_ERR_CUDA;
     if (launch_dispatch_rows(static_cast<const __nv_bfloat16 *>(x), w.row_of, s.T, s.k, s.H, xp, nullptr, nullptr,
-                           st) != cudaSuccess)
+                             st) != cudaSuccess)
         return MOE_ERR_CUDA;
     if (h && (!encode_bf16_2d_strided(&tm_hg, h, s.I, R, 2 * s.I, 32, 32) ||
               !encode_bf16_2d_strided(&tm_hu, static_cast<__nv_bfloat16 *>(h) + s.I, s.I, R, 2 * s.I, 32, 32)))
@@ -350,7 +350,7 @@ moe_status_t run_bwd_stage2_data(const moe_shape_t &s, const void *dy, const flo
         !encode_bf16_2d(&tm_aw, w.aw, s.I, R, 32, 32))
         return MOE_ERR_CUDA;
     moe_status_t r = cuda_status(launch_dispatch_rows(static_cast<const __nv_bfloat16 *>(dy), w.row_of, s.T, s.k,
-                                                    s.H, w.dyp, nullptr, nullptr, st));
+                                                      s.H, w.dyp, nullptr, nullptr, st));
     if (r != MOE_OK) return r;
     r = cuda_status(launch_zero_tail_rows(w.dh, w.aw, w.offsets + s.E, static_cast<int>(R), static_cast<int>(s.I),
                                           st));
@@ -1058,8 +1058,8 @@ moe_status_t moe_dispatch_rows(const void *x, const float *topk_w, const moe_sha
     if ((r = device_state(&d)) != MOE_OK) return r;
     const Ws w = carve(ws, *shape);
     return cuda_status(launch_dispatch_rows(static_cast<const __nv_bfloat16 *>(x), w.row_of, shape->T, shape->k,
-                                          shape->H, static_cast<__nv_bfloat16 *>(rows), topk_w, row_weight,
-                                          static_cast<cudaStream_t>(stream)));
+                                            shape->H, static_cast<__nv_bfloat16 *>(rows), topk_w, row_weight,
+                                            static_cast<cudaStream_t>(stream)));
 }
 
 moe_status_t moe_combine_rows(const void *rows, const moe_shape_t *shape, void *y, void *ws, size_t ws_bytes,

@@ -50,7 +50,7 @@ dispatch_rows_kernel(const __nv_bfloat16 *__restrict__ x, const int32_t *__restr
 }  // namespace
 
 cudaError_t launch_dispatch_rows(const __nv_bfloat16 *x, const int32_t *row_of, int64_t T, int k, int64_t H,
-                               __nv_bfloat16 *rows, const float *topk_w, float *row_w, cudaStream_t st) {
+                                 __nv_bfloat16 *rows, const float *topk_w, float *row_w, cudaStream_t st) {
     if (T == 0 || H == 0) return cudaSuccess;
     int64_t grid = (T + 7) / 8;                     // eight tokens (warps) per block
     if (grid > 152 * 8) grid = 152 * 8;
