@@ -110,26 +110,6 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_
                  : "memory");
 }
 
-// Prefetch the box at (x, y) into L2 (no shared memory, no completion signal).
-__device__ __forceinline__ void tma_prefetch_l2_2d(const CUtensorMap *map, int32_t x, int32_t y) {
-    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];"
-                 ::"l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y)
-                 : "memory");
-}
-
-// Row gather: four rows r0..r3, columns [x, x + box width), written to smem as
-// a 4-row box. The tensor map's box must be one row high.
-__device__ __forceinline__ void tma_gather4(uint32_t dst, const CUtensorMap *map, int32_t x,
-                                            int32_t r0, int32_t r1, int32_t r2, int32_t r3,
-                                            uint32_t bar) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cta.global.tile::gather4.mbarrier::complete_tx::bytes"
-        " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];"
-        ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(r0), "r"(r1), "r"(r2),
-          "r"(r3), "r"(bar)
-        : "memory");
-}
-
 // 2-D tiled store of the shared-memory box at `src` to (x, y) of the tensor;
 // completion is tracked by bulk groups of the issuing thread.
 __device__ __forceinline__ void tma_store_2d(const CUtensorMap *map, uint32_t src, int32_t x, int32_t y) {
@@ -178,23 +158,6 @@ __device__ __forceinline__ void bulk_wait() {
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
     asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d)
                  : "memory");
-}
-
-// ---------------------------------------------------------------- cp.async (row gather)
-
-// 16-byte asynchronous global -> shared copy; bytes past src_bytes (0 or 16)
-// are filled with zeros.
-__device__ __forceinline__ void cp_async_16(uint32_t dst, const void *src, uint32_t src_bytes) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes)
-                 : "memory");
-}
-
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-
-// Wait until at most N of this thread's committed cp.async groups are pending.
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
 // Order this thread's generic-proxy shared-memory writes before later
