@@ -287,6 +287,9 @@ ROUTER_CASES = {
     "zipf_offset_e128": _cfg(2048, 256, 64, 128, 8, zipf_s=1.2),
     "e1024_k32": _cfg(64, 128, 64, 1024, 32),
     "e3_k3": _cfg(50, 64, 64, 3, 3),
+    # E between 32 and 64 (each weight part padded to 64 accumulator columns), a K tail
+    # (H = 200) and a partial 256-token tile
+    "e40_k4_ktail": _cfg(300, 200, 64, 40, 4),
 }
 
 
