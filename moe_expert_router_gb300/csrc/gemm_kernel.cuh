@@ -1021,36 +1021,31 @@ tc_gemm_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs g) {
                     }
                     if (valid) g.dtw_part[static_cast<int64_t>(t.n) * g.R + r] = dtw;
                 } else if constexpr (kWeightGrad<MODE>) {
-                    // dW rows t.row0 + row of expert e, 32 x 64 boxes through a 3-D map
-                    // (rows past m_total and columns past n_out are clipped by the store)
+                    // dW rows t.row0 + row of expert e, 32 x 32 boxes through a 3-D map
+                    // (rows past m_total and columns past n_out are clipped by the store),
+                    // staged in the two halves of the warp's buffer in turn, so staging a
+                    // box waits only for the one two boxes back to be read out
                     const int col0 = t.n * BN;
                     const bool empty = t.kb1 == 0;      // expert without rows: zeros
                     if (slab0 < t.rows) {
 #pragma unroll 1
-                        for (int cc = 0; cc < BN; cc += 64) {
-                            if (col0 + cc >= g.n_out) break;
-                            if (lane == 0) bulk_wait_read<0>();
-                            __syncwarp();
+                        for (int c = 0; c < BN; c += 32) {
+                            if (col0 + c >= g.n_out) break;
+                            uint32_t pk[16];
+                            if (empty) {
 #pragma unroll
-                            for (int p = 0; p < 2; ++p) {
-                                uint32_t pk[16];
-                                if (empty) {
-#pragma unroll
-                                    for (int i = 0; i < 16; ++i) pk[i] = 0u;
-                                } else {
-                                    scaled_piece(tacc, cc + 32 * p, 1.0f, pk);
-                                }
-#pragma unroll
-                                for (int j = 0; j < 4; ++j) {
-                                    const int c16 = p * 4 + j;
-                                    st_shared_v4(buf + lane * 128 + ((c16 ^ (lane & 7)) << 4), pk[4 * j],
-                                                 pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
-                                }
+                                for (int i = 0; i < 16; ++i) pk[i] = 0u;
+                            } else {
+                                scaled_piece(tacc, c, 1.0f, pk);
                             }
+                            if (lane == 0) bulk_wait_read<1>();
+                            __syncwarp();
+                            const uint32_t b2 = buf + (boxes++ & 1u) * 2048;
+                            stage_row32(b2, lane, pk);
                             fence_proxy_async_smem();
                             __syncwarp();
                             if (lane == 0) {
-                                tma_store_3d(&maps.out, buf, col0 + cc, t.row0 + slab0, t.e);
+                                tma_store_3d(&maps.out, b2, col0 + c, t.row0 + slab0, t.e);
                                 bulk_commit();
                             }
                         }

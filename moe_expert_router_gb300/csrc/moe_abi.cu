@@ -394,7 +394,7 @@ moe_status_t run_bwd_stage2_weight(const moe_shape_t &s, void *dw2, const Ws &w,
     CUtensorMap tm_dy_mn, tm_aw_mn, tm_dw2;
     if (!encode_bf16_2d(&tm_dy_mn, w.dyp, s.H, R, 64, kBK) ||
         !encode_bf16_2d(&tm_aw_mn, w.aw, s.I, R, 64, kBK) ||
-        !encode_bf16_3d(&tm_dw2, dw2, s.I, s.H, s.E, 64, 32))
+        !encode_bf16_3d(&tm_dw2, dw2, s.I, s.H, s.E, 32, 32))
         return MOE_ERR_CUDA;
     GemmLaunch q = base_launch(s, w, d);
     q.tm_a = &tm_dy_mn;
@@ -480,7 +480,7 @@ moe_status_t run_bwd_stage1_weight(const moe_shape_t &s, void *dw1, const Ws &w,
     CUtensorMap tm_dh_mn, tm_x_mn, tm_dw1;
     if (!encode_bf16_2d(&tm_dh_mn, w.dh, 2 * s.I, R, 64, kBK) ||
         !encode_bf16_2d(&tm_x_mn, w.xp, s.H, R, 64, kBK) ||
-        !encode_bf16_3d(&tm_dw1, dw1, s.H, 2 * s.I, s.E, 64, 32))
+        !encode_bf16_3d(&tm_dw1, dw1, s.H, 2 * s.I, s.E, 32, 32))
         return MOE_ERR_CUDA;
     GemmLaunch q = base_launch(s, w, d);
     q.tm_a = &tm_dh_mn;
