@@ -256,3 +256,57 @@ def test_full_size_train_config_sampled():
                                    out["dtw"].cpu().double(), score=cfg.score, normalize=cfg.normalize,
                                    scale=cfg.scale)
     assert_close_y(out["dwr"], rfull.dw_r, "dW_r")
+
+
+def test_training_step_graph_capture_replays():
+    """The training step is sync-free too: router, forward and the five backward calls
+    captured in one CUDA graph and replayed give the eager results bit for bit (every
+    reduction in them has a fixed order)."""
+    cfg = _cfg(300, 256, 192, 8, 2)
+    inp = _inputs(cfg, seed=5)
+    T, H, I, E, k = cfg.T, cfg.H, cfg.I, cfg.E, cfg.k
+    shp = B.shape(T, H, I, E, k, training=True)
+    ws = B.new_workspace(shp, DEV)
+    rc = router_cfg_of(cfg)
+    o = {
+        "idx": torch.empty((T, k), dtype=torch.int32, device=DEV),
+        "w": torch.empty((T, k), dtype=torch.float32, device=DEV),
+        "logits": torch.empty((T, E), dtype=torch.float32, device=DEV),
+        "a": torch.empty((T * k, I), dtype=torch.bfloat16, device=DEV),
+        "h": torch.empty((T * k, 2 * I), dtype=torch.bfloat16, device=DEV),
+        "y": torch.empty((T, H), dtype=torch.bfloat16, device=DEV),
+        "dx": torch.empty((T, H), dtype=torch.bfloat16, device=DEV),
+        "dw1": torch.empty((E, 2 * I, H), dtype=torch.bfloat16, device=DEV),
+        "dw2": torch.empty((E, H, I), dtype=torch.bfloat16, device=DEV),
+        "dtw": torch.empty((T, k), dtype=torch.float32, device=DEV),
+        "dwr": torch.empty((E, H), dtype=torch.float32, device=DEV),
+    }
+
+    def step():
+        B.moe_router_train(inp["x"], inp["w_r"], shp, rc, o["idx"], o["w"], o["logits"], ws)
+        B.moe_routing_metadata(o["idx"], shp, ws)
+        B.moe_dispatch_gemm1_train(inp["x"], inp["w1"], shp, o["a"], o["h"], ws)
+        B.moe_swiglu_gemm2_combine(o["a"], o["w"], inp["w2"], shp, o["y"], ws)
+        B.moe_backward_stage2_data(inp["dy"], o["w"], inp["w2"], o["h"], shp, ws, dtopk_w=o["dtw"])
+        B.moe_backward_stage2_weight(inp["dy"], shp, o["dw2"], ws)
+        B.moe_router_backward(inp["x"], o["logits"], o["idx"], o["w"], o["dtw"], shp, rc, o["dwr"], ws)
+        B.moe_backward_stage1_data(inp["w1"], shp, o["dx"], ws, w_r=inp["w_r"], topk_idx=o["idx"], cfg=rc)
+        B.moe_backward_stage1_weight(inp["x"], shp, o["dw1"], ws)
+
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):   # eager run first (per-device set-up happens outside capture)
+        step()
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    eager = {name: t.clone() for name, t in o.items()}
+    for t in o.values():
+        t.zero_()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        step()
+    graph.replay()
+    torch.cuda.synchronize()
+    for name, t in o.items():
+        assert torch.equal(t.view(torch.uint8), eager[name].view(torch.uint8)), name
+    assert B.moe_get_device_error(ws) == 0
