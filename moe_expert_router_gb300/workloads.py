@@ -82,6 +82,11 @@ CONFIGS: dict[str, MoEConfig] = {
                                    group_topn=2, sel_bias=True,
                                    description="large_group per-expert geometry, 32 experts "
                                                "(profiling size)"),
+    # profiling size of zipf_prefill: its shapes and Zipf(1.2) expert popularity at a
+    # quarter of the tokens, so that a full ncu capture holds about 5 GB on the device
+    "zipf_prefill_slice": MoEConfig("zipf_prefill_slice", T=4096, H=4096, I=1536, E=128, k=8,
+                                    zipf_s=1.2,
+                                    description="zipf_prefill shapes at T=4096 (profiling size)"),
     # profiling size of the training step: the train geometry per expert (H, I, k,
     # about 768 routed rows per expert) with 16 experts, about 1 GB on the device
     "train_slice": MoEConfig("train_slice", T=2048, H=4096, I=1536, E=16, k=6, backward=True,
