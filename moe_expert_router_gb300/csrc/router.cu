@@ -55,6 +55,69 @@ router_split_kernel(const float *__restrict__ w_r, __nv_bfloat16 *__restrict__ w
     }
 }
 
+// Router logits for few tokens, on the CUDA cores: logits[t, e] = sum_h x[t, h] w_r[e, h]
+// in fp32 (x is bf16: each product is exact but for one fp32 rounding). With few
+// tokens the tensor-core path is all latency (a split kernel, a split-K GEMM whose
+// units hold a mostly empty 128-row tile, and its partials); here one warp takes one
+// expert and a group of kSmallTok tokens, each lane accumulates columns 8 lane +
+// 256 j of those tokens, and the warp sums its lanes in a fixed butterfly order.
+// Block 0 also clears the aux accumulators of this call, as the split kernel does on
+// the tensor-core path.
+constexpr int kSmallTok = 2;
+constexpr int kSmallMaxT = 256;
+
+__global__ void __launch_bounds__(256)
+router_logits_small_kernel(const __nv_bfloat16 *__restrict__ x, const float *__restrict__ w_r, int T, int H, int E,
+                           float *__restrict__ logits, float *__restrict__ score_sum, int32_t *__restrict__ counts,
+                           int32_t *__restrict__ ticket) {
+    griddep_wait();
+    if (blockIdx.x == 0) {
+        for (int e = threadIdx.x; e < E; e += blockDim.x) {
+            score_sum[e] = 0.0f;
+            counts[e] = 0;
+        }
+        if (threadIdx.x == 0) *ticket = 0;
+    }
+    const int lane = threadIdx.x & 31;
+    const int gw = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    const int tgroups = (T + kSmallTok - 1) / kSmallTok;
+    if (gw >= E * tgroups) return;                  // whole warp
+    const int e = gw / tgroups;
+    const int t0 = (gw - e * tgroups) * kSmallTok;
+    const float *wrow = w_r + static_cast<int64_t>(e) * H;
+    float acc[kSmallTok];
+#pragma unroll
+    for (int j = 0; j < kSmallTok; ++j) acc[j] = 0.0f;
+#pragma unroll 8
+    for (int h = lane * 8; h < H; h += 256) {
+        const float4 w0 = __ldg(reinterpret_cast<const float4 *>(wrow + h));
+        const float4 w1 = __ldg(reinterpret_cast<const float4 *>(wrow + h + 4));
+#pragma unroll
+        for (int j = 0; j < kSmallTok; ++j) {
+            if (t0 + j < T) {
+                const uint4 xv = __ldg(reinterpret_cast<const uint4 *>(x + static_cast<int64_t>(t0 + j) * H + h));
+                float a = acc[j];
+                a = fmaf(__uint_as_float(xv.x << 16), w0.x, a);
+                a = fmaf(__uint_as_float(xv.x & 0xffff0000u), w0.y, a);
+                a = fmaf(__uint_as_float(xv.y << 16), w0.z, a);
+                a = fmaf(__uint_as_float(xv.y & 0xffff0000u), w0.w, a);
+                a = fmaf(__uint_as_float(xv.z << 16), w1.x, a);
+                a = fmaf(__uint_as_float(xv.z & 0xffff0000u), w1.y, a);
+                a = fmaf(__uint_as_float(xv.w << 16), w1.z, a);
+                a = fmaf(__uint_as_float(xv.w & 0xffff0000u), w1.w, a);
+                acc[j] = a;
+            }
+        }
+    }
+#pragma unroll
+    for (int j = 0; j < kSmallTok; ++j) {
+        float v = acc[j];
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+        if (lane == 0 && t0 + j < T) logits[static_cast<int64_t>(t0 + j) * E + e] = v;
+    }
+}
+
 // Warp-wide arg-max in the order (value desc, index asc); every lane gets the winner.
 __device__ __forceinline__ void warp_argmax(float &v, int &i) {
 #pragma unroll
@@ -337,6 +400,16 @@ cudaError_t launch_selection(const RouterLaunch &p, const float *logits, int spl
 
 cudaError_t launch_router(const RouterLaunch &p, cudaStream_t st) {
     const RouterScratch &sc = p.scratch;
+    if (p.T <= kSmallMaxT) {
+        // few tokens: fp32 logits on the CUDA cores into the first partial, then the selection
+        const int64_t warps = static_cast<int64_t>(p.E) * ((p.T + kSmallTok - 1) / kSmallTok);
+        const cudaError_t e = launch_dep(router_logits_small_kernel, dim3(static_cast<int>((warps + 7) / 8)), dim3(256),
+                                         0, st, p.x, p.w_r, p.T, p.H, p.E, sc.logits_part, sc.score_sum, sc.counts,
+                                         sc.ticket);
+        note_launches(1);
+        if (e != cudaSuccess) return e;
+        return launch_selection(p, sc.logits_part, 1, st);
+    }
     const int64_t n = static_cast<int64_t>(p.E) * p.H;
     int64_t sblocks = (n + 255) / 256;
     if (sblocks > 152 * 8) sblocks = 152 * 8;
