@@ -28,6 +28,8 @@ CASES = [
     MoEConfig("noalloc_softmax", T=4096, H=1024, I=64, E=64, k=6),
     MoEConfig("noalloc_groups", T=2048, H=512, I=64, E=256, k=8, score="sigmoid", scale=2.5,
               n_group=8, topk_group=4, group_topn=2, sel_bias=True),
+    # decode-sized: the router's few-token path (logits on the CUDA cores)
+    MoEConfig("noalloc_decode", T=64, H=4096, I=64, E=128, k=8, zipf_s=1.2),
 ]
 
 
