@@ -44,19 +44,18 @@ __device__ __forceinline__ void load_lane_slots(const int32_t *__restrict__ topk
     }
 }
 
-__global__ void __launch_bounds__(kThreads)
-metadata_count_kernel(const int32_t *__restrict__ topk_idx, int R, int E, int n_chunks,
-                      int32_t *__restrict__ block_hist, int32_t *__restrict__ counts,
-                      int32_t *__restrict__ offsets, int32_t *__restrict__ mt_prefix,
-                      int32_t *__restrict__ ticket, int32_t *__restrict__ err) {
-    griddep_wait();
-    extern __shared__ int32_t hist[];    // [E]
+// The count kernel's work for chunk `chunk`, with hist = E ints of shared memory.
+__device__ __forceinline__ void metadata_count_body(const int32_t *__restrict__ topk_idx, int R, int E, int n_chunks,
+                                                    int chunk, int32_t *__restrict__ block_hist,
+                                                    int32_t *__restrict__ counts, int32_t *__restrict__ offsets,
+                                                    int32_t *__restrict__ mt_prefix, int32_t *__restrict__ ticket,
+                                                    int32_t *__restrict__ err, int32_t *hist) {
     __shared__ int is_last;
     __shared__ int32_t warp_tot_c[32], warp_tot_m[32];
     for (int e = threadIdx.x; e < E; e += kThreads) hist[e] = 0;
     __syncthreads();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int beg = blockIdx.x * kChunk + warp * kWarpSlots;
+    const int beg = chunk * kChunk + warp * kWarpSlots;
     const int end = min(R, beg + kWarpSlots);
     int bad = 0;
     int ev[kPerLane];
@@ -72,7 +71,7 @@ metadata_count_kernel(const int32_t *__restrict__ topk_idx, int R, int E, int n_
     }
     if (bad) atomicOr(err, MOE_DEVERR_BAD_EXPERT_INDEX);
     __syncthreads();
-    for (int e = threadIdx.x; e < E; e += kThreads) block_hist[static_cast<int64_t>(blockIdx.x) * E + e] = hist[e];
+    for (int e = threadIdx.x; e < E; e += kThreads) block_hist[static_cast<int64_t>(chunk) * E + e] = hist[e];
     __threadfence();
     __syncthreads();
     if (threadIdx.x == 0) is_last = (atomicAdd(ticket, 1) == static_cast<int>(gridDim.x) - 1);
@@ -149,20 +148,31 @@ metadata_count_kernel(const int32_t *__restrict__ topk_idx, int R, int E, int n_
 }
 
 __global__ void __launch_bounds__(kThreads)
-metadata_place_kernel(const int32_t *__restrict__ topk_idx, int R, int E,
-                      const int32_t *__restrict__ block_hist, const int32_t *__restrict__ offsets,
-                      int32_t *__restrict__ perm_slot, int32_t *__restrict__ row_of) {
+metadata_count_kernel(const int32_t *__restrict__ topk_idx, int R, int E, int n_chunks,
+                      int32_t *__restrict__ block_hist, int32_t *__restrict__ counts,
+                      int32_t *__restrict__ offsets, int32_t *__restrict__ mt_prefix,
+                      int32_t *__restrict__ ticket, int32_t *__restrict__ err) {
     griddep_wait();
-    extern __shared__ int32_t sh[];
+    extern __shared__ int32_t hist[];    // [E]
+    metadata_count_body(topk_idx, R, E, n_chunks, blockIdx.x, block_hist, counts, offsets, mt_prefix, ticket, err,
+                        hist);
+}
+
+// The place kernel's work for chunk `chunk`, with sh = (kWarps + 1) E ints of shared memory.
+__device__ __forceinline__ void metadata_place_body(const int32_t *__restrict__ topk_idx, int R, int E, int chunk,
+                                                    const int32_t *__restrict__ block_hist,
+                                                    const int32_t *__restrict__ offsets,
+                                                    int32_t *__restrict__ perm_slot, int32_t *__restrict__ row_of,
+                                                    int32_t *sh) {
     int32_t *base = sh;                  // [E]: first row of this chunk in each expert
     int32_t *whist = sh + E;             // [kWarps][E]: per-warp counts, then start ranks
     for (int e = threadIdx.x; e < E; e += kThreads) {
-        base[e] = offsets[e] + block_hist[static_cast<int64_t>(blockIdx.x) * E + e];
+        base[e] = offsets[e] + block_hist[static_cast<int64_t>(chunk) * E + e];
         for (int w = 0; w < kWarps; ++w) whist[w * E + e] = 0;
     }
     __syncthreads();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int beg = blockIdx.x * kChunk + warp * kWarpSlots;
+    const int beg = chunk * kChunk + warp * kWarpSlots;
     const int end = min(R, beg + kWarpSlots);
     int32_t *mine = whist + warp * E;
     int ev[kPerLane];
@@ -205,18 +215,54 @@ metadata_place_kernel(const int32_t *__restrict__ topk_idx, int R, int E,
     }
 }
 
+__global__ void __launch_bounds__(kThreads)
+metadata_place_kernel(const int32_t *__restrict__ topk_idx, int R, int E,
+                      const int32_t *__restrict__ block_hist, const int32_t *__restrict__ offsets,
+                      int32_t *__restrict__ perm_slot, int32_t *__restrict__ row_of) {
+    griddep_wait();
+    extern __shared__ int32_t sh[];
+    metadata_place_body(topk_idx, R, E, blockIdx.x, block_hist, offsets, perm_slot, row_of, sh);
+}
+
+// All slots in one chunk (at most kChunk, e.g. decode): one CTA runs the count and the
+// place work back to back, saving a launch. The CTA is its own last CTA, so the count
+// part also scans; its global writes are visible to the place part after the barrier.
+__global__ void __launch_bounds__(kThreads)
+metadata_single_chunk_kernel(const int32_t *__restrict__ topk_idx, int R, int E, int32_t *__restrict__ block_hist,
+                             int32_t *__restrict__ counts, int32_t *__restrict__ offsets,
+                             int32_t *__restrict__ mt_prefix, int32_t *__restrict__ ticket,
+                             int32_t *__restrict__ err, int32_t *__restrict__ perm_slot,
+                             int32_t *__restrict__ row_of) {
+    griddep_wait();
+    extern __shared__ int32_t sh[];
+    metadata_count_body(topk_idx, R, E, 1, 0, block_hist, counts, offsets, mt_prefix, ticket, err, sh);
+    __syncthreads();
+    metadata_place_body(topk_idx, R, E, 0, block_hist, offsets, perm_slot, row_of, sh);
+}
+
 size_t place_smem(int E) { return sizeof(int32_t) * static_cast<size_t>(kWarps + 1) * E; }
 
 }  // namespace
 
 cudaError_t setup_metadata_kernels() {
-    return cudaFuncSetAttribute(metadata_place_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                static_cast<int>(place_smem(1024)));
+    cudaError_t e = cudaFuncSetAttribute(metadata_place_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(place_smem(1024)));
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(metadata_single_chunk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(place_smem(1024)));
+    return e;
 }
 
 cudaError_t launch_routing_metadata(const MetadataLaunch &p, cudaStream_t st) {
     const int n_chunks = (p.R + kChunk - 1) / kChunk;
     if (n_chunks == 0) return cudaSuccess;
+    if (n_chunks == 1) {
+        const cudaError_t e = launch_dep(metadata_single_chunk_kernel, dim3(1), dim3(kThreads), place_smem(p.E), st,
+                                         p.topk_idx, p.R, p.E, p.block_hist, p.counts, p.offsets, p.mt_prefix,
+                                         p.ticket, p.err, p.perm_slot, p.row_of);
+        note_launches(1);
+        return e;
+    }
     cudaError_t e = launch_dep(metadata_count_kernel, dim3(n_chunks), dim3(kThreads), sizeof(int32_t) * p.E, st,
                                p.topk_idx, p.R, p.E, n_chunks, p.block_hist, p.counts, p.offsets, p.mt_prefix, p.ticket,
                                p.err);
