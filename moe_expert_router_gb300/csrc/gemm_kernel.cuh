@@ -943,15 +943,34 @@ tc_gemm_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs g) {
                             }
                         }
                     } else {
-                        // partial slab (the expert's last rows): masked direct stores
+                        // partial slab (the expert's last rows): masked direct stores. Stage 2
+                        // first reads the row's columns into packed registers, as its full-slab
+                        // path does, and releases the accumulator before storing (a unit's
+                        // release waits for its slowest warp); in stage 1 and dX the extra
+                        // registers spill and cost more than they save.
                         __nv_bfloat16 *dst = g.out + static_cast<int64_t>(t.row0 + row) * g.n_out + col0;
+                        if constexpr (MODE == kStage2) {
+                            constexpr int NPIECE = ncols / 32;
+                            uint32_t pk[NPIECE][16];
+#pragma unroll
+                            for (int p = 0; p < NPIECE; p += 2) scaled_piece2(tacc, 32 * p, w, pk[p], pk[p + 1]);
+                            tc_fence_before();
+                            mbar_arrive(smem_addr(&sm.acc_empty));
+                            released = true;
+                            if (valid) {
+#pragma unroll
+                                for (int p = 0; p < NPIECE; ++p)
+                                    if (col0 + 32 * p < g.n_out) store_row32(dst + 32 * p, g.n_out - col0 - 32 * p, pk[p]);
+                            }
+                        } else {
 #pragma unroll 1
-                        for (int c = 0; c < ncols; c += 32) {
-                            if (col0 + c >= g.n_out) break;
-                            uint32_t pk[16];
-                            if constexpr (MODE == kStage1) swiglu_piece(tacc, c, pk);
-                            else scaled_piece(tacc, c, w, pk);
-                            if (valid) store_row32(dst + c, g.n_out - col0 - c, pk);
+                            for (int c = 0; c < ncols; c += 32) {
+                                if (col0 + c >= g.n_out) break;
+                                uint32_t pk[16];
+                                if constexpr (MODE == kStage1) swiglu_piece(tacc, c, pk);
+                                else scaled_piece(tacc, c, w, pk);
+                                if (valid) store_row32(dst + c, g.n_out - col0 - c, pk);
+                            }
                         }
                     }
                 } else if constexpr (MODE == kBwdDA) {
