@@ -193,6 +193,18 @@ moe_status_t moe_router_noalloc(const void *x, const float *w_r, const float *lo
                                 float *aux, void *stream);
 
 /*
+ * The device error word of moe_router_noalloc (it has no workspace to hold
+ * one): wait for `stream`, then read and clear the word kept in the last bytes
+ * of the static array of the current device. Bits as for moe_get_device_error
+ * (MOE_DEVERR_WAIT_TIMEOUT: a pipeline wait of the router's GEMM ran out of
+ * time and that call's routing is invalid). Returns MOE_ERR_DEVICE_FLAGGED
+ * when it was non-zero, MOE_OK when it was zero. The word is shared by every
+ * moe_router_noalloc call on the device, so a flag stays until it is read here.
+ * Not for the hot path (it synchronises the stream).
+ */
+moe_status_t moe_router_noalloc_get_error(int32_t *code, void *stream);
+
+/*
  * Routing metadata: the local stand-in for the dispatch all-to-all (MegaMoE
  * guide, opening section, dispatch_grouped_gemm; section "Router force load
  * balancing": ragged per-expert counts absorbed without padding or host sync).

@@ -62,6 +62,7 @@ _SIG = {
                    _P, ctypes.c_size_t, _P],
     "moe_router_noalloc": [_P, _P, _P, _P, ctypes.POINTER(Shape), ctypes.POINTER(RouterCfg), _P,
                            _P, _P, _P],
+    "moe_router_noalloc_get_error": [ctypes.POINTER(ctypes.c_int32), _P],
     "moe_routing_metadata": [_P, ctypes.POINTER(Shape), _P, ctypes.c_size_t, _P],
     "moe_dispatch_gemm1": [_P, _P, ctypes.POINTER(Shape), _P, _P, ctypes.c_size_t, _P],
     "moe_swiglu_gemm2_combine": [_P, _P, _P, ctypes.POINTER(Shape), _P, _P, ctypes.c_size_t, _P],
@@ -184,6 +185,19 @@ def moe_router_noalloc(x, w_r, shp, cfg, topk_idx, topk_w, aux=None, logit_offse
     _check("moe_router_noalloc", load().moe_router_noalloc(
         _ptr(x), _ptr(w_r), _ptr(logit_offset), _ptr(sel_bias), ctypes.byref(shp),
         ctypes.byref(cfg), _ptr(topk_idx), _ptr(topk_w), _ptr(aux), _stream(stream, x)))
+
+
+def moe_router_noalloc_get_error(stream=None) -> int:
+    """Wait for the stream, return and clear moe_router_noalloc's error word on
+    the current device (0 = none)."""
+    import torch
+    code = ctypes.c_int32()
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    st = load().moe_router_noalloc_get_error(ctypes.byref(code), ctypes.c_void_p(stream.cuda_stream))
+    if st not in (MOE_OK, 5):
+        raise MoEError("moe_router_noalloc_get_error", st)
+    return int(code.value)
 
 
 def moe_routing_metadata(topk_idx, shp, ws, stream=None):

@@ -23,7 +23,9 @@ std::mutex g_mu;
 DeviceState g_dev[kMaxDevices];
 
 // Per-device set-up: check for an sm_103 GPU, cache the SM count, raise the
-// dynamic shared memory limits.
+// dynamic shared memory limits. A device is marked ready only once this
+// succeeded (an unsupported architecture is remembered); a failed CUDA call is
+// retried by the next entry point, and only the error it raised is cleared.
 moe_status_t device_state(DeviceState **out) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
@@ -31,21 +33,23 @@ moe_status_t device_state(DeviceState **out) {
     std::lock_guard<std::mutex> lock(g_mu);
     DeviceState &d = g_dev[dev];
     if (!d.ready) {
-        d.ready = true;
         int major = 0, minor = 0, sms = 0;
         if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
             cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
             cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
-            d.status = MOE_ERR_CUDA;
-        } else if (major != 10 || minor != 3) {
+            cudaGetLastError();
+            return MOE_ERR_CUDA;
+        }
+        if (major != 10 || minor != 3) {
             d.status = MOE_ERR_UNSUPPORTED;
+        } else if (setup_metadata_kernels() != cudaSuccess || setup_gemm_kernels() != cudaSuccess) {
+            cudaGetLastError();
+            return MOE_ERR_CUDA;
         } else {
             d.num_sms = sms;
-            if (setup_metadata_kernels() != cudaSuccess || setup_gemm_kernels() != cudaSuccess) {
-                d.status = MOE_ERR_CUDA;
-            }
+            d.status = MOE_OK;
         }
-        cudaGetLastError();  // do not leak a set-up error into the caller's error state
+        d.ready = true;
     }
     *out = &d;
     return d.status;
@@ -534,7 +538,8 @@ bool encode_ready() {
                                              &q) == cudaSuccess &&
             q == cudaDriverEntryPointSuccess)
             g_encode = reinterpret_cast<EncodeTiledFn>(fn);
-        cudaGetLastError();
+        else
+            cudaGetLastError();   // clear only the error the failed lookup raised
     });
     return g_encode != nullptr;
 }

@@ -40,36 +40,44 @@ int g_num_sms[kMaxDevices];
 
 // Once per device, with that device current: check the architecture and look
 // up the device address of the static array (a host-side use of its name is
-// only a stand-in, not a device pointer).
+// only a stand-in, not a device pointer). A device is marked ready only when
+// every step succeeded; an unsupported architecture is remembered, any other
+// failure is retried by the next call.
 moe_status_t scratch_for_current_device(unsigned char **out, int *num_sms) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
     if (dev < 0 || dev >= kMaxDevices) return MOE_ERR_UNSUPPORTED;
     std::lock_guard<std::mutex> lock(g_mu);
     if (!g_ready[dev]) {
-        g_ready[dev] = true;
         int major = 0, minor = 0, sms = 0;
         void *p = nullptr;
         if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
             cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
             cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
-            g_status[dev] = MOE_ERR_CUDA;
-        } else if (major != 10 || minor != 3) {
+            cudaGetLastError();   // clear only the error this set-up caused
+            return MOE_ERR_CUDA;
+        }
+        if (major != 10 || minor != 3) {
             g_status[dev] = MOE_ERR_UNSUPPORTED;
+            g_ready[dev] = true;
         } else if (cudaGetSymbolAddress(&p, g_router_scratch) != cudaSuccess || p == nullptr ||
                    setup_gemm_kernels() != cudaSuccess) {
-            g_status[dev] = MOE_ERR_CUDA;
+            cudaGetLastError();
+            return MOE_ERR_CUDA;
         } else {
             g_status[dev] = MOE_OK;
             g_scratch_ptr[dev] = static_cast<unsigned char *>(p);
             g_num_sms[dev] = sms;
+            g_ready[dev] = true;
         }
-        cudaGetLastError();
     }
     *out = g_scratch_ptr[dev];
     *num_sms = g_num_sms[dev];
     return g_status[dev];
 }
+
+// The error word sits at a fixed place in the array's last 256 bytes.
+int32_t *error_word(unsigned char *scratch) { return reinterpret_cast<int32_t *>(scratch + kScratchBytes - 256); }
 
 bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
@@ -149,10 +157,28 @@ extern "C" moe_status_t moe_router_noalloc(const void *x, const float *w_r,
     // depends on the shape: the counter must read zero at the start of every
     // launch, and a shape-dependent place could hold another call's logits.
     unsigned char *tail = scratch + kScratchBytes - 256;
-    p.err = reinterpret_cast<int32_t *>(tail);
+    p.err = error_word(scratch);
     p.num_sms = num_sms;
     p.scratch = carve_router_scratch(scratch, s.T, s.H, s.E, splits,
                                      reinterpret_cast<int32_t *>(tail + 64),
                                      reinterpret_cast<int32_t *>(tail + 128));
     return launch_router(p, static_cast<cudaStream_t>(stream)) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+extern "C" moe_status_t moe_router_noalloc_get_error(int32_t *code, void *stream) {
+    if (code == nullptr) return MOE_ERR_INVALID_ARG;
+    unsigned char *scratch = nullptr;
+    int num_sms = 0;
+    moe_status_t r = scratch_for_current_device(&scratch, &num_sms);
+    if (r != MOE_OK) return r;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    int32_t *word = error_word(scratch);
+    int32_t v = 0;
+    if (cudaMemcpyAsync(&v, word, sizeof(v), cudaMemcpyDeviceToHost, st) != cudaSuccess) return MOE_ERR_CUDA;
+    if (cudaStreamSynchronize(st) != cudaSuccess) return MOE_ERR_CUDA;
+    *code = v;
+    if (v == 0) return MOE_OK;
+    if (cudaMemsetAsync(word, 0, sizeof(int32_t), st) != cudaSuccess) return MOE_ERR_CUDA;
+    if (cudaStreamSynchronize(st) != cudaSuccess) return MOE_ERR_CUDA;
+    return MOE_ERR_DEVICE_FLAGGED;
 }

@@ -86,6 +86,30 @@ def test_noalloc_router_matches_workspace_router_twice_in_a_row():
     torch.cuda.synchronize()
     assert torch.equal(idx_n.cpu(), results[0][1])     # same call, same result
     np.testing.assert_allclose(aux_n.cpu().numpy(), results[0][3].numpy(), rtol=1e-6)
+    # no call above ran out of time in a pipeline wait: the static error word is clear
+    assert B.moe_router_noalloc_get_error() == 0
+
+
+def test_noalloc_router_at_the_weight_split_limit():
+    """E * H == 2**20 exactly: the bf16 x3 split of w_r fills its region of the array."""
+    c = MoEConfig("eh_limit", T=512, H=4096, I=64, E=256, k=8, score="sigmoid", scale=2.5,
+                  n_group=8, topk_group=4, group_topn=2, sel_bias=True)
+    inp = generate(c, seed=5, device="cuda")
+    shp = B.shape(c.T, c.H, c.I, c.E, c.k)
+    idx_n, w_n, aux_n = _outputs(c)
+    B.moe_router_noalloc(inp["x"], inp["w_r"], shp, _cfg(c), idx_n, w_n, aux=aux_n,
+                         sel_bias=inp["sel_bias"])
+    ws = B.new_workspace(shp)
+    idx_r, w_r, aux_r = _outputs(c)
+    B.moe_router(inp["x"], inp["w_r"], shp, _cfg(c), idx_r, w_r, ws, aux=aux_r, sel_bias=inp["sel_bias"])
+    torch.cuda.synchronize()
+    ref = oracle.router(inp["x"], inp["w_r"], c.k, score=c.score, normalize=c.normalize, scale=c.scale,
+                        n_group=c.n_group, topk_group=c.topk_group, group_topn=c.group_topn,
+                        sel_bias=inp["sel_bias"])
+    keep = torch.from_numpy((ref.sel_gap >= 1e-6) & (ref.group_gap >= 1e-6))
+    assert torch.equal(idx_n.cpu()[keep], idx_r.cpu()[keep])
+    np.testing.assert_allclose(w_n.cpu()[keep].numpy(), w_r.cpu()[keep].numpy(), rtol=1e-4, atol=1e-6)
+    assert B.moe_router_noalloc_get_error() == 0
 
 
 def test_noalloc_router_rejects_shapes_beyond_its_scratch():
@@ -97,3 +121,12 @@ def test_noalloc_router_rejects_shapes_beyond_its_scratch():
     with pytest.raises(B.MoEError) as e:
         B.moe_router_noalloc(x, w_r, shp, _cfg(c), idx, w, aux=aux)
     assert e.value.status == 2   # MOE_ERR_UNSUPPORTED
+    # E * H > 2**20: the bf16 x3 split of w_r would not fit its region
+    c = MoEConfig("too_wide", T=64, H=4104, I=64, E=256, k=8)
+    shp = B.shape(c.T, c.H, c.I, c.E, c.k)
+    x = torch.zeros((c.T, c.H), dtype=torch.bfloat16, device="cuda")
+    w_r = torch.zeros((c.E, c.H), dtype=torch.float32, device="cuda")
+    idx, w, aux = _outputs(c)
+    with pytest.raises(B.MoEError) as e:
+        B.moe_router_noalloc(x, w_r, shp, _cfg(c), idx, w, aux=aux)
+    assert e.value.status == 2
