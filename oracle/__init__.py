@@ -67,6 +67,8 @@ def _bind(lib):
     lib.oracle_mx_quantize_f64.restype = ctypes.c_int
     lib.oracle_expert_forward_mx.argtypes = [i64, i64, i64, i64, i32] + [vp] * 12
     lib.oracle_expert_forward_mx.restype = ctypes.c_int
+    lib.oracle_expert_backward_mx.argtypes = [i64, i64, i64, i64, i32] + [vp] * 16
+    lib.oracle_expert_backward_mx.restype = ctypes.c_int
     return lib
 
 
@@ -203,6 +205,37 @@ class Oracle:
             raise ValueError("oracle_expert_backward rejected its arguments")
         return Backward(dx, dw1, dw2, dtw)
 
+    def expert_backward_mx(self, x, xq, xs, topk_idx, topk_w, w1, w1q, w1s, w2, dy, *, want_dw=True,
+                           want_slots=False):
+        """Backward of the MXFP8 expert precision (see oracle_expert_backward_mx):
+        dX (expert path), dW1, dW2 from MXFP8 operands along the routed rows, the
+        routing-weight gradient; with want_slots also dH [T*k, 2I] and w a [T*k, I]
+        per slot before quantization (as a tuple after the Backward)."""
+        xb, w1b, w2b, dyb = _np(x), _np(w1), _np(w2), _np(dy)
+        assert all(a.dtype == np.uint16 for a in (xb, w1b, w2b, dyb))
+        xqn, xsn = _np(xq, np.uint8), _np(xs, np.uint8)
+        w1qn, w1sn = _np(w1q, np.uint8), _np(w1s, np.uint8)
+        idx = _np(topk_idx, np.int32)
+        w = _np(topk_w, np.float64)
+        T, H = xb.shape
+        E, twoI, _ = w1b.shape
+        I = twoI // 2
+        k = idx.shape[1]
+        dx = np.empty((T, H), np.float64)
+        dw1 = np.empty((E, 2 * I, H), np.float64) if want_dw else None
+        dw2 = np.empty((E, H, I), np.float64) if want_dw else None
+        dtw = np.empty((T, k), np.float64)
+        dh = np.zeros((T * k, 2 * I), np.float64) if want_slots else None
+        wa = np.zeros((T * k, I), np.float64) if want_slots else None
+        rc = self.lib.oracle_expert_backward_mx(T, H, I, E, k, _ptr(xb), _ptr(xqn), _ptr(xsn), _ptr(idx), _ptr(w),
+                                                _ptr(w1b), _ptr(w1qn), _ptr(w1sn), _ptr(w2b), _ptr(dyb), _ptr(dx),
+                                                _ptr(dw1), _ptr(dw2), _ptr(dtw), _ptr(dh), _ptr(wa))
+        if rc != 0:
+            raise ValueError("oracle_expert_backward_mx rejected its arguments")
+        if want_slots:
+            return Backward(dx, dw1, dw2, dtw), dh, wa
+        return Backward(dx, dw1, dw2, dtw)
+
     def mx_quantize(self, a):
         """MXFP8 quantization along the last dimension: (codes uint8, scales uint8 [.., cols/32]).
 
@@ -319,6 +352,10 @@ def router_backward(*args, **kwargs) -> RouterBackward:
 
 def mx_quantize(*args, **kwargs):
     return default().mx_quantize(*args, **kwargs)
+
+
+def expert_backward_mx(*args, **kwargs):
+    return default().expert_backward_mx(*args, **kwargs)
 
 
 def expert_forward_mx(*args, **kwargs):

@@ -404,6 +404,43 @@ int oracle_expert_forward(int64_t T, int64_t H, int64_t I, int64_t E, int32_t k,
  * slots in flat slot order. Slots with an index outside [0, E) contribute
  * nothing (their dtopk_w is 0).
  */
+/*
+ * The data-gradient path of one slot of expert e, given the slot's g, u and
+ * a = silu(g) u (bf16 weights W1 = w1[e], W2 = w2[e]; the chain rule of the
+ * forward above):
+ *   o = W2 a,  dw = <dY_t, o>,  dO = w dY_t,  dA_i = sum_h W2[h,i] dO_h,
+ *   dU_i = dA_i silu(g_i),  dG_i = dA_i u_i silu'(g_i),
+ *   dX_t += sum_i W1[i,:] dG_i + W1[I+i,:] dU_i
+ * dh receives [dG | dU] (2I values); o, dO, dA are scratch ([H], [H], [I]).
+ * Returns dw.
+ */
+static double slot_data_gradient(int64_t H, int64_t I, const uint16_t *W1, const uint16_t *W2, double w,
+                                 const double *dyt, const double *g, const double *u, const double *a,
+                                 double *o, double *dO, double *dA, double *dxt, double *dh) {
+    slot_output(H, I, W2, a, o);
+    double dwt = 0.0;
+    for (int64_t h = 0; h < H; ++h) {
+        dwt += dyt[h] * o[h];
+        dO[h] = w * dyt[h];
+    }
+    for (int64_t i = 0; i < I; ++i) {
+        double acc = 0.0;
+        for (int64_t h = 0; h < H; ++h) acc += bf16_value(W2[h * I + i]) * dO[h];
+        dA[i] = acc;
+    }
+    for (int64_t i = 0; i < I; ++i) {
+        const double sg = 1.0 / (1.0 + exp(-g[i]));
+        const double dsilu = sg * (1.0 + g[i] * (1.0 - sg));
+        const double dU = dA[i] * silu(g[i]);
+        const double dG = dA[i] * u[i] * dsilu;
+        for (int64_t h = 0; h < H; ++h)
+            dxt[h] += bf16_value(W1[i * H + h]) * dG + bf16_value(W1[(I + i) * H + h]) * dU;
+        dh[i] = dG;
+        dh[I + i] = dU;
+    }
+    return dwt;
+}
+
 int oracle_expert_backward(int64_t T, int64_t H, int64_t I, int64_t E, int32_t k,
                            const uint16_t *x, const int32_t *topk_idx, const double *topk_w,
                            const uint16_t *w1, const uint16_t *w2, const uint16_t *dy,
@@ -431,7 +468,8 @@ int oracle_expert_backward(int64_t T, int64_t H, int64_t I, int64_t E, int32_t k
         double *o = (double *)malloc(sizeof(double) * (size_t)H);
         double *dO = (double *)malloc(sizeof(double) * (size_t)H);
         double *dA = (double *)malloc(sizeof(double) * (size_t)I);
-        if (!xt || !dyt || !g || !u || !a || !o || !dO || !dA) {
+        double *dh = (double *)malloc(sizeof(double) * 2 * (size_t)I);
+        if (!xt || !dyt || !g || !u || !a || !o || !dO || !dA || !dh) {
 #pragma omp atomic write
             bad = 1;
         } else {
@@ -453,31 +491,10 @@ int oracle_expert_backward(int64_t T, int64_t H, int64_t I, int64_t E, int32_t k
                     const uint16_t *W1 = w1 + (int64_t)e * 2 * I * H;
                     const uint16_t *W2 = w2 + (int64_t)e * H * I;
                     slot_hidden(H, I, W1, xt, g, u, a);
-                    slot_output(H, I, W2, a, o);
                     const double w = topk_w[slot];
-                    double dwt = 0.0;
-                    for (int64_t h = 0; h < H; ++h) {
-                        dwt += dyt[h] * o[h];
-                        dO[h] = w * dyt[h];
-                    }
+                    const double dwt = slot_data_gradient(H, I, W1, W2, w, dyt, g, u, a, o, dO, dA, dxt, dh);
                     if (dtopk_w) dtopk_w[slot] = dwt;
-                    for (int64_t i = 0; i < I; ++i) {
-                        double acc = 0.0;
-                        for (int64_t h = 0; h < H; ++h) acc += bf16_value(W2[h * I + i]) * dO[h];
-                        dA[i] = acc;
-                    }
-                    for (int64_t i = 0; i < I; ++i) {
-                        const double sg = 1.0 / (1.0 + exp(-g[i]));
-                        const double dsilu = sg * (1.0 + g[i] * (1.0 - sg));
-                        const double dU = dA[i] * silu(g[i]);
-                        const double dG = dA[i] * u[i] * dsilu;
-                        for (int64_t h = 0; h < H; ++h)
-                            dxt[h] += bf16_value(W1[i * H + h]) * dG + bf16_value(W1[(I + i) * H + h]) * dU;
-                        if (dh_s) {
-                            dh_s[slot * 2 * I + i] = dG;
-                            dh_s[slot * 2 * I + I + i] = dU;
-                        }
-                    }
+                    if (dh_s) memcpy(dh_s + slot * 2 * I, dh, sizeof(double) * 2 * (size_t)I);
                     if (do_s) {
                         for (int64_t h = 0; h < H; ++h) do_s[slot * H + h] = dO[h];
                         for (int64_t i = 0; i < I; ++i) a_s[slot * I + i] = a[i];
@@ -485,7 +502,7 @@ int oracle_expert_backward(int64_t T, int64_t H, int64_t I, int64_t E, int32_t k
                 }
             }
         }
-        free(xt); free(dyt); free(g); free(u); free(a); free(o); free(dO); free(dA);
+        free(xt); free(dyt); free(g); free(u); free(a); free(o); free(dO); free(dA); free(dh);
     }
     if (!bad && (dw1 || dw2)) {
 #pragma omp parallel for schedule(dynamic, 1)
@@ -662,21 +679,27 @@ static double e8m0_value(uint8_t s) { return ldexp(1.0, (int)s - 127); }
  * rows: codes [rows, cols], scales [rows, cols / 32]. Input as bf16 bit
  * patterns (in_bf16) or doubles (in_f64); exactly one of them is non-NULL.
  */
+/* One block of 32 values: its E8M0 scale code, and each value's E4M3 code. */
+static uint8_t mx_quantize_block(const double *v, uint8_t *codes) {
+    double amax = 0.0;
+    for (int i = 0; i < 32; ++i)
+        if (fabs(v[i]) > amax) amax = fabs(v[i]);
+    const uint8_t s = mx_scale_code(amax);
+    for (int i = 0; i < 32; ++i) codes[i] = e4m3_encode(v[i] / e8m0_value(s));
+    return s;
+}
+
 static void mx_quantize_rows(int64_t rows, int64_t cols, const uint16_t *in_bf16, const double *in_f64,
                              uint8_t *codes, uint8_t *scales) {
 #pragma omp parallel for schedule(static)
     for (int64_t r = 0; r < rows; ++r) {
         for (int64_t b = 0; b < cols / 32; ++b) {
-            double v[32], amax = 0.0;
+            double v[32];
             for (int i = 0; i < 32; ++i) {
                 const int64_t j = r * cols + b * 32 + i;
                 v[i] = in_bf16 ? bf16_value(in_bf16[j]) : in_f64[j];
-                if (fabs(v[i]) > amax) amax = fabs(v[i]);
             }
-            const uint8_t s = mx_scale_code(amax);
-            scales[r * (cols / 32) + b] = s;
-            for (int i = 0; i < 32; ++i)
-                codes[r * cols + b * 32 + i] = e4m3_encode(v[i] / e8m0_value(s));
+            scales[r * (cols / 32) + b] = mx_quantize_block(v, codes + r * cols + b * 32);
         }
     }
 }
@@ -773,5 +796,185 @@ int oracle_expert_forward_mx(int64_t T, int64_t H, int64_t I, int64_t E, int32_t
         }
         free(xt); free(a); free(aq); free(ac); free(as);
     }
+    return bad ? -1 : 0;
+}
+
+/*
+ * MXFP8 quantization of one block of 32 values along the block, returned as
+ * their dequantized values (code value times block scale): the same rule as
+ * mx_quantize_rows, for a block gathered from a column.
+ */
+static void mx_block_values(const double *v, double *q) {
+    uint8_t c[32];
+    const uint8_t s = mx_quantize_block(v, c);
+    for (int i = 0; i < 32; ++i) q[i] = e4m3_value(c[i]) * e8m0_value(s);
+}
+
+/*
+ * Training backward of the MXFP8 expert precision (MegaMoE guide, section
+ * "Expert precision": mxfp8 runs fc1, the SwiGLU, fc2 and the dW1 / dW2
+ * weight gradients in MXFP8). Reading, where the pages name no more:
+ *
+ *   - The forward is that of oracle_expert_forward_mx: g, u from X(x) and
+ *     X(w1) (quantized along H), a = silu(g) u.
+ *   - The data-gradient path is the bf16 backward's (the pages list no MXFP8
+ *     data gradients), taken at that forward's g and u with the bf16 weights;
+ *     quantization passes the gradient through unchanged:
+ *       dw[t,j] = <dY_t, W2_e a>,  dO = w dY_t,  dA = W2_e^T dO,
+ *       dU = dA silu(g),  dG = dA u silu'(g),  dX_t += W1_e^T [dG ; dU].
+ *   - The two weight gradients take MXFP8 operands quantized along their
+ *     reduction dimension, the expert's routed rows: the rows of expert e are
+ *     its slots in increasing flat slot order (the routed order), cut into
+ *     blocks of 32 consecutive rows from its first row (a last, partial block
+ *     is completed with zeros); every column of an operand is quantized per
+ *     block. The routing weight is carried by the activation side, as the
+ *     forward multiplies it onto fc2's output:
+ *       dW2_e[h,i] = sum_r Q(dY)[r,h] Q(w a)[r,i]
+ *       dW1_e[j,h] = sum_r Q(dH)[r,j] Q(x)[r,h],   dH = [dG | dU]
+ *     with dY[r] and x[r] the rows of the slot's token.
+ *
+ * x, dy, w1, w2 are bf16 [T,H], [T,H], [E,2I,H], [E,H,I]; x_codes / x_scales
+ * and w1_codes / w1_scales the forward's quantization of x and w1 (along H).
+ * Outputs as in oracle_expert_backward; dh_slot [T*k, 2I] and wa_slot
+ * [T*k, I], when given, receive dH and w a per slot in flat slot order (zero
+ * for dropped slots), before quantization.
+ */
+int oracle_expert_backward_mx(int64_t T, int64_t H, int64_t I, int64_t E, int32_t k,
+                              const uint16_t *x, const uint8_t *x_codes, const uint8_t *x_scales,
+                              const int32_t *topk_idx, const double *topk_w,
+                              const uint16_t *w1, const uint8_t *w1_codes, const uint8_t *w1_scales,
+                              const uint16_t *w2, const uint16_t *dy,
+                              double *dx, double *dw1, double *dw2, double *dtopk_w,
+                              double *dh_slot, double *wa_slot) {
+    if (T < 0 || H <= 0 || I <= 0 || E <= 0 || k <= 0 || H % 32 || I % 32 || !x || !x_codes ||
+        !x_scales || !topk_idx || !topk_w || !w1 || !w1_codes || !w1_scales || !w2 || !dy || !dx)
+        return -1;
+    const int64_t R = T * k;
+    double *dh_s = (double *)calloc((size_t)(R > 0 ? R : 1) * 2 * I, sizeof(double));
+    double *wa_s = (double *)calloc((size_t)(R > 0 ? R : 1) * I, sizeof(double));
+    if (!dh_s || !wa_s) {
+        free(dh_s); free(wa_s);
+        return -1;
+    }
+    int bad = 0;
+#pragma omp parallel
+    {
+        double *xq = (double *)malloc(sizeof(double) * (size_t)H);
+        double *dyt = (double *)malloc(sizeof(double) * (size_t)H);
+        double *g = (double *)malloc(sizeof(double) * (size_t)I);
+        double *u = (double *)malloc(sizeof(double) * (size_t)I);
+        double *a = (double *)malloc(sizeof(double) * (size_t)I);
+        double *o = (double *)malloc(sizeof(double) * (size_t)H);
+        double *dO = (double *)malloc(sizeof(double) * (size_t)H);
+        double *dA = (double *)malloc(sizeof(double) * (size_t)I);
+        if (!xq || !dyt || !g || !u || !a || !o || !dO || !dA) {
+#pragma omp atomic write
+            bad = 1;
+        } else {
+#pragma omp for schedule(dynamic, 1)
+            for (int64_t t = 0; t < T; ++t) {
+                double *dxt = dx + t * H;
+                for (int64_t h = 0; h < H; ++h) {
+                    dxt[h] = 0.0;
+                    xq[h] = mx_value(x_codes, x_scales, H, t, h);
+                    dyt[h] = bf16_value(dy[t * H + h]);
+                }
+                for (int32_t j = 0; j < k; ++j) {
+                    const int64_t slot = t * k + j;
+                    const int32_t e = topk_idx[slot];
+                    if (e < 0 || e >= E) {
+                        if (dtopk_w) dtopk_w[slot] = 0.0;
+                        continue;
+                    }
+                    /* the MXFP8 forward's pre-activation: X(x) and X(w1) along H */
+                    const int64_t w1_row = (int64_t)e * 2 * I;
+                    for (int64_t i = 0; i < I; ++i) {
+                        double gacc = 0.0, uacc = 0.0;
+                        for (int64_t h = 0; h < H; ++h) {
+                            gacc += mx_value(w1_codes, w1_scales, H, w1_row + i, h) * xq[h];
+                            uacc += mx_value(w1_codes, w1_scales, H, w1_row + I + i, h) * xq[h];
+                        }
+                        g[i] = gacc;
+                        u[i] = uacc;
+                    }
+                    for (int64_t i = 0; i < I; ++i) a[i] = silu(g[i]) * u[i];
+                    /* the data-gradient path, bf16 weights */
+                    const double w = topk_w[slot];
+                    const double dwt = slot_data_gradient(H, I, w1 + (int64_t)e * 2 * I * H, w2 + (int64_t)e * H * I,
+                                                          w, dyt, g, u, a, o, dO, dA, dxt, dh_s + slot * 2 * I);
+                    if (dtopk_w) dtopk_w[slot] = dwt;
+                    for (int64_t i = 0; i < I; ++i) wa_s[slot * I + i] = w * a[i];
+                }
+            }
+        }
+        free(xq); free(dyt); free(g); free(u); free(a); free(o); free(dO); free(dA);
+    }
+    if (!bad && (dw1 || dw2)) {
+#pragma omp parallel
+        {
+            int64_t *rows = (int64_t *)malloc(sizeof(int64_t) * (size_t)(R > 0 ? R : 1));
+            double *col = (double *)malloc(sizeof(double) * 32);
+            double *cq = (double *)malloc(sizeof(double) * 32);
+            /* one block of 32 rows of each operand, dequantized: [32][cols] */
+            double *qdy = (double *)malloc(sizeof(double) * 32 * (size_t)H);
+            double *qwa = (double *)malloc(sizeof(double) * 32 * (size_t)I);
+            double *qdh = (double *)malloc(sizeof(double) * 32 * 2 * (size_t)I);
+            double *qx = (double *)malloc(sizeof(double) * 32 * (size_t)H);
+            if (!rows || !col || !cq || !qdy || !qwa || !qdh || !qx) {
+#pragma omp atomic write
+                bad = 1;
+            } else {
+#pragma omp for schedule(dynamic, 1)
+                for (int64_t e = 0; e < E; ++e) {
+                    double *DW1 = dw1 ? dw1 + e * 2 * I * H : NULL;
+                    double *DW2 = dw2 ? dw2 + e * H * I : NULL;
+                    if (DW1) for (int64_t q = 0; q < 2 * I * H; ++q) DW1[q] = 0.0;
+                    if (DW2) for (int64_t q = 0; q < H * I; ++q) DW2[q] = 0.0;
+                    int64_t c = 0;
+                    for (int64_t s = 0; s < R; ++s)
+                        if (topk_idx[s] == e) rows[c++] = s;
+                    for (int64_t b0 = 0; b0 < c; b0 += 32) {
+                        const int64_t n = (c - b0 < 32) ? c - b0 : 32;
+                        /* per column: gather the block's values (zeros past the expert's
+                           rows), quantize, keep the dequantized values */
+#define MOE_QCOL(DST, NCOL, VALUE)                                           \
+                        for (int64_t cc = 0; cc < (NCOL); ++cc) {            \
+                            for (int r = 0; r < 32; ++r) {                   \
+                                const int64_t s = (r < n) ? rows[b0 + r] : -1; \
+                                col[r] = (s >= 0) ? (VALUE) : 0.0;           \
+                            }                                                \
+                            mx_block_values(col, cq);                        \
+                            for (int r = 0; r < 32; ++r) (DST)[r * (NCOL) + cc] = cq[r]; \
+                        }
+                        if (DW2) {
+                            MOE_QCOL(qdy, H, bf16_value(dy[(s / k) * H + cc]))
+                            MOE_QCOL(qwa, I, wa_s[s * I + cc])
+                            for (int r = 0; r < 32; ++r)
+                                for (int64_t h = 0; h < H; ++h) {
+                                    const double d = qdy[r * H + h];
+                                    if (d == 0.0) continue;
+                                    for (int64_t i = 0; i < I; ++i) DW2[h * I + i] += d * qwa[r * I + i];
+                                }
+                        }
+                        if (DW1) {
+                            MOE_QCOL(qdh, 2 * I, dh_s[s * 2 * I + cc])
+                            MOE_QCOL(qx, H, bf16_value(x[(s / k) * H + cc]))
+                            for (int r = 0; r < 32; ++r)
+                                for (int64_t jj = 0; jj < 2 * I; ++jj) {
+                                    const double d = qdh[r * 2 * I + jj];
+                                    if (d == 0.0) continue;
+                                    for (int64_t h = 0; h < H; ++h) DW1[jj * H + h] += d * qx[r * H + h];
+                                }
+                        }
+#undef MOE_QCOL
+                    }
+                }
+            }
+            free(rows); free(col); free(cq); free(qdy); free(qwa); free(qdh); free(qx);
+        }
+    }
+    if (!bad && dh_slot) memcpy(dh_slot, dh_s, sizeof(double) * (size_t)R * 2 * I);
+    if (!bad && wa_slot) memcpy(wa_slot, wa_s, sizeof(double) * (size_t)R * I);
+    free(dh_s); free(wa_s);
     return bad ? -1 : 0;
 }

@@ -18,7 +18,10 @@ the oracle disagrees with something the pages or mathematics fix:
   round trip of every finite E4M3 code under several block scales, the
   shared-exponent rule on chosen maxima, and the MX forward as a composition
   of the bf16 oracle (on dequantized inputs), the quantizer and torch fp64
-  matmuls.
+  matmuls; the MX backward against the bf16 backward where MXFP8 holds the
+  forward's inputs exactly, against the MX forward's a, and its weight
+  gradients as a composition of the quantizer (along the expert's rows) and
+  fp64 matmuls.
 
 tests/test_oracle_mutants.py compiles deliberately broken copies of the oracle
 and checks that every one of them fails at least one pin.
@@ -641,6 +644,101 @@ def pin_mx_forward_composition(orc):
         o = torch.as_tensor(w2d[e]) @ aq[slot]
         y_ref[slot // k] += float(w.reshape(-1)[slot]) * o
     np.testing.assert_allclose(y, y_ref.numpy(), rtol=1e-11, atol=1e-12)
+
+
+def _mx_exact_bf16(gen, shape, scale=1.0):
+    """bf16 values that MXFP8 holds exactly in any block: each is in
+    {0, +-1/4, +-1/2, +-3/4, +-1, +-3/2} times `scale` (a power of two), so with
+    the block's scale 2^(floor(log2 amax) - 8) every value maps to an E4M3 code
+    (at most 1.5 * 2^8 = 384) without rounding."""
+    vals = torch.tensor([0.0, 0.25, 0.5, 0.75, 1.0, 1.5, -0.25, -0.5, -0.75, -1.0, -1.5], dtype=torch.float64)
+    pick = torch.randint(0, len(vals), shape, generator=gen)
+    return (vals[pick] * scale).to(torch.bfloat16)
+
+
+def _mx_backward_problem(seed, T=40, H=64, I=64, E=4, k=2, exact=False):
+    gen = torch.Generator().manual_seed(seed)
+    if exact:
+        x = _mx_exact_bf16(gen, (T, H))
+        w1 = _mx_exact_bf16(gen, (E, 2 * I, H), 0.125)
+    else:
+        x = _rand_bf16(gen, (T, H))
+        w1 = _rand_bf16(gen, (E, 2 * I, H), H ** -0.5)
+    w2 = _rand_bf16(gen, (E, H, I), I ** -0.5)
+    dy = _rand_bf16(gen, (T, H))
+    idx = torch.randint(0, E - 1, (T, k), generator=gen, dtype=torch.int32)   # expert E-1 gets no row
+    w = torch.rand((T, k), generator=gen, dtype=torch.float64) + 0.1
+    return x, w1, w2, dy, idx, w
+
+
+def pin_mx_backward_exact_forward_is_bf16(orc):
+    """When MXFP8 holds x and w1 exactly, the MX forward's g, u are the bf16 forward's,
+    so the MX backward's data-gradient path (dX, the routing-weight gradient, w a)
+    must be the bf16 backward oracle's (itself pinned by autograd and finite
+    differences) and the bf16 forward's a times the weight."""
+    import oracle as oracle_pkg
+    x, w1, w2, dy, idx, w = _mx_backward_problem(41, exact=True)
+    xq, xs = orc.mx_quantize(x)
+    w1q, w1s = orc.mx_quantize(w1)
+    assert np.array_equal(oracle_pkg.mx_dequantize(xq, xs), x.double().numpy())
+    assert np.array_equal(oracle_pkg.mx_dequantize(w1q, w1s), w1.double().numpy())
+    b_mx, dh, wa = orc.expert_backward_mx(x, xq, xs, idx, w, w1, w1q, w1s, w2, dy, want_slots=True)
+    b = orc.expert_backward(x, idx, w, w1, w2, dy, want_dw=False)
+    np.testing.assert_allclose(b_mx.dx, b.dx, rtol=1e-11, atol=1e-12)
+    np.testing.assert_allclose(b_mx.dtopk_w, b.dtopk_w, rtol=1e-11, atol=1e-12)
+    _, a_ref, _ = orc.expert_forward(x, idx, w, w1, w2, want_a=True)
+    np.testing.assert_allclose(wa, w.numpy().reshape(-1, 1) * a_ref, rtol=1e-12, atol=1e-14)
+    assert not b_mx.dw1[-1].any() and not b_mx.dw2[-1].any()          # the expert without rows
+
+
+def pin_mx_backward_forward_is_the_mx_forward(orc):
+    """With inputs MXFP8 rounds, w a per slot is the routing weight times the MX
+    forward oracle's a before its quantization (x and w1 quantized along H)."""
+    x, w1, w2, dy, idx, w = _mx_backward_problem(43)
+    xq, xs = orc.mx_quantize(x)
+    w1q, w1s = orc.mx_quantize(w1)
+    w2q, w2s = orc.mx_quantize(w2)
+    _, dh, wa = orc.expert_backward_mx(x, xq, xs, idx, w, w1, w1q, w1s, w2, dy, want_dw=False, want_slots=True)
+    _, a_pre, _, _ = orc.expert_forward_mx(xq, xs, idx, w, w1q, w1s, w2q, w2s, want_a=True)
+    np.testing.assert_allclose(wa, w.numpy().reshape(-1, 1) * a_pre, rtol=1e-12, atol=1e-14)
+    # x really is rounded here: the unquantized x would give other values of a
+    _, a_bf, _ = orc.expert_forward(x, idx, w, w1, w2, want_a=True)
+    assert np.abs(a_bf - a_pre).max() > 1e-3
+
+
+def pin_mx_backward_wgrad_composition(orc):
+    """dW1 and dW2 of the MX backward = per expert, the rows of its slots in
+    increasing slot order, zero-padded to whole blocks of 32 rows, each column
+    quantized by the (separately pinned) MXFP8 quantizer along the rows, then one
+    fp64 matmul of the dequantized operands: dW2_e = Q(dY)^T Q(w a),
+    dW1_e = Q(dH)^T Q(x)."""
+    import oracle as oracle_pkg
+    T, k = 70, 2
+    x, w1, w2, dy, idx, w = _mx_backward_problem(47, T=T, k=k)
+    xq, xs = orc.mx_quantize(x)
+    w1q, w1s = orc.mx_quantize(w1)
+    b, dh, wa = orc.expert_backward_mx(x, xq, xs, idx, w, w1, w1q, w1s, w2, dy, want_slots=True)
+    xd, dyd = x.double().numpy(), dy.double().numpy()
+    flat = idx.numpy().reshape(-1)
+
+    def q_rows(m):
+        n = m.shape[0]
+        pad = np.zeros((-(-n // 32) * 32, m.shape[1]))
+        pad[:n] = m
+        c, sc = orc.mx_quantize(np.ascontiguousarray(pad.T))
+        return oracle_pkg.mx_dequantize(c, sc).T
+
+    sizes = []
+    for e in range(w1.shape[0]):
+        slots = np.nonzero(flat == e)[0]
+        sizes.append(len(slots))
+        if len(slots) == 0:
+            assert not b.dw1[e].any() and not b.dw2[e].any()
+            continue
+        tok = slots // k
+        np.testing.assert_allclose(b.dw2[e], q_rows(dyd[tok]).T @ q_rows(wa[slots]), rtol=1e-12, atol=1e-12)
+        np.testing.assert_allclose(b.dw1[e], q_rows(dh[slots]).T @ q_rows(xd[tok]), rtol=1e-12, atol=1e-12)
+    assert any(s % 32 for s in sizes) and max(sizes) > 32        # partial blocks and several blocks
 
 
 ALL_PINS = [v for n, v in sorted(globals().items()) if n.startswith("pin_") and callable(v)]

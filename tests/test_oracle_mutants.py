@@ -76,6 +76,20 @@ MUTANTS = {
     "mx_a_not_requantized": ("for (int64_t i = 0; i < I; ++i) aq[i] = e4m3_value(ac[i]) * e8m0_value(as[i / 32]);",
                              "for (int64_t i = 0; i < I; ++i) aq[i] = a[i];"),
     "mx_overflow_to_nan": ("if (a >= 448.0) return sign | 0x7E;", "if (a >= 448.0) return sign | 0x7F;"),
+    # MXFP8 backward
+    "mxb_forward_x_unquantized": ("xq[h] = mx_value(x_codes, x_scales, H, t, h);",
+                                  "xq[h] = bf16_value(x[t * H + h]);"),
+    "mxb_wa_unweighted": ("for (int64_t i = 0; i < I; ++i) wa_s[slot * I + i] = w * a[i];",
+                          "for (int64_t i = 0; i < I; ++i) wa_s[slot * I + i] = a[i];"),
+    "mxb_wgrad_unquantized": ("mx_block_values(col, cq);", "memcpy(cq, col, sizeof(double) * 32);"),
+    "mxb_dy_weighted": ("MOE_QCOL(qdy, H, bf16_value(dy[(s / k) * H + cc]))",
+                        "MOE_QCOL(qdy, H, topk_w[s] * bf16_value(dy[(s / k) * H + cc]))"),
+    "mxb_dw1_x_wrong_token": ("MOE_QCOL(qx, H, bf16_value(x[(s / k) * H + cc]))",
+                              "MOE_QCOL(qx, H, bf16_value(x[(s % T) * H + cc]))"),
+    "mxb_blocks_of_16": ("const int64_t n = (c - b0 < 32) ? c - b0 : 32;",
+                         "const int64_t n = (c - b0 < 16) ? c - b0 : 16;"),
+    "mxb_gate_up_up": ("gacc += mx_value(w1_codes, w1_scales, H, w1_row + i, h) * xq[h];",
+                       "gacc += mx_value(w1_codes, w1_scales, H, w1_row + I + i, h) * xq[h];"),
     "rbwd_dwr_wrong_token": ("acc += dl[t * E + e] * bf16_value(x[t * H + h]);",
                              "acc += dl[t * E + e] * bf16_value(x[((t + 1) % T) * H + h]);"),
 }
