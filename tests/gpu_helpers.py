@@ -19,6 +19,9 @@ from moe_expert_router_gb300.workloads import MoEConfig
 GAP = 1e-6
 REL_FRO = 1e-2
 MAX_ABS_FRAC = 3e-2
+# stage 1's output a: one bf16 rounding (relative Frobenius ~1e-3) plus the
+# SiLU's tanh approximation away from the fp64 value, a tighter bound than y's
+A_REL_FRO = 5e-3
 
 
 def assert_close_y(y_gpu, y_ref, what="y"):
@@ -81,7 +84,9 @@ def oracle_router(inp, cfg: MoEConfig, rows=None):
 
 
 def routing_mismatches(idx_gpu, ref, cfg: MoEConfig):
-    """(number of compared tokens, list of mismatching tokens, excluded mask)."""
+    """(number of compared tokens, list of mismatching tokens, excluded mask).
+
+    Compares the per-token expert sets; order_mismatches checks the order."""
     g = idx_gpu.cpu().numpy() if isinstance(idx_gpu, torch.Tensor) else np.asarray(idx_gpu)
     excluded = ref.sel_gap < GAP
     if cfg.n_group > 1:
@@ -91,6 +96,44 @@ def routing_mismatches(idx_gpu, ref, cfg: MoEConfig):
         if sorted(g[t].tolist()) != sorted(ref.topk_idx[t].tolist()):
             bad.append(int(t))
     return int((~excluded).sum()), bad, excluded
+
+
+def order_mismatches(idx_gpu, ref, excluded, sel_bias=None):
+    """(number of order-checked tokens, tokens whose GPU order differs).
+
+    The ABI returns each token's experts best first by selection score. A token's
+    order is unique when every gap between consecutive chosen selection scores
+    (oracle, fp64) is at least GAP; only those tokens (and none excluded from the
+    set comparison) are checked, element by element."""
+    g = idx_gpu.cpu().numpy() if isinstance(idx_gpu, torch.Tensor) else np.asarray(idx_gpu)
+    sel = ref.scores
+    if sel_bias is not None:
+        b = sel_bias.detach().cpu().double().numpy() if isinstance(sel_bias, torch.Tensor) else np.asarray(sel_bias)
+        sel = sel + b[None, :]
+    chosen = np.take_along_axis(sel, ref.topk_idx.astype(np.int64), 1)
+    gaps = chosen[:, :-1] - chosen[:, 1:]
+    checkable = ~excluded
+    if gaps.shape[1]:
+        checkable &= (gaps >= GAP).all(1)
+    bad = np.nonzero(checkable & (g != ref.topk_idx).any(1))[0]
+    return int(checkable.sum()), [int(t) for t in bad]
+
+
+def tile_sample_tokens(counts, offsets, perm, k, extra=()):
+    """Tokens that reach every (expert, 256-row tile) work unit of the grouped
+    GEMMs: for each tile of each expert, the tokens of its first routed row, of
+    the first row of its second 128-row half (when present) and of its last row
+    (which lies in a partial 32-row slab whenever the tile is ragged). Each
+    token's output row spans every n-tile, so these tokens touch every unit."""
+    toks = set(int(t) for t in extra)
+    for e, c in enumerate(np.asarray(counts).tolist()):
+        base = int(offsets[e])
+        for m0 in range(0, int(c), 256):
+            rows = min(256, int(c) - m0)
+            for r in {0, 128, rows - 1}:
+                if r < rows:
+                    toks.add(int(perm[base + m0 + r]) // k)
+    return sorted(toks)
 
 
 def run_forward(inp, idx, w, cfg: MoEConfig, ws=None, staged=False):
@@ -109,8 +152,9 @@ def run_forward(inp, idx, w, cfg: MoEConfig, ws=None, staged=False):
     return y, ws, None
 
 
-def oracle_y_for_tokens(inp, idx, w, tokens):
-    """Oracle y rows for `tokens` only: copies just the experts those tokens use."""
+def oracle_y_for_tokens(inp, idx, w, tokens, want_a=False):
+    """Oracle y rows for `tokens` only: copies just the experts those tokens use.
+    With want_a, also a [len(tokens) * k, I] per slot (token-major)."""
     tokens = torch.as_tensor(tokens, dtype=torch.long)
     idx_s = idx[tokens.to(idx.device)].cpu().long()
     used = torch.unique(idx_s[(idx_s >= 0)])
@@ -122,4 +166,7 @@ def oracle_y_for_tokens(inp, idx, w, tokens):
     w2 = inp["w2"][used.to(dev)].cpu()
     x = inp["x"][tokens.to(dev)].cpu()
     ws_ = w[tokens.to(w.device)].cpu().double()
+    if want_a:
+        y, a, _ = oracle.expert_forward(x, idx_r.to(torch.int32), ws_, w1, w2, want_a=True)
+        return y, a
     return oracle.expert_forward(x, idx_r.to(torch.int32), ws_, w1, w2)

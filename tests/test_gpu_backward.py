@@ -12,7 +12,7 @@ import pytest
 import torch
 
 import oracle
-from gpu_helpers import assert_close_y, router_cfg_of
+from gpu_helpers import assert_close_y, read_metadata, router_cfg_of, tile_sample_tokens
 from moe_expert_router_gb300 import binding as B
 from moe_expert_router_gb300.workloads import CONFIGS, MoEConfig, generate, routing_with_counts
 
@@ -218,39 +218,69 @@ def test_zero_tokens_zero_weight_gradients():
     assert not dwr.abs().max().item()
 
 
+def weight_grad_experts(counts, n=8):
+    """At least n experts (when there are that many) spanning the row-count
+    regimes of the weight-gradient GEMMs, whose reduction runs over an expert's
+    routed rows: the most and the least loaded expert with rows, and experts
+    whose count leaves a last 256-row tile of at most 128 rows, of more than 128
+    rows, no partial 64-row k-block, a partial one, and an expert without rows."""
+    c = np.asarray(counts)
+    live = np.nonzero(c > 0)[0]
+    pick = [int(c.argmax()), int(live[np.argmin(c[live])])]
+    regimes = [lambda v: 0 < v % 256 <= 128, lambda v: v % 256 > 128, lambda v: v > 0 and v % 64 == 0,
+               lambda v: v % 64 != 0, lambda v: v == 0]
+    for test in regimes:
+        hit = [e for e in range(len(c)) if test(int(c[e])) and e not in pick]
+        if hit:
+            pick.append(hit[0])
+    for e in np.linspace(0, len(c) - 1, num=len(c)).astype(int).tolist():
+        if len(pick) >= n:
+            break
+        if e not in pick:
+            pick.append(int(e))
+    return pick
+
+
 @pytest.mark.slow
 def test_full_size_train_config_sampled():
     """The training configuration at full size, in the bench's staged launch
-    sequence: dX and dtopk_w on sampled tokens, dW1 / dW2 of two experts, dW_r
-    given the GPU's own routing-weight gradient."""
+    sequence: dX and dtopk_w on the tokens of the first, middle and last rows of
+    every 256-row tile of every expert (so every unit of the dA and dX GEMMs is
+    reached), dW1 / dW2 of at least eight experts spanning the row-count regimes
+    of the weight-gradient GEMMs, dW_r given the GPU's own routing-weight
+    gradient."""
     cfg = CONFIGS["train"]
     inp = _inputs(cfg, seed=0)
     out = train_step(inp, cfg)
     assert out["err"] == 0
     idx, w = out["idx"], out["w"]
     T, k, E = cfg.T, cfg.k, cfg.E
-    toks = [0, 1, T // 2, T - 1] + list(range(37, T, T // 12))[:12]
+    counts, offsets, _, perm, _ = read_metadata(out["ws"], out["shp"])
+    toks = tile_sample_tokens(counts, offsets, perm, k, extra=[0, 1, T // 2, T - 1])
     cpu = {k_: (v.cpu() if isinstance(v, torch.Tensor) else v) for k_, v in inp.items()}
     tok_t = torch.as_tensor(toks)
     b = oracle.expert_backward(cpu["x"][tok_t], idx.cpu()[tok_t], w.cpu()[tok_t].double(), cpu["w1"],
                                cpu["w2"], cpu["dy"][tok_t], want_dw=False)
-    assert_close_y(out["dtw"].cpu()[tok_t], b.dtopk_w, "dtopk_w (sampled tokens)")
+    assert_close_y(out["dtw"].cpu()[tok_t], b.dtopk_w, f"dtopk_w ({len(toks)} tokens)")
     # dX adds the router term, which needs the token's logit gradient: from the oracle's
     # router backward fed with the oracle's own routing-weight gradient of those tokens
     rb = oracle.router_backward(cpu["x"][tok_t], cpu["w_r"], idx.cpu()[tok_t], w.cpu()[tok_t].double(),
                                 b.dtopk_w, score=cfg.score, normalize=cfg.normalize, scale=cfg.scale)
-    assert_close_y(out["dx"].cpu()[tok_t], b.dx + rb.dx_add, "dX (sampled tokens)")
-    # weight gradients of the most and the least loaded expert
+    assert_close_y(out["dx"].cpu()[tok_t], b.dx + rb.dx_add, f"dX ({len(toks)} tokens)")
+    # weight gradients of experts in every row-count regime
     flat = idx.cpu().reshape(-1).long()
-    counts = torch.bincount(flat, minlength=E)
-    for e in (int(counts.argmax()), int(counts.argmin())):
+    for e in weight_grad_experts(counts):
         slots = torch.nonzero(flat == e).flatten()
+        if len(slots) == 0:
+            assert not out["dw1"][e].float().abs().max().item()
+            assert not out["dw2"][e].float().abs().max().item()
+            continue
         tk = slots // k
         one = torch.zeros((len(tk), 1), dtype=torch.int32)
         be = oracle.expert_backward(cpu["x"][tk], one, w.cpu().reshape(-1)[slots].double().unsqueeze(1),
                                     cpu["w1"][e:e + 1], cpu["w2"][e:e + 1], cpu["dy"][tk])
-        assert_close_y(out["dw2"][e], be.dw2[0], f"dW2[{e}]")
-        assert_close_y(out["dw1"][e], be.dw1[0], f"dW1[{e}]")
+        assert_close_y(out["dw2"][e], be.dw2[0], f"dW2[{e}] ({len(slots)} rows)")
+        assert_close_y(out["dw1"][e], be.dw1[0], f"dW1[{e}] ({len(slots)} rows)")
     # dW_r from the GPU's own routing-weight gradient (the router backward stage alone)
     rfull = oracle.router_backward(cpu["x"], cpu["w_r"], idx.cpu(), w.cpu().double(),
                                    out["dtw"].cpu().double(), score=cfg.score, normalize=cfg.normalize,

@@ -9,8 +9,8 @@ import pytest
 import torch
 
 import oracle
-from gpu_helpers import (assert_close_y, oracle_router, oracle_y_for_tokens, read_metadata,
-                         routing_mismatches, run_forward, run_router)
+from gpu_helpers import (A_REL_FRO, assert_close_y, oracle_router, oracle_y_for_tokens, order_mismatches,
+                         read_metadata, routing_mismatches, run_forward, run_router, tile_sample_tokens)
 from moe_expert_router_gb300 import binding as B
 from moe_expert_router_gb300.workloads import (CONFIGS, MoEConfig, even_routing, generate,
                                                routing_with_counts)
@@ -144,8 +144,6 @@ SHAPES = [
     (33, 8, 8, 3, 2),          # smallest dimensions
 ]
 
-
-A_REL_FRO = 5e-3
 
 
 @pytest.mark.parametrize("shape", SHAPES, ids=lambda s: "x".join(map(str, s)))
@@ -301,6 +299,8 @@ def test_router_vs_oracle(name):
     ref = oracle_router(inp, cfg)
     n, bad, excluded = routing_mismatches(idx, ref, cfg)
     assert not bad, f"{len(bad)} of {n} tokens routed differently, e.g. {bad[:5]}"
+    n_ord, bad_ord = order_mismatches(idx, ref, excluded, inp.get("sel_bias"))
+    assert n_ord > 0 and not bad_ord, f"{len(bad_ord)} of {n_ord} tokens not best first, e.g. {bad_ord[:5]}"
     keep = ~excluded
     ref_sets = np.sort(ref.topk_idx, 1)
     g = idx.cpu().numpy()
@@ -322,23 +322,31 @@ def test_router_vs_oracle(name):
 # ------------------------------------------------------------------ full sizes
 
 FULL = ["mid", "large_group", "zipf_prefill", "zipf_decode", "train"]
+# workloads whose every token is compared with the oracle (the others: a sample
+# that reaches every (expert, 256-row tile) work unit)
+ALL_TOKENS = {"mid", "zipf_decode"}
 
 
 @pytest.mark.slow
 @pytest.mark.parametrize("name", FULL)
 def test_full_size_config(name):
     """Full-size workload in the bench's launch configuration (staged C-ABI calls):
-    routing of every token against the oracle; y on sampled tokens (first, last,
-    and tokens of the most and least loaded experts) against the oracle."""
+    routing of every token against the oracle (sets, and the best-first order of
+    tokens without near-ties); y of every token (mid, zipf_decode) or of the tokens
+    of the first, middle and last rows of every 256-row tile of every expert, plus
+    the first, last and middle tokens and tokens of the most and least loaded
+    experts; stage 1's a rows of the sampled tokens' slots."""
     cfg = CONFIGS[name]
     inp = generate(cfg, seed=0, device=DEV)
     idx, w, aux, ws = run_router(inp, cfg)
     ref = oracle_router(inp, cfg)
     n, bad, excluded = routing_mismatches(idx, ref, cfg)
     assert not bad, f"{len(bad)} of {n} tokens routed differently, e.g. {bad[:5]}"
+    n_ord, bad_ord = order_mismatches(idx, ref, excluded, inp.get("sel_bias"))
+    assert n_ord > 0 and not bad_ord, f"{len(bad_ord)} of {n_ord} tokens not best first, e.g. {bad_ord[:5]}"
     y, ws, a = run_forward(inp, idx, w, cfg, ws=ws, staged=True)
     shp = B.shape(cfg.T, cfg.H, cfg.I, cfg.E, cfg.k)
-    counts, offsets, _, perm, _ = read_metadata(ws, shp)
+    counts, offsets, _, perm, row_of = read_metadata(ws, shp)
     ref_counts = np.bincount(ref.topk_idx.reshape(-1), minlength=cfg.E)
     if not excluded.any():
         np.testing.assert_array_equal(counts, ref_counts)
@@ -357,9 +365,18 @@ def test_full_size_config(name):
     small = int(np.argmin(np.where(counts > 0, counts, np.iinfo(np.int32).max)))
     t_big = int(np.nonzero((g == big).any(1))[0][-1])
     t_small = int(np.nonzero((g == small).any(1))[0][0])
-    tokens = sorted({0, 1, cfg.T // 2, cfg.T - 1, t_big, t_small})
-    y_ref = oracle_y_for_tokens(inp, idx, w, tokens)
-    assert_close_y(y[tokens], y_ref, what=f"{name} y[sampled tokens]")
+    extra = {0, 1, cfg.T // 2, cfg.T - 1, t_big, t_small}
+    if name in ALL_TOKENS:
+        tokens = list(range(cfg.T))
+    else:
+        tokens = tile_sample_tokens(counts, offsets, perm, cfg.k, extra)
+    y_ref, a_ref = oracle_y_for_tokens(inp, idx, w, tokens, want_a=True)
+    assert_close_y(y[tokens], y_ref, what=f"{name} y[{len(tokens)} tokens]")
+    # stage 1 alone: the a rows of those tokens' slots, in routed order on the GPU
+    slots = (np.asarray(tokens)[:, None] * cfg.k + np.arange(cfg.k)[None, :]).reshape(-1)
+    rows = torch.as_tensor(row_of[slots], dtype=torch.long)
+    rel, _ = assert_close_y(a[rows.to(DEV)], a_ref, what=f"{name} a[{len(slots)} slots]")
+    assert rel <= A_REL_FRO, f"a: relative Frobenius error {rel:.3e} > {A_REL_FRO}"
     assert torch.isfinite(y.float()).all()
     assert B.moe_get_device_error(ws) == 0
 
