@@ -6,6 +6,10 @@ of one node.
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
                     [--impl ours|reference] [--no-cpu-baseline]
 
+The default workload is large_group (T=8192, H=7168, I=2048, E=256, k=8,
+sigmoid scores with a selection bias, 8 groups keep 4, weights x2.5): the
+largest configuration that fits one GPU.
+
 A step is one pass of the whole path over one batch of seeded synthetic
 inputs already resident in HBM. Each rank runs its own independent replica
 (the path has no exchange step at expert parallelism 1), so scaling is weak.
@@ -149,15 +153,34 @@ def bytes_and_flops(cfg, counts, precision="bf16"):
     active = int((counts > 0).sum())
     if precision == "mxfp8":
         q = 1.0 + 1.0 / 32           # E4M3 byte + one E8M0 byte per 32 elements
-        return {"stages": {
+        st = {
             "gemm1": {"flops": 4.0 * R * H * I,
-                      "bytes": 2.0 * H * I * q * active + R * H * q + R * I * q,
+                      "bytes": 2.0 * H * I * q * active + R * H * q + R * I * q + (4.0 * R * I if cfg.backward else 0),
                       "kernel": "tc_gemm_kernel<kStage1Mx> (stage 1 in MXFP8: dispatched E4M3 x rows, "
-                                "block-scaled MMA, SwiGLU + MXFP8 quantization of a)"},
+                                "block-scaled MMA, SwiGLU + MXFP8 quantization of a%s)"
+                                % (", h saved in bf16" if cfg.backward else ""), "precision": "mxfp8"},
             "gemm2_combine": {"flops": 2.0 * R * H * I,
                               "bytes": H * I * q * active + R * I * q + 2.0 * T * H,
-                              "kernel": "tc_gemm_kernel<kStage2Mx> + combine_kernel (stage 2 in MXFP8)"},
-        }, "active_experts": active}
+                              "kernel": "tc_gemm_kernel<kStage2Mx> + combine_kernel (stage 2 in MXFP8)",
+                              "precision": "mxfp8"},
+        }
+        if cfg.backward:
+            bf = bytes_and_flops(cfg, counts, "bf16")["stages"]
+            st["bwd_stage2_data"] = bf["bwd_stage2_data"]
+            st["bwd_stage1_data"] = bf["bwd_stage1_data"]
+            # quantization of dY and w a (read 2 R (H + I), write (R + 128 E)(H + I) q), then the GEMM
+            ld = R + 128 * E
+            st["bwd_stage2_weight"] = {
+                "flops": 2.0 * R * H * I,
+                "bytes": 2.0 * R * (H + I) + 2.0 * ld * (H + I) * q + 2.0 * E * H * I,
+                "kernel": "mx_quantize_rows_t_kernel x2 + tc_gemm_kernel<kWgradMx>: dW2 in MXFP8",
+                "precision": "mxfp8"}
+            st["bwd_stage1_weight"] = {
+                "flops": 4.0 * R * H * I,
+                "bytes": 2.0 * R * (2 * I) + 2.0 * T * H + 2.0 * ld * (2 * I + H) * q + 4.0 * E * H * I,
+                "kernel": "mx_quantize_rows_t_kernel x2 + tc_gemm_kernel<kWgradMx>: dW1 in MXFP8",
+                "precision": "mxfp8"}
+        return {"stages": st, "active_experts": active}
     st = {
         "gemm1": {"flops": 4.0 * R * H * I,
                   "bytes": 4.0 * H * I * active + 2.0 * T * H + 2.0 * R * I * (3 if cfg.backward else 1),
@@ -236,10 +259,8 @@ def run_ours(args, cfg, rank, world, local_rank):
         w1_f, w2_f = B.moe_pack_weights(inp["w1"], inp["w2"], shp)
         torch.cuda.synchronize(dev)
     if mx:
-        if train:
-            raise SystemExit("--precision mxfp8 covers the forward expert path; the train workload is bf16")
         from moe_expert_router_gb300.mx_cache import MxWeightCache
-        shp = B.shape(cfg.T, cfg.H, cfg.I, cfg.E, cfg.k, mxfp8=True)
+        shp = B.shape(cfg.T, cfg.H, cfg.I, cfg.E, cfg.k, training=train, mxfp8=True)
         ws = B.new_workspace(shp, dev)
         cache = MxWeightCache()           # weights quantized once, outside the timed region
         w1q, w1s = cache.get(inp["w1"])
@@ -278,8 +299,24 @@ def run_ours(args, cfg, rank, world, local_rank):
         yield lambda: B.moe_routing_metadata(idx, shp, ws)
         if mx:
             yield lambda: B.moe_mx_quantize_dispatch(x_in, shp, ws)
-            yield lambda: B.moe_dispatch_gemm1_mx(w1q, w1s, shp, aq, as_, ws)
+            if train:
+                yield lambda: B.moe_dispatch_gemm1_mx_train(w1q, w1s, shp, aq, as_, h, ws)
+            else:
+                yield lambda: B.moe_dispatch_gemm1_mx(w1q, w1s, shp, aq, as_, ws)
             yield lambda: B.moe_swiglu_gemm2_combine_mx(aq, as_, w, w2q, w2s, shp, y, ws)
+            if not train:
+                return
+            # the guide's mxfp8 training: bf16 data gradients, MXFP8 weight gradients
+            yield lambda: B.moe_backward_stage2_data(dy_in, w, inp["w2"], h, shp, ws, dtopk_w=dtw)
+            yield lambda: B.moe_backward_stage2_weight_mx(dy_in, shp, dw2, ws)
+            if uniform:
+                yield lambda: None
+                yield lambda: B.moe_backward_stage1_data(inp["w1"], shp, dx, ws)
+            else:
+                yield lambda: B.moe_router_backward(x_in, logits, idx, w, dtw, shp, rcfg, dwr, ws)
+                yield lambda: B.moe_backward_stage1_data(inp["w1"], shp, dx, ws, w_r=inp["w_r"],
+                                                         topk_idx=idx, cfg=rcfg)
+            yield lambda: B.moe_backward_stage1_weight_mx(x_in, shp, dw1, ws)
             return
         if train:
             yield lambda: B.moe_dispatch_gemm1_train(x_in, inp["w1"], shp, a, h, ws)
@@ -465,6 +502,12 @@ def oracle_sample(cfg, n_tokens, seed=0, inputs=None, routing="router", precisio
         w1q, w1s, w2q, w2s = _MX_WEIGHTS[cfg.name]
         xq, xs = oracle.mx_quantize(x)
         oracle.expert_forward_mx(xq, xs, r.topk_idx, r.topk_w, w1q, w1s, w2q, w2s)
+        if cfg.backward:
+            b = oracle.expert_backward_mx(x, xq, xs, r.topk_idx, r.topk_w, inp["w1"], w1q, w1s, inp["w2"],
+                                          inp["dy"][:n_tokens])
+            if routing != "uniform":
+                oracle.router_backward(x, inp["w_r"], r.topk_idx, r.topk_w, b.dtopk_w, score=cfg.score,
+                                       normalize=cfg.normalize, scale=cfg.scale, logit_offset=inp["logit_offset"])
         return time.perf_counter() - t0
     oracle.expert_forward(x, r.topk_idx, r.topk_w, inp["w1"], inp["w2"])
     if cfg.backward and routing == "uniform":
@@ -569,7 +612,8 @@ def main():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--workload", default="mid", choices=sorted(CONFIGS))
+    # default: the largest single-GPU configuration (DeepSeek-V3 geometry, group-limited routing)
+    ap.add_argument("--workload", default="large_group", choices=sorted(CONFIGS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--precision", default="bf16", choices=["bf16", "mxfp8"],
@@ -610,8 +654,10 @@ def main():
         dom_ms = stage_avg[dom]
         f, b = bf["stages"][dom]["flops"], bf["stages"][dom]["bytes"]
         # an MXFP8 contraction takes the fp8 peak: the measured bf16 peak times the
-        # nominal fp8 / bf16 ratio (4.5 / 2.25 PFLOP/s dense)
-        tc_peak = peaks["bf16_tflops"] * (2.0 if args.precision == "mxfp8" else 1.0)
+        # nominal fp8 / bf16 ratio (4.5 / 2.25 PFLOP/s dense); the MXFP8 training
+        # step's data gradients stay bf16
+        dom_mx = bf["stages"][dom].get("precision", args.precision) == "mxfp8"
+        tc_peak = peaks["bf16_tflops"] * (2.0 if dom_mx else 1.0)
         t_tc = f / (tc_peak * 1e12)
         t_hbm = b / (peaks["hbm_gbs"] * 1e9)
         if t_tc >= t_hbm:
@@ -631,14 +677,16 @@ def main():
         roof["kernel"] = bf["stages"][dom]["kernel"]
         roof["stage"] = dom
         roof["peak_kind"] = (f"{peaks['source']} bf16 burst x 2 (nominal fp8/bf16 ratio)"
-                             if args.precision == "mxfp8" and roof["bound"] == "tensor"
+                             if dom_mx and roof["bound"] == "tensor"
                              else f"{peaks['source']} burst")
         roof["kernel_ms"] = dom_ms
         out = {
             "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": total_ms / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-            "dtype": "mxfp8 (e4m3 + e8m0 scales, fp32 accumulate)" if args.precision == "mxfp8" else "bf16",
+            "dtype": ("bf16" if args.precision != "mxfp8" else
+                      "mxfp8 (e4m3 + e8m0 scales, fp32 accumulate)" if not cfg.backward else
+                      "mxfp8 expert stages and weight gradients (e4m3 + e8m0, fp32 accumulate), bf16 data gradients"),
             "data": "synthetic", "config": config_dict(cfg, args),
             "tokens_per_s": tokens_per_s,
             "stage_ms": {n: round(v, 5) for n, v in stage_avg.items()},

@@ -55,6 +55,7 @@ typedef enum moe_status {
 /* Bits of the device error word. */
 #define MOE_DEVERR_BAD_EXPERT_INDEX 0x1  /* a topk_idx entry outside [0, E): that slot was dropped */
 #define MOE_DEVERR_WAIT_TIMEOUT     0x2  /* a pipeline wait ran out of time: outputs are invalid */
+#define MOE_DEVERR_CAPACITY         0x4  /* expert parallelism: a routed row beyond a block's capacity was dropped */
 
 typedef struct moe_shape {
     int64_t T;   /* tokens */
@@ -102,6 +103,8 @@ typedef struct moe_ws_layout {
                           before stage 2 writes them, stage 1 (outside training)
                           holds x's rows dispatched into routed order here; the
                           backward's dX rows (unweighted, routed order) reuse it */
+    size_t combine;    /* int32 [T, ceil(H/256)] counters of stage 2's fused k-way sum, used
+                          when T*k <= 8192 (set by moe_routing_metadata) */
     /* training workspaces only (flags = MOE_SHAPE_TRAINING), else equal to total: */
     size_t dh;         /* bf16 [T*k, 2I] gradient of h = [gate | up], routed order */
     size_t aw;         /* bf16 [T*k, I] routing weight times a, routed order */
@@ -115,6 +118,8 @@ typedef struct moe_ws_layout {
     size_t x_scales;   /* E8M0 [T*k, H/32] */
     size_t a_codes;    /* E4M3 [T*k, I] quantized SwiGLU output, routed order (moe_forward_mx) */
     size_t a_scales;   /* E8M0 [T*k, I/32] */
+    /* training + MXFP8 workspaces only, else equal to total: */
+    size_t mx_wgrad;   /* the MXFP8 weight gradients' operands, quantized along the routed rows */
     size_t total;      /* == moe_workspace_size */
 } moe_ws_layout_t;
 
@@ -283,6 +288,49 @@ moe_status_t moe_dispatch_rows(const void *x, const float *topk_w, const moe_sha
  */
 moe_status_t moe_combine_rows(const void *rows, const moe_shape_t *shape, void *y, void *ws, size_t ws_bytes,
                               void *stream);
+
+/*
+ * Expert parallelism without host synchronisation (the guide's "Example 2"
+ * runs the whole layer under one CUDA graph). P ranks, rank q owning experts
+ * [q E_loc, (q+1) E_loc), E = P E_loc. Every rank sends every rank a block of
+ * `capacity` rows (C), so the caller's collective (an all-to-all with equal
+ * splits) needs no per-step sizes from the device; C = T k can never drop a
+ * row. A step on rank p:
+ *   1. moe_routing_metadata of its tokens, then moe_ep_pack: send_rows [P*C, H]
+ *      (block q: the rows of rank q's experts in routed order, from place 0),
+ *      send_w [P*C] their routing weights, send_counts [P, E_loc] the rows of
+ *      each expert that were sent.
+ *   2. the caller exchanges the counts, rows and weights (equal splits).
+ *   3. moe_ep_receive_metadata on a second workspace, shaped (T = P*C, k = 1,
+ *      E = E_loc, H, I), from the received counts; then moe_dispatch_gemm1 and
+ *      moe_swiglu_gemm2_combine on the received rows with the received weights
+ *      as topk_w [P*C, 1]: y_recv [P*C, H] holds each received row's weighted
+ *      output at the place it arrived (zero where nothing arrived).
+ *   4. the caller returns y_recv (equal splits), and moe_ep_combine sums each
+ *      token's returned rows into y.
+ * Places not filled by a sender are never read as rows of a token.
+ */
+
+/* Step 1 (sender). x bf16 [T,H], topk_w fp32 [T,k]; the metadata of
+ * moe_routing_metadata for `shape` in ws. Rows past `capacity` in a block are
+ * dropped and flag MOE_DEVERR_CAPACITY. n_ranks must divide E. */
+moe_status_t moe_ep_pack(const void *x, const float *topk_w, const moe_shape_t *shape, int32_t n_ranks,
+                         int64_t capacity, void *send_rows, float *send_w, int32_t *send_counts, void *ws,
+                         size_t ws_bytes, void *stream);
+
+/* Step 3 (receiver): the routing metadata of the received rows, from
+ * recv_counts int32 [n_ranks, E_loc] (row p: what source p sent), into ws for
+ * recv_shape = (T = n_ranks * capacity, k = 1, E = E_loc, H, I). Received row
+ * p*C + i is a token with one slot; the routed order is expert-major, then
+ * source, then place (the order moe_routing_metadata gives for those slots). */
+moe_status_t moe_ep_receive_metadata(const int32_t *recv_counts, int32_t n_ranks, int64_t capacity,
+                                     const moe_shape_t *recv_shape, void *ws, size_t ws_bytes, void *stream);
+
+/* Step 4 (sender): y[t] = sum over the token's slots of back_rows[place of the
+ * slot's row] (fp32 in slot order, bf16 y [T,H], fully written). back_rows
+ * bf16 [n_ranks*capacity, H]; the metadata of step 1 in ws. */
+moe_status_t moe_ep_combine(const void *back_rows, const moe_shape_t *shape, int32_t n_ranks, int64_t capacity,
+                            void *y, void *ws, size_t ws_bytes, void *stream);
 
 /* ------------------------------------------------------------------ training
  *
@@ -481,6 +529,51 @@ moe_status_t moe_forward_mx(const void *x, const int32_t *topk_idx, const float 
                             const void *w1_codes, const void *w1_scales, const void *w2_codes,
                             const void *w2_scales, const moe_shape_t *shape, void *y, void *ws,
                             size_t ws_bytes, void *stream);
+
+/* ------------------------------------------------------------------ MXFP8 training
+ *
+ * The guide's mxfp8 also runs the dW1 / dW2 weight gradients in MXFP8
+ * (section "Expert precision"). A training step in MXFP8 runs, on one
+ * workspace sized with flags = MOE_SHAPE_TRAINING | MOE_SHAPE_MXFP8:
+ * moe_router_train, moe_routing_metadata, moe_mx_quantize_dispatch,
+ * moe_dispatch_gemm1_mx_train, moe_swiglu_gemm2_combine_mx, then
+ * moe_backward_stage2_data (bf16 w2), moe_backward_stage2_weight_mx,
+ * moe_router_backward, moe_backward_stage1_data (bf16 w1) and
+ * moe_backward_stage1_weight_mx. The data gradients are those of the bf16
+ * backward at the MXFP8 forward's pre-activation h (quantization passes the
+ * gradient through); the weight gradients quantize both operands to MXFP8
+ * along their reduction dimension, the expert's routed rows: blocks of 32
+ * consecutive routed rows of the expert from its first row (the last block
+ * zero-padded), with the routing weight on the activation side:
+ *   dW2[e] = Q(dY rows)^T Q(w a rows),   dW1[e] = Q(dH rows)^T Q(x rows).
+ * H and I must be multiples of 128.
+ */
+
+/*
+ * moe_dispatch_gemm1_mx that also stores the pre-activation h [T*k, 2I] bf16
+ * (routed order; the fp32 accumulator of the MXFP8 GEMM rounded to bf16) for
+ * moe_backward_stage2_data.
+ */
+moe_status_t moe_dispatch_gemm1_mx_train(const void *w1_codes, const void *w1_scales, const moe_shape_t *shape,
+                                         void *a_codes, void *a_scales, void *h, void *ws, size_t ws_bytes,
+                                         void *stream);
+
+/*
+ * dW2[e] = Q(dY rows of e)^T Q(w a rows of e) into dw2 bf16 [E,H,I] (experts
+ * without rows get 0), fp32 accumulation of the block-scaled products. Needs
+ * moe_backward_stage2_data on this workspace (its routed-order dY rows and w a);
+ * dy is only checked for NULL and alignment.
+ */
+moe_status_t moe_backward_stage2_weight_mx(const void *dy, const moe_shape_t *shape, void *dw2, void *ws,
+                                           size_t ws_bytes, void *stream);
+
+/*
+ * dW1[e] = Q(dH rows of e)^T Q(x rows of e) into dw1 bf16 [E,2I,H]. x bf16
+ * [T,H] (the tensor of the forward); needs moe_backward_stage2_data on this
+ * workspace (dH).
+ */
+moe_status_t moe_backward_stage1_weight_mx(const void *x, const moe_shape_t *shape, void *dw1, void *ws,
+                                           size_t ws_bytes, void *stream);
 
 /*
  * Wait for `stream`, then read and clear the workspace error word into *code.

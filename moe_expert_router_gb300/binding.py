@@ -21,6 +21,7 @@ STATUS_NAMES = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED",
                 3: "MOE_ERR_CUDA", 4: "MOE_ERR_WORKSPACE", 5: "MOE_ERR_DEVICE_FLAGGED"}
 DEVERR_BAD_EXPERT_INDEX = 0x1
 DEVERR_WAIT_TIMEOUT = 0x2
+DEVERR_CAPACITY = 0x4
 SCORE_SOFTMAX = 0
 SCORE_SIGMOID = 1
 SHAPE_TRAINING = 0x1
@@ -48,8 +49,8 @@ class RouterCfg(ctypes.Structure):
 class WsLayout(ctypes.Structure):
     _fields_ = [(n, ctypes.c_size_t) for n in
                 ("err", "counts", "offsets", "mt_prefix", "perm_slot", "row_of", "meta", "router", "a",
-                 "obuf", "dh", "aw", "dtw_part", "dlogits", "xp", "dyp", "dwr_part", "x_codes", "x_scales", "a_codes", "a_scales",
-                 "total")]
+                 "obuf", "combine", "dh", "aw", "dtw_part", "dlogits", "xp", "dyp", "dwr_part", "x_codes", "x_scales", "a_codes", "a_scales",
+                 "mx_wgrad", "total")]
 
 
 # name -> argument types (all return moe_status_t unless listed in _RESTYPES)
@@ -84,10 +85,18 @@ _SIG = {
     "moe_mx_quantize": [_P, ctypes.c_int64, ctypes.c_int64, _P, _P, _P],
     "moe_mx_quantize_dispatch": [_P, ctypes.POINTER(Shape), _P, ctypes.c_size_t, _P],
     "moe_dispatch_gemm1_mx": [_P, _P, ctypes.POINTER(Shape), _P, _P, _P, ctypes.c_size_t, _P],
+    "moe_dispatch_gemm1_mx_train": [_P, _P, ctypes.POINTER(Shape), _P, _P, _P, _P, ctypes.c_size_t, _P],
+    "moe_backward_stage2_weight_mx": [_P, ctypes.POINTER(Shape), _P, _P, ctypes.c_size_t, _P],
+    "moe_backward_stage1_weight_mx": [_P, ctypes.POINTER(Shape), _P, _P, ctypes.c_size_t, _P],
     "moe_swiglu_gemm2_combine_mx": [_P, _P, _P, _P, _P, ctypes.POINTER(Shape), _P, _P, ctypes.c_size_t, _P],
     "moe_forward_mx": [_P, _P, _P, _P, _P, _P, _P, ctypes.POINTER(Shape), _P, _P, ctypes.c_size_t, _P],
     "moe_dispatch_rows": [_P, _P, ctypes.POINTER(Shape), _P, _P, _P, ctypes.c_size_t, _P],
     "moe_combine_rows": [_P, ctypes.POINTER(Shape), _P, _P, ctypes.c_size_t, _P],
+    "moe_ep_pack": [_P, _P, ctypes.POINTER(Shape), ctypes.c_int32, ctypes.c_int64, _P, _P, _P, _P,
+                    ctypes.c_size_t, _P],
+    "moe_ep_receive_metadata": [_P, ctypes.c_int32, ctypes.c_int64, ctypes.POINTER(Shape), _P, ctypes.c_size_t,
+                                _P],
+    "moe_ep_combine": [_P, ctypes.POINTER(Shape), ctypes.c_int32, ctypes.c_int64, _P, _P, ctypes.c_size_t, _P],
     "moe_packed_weights_size": [ctypes.POINTER(Shape), ctypes.POINTER(ctypes.c_size_t),
                                 ctypes.POINTER(ctypes.c_size_t)],
     "moe_pack_weights": [_P, _P, ctypes.POINTER(Shape), _P, _P, _P],
@@ -313,6 +322,22 @@ def moe_dispatch_gemm1_mx(w1q, w1s, shp, aq, as_, ws, stream=None):
         _stream(stream, ws)))
 
 
+def moe_dispatch_gemm1_mx_train(w1q, w1s, shp, aq, as_, h, ws, stream=None):
+    _check("moe_dispatch_gemm1_mx_train", load().moe_dispatch_gemm1_mx_train(
+        _ptr(w1q), _ptr(w1s), ctypes.byref(shp), _ptr(aq), _ptr(as_), _ptr(h), _ptr(ws), _nbytes(ws),
+        _stream(stream, ws)))
+
+
+def moe_backward_stage2_weight_mx(dy, shp, dw2, ws, stream=None):
+    _check("moe_backward_stage2_weight_mx", load().moe_backward_stage2_weight_mx(
+        _ptr(dy), ctypes.byref(shp), _ptr(dw2), _ptr(ws), _nbytes(ws), _stream(stream, ws)))
+
+
+def moe_backward_stage1_weight_mx(x, shp, dw1, ws, stream=None):
+    _check("moe_backward_stage1_weight_mx", load().moe_backward_stage1_weight_mx(
+        _ptr(x), ctypes.byref(shp), _ptr(dw1), _ptr(ws), _nbytes(ws), _stream(stream, ws)))
+
+
 def moe_swiglu_gemm2_combine_mx(aq, as_, topk_w, w2q, w2s, shp, y, ws, stream=None):
     _check("moe_swiglu_gemm2_combine_mx", load().moe_swiglu_gemm2_combine_mx(
         _ptr(aq), _ptr(as_), _ptr(topk_w), _ptr(w2q), _ptr(w2s), ctypes.byref(shp), _ptr(y), _ptr(ws),
@@ -330,6 +355,27 @@ def moe_dispatch_rows(x, shp, rows, ws, topk_w=None, row_weight=None, stream=Non
     send buffer of an expert-parallel dispatch."""
     _check("moe_dispatch_rows", load().moe_dispatch_rows(
         _ptr(x), _ptr(topk_w), ctypes.byref(shp), _ptr(rows), _ptr(row_weight), _ptr(ws), _nbytes(ws),
+        _stream(stream, ws)))
+
+
+def moe_ep_pack(x, topk_w, shp, n_ranks, capacity, send_rows, send_w, send_counts, ws, stream=None):
+    """Expert parallelism, sender: fixed-size send blocks of capacity rows per rank."""
+    _check("moe_ep_pack", load().moe_ep_pack(
+        _ptr(x), _ptr(topk_w), ctypes.byref(shp), int(n_ranks), int(capacity), _ptr(send_rows), _ptr(send_w),
+        _ptr(send_counts), _ptr(ws), _nbytes(ws), _stream(stream, ws)))
+
+
+def moe_ep_receive_metadata(recv_counts, n_ranks, capacity, recv_shp, ws, stream=None):
+    """Expert parallelism, receiver: routing metadata of the received blocks from their counts."""
+    _check("moe_ep_receive_metadata", load().moe_ep_receive_metadata(
+        _ptr(recv_counts), int(n_ranks), int(capacity), ctypes.byref(recv_shp), _ptr(ws), _nbytes(ws),
+        _stream(stream, ws)))
+
+
+def moe_ep_combine(back_rows, shp, n_ranks, capacity, y, ws, stream=None):
+    """Expert parallelism, sender: the sum of each token's returned rows."""
+    _check("moe_ep_combine", load().moe_ep_combine(
+        _ptr(back_rows), ctypes.byref(shp), int(n_ranks), int(capacity), _ptr(y), _ptr(ws), _nbytes(ws),
         _stream(stream, ws)))
 
 

@@ -96,22 +96,25 @@ enum Mode : int {
     kBwdDA = 3, kBwdDX = 4, kBwdDW2 = 5, kBwdDW1 = 6,
     kStage1SaveH = 7,           // stage 1 that also stores h for the backward
     kStage1Mx = 8,              // stage 1 in MXFP8: E4M3 x and w1, a quantized in the epilogue
-    kStage2Mx = 9               // stage 2 in MXFP8: E4M3 a and w2
+    kStage2Mx = 9,              // stage 2 in MXFP8: E4M3 a and w2
+    kWgradMx = 10               // MXFP8 weight gradient: operands quantized along the expert's routed rows
 };
 
-template <int MODE> constexpr bool kIsMx = MODE == kStage1Mx || MODE == kStage2Mx;
+template <int MODE> constexpr bool kIsMx = MODE == kStage1Mx || MODE == kStage2Mx || MODE == kWgradMx;
 template <int MODE> constexpr bool kIsStage1 = MODE == kStage1 || MODE == kStage1SaveH || MODE == kStage1Mx;
 template <int MODE> constexpr bool kRing = MODE == kStage1 || MODE == kStage2;
 template <int MODE> constexpr bool kAMn = MODE == kBwdDW2 || MODE == kBwdDW1;
 template <int MODE> constexpr bool kBMn = MODE >= kBwdDA && MODE <= kBwdDW1;
 template <int MODE> constexpr bool kWeightGrad = MODE == kBwdDW2 || MODE == kBwdDW1;
+// units (expert, m-tile, n-tile) reducing over the expert's rows, written per expert
+template <int MODE> constexpr bool kPerExpertOut = kWeightGrad<MODE> || MODE == kWgradMx;
 // warps 10..13: the reduction-tail zeroing of the weight gradients, and in the
 // MXFP8 modes the scale factors
 template <int MODE> constexpr bool kHelpers = kWeightGrad<MODE> || kIsMx<MODE>;
 // accumulator columns of one 128-row half (a unit's output columns): 2 x 96
 // (gate, up) in stage 1 MXFP8, 224 in stage 2 MXFP8, else 256; the MXFP8 modes
 // keep the rest of tensor memory for per-stage scale factors
-template <int MODE> constexpr int kUnitN = MODE == kStage1Mx ? 192 : (MODE == kStage2Mx ? 224 : BN);
+template <int MODE> constexpr int kUnitN = MODE == kStage1Mx ? 192 : ((MODE == kStage2Mx || MODE == kWgradMx) ? 224 : BN);
 // K elements per pipeline stage (128-byte rows either way)
 template <int MODE> constexpr int kStageK = kIsMx<MODE> ? 128 : BK;
 template <int MODE> constexpr int kElemBytes = kIsMx<MODE> ? 1 : 2;
@@ -170,6 +173,9 @@ struct GemmArgs {
     int32_t *err;
     int32_t *sched;             // [0] next unit, [1] CTAs finished
     const float *topk_w;
+    const int32_t *row_of;      // stage 2, fused combine: routed row of each slot (-1: dropped)
+    __nv_bfloat16 *y;           // stage 2, fused combine: y [T, H]
+    int32_t *ccnt;              // stage 2, fused combine: counters [T, n_tiles], or null (combine kernel)
     __nv_bfloat16 *out;         // masked direct stores of partial row slabs
     __nv_bfloat16 *out2, *out3; // kStage1SaveH: h gate / up halves; dA: dH up half, w a
     float *logits_part;         // router
@@ -190,6 +196,9 @@ struct GemmArgs {
                                 //   3 router_seg with the parts fused)
     int router_seg;             // router: accumulator columns of each of the hi / mid / lo parts when one
                                 //   MMA covers all three (E <= 64), else 0
+    int gather_a;               // stage 1: A rows gathered from x by token (maps.a: box one row high)
+    const int32_t *kpad;        // MXFP8 weight gradients: [E+1] start of each expert's rows in the
+                                //   quantized operands, a multiple of 128 (rows padded to whole k-blocks)
     const uint8_t *bpack;       // stage 1 / 2: the tile-packed weights (pack.cu), or null for the TMA views
     int kb_tiles;               // K tiles per packed weight slab
     int total_units;            // router / weight gradients: known on the host; else -1
@@ -216,6 +225,20 @@ __device__ __forceinline__ Unit decode_unit(int u, const GemmArgs &g) {
         t.rows = min(UM, g.T - t.row0);
         t.kb0 = t.split * g.kb_per_split;
         t.kb1 = min(g.kb_total, t.kb0 + g.kb_per_split);
+    } else if constexpr (MODE == kWgradMx) {
+        // K runs over the expert's rows in the quantized operands: k-blocks of 128
+        // rows from kpad[e] (a multiple of 128), rows past the count are zero codes
+        const int per_e = g.m_tiles * g.n_tiles;
+        t.e = u / per_e;
+        const int rem = u - t.e * per_e;
+        const int m = rem / g.n_tiles;
+        t.n = rem - m * g.n_tiles;
+        t.row0 = m * UM;
+        t.rows = min(UM, g.m_total - t.row0);
+        t.kcount = g.counts[t.e];
+        t.kb0 = g.kpad[t.e] / kStageK<MODE>;
+        t.kb1 = t.kb0 + (t.kcount + kStageK<MODE> - 1) / kStageK<MODE>;
+        t.split = 0;
     } else if constexpr (kWeightGrad<MODE>) {
         const int per_e = g.m_tiles * g.n_tiles;
         t.e = u / per_e;
@@ -323,6 +346,75 @@ __device__ __forceinline__ void store_row32(__nv_bfloat16 *dst, int cols_left, c
             *reinterpret_cast<uint4 *>(dst + j * 8) = make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
 }
 
+// ---------------------------------------------------------------- fused combine (stage 2)
+
+// The k-way sum of grouped_gemm_combine, fused into stage 2's epilogue. Each
+// weighted expert row r (token t) is first stored to obuf; then the warp counts
+// it in cnt[t, n] (n: the unit's 256-column tile), which the routing metadata
+// set to the token's number of dropped slots. The lane whose row brings the
+// counter to k owns the sum: the warp reads the token's k rows of that tile back
+// (L2) and writes y[t, tile] = sum_j obuf[row_of[t k + j], tile] in fp32, in
+// slot order, rounded to bf16 once -- the same arithmetic, in the same order,
+// as combine_kernel, wherever and whenever the last row lands. It then resets
+// the counter, so the metadata serve a later stage-2 call as well.
+// Call with the warp converged, after this thread's rows of the unit are
+// stored and visible (a generic store, or a completed bulk store followed by
+// fence_proxy_async_global); `valid` and `tok` describe this lane's row.
+__device__ __forceinline__ void fused_combine(const GemmArgs &g, int n, int col0, bool valid, int tok, int lane) {
+    __threadfence();                                   // release: this row before the count
+    bool last = false;
+    if (valid) last = atomicAdd(&g.ccnt[static_cast<int64_t>(tok) * g.n_tiles + n], 1) == g.k - 1;
+    unsigned done = __ballot_sync(0xffffffffu, last);
+    if (done == 0u) return;
+    __threadfence();                                   // acquire: the token's other rows
+    const int c = col0 + 8 * lane;                     // 8 columns per lane, 256 per warp
+    const bool live = c < g.n_out;
+    while (done != 0u) {
+        const int src = __ffs(done) - 1;
+        done &= done - 1u;
+        const int t = __shfl_sync(0xffffffffu, tok, src);
+        const int my_row = lane < g.k ? __ldg(&g.row_of[static_cast<int64_t>(t) * g.k + lane]) : -1;
+        const int n_valid = __popc(__ballot_sync(0xffffffffu, my_row >= 0));
+        float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        for (int j0 = 0; j0 < g.k; j0 += 8) {
+            uint4 v[8];
+#pragma unroll
+            for (int jj = 0; jj < 8; ++jj) {
+                const int r = __shfl_sync(0xffffffffu, my_row, (j0 + jj) & 31);
+                v[jj] = (live && j0 + jj < g.k && r >= 0)
+                            ? ld_cg_v4(g.out + static_cast<int64_t>(r) * g.n_out + c)
+                            : make_uint4(0u, 0u, 0u, 0u);
+            }
+#pragma unroll
+            for (int jj = 0; jj < 8; ++jj) {
+                const uint32_t w[4] = {v[jj].x, v[jj].y, v[jj].z, v[jj].w};
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    acc[2 * q] += bf16_lo(w[q]);
+                    acc[2 * q + 1] += bf16_hi(w[q]);
+                }
+            }
+        }
+        if (live)
+            *reinterpret_cast<uint4 *>(g.y + static_cast<int64_t>(t) * g.n_out + c) =
+                make_uint4(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]), pack_bf16x2(acc[4], acc[5]),
+                           pack_bf16x2(acc[6], acc[7]));
+        if (lane == src) g.ccnt[static_cast<int64_t>(t) * g.n_tiles + n] = g.k - n_valid;
+    }
+}
+
+// Tokens whose every slot was dropped get no row, so no count: their y rows are
+// zeroed here (threads first, first + stride, ... over the tokens).
+__device__ __forceinline__ void zero_dropped_tokens(const GemmArgs &g, int first, int stride) {
+    for (int t = first; t < g.T; t += stride) {
+        bool any = false;
+        for (int j = 0; j < g.k; ++j) any |= __ldg(&g.row_of[static_cast<int64_t>(t) * g.k + j]) >= 0;
+        if (any) continue;
+        uint4 *dst = reinterpret_cast<uint4 *>(g.y + static_cast<int64_t>(t) * g.n_out);
+        for (int c = 0; c < g.n_out / 8; ++c) dst[c] = make_uint4(0u, 0u, 0u, 0u);
+    }
+}
+
 // ---------------------------------------------------------------- epilogue pieces
 
 // Stage 1: the SwiGLU of accumulator columns [c, c+32) (gate) and
@@ -420,6 +512,8 @@ __device__ __forceinline__ void scale_rows(const GemmArgs &g, const Unit &t, int
             if (j < 6 && c < g.n_out)
                 b_off[j] = (static_cast<int64_t>(t.e) * g.b_rows + c + (j >= 3 ? g.half : 0)) * ld;
         } else {
+            // stage 2: weight rows of expert e; weight gradients (b_rows = 0): rows of
+            // the quantized operand, shared by every expert
             const int c = t.n * kUnitN<MODE> + 32 * j + lane;
             if (j < 7 && c < g.n_out) b_off[j] = (static_cast<int64_t>(t.e) * g.b_rows + c) * ld;
         }
@@ -475,7 +569,7 @@ tc_gemm_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs g) {
 
     if (warp == 0) {
         // ------------------------------------------------ scheduler + TMA producer
-        const int total = (MODE == kRouter || kWeightGrad<MODE>) ? g.total_units : g.mt_prefix[g.E] * g.n_tiles;
+        const int total = (MODE == kRouter || kPerExpertOut<MODE>) ? g.total_units : g.mt_prefix[g.E] * g.n_tiles;
         int stage = 0, issued = 0, q = 0;
         uint32_t phase = 0, qphase = 0;
         bool ok = true;
@@ -506,6 +600,18 @@ tc_gemm_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs g) {
 
             const Unit t = decode_unit<MODE>(u, g);
             const bool two = t.rows > BM;            // second half present
+            // stage 1 with the gathered dispatch: this lane's eight rows 8 lane .. 8 lane + 7
+            // of the unit, as token indices (rows past the count repeat the first row)
+            int tok8[8];
+            if constexpr (MODE == kStage1) {
+                if (g.gather_a) {
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        const int r = 8 * lane + j;
+                        tok8[j] = __ldg(&g.perm_slot[t.row0 + (r < t.rows ? r : 0)]) / g.k;
+                    }
+                }
+            }
             // one or two 128-row halves of A (K-major rows or MN-major atoms) and the B tile
             const uint32_t a_bytes = unit_a_bytes(t);
             const uint32_t tx_bytes = a_bytes + (MODE == kRouter ? g.n_mma : kUnitN<MODE>) * 128;
@@ -551,14 +657,30 @@ tc_gemm_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs g) {
                     sa = smem_addr(sm.a[stage]);
                     sb = smem_addr(sm.b[stage]);
                 }
+                if constexpr (MODE == kStage1) {
+                    if (g.gather_a) {
+                        // the dispatch fused into the load: four x rows per gather, the
+                        // warp's lanes covering the unit's rows (after lane 0's expect_tx)
+                        if (lane == 0) mbar_arrive_expect_tx(full, tx_bytes);
+                        __syncwarp();
+                        if (8 * lane < (two ? UM : BM)) {
+                            const int kx = kb * kStageK<MODE>;
+                            const uint32_t dst = sa + 8 * lane * ROW_BYTES;
+                            tma_gather4(dst, &maps.a, kx, tok8[0], tok8[1], tok8[2], tok8[3], full);
+                            tma_gather4(dst + 4 * ROW_BYTES, &maps.a, kx, tok8[4], tok8[5], tok8[6], tok8[7], full);
+                        }
+                    }
+                }
                 if (lane == 0) {
-                    mbar_arrive_expect_tx(full, tx_bytes);
+                    if (!(MODE == kStage1 && g.gather_a)) mbar_arrive_expect_tx(full, tx_bytes);
                     if constexpr (kIsStage1<MODE>) {
                         constexpr int hn = kUnitN<MODE> / 2;                                 // gate (= up) rows
                         const int row = t.e * g.b_rows + t.n * hn;
                         const int kx = kb * kStageK<MODE>;
-                        tma_load_2d(sa, &maps.a, kx, t.row0, full);                         // dispatched x rows
-                        if (two) tma_load_2d(sa + A_HALF_BYTES, &maps.a, kx, t.row0 + BM, full);
+                        if (!(MODE == kStage1 && g.gather_a)) {
+                            tma_load_2d(sa, &maps.a, kx, t.row0, full);                     // dispatched x rows
+                            if (two) tma_load_2d(sa + A_HALF_BYTES, &maps.a, kx, t.row0 + BM, full);
+                        }
                         if (MODE == kStage1 && g.bpack != nullptr) {                        // packed gate + up slab
                             bulk_load(sb, g.bpack + ((static_cast<int64_t>(t.e) * g.n_tiles + t.n) * g.kb_tiles + kb) *
                                                         B_BYTES, B_BYTES, full);
@@ -566,6 +688,13 @@ tc_gemm_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs g) {
                             tma_load_2d(sb, &maps.b, kx, row, full);                        // gate rows
                             tma_load_2d(sb + hn * 128, &maps.b, kx, row + g.half, full);    // up rows
                         }
+                    } else if constexpr (MODE == kWgradMx) {
+                        // rows of the m-tile / n-tile of the two quantized operands, K = the
+                        // k-block's 128 rows of the expert (absolute column of the operands)
+                        const int kx = kb * kStageK<MODE>;
+                        tma_load_2d(sa, &maps.a, kx, t.row0, full);
+                        if (two) tma_load_2d(sa + A_HALF_BYTES, &maps.a, kx, t.row0 + BM, full);
+                        tma_load_2d(sb, &maps.b, kx, t.n * kUnitN<MODE>, full);
                     } else if constexpr (MODE == kStage2 || MODE == kStage2Mx) {
                         const int kx = kb * kStageK<MODE>;
                         tma_load_2d(sa, &maps.a, kx, t.row0, full);
@@ -743,6 +872,10 @@ tc_gemm_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs g) {
         uint32_t boxes = 0;                         // 32 x 32 boxes stored so far (ping-pong halves)
         int q = 0;
         uint32_t acc_phase = 0, qphase = 0;
+        if constexpr (MODE == kStage2) {
+            if (g.ccnt != nullptr)
+                zero_dropped_tokens(g, blockIdx.x * EPI_THREADS + (threadIdx.x - 64), gridDim.x * EPI_THREADS);
+        }
         while (true) {
             bool ok = true;
             int u = -1;
@@ -760,8 +893,11 @@ tc_gemm_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs g) {
             const Unit t = decode_unit<MODE>(u, g);
             const bool valid = row < t.rows;
             float w = 1.0f;                             // routing weight of the row's slot
+            int tok = -1;                               // stage 2: the row's token (fused combine)
             if constexpr (MODE == kStage2 || MODE == kBwdDA || MODE == kStage2Mx) {
-                w = valid ? g.topk_w[g.perm_slot[t.row0 + row]] : 0.0f;
+                const int slot = valid ? g.perm_slot[t.row0 + row] : 0;
+                w = valid ? g.topk_w[slot] : 0.0f;
+                tok = valid ? slot / g.k : -1;
             }
             // dA: the saved h (gate and up) of the row's first 32 columns, loaded while
             // the unit's MMAs still run; each later piece's h is loaded before the
@@ -794,6 +930,17 @@ tc_gemm_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs g) {
                         tmem_wait_ld();
                         tmem_reg_fence(gv);
                         tmem_reg_fence(uv);
+                        if (g.out2 != nullptr && valid) {
+                            // training: the pre-activation h (gate and up halves, bf16) for the backward
+                            uint32_t pg[16], pu[16];
+#pragma unroll
+                            for (int i = 0; i < 16; ++i) {
+                                pg[i] = pack_bf16x2(__uint_as_float(gv[2 * i]), __uint_as_float(gv[2 * i + 1]));
+                                pu[i] = pack_bf16x2(__uint_as_float(uv[2 * i]), __uint_as_float(uv[2 * i + 1]));
+                            }
+                            store_row32(g.out2 + r * g.out_ld + col0 + c, g.n_out - col0 - c, pg);
+                            store_row32(g.out3 + r * g.out_ld + col0 + c, g.n_out - col0 - c, pu);
+                        }
                         float av[32];
 #pragma unroll
                         for (int i = 0; i < 32; ++i) av[i] = silu_mul(__uint_as_float(gv[i]), __uint_as_float(uv[i]));
@@ -933,13 +1080,23 @@ tc_gemm_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs g) {
                             fence_proxy_async_smem();
                             __syncwarp();
                             if (lane == 0) {
-                                // stage 2's weighted rows are read again by the combine right
-                                // after this kernel: keep them in L2 ahead of the weight stream
+                                // stage 2's weighted rows are read again by the combine: keep
+                                // them in L2 ahead of the weight stream
                                 if constexpr (MODE == kStage2)
                                     tma_store_2d_hint(&maps.out, buf, col0 + 64 * b, y, l2_policy_evict_last());
                                 else
                                     tma_store_2d(&maps.out, buf, col0 + 64 * b, y);
                                 bulk_commit();
+                            }
+                        }
+                        if constexpr (MODE == kStage2) {
+                            if (g.ccnt != nullptr) {
+                                if (lane == 0) {
+                                    bulk_wait<0>();                 // the slab's rows are in global memory
+                                    fence_proxy_async_global();
+                                }
+                                __syncwarp();
+                                fused_combine(g, t.n, col0, valid, tok, lane);
                             }
                         }
                     } else {
@@ -961,6 +1118,10 @@ tc_gemm_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs g) {
 #pragma unroll
                                 for (int p = 0; p < NPIECE; ++p)
                                     if (col0 + 32 * p < g.n_out) store_row32(dst + 32 * p, g.n_out - col0 - 32 * p, pk[p]);
+                            }
+                            if (g.ccnt != nullptr) {
+                                __syncwarp();
+                                fused_combine(g, t.n, col0, valid, tok, lane);
                             }
                         } else {
 #pragma unroll 1
@@ -1039,16 +1200,17 @@ tc_gemm_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs g) {
                         }
                     }
                     if (valid) g.dtw_part[static_cast<int64_t>(t.n) * g.R + r] = dtw;
-                } else if constexpr (kWeightGrad<MODE>) {
+                } else if constexpr (kPerExpertOut<MODE>) {
                     // dW rows t.row0 + row of expert e, 32 x 32 boxes through a 3-D map
                     // (rows past m_total and columns past n_out are clipped by the store),
                     // staged in the two halves of the warp's buffer in turn, so staging a
                     // box waits only for the one two boxes back to be read out
-                    const int col0 = t.n * BN;
-                    const bool empty = t.kb1 == 0;      // expert without rows: zeros
+                    constexpr int NC = kUnitN<MODE>;
+                    const int col0 = t.n * NC;
+                    const bool empty = t.kb1 == t.kb0;  // expert without rows: zeros
                     if (slab0 < t.rows) {
 #pragma unroll 1
-                        for (int c = 0; c < BN; c += 32) {
+                        for (int c = 0; c < NC; c += 32) {
                             if (col0 + c >= g.n_out) break;
                             uint32_t pk[16];
                             if (empty) {
@@ -1220,6 +1382,10 @@ inline GemmArgs grouped_args(const GemmLaunch &p) {
     g.err = p.err;
     g.sched = p.sched;
     g.topk_w = p.topk_w;
+    g.row_of = p.row_of;
+    g.y = p.y;
+    g.ccnt = p.ccnt;
+    g.T = p.T;
     g.out = p.out;
     g.out2 = p.out2;
     g.out3 = p.out3;
@@ -1228,6 +1394,8 @@ inline GemmArgs grouped_args(const GemmLaunch &p) {
     g.sfb = p.sfb;
     g.out_sf = p.out_sf;
     g.bpack = p.bpack;
+    g.gather_a = p.gather_a;
+    g.kpad = p.kpad;
     g.kb_tiles = (p.K + BK - 1) / BK;
     g.E = p.E;
     g.k = p.k;

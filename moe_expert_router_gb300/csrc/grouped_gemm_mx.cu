@@ -75,7 +75,114 @@ mx_quantize_dispatch_kernel(const __nv_bfloat16 *__restrict__ x, const int32_t *
     }
 }
 
+// Row offsets of the MXFP8 weight-gradient operands: expert e's rows start at
+// kpad[e], a multiple of 128 (one k-block of the block-scaled MMA), so each
+// expert's reduction covers whole k-blocks; kpad[e+1] - kpad[e] =
+// ceil(counts[e] / 128) * 128. One warp: a running sum over the experts in
+// chunks of 32.
+__global__ void __launch_bounds__(32) mx_wgrad_offsets_kernel(const int32_t *__restrict__ counts, int E,
+                                                              int32_t *__restrict__ kpad) {
+    griddep_wait();
+    const int lane = threadIdx.x;
+    int base = 0;
+    if (lane == 0) kpad[0] = 0;
+    for (int e0 = 0; e0 < E; e0 += 32) {
+        const int e = e0 + lane;
+        int v = (e < E) ? (counts[e] + 127) / 128 * 128 : 0;
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) {
+            const int o = __shfl_up_sync(0xffffffffu, v, d);
+            if (lane >= d) v += o;
+        }
+        if (e < E) kpad[e + 1] = base + v;
+        base += __shfl_sync(0xffffffffu, v, 31);
+    }
+}
+
+// The operands of an MXFP8 weight gradient, quantized along the expert's routed
+// rows (the GEMM's reduction dimension) and stored transposed, K-major:
+// codes [C, ld] and scales [C, ld / 32], where column r of expert e's segment
+// [kpad[e], kpad[e+1]) holds routed row offsets[e] + (r - kpad[e]) of the
+// source (zero past the expert's count). Source row of routed row q: src[q, :]
+// (row stride src_ld), or with perm_slot the token's row src[perm_slot[q] / k, :].
+// One CTA per 32-row block and 256 columns: the block's rows are staged in
+// shared memory, then each thread quantizes one column's 32 values.
+constexpr int kQtCols = 256;
+__global__ void __launch_bounds__(kQtCols)
+mx_quantize_rows_t_kernel(const __nv_bfloat16 *__restrict__ src, int64_t src_ld, const int32_t *__restrict__ perm_slot,
+                          int k, const int32_t *__restrict__ counts, const int32_t *__restrict__ offsets,
+                          const int32_t *__restrict__ kpad, int E, int C, int64_t ld, uint8_t *__restrict__ codes,
+                          uint8_t *__restrict__ scales) {
+    __shared__ uint32_t tile[32][kQtCols / 2 + 1];   // 32 rows x 256 bf16, padded against bank conflicts
+    griddep_wait();
+    const int64_t r0 = static_cast<int64_t>(blockIdx.x) * 32;   // first padded row of the block
+    if (r0 >= kpad[E]) return;                                   // past every expert's segment
+    int lo = 0, hi = E;                                          // expert with kpad[e] <= r0 < kpad[e+1]
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (kpad[mid] <= r0) lo = mid; else hi = mid;
+    }
+    const int e = lo;
+    const int local = static_cast<int>(r0 - kpad[e]);           // row of the expert's segment
+    const int c0 = blockIdx.y * kQtCols;
+    // stage: row i of the block, columns [c0, c0 + 256): 16-byte loads, 8 threads per 128 columns
+    for (int i = threadIdx.x; i < 32 * (kQtCols / 8); i += blockDim.x) {
+        const int row = i / (kQtCols / 8);
+        const int cc = (i % (kQtCols / 8)) * 8;
+        uint4 v = make_uint4(0u, 0u, 0u, 0u);
+        if (local + row < counts[e] && c0 + cc < C) {
+            const int64_t q = offsets[e] + local + row;
+            const int64_t srow = perm_slot ? perm_slot[q] / k : q;
+            v = __ldg(reinterpret_cast<const uint4 *>(src + srow * src_ld + c0 + cc));
+        }
+        tile[row][cc / 2] = v.x;
+        tile[row][cc / 2 + 1] = v.y;
+        tile[row][cc / 2 + 2] = v.z;
+        tile[row][cc / 2 + 3] = v.w;
+    }
+    __syncthreads();
+    const int c = c0 + threadIdx.x;
+    if (c >= C) return;
+    float v[32];
+#pragma unroll
+    for (int row = 0; row < 32; ++row) {
+        const uint32_t w = tile[row][threadIdx.x / 2];
+        v[row] = (threadIdx.x & 1) ? bf16_hi(w) : bf16_lo(w);
+    }
+    uint32_t qw[8];
+    const uint32_t sc = mx_quantize32(v, qw);
+    uint4 *dst = reinterpret_cast<uint4 *>(codes + static_cast<int64_t>(c) * ld + r0);
+    dst[0] = make_uint4(qw[0], qw[1], qw[2], qw[3]);
+    dst[1] = make_uint4(qw[4], qw[5], qw[6], qw[7]);
+    scales[static_cast<int64_t>(c) * (ld / 32) + r0 / 32] = static_cast<uint8_t>(sc);
+}
+
 }  // namespace
+
+cudaError_t launch_mx_wgrad_offsets(const int32_t *counts, int E, int32_t *kpad, cudaStream_t st) {
+    const cudaError_t e = launch_dep(mx_wgrad_offsets_kernel, dim3(1), dim3(32), 0, st, counts, E, kpad);
+    note_launches(1);
+    return e;
+}
+
+cudaError_t launch_mx_quantize_rows_t(const __nv_bfloat16 *src, int64_t src_ld, const int32_t *perm_slot, int k,
+                                      const int32_t *counts, const int32_t *offsets, const int32_t *kpad, int E,
+                                      int C, int64_t ld, uint8_t *codes, uint8_t *scales, cudaStream_t st) {
+    if (ld <= 0 || C <= 0) return cudaSuccess;
+    const dim3 grid(static_cast<unsigned>(ld / 32), static_cast<unsigned>((C + kQtCols - 1) / kQtCols));
+    const cudaError_t e = launch_dep(mx_quantize_rows_t_kernel, grid, dim3(kQtCols), 0, st, src, src_ld, perm_slot,
+                                     k, counts, offsets, kpad, E, C, ld, codes, scales);
+    note_launches(1);
+    return e;
+}
+
+cudaError_t launch_wgrad_mx(const GemmLaunch &p, cudaStream_t st) {
+    GemmArgs g = grouped_args(p);
+    g.total_units = g.E * g.m_tiles * g.n_tiles;
+    const int grid = g.total_units < p.num_sms ? g.total_units : p.num_sms;
+    if (grid <= 0) return cudaSuccess;
+    return launch_tc_gemm<kWgradMx>(maps_of(p), g, grid, st);
+}
 
 cudaError_t launch_mx_quantize_dispatch(const __nv_bfloat16 *x, const int32_t *perm_slot, const int32_t *routed,
                                         int k, int64_t R, int64_t cols, uint8_t *codes, uint8_t *scales,
@@ -93,6 +200,7 @@ cudaError_t launch_mx_quantize_dispatch(const __nv_bfloat16 *x, const int32_t *p
 cudaError_t setup_mx_gemm_kernels() {
     cudaError_t e = set_gemm_smem<kStage1Mx>();
     if (e == cudaSuccess) e = set_gemm_smem<kStage2Mx>();
+    if (e == cudaSuccess) e = set_gemm_smem<kWgradMx>();
     return e;
 }
 

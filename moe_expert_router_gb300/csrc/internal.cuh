@@ -134,17 +134,28 @@ struct RouterLaunch {
     RouterScratch scratch;
 };
 
+// Counters of stage 2's fused k-way combine: int32 [T, n_tiles], n_tiles =
+// ceil(H / 256) output tiles per row; the metadata sets each to the number of
+// the token's dropped slots (cnt may be null: no counters).
+struct CombineCounters {
+    int32_t *cnt;
+    int T, k, n_tiles;
+};
+
 struct MetadataLaunch {
     const int32_t *topk_idx;
     int R, E;
     int32_t *counts, *offsets, *mt_prefix, *perm_slot, *row_of, *err;
     int32_t *block_hist;        // [ceil(R / kMetaChunk), E]
     int32_t *ticket;
+    CombineCounters combine;
 };
 
 // One grouped GEMM launch (forward stages 1 and 2, backward dA / dX / dW2 / dW1).
 struct GemmLaunch {
     const uint8_t *bpack;       // stage 1 / 2: tile-packed weights (pack.cu) instead of tm_b, or null
+    const int32_t *kpad;        // MXFP8 weight gradients: [E+1] padded row offsets of the quantized operands
+    int gather_a;               // stage 1: A rows gathered from x by token (tm_a: x with a one-row box)
     const CUtensorMap *tm_a;    // host-encoded tensor maps (copied into the launch);
     const CUtensorMap *tm_b;    // tm_a, tm_out2 and tm_out3 may be null when unused
     const CUtensorMap *tm_out;
@@ -155,6 +166,10 @@ struct GemmLaunch {
     int32_t *err;
     int32_t *sched;             // [2] unit scheduler of this launch
     const float *topk_w;        // stage 2 and dA
+    const int32_t *row_of;      // stage 2 with the fused combine: routed row of each slot
+    __nv_bfloat16 *y;           // stage 2 with the fused combine: y [T, H]
+    int32_t *ccnt;              // stage 2 with the fused combine: counters [T, ceil(H / 256)], or null
+    int T;
     __nv_bfloat16 *out;         // row-grouped output (masked stores of partial slabs)
     __nv_bfloat16 *out2, *out3; // stage 1 with h: h gate / up halves; dA: dH up half, w a
     float *dtw_part;            // dA: [ceil(I / 256), R]
@@ -244,6 +259,39 @@ struct CombineBwdLaunch {
     int T, H, E, k;
 };
 
+// Expert parallelism with fixed-size exchange buffers (ep.cu): P ranks, E_loc
+// experts each, C rows per (sender, receiver) block.
+struct EpPackLaunch {
+    const __nv_bfloat16 *x;
+    const float *topk_w;
+    const int32_t *row_of, *counts, *offsets;
+    int T, k;
+    int64_t H;
+    int E, E_loc;
+    int64_t C;
+    __nv_bfloat16 *send_rows;   // [P * C, H]
+    float *send_w;              // [P * C]
+    int32_t *send_counts;       // [P, E_loc] (= [E])
+    int32_t *err;
+};
+struct EpRecvLaunch {
+    const int32_t *recv;        // [P, E_loc] rows received per (source, local expert)
+    int P, E_loc;
+    int64_t C;
+    int n_tiles;                // ceil(H / 256): combine counters per received row
+    int32_t *counts, *offsets, *mt_prefix, *perm_slot, *row_of, *ccnt, *err;
+};
+struct EpCombineLaunch {
+    const __nv_bfloat16 *back;  // [P * C, H] returned rows, in the send buffer's places
+    const int32_t *row_of, *offsets;
+    int T, k, H, E, E_loc;
+    int64_t C;
+    __nv_bfloat16 *y;
+};
+cudaError_t launch_ep_pack(const EpPackLaunch &p, cudaStream_t st);
+cudaError_t launch_ep_receive_metadata(const EpRecvLaunch &p, cudaStream_t st);
+cudaError_t launch_ep_combine(const EpCombineLaunch &p, cudaStream_t st);
+
 cudaError_t launch_dtw_reduce(const DtwReduceLaunch &p, cudaStream_t st);
 // Zero rows [*routed_rows, R) of dH [R, 2I] and w a [R, I] (rows of dropped slots).
 cudaError_t launch_zero_tail_rows(__nv_bfloat16 *dh, __nv_bfloat16 *aw, const int32_t *routed_rows, int R,
@@ -262,6 +310,16 @@ cudaError_t launch_mx_quantize(const __nv_bfloat16 *in, int64_t rows, int64_t co
 cudaError_t launch_mx_quantize_dispatch(const __nv_bfloat16 *x, const int32_t *perm_slot, const int32_t *routed,
                                         int k, int64_t R, int64_t cols, uint8_t *codes, uint8_t *scales,
                                         cudaStream_t st);
+// MXFP8 weight gradients: padded row offsets kpad [E+1] of the quantized operands
+// (each expert's rows rounded up to whole 128-row k-blocks), the quantization of
+// an operand along the routed rows into transposed codes [C, ld] / scales
+// [C, ld / 32] (rows of routed row q: src[q] or, with perm_slot, src[perm_slot[q] / k]),
+// and the block-scaled weight-gradient GEMM.
+cudaError_t launch_mx_wgrad_offsets(const int32_t *counts, int E, int32_t *kpad, cudaStream_t st);
+cudaError_t launch_mx_quantize_rows_t(const __nv_bfloat16 *src, int64_t src_ld, const int32_t *perm_slot, int k,
+                                      const int32_t *counts, const int32_t *offsets, const int32_t *kpad, int E,
+                                      int C, int64_t ld, uint8_t *codes, uint8_t *scales, cudaStream_t st);
+cudaError_t launch_wgrad_mx(const GemmLaunch &p, cudaStream_t st);
 cudaError_t launch_gemm1_mx(const GemmLaunch &p, cudaStream_t st);
 cudaError_t launch_gemm2_mx(const GemmLaunch &p, cudaStream_t st);
 cudaError_t setup_mx_gemm_kernels();

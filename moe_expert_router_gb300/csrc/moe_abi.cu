@@ -73,6 +73,12 @@ moe_status_t check_shape(const moe_shape_t *s) {
     return MOE_OK;
 }
 
+// Columns of the MXFP8 weight-gradient operands: every expert's rows padded to
+// whole 128-row k-blocks, at most T*k + 128 E in all (a multiple of 128).
+size_t mx_wgrad_ld(const moe_shape_t &s) {
+    return (static_cast<size_t>(s.T) * s.k + 128 * static_cast<size_t>(s.E) + 127) / 128 * 128;
+}
+
 moe_ws_layout_t make_layout(const moe_shape_t &s) {
     const size_t T = s.T, H = s.H, I = s.I, E = s.E, R = s.T * s.k;
     moe_ws_layout_t L;
@@ -87,6 +93,7 @@ moe_ws_layout_t make_layout(const moe_shape_t &s) {
     L.router = off;    off = align256(off + router_scratch_bytes(T, H, E, router_splits(T, H, E)));
     L.a = off;         off = align256(off + 2 * R * I);
     L.obuf = off;      off = align256(off + 2 * R * H);
+    L.combine = off;   off = align256(off + 4 * T * ((H + kBN - 1) / kBN));
     if (s.flags & MOE_SHAPE_TRAINING) {
         L.dh = off;       off = align256(off + 2 * R * 2 * I);
         L.aw = off;       off = align256(off + 2 * R * I);
@@ -106,12 +113,55 @@ moe_ws_layout_t make_layout(const moe_shape_t &s) {
     } else {
         L.x_codes = L.x_scales = L.a_codes = L.a_scales = off;
     }
+    if ((s.flags & MOE_SHAPE_MXFP8) && (s.flags & MOE_SHAPE_TRAINING)) {
+        // the weight gradients' operands quantized along the routed rows, transposed:
+        // dY, w a, dH and x, each [columns, mx_wgrad_ld(s)] codes + [columns, ld / 32] scales
+        const size_t ld = mx_wgrad_ld(s);
+        L.mx_wgrad = off;
+        off = align256(off + 4 * (E + 1));
+        off = align256(off + (2 * H + 3 * I) * ld);
+        off = align256(off + (2 * H + 3 * I) * (ld / 32));
+    } else {
+        L.mx_wgrad = off;
+    }
     L.total = off;
     return L;
 }
 
+// MXFP8 weight-gradient operands (training + MXFP8 workspaces): the padded row
+// offsets, then codes and scales of dY^T [H, ld], (w a)^T [I, ld], dH^T [2I, ld]
+// and x^T [H, ld], ld = mx_wgrad_ld.
+struct MxWgradWs {
+    int32_t *kpad;
+    uint8_t *dy_c, *aw_c, *dh_c, *x_c;
+    uint8_t *dy_s, *aw_s, *dh_s, *x_s;
+    int64_t ld;
+};
+
+MxWgradWs carve_mx_wgrad(void *ws, const moe_shape_t &s) {
+    const moe_ws_layout_t L = make_layout(s);
+    const size_t H = s.H, I = s.I, E = s.E;
+    MxWgradWs m;
+    m.ld = static_cast<int64_t>(mx_wgrad_ld(s));
+    uint8_t *b = static_cast<uint8_t *>(ws) + L.mx_wgrad;
+    m.kpad = reinterpret_cast<int32_t *>(b);
+    uint8_t *c = b + align256(4 * (E + 1));
+    m.dy_c = c;
+    m.aw_c = m.dy_c + H * m.ld;
+    m.dh_c = m.aw_c + I * m.ld;
+    m.x_c = m.dh_c + 2 * I * m.ld;
+    uint8_t *sc = c + align256((2 * H + 3 * I) * m.ld);
+    const size_t lds = m.ld / 32;
+    m.dy_s = sc;
+    m.aw_s = m.dy_s + H * lds;
+    m.dh_s = m.aw_s + I * lds;
+    m.x_s = m.dh_s + 2 * I * lds;
+    return m;
+}
+
 // Workspace header words (see internal.cuh for bytes 0-32).
 constexpr size_t kHdrSchedDA = 40, kHdrSchedDX = 48, kHdrSchedDW2 = 56, kHdrSchedDW1 = 64;
+constexpr size_t kHdrSchedDW2Mx = 72, kHdrSchedDW1Mx = 80;
 
 struct Ws {
     int32_t *err, *ticket, *counts, *offsets, *mt_prefix, *perm_slot, *row_of, *sched1, *sched2;
@@ -119,6 +169,7 @@ struct Ws {
     int32_t *sched_da, *sched_dx, *sched_dw2, *sched_dw1;
     RouterScratch router;
     __nv_bfloat16 *a, *obuf;
+    int32_t *combine;           // stage 2's fused-combine counters [T, ceil(H / 256)]
     __nv_bfloat16 *dh, *aw;     // training only
     float *dtw_part, *dlogits;  // training only
     __nv_bfloat16 *xp, *dyp;    // training only: x and dY rows in routed order
@@ -150,6 +201,7 @@ Ws carve(void *ws, const moe_shape_t &s) {
                                     w.ticket, reinterpret_cast<int32_t *>(b + 24));
     w.a = reinterpret_cast<__nv_bfloat16 *>(b + L.a);
     w.obuf = reinterpret_cast<__nv_bfloat16 *>(b + L.obuf);
+    w.combine = reinterpret_cast<int32_t *>(b + L.combine);
     w.training = (s.flags & MOE_SHAPE_TRAINING) != 0;
     w.dh = reinterpret_cast<__nv_bfloat16 *>(b + L.dh);
     w.aw = reinterpret_cast<__nv_bfloat16 *>(b + L.aw);
@@ -185,6 +237,7 @@ GemmLaunch base_launch(const moe_shape_t &s, const Ws &w, const DeviceState &d) 
     p.E = static_cast<int>(s.E);
     p.k = s.k;
     p.R = static_cast<int>(s.T * s.k);
+    p.T = static_cast<int>(s.T);
     p.num_sms = d.num_sms;
     return p;
 }
@@ -194,18 +247,26 @@ GemmLaunch base_launch(const moe_shape_t &s, const Ws &w, const DeviceState &d) 
 // until stage 2 writes its rows there, or with h (training) to xp, which the
 // backward reads again. With h, the pre-activation is stored too (a, h gate and
 // h up in 32 x 32 boxes).
+// Stage 1's dispatch outside training: 0 = the copy kernel writes x's rows in
+// routed order and the GEMM loads whole tiles of them; 1 = the GEMM's producer
+// gathers the rows from x itself, four per tile::gather4 copy.
+#ifndef MOE_STAGE1_GATHER
+#define MOE_STAGE1_GATHER 0
+#endif
+
 moe_status_t run_gemm1(const moe_shape_t &s, const void *x, const void *w1, void *a, void *h, const Ws &w,
                        const DeviceState &d, cudaStream_t st) {
     const uint64_t R = static_cast<uint64_t>(s.T) * s.k;
     __nv_bfloat16 *xp = h ? w.xp : w.obuf;
+    const bool gather = MOE_STAGE1_GATHER && h == nullptr;
     CUtensorMap tm_x, tm_w1, tm_out, tm_hg, tm_hu;
     const uint32_t box = h ? 32 : 64;
-    if (!encode_bf16_2d(&tm_x, xp, s.H, R, kBK, 128) ||
+    if (!(gather ? encode_bf16_2d(&tm_x, x, s.H, s.T, kBK, 1) : encode_bf16_2d(&tm_x, xp, s.H, R, kBK, 128)) ||
         !encode_bf16_2d(&tm_w1, w1, s.H, static_cast<uint64_t>(s.E) * 2 * s.I, kBK, 128) ||
         !encode_bf16_2d(&tm_out, a, s.I, R, box, 32))
         return MOE_ERR_CUDA;
-    if (launch_dispatch_rows(static_cast<const __nv_bfloat16 *>(x), w.row_of, s.T, s.k, s.H, xp, nullptr, nullptr,
-                             st) != cudaSuccess)
+    if (!gather && launch_dispatch_rows(static_cast<const __nv_bfloat16 *>(x), w.row_of, s.T, s.k, s.H, xp, nullptr,
+                                        nullptr, st) != cudaSuccess)
         return MOE_ERR_CUDA;
     if (h && (!encode_bf16_2d_strided(&tm_hg, h, s.I, R, 2 * s.I, 32, 32) ||
               !encode_bf16_2d_strided(&tm_hu, static_cast<__nv_bfloat16 *>(h) + s.I, s.I, R, 2 * s.I, 32, 32)))
@@ -231,10 +292,23 @@ moe_status_t run_gemm1(const moe_shape_t &s, const void *x, const void *w1, void
     p.half = static_cast<int>(s.I);
     p.out_ld = static_cast<int>(2 * s.I);
     p.save_h = h != nullptr;
+    p.gather_a = gather ? 1 : 0;
     return cuda_status(launch_gemm1_swiglu(p, st));
 }
 
-// Stage 2: GEMM2 with the weighted scatter, then the k-way combine.
+// Where stage 2 sums each token's k rows. Fused into its epilogue (counters set
+// by the routing metadata) the sum costs no launch and no second pass, but each
+// epilogue warp then waits for its stores to land and reads the completed
+// tokens' rows back before it can take the next accumulator; with many units
+// per SM that delays the MMAs more than the separate combine kernel costs
+// (same box: mid stage 2 + combine 0.149 -> 0.192 ms, large_group 1.859 ->
+// 1.933 ms fused), while a few hundred routed rows gain (zipf_decode 0.184 ->
+// 0.169 ms). Fused up to kFusedCombineMaxRows routed rows.
+constexpr int64_t kFusedCombineMaxRows = 8192;
+bool fused_combine(const moe_shape_t &s) { return s.T * s.k <= kFusedCombineMaxRows; }
+
+// Stage 2: GEMM2 with the weighted scatter, then the k-way combine (fused into
+// the GEMM's epilogue for few routed rows, else the combine kernel).
 moe_status_t run_gemm2(const moe_shape_t &s, const void *a, const float *topk_w, const void *w2,
                        void *y, const Ws &w, const DeviceState &d, cudaStream_t st) {
     CUtensorMap tm_a, tm_w2, tm_out;
@@ -254,12 +328,18 @@ moe_status_t run_gemm2(const moe_shape_t &s, const void *a, const float *topk_w,
     p.sched = w.sched2;
     p.topk_w = topk_w;
     p.out = w.obuf;
+    const bool fused = fused_combine(s);
+    if (fused) {
+        p.row_of = w.row_of;
+        p.y = static_cast<__nv_bfloat16 *>(y);
+        p.ccnt = w.combine;
+    }
     p.K = static_cast<int>(s.I);
     p.n_out = static_cast<int>(s.H);
     p.n_tile = kBN;
     p.b_rows = static_cast<int>(s.H);
     moe_status_t r = cuda_status(launch_gemm2_scatter(p, st));
-    if (r != MOE_OK) return r;
+    if (r != MOE_OK || fused) return r;
     CombineLaunch c;
     c.obuf = w.obuf;
     c.row_of = w.row_of;
@@ -273,8 +353,8 @@ moe_status_t run_gemm2(const moe_shape_t &s, const void *a, const float *topk_w,
 // Stage 1 in MXFP8: the dispatched E4M3 x rows (routed order, in ws) and E4M3
 // w1 through TMA, scales into tensor memory per stage; the epilogue quantizes a
 // per 32 columns.
-moe_status_t run_gemm1_mx(const moe_shape_t &s, const void *w1q, const void *w1s, void *aq, void *as, const Ws &w,
-                          const DeviceState &d, cudaStream_t st) {
+moe_status_t run_gemm1_mx(const moe_shape_t &s, const void *w1q, const void *w1s, void *aq, void *as, void *h,
+                          const Ws &w, const DeviceState &d, cudaStream_t st) {
     const uint64_t R = static_cast<uint64_t>(s.T) * s.k;
     CUtensorMap tm_x, tm_w1;
     if (!encode_u8_2d(&tm_x, w.x_codes, s.H, R, 128, 128) ||
@@ -289,6 +369,9 @@ moe_status_t run_gemm1_mx(const moe_shape_t &s, const void *w1q, const void *w1s
     p.sched = w.sched1;
     p.out = static_cast<__nv_bfloat16 *>(aq);             // E4M3 codes [R, I]
     p.out_sf = static_cast<uint8_t *>(as);
+    p.out2 = static_cast<__nv_bfloat16 *>(h);             // training: h gate / up halves [R, 2I]
+    p.out3 = h ? static_cast<__nv_bfloat16 *>(h) + s.I : nullptr;
+    p.out_ld = static_cast<int>(2 * s.I);
     p.K = static_cast<int>(s.H);
     p.n_out = static_cast<int>(s.I);
     p.n_tile = 96;
@@ -497,6 +580,66 @@ moe_status_t run_bwd_stage1_weight(const moe_shape_t &s, void *dw1, const Ws &w,
     return cuda_status(launch_bwd_dw1(q, st));
 }
 
+// An MXFP8 weight gradient: dW[e] = Q(A_e)^T Q(B_e) over expert e's routed rows,
+// from the transposed, row-quantized operands (M = a_cols rows, N = b_cols).
+moe_status_t run_wgrad_mx(const moe_shape_t &s, const MxWgradWs &m, const uint8_t *a_c, const uint8_t *a_s,
+                          int64_t a_cols, const uint8_t *b_c, const uint8_t *b_s, int64_t b_cols, void *dw,
+                          int32_t *sched, const Ws &w, const DeviceState &d, cudaStream_t st) {
+    CUtensorMap tm_a, tm_b, tm_dw;
+    if (!encode_u8_2d(&tm_a, a_c, m.ld, a_cols, 128, 128) || !encode_u8_2d(&tm_b, b_c, m.ld, b_cols, 128, 224) ||
+        !encode_bf16_3d(&tm_dw, dw, b_cols, a_cols, s.E, 32, 32))
+        return MOE_ERR_CUDA;
+    GemmLaunch q = base_launch(s, w, d);
+    q.tm_a = &tm_a;
+    q.tm_b = &tm_b;
+    q.tm_out = &tm_dw;
+    q.kpad = m.kpad;
+    q.sfa = a_s;
+    q.sfb = b_s;
+    q.sched = sched;
+    q.K = static_cast<int>(m.ld);     // scale bytes per operand row: K / 32
+    q.n_out = static_cast<int>(b_cols);
+    q.n_tile = 224;
+    q.m_total = static_cast<int>(a_cols);
+    q.b_rows = 0;                     // the B operand's rows are shared by every expert
+    return cuda_status(launch_wgrad_mx(q, st));
+}
+
+// Stage 2 backward, weights, MXFP8: dW2[e] = Q(dY)^T Q(w a) over e's rows (the
+// dY rows and w a left in the workspace by the stage-2 data part).
+moe_status_t run_bwd_stage2_weight_mx(const moe_shape_t &s, void *dw2, const Ws &w, const DeviceState &d,
+                                      cudaStream_t st, void *ws) {
+    const MxWgradWs m = carve_mx_wgrad(ws, s);
+    const int E = static_cast<int>(s.E);
+    moe_status_t r = cuda_status(launch_mx_wgrad_offsets(w.counts, E, m.kpad, st));
+    if (r != MOE_OK) return r;
+    if ((r = cuda_status(launch_mx_quantize_rows_t(w.dyp, s.H, nullptr, s.k, w.counts, w.offsets, m.kpad, E,
+                                                   static_cast<int>(s.H), m.ld, m.dy_c, m.dy_s, st))) != MOE_OK ||
+        (r = cuda_status(launch_mx_quantize_rows_t(w.aw, s.I, nullptr, s.k, w.counts, w.offsets, m.kpad, E,
+                                                   static_cast<int>(s.I), m.ld, m.aw_c, m.aw_s, st))) != MOE_OK)
+        return r;
+    int32_t *sched = reinterpret_cast<int32_t *>(reinterpret_cast<uint8_t *>(ws) + kHdrSchedDW2Mx);
+    return run_wgrad_mx(s, m, m.dy_c, m.dy_s, s.H, m.aw_c, m.aw_s, s.I, dw2, sched, w, d, st);
+}
+
+// Stage 1 backward, weights, MXFP8: dW1[e] = Q(dH)^T Q(x) over e's rows (dH from
+// the stage-2 data part; x's rows gathered by token).
+moe_status_t run_bwd_stage1_weight_mx(const moe_shape_t &s, const void *x, void *dw1, const Ws &w,
+                                      const DeviceState &d, cudaStream_t st, void *ws) {
+    const MxWgradWs m = carve_mx_wgrad(ws, s);
+    const int E = static_cast<int>(s.E);
+    moe_status_t r = cuda_status(launch_mx_wgrad_offsets(w.counts, E, m.kpad, st));
+    if (r != MOE_OK) return r;
+    if ((r = cuda_status(launch_mx_quantize_rows_t(w.dh, 2 * s.I, nullptr, s.k, w.counts, w.offsets, m.kpad, E,
+                                                   static_cast<int>(2 * s.I), m.ld, m.dh_c, m.dh_s, st))) != MOE_OK ||
+        (r = cuda_status(launch_mx_quantize_rows_t(static_cast<const __nv_bfloat16 *>(x), s.H, w.perm_slot, s.k,
+                                                   w.counts, w.offsets, m.kpad, E, static_cast<int>(s.H), m.ld,
+                                                   m.x_c, m.x_s, st))) != MOE_OK)
+        return r;
+    int32_t *sched = reinterpret_cast<int32_t *>(reinterpret_cast<uint8_t *>(ws) + kHdrSchedDW1Mx);
+    return run_wgrad_mx(s, m, m.dh_c, m.dh_s, 2 * s.I, m.x_c, m.x_s, s.H, dw1, sched, w, d, st);
+}
+
 moe_status_t run_metadata(const moe_shape_t &s, const int32_t *topk_idx, const Ws &w, cudaStream_t st) {
     MetadataLaunch m;
     m.topk_idx = topk_idx;
@@ -510,6 +653,10 @@ moe_status_t run_metadata(const moe_shape_t &s, const int32_t *topk_idx, const W
     m.err = w.err;
     m.block_hist = w.meta;
     m.ticket = w.meta_ticket;
+    m.combine.cnt = fused_combine(s) ? w.combine : nullptr;
+    m.combine.T = static_cast<int>(s.T);
+    m.combine.k = s.k;
+    m.combine.n_tiles = static_cast<int>((s.H + kBN - 1) / kBN);
     return cuda_status(launch_routing_metadata(m, st));
 }
 
@@ -1001,7 +1148,7 @@ moe_status_t moe_dispatch_gemm1_mx(const void *w1_codes, const void *w1_scales, 
     if (!(shape->flags & MOE_SHAPE_MXFP8)) return MOE_ERR_INVALID_ARG;
     DeviceState *d = nullptr;
     if ((r = device_state(&d)) != MOE_OK) return r;
-    return run_gemm1_mx(*shape, w1_codes, w1_scales, a_codes, a_scales, carve(ws, *shape), *d,
+    return run_gemm1_mx(*shape, w1_codes, w1_scales, a_codes, a_scales, nullptr, carve(ws, *shape), *d,
                         static_cast<cudaStream_t>(stream));
 }
 
@@ -1045,8 +1192,65 @@ moe_status_t moe_forward_mx(const void *x, const int32_t *topk_idx, const float 
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     if ((r = run_metadata(*shape, topk_idx, w, st)) != MOE_OK) return r;
     if ((r = run_mx_dispatch(*shape, x, w, st)) != MOE_OK) return r;
-    if ((r = run_gemm1_mx(*shape, w1_codes, w1_scales, w.a_codes, w.a_scales, w, *d, st)) != MOE_OK) return r;
+    if ((r = run_gemm1_mx(*shape, w1_codes, w1_scales, w.a_codes, w.a_scales, nullptr, w, *d, st)) != MOE_OK)
+        return r;
     return run_gemm2_mx(*shape, w.a_codes, w.a_scales, topk_w, w2_codes, w2_scales, y, w, *d, st);
+}
+
+moe_status_t moe_dispatch_gemm1_mx_train(const void *w1_codes, const void *w1_scales, const moe_shape_t *shape,
+                                         void *a_codes, void *a_scales, void *h, void *ws, size_t ws_bytes,
+                                         void *stream) {
+    moe_status_t r = check_shape(shape);
+    if (r != MOE_OK) return r;
+    if (shape->H % 128 || shape->I % 128) return MOE_ERR_UNSUPPORTED;
+    if (shape->T == 0) return MOE_OK;
+    if (!w1_codes || !w1_scales || !a_codes || !a_scales || !h) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(w1_codes) || !aligned16(w1_scales) || !aligned16(a_codes) || !aligned16(a_scales) ||
+        !aligned16(h))
+        return MOE_ERR_INVALID_ARG;
+    if ((r = check_training(shape, ws, ws_bytes)) != MOE_OK) return r;
+    if (!(shape->flags & MOE_SHAPE_MXFP8)) return MOE_ERR_INVALID_ARG;
+    DeviceState *d = nullptr;
+    if ((r = device_state(&d)) != MOE_OK) return r;
+    return run_gemm1_mx(*shape, w1_codes, w1_scales, a_codes, a_scales, h, carve(ws, *shape), *d,
+                        static_cast<cudaStream_t>(stream));
+}
+
+// Common checks of the MXFP8 weight-gradient entry points.
+static moe_status_t check_wgrad_mx(const moe_shape_t *shape, const void *in, void *dw, void *ws,
+                                   size_t ws_bytes) {
+    moe_status_t r = check_shape(shape);
+    if (r != MOE_OK) return r;
+    if (shape->H % 128 || shape->I % 128) return MOE_ERR_UNSUPPORTED;
+    if (dw == nullptr || !aligned16(dw)) return MOE_ERR_INVALID_ARG;
+    if (shape->T == 0) return MOE_OK;
+    if (in == nullptr || !aligned16(in)) return MOE_ERR_INVALID_ARG;
+    if ((r = check_training(shape, ws, ws_bytes)) != MOE_OK) return r;
+    return (shape->flags & MOE_SHAPE_MXFP8) ? MOE_OK : MOE_ERR_INVALID_ARG;
+}
+
+moe_status_t moe_backward_stage2_weight_mx(const void *dy, const moe_shape_t *shape, void *dw2, void *ws,
+                                           size_t ws_bytes, void *stream) {
+    moe_status_t r = check_wgrad_mx(shape, dy, dw2, ws, ws_bytes);
+    if (r != MOE_OK) return r;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (shape->T == 0)
+        return cuda_status(cudaMemsetAsync(dw2, 0, 2 * static_cast<size_t>(shape->E) * shape->H * shape->I, st));
+    DeviceState *d = nullptr;
+    if ((r = device_state(&d)) != MOE_OK) return r;
+    return run_bwd_stage2_weight_mx(*shape, dw2, carve(ws, *shape), *d, st, ws);
+}
+
+moe_status_t moe_backward_stage1_weight_mx(const void *x, const moe_shape_t *shape, void *dw1, void *ws,
+                                           size_t ws_bytes, void *stream) {
+    moe_status_t r = check_wgrad_mx(shape, x, dw1, ws, ws_bytes);
+    if (r != MOE_OK) return r;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (shape->T == 0)
+        return cuda_status(cudaMemsetAsync(dw1, 0, 4 * static_cast<size_t>(shape->E) * shape->I * shape->H, st));
+    DeviceState *d = nullptr;
+    if ((r = device_state(&d)) != MOE_OK) return r;
+    return run_bwd_stage1_weight_mx(*shape, x, dw1, carve(ws, *shape), *d, st, ws);
 }
 
 moe_status_t moe_dispatch_rows(const void *x, const float *topk_w, const moe_shape_t *shape, void *rows,
@@ -1085,6 +1289,96 @@ moe_status_t moe_combine_rows(const void *rows, const moe_shape_t *shape, void *
     c.H = static_cast<int>(shape->H);
     c.k = shape->k;
     return cuda_status(launch_combine(c, static_cast<cudaStream_t>(stream)));
+}
+
+moe_status_t moe_ep_pack(const void *x, const float *topk_w, const moe_shape_t *shape, int32_t n_ranks,
+                         int64_t capacity, void *send_rows, float *send_w, int32_t *send_counts, void *ws,
+                         size_t ws_bytes, void *stream) {
+    moe_status_t r = check_shape(shape);
+    if (r != MOE_OK) return r;
+    if (n_ranks < 1 || shape->E % n_ranks != 0 || capacity < 1) return MOE_ERR_INVALID_ARG;
+    if (capacity * n_ranks >= (int64_t(1) << 31)) return MOE_ERR_UNSUPPORTED;
+    if (send_rows == nullptr || send_w == nullptr || send_counts == nullptr || !aligned16(send_rows) ||
+        (reinterpret_cast<uintptr_t>(send_w) & 3u) || (reinterpret_cast<uintptr_t>(send_counts) & 3u))
+        return MOE_ERR_INVALID_ARG;
+    if (shape->T == 0)      // nothing to send: every count is zero
+        return cuda_status(cudaMemsetAsync(send_counts, 0, 4 * static_cast<size_t>(shape->E),
+                                           static_cast<cudaStream_t>(stream)));
+    if (x == nullptr || topk_w == nullptr || !aligned16(x) || (reinterpret_cast<uintptr_t>(topk_w) & 3u))
+        return MOE_ERR_INVALID_ARG;
+    if ((r = check_ws(*shape, ws, ws_bytes)) != MOE_OK) return r;
+    DeviceState *d = nullptr;
+    if ((r = device_state(&d)) != MOE_OK) return r;
+    const Ws w = carve(ws, *shape);
+    EpPackLaunch p;
+    p.x = static_cast<const __nv_bfloat16 *>(x);
+    p.topk_w = topk_w;
+    p.row_of = w.row_of;
+    p.counts = w.counts;
+    p.offsets = w.offsets;
+    p.T = static_cast<int>(shape->T);
+    p.k = shape->k;
+    p.H = shape->H;
+    p.E = static_cast<int>(shape->E);
+    p.E_loc = static_cast<int>(shape->E / n_ranks);
+    p.C = capacity;
+    p.send_rows = static_cast<__nv_bfloat16 *>(send_rows);
+    p.send_w = send_w;
+    p.send_counts = send_counts;
+    p.err = w.err;
+    return cuda_status(launch_ep_pack(p, static_cast<cudaStream_t>(stream)));
+}
+
+moe_status_t moe_ep_receive_metadata(const int32_t *recv_counts, int32_t n_ranks, int64_t capacity,
+                                     const moe_shape_t *recv_shape, void *ws, size_t ws_bytes, void *stream) {
+    moe_status_t r = check_shape(recv_shape);
+    if (r != MOE_OK) return r;
+    if (n_ranks < 1 || capacity < 1 || recv_shape->k != 1 || recv_shape->T != n_ranks * capacity)
+        return MOE_ERR_INVALID_ARG;
+    if (recv_counts == nullptr || (reinterpret_cast<uintptr_t>(recv_counts) & 3u)) return MOE_ERR_INVALID_ARG;
+    if ((r = check_ws(*recv_shape, ws, ws_bytes)) != MOE_OK) return r;
+    DeviceState *d = nullptr;
+    if ((r = device_state(&d)) != MOE_OK) return r;
+    const Ws w = carve(ws, *recv_shape);
+    EpRecvLaunch p;
+    p.recv = recv_counts;
+    p.P = n_ranks;
+    p.E_loc = static_cast<int>(recv_shape->E);
+    p.C = capacity;
+    p.n_tiles = static_cast<int>((recv_shape->H + kBN - 1) / kBN);
+    p.counts = w.counts;
+    p.offsets = w.offsets;
+    p.mt_prefix = w.mt_prefix;
+    p.perm_slot = w.perm_slot;
+    p.row_of = w.row_of;
+    p.ccnt = w.combine;
+    p.err = w.err;
+    return cuda_status(launch_ep_receive_metadata(p, static_cast<cudaStream_t>(stream)));
+}
+
+moe_status_t moe_ep_combine(const void *back_rows, const moe_shape_t *shape, int32_t n_ranks, int64_t capacity,
+                            void *y, void *ws, size_t ws_bytes, void *stream) {
+    moe_status_t r = check_shape(shape);
+    if (r != MOE_OK) return r;
+    if (n_ranks < 1 || shape->E % n_ranks != 0 || capacity < 1) return MOE_ERR_INVALID_ARG;
+    if (shape->T == 0) return MOE_OK;
+    if (back_rows == nullptr || y == nullptr || !aligned16(back_rows) || !aligned16(y)) return MOE_ERR_INVALID_ARG;
+    if ((r = check_ws(*shape, ws, ws_bytes)) != MOE_OK) return r;
+    DeviceState *d = nullptr;
+    if ((r = device_state(&d)) != MOE_OK) return r;
+    const Ws w = carve(ws, *shape);
+    EpCombineLaunch p;
+    p.back = static_cast<const __nv_bfloat16 *>(back_rows);
+    p.row_of = w.row_of;
+    p.offsets = w.offsets;
+    p.T = static_cast<int>(shape->T);
+    p.k = shape->k;
+    p.H = static_cast<int>(shape->H);
+    p.E = static_cast<int>(shape->E);
+    p.E_loc = static_cast<int>(shape->E / n_ranks);
+    p.C = capacity;
+    p.y = static_cast<__nv_bfloat16 *>(y);
+    return cuda_status(launch_ep_combine(p, static_cast<cudaStream_t>(stream)));
 }
 
 moe_status_t moe_get_device_error(void *ws, int32_t *code, void *stream) {

@@ -215,13 +215,31 @@ __device__ __forceinline__ void metadata_place_body(const int32_t *__restrict__ 
     }
 }
 
+// Counters of stage 2's fused k-way sum, one per (token, 256-column output
+// tile): each starts at the number of the token's dropped slots, so the token's
+// sum over a tile is complete when its counter reaches k (threads first,
+// first + stride, ... over the tokens).
+__device__ __forceinline__ void init_combine_counters(const int32_t *__restrict__ topk_idx, int E,
+                                                      const CombineCounters &c, int first, int stride) {
+    if (c.cnt == nullptr) return;
+    for (int t = first; t < c.T; t += stride) {
+        int dropped = 0;
+        for (int j = 0; j < c.k; ++j) {
+            const int e = __ldg(&topk_idx[static_cast<int64_t>(t) * c.k + j]);
+            dropped += (e < 0 || e >= E) ? 1 : 0;
+        }
+        for (int n = 0; n < c.n_tiles; ++n) c.cnt[static_cast<int64_t>(t) * c.n_tiles + n] = dropped;
+    }
+}
+
 __global__ void __launch_bounds__(kThreads)
 metadata_place_kernel(const int32_t *__restrict__ topk_idx, int R, int E,
                       const int32_t *__restrict__ block_hist, const int32_t *__restrict__ offsets,
-                      int32_t *__restrict__ perm_slot, int32_t *__restrict__ row_of) {
+                      int32_t *__restrict__ perm_slot, int32_t *__restrict__ row_of, CombineCounters cc) {
     griddep_wait();
     extern __shared__ int32_t sh[];
     metadata_place_body(topk_idx, R, E, blockIdx.x, block_hist, offsets, perm_slot, row_of, sh);
+    init_combine_counters(topk_idx, E, cc, blockIdx.x * kThreads + threadIdx.x, gridDim.x * kThreads);
 }
 
 // All slots in one chunk (at most kChunk, e.g. decode): one CTA runs the count and the
@@ -232,12 +250,13 @@ metadata_single_chunk_kernel(const int32_t *__restrict__ topk_idx, int R, int E,
                              int32_t *__restrict__ counts, int32_t *__restrict__ offsets,
                              int32_t *__restrict__ mt_prefix, int32_t *__restrict__ ticket,
                              int32_t *__restrict__ err, int32_t *__restrict__ perm_slot,
-                             int32_t *__restrict__ row_of) {
+                             int32_t *__restrict__ row_of, CombineCounters cc) {
     griddep_wait();
     extern __shared__ int32_t sh[];
     metadata_count_body(topk_idx, R, E, 1, 0, block_hist, counts, offsets, mt_prefix, ticket, err, sh);
     __syncthreads();
     metadata_place_body(topk_idx, R, E, 0, block_hist, offsets, perm_slot, row_of, sh);
+    init_combine_counters(topk_idx, E, cc, threadIdx.x, kThreads);
 }
 
 size_t place_smem(int E) { return sizeof(int32_t) * static_cast<size_t>(kWarps + 1) * E; }
@@ -259,7 +278,7 @@ cudaError_t launch_routing_metadata(const MetadataLaunch &p, cudaStream_t st) {
     if (n_chunks == 1) {
         const cudaError_t e = launch_dep(metadata_single_chunk_kernel, dim3(1), dim3(kThreads), place_smem(p.E), st,
                                          p.topk_idx, p.R, p.E, p.block_hist, p.counts, p.offsets, p.mt_prefix,
-                                         p.ticket, p.err, p.perm_slot, p.row_of);
+                                         p.ticket, p.err, p.perm_slot, p.row_of, p.combine);
         note_launches(1);
         return e;
     }
@@ -268,7 +287,7 @@ cudaError_t launch_routing_metadata(const MetadataLaunch &p, cudaStream_t st) {
                                p.err);
     if (e == cudaSuccess)
         e = launch_dep(metadata_place_kernel, dim3(n_chunks), dim3(kThreads), place_smem(p.E), st, p.topk_idx, p.R,
-                       p.E, p.block_hist, p.offsets, p.perm_slot, p.row_of);
+                       p.E, p.block_hist, p.offsets, p.perm_slot, p.row_of, p.combine);
     note_launches(2);
     return e;
 }

@@ -1,28 +1,30 @@
-"""Expert parallelism across devices (EP > 1), with the exchange staged locally.
+"""Expert parallelism across devices (EP > 1) without host synchronisation.
 
 The MegaMoE guide (opening section) fuses the expert-parallel all-to-all into
 its two grouped GEMMs: dispatch_grouped_gemm sends each routed token row to the
 rank that owns its expert, grouped_gemm_combine sends the expert outputs back
-and forms the weighted sum. Here the exchange is a plain collective into local
-receive buffers, between device steps of this library:
+and forms the weighted sum; its "Example 2" runs the whole layer under one CUDA
+graph, so no step may wait for the host. Here the exchange is a plain
+collective into local receive buffers, between device steps of this library,
+with every buffer of a fixed size so that the collectives need no split sizes
+and the per-expert counts never leave the device:
 
-    rank p, experts [p E/P, (p+1) E/P) of E; its own T tokens and their routing
-    1. routing metadata of its T*k slots (moe_routing_metadata). Routed rows are
-       expert-major, so the rows bound for rank q are one contiguous range.
-    2. send buffer: x rows in routed order and each row's routing weight
-       (moe_dispatch_rows).
-    3. all-to-all of the per-(rank, local expert) row counts, then of the rows
-       and the weights (variable splits).
-    4. the received rows are tokens with k = 1 for the local experts (their
-       expert index follows from the counts): the single-device expert path
-       (moe_forward) gives each received row's weighted output.
-    5. all-to-all back (the reverse splits): every row returns to its source
-       rank in that rank's routed order.
-    6. combine: y[t] = sum of the token's returned rows (moe_combine_rows).
+    rank p of P, experts [p E/P, (p+1) E/P); its own T tokens and their routing;
+    C = capacity rows per (sender, receiver) block, the same on every rank
+        (default: the largest T k of the group, so nothing drops)
+    1. routing metadata of its T k slots, then the send buffer (moe_ep_pack):
+       block q holds the rows of rank q's experts in routed order from place 0,
+       with each row's routing weight, and the per-(rank, local expert) counts.
+    2. all-to-all (equal splits) of the counts, the rows and the weights.
+    3. the receiver's routing metadata from the received counts alone
+       (moe_ep_receive_metadata), then the single-device expert path on the
+       P C received rows as tokens with k = 1: each received row's weighted
+       output at the place it arrived.
+    4. all-to-all back (equal splits), and the sum of each token's returned
+       rows (moe_ep_combine).
 
-The split sizes are needed on the host by the collective, so step 3 reads the
-counts back once per step (the guide's fused kernels avoid that with a symmetric
-buffer and a cross-rank handshake).
+Buffers and workspaces are allocated once, when the ``ExpertParallel`` is built;
+a forward allocates nothing and reads nothing back to the host.
 
 ``ExpertParallel`` holds only this bookkeeping and calls the device work through
 an ``ops`` object: ``LibmoeOps`` (the CUDA kernels of libmoe) by default. There is
@@ -30,7 +32,6 @@ no CPU fallback; tests of the exchange logic on CPU ranks pass their own ops.
 """
 from __future__ import annotations
 
-import numpy as np
 import torch
 import torch.distributed as dist
 
@@ -38,103 +39,84 @@ from . import binding as B
 
 
 class LibmoeOps:
-    """The device steps of one rank, through libmoe (CUDA tensors only)."""
+    """The device steps of one rank, through libmoe (CUDA tensors only). setup()
+    allocates every buffer once; the steps only enqueue kernels."""
 
     def __init__(self, device):
         B.load()
         self.device = torch.device(device)
 
-    def route(self, x, topk_idx, topk_w, E):
-        """Metadata, send rows and row weights of this rank's slots; returns
-        (per-expert counts as a host array, rows, row weights, state)."""
-        T, H = x.shape
-        k = topk_idx.shape[1]
-        shp = B.shape(T, H, 8, E, k)
-        ws = B.new_workspace(shp, self.device)
-        B.moe_routing_metadata(topk_idx, shp, ws)
-        rows = torch.empty((T * k, H), dtype=torch.bfloat16, device=self.device)
-        row_w = torch.empty((T * k,), dtype=torch.float32, device=self.device)
-        B.moe_dispatch_rows(x, shp, rows, ws, topk_w=topk_w, row_weight=row_w)
-        L = B.moe_workspace_layout(shp)
-        counts = ws[L.counts:L.counts + 4 * E].view(torch.int32).cpu().numpy()
-        return counts, rows, row_w, (shp, ws)
+    def setup(self, T, H, I, E, k, P, C):
+        dev = self.device
+        self.P, self.C, self.E_loc = P, C, E // P
+        self.shp = B.shape(T, H, I, E, k)
+        self.ws = B.new_workspace(self.shp, dev)
+        self.rshp = B.shape(P * C, H, I, E // P, 1)
+        self.rws = B.new_workspace(self.rshp, dev)
+        self.send_rows = torch.empty((P * C, H), dtype=torch.bfloat16, device=dev)
+        self.send_w = torch.empty((P * C,), dtype=torch.float32, device=dev)
+        self.send_counts = torch.empty((P, E // P), dtype=torch.int32, device=dev)
+        self.a = torch.empty((P * C, I), dtype=torch.bfloat16, device=dev)
+        self.y_recv = torch.empty((P * C, H), dtype=torch.bfloat16, device=dev)
+        self.y = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
 
-    def expert_forward(self, rows, expert, weight, w1, w2):
-        """Weighted outputs of received rows (k = 1) on the local experts."""
-        R, H = rows.shape
-        E_loc, twoI, _ = w1.shape
-        out = torch.empty((R, H), dtype=torch.bfloat16, device=self.device)
-        if R == 0:
-            return out
-        shp = B.shape(R, H, twoI // 2, E_loc, 1)
-        ws = B.new_workspace(shp, self.device)
-        B.moe_forward(rows, expert.view(R, 1), weight.view(R, 1), w1, w2, shp, out, ws)
-        return out
+    def receive_buffers(self):
+        """(rows, weights, counts, returned rows): the receiving ends of the collectives."""
+        return (torch.empty_like(self.send_rows), torch.empty_like(self.send_w),
+                torch.empty_like(self.send_counts), torch.empty_like(self.send_rows))
 
-    def combine(self, rows_back, state, T, H):
-        shp, ws = state
-        y = torch.empty((T, H), dtype=torch.bfloat16, device=self.device)
-        B.moe_combine_rows(rows_back, shp, y, ws)
-        return y
+    def pack(self, x, topk_idx, topk_w):
+        B.moe_routing_metadata(topk_idx, self.shp, self.ws)
+        B.moe_ep_pack(x, topk_w, self.shp, self.P, self.C, self.send_rows, self.send_w, self.send_counts, self.ws)
+        return self.send_rows, self.send_w, self.send_counts
 
-    def to_device(self, array, dtype):
-        return torch.as_tensor(array, dtype=dtype).to(self.device)
+    def expert_forward(self, recv_counts, recv_rows, recv_w, w1, w2):
+        B.moe_ep_receive_metadata(recv_counts, self.P, self.C, self.rshp, self.rws)
+        B.moe_dispatch_gemm1(recv_rows, w1, self.rshp, self.a, self.rws)
+        B.moe_swiglu_gemm2_combine(self.a, recv_w.view(-1, 1), w2, self.rshp, self.y_recv, self.rws)
+        return self.y_recv
 
+    def combine(self, back_rows):
+        B.moe_ep_combine(back_rows, self.shp, self.P, self.C, self.y, self.ws)
+        return self.y
 
-def plan_splits(counts_all: np.ndarray, P: int) -> tuple[np.ndarray, np.ndarray]:
-    """Rows this rank sends to each rank, from its per-expert counts [E] (experts of
-    rank q are [q E/P, (q+1) E/P)): (send counts [P], per-(rank, local expert) counts [P, E/P])."""
-    E = counts_all.shape[0]
-    per = counts_all.reshape(P, E // P)
-    return per.sum(axis=1), per
-
-
-def local_expert_index(recv_per: np.ndarray) -> np.ndarray:
-    """Local expert of every received row: source segments in rank order, each
-    grouped by local expert (the sender's routed order). recv_per [P, E/P]."""
-    P, E_loc = recv_per.shape
-    return np.concatenate([np.repeat(np.arange(E_loc, dtype=np.int32), recv_per[p]) for p in range(P)]
-                          ) if recv_per.sum() else np.zeros((0,), np.int32)
+    def device_errors(self):
+        """The two workspaces' error words (a host sync; not for the step itself)."""
+        return B.moe_get_device_error(self.ws) | B.moe_get_device_error(self.rws)
 
 
 class ExpertParallel:
-    """The expert path with experts sharded over the ranks of ``group``."""
+    """The expert path with experts sharded over the ranks of ``group``, for T
+    tokens of hidden size H per rank (intermediate size I, k experts per token)."""
 
-    def __init__(self, E: int, group=None, ops=None, device=None):
+    def __init__(self, E: int, T: int, H: int, I: int, k: int, group=None, ops=None, device=None,
+                 capacity: int | None = None):
         self.group = group
         self.P = dist.get_world_size(group)
         self.rank = dist.get_rank(group)
         if E % self.P:
             raise ValueError("E must be a multiple of the number of ranks")
-        self.E = E
+        self.E, self.T, self.k = E, T, k
         self.E_loc = E // self.P
+        if capacity is None:
+            # every rank's blocks must have one size: the largest T k of the group
+            # (agreed once, here; a forward never talks to the host)
+            sizes = [None] * self.P
+            dist.all_gather_object(sizes, int(T) * int(k), group=group)
+            capacity = max(1, max(sizes))
+        self.C = int(capacity)
         self.ops = ops if ops is not None else LibmoeOps(device)
-
-    def _all_to_all(self, send, send_counts, recv_counts, row_shape, dtype, device):
-        recv = torch.empty((int(recv_counts.sum()),) + row_shape, dtype=dtype, device=device)
-        dist.all_to_all_single(recv, send[: int(send_counts.sum())].contiguous(),
-                               output_split_sizes=[int(c) for c in recv_counts],
-                               input_split_sizes=[int(c) for c in send_counts], group=self.group)
-        return recv
+        self.ops.setup(T, H, I, E, k, self.P, self.C)
+        self.recv_rows, self.recv_w, self.recv_counts, self.back = self.ops.receive_buffers()
 
     def forward(self, x, topk_idx, topk_w, w1_local, w2_local):
         """y [T, H] for this rank's tokens; w1_local / w2_local hold this rank's experts."""
-        T, H = x.shape
-        counts, rows, row_w, state = self.ops.route(x, topk_idx, topk_w, self.E)
-        send_counts, send_per = plan_splits(counts, self.P)
-        # exchange the per-(rank, local expert) counts: row q of send_per goes to rank q
-        per_t = torch.as_tensor(send_per.astype(np.int64))
-        recv_per_t = torch.empty_like(per_t)
-        if x.is_cuda:
-            per_t, recv_per_t = per_t.to(x.device), recv_per_t.to(x.device)
-        dist.all_to_all_single(recv_per_t, per_t, group=self.group)
-        recv_per = recv_per_t.cpu().numpy()
-        recv_counts = recv_per.sum(axis=1)
-        # the rows and their weights
-        rows_recv = self._all_to_all(rows, send_counts, recv_counts, (H,), rows.dtype, rows.device)
-        w_recv = self._all_to_all(row_w, send_counts, recv_counts, (), row_w.dtype, row_w.device)
-        expert = self.ops.to_device(local_expert_index(recv_per), torch.int32)
-        out = self.ops.expert_forward(rows_recv, expert, w_recv, w1_local, w2_local)
-        # back to the sources, in their routed order
-        rows_back = self._all_to_all(out, recv_counts, send_counts, (H,), out.dtype, out.device)
-        return self.ops.combine(rows_back, state, T, H)
+        if x.shape[0] != self.T:
+            raise ValueError("x must have the T rows the ExpertParallel was built for")
+        send_rows, send_w, send_counts = self.ops.pack(x, topk_idx, topk_w)
+        dist.all_to_all_single(self.recv_counts, send_counts, group=self.group)
+        dist.all_to_all_single(self.recv_rows, send_rows, group=self.group)
+        dist.all_to_all_single(self.recv_w, send_w, group=self.group)
+        y_recv = self.ops.expert_forward(self.recv_counts, self.recv_rows, self.recv_w, w1_local, w2_local)
+        dist.all_to_all_single(self.back, y_recv, group=self.group)
+        return self.ops.combine(self.back)

@@ -69,6 +69,8 @@ def _bind(lib):
     lib.oracle_expert_forward_mx.restype = ctypes.c_int
     lib.oracle_expert_backward_mx.argtypes = [i64, i64, i64, i64, i32] + [vp] * 16
     lib.oracle_expert_backward_mx.restype = ctypes.c_int
+    lib.oracle_mx_wgrad.argtypes = [i64, vp, i64, i64, vp, vp, vp]
+    lib.oracle_mx_wgrad.restype = ctypes.c_int
     return lib
 
 
@@ -236,6 +238,24 @@ class Oracle:
             return Backward(dx, dw1, dw2, dtw), dh, wa
         return Backward(dx, dw1, dw2, dtw)
 
+    def mx_wgrad(self, offsets, a_rows, b_rows):
+        """MXFP8 weight gradient of given operands: per expert e (rows offsets[e] ..
+        offsets[e+1]-1 of a_rows [R, M] and b_rows [R, N]), Q(A_e)^T Q(B_e) with Q the
+        MXFP8 quantization along the rows in blocks of 32 from the expert's first row.
+        Returns float64 [E, M, N]. bf16 tensors are taken at their exact values."""
+        off = _np(offsets, np.int32)
+        A = _np(a_rows)
+        B = _np(b_rows)
+        A = bf16_bits_to_f64(A) if A.dtype == np.uint16 else np.ascontiguousarray(A, np.float64)
+        B = bf16_bits_to_f64(B) if B.dtype == np.uint16 else np.ascontiguousarray(B, np.float64)
+        E = len(off) - 1
+        M, N = A.shape[1], B.shape[1]
+        dw = np.empty((E, M, N), np.float64)
+        rc = self.lib.oracle_mx_wgrad(E, _ptr(off), M, N, _ptr(A), _ptr(B), _ptr(dw))
+        if rc != 0:
+            raise ValueError("oracle_mx_wgrad rejected its arguments")
+        return dw
+
     def mx_quantize(self, a):
         """MXFP8 quantization along the last dimension: (codes uint8, scales uint8 [.., cols/32]).
 
@@ -356,6 +376,16 @@ def mx_quantize(*args, **kwargs):
 
 def expert_backward_mx(*args, **kwargs):
     return default().expert_backward_mx(*args, **kwargs)
+
+
+def mx_wgrad(*args, **kwargs):
+    return default().mx_wgrad(*args, **kwargs)
+
+
+def bf16_bits_to_f64(bits):
+    """Exact values of bf16 bit patterns (uint16) as float64."""
+    b = np.ascontiguousarray(bits, np.uint16)
+    return (b.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
 
 
 def expert_forward_mx(*args, **kwargs):

@@ -811,6 +811,62 @@ static void mx_block_values(const double *v, double *q) {
 }
 
 /*
+ * An MXFP8 weight gradient from given operands (the last step of the MXFP8
+ * training backward below). A [R, M] and B [R, N] hold one row per routed row;
+ * rows offsets[e] .. offsets[e+1]-1 belong to expert e. Per expert, its rows
+ * are cut into blocks of 32 consecutive rows from its first row (a last,
+ * partial block is completed with zeros), every column of A and of B is
+ * quantized to MXFP8 per block, and
+ *   dW[e][m][n] = sum over e's rows r of Q(A)[r,m] Q(B)[r,n]      dW [E, M, N]
+ */
+int oracle_mx_wgrad(int64_t E, const int32_t *offsets, int64_t M, int64_t N, const double *A, const double *B,
+                    double *dW) {
+    if (E <= 0 || M <= 0 || N <= 0 || !offsets || !A || !B || !dW) return -1;
+    int bad = 0;
+#pragma omp parallel
+    {
+        double *col = (double *)malloc(sizeof(double) * 32);
+        double *cq = (double *)malloc(sizeof(double) * 32);
+        double *qa = (double *)malloc(sizeof(double) * 32 * (size_t)M);   /* a block of Q(A): [32][M] */
+        double *qb = (double *)malloc(sizeof(double) * 32 * (size_t)N);
+        if (!col || !cq || !qa || !qb) {
+#pragma omp atomic write
+            bad = 1;
+        } else {
+#pragma omp for schedule(dynamic, 1)
+            for (int64_t e = 0; e < E; ++e) {
+                double *D = dW + e * M * N;
+                for (int64_t q = 0; q < M * N; ++q) D[q] = 0.0;
+                const int64_t end = offsets[e + 1];
+                for (int64_t b0 = offsets[e]; b0 < end; b0 += 32) {
+                    const int64_t n = (end - b0 < 32) ? end - b0 : 32;
+                    /* per column: the block's values (zeros past the expert's rows),
+                       quantized, kept dequantized */
+                    for (int64_t m = 0; m < M; ++m) {
+                        for (int r = 0; r < 32; ++r) col[r] = (r < n) ? A[(b0 + r) * M + m] : 0.0;
+                        mx_block_values(col, cq);
+                        for (int r = 0; r < 32; ++r) qa[r * M + m] = cq[r];
+                    }
+                    for (int64_t c = 0; c < N; ++c) {
+                        for (int r = 0; r < 32; ++r) col[r] = (r < n) ? B[(b0 + r) * N + c] : 0.0;
+                        mx_block_values(col, cq);
+                        for (int r = 0; r < 32; ++r) qb[r * N + c] = cq[r];
+                    }
+                    for (int r = 0; r < 32; ++r)
+                        for (int64_t m = 0; m < M; ++m) {
+                            const double d = qa[r * M + m];
+                            if (d == 0.0) continue;
+                            for (int64_t c = 0; c < N; ++c) D[m * N + c] += d * qb[r * N + c];
+                        }
+                }
+            }
+        }
+        free(col); free(cq); free(qa); free(qb);
+    }
+    return bad ? -1 : 0;
+}
+
+/*
  * Training backward of the MXFP8 expert precision (MegaMoE guide, section
  * "Expert precision": mxfp8 runs fc1, the SwiGLU, fc2 and the dW1 / dW2
  * weight gradients in MXFP8). Reading, where the pages name no more:
@@ -910,68 +966,35 @@ int oracle_expert_backward_mx(int64_t T, int64_t H, int64_t I, int64_t E, int32_
         free(xq); free(dyt); free(g); free(u); free(a); free(o); free(dO); free(dA);
     }
     if (!bad && (dw1 || dw2)) {
-#pragma omp parallel
-        {
-            int64_t *rows = (int64_t *)malloc(sizeof(int64_t) * (size_t)(R > 0 ? R : 1));
-            double *col = (double *)malloc(sizeof(double) * 32);
-            double *cq = (double *)malloc(sizeof(double) * 32);
-            /* one block of 32 rows of each operand, dequantized: [32][cols] */
-            double *qdy = (double *)malloc(sizeof(double) * 32 * (size_t)H);
-            double *qwa = (double *)malloc(sizeof(double) * 32 * (size_t)I);
-            double *qdh = (double *)malloc(sizeof(double) * 32 * 2 * (size_t)I);
-            double *qx = (double *)malloc(sizeof(double) * 32 * (size_t)H);
-            if (!rows || !col || !cq || !qdy || !qwa || !qdh || !qx) {
-#pragma omp atomic write
-                bad = 1;
-            } else {
-#pragma omp for schedule(dynamic, 1)
-                for (int64_t e = 0; e < E; ++e) {
-                    double *DW1 = dw1 ? dw1 + e * 2 * I * H : NULL;
-                    double *DW2 = dw2 ? dw2 + e * H * I : NULL;
-                    if (DW1) for (int64_t q = 0; q < 2 * I * H; ++q) DW1[q] = 0.0;
-                    if (DW2) for (int64_t q = 0; q < H * I; ++q) DW2[q] = 0.0;
-                    int64_t c = 0;
-                    for (int64_t s = 0; s < R; ++s)
-                        if (topk_idx[s] == e) rows[c++] = s;
-                    for (int64_t b0 = 0; b0 < c; b0 += 32) {
-                        const int64_t n = (c - b0 < 32) ? c - b0 : 32;
-                        /* per column: gather the block's values (zeros past the expert's
-                           rows), quantize, keep the dequantized values */
-#define MOE_QCOL(DST, NCOL, VALUE)                                           \
-                        for (int64_t cc = 0; cc < (NCOL); ++cc) {            \
-                            for (int r = 0; r < 32; ++r) {                   \
-                                const int64_t s = (r < n) ? rows[b0 + r] : -1; \
-                                col[r] = (s >= 0) ? (VALUE) : 0.0;           \
-                            }                                                \
-                            mx_block_values(col, cq);                        \
-                            for (int r = 0; r < 32; ++r) (DST)[r * (NCOL) + cc] = cq[r]; \
-                        }
-                        if (DW2) {
-                            MOE_QCOL(qdy, H, bf16_value(dy[(s / k) * H + cc]))
-                            MOE_QCOL(qwa, I, wa_s[s * I + cc])
-                            for (int r = 0; r < 32; ++r)
-                                for (int64_t h = 0; h < H; ++h) {
-                                    const double d = qdy[r * H + h];
-                                    if (d == 0.0) continue;
-                                    for (int64_t i = 0; i < I; ++i) DW2[h * I + i] += d * qwa[r * I + i];
-                                }
-                        }
-                        if (DW1) {
-                            MOE_QCOL(qdh, 2 * I, dh_s[s * 2 * I + cc])
-                            MOE_QCOL(qx, H, bf16_value(x[(s / k) * H + cc]))
-                            for (int r = 0; r < 32; ++r)
-                                for (int64_t jj = 0; jj < 2 * I; ++jj) {
-                                    const double d = qdh[r * 2 * I + jj];
-                                    if (d == 0.0) continue;
-                                    for (int64_t h = 0; h < H; ++h) DW1[jj * H + h] += d * qx[r * H + h];
-                                }
-                        }
-#undef MOE_QCOL
-                    }
+        /* the weight gradients' operands, one row per routed row (the routing
+           metadata's stable order: expert-major, slots in increasing order) */
+        int32_t *counts = (int32_t *)malloc(sizeof(int32_t) * (size_t)E);
+        int32_t *offsets = (int32_t *)malloc(sizeof(int32_t) * (size_t)(E + 1));
+        int32_t *perm = (int32_t *)malloc(sizeof(int32_t) * (size_t)(R > 0 ? R : 1));
+        int32_t *row_of = (int32_t *)malloc(sizeof(int32_t) * (size_t)(R > 0 ? R : 1));
+        double *ady = (double *)malloc(sizeof(double) * (size_t)(R > 0 ? R : 1) * (size_t)H);
+        double *awa = (double *)malloc(sizeof(double) * (size_t)(R > 0 ? R : 1) * (size_t)I);
+        double *adh = (double *)malloc(sizeof(double) * (size_t)(R > 0 ? R : 1) * 2 * (size_t)I);
+        double *ax = (double *)malloc(sizeof(double) * (size_t)(R > 0 ? R : 1) * (size_t)H);
+        if (!counts || !offsets || !perm || !row_of || !ady || !awa || !adh || !ax) {
+            bad = 1;
+        } else {
+            oracle_routing_metadata(T, k, E, topk_idx, counts, offsets, perm, row_of);
+            const int64_t routed = offsets[E];
+            for (int64_t r = 0; r < routed; ++r) {
+                const int64_t slot = perm[r];
+                const int64_t tok = slot / k;
+                for (int64_t h = 0; h < H; ++h) {
+                    ady[r * H + h] = bf16_value(dy[tok * H + h]);
+                    ax[r * H + h] = bf16_value(x[tok * H + h]);
                 }
+                memcpy(awa + r * I, wa_s + slot * I, sizeof(double) * (size_t)I);
+                memcpy(adh + r * 2 * I, dh_s + slot * 2 * I, sizeof(double) * 2 * (size_t)I);
             }
-            free(rows); free(col); free(cq); free(qdy); free(qwa); free(qdh); free(qx);
+            if (dw2 && oracle_mx_wgrad(E, offsets, H, I, ady, awa, dw2) != 0) bad = 1;
+            if (dw1 && oracle_mx_wgrad(E, offsets, 2 * I, H, adh, ax, dw1) != 0) bad = 1;
         }
+        free(counts); free(offsets); free(perm); free(row_of); free(ady); free(awa); free(adh); free(ax);
     }
     if (!bad && dh_slot) memcpy(dh_slot, dh_s, sizeof(double) * (size_t)R * 2 * I);
     if (!bad && wa_slot) memcpy(wa_slot, wa_s, sizeof(double) * (size_t)R * I);

@@ -1,6 +1,8 @@
-"""Expert parallelism across ranks: the exchange logic on two and three CPU ranks
-(gloo), with the oracle doing the per-rank device steps. Each rank's result must
-equal the single-device oracle forward of its tokens over all experts."""
+"""Expert parallelism across ranks: the exchange logic (fixed-size blocks, no
+host-side split sizes) on two and three CPU ranks (gloo), with the oracle doing
+the per-rank device steps. Each rank's result must equal the single-device
+oracle forward of its tokens over all experts; with a capacity below T k, the
+forward with the slots past a block's capacity dropped."""
 import multiprocessing as mp
 import os
 import socket
@@ -10,7 +12,6 @@ import pytest
 import torch
 
 import oracle
-from moe_expert_router_gb300.ep import local_expert_index, plan_splits
 
 
 def _free_port():
@@ -36,7 +37,21 @@ def _problem(rank, T, H, I, E, k, skew):
     return x, idx, w, w1, w2
 
 
-def _worker(rank, world, port, T_per_rank, E, skew, q):
+def _capacity_dropped(idx, E, world, C):
+    """The routing with every slot whose routed row lies past its block's capacity
+    dropped (-1): the block of rank q holds the routed rows of q's experts from place 0."""
+    md = oracle.routing_metadata(idx, E)
+    E_loc = E // world
+    out = idx.clone().reshape(-1)
+    for r, slot in enumerate(md.perm_slot.tolist()):
+        e = int(np.searchsorted(md.offsets, r, side="right")) - 1
+        q = e // E_loc
+        if r - int(md.offsets[q * E_loc]) >= C:
+            out[slot] = -1
+    return out.view(idx.shape)
+
+
+def _worker(rank, world, port, T_per_rank, E, skew, q, capacity=None):
     os.environ["MASTER_ADDR"] = "127.0.0.1"
     os.environ["MASTER_PORT"] = str(port)
     import sys
@@ -49,10 +64,11 @@ def _worker(rank, world, port, T_per_rank, E, skew, q):
         H, I, k = 32, 16, 3
         T = T_per_rank[rank]
         x, idx, w, w1, w2 = _problem(rank, T, H, I, E, k, skew)
-        ep = ExpertParallel(E, ops=OracleOps())
+        ep = ExpertParallel(E, T, H, I, k, ops=OracleOps(), capacity=capacity)
         lo, hi = rank * E // world, (rank + 1) * E // world
         y = ep.forward(x, idx, w, w1[lo:hi].contiguous(), w2[lo:hi].contiguous())
-        ref = oracle.expert_forward(x, idx, w, w1, w2)
+        kept = idx if capacity is None else _capacity_dropped(idx, E, world, ep.C)
+        ref = oracle.expert_forward(x, kept, w, w1, w2)
         assert tuple(y.shape) == (T, H)
         err = float(np.abs(y.numpy() - ref).max()) if T else 0.0
         q.put((rank, err, float(np.abs(ref).max()) if T else 0.0))
@@ -61,17 +77,19 @@ def _worker(rank, world, port, T_per_rank, E, skew, q):
         q.put((rank, repr(e), None))
 
 
-@pytest.mark.parametrize("world,T_per_rank,E,skew", [
-    (2, [40, 25], 8, 0.0),
-    (2, [64, 1], 8, 2.0),            # skewed: one rank receives far more rows
-    (3, [30, 0, 17], 6, 1.0),        # a rank with no tokens
+@pytest.mark.parametrize("world,T_per_rank,E,skew,capacity", [
+    (2, [40, 25], 8, 0.0, None),
+    (2, [64, 1], 8, 2.0, None),            # skewed: one rank receives far more rows
+    (3, [30, 0, 17], 6, 1.0, None),        # a rank with no tokens
+    (2, [40, 40], 8, 2.0, 20),             # a capacity below T k: skewed blocks overflow and drop rows
 ])
-def test_expert_parallel_matches_single_device(world, T_per_rank, E, skew):
+def test_expert_parallel_matches_single_device(world, T_per_rank, E, skew, capacity):
     oracle.build()
     ctx = mp.get_context("spawn")
     q = ctx.Queue()
     port = _free_port()
-    procs = [ctx.Process(target=_worker, args=(r, world, port, T_per_rank, E, skew, q)) for r in range(world)]
+    procs = [ctx.Process(target=_worker, args=(r, world, port, T_per_rank, E, skew, q, capacity))
+             for r in range(world)]
     for p in procs:
         p.start()
     res = [q.get(timeout=180) for _ in procs]
@@ -80,14 +98,3 @@ def test_expert_parallel_matches_single_device(world, T_per_rank, E, skew):
     for rank, err, mx in res:
         assert mx is not None, f"rank {rank}: {err}"
         assert err <= 1e-12 * max(1.0, mx), (rank, err, mx)
-
-
-def test_plan_splits_and_local_experts():
-    counts = np.array([3, 0, 2, 5, 1, 4], np.int32)          # E = 6 over P = 3
-    send, per = plan_splits(counts, 3)
-    assert send.tolist() == [3, 7, 5]
-    assert per.tolist() == [[3, 0], [2, 5], [1, 4]]
-    # received from three sources, two local experts
-    recv_per = np.array([[1, 2], [0, 0], [3, 1]])
-    assert local_expert_index(recv_per).tolist() == [0, 1, 1, 0, 0, 0, 1]
-    assert local_expert_index(np.zeros((2, 2), np.int64)).size == 0

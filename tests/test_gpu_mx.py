@@ -12,7 +12,7 @@ import pytest
 import torch
 
 import oracle
-from gpu_helpers import assert_close_y, read_metadata
+from gpu_helpers import MAX_ABS_FRAC, assert_close_y, read_metadata, tile_sample_tokens
 from moe_expert_router_gb300 import binding as B
 from moe_expert_router_gb300.workloads import CONFIGS, MoEConfig, generate, routing_with_counts
 
@@ -75,6 +75,18 @@ def mx_inputs(cfg, seed=0, idx=None, w=None):
     return inp, idx, w, w1q.view(E, 2 * I, H), w1s.view(E, 2 * I, H // 32), w2q.view(E, H, I), w2s.view(E, H, I // 32)
 
 
+def oracle_weights(inp, cfg, experts=None):
+    """The oracle's own MXFP8 quantization of w1 and w2 (of `experts` only when
+    given), from the bf16 weights: the codes and scales the oracle's forward is fed."""
+    w1, w2 = inp["w1"], inp["w2"]
+    if experts is not None:
+        sel = torch.as_tensor(experts, dtype=torch.long).to(w1.device)
+        w1, w2 = w1[sel], w2[sel]
+    w1q, w1s = oracle.mx_quantize(w1.cpu())
+    w2q, w2s = oracle.mx_quantize(w2.cpu())
+    return w1q, w1s, w2q, w2s
+
+
 def run_mx(cfg, inp, idx, w, w1q, w1s, w2q, w2s, staged):
     shp = B.shape(cfg.T, cfg.H, cfg.I, cfg.E, cfg.k, mxfp8=True)
     ws = B.new_workspace(shp, DEV)
@@ -132,8 +144,12 @@ def test_mx_forward_matches_oracle(name, staged):
     y, aq, as_, ws, shp, err = run_mx(cfg, inp, idx, w, w1q, w1s, w2q, w2s, staged)
     assert err == 0, f"device error word {err:#x}"
     xq, xs = oracle.mx_quantize(inp["x"])
-    y_ref, _, ac_ref, as_ref = oracle.expert_forward_mx(xq, xs, idx.cpu(), w.cpu().double(), w1q.cpu(), w1s.cpu(),
-                                                        w2q.cpu(), w2s.cpu(), want_a=True)
+    o1q, o1s, o2q, o2s = oracle_weights(inp, cfg)
+    # the weight quantization the GPU path was given is the oracle's, bit for bit
+    for gq, oq in ((w1q, o1q), (w1s, o1s), (w2q, o2q), (w2s, o2s)):
+        np.testing.assert_array_equal(gq.cpu().numpy(), oq)
+    y_ref, _, ac_ref, as_ref = oracle.expert_forward_mx(xq, xs, idx.cpu(), w.cpu().double(), o1q, o1s, o2q, o2s,
+                                                        want_a=True)
     assert_close_y(y, y_ref, "y (MXFP8)")
     # a: codes in routed order on the GPU, in slot order in the oracle
     _, _, _, perm, _ = read_metadata(ws, shp)
@@ -184,19 +200,156 @@ def test_mx_bf16_agreement_is_within_quantization_error():
 
 
 @pytest.mark.slow
-def test_mx_full_size_mid_sampled():
-    """The mid configuration in MXFP8 at full size (one-shot call): y on sampled tokens."""
-    cfg = CONFIGS["mid"]
+@pytest.mark.parametrize("name", ["mid", "large_group"])
+def test_mx_full_size_sampled(name):
+    """A full-size configuration in MXFP8 (one-shot call): y on the tokens of the
+    first, middle and last rows of every 256-row tile of every expert (so every
+    unit of both MXFP8 GEMMs is reached), plus the first, middle and last
+    tokens, against the oracle's MXFP8 forward on its own quantization of x and
+    of the weights."""
+    cfg = CONFIGS[name]
     inp, idx, w, w1q, w1s, w2q, w2s = mx_inputs(cfg, seed=0)
     y, aq, as_, ws, shp, err = run_mx(cfg, inp, idx, w, w1q, w1s, w2q, w2s, staged=False)
     assert err == 0
-    toks = torch.as_tensor([0, 1, 2, cfg.T // 2, cfg.T - 1] + list(range(101, cfg.T, cfg.T // 10))[:10])
+    counts, offsets, _, perm, _ = read_metadata(ws, shp)
+    toks = torch.as_tensor(tile_sample_tokens(counts, offsets, perm, cfg.k, extra=[0, 1, cfg.T // 2, cfg.T - 1]))
     xq, xs = oracle.mx_quantize(inp["x"][toks.to(DEV)])
     idx_s = idx.cpu()[toks].long()
     used = torch.unique(idx_s)
     remap = torch.full((cfg.E,), -1, dtype=torch.long)
     remap[used] = torch.arange(used.numel())
-    u = used.to(DEV)
+    o1q, o1s, o2q, o2s = oracle_weights(inp, cfg, experts=used)
     y_ref = oracle.expert_forward_mx(xq, xs, remap[idx_s].to(torch.int32), w.cpu()[toks].double(),
-                                     w1q[u].cpu(), w1s[u].cpu(), w2q[u].cpu(), w2s[u].cpu())
-    assert_close_y(y.cpu()[toks], y_ref, "y (MXFP8, sampled tokens)")
+                                     o1q, o1s, o2q, o2s)
+    assert_close_y(y.cpu()[toks], y_ref, f"y (MXFP8, {len(toks)} tokens)")
+
+
+# ------------------------------------------------------------------ MXFP8 training step
+
+def mx_train_step(cfg, inp, idx, w, w1q, w1s, w2q, w2s):
+    """The MXFP8 training step through the C ABI: MXFP8 forward saving h, the
+    bf16 data-gradient backward on it, MXFP8 weight gradients."""
+    T, H, I, E, k = cfg.T, cfg.H, cfg.I, cfg.E, cfg.k
+    shp = B.shape(T, H, I, E, k, training=True, mxfp8=True)
+    ws = B.new_workspace(shp, DEV)
+    R = T * k
+    aq = torch.empty((R, I), dtype=torch.uint8, device=DEV)
+    as_ = torch.empty((R, I // 32), dtype=torch.uint8, device=DEV)
+    h = torch.empty((R, 2 * I), dtype=torch.bfloat16, device=DEV)
+    y = torch.empty((T, H), dtype=torch.bfloat16, device=DEV)
+    dx = torch.empty((T, H), dtype=torch.bfloat16, device=DEV)
+    dw1 = torch.full((E, 2 * I, H), float("nan"), dtype=torch.bfloat16, device=DEV)
+    dw2 = torch.full((E, H, I), float("nan"), dtype=torch.bfloat16, device=DEV)
+    dtw = torch.full((T, k), float("nan"), dtype=torch.float32, device=DEV)
+    B.moe_routing_metadata(idx, shp, ws)
+    B.moe_mx_quantize_dispatch(inp["x"], shp, ws)
+    B.moe_dispatch_gemm1_mx_train(w1q, w1s, shp, aq, as_, h, ws)
+    B.moe_swiglu_gemm2_combine_mx(aq, as_, w, w2q, w2s, shp, y, ws)
+    B.moe_backward_stage2_data(inp["dy"], w, inp["w2"], h, shp, ws, dtopk_w=dtw)
+    B.moe_backward_stage2_weight_mx(inp["dy"], shp, dw2, ws)
+    B.moe_backward_stage1_data(inp["w1"], shp, dx, ws)
+    B.moe_backward_stage1_weight_mx(inp["x"], shp, dw1, ws)
+    err = B.moe_get_device_error(ws)
+    return {"y": y, "h": h, "dx": dx, "dw1": dw1, "dw2": dw2, "dtw": dtw, "err": err, "ws": ws, "shp": shp}
+
+
+def _with_dy(inp, cfg, seed):
+    g = torch.Generator(device=DEV).manual_seed(seed + 100)
+    inp["dy"] = torch.randn((cfg.T, cfg.H), generator=g, device=DEV).to(torch.bfloat16)
+    return inp
+
+
+TRAIN_CASES = {
+    # about 64 rows per expert: one partial k-block of 128 rows, partial 32-row blocks
+    "small": (_cfg(256, 256, 256, 8, 2), None),
+    # counts around the 32-row block and 128-row k-block edges, an expert without rows;
+    # I = 384 leaves a partial 224-column n-tile of dW2 and 2I = 768 three m-tiles of dW1
+    "ragged": (_cfg(320, 256, 384, 8, 2), [0, 1, 33, 128, 129, 300, 5, 44]),
+    # 256 rows per expert: two full k-blocks
+    "two_kblocks": (_cfg(512, 512, 256, 4, 2), None),
+}
+
+
+# The MXFP8 weight gradients quantize dH and w a, which the GPU keeps in bf16
+# while the oracle carries them in fp64. A perturbation delta (relative) of a
+# value moves its E4M3 code by one step Delta (2^-4 .. 2^-3 relative) with
+# probability about delta / Delta, so the quantized operand differs from the
+# oracle's by a relative RMS of about sqrt(delta * Delta); with delta of a bf16
+# rounding and the SiLU's approximation (a few 2^-10) that is 1-2 %, which no
+# summation averages away. Hence two checks: the weight-gradient kernels against
+# the oracle's MXFP8 weight gradient of the GPU's own bf16 operands (the same
+# codes on both sides: only the fp32 accumulation and the bf16 output differ),
+# and the whole chain against the oracle with the bound MX_WGRAD_REL_FRO.
+MX_WGRAD_REL_FRO = 3e-2
+MX_WGRAD_MAX_ABS_FRAC = 1e-1
+# one bf16 rounding of the output (RMS ~2^-9 / sqrt(3) relative) plus fp32 sums
+WGRAD_KERNEL_REL_FRO = 5e-3
+
+
+def _assert_close_bound(g, r, rel_bound, abs_frac, what):
+    g = g.detach().float().cpu().double().numpy() if isinstance(g, torch.Tensor) else np.asarray(g, np.float64)
+    r = np.asarray(r, np.float64)
+    assert np.isfinite(g).all(), f"{what}: non-finite values"
+    rel = np.linalg.norm(g - r) / max(np.linalg.norm(r), 1e-300)
+    assert rel <= rel_bound, f"{what}: relative Frobenius error {rel:.3e} > {rel_bound}"
+    assert np.abs(g - r).max() <= abs_frac * np.abs(r).max(), f"{what}: max abs error"
+    return rel
+
+
+@pytest.mark.parametrize("name", sorted(TRAIN_CASES))
+def test_mx_training_step_matches_oracle(name):
+    cfg, counts = TRAIN_CASES[name]
+    idx = w = None
+    if counts is not None:
+        idx, w = routing_with_counts(counts, cfg.T, cfg.k, seed=9, device=DEV)
+    inp, idx, w, w1q, w1s, w2q, w2s = mx_inputs(cfg, seed=4, idx=idx, w=w)
+    inp = _with_dy(inp, cfg, 4)
+    out = mx_train_step(cfg, inp, idx, w, w1q, w1s, w2q, w2s)
+    assert out["err"] == 0, f"device error word {out['err']:#x}"
+    xq, xs = oracle.mx_quantize(inp["x"])
+    o1q, o1s, o2q, o2s = oracle_weights(inp, cfg)
+    y_ref = oracle.expert_forward_mx(xq, xs, idx.cpu(), w.cpu().double(), o1q, o1s, o2q, o2s)
+    assert_close_y(out["y"], y_ref, "y (MXFP8 training forward)")
+    b, dh_ref, wa_ref = oracle.expert_backward_mx(inp["x"], xq, xs, idx.cpu(), w.cpu().double(), inp["w1"], o1q,
+                                                  o1s, inp["w2"], inp["dy"], want_slots=True)
+    # the data-gradient path (bf16): its outputs and the operands it leaves for the weight gradients
+    assert_close_y(out["dtw"], b.dtopk_w, "dtopk_w")
+    assert_close_y(out["dx"], b.dx, "dX")
+    ws, shp = out["ws"], out["shp"]
+    _, offsets, _, perm, _ = read_metadata(ws, shp)
+    L = B.moe_workspace_layout(shp)
+    R, n = cfg.T * cfg.k, len(perm)
+    dh = ws[L.dh:L.dh + 2 * R * 2 * cfg.I].view(torch.bfloat16).view(R, 2 * cfg.I)[:n]
+    aw = ws[L.aw:L.aw + 2 * R * cfg.I].view(torch.bfloat16).view(R, cfg.I)[:n]
+    dyp = ws[L.dyp:L.dyp + 2 * R * cfg.H].view(torch.bfloat16).view(R, cfg.H)[:n]
+    assert_close_y(dh, dh_ref[perm], "dH (routed order)")
+    assert_close_y(aw, wa_ref[perm], "w a (routed order)")
+    tok = torch.as_tensor(perm // cfg.k, dtype=torch.long)
+    assert torch.equal(dyp.cpu(), inp["dy"].cpu()[tok])
+    # the MXFP8 weight-gradient kernels on the GPU's own operands
+    dw2_k = oracle.mx_wgrad(offsets, dyp, aw)
+    dw1_k = oracle.mx_wgrad(offsets, dh, inp["x"].cpu()[tok])
+    _assert_close_bound(out["dw2"], dw2_k, WGRAD_KERNEL_REL_FRO, MAX_ABS_FRAC, "dW2 kernel (own operands)")
+    _assert_close_bound(out["dw1"], dw1_k, WGRAD_KERNEL_REL_FRO, MAX_ABS_FRAC, "dW1 kernel (own operands)")
+    # the whole chain against the oracle
+    _assert_close_bound(out["dw2"], b.dw2, MX_WGRAD_REL_FRO, MX_WGRAD_MAX_ABS_FRAC, "dW2 (MXFP8)")
+    _assert_close_bound(out["dw1"], b.dw1, MX_WGRAD_REL_FRO, MX_WGRAD_MAX_ABS_FRAC, "dW1 (MXFP8)")
+    flat = idx.cpu().reshape(-1)
+    for e in range(cfg.E):
+        if int((flat == e).sum()) == 0:
+            assert not out["dw1"][e].float().abs().max().item()
+            assert not out["dw2"][e].float().abs().max().item()
+
+
+def test_mx_training_weight_gradients_differ_from_bf16_by_quantization_only():
+    """Sanity of the precision: the MXFP8 weight gradients stay within a few percent
+    of the bf16 backward's and are not identical to them."""
+    cfg, _ = TRAIN_CASES["small"]
+    inp, idx, w, w1q, w1s, w2q, w2s = mx_inputs(cfg, seed=8)
+    inp = _with_dy(inp, cfg, 8)
+    out = mx_train_step(cfg, inp, idx, w, w1q, w1s, w2q, w2s)
+    b = oracle.expert_backward(inp["x"], idx.cpu(), w.cpu().double(), inp["w1"], inp["w2"], inp["dy"])
+    for name, ref in (("dw1", b.dw1), ("dw2", b.dw2)):
+        g = out[name].float().cpu().double().numpy()
+        rel = np.linalg.norm(g - ref) / np.linalg.norm(ref)
+        assert 1e-3 < rel < 0.1, (name, rel)

@@ -81,13 +81,16 @@ MUTANTS = {
                                   "xq[h] = bf16_value(x[t * H + h]);"),
     "mxb_wa_unweighted": ("for (int64_t i = 0; i < I; ++i) wa_s[slot * I + i] = w * a[i];",
                           "for (int64_t i = 0; i < I; ++i) wa_s[slot * I + i] = a[i];"),
-    "mxb_wgrad_unquantized": ("mx_block_values(col, cq);", "memcpy(cq, col, sizeof(double) * 32);"),
-    "mxb_dy_weighted": ("MOE_QCOL(qdy, H, bf16_value(dy[(s / k) * H + cc]))",
-                        "MOE_QCOL(qdy, H, topk_w[s] * bf16_value(dy[(s / k) * H + cc]))"),
-    "mxb_dw1_x_wrong_token": ("MOE_QCOL(qx, H, bf16_value(x[(s / k) * H + cc]))",
-                              "MOE_QCOL(qx, H, bf16_value(x[(s % T) * H + cc]))"),
-    "mxb_blocks_of_16": ("const int64_t n = (c - b0 < 32) ? c - b0 : 32;",
-                         "const int64_t n = (c - b0 < 16) ? c - b0 : 16;"),
+    "mxb_wgrad_a_unquantized": ("for (int r = 0; r < 32; ++r) qa[r * M + m] = cq[r];",
+                                "for (int r = 0; r < 32; ++r) qa[r * M + m] = col[r];"),
+    "mxb_wgrad_b_unquantized": ("for (int r = 0; r < 32; ++r) qb[r * N + c] = cq[r];",
+                                "for (int r = 0; r < 32; ++r) qb[r * N + c] = col[r];"),
+    "mxb_dy_weighted": ("ady[r * H + h] = bf16_value(dy[tok * H + h]);",
+                        "ady[r * H + h] = topk_w[slot] * bf16_value(dy[tok * H + h]);"),
+    "mxb_dw1_x_wrong_token": ("ax[r * H + h] = bf16_value(x[tok * H + h]);",
+                              "ax[r * H + h] = bf16_value(x[((tok + 1) % T) * H + h]);"),
+    "mxb_blocks_of_16": ("const int64_t n = (end - b0 < 32) ? end - b0 : 32;",
+                         "const int64_t n = (end - b0 < 16) ? end - b0 : 16;"),
     "mxb_gate_up_up": ("gacc += mx_value(w1_codes, w1_scales, H, w1_row + i, h) * xq[h];",
                        "gacc += mx_value(w1_codes, w1_scales, H, w1_row + I + i, h) * xq[h];"),
     "rbwd_dwr_wrong_token": ("acc += dl[t * E + e] * bf16_value(x[t * H + h]);",
