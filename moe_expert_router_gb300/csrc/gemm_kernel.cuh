@@ -196,7 +196,6 @@ struct GemmArgs {
                                 //   3 router_seg with the parts fused)
     int router_seg;             // router: accumulator columns of each of the hi / mid / lo parts when one
                                 //   MMA covers all three (E <= 64), else 0
-    int gather_a;               // stage 1: A rows gathered from x by token (maps.a: box one row high)
     const int32_t *kpad;        // MXFP8 weight gradients: [E+1] start of each expert's rows in the
                                 //   quantized operands, a multiple of 128 (rows padded to whole k-blocks)
     const uint8_t *bpack;       // stage 1 / 2: the tile-packed weights (pack.cu), or null for the TMA views
@@ -600,18 +599,6 @@ tc_gemm_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs g) {
 
             const Unit t = decode_unit<MODE>(u, g);
             const bool two = t.rows > BM;            // second half present
-            // stage 1 with the gathered dispatch: this lane's eight rows 8 lane .. 8 lane + 7
-            // of the unit, as token indices (rows past the count repeat the first row)
-            int tok8[8];
-            if constexpr (MODE == kStage1) {
-                if (g.gather_a) {
-#pragma unroll
-                    for (int j = 0; j < 8; ++j) {
-                        const int r = 8 * lane + j;
-                        tok8[j] = __ldg(&g.perm_slot[t.row0 + (r < t.rows ? r : 0)]) / g.k;
-                    }
-                }
-            }
             // one or two 128-row halves of A (K-major rows or MN-major atoms) and the B tile
             const uint32_t a_bytes = unit_a_bytes(t);
             const uint32_t tx_bytes = a_bytes + (MODE == kRouter ? g.n_mma : kUnitN<MODE>) * 128;
@@ -657,30 +644,14 @@ tc_gemm_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs g) {
                     sa = smem_addr(sm.a[stage]);
                     sb = smem_addr(sm.b[stage]);
                 }
-                if constexpr (MODE == kStage1) {
-                    if (g.gather_a) {
-                        // the dispatch fused into the load: four x rows per gather, the
-                        // warp's lanes covering the unit's rows (after lane 0's expect_tx)
-                        if (lane == 0) mbar_arrive_expect_tx(full, tx_bytes);
-                        __syncwarp();
-                        if (8 * lane < (two ? UM : BM)) {
-                            const int kx = kb * kStageK<MODE>;
-                            const uint32_t dst = sa + 8 * lane * ROW_BYTES;
-                            tma_gather4(dst, &maps.a, kx, tok8[0], tok8[1], tok8[2], tok8[3], full);
-                            tma_gather4(dst + 4 * ROW_BYTES, &maps.a, kx, tok8[4], tok8[5], tok8[6], tok8[7], full);
-                        }
-                    }
-                }
                 if (lane == 0) {
-                    if (!(MODE == kStage1 && g.gather_a)) mbar_arrive_expect_tx(full, tx_bytes);
+                    mbar_arrive_expect_tx(full, tx_bytes);
                     if constexpr (kIsStage1<MODE>) {
                         constexpr int hn = kUnitN<MODE> / 2;                                 // gate (= up) rows
                         const int row = t.e * g.b_rows + t.n * hn;
                         const int kx = kb * kStageK<MODE>;
-                        if (!(MODE == kStage1 && g.gather_a)) {
-                            tma_load_2d(sa, &maps.a, kx, t.row0, full);                     // dispatched x rows
-                            if (two) tma_load_2d(sa + A_HALF_BYTES, &maps.a, kx, t.row0 + BM, full);
-                        }
+                        tma_load_2d(sa, &maps.a, kx, t.row0, full);                         // dispatched x rows
+                        if (two) tma_load_2d(sa + A_HALF_BYTES, &maps.a, kx, t.row0 + BM, full);
                         if (MODE == kStage1 && g.bpack != nullptr) {                        // packed gate + up slab
                             bulk_load(sb, g.bpack + ((static_cast<int64_t>(t.e) * g.n_tiles + t.n) * g.kb_tiles + kb) *
                                                         B_BYTES, B_BYTES, full);
@@ -1394,7 +1365,6 @@ inline GemmArgs grouped_args(const GemmLaunch &p) {
     g.sfb = p.sfb;
     g.out_sf = p.out_sf;
     g.bpack = p.bpack;
-    g.gather_a = p.gather_a;
     g.kpad = p.kpad;
     g.kb_tiles = (p.K + BK - 1) / BK;
     g.E = p.E;

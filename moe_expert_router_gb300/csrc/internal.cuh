@@ -155,7 +155,6 @@ struct MetadataLaunch {
 struct GemmLaunch {
     const uint8_t *bpack;       // stage 1 / 2: tile-packed weights (pack.cu) instead of tm_b, or null
     const int32_t *kpad;        // MXFP8 weight gradients: [E+1] padded row offsets of the quantized operands
-    int gather_a;               // stage 1: A rows gathered from x by token (tm_a: x with a one-row box)
     const CUtensorMap *tm_a;    // host-encoded tensor maps (copied into the launch);
     const CUtensorMap *tm_b;    // tm_a, tm_out2 and tm_out3 may be null when unused
     const CUtensorMap *tm_out;

@@ -247,26 +247,18 @@ GemmLaunch base_launch(const moe_shape_t &s, const Ws &w, const DeviceState &d) 
 // until stage 2 writes its rows there, or with h (training) to xp, which the
 // backward reads again. With h, the pre-activation is stored too (a, h gate and
 // h up in 32 x 32 boxes).
-// Stage 1's dispatch outside training: 0 = the copy kernel writes x's rows in
-// routed order and the GEMM loads whole tiles of them; 1 = the GEMM's producer
-// gathers the rows from x itself, four per tile::gather4 copy.
-#ifndef MOE_STAGE1_GATHER
-#define MOE_STAGE1_GATHER 0
-#endif
-
 moe_status_t run_gemm1(const moe_shape_t &s, const void *x, const void *w1, void *a, void *h, const Ws &w,
                        const DeviceState &d, cudaStream_t st) {
     const uint64_t R = static_cast<uint64_t>(s.T) * s.k;
     __nv_bfloat16 *xp = h ? w.xp : w.obuf;
-    const bool gather = MOE_STAGE1_GATHER && h == nullptr;
     CUtensorMap tm_x, tm_w1, tm_out, tm_hg, tm_hu;
     const uint32_t box = h ? 32 : 64;
-    if (!(gather ? encode_bf16_2d(&tm_x, x, s.H, s.T, kBK, 1) : encode_bf16_2d(&tm_x, xp, s.H, R, kBK, 128)) ||
+    if (!encode_bf16_2d(&tm_x, xp, s.H, R, kBK, 128) ||
         !encode_bf16_2d(&tm_w1, w1, s.H, static_cast<uint64_t>(s.E) * 2 * s.I, kBK, 128) ||
         !encode_bf16_2d(&tm_out, a, s.I, R, box, 32))
         return MOE_ERR_CUDA;
-    if (!gather && launch_dispatch_rows(static_cast<const __nv_bfloat16 *>(x), w.row_of, s.T, s.k, s.H, xp, nullptr,
-                                        nullptr, st) != cudaSuccess)
+    if (launch_dispatch_rows(static_cast<const __nv_bfloat16 *>(x), w.row_of, s.T, s.k, s.H, xp, nullptr, nullptr,
+                             st) != cudaSuccess)
         return MOE_ERR_CUDA;
     if (h && (!encode_bf16_2d_strided(&tm_hg, h, s.I, R, 2 * s.I, 32, 32) ||
               !encode_bf16_2d_strided(&tm_hu, static_cast<__nv_bfloat16 *>(h) + s.I, s.I, R, 2 * s.I, 32, 32)))
@@ -292,7 +284,6 @@ moe_status_t run_gemm1(const moe_shape_t &s, const void *x, const void *w1, void
     p.half = static_cast<int>(s.I);
     p.out_ld = static_cast<int>(2 * s.I);
     p.save_h = h != nullptr;
-    p.gather_a = gather ? 1 : 0;
     return cuda_status(launch_gemm1_swiglu(p, st));
 }
 
