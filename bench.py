@@ -40,15 +40,17 @@ from moe_expert_router_gb300.workloads import CONFIGS, generate  # noqa: E402
 METRIC = "MoE expert-path TFLOP/s and tokens/s (1 GB300) and fraction of bf16/HBM roofline"
 L2_FLUSH_BYTES = 256 << 20
 
-# DRAM bytes (read + write) per launch of the stage-1 kernel, from ncu captures
+# DRAM bytes (read + write) per launch of stage 1 -- the dispatch copy plus the
+# stage-1 GEMM, the two kernels its CUDA-event time covers -- from ncu captures
 # of `bench.py --workload <name> --steps 2 --warmup 1 --no-cpu-baseline`
 # (summaries under profiles/). Reported only while the kernel sources still
 # hash to the value recorded with the capture; otherwise traffic is null.
 KERNEL_SOURCES = ("moe_expert_router_gb300/csrc/gemm_kernel.cuh", "moe_expert_router_gb300/csrc/grouped_gemm.cu",
                   "moe_expert_router_gb300/csrc/ptx.cuh", "moe_expert_router_gb300/csrc/internal.cuh")
 STAGE1_TRAFFIC = {
-    # profiles/tc_gemm_mid_ncu.md: 840.0 MB read + 63.5 MB written by tc_gemm_kernel<0>
-    "mid": {"src": "97d43b32136ac542", "bytes": 903.5e6},
+    # profiles/tc_gemm_large_group_ncu.md, one step at full size: dispatch copy
+    # 117.74 MB read + 875.72 MB written, tc_gemm_kernel<0> 16.19 GB + 264.28 MB
+    "large_group": {"src": "cbf9f1f31930f6b0", "bytes": 117.74e6 + 875.72e6 + 16.19e9 + 264.28e6},
 }
 
 

@@ -104,7 +104,7 @@ typedef struct moe_ws_layout {
                           holds x's rows dispatched into routed order here; the
                           backward's dX rows (unweighted, routed order) reuse it */
     size_t combine;    /* int32 [T, ceil(H/256)] counters of stage 2's fused k-way sum, used
-                          when T*k <= 8192 (set by moe_routing_metadata) */
+                          when T*k <= 64 E (set by moe_routing_metadata) */
     /* training workspaces only (flags = MOE_SHAPE_TRAINING), else equal to total: */
     size_t dh;         /* bf16 [T*k, 2I] gradient of h = [gate | up], routed order */
     size_t aw;         /* bf16 [T*k, I] routing weight times a, routed order */

@@ -290,13 +290,14 @@ moe_status_t run_gemm1(const moe_shape_t &s, const void *x, const void *w1, void
 // Where stage 2 sums each token's k rows. Fused into its epilogue (counters set
 // by the routing metadata) the sum costs no launch and no second pass, but each
 // epilogue warp then waits for its stores to land and reads the completed
-// tokens' rows back before it can take the next accumulator; with many units
-// per SM that delays the MMAs more than the separate combine kernel costs
-// (same box: mid stage 2 + combine 0.149 -> 0.192 ms, large_group 1.859 ->
-// 1.933 ms fused), while a few hundred routed rows gain (zipf_decode 0.184 ->
-// 0.169 ms). Fused up to kFusedCombineMaxRows routed rows.
-constexpr int64_t kFusedCombineMaxRows = 8192;
-bool fused_combine(const moe_shape_t &s) { return s.T * s.k <= kFusedCombineMaxRows; }
+// tokens' rows back before it can take the next accumulator: the more rows a
+// unit holds, the longer that delays the MMAs. Measured fused against the
+// combine kernel: mid (384 rows per expert) stage 2 + combine 0.149 -> 0.192 ms,
+// large_group (256) 1.859 -> 1.933 ms, its 32-expert slice slower as well, while
+// zipf_decode (4 rows per expert) gains, 0.184 -> 0.167 ms. Fused while the
+// experts average at most kFusedCombineMaxRowsPerExpert routed rows.
+constexpr int64_t kFusedCombineMaxRowsPerExpert = 64;
+bool fused_combine(const moe_shape_t &s) { return s.T * s.k <= kFusedCombineMaxRowsPerExpert * s.E; }
 
 // Stage 2: GEMM2 with the weighted scatter, then the k-way combine (fused into
 // the GEMM's epilogue for few routed rows, else the combine kernel).
