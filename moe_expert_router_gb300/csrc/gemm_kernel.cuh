@@ -482,8 +482,20 @@ __device__ __forceinline__ void scaled_piece(uint32_t tacc, int c, float w, uint
 // K steps. Offsets are byte offsets of a row's scales (-1: none). The words of
 // the next stage are loaded while the current one is consumed, so the global
 // latency stays off the pipeline's critical path.
+template <int MODE>
 __device__ __forceinline__ void load_scales(const GemmArgs &g, int kb, bool any, const int64_t (&a_off)[8],
                                             const int64_t (&b_off)[8], uint32_t (&r)[16]) {
+    if constexpr (MODE == kWgradMx) {
+        // the weight-gradient operands' scales are k-block-major: the word of row c
+        // for k-block kb at [kb][c], so a warp's 32 consecutive rows are 128 bytes
+        const uint32_t *sa = reinterpret_cast<const uint32_t *>(g.sfa) + static_cast<int64_t>(kb) * g.m_total;
+        const uint32_t *sb = reinterpret_cast<const uint32_t *>(g.sfb) + static_cast<int64_t>(kb) * g.n_out;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) r[j] = (any && a_off[j] >= 0) ? __ldg(sa + a_off[j]) : 0u;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) r[8 + j] = (any && b_off[j] >= 0) ? __ldg(sb + b_off[j]) : 0u;
+        return;
+    }
 #pragma unroll
     for (int j = 0; j < 8; ++j)
         r[j] = (any && a_off[j] >= 0) ? __ldg(reinterpret_cast<const uint32_t *>(g.sfa + a_off[j]) + kb) : 0u;
@@ -496,7 +508,9 @@ __device__ __forceinline__ void load_scales(const GemmArgs &g, int kb, bool any,
 template <int MODE>
 __device__ __forceinline__ void scale_rows(const GemmArgs &g, const Unit &t, int lane, int64_t (&a_off)[8],
                                            int64_t (&b_off)[8]) {
-    const int64_t ld = g.K / 32;                      // scale bytes per row (A rows in routed order)
+    // weight gradients: row indices into the k-block-major scale words; otherwise
+    // byte offsets of each row's scales
+    const int64_t ld = MODE == kWgradMx ? 1 : g.K / 32;
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
         const int r = 32 * j + lane;
@@ -1308,7 +1322,7 @@ tc_gemm_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs g) {
                 int64_t a_off[8], b_off[8];
                 uint32_t sfw[16];
                 scale_rows<MODE>(g, t, lane, a_off, b_off);
-                load_scales(g, t.kb0, t.kb0 < t.kb1, a_off, b_off, sfw);
+                load_scales<MODE>(g, t.kb0, t.kb0 < t.kb1, a_off, b_off, sfw);
                 const uint32_t sf_lane = tmem_base + (static_cast<uint32_t>((warp & 3) * 32) << 16) + kSfBase<MODE>;
                 for (int kb = t.kb0; kb < t.kb1; ++kb) {
                     if (lane == 0) ok = mbar_wait(smem_addr(&sm.empty[stage]), phase ^ 1u, abort_flag, g.err);
@@ -1316,7 +1330,7 @@ tc_gemm_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs g) {
                     if (!ok) break;
                     tc_fence_after();
                     tmem_st16(sf_lane + stage * kSfStride, sfw);
-                    load_scales(g, kb + 1, kb + 1 < t.kb1, a_off, b_off, sfw);
+                    load_scales<MODE>(g, kb + 1, kb + 1 < t.kb1, a_off, b_off, sfw);
                     tmem_wait_st();
                     tc_fence_before();
                     mbar_arrive(smem_addr(&sm.full[stage]));

@@ -100,62 +100,71 @@ __global__ void __launch_bounds__(32) mx_wgrad_offsets_kernel(const int32_t *__r
 }
 
 // The operands of an MXFP8 weight gradient, quantized along the expert's routed
-// rows (the GEMM's reduction dimension) and stored transposed, K-major:
-// codes [C, ld] and scales [C, ld / 32], where column r of expert e's segment
-// [kpad[e], kpad[e+1]) holds routed row offsets[e] + (r - kpad[e]) of the
-// source (zero past the expert's count). Source row of routed row q: src[q, :]
-// (row stride src_ld), or with perm_slot the token's row src[perm_slot[q] / k, :].
-// One CTA per 32-row block and 256 columns: the block's rows are staged in
-// shared memory, then each thread quantizes one column's 32 values.
-constexpr int kQtCols = 256;
+// rows (the GEMM's reduction dimension) and stored transposed, K-major: codes
+// [C, ld], where column r of expert e's segment [kpad[e], kpad[e+1]) holds
+// routed row offsets[e] + (r - kpad[e]) of the source (zero past the expert's
+// count), and the scales k-block-major: word [kb][c] holds the four E8M0 codes
+// of rows [128 kb, 128 kb + 128) of column c, 32 rows each, so the GEMM's
+// scale-factor warps read 32 consecutive columns' words as one 128-byte line.
+// Source row of routed row q: src[q, :] (row stride src_ld), or with perm_slot
+// the token's row src[perm_slot[q] / k, :]. One CTA per 128-row k-block and 128
+// columns: the block's rows are staged in shared memory with 16-byte loads,
+// then each thread quantizes one column's four 32-value blocks and writes its
+// 128 codes as one 128-byte line and its four scales as one word.
+constexpr int kQtCols = 128;
+constexpr int kQtRows = 128;
 __global__ void __launch_bounds__(kQtCols)
 mx_quantize_rows_t_kernel(const __nv_bfloat16 *__restrict__ src, int64_t src_ld, const int32_t *__restrict__ perm_slot,
                           int k, const int32_t *__restrict__ counts, const int32_t *__restrict__ offsets,
                           const int32_t *__restrict__ kpad, int E, int C, int64_t ld, uint8_t *__restrict__ codes,
                           uint8_t *__restrict__ scales) {
-    __shared__ uint32_t tile[32][kQtCols / 2 + 1];   // 32 rows x 256 bf16, padded against bank conflicts
+    extern __shared__ __align__(16) uint32_t qt_tile[];   // [kQtRows][kQtCols / 2 + 4]
+    constexpr int kStride = kQtCols / 2 + 4;             // words per staged row (16-byte aligned)
     griddep_wait();
-    const int64_t r0 = static_cast<int64_t>(blockIdx.x) * 32;   // first padded row of the block
-    if (r0 >= kpad[E]) return;                                   // past every expert's segment
-    int lo = 0, hi = E;                                          // expert with kpad[e] <= r0 < kpad[e+1]
+    const int64_t r0 = static_cast<int64_t>(blockIdx.x) * kQtRows;   // first padded row of the k-block
+    if (r0 >= kpad[E]) return;                                         // past every expert's segment
+    int lo = 0, hi = E;                                                // expert with kpad[e] <= r0 < kpad[e+1]
     while (hi - lo > 1) {
         const int mid = (lo + hi) >> 1;
         if (kpad[mid] <= r0) lo = mid; else hi = mid;
     }
     const int e = lo;
-    const int local = static_cast<int>(r0 - kpad[e]);           // row of the expert's segment
+    const int local = static_cast<int>(r0 - kpad[e]);                 // row of the expert's segment
     const int c0 = blockIdx.y * kQtCols;
-    // stage: row i of the block, columns [c0, c0 + 256): 16-byte loads, 8 threads per 128 columns
-    for (int i = threadIdx.x; i < 32 * (kQtCols / 8); i += blockDim.x) {
+    const int cnt = counts[e];
+    for (int i = threadIdx.x; i < kQtRows * (kQtCols / 8); i += blockDim.x) {
         const int row = i / (kQtCols / 8);
         const int cc = (i % (kQtCols / 8)) * 8;
         uint4 v = make_uint4(0u, 0u, 0u, 0u);
-        if (local + row < counts[e] && c0 + cc < C) {
+        if (local + row < cnt && c0 + cc < C) {
             const int64_t q = offsets[e] + local + row;
             const int64_t srow = perm_slot ? perm_slot[q] / k : q;
             v = __ldg(reinterpret_cast<const uint4 *>(src + srow * src_ld + c0 + cc));
         }
-        tile[row][cc / 2] = v.x;
-        tile[row][cc / 2 + 1] = v.y;
-        tile[row][cc / 2 + 2] = v.z;
-        tile[row][cc / 2 + 3] = v.w;
+        *reinterpret_cast<uint4 *>(qt_tile + row * kStride + cc / 2) = v;
     }
     __syncthreads();
     const int c = c0 + threadIdx.x;
     if (c >= C) return;
-    float v[32];
-#pragma unroll
-    for (int row = 0; row < 32; ++row) {
-        const uint32_t w = tile[row][threadIdx.x / 2];
-        v[row] = (threadIdx.x & 1) ? bf16_hi(w) : bf16_lo(w);
-    }
-    uint32_t qw[8];
-    const uint32_t sc = mx_quantize32(v, qw);
+    uint32_t sw = 0;
     uint4 *dst = reinterpret_cast<uint4 *>(codes + static_cast<int64_t>(c) * ld + r0);
-    dst[0] = make_uint4(qw[0], qw[1], qw[2], qw[3]);
-    dst[1] = make_uint4(qw[4], qw[5], qw[6], qw[7]);
-    scales[static_cast<int64_t>(c) * (ld / 32) + r0 / 32] = static_cast<uint8_t>(sc);
+#pragma unroll 1
+    for (int b = 0; b < kQtRows / 32; ++b) {
+        float v[32];
+#pragma unroll
+        for (int row = 0; row < 32; ++row) {
+            const uint32_t w = qt_tile[(32 * b + row) * kStride + threadIdx.x / 2];
+            v[row] = (threadIdx.x & 1) ? bf16_hi(w) : bf16_lo(w);
+        }
+        uint32_t qw[8];
+        sw |= mx_quantize32(v, qw) << (8 * b);
+        dst[2 * b] = make_uint4(qw[0], qw[1], qw[2], qw[3]);
+        dst[2 * b + 1] = make_uint4(qw[4], qw[5], qw[6], qw[7]);
+    }
+    reinterpret_cast<uint32_t *>(scales)[(r0 / kQtRows) * C + c] = sw;
 }
+
+size_t qt_smem() { return sizeof(uint32_t) * kQtRows * (kQtCols / 2 + 4); }
 
 }  // namespace
 
@@ -169,9 +178,9 @@ cudaError_t launch_mx_quantize_rows_t(const __nv_bfloat16 *src, int64_t src_ld, 
                                       const int32_t *counts, const int32_t *offsets, const int32_t *kpad, int E,
                                       int C, int64_t ld, uint8_t *codes, uint8_t *scales, cudaStream_t st) {
     if (ld <= 0 || C <= 0) return cudaSuccess;
-    const dim3 grid(static_cast<unsigned>(ld / 32), static_cast<unsigned>((C + kQtCols - 1) / kQtCols));
-    const cudaError_t e = launch_dep(mx_quantize_rows_t_kernel, grid, dim3(kQtCols), 0, st, src, src_ld, perm_slot,
-                                     k, counts, offsets, kpad, E, C, ld, codes, scales);
+    const dim3 grid(static_cast<unsigned>(ld / kQtRows), static_cast<unsigned>((C + kQtCols - 1) / kQtCols));
+    const cudaError_t e = launch_dep(mx_quantize_rows_t_kernel, grid, dim3(kQtCols), qt_smem(), st, src, src_ld,
+                                     perm_slot, k, counts, offsets, kpad, E, C, ld, codes, scales);
     note_launches(1);
     return e;
 }
@@ -201,6 +210,9 @@ cudaError_t setup_mx_gemm_kernels() {
     cudaError_t e = set_gemm_smem<kStage1Mx>();
     if (e == cudaSuccess) e = set_gemm_smem<kStage2Mx>();
     if (e == cudaSuccess) e = set_gemm_smem<kWgradMx>();
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(mx_quantize_rows_t_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(qt_smem()));
     return e;
 }
 

@@ -311,9 +311,9 @@ cudaError_t launch_mx_quantize_dispatch(const __nv_bfloat16 *x, const int32_t *p
                                         cudaStream_t st);
 // MXFP8 weight gradients: padded row offsets kpad [E+1] of the quantized operands
 // (each expert's rows rounded up to whole 128-row k-blocks), the quantization of
-// an operand along the routed rows into transposed codes [C, ld] / scales
-// [C, ld / 32] (rows of routed row q: src[q] or, with perm_slot, src[perm_slot[q] / k]),
-// and the block-scaled weight-gradient GEMM.
+// an operand along the routed rows into transposed codes [C, ld] and k-block-major
+// scale words [ld / 128, C] (four E8M0 bytes each; rows of routed row q: src[q]
+// or, with perm_slot, src[perm_slot[q] / k]), and the block-scaled GEMM.
 cudaError_t launch_mx_wgrad_offsets(const int32_t *counts, int E, int32_t *kpad, cudaStream_t st);
 cudaError_t launch_mx_quantize_rows_t(const __nv_bfloat16 *src, int64_t src_ld, const int32_t *perm_slot, int k,
                                       const int32_t *counts, const int32_t *offsets, const int32_t *kpad, int E,
