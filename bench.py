@@ -268,7 +268,7 @@ def run_ours(args, cfg, rank, world, local_rank):
         w1q, w1s = cache.get(inp["w1"])
         w2q, w2s = cache.get(inp["w2"])
         aq = torch.empty((cfg.R, cfg.I), dtype=torch.uint8, device=dev)
-        as_ = torch.empty((cfg.R, cfg.I // 32), dtype=torch.uint8, device=dev)
+        as_ = B.mx_scales_empty((cfg.R, cfg.I), dev)
     if uniform:
         # the guide's `uniform` force-balance mode: each step routes fresh N(0,1)
         # logits (drawn before the timed region; a pool of 8 steps' worth is cycled)

@@ -115,9 +115,9 @@ typedef struct moe_ws_layout {
     size_t dwr_part;   /* fp32 [8, E, H] partial sums of the router weight gradient */
     /* MXFP8 workspaces only (flags & MOE_SHAPE_MXFP8), else equal to total: */
     size_t x_codes;    /* E4M3 [T*k, H] quantized x rows in routed order (the MXFP8 dispatch) */
-    size_t x_scales;   /* E8M0 [T*k, H/32] */
+    size_t x_scales;   /* E8M0, k-block-major over T*k rows (rows4(T*k)*H/32 bytes) */
     size_t a_codes;    /* E4M3 [T*k, I] quantized SwiGLU output, routed order (moe_forward_mx) */
-    size_t a_scales;   /* E8M0 [T*k, I/32] */
+    size_t a_scales;   /* E8M0, k-block-major over T*k rows (rows4(T*k)*I/32 bytes) */
     /* training + MXFP8 workspaces only, else equal to total: */
     size_t mx_wgrad;   /* the MXFP8 weight gradients' operands, quantized along the routed rows */
     size_t total;      /* == moe_workspace_size */
@@ -477,16 +477,24 @@ moe_status_t moe_pack_weights(const void *w1, const void *w2, const moe_shape_t 
  * reduction dimension share a power-of-two scale 2^(floor(log2 max|v|) - 8),
  * stored as E8M0 (one byte, bias 127); elements are FP8 E4M3 (one byte),
  * rounded to nearest even and saturated to +-448. A matrix [rows, cols] is
- * stored as codes [rows, cols] and scales [rows, cols/32], row-major.
+ * stored as codes uint8 [rows, cols], row-major, and scales in k-block-major
+ * order: 32-bit words [cols/128][rows4], rows4 = rows rounded up to a multiple
+ * of 4, byte j (j = 0..3, little-endian) of word [kb][r] being the scale of
+ * elements r, 128 kb + 32 j .. 128 kb + 32 j + 31 (rows4*cols/32 bytes; the
+ * words of rows rows..rows4-1 are padding, never written or read). A word is
+ * one row's scales for one 128-deep k-block of the block-scaled MMA; the GEMMs
+ * copy the words of a unit's rows for each k-block into shared memory with
+ * TMA, next to its operand tiles.
  * The MXFP8 calls need H and I multiples of 128 (else MOE_ERR_UNSUPPORTED).
  */
 
 /*
- * Quantize a bf16 [rows, cols] matrix (cols a multiple of 32) along its rows:
- * codes uint8 [rows, cols] (E4M3) and scales uint8 [rows, cols/32] (E8M0).
- * in and codes 16-byte aligned. For the weights, quantize w1 [E*2I, H] and
- * w2 [E*H, I] once per weight update and keep the result (the guide's
- * weight-quant cache); x is quantized every step (moe_forward_mx does it).
+ * Quantize a bf16 [rows, cols] matrix (cols a multiple of 128) along its rows:
+ * codes uint8 [rows, cols] (E4M3) and k-block-major scales (E8M0, words
+ * [cols/128][rows4], layout above). in, codes and scales 16-byte aligned.
+ * For the weights, quantize w1 as [E*2I, H] and w2 as [E*H, I] once per weight
+ * update and keep the result (the guide's weight-quant cache); x is quantized
+ * every step (moe_forward_mx does it).
  */
 moe_status_t moe_mx_quantize(const void *in, int64_t rows, int64_t cols, void *codes, void *scales,
                              void *stream);
@@ -494,8 +502,8 @@ moe_status_t moe_mx_quantize(const void *in, int64_t rows, int64_t cols, void *c
 /*
  * The dispatch of the MXFP8 path, fused into the quantization of x: routed row
  * r of the metadata (token t = perm_slot[r] / k) gets MXFP8 codes and scales of
- * x[t,:] in the workspace (x_codes [T*k, H], x_scales [T*k, H/32], routed
- * order), so stage 1 reads whole tiles. x bf16 [T,H]. Needs the metadata of
+ * x[t,:] in the workspace (x_codes [T*k, H]; x_scales words [H/128][rows4(T*k)];
+ * routed order), so stage 1 reads whole tiles. x bf16 [T,H]. Needs the metadata of
  * moe_routing_metadata in ws and flags containing MOE_SHAPE_MXFP8.
  */
 moe_status_t moe_mx_quantize_dispatch(const void *x, const moe_shape_t *shape, void *ws, size_t ws_bytes,
@@ -506,15 +514,17 @@ moe_status_t moe_mx_quantize_dispatch(const void *x, const moe_shape_t *shape, v
  * routed row r of expert e,
  *   h = X(x)[r,:] . X(w1)[e]^T (fp32 accumulate from E4M3 products scaled per block)
  *   a[r, i] = silu(h[i]) * h[I + i], then quantized per 32 columns of i
- * w1_codes / w1_scales [E,2I,H] / [E,2I,H/32]; a_codes / a_scales [T*k, I] /
- * [T*k, I/32] (outputs, routed order).
+ * w1_codes [E,2I,H] with w1_scales words [H/128][E*2I] (moe_mx_quantize of w1
+ * as [E*2I, H]); outputs a_codes [T*k, I] and a_scales words
+ * [I/128][rows4(T*k)] (routed order; rows4(T*k)*I/32 bytes).
  */
 moe_status_t moe_dispatch_gemm1_mx(const void *w1_codes, const void *w1_scales, const moe_shape_t *shape,
                                    void *a_codes, void *a_scales, void *ws, size_t ws_bytes, void *stream);
 
 /*
  * Stage 2 in MXFP8: o[r,:] = X(a)[r,:] . X(w2)[e]^T, y[t,:] = sum_j topk_w[t,j] o[row_of[t*k+j],:]
- * (bf16 y, fp32 sum). w2_codes / w2_scales [E,H,I] / [E,H,I/32].
+ * (bf16 y, fp32 sum). a_codes / a_scales as stage 1 writes them; w2_codes
+ * [E,H,I] with w2_scales words [I/128][E*H] (moe_mx_quantize of w2 as [E*H, I]).
  */
 moe_status_t moe_swiglu_gemm2_combine_mx(const void *a_codes, const void *a_scales, const float *topk_w,
                                          const void *w2_codes, const void *w2_scales,

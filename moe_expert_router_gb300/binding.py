@@ -301,11 +301,27 @@ def moe_backward(x, topk_idx, topk_w, w1, w2, h, dy, shp, dx, dw1, dw2, ws, w_r=
         _ptr(dtopk_w), _ptr(ws), _nbytes(ws), _stream(stream, ws)))
 
 
+def mx_scales_empty(shape, device):
+    """An uninitialised buffer for the k-block-major E8M0 scales of an MXFP8
+    tensor of `shape` (rows = the product of the leading dimensions, cols the
+    last, a multiple of 128): uint8 [cols / 128, *shape[:-1], 4] when rows is a
+    multiple of 4, else [cols / 128, rows rounded up to 4, 4] -- one 32-bit word
+    per row and 128-column block, rows consecutive within a block."""
+    shape = tuple(shape)
+    rows = 1
+    for d in shape[:-1]:
+        rows *= d
+    lead = shape[:-1] if rows % 4 == 0 else ((rows + 3) // 4 * 4,)
+    return torch.empty((shape[-1] // 128,) + lead + (4,), dtype=torch.uint8, device=device)
+
+
 def moe_mx_quantize(t, codes, scales, stream=None):
-    """MXFP8 quantization of a bf16 tensor along its last dimension (multiple of 32):
-    codes uint8 of the same shape, scales uint8 [..., cols / 32]."""
+    """MXFP8 quantization of a bf16 tensor along its last dimension (a multiple of
+    128): codes uint8 of the same shape, scales k-block-major (``mx_scales_empty``)."""
     cols = t.shape[-1]
     rows = t.numel() // cols if cols else 0
+    if codes.numel() != t.numel() or scales.numel() * 32 != (rows + 3) // 4 * 4 * cols:
+        raise ValueError("codes must match t and scales hold the k-block-major words of rows rounded up to 4")
     _check("moe_mx_quantize", load().moe_mx_quantize(_ptr(t), rows, cols, _ptr(codes), _ptr(scales),
                                                      _stream(stream, t)))
 

@@ -124,6 +124,23 @@ template <int MODE> constexpr int kSfBase = 2 * kUnitN<MODE>;
 constexpr int kSfStride = 16;
 static_assert(2 * 224 + STAGES * kSfStride <= 512, "MXFP8 scale factors must fit in tensor memory");
 static_assert(BK == 64, "the MXFP8 modes share the 128-byte stage rows of BK = 64");
+// MXFP8: each stage's scale words arrive by TMA with its operands, into the tail
+// of the stage's B slot (past the widest MXFP8 B tile, 224 rows x 128 bytes).
+// The scales are k-block-major 32-bit words (one per row and 128-deep k-block),
+// so a stage needs one word per A row and per B row. An A box starts at the
+// unit's first row rounded down to 4 words (a TMA copy starts on a 16-byte
+// boundary) and holds 132 words, so it covers the 128 rows of one half.
+constexpr uint32_t kSfSmemOff = 224 * 128;
+constexpr int kSfBoxA = kSfBoxRowsA;         // words per A box (132)
+constexpr uint32_t kSfA1 = 640;              // second half's A box (bytes from kSfSmemOff)
+constexpr uint32_t kSfB0 = 1280;             // B words: stage 1 gate rows, else all rows
+constexpr uint32_t kSfB1 = kSfB0 + 96 * 4;   // stage 1: up rows
+static_assert(kSfA1 >= kSfBoxA * 4 && kSfB0 >= kSfA1 + kSfBoxA * 4, "MXFP8 scale boxes overlap");
+static_assert(kSfSmemOff + kSfB0 + 224 * 4 <= static_cast<uint32_t>(B_BYTES), "MXFP8 scale words must fit the B slot");
+// bytes of one stage's scale boxes
+__host__ __device__ constexpr uint32_t sf_stage_bytes(int mode, bool two) {
+    return (two ? 2u : 1u) * kSfBoxA * 4u + (mode == kStage1Mx ? 2u * 96u * 4u : 224u * 4u);
+}
 
 // warps: 0 scheduler + TMA producer, 1 MMA issuer, 2..9 epilogue, 10..13 helpers
 template <int MODE>
@@ -139,6 +156,8 @@ struct __align__(1024) Smem {
     uint8_t stage_out[EPI_WARPS][32 * 128];  // per epilogue warp: one 32 x 64 or two 32 x 32 bf16 boxes
     uint64_t full[STAGES > kRingSlots ? STAGES : kRingSlots];   // stages, or ring slots (stages 1 / 2)
     uint64_t empty[STAGES > kRingSlots ? STAGES : kRingSlots];
+    uint64_t sf_full[STAGES];                // MXFP8: the stage's scale words have landed (TMA)
+    uint64_t sf_ready[STAGES];               // MXFP8: ... and are in tensor memory
     uint64_t acc_full;
     uint64_t acc_empty;
     uint64_t uq_full[UQ];
@@ -162,6 +181,8 @@ struct GemmMaps {
     CUtensorMap out;   // primary output
     CUtensorMap out2;  // kStage1SaveH: h gate half; dA: dH up half
     CUtensorMap out3;  // kStage1SaveH: h up half;   dA: w a
+    CUtensorMap sfa;   // MXFP8: k-block-major scale words of the A rows (32-bit, [K / 128][rows])
+    CUtensorMap sfb;   // MXFP8: ... of the B rows
 };
 
 struct GemmArgs {
@@ -180,9 +201,8 @@ struct GemmArgs {
     __nv_bfloat16 *out2, *out3; // kStage1SaveH: h gate / up halves; dA: dH up half, w a
     float *logits_part;         // router
     float *dtw_part;            // dA: [n_tiles, R] partial routing-weight gradients
-    const uint8_t *sfa;         // MXFP8: E8M0 scales of the A rows (x per token, or a per routed row)
-    const uint8_t *sfb;         // MXFP8: E8M0 scales of the weight rows
-    uint8_t *out_sf;            // stage 1 MXFP8: scales of a [R, I / 32]
+    uint8_t *out_sf;            // stage 1 MXFP8: scales of a, k-block-major over sf_rows rows
+    int64_t sf_rows;            // stage 1 MXFP8: rows of the scale arrays of x and a (T k rounded up to 4)
     int E, k, K;
     int n_out;                  // valid output columns
     int n_tiles;                // n-tiles per expert (grouped) or per row tile (router)
@@ -476,59 +496,30 @@ __device__ __forceinline__ void scaled_piece(uint32_t tacc, int c, float w, uint
         pk[i] = pack_bf16x2(w * __uint_as_float(v[2 * i]), w * __uint_as_float(v[2 * i + 1]));
 }
 
-// MXFP8 scale factors of one stage, this thread's lane of the 16 scale
-// columns: column j < 8 = A row 32 j + lane (j >= 4: the second half), column
-// 8 + j = B row 32 j + lane. Each word holds the four E8M0 codes of the stage's
-// K steps. Offsets are byte offsets of a row's scales (-1: none). The words of
-// the next stage are loaded while the current one is consumed, so the global
-// latency stays off the pipeline's critical path.
+// One stage's scale words, from the tail of its B slot, in the tensor-memory
+// columns the block-scaled MMA reads: column j < 8 = A row 32 j + lane (j >= 4:
+// the second half), column 8 + j = B row 32 j + lane (stage 1: j < 3 the gate
+// rows, 3..5 the matching up rows). Each word holds the four E8M0 codes of the
+// stage's K steps. Rows past the unit's rows or past n_out get 0 (2^-127), so
+// nothing outside the unit enters its accumulators' valid part.
 template <int MODE>
-__device__ __forceinline__ void load_scales(const GemmArgs &g, int kb, bool any, const int64_t (&a_off)[8],
-                                            const int64_t (&b_off)[8], uint32_t (&r)[16]) {
-    if constexpr (MODE == kWgradMx) {
-        // the weight-gradient operands' scales are k-block-major: the word of row c
-        // for k-block kb at [kb][c], so a warp's 32 consecutive rows are 128 bytes
-        const uint32_t *sa = reinterpret_cast<const uint32_t *>(g.sfa) + static_cast<int64_t>(kb) * g.m_total;
-        const uint32_t *sb = reinterpret_cast<const uint32_t *>(g.sfb) + static_cast<int64_t>(kb) * g.n_out;
-#pragma unroll
-        for (int j = 0; j < 8; ++j) r[j] = (any && a_off[j] >= 0) ? __ldg(sa + a_off[j]) : 0u;
-#pragma unroll
-        for (int j = 0; j < 8; ++j) r[8 + j] = (any && b_off[j] >= 0) ? __ldg(sb + b_off[j]) : 0u;
-        return;
-    }
-#pragma unroll
-    for (int j = 0; j < 8; ++j)
-        r[j] = (any && a_off[j] >= 0) ? __ldg(reinterpret_cast<const uint32_t *>(g.sfa + a_off[j]) + kb) : 0u;
-#pragma unroll
-    for (int j = 0; j < 8; ++j)
-        r[8 + j] = (any && b_off[j] >= 0) ? __ldg(reinterpret_cast<const uint32_t *>(g.sfb + b_off[j]) + kb) : 0u;
-}
-
-// Byte offsets of the scale rows a helper thread writes for unit t (see write_scales).
-template <int MODE>
-__device__ __forceinline__ void scale_rows(const GemmArgs &g, const Unit &t, int lane, int64_t (&a_off)[8],
-                                           int64_t (&b_off)[8]) {
-    // weight gradients: row indices into the k-block-major scale words; otherwise
-    // byte offsets of each row's scales
-    const int64_t ld = MODE == kWgradMx ? 1 : g.K / 32;
+__device__ __forceinline__ void stage_scale_words(uint32_t sf_smem, const Unit &t, int rem, int n0, int n_out,
+                                                  int lane, uint32_t (&r)[16]) {
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
-        const int r = 32 * j + lane;
-        a_off[j] = (r < t.rows) ? static_cast<int64_t>(t.row0 + r) * ld : -1;
+        const int row = 32 * j + lane;
+        const uint32_t off = (j < 4 ? 0u : kSfA1) + 4u * static_cast<uint32_t>(rem + (row & 127));
+        r[j] = row < t.rows ? ld_shared_u32(sf_smem + off) : 0u;
     }
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
-        b_off[j] = -1;
+        r[8 + j] = 0u;
         if constexpr (MODE == kStage1Mx) {
-            // gate rows, then the matching up rows, of the unit's 96-column slice
-            const int c = t.n * 96 + 32 * (j % 3) + lane;
-            if (j < 6 && c < g.n_out)
-                b_off[j] = (static_cast<int64_t>(t.e) * g.b_rows + c + (j >= 3 ? g.half : 0)) * ld;
+            const int c = 32 * (j % 3) + lane;
+            if (j < 6 && n0 + c < n_out) r[8 + j] = ld_shared_u32(sf_smem + (j < 3 ? kSfB0 : kSfB1) + 4u * c);
         } else {
-            // stage 2: weight rows of expert e; weight gradients (b_rows = 0): rows of
-            // the quantized operand, shared by every expert
-            const int c = t.n * kUnitN<MODE> + 32 * j + lane;
-            if (j < 7 && c < g.n_out) b_off[j] = (static_cast<int64_t>(t.e) * g.b_rows + c) * ld;
+            const int c = 32 * j + lane;
+            if (j < 7 && n0 + c < n_out) r[8 + j] = ld_shared_u32(sf_smem + kSfB0 + 4u * c);
         }
     }
 }
@@ -552,9 +543,12 @@ tc_gemm_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs g) {
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < (STAGES > kRingSlots ? STAGES : kRingSlots); ++s) {
-            // MXFP8: the producer's expect_tx arrival plus one per scale-factor thread
-            mbar_init(smem_addr(&sm.full[s]), kIsMx<MODE> ? 1 + HELPER_THREADS : 1);
+            mbar_init(smem_addr(&sm.full[s]), 1);
             mbar_init(smem_addr(&sm.empty[s]), 1);
+        }
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(smem_addr(&sm.sf_full[s]), 1);
+            mbar_init(smem_addr(&sm.sf_ready[s]), HELPER_THREADS);
         }
         mbar_init(smem_addr(&sm.acc_full), 1);
         mbar_init(smem_addr(&sm.acc_empty), EPI_THREADS);
@@ -569,6 +563,10 @@ tc_gemm_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs g) {
         fence_mbar_init();
         tma_prefetch_desc(&maps.a);
         tma_prefetch_desc(&maps.b);
+        if constexpr (kIsMx<MODE>) {
+            tma_prefetch_desc(&maps.sfa);
+            tma_prefetch_desc(&maps.sfb);
+        }
     }
     if (warp == 1) {
         tmem_alloc(smem_addr(&sm.tmem_base), TMEM_COLS);
@@ -659,6 +657,25 @@ tc_gemm_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs g) {
                     sb = smem_addr(sm.b[stage]);
                 }
                 if (lane == 0) {
+                    if constexpr (kIsMx<MODE>) {
+                        // first the stage's scale words (their own barrier, so that the
+                        // helper warps can move them into tensor memory while the
+                        // operand tiles are still in flight): k-block kb of the unit's A
+                        // rows (from the first row rounded down to 4 words) and B rows
+                        const uint32_t sff = smem_addr(&sm.sf_full[stage]);
+                        const uint32_t sfs = sb + kSfSmemOff;
+                        const int ax = t.row0 & ~3;
+                        mbar_arrive_expect_tx(sff, sf_stage_bytes(MODE, two));
+                        tma_load_2d(sfs, &maps.sfa, ax, kb, sff);
+                        if (two) tma_load_2d(sfs + kSfA1, &maps.sfa, ax + BM, kb, sff);
+                        if constexpr (MODE == kStage1Mx) {
+                            const int row = t.e * g.b_rows + t.n * (kUnitN<MODE> / 2);
+                            tma_load_2d(sfs + kSfB0, &maps.sfb, row, kb, sff);              // gate rows
+                            tma_load_2d(sfs + kSfB1, &maps.sfb, row + g.half, kb, sff);     // up rows
+                        } else {
+                            tma_load_2d(sfs + kSfB0, &maps.sfb, t.e * g.b_rows + t.n * kUnitN<MODE>, kb, sff);
+                        }
+                    }
                     mbar_arrive_expect_tx(full, tx_bytes);
                     if constexpr (kIsStage1<MODE>) {
                         constexpr int hn = kUnitN<MODE> / 2;                                 // gate (= up) rows
@@ -742,6 +759,7 @@ tc_gemm_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs g) {
                 for (int i = 0; i < min(issued, STAGES); ++i) {
                     if (--s < 0) { s = STAGES - 1; ph ^= 1u; }
                     drain_wait(smem_addr(&sm.full[s]), ph);
+                    if constexpr (kIsMx<MODE>) drain_wait(smem_addr(&sm.sf_full[s]), ph);
                 }
             }
         }
@@ -788,6 +806,13 @@ tc_gemm_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs g) {
                     if (!mbar_wait(full_bar, fparity, abort_flag, g.err)) {
                         ok = false;
                         break;
+                    }
+                    if constexpr (kIsMx<MODE>) {
+                        // ... and the helper warps have put its scale factors in tensor memory
+                        if (!mbar_wait(smem_addr(&sm.sf_ready[stage]), fparity, abort_flag, g.err)) {
+                            ok = false;
+                            break;
+                        }
                     }
                     tc_fence_after();
                     if constexpr (kWeightGrad<MODE>) {
@@ -935,7 +960,10 @@ tc_gemm_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs g) {
                             uint4 *dst = reinterpret_cast<uint4 *>(reinterpret_cast<uint8_t *>(g.out) + r * g.n_out + col0 + c);
                             dst[0] = make_uint4(q[0], q[1], q[2], q[3]);
                             dst[1] = make_uint4(q[4], q[5], q[6], q[7]);
-                            g.out_sf[r * (g.n_out / 32) + (col0 + c) / 32] = static_cast<uint8_t>(sc);
+                            // k-block-major scales: byte (col / 32) % 4 of word [col / 128][r]
+                            const int col = col0 + c;
+                            g.out_sf[((static_cast<int64_t>(col >> 7) * g.sf_rows + r) << 2) + ((col >> 5) & 3)] =
+                                static_cast<uint8_t>(sc);
                         }
                     }
                 } else if constexpr (MODE == kStage2Mx) {
@@ -1318,22 +1346,27 @@ tc_gemm_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs g) {
                 }
                 stage = (stage + nkb) % STAGES;
             } else if constexpr (kIsMx<MODE>) {
-                // A and B arrive through TMA; these warps only write the scale factors
-                int64_t a_off[8], b_off[8];
-                uint32_t sfw[16];
-                scale_rows<MODE>(g, t, lane, a_off, b_off);
-                load_scales<MODE>(g, t.kb0, t.kb0 < t.kb1, a_off, b_off, sfw);
+                // A, B and their scale words arrive through TMA, the scale words on
+                // their own barrier; these warps move them into tensor memory and
+                // then release the stage's scale factors to the MMA issuer
+                const int rem = t.row0 & 3;                 // the A boxes start 16-byte aligned
+                const int n0 = t.n * (MODE == kStage1Mx ? kUnitN<MODE> / 2 : kUnitN<MODE>);
                 const uint32_t sf_lane = tmem_base + (static_cast<uint32_t>((warp & 3) * 32) << 16) + kSfBase<MODE>;
                 for (int kb = t.kb0; kb < t.kb1; ++kb) {
-                    if (lane == 0) ok = mbar_wait(smem_addr(&sm.empty[stage]), phase ^ 1u, abort_flag, g.err);
+                    const uint32_t sff = smem_addr(&sm.sf_full[stage]);
+                    if (lane == 0) ok = mbar_wait(sff, phase, abort_flag, g.err);
                     ok = __shfl_sync(0xffffffffu, ok, 0);
                     if (!ok) break;
+                    // the phase is complete (the stage cannot be refilled before this
+                    // warp's release below); every lane observes it before reading
+                    (void)mbar_try_wait(sff, phase);
+                    uint32_t sfw[16];
+                    stage_scale_words<MODE>(smem_addr(sm.b[stage]) + kSfSmemOff, t, rem, n0, g.n_out, lane, sfw);
                     tc_fence_after();
                     tmem_st16(sf_lane + stage * kSfStride, sfw);
-                    load_scales<MODE>(g, kb + 1, kb + 1 < t.kb1, a_off, b_off, sfw);
                     tmem_wait_st();
                     tc_fence_before();
-                    mbar_arrive(smem_addr(&sm.full[stage]));
+                    mbar_arrive(smem_addr(&sm.sf_ready[stage]));
                     if (++stage == STAGES) { stage = 0; phase ^= 1u; }
                 }
             }
@@ -1375,9 +1408,8 @@ inline GemmArgs grouped_args(const GemmLaunch &p) {
     g.out2 = p.out2;
     g.out3 = p.out3;
     g.dtw_part = p.dtw_part;
-    g.sfa = p.sfa;
-    g.sfb = p.sfb;
     g.out_sf = p.out_sf;
+    g.sf_rows = p.sf_rows;
     g.bpack = p.bpack;
     g.kpad = p.kpad;
     g.kb_tiles = (p.K + BK - 1) / BK;
@@ -1403,6 +1435,8 @@ inline GemmMaps maps_of(const GemmLaunch &p) {
     m.out = *p.tm_out;
     m.out2 = *(p.tm_out2 ? p.tm_out2 : p.tm_out);
     m.out3 = *(p.tm_out3 ? p.tm_out3 : p.tm_out);
+    m.sfa = *(p.tm_sfa ? p.tm_sfa : p.tm_b);
+    m.sfb = *(p.tm_sfb ? p.tm_sfb : p.tm_b);
     return m;
 }
 

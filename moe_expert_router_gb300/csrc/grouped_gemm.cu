@@ -103,6 +103,8 @@ cudaError_t launch_router_gemm(const RouterGemmLaunch &p, cudaStream_t st) {
     m.out = *p.tm_w3;
     m.out2 = *p.tm_w3;
     m.out3 = *p.tm_w3;
+    m.sfa = *p.tm_w3;
+    m.sfb = *p.tm_w3;
     return launch_tc_gemm<kRouter>(m, g, grid, st);
 }
 

@@ -9,12 +9,21 @@ namespace moe {
 
 namespace {
 
+// Byte of block c (columns 32 c .. 32 c + 31) of row r in k-block-major scales
+// over sf_rows rows: byte c % 4 of the 32-bit word [c / 4][r], one word per row
+// and 128-column k-block of the block-scaled MMA.
+__device__ __forceinline__ int64_t kmajor_scale_byte(int64_t r, int64_t c, int64_t sf_rows) {
+    return (((c >> 2) * sf_rows + r) << 2) + (c & 3);
+}
+
 // One thread per 32-element block; block b of a row-major [rows, cols] matrix
-// (cols % 32 == 0) is elements [32 b, 32 b + 32) and scale b.
+// (cols % 128 == 0) is elements [32 b, 32 b + 32) of the codes; the scales are
+// k-block-major over sf_rows (rows rounded up to 4) rows.
 __global__ void __launch_bounds__(256)
-mx_quantize_kernel(const __nv_bfloat16 *__restrict__ in, int64_t blocks, uint8_t *__restrict__ codes,
-                   uint8_t *__restrict__ scales) {
+mx_quantize_kernel(const __nv_bfloat16 *__restrict__ in, int64_t rows, int64_t per_row, int64_t sf_rows,
+                   uint8_t *__restrict__ codes, uint8_t *__restrict__ scales) {
     griddep_wait();
+    const int64_t blocks = rows * per_row;
     for (int64_t b = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; b < blocks;
          b += static_cast<int64_t>(gridDim.x) * blockDim.x) {
         const uint4 *src = reinterpret_cast<const uint4 *>(in + b * 32);
@@ -34,18 +43,19 @@ mx_quantize_kernel(const __nv_bfloat16 *__restrict__ in, int64_t blocks, uint8_t
         uint4 *dst = reinterpret_cast<uint4 *>(codes + b * 32);
         dst[0] = make_uint4(qw[0], qw[1], qw[2], qw[3]);
         dst[1] = make_uint4(qw[4], qw[5], qw[6], qw[7]);
-        scales[b] = static_cast<uint8_t>(sc);
+        const int64_t r = b / per_row;
+        scales[kmajor_scale_byte(r, b - r * per_row, sf_rows)] = static_cast<uint8_t>(sc);
     }
 }
 
 // The dispatch of the MXFP8 path, fused into the quantization of x: routed
 // row r (r < *routed) is token perm_slot[r] / k, quantized into row r of
-// codes [R, cols] and scales [R, cols / 32], so stage 1 reads its A tiles with
-// plain TMA copies.
+// codes [R, cols] and of the k-block-major scales over sf_rows rows (R rounded
+// up to 4), so stage 1 reads its A tiles and scale words with plain TMA copies.
 __global__ void __launch_bounds__(256)
 mx_quantize_dispatch_kernel(const __nv_bfloat16 *__restrict__ x, const int32_t *__restrict__ perm_slot,
-                            const int32_t *__restrict__ routed, int k, int64_t cols, uint8_t *__restrict__ codes,
-                            uint8_t *__restrict__ scales) {
+                            const int32_t *__restrict__ routed, int k, int64_t sf_rows, int64_t cols,
+                            uint8_t *__restrict__ codes, uint8_t *__restrict__ scales) {
     griddep_wait();
     const int64_t per_row = cols / 32;
     const int64_t blocks = static_cast<int64_t>(*routed) * per_row;
@@ -71,7 +81,7 @@ mx_quantize_dispatch_kernel(const __nv_bfloat16 *__restrict__ x, const int32_t *
         uint4 *dst = reinterpret_cast<uint4 *>(codes + b * 32);
         dst[0] = make_uint4(qw[0], qw[1], qw[2], qw[3]);
         dst[1] = make_uint4(qw[4], qw[5], qw[6], qw[7]);
-        scales[b] = static_cast<uint8_t>(sc);
+        scales[kmajor_scale_byte(r, c, sf_rows)] = static_cast<uint8_t>(sc);
     }
 }
 
@@ -201,7 +211,7 @@ cudaError_t launch_mx_quantize_dispatch(const __nv_bfloat16 *x, const int32_t *p
     int64_t grid = (blocks + 255) / 256;
     if (grid > 152 * 16) grid = 152 * 16;
     const cudaError_t e = launch_dep(mx_quantize_dispatch_kernel, dim3(static_cast<int>(grid)), dim3(256), 0, st, x,
-                                     perm_slot, routed, k, cols, codes, scales);
+                                     perm_slot, routed, k, static_cast<int64_t>(mx_rows(R)), cols, codes, scales);
     note_launches(1);
     return e;
 }
@@ -222,8 +232,8 @@ cudaError_t launch_mx_quantize(const __nv_bfloat16 *in, int64_t rows, int64_t co
     if (blocks == 0) return cudaSuccess;
     int64_t grid = (blocks + 255) / 256;
     if (grid > 152 * 16) grid = 152 * 16;
-    const cudaError_t e = launch_dep(mx_quantize_kernel, dim3(static_cast<int>(grid)), dim3(256), 0, st, in, blocks,
-                                     codes, scales);
+    const cudaError_t e = launch_dep(mx_quantize_kernel, dim3(static_cast<int>(grid)), dim3(256), 0, st, in, rows,
+                                     cols / 32, static_cast<int64_t>(mx_rows(rows)), codes, scales);
     note_launches(1);
     return e;
 }

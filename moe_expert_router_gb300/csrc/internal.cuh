@@ -17,6 +17,9 @@ namespace moe {
 // counts row tiles in units of kUnitM, so every grouped GEMM uses that value.
 constexpr int kBM = 128;
 constexpr int kUnitM = 256;
+// MXFP8: words of a TMA box of one 128-row half's scale words (128 rows plus up
+// to 3 before them, the box starting at the half's first row rounded down to 4)
+constexpr int kSfBoxRowsA = kBM + 4;
 // Reduction depth of one pipeline stage: 32 bf16 = 64-byte rows with the 64-byte
 // swizzle (six 32 KB stages), or 64 = 128-byte rows with the 128-byte swizzle
 // (three 64 KB stages).
@@ -172,8 +175,10 @@ struct GemmLaunch {
     __nv_bfloat16 *out;         // row-grouped output (masked stores of partial slabs)
     __nv_bfloat16 *out2, *out3; // stage 1 with h: h gate / up halves; dA: dH up half, w a
     float *dtw_part;            // dA: [ceil(I / 256), R]
-    const uint8_t *sfa, *sfb;   // MXFP8: E8M0 scales of the A rows and of the weight rows
-    uint8_t *out_sf;            // stage 1 MXFP8: E8M0 scales of a [R, I / 32]
+    const CUtensorMap *tm_sfa;  // MXFP8: k-block-major scale words of the A rows, box 132 x 1
+    const CUtensorMap *tm_sfb;  // MXFP8: ... of the B rows, box 96 x 1 (stage 1) or 224 x 1
+    uint8_t *out_sf;            // stage 1 MXFP8: E8M0 scales of a, k-block-major [I / 128][sf_rows] words
+    int64_t sf_rows;            // stage 1 MXFP8: rows of the scale arrays of x and a (T k rounded up to 4)
     int E, k;
     int K;                      // reduction length of the row-grouped modes
     int n_out;                  // output columns
@@ -323,6 +328,12 @@ cudaError_t launch_gemm1_mx(const GemmLaunch &p, cudaStream_t st);
 cudaError_t launch_gemm2_mx(const GemmLaunch &p, cudaStream_t st);
 cudaError_t setup_mx_gemm_kernels();
 
+// MXFP8 scale words ([k_blocks][rows] 32-bit words, k-block-major; rows a
+// multiple of 4), boxes of box_rows words of one k-block, unswizzled.
+bool encode_sf_words(CUtensorMap *map, const void *base, uint64_t rows, uint64_t k_blocks, uint32_t box_rows);
+// Rows of the k-block-major MXFP8 scale array of a matrix with `rows` rows
+// (rounded up to 4, so that each k-block's words start 16-byte aligned).
+inline uint64_t mx_rows(uint64_t rows) { return (rows + 3) & ~static_cast<uint64_t>(3); }
 // uint8 tensor [rows, inner] (e.g. E4M3 codes) with a box_inner x box_rows box,
 // 128-byte swizzle (box_inner = 128).
 bool encode_u8_2d(CUtensorMap *map, const void *base, uint64_t inner, uint64_t rows, uint32_t box_inner,

@@ -107,9 +107,10 @@ moe_ws_layout_t make_layout(const moe_shape_t &s) {
     }
     if (s.flags & MOE_SHAPE_MXFP8) {
         L.x_codes = off;  off = align256(off + R * H);
-        L.x_scales = off; off = align256(off + R * (H / 32));
+        // scales: k-block-major words over the routed rows rounded up to 4
+        L.x_scales = off; off = align256(off + mx_rows(R) * (H / 32));
         L.a_codes = off;  off = align256(off + R * I);
-        L.a_scales = off; off = align256(off + R * (I / 32));
+        L.a_scales = off; off = align256(off + mx_rows(R) * (I / 32));
     } else {
         L.x_codes = L.x_scales = L.a_codes = L.a_scales = off;
     }
@@ -348,16 +349,19 @@ moe_status_t run_gemm2(const moe_shape_t &s, const void *a, const float *topk_w,
 moe_status_t run_gemm1_mx(const moe_shape_t &s, const void *w1q, const void *w1s, void *aq, void *as, void *h,
                           const Ws &w, const DeviceState &d, cudaStream_t st) {
     const uint64_t R = static_cast<uint64_t>(s.T) * s.k;
-    CUtensorMap tm_x, tm_w1;
+    CUtensorMap tm_x, tm_w1, tm_xs, tm_w1s;
     if (!encode_u8_2d(&tm_x, w.x_codes, s.H, R, 128, 128) ||
-        !encode_u8_2d(&tm_w1, w1q, s.H, static_cast<uint64_t>(s.E) * 2 * s.I, 128, 96))
+        !encode_u8_2d(&tm_w1, w1q, s.H, static_cast<uint64_t>(s.E) * 2 * s.I, 128, 96) ||
+        !encode_sf_words(&tm_xs, w.x_scales, mx_rows(R), s.H / 128, kSfBoxRowsA) ||
+        !encode_sf_words(&tm_w1s, w1s, static_cast<uint64_t>(s.E) * 2 * s.I, s.H / 128, 96))
         return MOE_ERR_CUDA;
     GemmLaunch p = base_launch(s, w, d);
     p.tm_a = &tm_x;
     p.tm_b = &tm_w1;
     p.tm_out = &tm_w1;
-    p.sfa = w.x_scales;
-    p.sfb = static_cast<const uint8_t *>(w1s);
+    p.tm_sfa = &tm_xs;
+    p.tm_sfb = &tm_w1s;
+    p.sf_rows = static_cast<int64_t>(mx_rows(R));         // the scale rows of x and a
     p.sched = w.sched1;
     p.out = static_cast<__nv_bfloat16 *>(aq);             // E4M3 codes [R, I]
     p.out_sf = static_cast<uint8_t *>(as);
@@ -383,17 +387,19 @@ moe_status_t run_gemm2_mx(const moe_shape_t &s, const void *aq, const void *as, 
                           const void *w2q, const void *w2s, void *y, const Ws &w, const DeviceState &d,
                           cudaStream_t st) {
     const uint64_t R = static_cast<uint64_t>(s.T) * s.k;
-    CUtensorMap tm_a, tm_w2, tm_out;
+    CUtensorMap tm_a, tm_w2, tm_out, tm_as, tm_w2s;
     if (!encode_u8_2d(&tm_a, aq, s.I, R, 128, 128) ||
         !encode_u8_2d(&tm_w2, w2q, s.I, static_cast<uint64_t>(s.E) * s.H, 128, 224) ||
-        !encode_bf16_2d(&tm_out, w.obuf, s.H, R, 32, 32))
+        !encode_bf16_2d(&tm_out, w.obuf, s.H, R, 32, 32) ||
+        !encode_sf_words(&tm_as, as, mx_rows(R), s.I / 128, kSfBoxRowsA) ||
+        !encode_sf_words(&tm_w2s, w2s, static_cast<uint64_t>(s.E) * s.H, s.I / 128, 224))
         return MOE_ERR_CUDA;
     GemmLaunch p = base_launch(s, w, d);
     p.tm_a = &tm_a;
     p.tm_b = &tm_w2;
     p.tm_out = &tm_out;
-    p.sfa = static_cast<const uint8_t *>(as);
-    p.sfb = static_cast<const uint8_t *>(w2s);
+    p.tm_sfa = &tm_as;
+    p.tm_sfb = &tm_w2s;
     p.sched = w.sched2;
     p.topk_w = topk_w;
     p.out = w.obuf;
@@ -577,17 +583,19 @@ moe_status_t run_bwd_stage1_weight(const moe_shape_t &s, void *dw1, const Ws &w,
 moe_status_t run_wgrad_mx(const moe_shape_t &s, const MxWgradWs &m, const uint8_t *a_c, const uint8_t *a_s,
                           int64_t a_cols, const uint8_t *b_c, const uint8_t *b_s, int64_t b_cols, void *dw,
                           int32_t *sched, const Ws &w, const DeviceState &d, cudaStream_t st) {
-    CUtensorMap tm_a, tm_b, tm_dw;
+    CUtensorMap tm_a, tm_b, tm_dw, tm_as, tm_bs;
     if (!encode_u8_2d(&tm_a, a_c, m.ld, a_cols, 128, 128) || !encode_u8_2d(&tm_b, b_c, m.ld, b_cols, 128, 224) ||
-        !encode_bf16_3d(&tm_dw, dw, b_cols, a_cols, s.E, 32, 32))
+        !encode_bf16_3d(&tm_dw, dw, b_cols, a_cols, s.E, 32, 32) ||
+        !encode_sf_words(&tm_as, a_s, a_cols, m.ld / 128, kSfBoxRowsA) ||
+        !encode_sf_words(&tm_bs, b_s, b_cols, m.ld / 128, 224))
         return MOE_ERR_CUDA;
     GemmLaunch q = base_launch(s, w, d);
     q.tm_a = &tm_a;
     q.tm_b = &tm_b;
     q.tm_out = &tm_dw;
     q.kpad = m.kpad;
-    q.sfa = a_s;
-    q.sfb = b_s;
+    q.tm_sfa = &tm_as;
+    q.tm_sfb = &tm_bs;
     q.sched = sched;
     q.K = static_cast<int>(m.ld);     // scale bytes per operand row: K / 32
     q.n_out = static_cast<int>(b_cols);
@@ -711,6 +719,17 @@ bool encode_u8_2d(CUtensorMap *map, const void *base, uint64_t inner, uint64_t r
     cuuint32_t estr[2] = {1, 1};
     return g_encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims, strides, box, estr,
                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool encode_sf_words(CUtensorMap *map, const void *base, uint64_t rows, uint64_t k_blocks, uint32_t box_rows) {
+    if (!encode_ready() || rows % 4 != 0) return false;
+    cuuint64_t dims[2] = {rows, k_blocks};
+    cuuint64_t strides[1] = {rows * 4};
+    cuuint32_t box[2] = {box_rows, 1};
+    cuuint32_t estr[2] = {1, 1};
+    return g_encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<void *>(base), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -1101,9 +1120,10 @@ moe_status_t moe_backward(const void *x, const float *w_r, const float *logits, 
 
 moe_status_t moe_mx_quantize(const void *in, int64_t rows, int64_t cols, void *codes, void *scales,
                              void *stream) {
-    if (rows < 0 || cols <= 0 || cols % 32 != 0) return MOE_ERR_INVALID_ARG;
+    if (rows < 0 || cols <= 0 || cols % 128 != 0) return MOE_ERR_INVALID_ARG;
     if (rows == 0) return MOE_OK;
-    if (in == nullptr || codes == nullptr || scales == nullptr || !aligned16(in) || !aligned16(codes))
+    if (in == nullptr || codes == nullptr || scales == nullptr || !aligned16(in) || !aligned16(codes) ||
+        !aligned16(scales))
         return MOE_ERR_INVALID_ARG;
     DeviceState *d = nullptr;
     moe_status_t r = device_state(&d);

@@ -15,9 +15,10 @@ from . import binding as B
 
 
 def _gpu_quantize(w: torch.Tensor):
-    """codes, scales of a bf16 [E, rows, K] weight, quantized along K by libmoe."""
+    """codes, scales of a bf16 [E, rows, K] weight, quantized along K by libmoe
+    (scales k-block-major: [K / 128, E, rows, 4])."""
     codes = torch.empty(w.shape, dtype=torch.uint8, device=w.device)
-    scales = torch.empty(w.shape[:-1] + (w.shape[-1] // 32,), dtype=torch.uint8, device=w.device)
+    scales = B.mx_scales_empty(w.shape, w.device)
     B.moe_mx_quantize(w, codes, scales)
     return codes, scales
 

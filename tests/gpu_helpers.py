@@ -40,6 +40,17 @@ def assert_close_y(y_gpu, y_ref, what="y"):
     return rel, max_abs
 
 
+def kmajor_scales_to_rows(s, rows=None):
+    """MXFP8 scales in the library's k-block-major layout, uint8 [cols / 128, *lead, 4],
+    as the row-major [*lead, cols / 32] the oracle's quantizer returns (only the
+    first `rows` rows when given, dropping the padding to a multiple of 4): byte j
+    of word [kb][r] is the scale of columns 128 kb + 32 j .. + 31 of row r."""
+    s = np.asarray(s)
+    lead = s.shape[1:-1]
+    out = np.moveaxis(s, 0, -2).reshape(lead + (s.shape[0] * 4,))
+    return out if rows is None else out.reshape(-1, out.shape[-1])[:rows]
+
+
 def ws_view(ws, layout_off, count, dtype=torch.int32):
     """A typed view of `count` elements of the workspace at byte offset `layout_off`."""
     nbytes = count * torch.tensor([], dtype=dtype).element_size()

@@ -12,7 +12,7 @@ import pytest
 import torch
 
 import oracle
-from gpu_helpers import MAX_ABS_FRAC, assert_close_y, read_metadata, tile_sample_tokens
+from gpu_helpers import MAX_ABS_FRAC, assert_close_y, kmajor_scales_to_rows, read_metadata, tile_sample_tokens
 from moe_expert_router_gb300 import binding as B
 from moe_expert_router_gb300.workloads import CONFIGS, MoEConfig, generate, routing_with_counts
 
@@ -29,8 +29,9 @@ def _device():
 
 
 def gpu_quantize(t):
+    """codes [..., cols] and k-block-major scales [cols / 128, ..., 4] of t."""
     codes = torch.empty(t.shape, dtype=torch.uint8, device=DEV)
-    scales = torch.empty(t.shape[:-1] + (t.shape[-1] // 32,), dtype=torch.uint8, device=DEV)
+    scales = B.mx_scales_empty(t.shape, DEV)
     B.moe_mx_quantize(t, codes, scales)
     return codes, scales
 
@@ -51,7 +52,7 @@ def test_quantizer_bit_exact(kind):
     xb = x.to(torch.bfloat16)
     codes, scales = gpu_quantize(xb.to(DEV))
     rc, rs = oracle.mx_quantize(xb)
-    np.testing.assert_array_equal(scales.cpu().numpy(), rs)
+    np.testing.assert_array_equal(kmajor_scales_to_rows(scales.cpu().numpy(), rows=xb.shape[0]), rs)
     np.testing.assert_array_equal(codes.cpu().numpy(), rc)
 
 
@@ -72,7 +73,9 @@ def mx_inputs(cfg, seed=0, idx=None, w=None):
     E, I, H = cfg.E, cfg.I, cfg.H
     w1q, w1s = gpu_quantize(inp["w1"].view(E * 2 * I, H))
     w2q, w2s = gpu_quantize(inp["w2"].view(E * H, I))
-    return inp, idx, w, w1q.view(E, 2 * I, H), w1s.view(E, 2 * I, H // 32), w2q.view(E, H, I), w2s.view(E, H, I // 32)
+    # scales k-block-major: [H / 128, E, 2I, 4] and [I / 128, E, H, 4]
+    return (inp, idx, w, w1q.view(E, 2 * I, H), w1s.view(H // 128, E, 2 * I, 4), w2q.view(E, H, I),
+            w2s.view(I // 128, E, H, 4))
 
 
 def oracle_weights(inp, cfg, experts=None):
@@ -93,7 +96,7 @@ def run_mx(cfg, inp, idx, w, w1q, w1s, w2q, w2s, staged):
     y = torch.empty((cfg.T, cfg.H), dtype=torch.bfloat16, device=DEV)
     R = cfg.T * cfg.k
     aq = torch.empty((R, cfg.I), dtype=torch.uint8, device=DEV)
-    as_ = torch.empty((R, cfg.I // 32), dtype=torch.uint8, device=DEV)
+    as_ = B.mx_scales_empty((R, cfg.I), DEV)
     if staged:
         B.moe_routing_metadata(idx, shp, ws)
         B.moe_mx_quantize_dispatch(inp["x"], shp, ws)
@@ -103,7 +106,8 @@ def run_mx(cfg, inp, idx, w, w1q, w1s, w2q, w2s, staged):
         B.moe_forward_mx(inp["x"], idx, w, w1q, w1s, w2q, w2s, shp, y, ws)
         L = B.moe_workspace_layout(shp)
         aq = ws[L.a_codes:L.a_codes + R * cfg.I].view(R, cfg.I)
-        as_ = ws[L.a_scales:L.a_scales + R * cfg.I // 32].view(R, cfg.I // 32)
+        R4 = (R + 3) // 4 * 4
+        as_ = ws[L.a_scales:L.a_scales + R4 * cfg.I // 32].view(cfg.I // 128, R4, 4)
     err = B.moe_get_device_error(ws)
     return y, aq, as_, ws, shp, err
 
@@ -115,6 +119,8 @@ CASES = {
     "sigmoid_groups": _cfg(128, 256, 640, 16, 4, score="sigmoid", scale=2.5, n_group=4, topk_group=2,
                            sel_bias=True),
     "one_token": _cfg(1, 128, 128, 4, 2),
+    # T k = 999: the scale arrays' rows are padded to 1000 (k-block-major words)
+    "odd_rows": _cfg(333, 384, 256, 5, 3),
 }
 
 
@@ -128,7 +134,9 @@ def test_quantizing_dispatch_is_the_quantizer_in_routed_order():
     L = B.moe_workspace_layout(shp)
     R = cfg.T * cfg.k
     codes = ws[L.x_codes:L.x_codes + R * cfg.H].view(R, cfg.H).cpu().numpy()
-    scales = ws[L.x_scales:L.x_scales + R * cfg.H // 32].view(R, cfg.H // 32).cpu().numpy()
+    R4 = (R + 3) // 4 * 4
+    scales = kmajor_scales_to_rows(ws[L.x_scales:L.x_scales + R4 * cfg.H // 32].view(cfg.H // 128, R4, 4).cpu().numpy(),
+                                   rows=R)
     _, _, _, perm, _ = read_metadata(ws, shp)
     rc, rs = oracle.mx_quantize(inp["x"])
     tok = perm // cfg.k
@@ -146,8 +154,10 @@ def test_mx_forward_matches_oracle(name, staged):
     xq, xs = oracle.mx_quantize(inp["x"])
     o1q, o1s, o2q, o2s = oracle_weights(inp, cfg)
     # the weight quantization the GPU path was given is the oracle's, bit for bit
-    for gq, oq in ((w1q, o1q), (w1s, o1s), (w2q, o2q), (w2s, o2s)):
+    for gq, oq in ((w1q, o1q), (w2q, o2q)):
         np.testing.assert_array_equal(gq.cpu().numpy(), oq)
+    for gs, os_ in ((w1s, o1s), (w2s, o2s)):
+        np.testing.assert_array_equal(kmajor_scales_to_rows(gs.cpu().numpy()), os_)
     y_ref, _, ac_ref, as_ref = oracle.expert_forward_mx(xq, xs, idx.cpu(), w.cpu().double(), o1q, o1s, o2q, o2s,
                                                         want_a=True)
     assert_close_y(y, y_ref, "y (MXFP8)")
@@ -155,7 +165,7 @@ def test_mx_forward_matches_oracle(name, staged):
     _, _, _, perm, _ = read_metadata(ws, shp)
     g_codes = aq.cpu().numpy()[: len(perm)]
     r_codes = ac_ref[perm]
-    g_sc = as_.cpu().numpy()[: len(perm)]
+    g_sc = kmajor_scales_to_rows(as_.cpu().numpy(), rows=cfg.T * cfg.k)[: len(perm)]
     r_sc = as_ref[perm]
     assert (g_sc != r_sc).mean() <= 0.01, "block scales of a differ too often"
     same = np.repeat(g_sc == r_sc, 32, axis=1)
@@ -181,8 +191,8 @@ def test_mx_unused_experts_with_nan_codes_are_never_read():
         if c == 0:
             w1q[e] = 0x7F      # E4M3 NaN
             w2q[e] = 0x7F
-            w1s[e] = 0xFF      # E8M0 NaN
-            w2s[e] = 0xFF
+            w1s[:, e] = 0xFF   # E8M0 NaN (scales are [K / 128, E, rows, 4])
+            w2s[:, e] = 0xFF
     y1, *_rest, err = run_mx(cfg, inp, idx, w, w1q, w1s, w2q, w2s, staged=True)
     assert err == 0
     assert torch.isfinite(y1.float()).all()
@@ -234,7 +244,7 @@ def mx_train_step(cfg, inp, idx, w, w1q, w1s, w2q, w2s):
     ws = B.new_workspace(shp, DEV)
     R = T * k
     aq = torch.empty((R, I), dtype=torch.uint8, device=DEV)
-    as_ = torch.empty((R, I // 32), dtype=torch.uint8, device=DEV)
+    as_ = B.mx_scales_empty((R, I), DEV)
     h = torch.empty((R, 2 * I), dtype=torch.bfloat16, device=DEV)
     y = torch.empty((T, H), dtype=torch.bfloat16, device=DEV)
     dx = torch.empty((T, H), dtype=torch.bfloat16, device=DEV)
