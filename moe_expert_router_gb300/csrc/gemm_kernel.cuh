@@ -157,7 +157,7 @@ struct __align__(1024) Smem {
     uint64_t full[STAGES > kRingSlots ? STAGES : kRingSlots];   // stages, or ring slots (stages 1 / 2)
     uint64_t empty[STAGES > kRingSlots ? STAGES : kRingSlots];
     uint64_t sf_full[STAGES];                // MXFP8: the stage's scale words have landed (TMA)
-    uint64_t sf_ready[STAGES];               // MXFP8: ... and are in tensor memory
+    uint64_t sf_ready[STAGES];               // MXFP8: ... and are in tensor memory (one arrival per helper warp)
     uint64_t acc_full;
     uint64_t acc_empty;
     uint64_t uq_full[UQ];
@@ -548,7 +548,7 @@ tc_gemm_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs g) {
         }
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(smem_addr(&sm.sf_full[s]), 1);
-            mbar_init(smem_addr(&sm.sf_ready[s]), HELPER_THREADS);
+            mbar_init(smem_addr(&sm.sf_ready[s]), HELPER_WARPS);
         }
         mbar_init(smem_addr(&sm.acc_full), 1);
         mbar_init(smem_addr(&sm.acc_empty), EPI_THREADS);
@@ -1366,7 +1366,8 @@ tc_gemm_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs g) {
                     tmem_st16(sf_lane + stage * kSfStride, sfw);
                     tmem_wait_st();
                     tc_fence_before();
-                    mbar_arrive(smem_addr(&sm.sf_ready[stage]));
+                    __syncwarp();           // every lane's stores are complete: one arrival per warp
+                    if (lane == 0) mbar_arrive(smem_addr(&sm.sf_ready[stage]));
                     if (++stage == STAGES) { stage = 0; phase ^= 1u; }
                 }
             }

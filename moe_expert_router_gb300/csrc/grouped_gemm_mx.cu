@@ -16,35 +16,52 @@ __device__ __forceinline__ int64_t kmajor_scale_byte(int64_t r, int64_t c, int64
     return (((c >> 2) * sf_rows + r) << 2) + (c & 3);
 }
 
-// One thread per 32-element block; block b of a row-major [rows, cols] matrix
-// (cols % 128 == 0) is elements [32 b, 32 b + 32) of the codes; the scales are
+// Quantizes the 32 bf16 values at src into E4M3 codes at dst (32 bytes) and
+// returns their E8M0 scale code.
+__device__ __forceinline__ uint32_t quantize_block32(const __nv_bfloat16 *src, uint8_t *dst) {
+    const uint4 *s4 = reinterpret_cast<const uint4 *>(src);
+    float v[32];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        const uint4 w = __ldg(s4 + q);
+        const uint32_t u[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            v[8 * q + 2 * j] = bf16_lo(u[j]);
+            v[8 * q + 2 * j + 1] = bf16_hi(u[j]);
+        }
+    }
+    uint32_t qw[8];
+    const uint32_t sc = mx_quantize32(v, qw);
+    uint4 *d4 = reinterpret_cast<uint4 *>(dst);
+    d4[0] = make_uint4(qw[0], qw[1], qw[2], qw[3]);
+    d4[1] = make_uint4(qw[4], qw[5], qw[6], qw[7]);
+    return sc;
+}
+
+// Both quantizers give a warp 8 rows x one 128-column k-block per step: lane
+// (i, j) = (lane / 4, lane % 4) quantizes block 4 kb + j of row 8 g + i, so the
+// warp reads and writes 8 runs of 256 / 128 contiguous bytes and its 32 scale
+// bytes are the 8 consecutive words [kb][8 g .. 8 g + 7], one 32-byte sector.
+
+// A row-major [rows, cols] matrix (cols % 128 == 0): codes [rows, cols], scales
 // k-block-major over sf_rows (rows rounded up to 4) rows.
 __global__ void __launch_bounds__(256)
-mx_quantize_kernel(const __nv_bfloat16 *__restrict__ in, int64_t rows, int64_t per_row, int64_t sf_rows,
+mx_quantize_kernel(const __nv_bfloat16 *__restrict__ in, int64_t rows, int64_t cols, int64_t sf_rows,
                    uint8_t *__restrict__ codes, uint8_t *__restrict__ scales) {
     griddep_wait();
-    const int64_t blocks = rows * per_row;
-    for (int64_t b = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; b < blocks;
-         b += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-        const uint4 *src = reinterpret_cast<const uint4 *>(in + b * 32);
-        float v[32];
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            const uint4 w = __ldg(src + q);
-            const uint32_t u[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                v[8 * q + 2 * j] = bf16_lo(u[j]);
-                v[8 * q + 2 * j + 1] = bf16_hi(u[j]);
-            }
+    const int lane = threadIdx.x & 31;
+    const int64_t kbs = cols / 128;
+    const int64_t steps = (rows + 7) / 8 * kbs;
+    const int64_t warps = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
+    for (int64_t w = blockIdx.x * static_cast<int64_t>(blockDim.x >> 5) + (threadIdx.x >> 5); w < steps; w += warps) {
+        const int64_t grp = w / kbs, kb = w - grp * kbs;
+        const int64_t r = grp * 8 + (lane >> 2);
+        const int64_t c = kb * 4 + (lane & 3);
+        if (r < rows) {
+            const uint32_t sc = quantize_block32(in + r * cols + c * 32, codes + r * cols + c * 32);
+            scales[kmajor_scale_byte(r, c, sf_rows)] = static_cast<uint8_t>(sc);
         }
-        uint32_t qw[8];
-        const uint32_t sc = mx_quantize32(v, qw);
-        uint4 *dst = reinterpret_cast<uint4 *>(codes + b * 32);
-        dst[0] = make_uint4(qw[0], qw[1], qw[2], qw[3]);
-        dst[1] = make_uint4(qw[4], qw[5], qw[6], qw[7]);
-        const int64_t r = b / per_row;
-        scales[kmajor_scale_byte(r, b - r * per_row, sf_rows)] = static_cast<uint8_t>(sc);
     }
 }
 
@@ -57,31 +74,20 @@ mx_quantize_dispatch_kernel(const __nv_bfloat16 *__restrict__ x, const int32_t *
                             const int32_t *__restrict__ routed, int k, int64_t sf_rows, int64_t cols,
                             uint8_t *__restrict__ codes, uint8_t *__restrict__ scales) {
     griddep_wait();
-    const int64_t per_row = cols / 32;
-    const int64_t blocks = static_cast<int64_t>(*routed) * per_row;
-    for (int64_t b = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; b < blocks;
-         b += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-        const int64_t r = b / per_row;
-        const int64_t c = b - r * per_row;
-        const int64_t t = perm_slot[r] / k;
-        const uint4 *src = reinterpret_cast<const uint4 *>(x + t * cols + c * 32);
-        float v[32];
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            const uint4 w = __ldg(src + q);
-            const uint32_t u[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                v[8 * q + 2 * j] = bf16_lo(u[j]);
-                v[8 * q + 2 * j + 1] = bf16_hi(u[j]);
-            }
+    const int lane = threadIdx.x & 31;
+    const int64_t rows = *routed;
+    const int64_t kbs = cols / 128;
+    const int64_t steps = (rows + 7) / 8 * kbs;
+    const int64_t warps = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
+    for (int64_t w = blockIdx.x * static_cast<int64_t>(blockDim.x >> 5) + (threadIdx.x >> 5); w < steps; w += warps) {
+        const int64_t grp = w / kbs, kb = w - grp * kbs;
+        const int64_t r = grp * 8 + (lane >> 2);
+        const int64_t c = kb * 4 + (lane & 3);
+        if (r < rows) {
+            const int64_t t = perm_slot[r] / k;
+            const uint32_t sc = quantize_block32(x + t * cols + c * 32, codes + r * cols + c * 32);
+            scales[kmajor_scale_byte(r, c, sf_rows)] = static_cast<uint8_t>(sc);
         }
-        uint32_t qw[8];
-        const uint32_t sc = mx_quantize32(v, qw);
-        uint4 *dst = reinterpret_cast<uint4 *>(codes + b * 32);
-        dst[0] = make_uint4(qw[0], qw[1], qw[2], qw[3]);
-        dst[1] = make_uint4(qw[4], qw[5], qw[6], qw[7]);
-        scales[kmajor_scale_byte(r, c, sf_rows)] = static_cast<uint8_t>(sc);
     }
 }
 
@@ -233,7 +239,7 @@ cudaError_t launch_mx_quantize(const __nv_bfloat16 *in, int64_t rows, int64_t co
     int64_t grid = (blocks + 255) / 256;
     if (grid > 152 * 16) grid = 152 * 16;
     const cudaError_t e = launch_dep(mx_quantize_kernel, dim3(static_cast<int>(grid)), dim3(256), 0, st, in, rows,
-                                     cols / 32, static_cast<int64_t>(mx_rows(rows)), codes, scales);
+                                     cols, static_cast<int64_t>(mx_rows(rows)), codes, scales);
     note_launches(1);
     return e;
 }
