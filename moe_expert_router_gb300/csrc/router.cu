@@ -28,6 +28,7 @@ namespace moe {
 namespace {
 
 constexpr int kTopkWarps = 8;
+constexpr int kTopkFastSplits = 4;          // split counts the top-k loads all at once
 constexpr int kMaxE = 1024;
 
 __global__ void __launch_bounds__(256)
@@ -182,24 +183,56 @@ router_topk_kernel(const TopkArgs p) {
         bool elig[V];
         const int64_t split_stride = static_cast<int64_t>(p.T) * p.E;
         const float *lrow = p.logits_part + static_cast<int64_t>(t) * p.E;
+        // each logit is the sum of its split partials in split order
+        bool loaded = false;
+        if constexpr (V <= 8) {
+            if (p.splits <= kTopkFastSplits) {
+            // every partial of the lane's experts in flight at once
+            float part[V][kTopkFastSplits];
+#pragma unroll
+            for (int i = 0; i < V; ++i) {
+                const int e = lane + 32 * i;
+#pragma unroll
+                for (int j = 0; j < kTopkFastSplits; ++j)
+                    part[i][j] = (e < p.E && j < p.splits) ? __ldcg(&lrow[j * split_stride + e]) : 0.0f;
+            }
+#pragma unroll
+            for (int i = 0; i < V; ++i) {
+                float l = 0.0f;
+#pragma unroll
+                for (int j = 0; j < kTopkFastSplits; ++j)
+                    if (j < p.splits) l += part[i][j];
+                s[i] = l;
+            }
+            loaded = true;
+            }
+        }
+        if (!loaded) {
+#pragma unroll
+            for (int i = 0; i < V; ++i) {
+                const int e = lane + 32 * i;
+                float l = 0.0f;
+                if (e < p.E) {
+                    // eight loads in flight at a time
+                    for (int sp0 = 0; sp0 < p.splits; sp0 += 8) {
+                        float part[8];
+#pragma unroll
+                        for (int j = 0; j < 8; ++j)
+                            part[j] = (sp0 + j < p.splits) ? __ldcg(&lrow[(sp0 + j) * split_stride + e]) : 0.0f;
+#pragma unroll
+                        for (int j = 0; j < 8; ++j)
+                            if (sp0 + j < p.splits) l += part[j];
+                    }
+                }
+                s[i] = l;
+            }
+        }
 #pragma unroll
         for (int i = 0; i < V; ++i) {
             const int e = lane + 32 * i;
             if (e < p.E) {
-                // the split partials in a fixed order, eight loads in flight at a time
-                float l = 0.0f;
-                for (int sp0 = 0; sp0 < p.splits; sp0 += 8) {
-                    float part[8];
-#pragma unroll
-                    for (int j = 0; j < 8; ++j)
-                        part[j] = (sp0 + j < p.splits) ? __ldcg(&lrow[(sp0 + j) * split_stride + e]) : 0.0f;
-#pragma unroll
-                    for (int j = 0; j < 8; ++j)
-                        if (sp0 + j < p.splits) l += part[j];
-                }
-                if (p.logit_offset) l += p.logit_offset[e];
-                if (p.logits_out) p.logits_out[static_cast<int64_t>(t) * p.E + e] = l;
-                s[i] = l;
+                if (p.logit_offset) s[i] += p.logit_offset[e];
+                if (p.logits_out) p.logits_out[static_cast<int64_t>(t) * p.E + e] = s[i];
             } else {
                 s[i] = -INFINITY;
             }
@@ -235,7 +268,40 @@ router_topk_kernel(const TopkArgs p) {
             if (elig[i]) atomicAdd(&blk_sum[e], s[i]);
         }
 
-        if (p.n_group > 1) {
+        if (p.n_group > 1 && p.E == 32 * p.n_group && p.group_topn <= 2) {
+            // groups of 32 experts: group g is register g across the warp's lanes, so
+            // each group's sum of its best group_topn (1 or 2) sel values is a warp
+            // reduction of the top two; lane g keeps group g's sum
+            float gscore = -INFINITY;
+#pragma unroll
+            for (int i = 0; i < V; ++i) {
+                if (i < p.n_group) {
+                    float a1 = sel[i], a2 = -INFINITY;        // the best two seen (a1 >= a2)
+#pragma unroll
+                    for (int off = 16; off > 0; off >>= 1) {
+                        const float b1 = __shfl_xor_sync(0xffffffffu, a1, off);
+                        const float b2 = __shfl_xor_sync(0xffffffffu, a2, off);
+                        const float hi = fmaxf(a1, b1);
+                        a2 = fmaxf(fminf(a1, b1), fmaxf(a2, b2));
+                        a1 = hi;
+                    }
+                    const float sum = p.group_topn == 1 ? a1 : a1 + a2;
+                    if (lane == i) gscore = sum;
+                }
+            }
+            unsigned kept = 0;
+            float gv = gscore;
+            for (int n = 0; n < p.topk_group; ++n) {
+                float v = gv;
+                int i = (lane < p.n_group) ? lane : 0x7fffffff;
+                warp_argmax(v, i);
+                kept |= 1u << i;
+                if (lane == i) gv = -INFINITY;
+            }
+#pragma unroll
+            for (int i = 0; i < V; ++i)
+                if (!((kept >> i) & 1u)) elig[i] = false;
+        } else if (p.n_group > 1) {
             const int gs = p.E / p.n_group;
             float *row = sel_sh[warp];
 #pragma unroll

@@ -283,6 +283,11 @@ ROUTER_CASES = {
     "sigmoid_groups_e256": _cfg(512, 256, 64, 256, 8, score="sigmoid", scale=2.5, n_group=8,
                                 topk_group=4, group_topn=2, sel_bias=True),
     "zipf_offset_e128": _cfg(2048, 256, 64, 128, 8, zipf_s=1.2),
+    # groups of exactly 32 experts (the warp-wide group sums): the best one per group,
+    # and 16 groups of E = 512
+    "softmax_groups_e128_top1": _cfg(700, 256, 64, 128, 6, n_group=4, topk_group=2, group_topn=1),
+    "sigmoid_groups_e512": _cfg(300, 256, 64, 512, 8, score="sigmoid", scale=2.5, n_group=16,
+                                topk_group=4, group_topn=2, sel_bias=True),
     "e1024_k32": _cfg(64, 128, 64, 1024, 32),
     "e3_k3": _cfg(50, 64, 64, 3, 3),
     # E between 32 and 64 (each weight part padded to 64 accumulator columns), a K tail
