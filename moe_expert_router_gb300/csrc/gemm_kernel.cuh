@@ -927,19 +927,27 @@ tc_gemm_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs g) {
             const bool full_slab = slab0 + 32 <= t.rows;
             if (t.rows > half * BM) {                   // this half was computed
                 if constexpr (MODE == kStage1Mx) {
-                    // SwiGLU of 32 gate / up columns, then the MXFP8 quantization of
-                    // that 32-column block of a: 32 E4M3 codes and one E8M0 scale
+                    // per 32 output columns: SwiGLU of the gate / up columns, then the
+                    // MXFP8 quantization of that block of a (32 E4M3 codes, one E8M0
+                    // scale). The accumulator is released as soon as the last piece has
+                    // been read from tensor memory, before that piece's arithmetic.
                     const int col0 = t.n * (kUnitN<MODE> / 2);
+                    const int np = min(kUnitN<MODE> / 64, (g.n_out - col0 + 31) / 32);   // pieces inside n_out
                     const int64_t r = t.row0 + row;
 #pragma unroll 1
-                    for (int c = 0; c < kUnitN<MODE> / 2; c += 32) {
-                        if (col0 + c >= g.n_out) break;
+                    for (int p = 0; p < np; ++p) {
+                        const int c = 32 * p;
                         uint32_t gv[32], uv[32];
                         tmem_ld32(tacc + c, gv);
                         tmem_ld32(tacc + kUnitN<MODE> / 2 + c, uv);
                         tmem_wait_ld();
                         tmem_reg_fence(gv);
                         tmem_reg_fence(uv);
+                        if (p == np - 1) {
+                            tc_fence_before();
+                            mbar_arrive(smem_addr(&sm.acc_empty));
+                            released = true;
+                        }
                         if (g.out2 != nullptr && valid) {
                             // training: the pre-activation h (gate and up halves, bf16) for the backward
                             uint32_t pg[16], pu[16];
@@ -968,28 +976,54 @@ tc_gemm_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs g) {
                     }
                 } else if constexpr (MODE == kStage2Mx) {
                     // weighted rows into obuf, 32 x 32 boxes (the unit is 224 columns wide)
+                    constexpr int NP = kUnitN<MODE> / 32;
                     const int col0 = t.n * kUnitN<MODE>;
                     const int y = t.row0 + slab0;
-                    __nv_bfloat16 *dst = g.out + static_cast<int64_t>(t.row0 + row) * g.n_out;
-#pragma unroll 1
-                    for (int c = 0; c < kUnitN<MODE>; c += 32) {
-                        const int col = col0 + c;
-                        if (col >= g.n_out) break;
-                        uint32_t pk[16];
-                        scaled_piece(tacc, c, w, pk);
-                        if (full_slab) {
-                            if (lane == 0) bulk_wait_read<1>();   // the box two boxes ago is read out
-                            __syncwarp();
-                            const uint32_t b2 = buf + (boxes++ & 1u) * 2048;
-                            stage_row32(b2, lane, pk);
-                            fence_proxy_async_smem();
-                            __syncwarp();
+                    if (full_slab) {
+                        // the first two boxes are staged at once (both staging halves), the
+                        // rest of the row read into packed bf16 registers; then the
+                        // accumulator is released and the stores overlap the next unit's MMAs
+                        uint32_t pks[NP][16];
+                        scaled_piece2(tacc, 0, w, pks[0], pks[1]);
+                        if (lane == 0) bulk_wait_read<0>();       // the previous unit's boxes are read out
+                        __syncwarp();
+                        stage_row32(buf, lane, pks[0]);
+                        stage_row32(buf + 2048, lane, pks[1]);
+#pragma unroll
+                        for (int p = 2; p + 1 < NP; p += 2) scaled_piece2(tacc, 32 * p, w, pks[p], pks[p + 1]);
+                        if constexpr (NP % 2 == 1) scaled_piece(tacc, 32 * (NP - 1), w, pks[NP - 1]);
+                        tc_fence_before();
+                        mbar_arrive(smem_addr(&sm.acc_empty));
+                        released = true;
+                        fence_proxy_async_smem();
+                        __syncwarp();
+#pragma unroll
+                        for (int p = 0; p < NP; ++p) {
+                            const int col = col0 + 32 * p;
+                            if (col >= g.n_out) break;
+                            const uint32_t b2 = buf + (p & 1) * 2048;
+                            if (p >= 2) {
+                                if (lane == 0) bulk_wait_read<1>();   // the box two boxes ago is read out
+                                __syncwarp();
+                                stage_row32(b2, lane, pks[p]);
+                                fence_proxy_async_smem();
+                                __syncwarp();
+                            }
                             if (lane == 0) {
                                 tma_store_2d(&maps.out, b2, col, y);
                                 bulk_commit();
                             }
-                        } else if (valid) {
-                            store_row32(dst + col, g.n_out - col, pk);
+                        }
+                    } else {
+                        // partial slab: masked direct stores, piece by piece
+                        __nv_bfloat16 *dst = g.out + static_cast<int64_t>(t.row0 + row) * g.n_out;
+#pragma unroll 1
+                        for (int c = 0; c < kUnitN<MODE>; c += 32) {
+                            const int col = col0 + c;
+                            if (col >= g.n_out) break;
+                            uint32_t pk[16];
+                            scaled_piece(tacc, c, w, pk);
+                            if (valid) store_row32(dst + col, g.n_out - col, pk);
                         }
                     }
                 } else if constexpr (kIsStage1<MODE> || MODE == kStage2 || MODE == kBwdDX) {
