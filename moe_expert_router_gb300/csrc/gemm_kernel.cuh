@@ -1247,6 +1247,73 @@ tc_gemm_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs g) {
                         }
                     }
                     if (valid) g.dtw_part[static_cast<int64_t>(t.n) * g.R + r] = dtw;
+                } else if constexpr (MODE == kWgradMx) {
+                    // as stage 2 in MXFP8: dW rows t.row0 + row of expert e through a 3-D
+                    // map (rows past m_total and columns past n_out clipped by the store);
+                    // the first two 32 x 32 boxes staged at once, the rest of the row in
+                    // packed registers, then the accumulator released (a unit reduces over
+                    // only its expert's rows, so its MMAs are short and its stores are
+                    // better spent under the next unit's)
+                    constexpr int NP = kUnitN<MODE> / 32;
+                    const int col0 = t.n * kUnitN<MODE>;
+                    const bool empty = t.kb1 == t.kb0;  // expert without rows: zeros
+                    if (slab0 < t.rows && empty) {
+                        // expert without rows: zero boxes, the accumulator untouched
+                        uint32_t pk[16];
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) pk[i] = 0u;
+#pragma unroll 1
+                        for (int p = 0; p < NP; ++p) {
+                            const int col = col0 + 32 * p;
+                            if (col >= g.n_out) break;
+                            // the first box: the previous unit's last box may be in either half
+                            if (lane == 0) {
+                                if (p == 0) bulk_wait_read<0>();
+                                else bulk_wait_read<1>();
+                            }
+                            __syncwarp();
+                            const uint32_t b2 = buf + (p & 1) * 2048;
+                            stage_row32(b2, lane, pk);
+                            fence_proxy_async_smem();
+                            __syncwarp();
+                            if (lane == 0) {
+                                tma_store_3d(&maps.out, b2, col, t.row0 + slab0, t.e);
+                                bulk_commit();
+                            }
+                        }
+                    } else if (slab0 < t.rows) {
+                        uint32_t pks[NP][16];
+                        scaled_piece2(tacc, 0, 1.0f, pks[0], pks[1]);
+                        if (lane == 0) bulk_wait_read<0>();       // the previous unit's boxes are read out
+                        __syncwarp();
+                        stage_row32(buf, lane, pks[0]);
+                        stage_row32(buf + 2048, lane, pks[1]);
+#pragma unroll
+                        for (int p = 2; p + 1 < NP; p += 2) scaled_piece2(tacc, 32 * p, 1.0f, pks[p], pks[p + 1]);
+                        if constexpr (NP % 2 == 1) scaled_piece(tacc, 32 * (NP - 1), 1.0f, pks[NP - 1]);
+                        tc_fence_before();
+                        mbar_arrive(smem_addr(&sm.acc_empty));
+                        released = true;
+                        fence_proxy_async_smem();
+                        __syncwarp();
+#pragma unroll
+                        for (int p = 0; p < NP; ++p) {
+                            const int col = col0 + 32 * p;
+                            if (col >= g.n_out) break;
+                            const uint32_t b2 = buf + (p & 1) * 2048;
+                            if (p >= 2) {
+                                if (lane == 0) bulk_wait_read<1>();   // the box two boxes ago is read out
+                                __syncwarp();
+                                stage_row32(b2, lane, pks[p]);
+                                fence_proxy_async_smem();
+                                __syncwarp();
+                            }
+                            if (lane == 0) {
+                                tma_store_3d(&maps.out, b2, col, t.row0 + slab0, t.e);
+                                bulk_commit();
+                            }
+                        }
+                    }
                 } else if constexpr (kPerExpertOut<MODE>) {
                     // dW rows t.row0 + row of expert e, 32 x 32 boxes through a 3-D map
                     // (rows past m_total and columns past n_out are clipped by the store),
