@@ -31,6 +31,14 @@
 //   kBwdDW1  dW1[e] = sum over e's rows of dH[r]^T x[token(r)]: M = 2I, N = H,
 //            K = the expert's rows; dispatched x rows read MN-major.
 //
+// MXFP8 modes (the guide's section "Expert precision"): kStage1Mx and kStage2Mx
+// run the two expert stages, kWgradMx the dW1 / dW2 weight gradients (operands
+// transposed and quantized along the routed rows beforehand), as
+// kind::mxf8f6f4.block_scale MMAs on E4M3 operands with E8M0 scales per 32
+// K-elements. The scales are k-block-major 32-bit words; each stage's words
+// arrive by TMA on a barrier of their own and the helper warps copy them into
+// tensor memory.
+//
 // Kernel design (one CTA per SM, persistent):
 //   work unit  = (expert e, n-tile, 256-row tile of e's routed rows) for the
 //                row-grouped modes, (256-row tile, n-tile, k split) for the

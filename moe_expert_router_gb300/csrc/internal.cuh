@@ -305,12 +305,14 @@ cudaError_t launch_router_dwr(const RouterBwdLaunch &p, cudaStream_t st);
 cudaError_t launch_combine_bwd(const CombineBwdLaunch &p, cudaStream_t st);
 
 // MXFP8 (grouped_gemm_mx.cu): quantization of a bf16 [rows, cols] matrix along its
-// rows (cols % 32 == 0) into E4M3 codes and E8M0 block scales; the two MXFP8
+// rows (cols % 128 == 0) into E4M3 codes [rows, cols] and E8M0 block scales as
+// k-block-major 32-bit words [cols / 128][rows rounded up to 4]; the two MXFP8
 // expert stages (stage 1: out = a codes, out_sf = a scales; stage 2 as kStage2).
 cudaError_t launch_mx_quantize(const __nv_bfloat16 *in, int64_t rows, int64_t cols, uint8_t *codes,
                                uint8_t *scales, cudaStream_t st);
 // The MXFP8 dispatch: quantize the x rows of routed rows [0, *routed) (token
-// perm_slot[r] / k) into codes [R, cols] / scales [R, cols / 32], routed order.
+// perm_slot[r] / k) into codes [R, cols] and k-block-major scale words
+// [cols / 128][R rounded up to 4], routed order.
 cudaError_t launch_mx_quantize_dispatch(const __nv_bfloat16 *x, const int32_t *perm_slot, const int32_t *routed,
                                         int k, int64_t R, int64_t cols, uint8_t *codes, uint8_t *scales,
                                         cudaStream_t st);
