@@ -189,8 +189,9 @@ def test_mxfp8_layout_and_argument_checks(lib):
     big = 1 << 40
     shp = B.shape(16, 256, 256, 4, 2, mxfp8=True)
     odd = B.shape(16, 192, 256, 4, 2, mxfp8=True)           # H % 128 != 0
-    assert lib.moe_mx_quantize(p, 4, 48, p, p, None) == 1     # cols % 32
-    assert lib.moe_mx_quantize(None, 4, 64, p, p, None) == 1
+    assert lib.moe_mx_quantize(p, 4, 48, p, p, None) == 1     # cols % 128
+    assert lib.moe_mx_quantize(p, 4, 64, p, p, None) == 1
+    assert lib.moe_mx_quantize(None, 4, 128, p, p, None) == 1
     assert lib.moe_dispatch_gemm1_mx(p, p, ctypes.byref(odd), p, p, p, big, None) == 2
     assert lib.moe_dispatch_gemm1_mx(p, p, ctypes.byref(shp), p, None, p, big, None) == 1
     assert lib.moe_mx_quantize_dispatch(p, ctypes.byref(odd), p, big, None) == 2
@@ -217,3 +218,26 @@ def test_packed_weight_sizes_and_flag_checks(lib):
     assert lib.moe_pack_weights(None, p, ctypes.byref(shp), None, None, None) == 1
     misaligned = ctypes.c_void_p((1 << 20) + 8)
     assert lib.moe_pack_weights(p, None, ctypes.byref(shp), misaligned, None, None) == 1
+
+
+def test_mx_scale_layout_helpers():
+    """The k-block-major scale buffers (rows rounded up to 4) and the test-side
+    re-layout to the oracle's row-major scales, on host tensors (no device call)."""
+    import numpy as np
+    import torch
+    from gpu_helpers import kmajor_scales_to_rows
+    assert tuple(B.mx_scales_empty((5, 3, 256), "cpu").shape) == (2, 16, 4)   # 15 rows -> 16
+    assert tuple(B.mx_scales_empty((2, 8, 384), "cpu").shape) == (3, 2, 8, 4)
+    # byte j of word [kb][r] is the scale of columns 128 kb + 32 j .. of row r
+    rows, cols = 6, 512
+    rs = np.arange(rows * cols // 32, dtype=np.uint8).reshape(rows, cols // 32)
+    km = np.zeros((cols // 128, 8, 4), np.uint8)
+    for r in range(rows):
+        for c in range(cols // 32):
+            km[c // 4, r, c % 4] = rs[r, c]
+    np.testing.assert_array_equal(kmajor_scales_to_rows(km, rows=rows), rs)
+    # a scale buffer of the wrong size is refused before any library call
+    t = torch.zeros((6, 512), dtype=torch.bfloat16)
+    codes = torch.empty((6, 512), dtype=torch.uint8)
+    with pytest.raises(ValueError):
+        B.moe_mx_quantize(t, codes, torch.empty((6 * 16,), dtype=torch.uint8))
