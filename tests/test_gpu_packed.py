@@ -6,7 +6,6 @@ weights bit-identical to the forward with the row-major weights (the same
 operand values reach the same MMAs in the same order), and within the parity
 bars of the oracle.
 """
-import numpy as np
 import pytest
 import torch
 

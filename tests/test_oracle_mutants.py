@@ -4,7 +4,6 @@ Each mutant is the oracle's C source with one textual change (a dropped term,
 a wrong sign or index, a transposed operand, a flipped tie-break ...), compiled
 on the CPU into a temporary library. The real oracle is never modified.
 """
-import os
 
 import pytest
 
