@@ -1,0 +1,45 @@
+"""The torch.library operators through torch.compile (whole graph, no break) against
+the direct ctypes calls: bit-identical routing and y, the aux score to rounding."""
+import pytest
+import torch
+
+from gpu_helpers import router_cfg_of
+from moe_expert_router_gb300 import binding as B
+from moe_expert_router_gb300 import torch_ops  # noqa: F401  (registers the operators)
+from moe_expert_router_gb300.workloads import MoEConfig, generate
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _device():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    B.load()
+
+
+def test_compiled_router_and_forward_equal_the_direct_calls():
+    cfg = MoEConfig("case", T=300, H=256, I=384, E=16, k=4, score="sigmoid", scale=2.5, n_group=4, topk_group=2,
+                    group_topn=2, sel_bias=True)
+    inp = generate(cfg, seed=3, device="cuda")
+
+    def layer(x, w_r, bias, w1, w2):
+        idx, w, aux = torch.ops.moe_gb300.router(x, w_r, cfg.k, cfg.score, cfg.normalize, cfg.scale, cfg.n_group,
+                                                 cfg.topk_group, cfg.group_topn, bias, None)
+        return torch.ops.moe_gb300.forward(x, idx, w, w1, w2), idx, aux
+
+    compiled = torch.compile(layer, fullgraph=True, backend="eager")
+    y_c, idx_c, aux_c = compiled(inp["x"], inp["w_r"], inp["sel_bias"], inp["w1"], inp["w2"])
+
+    shp = B.shape(cfg.T, cfg.H, cfg.I, cfg.E, cfg.k)
+    ws = B.new_workspace(shp, "cuda")
+    idx = torch.empty((cfg.T, cfg.k), dtype=torch.int32, device="cuda")
+    w = torch.empty((cfg.T, cfg.k), dtype=torch.float32, device="cuda")
+    aux = torch.zeros((1,), dtype=torch.float32, device="cuda")
+    B.moe_router(inp["x"], inp["w_r"], shp, router_cfg_of(cfg), idx, w, ws, aux=aux, sel_bias=inp["sel_bias"])
+    y = torch.empty((cfg.T, cfg.H), dtype=torch.bfloat16, device="cuda")
+    B.moe_forward(inp["x"], idx, w, inp["w1"], inp["w2"], shp, y, ws)
+    assert torch.equal(idx_c, idx)
+    # the aux score's per-expert sums are accumulated with atomics: equal to rounding
+    assert torch.allclose(aux_c, aux, rtol=1e-5, atol=0.0)
+    assert torch.equal(y_c, y)

@@ -1,0 +1,31 @@
+"""The torch.library operators (moe_expert_router_gb300/torch_ops.py): schemas and
+shape functions on the host (fake tensors, no device call)."""
+import torch
+from torch._subclasses.fake_tensor import FakeTensorMode
+
+from moe_expert_router_gb300 import torch_ops  # noqa: F401  (registers the operators)
+
+
+def test_operators_are_registered():
+    for name in ("router", "forward", "forward_mx"):
+        assert hasattr(torch.ops.moe_gb300, name)
+
+
+def test_fake_shapes():
+    T, H, I, E, k = 24, 256, 128, 8, 3
+    with FakeTensorMode():
+        x = torch.empty((T, H), dtype=torch.bfloat16, device="cuda")
+        w_r = torch.empty((E, H), dtype=torch.float32, device="cuda")
+        idx, w, aux = torch.ops.moe_gb300.router(x, w_r, k, "sigmoid", True, 2.5, 4, 2, 2)
+        assert idx.shape == (T, k) and idx.dtype == torch.int32
+        assert w.shape == (T, k) and w.dtype == torch.float32 and aux.shape == (1,)
+        w1 = torch.empty((E, 2 * I, H), dtype=torch.bfloat16, device="cuda")
+        w2 = torch.empty((E, H, I), dtype=torch.bfloat16, device="cuda")
+        y = torch.ops.moe_gb300.forward(x, idx, w, w1, w2)
+        assert y.shape == (T, H) and y.dtype == torch.bfloat16
+        c1 = torch.empty((E, 2 * I, H), dtype=torch.uint8, device="cuda")
+        s1 = torch.empty((H // 128, E, 2 * I, 4), dtype=torch.uint8, device="cuda")
+        c2 = torch.empty((E, H, I), dtype=torch.uint8, device="cuda")
+        s2 = torch.empty((I // 128, E, H, 4), dtype=torch.uint8, device="cuda")
+        y = torch.ops.moe_gb300.forward_mx(x, idx, w, c1, s1, c2, s2)
+        assert y.shape == (T, H) and y.dtype == torch.bfloat16
