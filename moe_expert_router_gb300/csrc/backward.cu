@@ -60,7 +60,10 @@ router_dlogits_kernel(const RouterBwdLaunch p) {
     const bool ok = mine && e >= 0 && e < p.E;
     const float w = ok ? p.topk_w[static_cast<int64_t>(t) * p.k + lane] : 0.0f;
     const float dw = ok ? p.dtopk_w[static_cast<int64_t>(t) * p.k + lane] : 0.0f;
-    const float sum_wdw = warp_sum(w * dw);
+    // products rounded on their own (no fused multiply-add), so that where the
+    // normalisation makes a weight constant (k = 1: w = scale) its terms cancel
+    // exactly and the logit gradient is exactly 0
+    const float sum_wdw = warp_sum(__fmul_rn(w, dw));
     if (p.score_fn == MOE_SCORE_SOFTMAX && !p.normalize) {
         float m = -INFINITY;
         for (int i = lane; i < p.E; i += 32) m = fmaxf(m, lrow[i]);
@@ -79,13 +82,13 @@ router_dlogits_kernel(const RouterBwdLaunch p) {
     for (int i = lane; i < p.E; i += 32) dl[i] = 0.0f;
     __syncwarp();
     if (p.score_fn == MOE_SCORE_SOFTMAX) {
-        if (ok) atomicAdd(&dl[e], w * dw - (w / p.scale) * sum_wdw);
+        if (ok) atomicAdd(&dl[e], __fmul_rn(w, dw) - __fmul_rn(w / p.scale, sum_wdw));
         return;
     }
     const float s = ok ? 1.0f / (1.0f + expf(-lrow[e])) : 0.0f;
     if (p.normalize) {
         const float S = warp_sum(s);
-        if (ok) atomicAdd(&dl[e], s * (1.0f - s) / S * (p.scale * dw - sum_wdw));
+        if (ok) atomicAdd(&dl[e], s * (1.0f - s) / S * (__fmul_rn(p.scale, dw) - sum_wdw));
     } else {
         if (ok) atomicAdd(&dl[e], p.scale * s * (1.0f - s) * dw);
     }

@@ -118,6 +118,10 @@ CASES = {
     "sigmoid_plain": _cfg(200, 256, 128, 8, 3, score="sigmoid", normalize=False, scale=2.0),
     "zipf_offsets": _cfg(512, 256, 192, 32, 4, zipf_s=1.2),
     "h8_i8": _cfg(5, 8, 8, 3, 2),
+    # top-1 with normalised weights: every weight is the constant scale, so the
+    # router's gradients are exactly zero (the oracle's are)
+    "top1_normalized_softmax": _cfg(150, 128, 128, 8, 1),
+    "top1_normalized_sigmoid": _cfg(150, 128, 128, 8, 1, score="sigmoid", scale=2.5),
     "one_token": _cfg(1, 64, 64, 4, 2),
 }
 
