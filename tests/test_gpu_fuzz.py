@@ -3,7 +3,8 @@ group limits, selection bias, both score functions, the few-token router below 2
 tokens), the routing metadata and both stages, on randomly drawn small shapes —
 K and N tails (H and I any multiple of 8), ragged expert counts, one to eight
 experts per token — in bf16, and MXFP8 shapes (H and I multiples of 128); and the
-backward (dX, dW1, dW2, the routing-weight and router gradients) on bf16 draws. Each
+backward (dX, dW1, dW2, the routing-weight and router gradients) on bf16 draws, and
+the MXFP8 training step on MXFP8 draws. Each
 draw is fixed by its seed. Bars as everywhere: routing sets bit-exact away from
 near-ties, y and the gradients within the output bound."""
 import numpy as np
@@ -96,3 +97,11 @@ def test_fuzz_backward_bf16(seed):
     out = train_step(inp, cfg, staged=bool(seed % 2))
     ref = oracle_grads(inp, cfg, out["idx"], out["w"])
     check_all(out, ref)
+
+
+@pytest.mark.parametrize("seed", range(8))
+def test_fuzz_training_mxfp8(seed):
+    from dataclasses import replace
+    from test_gpu_mx import check_mx_training
+    cfg = draw_cfg(200 + seed, mx=True)
+    check_mx_training(replace(cfg, T=min(cfg.T, 400), backward=True), seed=seed)

@@ -312,8 +312,15 @@ def test_mx_training_step_matches_oracle(name):
     idx = w = None
     if counts is not None:
         idx, w = routing_with_counts(counts, cfg.T, cfg.k, seed=9, device=DEV)
-    inp, idx, w, w1q, w1s, w2q, w2s = mx_inputs(cfg, seed=4, idx=idx, w=w)
-    inp = _with_dy(inp, cfg, 4)
+    check_mx_training(cfg, idx, w, seed=4)
+
+
+def check_mx_training(cfg, idx=None, w=None, seed=4):
+    """The MXFP8 training step against the oracle: the forward, the bf16 data
+    gradients and the operands they leave, the weight-gradient kernels on the
+    GPU's own operands, and the whole chain."""
+    inp, idx, w, w1q, w1s, w2q, w2s = mx_inputs(cfg, seed=seed, idx=idx, w=w)
+    inp = _with_dy(inp, cfg, seed)
     out = mx_train_step(cfg, inp, idx, w, w1q, w1s, w2q, w2s)
     assert out["err"] == 0, f"device error word {out['err']:#x}"
     xq, xs = oracle.mx_quantize(inp["x"])
