@@ -148,6 +148,9 @@ moe_status_t moe_workspace_init(void *ws, size_t ws_bytes, void *stream);
  *
  * x bf16 [T,H]; w_r fp32 [E,H]; logit_offset, sel_bias fp32 [E] or NULL;
  * topk_idx int32 [T,k], topk_w fp32 [T,k], aux fp32 [1] or NULL (outputs).
+ * topk_idx and topk_w are the same bits on every call with the same inputs;
+ * the per-expert score sums of aux are float atomics whose order varies, so
+ * aux can differ from call to call in its last bits.
  */
 moe_status_t moe_router(const void *x, const float *w_r, const float *logit_offset,
                         const float *sel_bias, const moe_shape_t *shape,

@@ -181,3 +181,34 @@ def oracle_y_for_tokens(inp, idx, w, tokens, want_a=False):
         y, a, _ = oracle.expert_forward(x, idx_r.to(torch.int32), ws_, w1, w2, want_a=True)
         return y, a
     return oracle.expert_forward(x, idx_r.to(torch.int32), ws_, w1, w2)
+
+
+def check_router_against_oracle(inp, cfg: MoEConfig, require_order=True):
+    """The router on the device against the oracle: the expert sets of every token
+    away from near-ties bit-exact, the best-first order of every token whose chosen
+    scores are all GAP apart, the weights to 1e-4, distinct in-range experts, the
+    softmax aux score, and a clean error word. Returns (idx, w, aux, ws)."""
+    idx, w, aux, ws = run_router(inp, cfg)
+    ref = oracle_router(inp, cfg)
+    n, bad, excluded = routing_mismatches(idx, ref, cfg)
+    assert not bad, f"{len(bad)} of {n} tokens routed differently, e.g. {bad[:5]}"
+    n_ord, bad_ord = order_mismatches(idx, ref, excluded, inp.get("sel_bias"))
+    assert not bad_ord, f"{len(bad_ord)} of {n_ord} tokens not best first, e.g. {bad_ord[:5]}"
+    if require_order:
+        assert n_ord > 0
+    keep = ~excluded
+    ref_sets = np.sort(ref.topk_idx, 1)
+    g = idx.cpu().numpy()
+    order = np.argsort(g, 1)
+    g_sorted = np.take_along_axis(g, order, 1)
+    w_sorted = np.take_along_axis(w.cpu().numpy().astype(np.float64), order, 1)
+    r_order = np.argsort(ref.topk_idx, 1)
+    rw_sorted = np.take_along_axis(ref.topk_w, r_order, 1)
+    np.testing.assert_array_equal(g_sorted[keep], ref_sets[keep])
+    np.testing.assert_allclose(w_sorted[keep], rw_sorted[keep], rtol=1e-4, atol=1e-6)
+    assert (g >= 0).all() and (g < cfg.E).all()
+    assert all(len(set(r)) == cfg.k for r in g.tolist())
+    if cfg.score == "softmax":
+        assert abs(aux.item() - ref.aux) <= 1e-4 * abs(ref.aux) + (excluded.sum() * 4.0 / cfg.T)
+    assert B.moe_get_device_error(ws) == 0
+    return idx, w, aux, ws

@@ -9,8 +9,9 @@ import pytest
 import torch
 
 import oracle
-from gpu_helpers import (A_REL_FRO, assert_close_y, oracle_router, oracle_y_for_tokens, order_mismatches,
-                         read_metadata, routing_mismatches, run_forward, run_router, tile_sample_tokens)
+from gpu_helpers import (A_REL_FRO, assert_close_y, check_router_against_oracle, oracle_router, oracle_y_for_tokens,
+                         order_mismatches, read_metadata, routing_mismatches, run_forward, run_router,
+                         tile_sample_tokens)
 from moe_expert_router_gb300 import binding as B
 from moe_expert_router_gb300.workloads import (CONFIGS, MoEConfig, even_routing, generate,
                                                routing_with_counts)
@@ -300,28 +301,7 @@ ROUTER_CASES = {
 def test_router_vs_oracle(name):
     cfg = ROUTER_CASES[name]
     inp = generate(cfg, seed=11, device=DEV)
-    idx, w, aux, ws = run_router(inp, cfg)
-    ref = oracle_router(inp, cfg)
-    n, bad, excluded = routing_mismatches(idx, ref, cfg)
-    assert not bad, f"{len(bad)} of {n} tokens routed differently, e.g. {bad[:5]}"
-    n_ord, bad_ord = order_mismatches(idx, ref, excluded, inp.get("sel_bias"))
-    assert n_ord > 0 and not bad_ord, f"{len(bad_ord)} of {n_ord} tokens not best first, e.g. {bad_ord[:5]}"
-    keep = ~excluded
-    ref_sets = np.sort(ref.topk_idx, 1)
-    g = idx.cpu().numpy()
-    order = np.argsort(g, 1)
-    g_sorted = np.take_along_axis(g, order, 1)
-    w_sorted = np.take_along_axis(w.cpu().numpy().astype(np.float64), order, 1)
-    r_order = np.argsort(ref.topk_idx, 1)
-    rw_sorted = np.take_along_axis(ref.topk_w, r_order, 1)
-    np.testing.assert_array_equal(g_sorted[keep], ref_sets[keep])
-    np.testing.assert_allclose(w_sorted[keep], rw_sorted[keep], rtol=1e-4, atol=1e-6)
-    # every token's k experts are distinct and in range
-    assert (g >= 0).all() and (g < cfg.E).all()
-    assert all(len(set(r)) == cfg.k for r in g.tolist())
-    if cfg.score == "softmax":
-        assert abs(aux.item() - ref.aux) <= 1e-4 * abs(ref.aux) + (excluded.sum() * 4.0 / cfg.T)
-    assert B.moe_get_device_error(ws) == 0
+    check_router_against_oracle(inp, cfg)
 
 
 # ------------------------------------------------------------------ full sizes
