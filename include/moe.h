@@ -507,7 +507,10 @@ moe_status_t moe_mx_quantize(const void *in, int64_t rows, int64_t cols, void *c
  * r of the metadata (token t = perm_slot[r] / k) gets MXFP8 codes and scales of
  * x[t,:] in the workspace (x_codes [T*k, H]; x_scales words [H/128][rows4(T*k)];
  * routed order), so stage 1 reads whole tiles. x bf16 [T,H]. Needs the metadata of
- * moe_routing_metadata in ws and flags containing MOE_SHAPE_MXFP8.
+ * moe_routing_metadata in ws and flags containing MOE_SHAPE_MXFP8. Each token's
+ * row is read and quantized once and written to its k routed rows; the scales
+ * pass through the workspace's obuf region (idle until stage 2), which this call
+ * overwrites.
  */
 moe_status_t moe_mx_quantize_dispatch(const void *x, const moe_shape_t *shape, void *ws, size_t ws_bytes,
                                       void *stream);

@@ -310,11 +310,12 @@ cudaError_t launch_combine_bwd(const CombineBwdLaunch &p, cudaStream_t st);
 // expert stages (stage 1: out = a codes, out_sf = a scales; stage 2 as kStage2).
 cudaError_t launch_mx_quantize(const __nv_bfloat16 *in, int64_t rows, int64_t cols, uint8_t *codes,
                                uint8_t *scales, cudaStream_t st);
-// The MXFP8 dispatch: quantize the x rows of routed rows [0, *routed) (token
-// perm_slot[r] / k) into codes [R, cols] and k-block-major scale words
-// [cols / 128][R rounded up to 4], routed order.
-cudaError_t launch_mx_quantize_dispatch(const __nv_bfloat16 *x, const int32_t *perm_slot, const int32_t *routed,
-                                        int k, int64_t R, int64_t cols, uint8_t *codes, uint8_t *scales,
+// The MXFP8 dispatch: quantize each token's x row once into its routed rows
+// row_of[t k + j] of codes [R = T k, cols] and of the k-block-major scale words
+// [cols / 128][R rounded up to 4] (rows [0, *routed)); sc_tmp holds R * cols / 32
+// bytes of row-major scales in between (two launches).
+cudaError_t launch_mx_quantize_dispatch(const __nv_bfloat16 *x, const int32_t *row_of, const int32_t *routed, int k,
+                                        int64_t T, int64_t cols, uint8_t *codes, uint8_t *scales, uint8_t *sc_tmp,
                                         cudaStream_t st);
 // MXFP8 weight gradients: padded row offsets kpad [E+1] of the quantized operands
 // (each expert's rows rounded up to whole 128-row k-blocks), the quantization of

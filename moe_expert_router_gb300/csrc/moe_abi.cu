@@ -376,10 +376,12 @@ moe_status_t run_gemm1_mx(const moe_shape_t &s, const void *w1q, const void *w1s
     return cuda_status(launch_gemm1_mx(p, st));
 }
 
-// The MXFP8 dispatch: x quantized straight into routed order (needs the metadata).
+// The MXFP8 dispatch: x quantized straight into routed order (needs the metadata;
+// obuf, idle until stage 2, holds the row-major scales in between).
 moe_status_t run_mx_dispatch(const moe_shape_t &s, const void *x, const Ws &w, cudaStream_t st) {
-    return cuda_status(launch_mx_quantize_dispatch(static_cast<const __nv_bfloat16 *>(x), w.perm_slot,
-                                                   w.offsets + s.E, s.k, s.T * s.k, s.H, w.x_codes, w.x_scales, st));
+    return cuda_status(launch_mx_quantize_dispatch(static_cast<const __nv_bfloat16 *>(x), w.row_of, w.offsets + s.E,
+                                                   s.k, s.T, s.H, w.x_codes, w.x_scales,
+                                                   reinterpret_cast<uint8_t *>(w.obuf), st));
 }
 
 // Stage 2 in MXFP8: E4M3 a and w2 through TMA, weighted rows into obuf, then the k-way combine.
