@@ -144,6 +144,47 @@ def test_quantizing_dispatch_is_the_quantizer_in_routed_order():
     np.testing.assert_array_equal(scales[: len(perm)], rs[tok])
 
 
+@pytest.mark.parametrize("T,H,E,k,drop", [
+    (70, 1152, 8, 3, True),     # a full and a partial 1024-column chunk per token; 207 routed rows
+    (50, 4224, 6, 2, False),    # 33 k-blocks: the scale transpose takes two column tiles
+    (1, 128, 4, 4, True),       # one token, one k-block, a dropped slot
+])
+def test_quantizing_dispatch_ragged_and_dropped(T, H, E, k, drop):
+    """The token-major dispatch at the edges of its tiling: codes and scale words of the
+    routed rows [0, routed) are the oracle's quantization of each row's token, and
+    the rows past the routed count (those of dropped slots) are left untouched."""
+    g = torch.Generator().manual_seed(T + H)
+    x = (torch.randn(T, H, generator=g) * 3.0).to(torch.bfloat16)
+    idx = torch.stack([torch.randperm(E, generator=g)[:k] for _ in range(T)]).to(torch.int32)
+    if drop:
+        idx[0, k - 1] = -1
+        idx[T // 2, 0] = E
+    shp = B.shape(T, H, 128, E, k, mxfp8=True)
+    ws = B.new_workspace(shp, DEV)
+    L = B.moe_workspace_layout(shp)
+    R = T * k
+    R4 = (R + 3) // 4 * 4
+    ws[L.x_codes:L.x_codes + R * H] = 0xAB
+    ws[L.x_scales:L.x_scales + R4 * H // 32] = 0xCD
+    B.moe_routing_metadata(idx.to(DEV), shp, ws)
+    B.moe_mx_quantize_dispatch(x.to(DEV), shp, ws)
+    torch.cuda.synchronize()
+    err = B.moe_get_device_error(ws)
+    assert bool(err & B.DEVERR_BAD_EXPERT_INDEX) == drop
+    codes = ws[L.x_codes:L.x_codes + R * H].view(R, H).cpu().numpy()
+    raw = ws[L.x_scales:L.x_scales + R4 * H // 32].view(H // 128, R4, 4).cpu().numpy()
+    scales = kmajor_scales_to_rows(raw, rows=R)
+    _, _, _, perm, _ = read_metadata(ws, shp)
+    n = len(perm)
+    assert n == R - (2 if drop else 0)
+    rc, rs = oracle.mx_quantize(x)
+    tok = perm // k
+    np.testing.assert_array_equal(codes[:n], rc[tok])
+    np.testing.assert_array_equal(scales[:n], rs[tok])
+    assert (codes[n:] == 0xAB).all()
+    assert (raw[:, n:R4, :] == 0xCD).all()
+
+
 @pytest.mark.parametrize("name", sorted(CASES))
 @pytest.mark.parametrize("staged", [True, False])
 def test_mx_forward_matches_oracle(name, staged):
@@ -306,6 +347,42 @@ def _assert_close_bound(g, r, rel_bound, abs_frac, what):
     return rel
 
 
+def check_wgrad_operands(ws, shp, cfg, idx, inp):
+    """The transposed MXFP8 operands the weight gradients read, bit-exact against the
+    oracle's quantizer: dY^T and x^T over every expert's rows (the oracle's routing
+    metadata), quantized along the rows in 32-row blocks from the expert's first row,
+    each expert's segment padded with zero rows to whole 128-row k-blocks. Workspace
+    layout (white box): after the padded offsets, codes of dY^T [H, ld], (w a)^T,
+    dH^T and x^T [H, ld], then their scales as k-block-major words [ld / 128][C]."""
+    H, I, E, k = cfg.H, cfg.I, cfg.E, cfg.k
+    md = oracle.routing_metadata(idx.cpu(), E)
+    L = B.moe_workspace_layout(shp)
+    ld = (cfg.T * k + 128 * E + 127) // 128 * 128
+    align = lambda v: (v + 255) // 256 * 256
+    codes0 = L.mx_wgrad + align(4 * (E + 1))
+    scales0 = codes0 + align((2 * H + 3 * I) * ld)
+    operands = {"dY": (0, inp["dy"]), "x": (H + 3 * I, inp["x"])}
+    for name, (row_off, src) in operands.items():
+        codes = ws[codes0 + row_off * ld:codes0 + (row_off + H) * ld].view(H, ld).cpu().numpy()
+        words = ws[scales0 + row_off * (ld // 32):scales0 + (row_off + H) * (ld // 32)].view(ld // 128, H, 4)
+        words = words.cpu().numpy()
+        kp = 0
+        for e in range(E):
+            cnt = int(md.counts[e])
+            seg = (cnt + 127) // 128 * 128
+            if seg == 0:
+                continue
+            tok = torch.as_tensor(md.perm_slot[md.offsets[e]:md.offsets[e + 1]] // k, dtype=torch.long)
+            m = torch.zeros((seg, H), dtype=torch.bfloat16)
+            m[:cnt] = src.cpu()[tok]
+            rc, rs = oracle.mx_quantize(m.t().contiguous())
+            np.testing.assert_array_equal(codes[:, kp:kp + seg], rc, err_msg=f"{name}^T codes, expert {e}")
+            blocks = range(kp // 32, (kp + seg) // 32)
+            got = np.stack([words[b // 4, :, b % 4] for b in blocks], axis=1)
+            np.testing.assert_array_equal(got, rs, err_msg=f"{name}^T scales, expert {e}")
+            kp += seg
+
+
 @pytest.mark.parametrize("name", sorted(TRAIN_CASES))
 def test_mx_training_step_matches_oracle(name):
     cfg, counts = TRAIN_CASES[name]
@@ -343,6 +420,7 @@ def check_mx_training(cfg, idx=None, w=None, seed=4):
     assert_close_y(aw, wa_ref[perm], "w a (routed order)")
     tok = torch.as_tensor(perm // cfg.k, dtype=torch.long)
     assert torch.equal(dyp.cpu(), inp["dy"].cpu()[tok])
+    check_wgrad_operands(ws, shp, cfg, idx, inp)
     # the MXFP8 weight-gradient kernels on the GPU's own operands
     dw2_k = oracle.mx_wgrad(offsets, dyp, aw)
     dw1_k = oracle.mx_wgrad(offsets, dh, inp["x"].cpu()[tok])
