@@ -423,6 +423,7 @@ def run_ours(args, cfg, rank, world, local_rank):
         start to the last download's end."""
         uploaded = [torch.cuda.Event() for _ in range(2)]
         computed = [torch.cuda.Event() for _ in range(2)]
+        downloaded = [torch.cuda.Event() for _ in range(2)]
         t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
 
         def upload(j):
@@ -437,6 +438,8 @@ def run_ours(args, cfg, rank, world, local_rank):
         for i in range(n):
             cur, nxt = i % 2, (i + 1) % 2
             stream.wait_event(uploaded[cur])
+            if i >= 2:
+                stream.wait_event(downloaded[cur])   # step i - 2's outputs have reached the host
             for call in calls(x_buf[cur], dy_buf[cur] if train else None, y=y_buf[cur], aux=aux_buf[cur],
                               dx=dx_buf[cur] if train else None):
                 call()
@@ -451,6 +454,7 @@ def run_ours(args, cfg, rank, world, local_rank):
                 aux_host[cur].copy_(aux_buf[cur], non_blocking=True)
                 if train:
                     dx_host[cur].copy_(dx_buf[cur], non_blocking=True)
+            downloaded[cur].record(down)
         up.wait_stream(down)
         t1.record(up)
         t1.synchronize()                     # the host holds every step's result
