@@ -49,8 +49,8 @@ KERNEL_SOURCES = ("moe_expert_router_gb300/csrc/gemm_kernel.cuh", "moe_expert_ro
                   "moe_expert_router_gb300/csrc/ptx.cuh", "moe_expert_router_gb300/csrc/internal.cuh")
 STAGE1_TRAFFIC = {
     # profiles/tc_gemm_large_group_ncu.md, one step at full size: dispatch copy
-    # 117.74 MB read + 875.56 MB written, tc_gemm_kernel<0> 16.213 GB + 264.25 MB
-    "large_group": {"src": "c68ce97224732ff5", "bytes": 117.74e6 + 875.56e6 + 16.213e9 + 264.25e6},
+    # 117.76 MB read + 875.45 MB written, tc_gemm_kernel<0> 16.274 GB + 263.98 MB
+    "large_group": {"src": "76bbf096a270446f", "bytes": 117.76e6 + 875.45e6 + 16.274e9 + 263.98e6},
 }
 
 

@@ -219,7 +219,7 @@ struct GemmArgs {
     int half;                   // stage 1: row offset of the up projection (= I); dA: I
     int out_ld;                 // row stride (elements) of out / out2 / out3
     int R;                      // routed rows
-    int T, splits, kb_per_split, kb_total, kb_h;   // router
+    int T, splits, kb_per_split, kb_total;         // router
     int n_mma;                  // router: N of its MMAs and rows of its weight tile (E rounded up to 32, <= 256;
                                 //   3 router_seg with the parts fused)
     int router_seg;             // router: accumulator columns of each of the hi / mid / lo parts when one
@@ -723,8 +723,11 @@ tc_gemm_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs g) {
                             for (int part = 0; part < 3; ++part)
                                 tma_load_2d(sb + part * g.router_seg * ROW_BYTES, &maps.b, kx, part * g.E, full);
                         } else {
-                            const int seg = kb / g.kb_h;              // 0: hi, 1: mid, 2: lo
-                            const int kx = (kb - seg * g.kb_h) * BK;
+                            // the hi, mid and lo parts of one x k-block in consecutive
+                            // k-blocks: the x tile's second and third copies hit L2
+                            const int kh = kb / 3;
+                            const int seg = kb - 3 * kh;              // 0: hi, 1: mid, 2: lo
+                            const int kx = kh * BK;
                             tma_load_2d(sa, &maps.a, kx, t.row0, full);
                             if (two) tma_load_2d(sa + A_HALF_BYTES, &maps.a, kx, t.row0 + BM, full);
                             tma_load_2d(sb, &maps.b, kx, seg * g.E + t.n * BN, full);

@@ -88,7 +88,6 @@ cudaError_t launch_router_gemm(const RouterGemmLaunch &p, cudaStream_t st) {
     g.n_mma = g.router_seg ? 3 * g.router_seg : router_n_mma(p.E);
     g.n_tiles = (p.E + BN - 1) / BN;
     g.T = p.T;
-    g.kb_h = (p.H + BK - 1) / BK;
     g.kb_total = static_cast<int>(router_kb_total(p.H, p.E));
     g.splits = p.splits;
     g.kb_per_split = (g.kb_total + p.splits - 1) / p.splits;

@@ -47,7 +47,8 @@ inline size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255);
 // Router GEMM layout (logits = x . w_r^T with w_r split into three bf16 parts). With E <= 64 one MMA of N = 3 * router_seg(E) multiplies
 // an x tile by the hi, mid and lo parts of w_r at once (each part's rows padded
 // to router_seg(E) accumulator columns), so x is loaded once per k-block;
-// otherwise the three parts are separate k-blocks of the reduction.
+// otherwise the three parts are separate k-blocks of the reduction, the three
+// of one x k-block consecutive.
 inline int router_seg(int64_t E) { return E <= 32 ? 32 : (E <= 64 ? 64 : 0); }
 inline int64_t router_kb_total(int64_t H, int64_t E) {
     const int64_t kb_h = (H + kBK - 1) / kBK;
