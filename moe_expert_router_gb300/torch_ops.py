@@ -19,6 +19,14 @@ libmoe's, and there is no CPU implementation.
 Shapes: x bf16 [T, H]; w_r fp32 [E, H]; w1 [E, 2I, H], w2 [E, H, I] (bf16, or
 E4M3 codes with k-block-major E8M0 scales from `moe_mx_quantize`); topk_idx int32
 [T, k]; topk_w fp32 [T, k]; y bf16 [T, H].
+
+For training, `moe_layer(x, w_r, w1, w2, k, ...)` is the whole layer (router and
+expert path, bf16) as one differentiable call: `torch.ops.moe_gb300.layer_train`
+runs the router (keeping the fp32 logits), the routing metadata and both stages
+(keeping the pre-activation h), and `torch.ops.moe_gb300.layer_backward` runs the
+library's backward (dX with the router's term, dW_r, dW1, dW2); `register_autograd`
+joins them. Gradients reach the router through y only: topk_idx, topk_w and aux
+are returned without a gradient (the library does not differentiate aux).
 """
 from typing import Optional, Tuple
 
@@ -86,3 +94,112 @@ def forward_mx(x: torch.Tensor, topk_idx: torch.Tensor, topk_w: torch.Tensor, w1
 @forward_mx.register_fake
 def _forward_mx_fake(x, topk_idx, topk_w, w1_codes, w1_scales, w2_codes, w2_scales):
     return x.new_empty(x.shape, dtype=torch.bfloat16)
+
+
+def _train_workspace(shp, device) -> torch.Tensor:
+    # a whole allocation (the caching allocator aligns it to 512 bytes), so the
+    # workspace can be an operator output that aliases nothing
+    ws = torch.empty(B.moe_workspace_size(shp), dtype=torch.uint8, device=device)
+    if ws.data_ptr() % 256:
+        raise RuntimeError("libmoe needs a 256-byte aligned workspace")
+    B.moe_workspace_init(ws)
+    return ws
+
+
+@torch.library.custom_op(f"{_LIB}::layer_train", mutates_args=())
+def layer_train(x: torch.Tensor, w_r: torch.Tensor, w1: torch.Tensor, w2: torch.Tensor, k: int,
+                score: str = "softmax", normalize: bool = True, scale: float = 1.0, n_group: int = 1,
+                topk_group: int = 1, group_topn: int = 2, sel_bias: Optional[torch.Tensor] = None,
+                logit_offset: Optional[torch.Tensor] = None
+                ) -> Tuple[torch.Tensor, torch.Tensor, torch.Tensor, torch.Tensor, torch.Tensor, torch.Tensor,
+                           torch.Tensor]:
+    """The layer's training forward: (y, topk_idx, topk_w, aux, h, logits, ws); the last
+    three are what layer_backward reads."""
+    T, H = x.shape
+    E, two_i, _ = w1.shape
+    I = two_i // 2
+    shp = B.shape(T, H, I, E, k, training=True)
+    ws = _train_workspace(shp, x.device)
+    idx = torch.empty((T, k), dtype=torch.int32, device=x.device)
+    w = torch.empty((T, k), dtype=torch.float32, device=x.device)
+    aux = torch.zeros((1,), dtype=torch.float32, device=x.device)
+    logits = torch.empty((T, E), dtype=torch.float32, device=x.device)
+    a = torch.empty((T * k, I), dtype=torch.bfloat16, device=x.device)
+    h = torch.empty((T * k, 2 * I), dtype=torch.bfloat16, device=x.device)
+    y = torch.empty((T, H), dtype=torch.bfloat16, device=x.device)
+    cfg = B.router_cfg(score, normalize, scale, n_group, topk_group, group_topn)
+    B.moe_router_train(x, w_r, shp, cfg, idx, w, logits, ws, aux=aux, logit_offset=logit_offset,
+                       sel_bias=sel_bias)
+    B.moe_routing_metadata(idx, shp, ws)
+    B.moe_dispatch_gemm1_train(x, w1, shp, a, h, ws)
+    B.moe_swiglu_gemm2_combine(a, w, w2, shp, y, ws)
+    return y, idx, w, aux, h, logits, ws
+
+
+@layer_train.register_fake
+def _layer_train_fake(x, w_r, w1, w2, k, score="softmax", normalize=True, scale=1.0, n_group=1, topk_group=1,
+                      group_topn=2, sel_bias=None, logit_offset=None):
+    T, H = x.shape
+    E, two_i, _ = w1.shape
+    n = B.moe_workspace_size(B.shape(int(T), int(H), int(two_i) // 2, int(E), k, training=True))
+    return (x.new_empty((T, H), dtype=torch.bfloat16), x.new_empty((T, k), dtype=torch.int32),
+            x.new_empty((T, k), dtype=torch.float32), x.new_empty((1,), dtype=torch.float32),
+            x.new_empty((T * k, two_i), dtype=torch.bfloat16), x.new_empty((T, E), dtype=torch.float32),
+            x.new_empty((n,), dtype=torch.uint8))
+
+
+@torch.library.custom_op(f"{_LIB}::layer_backward", mutates_args=("ws",))
+def layer_backward(dy: torch.Tensor, x: torch.Tensor, w_r: torch.Tensor, w1: torch.Tensor, w2: torch.Tensor,
+                   topk_idx: torch.Tensor, topk_w: torch.Tensor, h: torch.Tensor, logits: torch.Tensor,
+                   ws: torch.Tensor, score: str = "softmax", normalize: bool = True, scale: float = 1.0,
+                   n_group: int = 1, topk_group: int = 1, group_topn: int = 2
+                   ) -> Tuple[torch.Tensor, torch.Tensor, torch.Tensor, torch.Tensor]:
+    """The layer's backward from dY: (dX, dW_r, dW1, dW2). ws is layer_train's workspace
+    (its routing metadata and dispatched rows; the backward also uses it as scratch)."""
+    T, H = x.shape
+    E, two_i, _ = w1.shape
+    k = topk_idx.shape[1]
+    shp = B.shape(T, H, two_i // 2, E, k, training=True)
+    dx = torch.empty((T, H), dtype=torch.bfloat16, device=x.device)
+    dw_r = torch.empty((E, H), dtype=torch.float32, device=x.device)
+    dw1 = torch.empty_like(w1)
+    dw2 = torch.empty_like(w2)
+    dtw = torch.empty((T, k), dtype=torch.float32, device=x.device)   # routing-weight gradient, for dW_r
+    cfg = B.router_cfg(score, normalize, scale, n_group, topk_group, group_topn)
+    B.moe_backward(x, topk_idx, topk_w, w1, w2, h, dy.contiguous(), shp, dx, dw1, dw2, ws, w_r=w_r,
+                   logits=logits, cfg=cfg, dw_r=dw_r, dtopk_w=dtw)
+    return dx, dw_r, dw1, dw2
+
+
+@layer_backward.register_fake
+def _layer_backward_fake(dy, x, w_r, w1, w2, topk_idx, topk_w, h, logits, ws, score="softmax", normalize=True,
+                         scale=1.0, n_group=1, topk_group=1, group_topn=2):
+    return (x.new_empty(x.shape, dtype=torch.bfloat16), w_r.new_empty(w_r.shape, dtype=torch.float32),
+            w1.new_empty(w1.shape), w2.new_empty(w2.shape))
+
+
+def _layer_setup_context(ctx, inputs, output):
+    x, w_r, w1, w2, k, score, normalize, scale, n_group, topk_group, group_topn, sel_bias, logit_offset = inputs
+    _, idx, w, _, h, logits, ws = output
+    ctx.save_for_backward(x, w_r, w1, w2, idx, w, h, logits, ws)
+    ctx.cfg = (score, normalize, scale, n_group, topk_group, group_topn)
+    ctx.mark_non_differentiable(*output[1:])
+
+
+def _layer_backward_rule(ctx, dy, *unused):
+    x, w_r, w1, w2, idx, w, h, logits, ws = ctx.saved_tensors
+    dx, dw_r, dw1, dw2 = layer_backward(dy, x, w_r, w1, w2, idx, w, h, logits, ws, *ctx.cfg)
+    return dx, dw_r, dw1, dw2, None, None, None, None, None, None, None, None, None
+
+
+layer_train.register_autograd(_layer_backward_rule, setup_context=_layer_setup_context)
+
+
+def moe_layer(x, w_r, w1, w2, k, score="softmax", normalize=True, scale=1.0, n_group=1, topk_group=1,
+              group_topn=2, sel_bias=None, logit_offset=None):
+    """The MoE layer as one differentiable call: (y, topk_idx, topk_w, aux). x bf16 [T, H],
+    w_r fp32 [E, H], w1 bf16 [E, 2I, H], w2 bf16 [E, H, I]; y.backward(dy) fills x.grad
+    (with the router's term), w_r.grad, w1.grad and w2.grad through the library."""
+    y, idx, w, aux, _, _, _ = layer_train(x, w_r, w1, w2, k, score, normalize, scale, n_group, topk_group,
+                                          group_topn, sel_bias, logit_offset)
+    return y, idx, w, aux

@@ -43,3 +43,49 @@ def test_compiled_router_and_forward_equal_the_direct_calls():
     # the aux score's per-expert sums are accumulated with atomics: equal to rounding
     assert torch.allclose(aux_c, aux, rtol=1e-5, atol=0.0)
     assert torch.equal(y_c, y)
+
+
+def _layer_grads(fn, inp):
+    x = inp["x"].clone().requires_grad_(True)
+    w_r = inp["w_r"].clone().requires_grad_(True)
+    w1 = inp["w1"].clone().requires_grad_(True)
+    w2 = inp["w2"].clone().requires_grad_(True)
+    y, idx, w, _ = fn(x, w_r, w1, w2)
+    y.backward(inp["dy"])
+    return y.detach(), idx, w, x.grad, w_r.grad, w1.grad, w2.grad
+
+
+def _layer_fn(cfg, inp):
+    def fn(x, w_r, w1, w2):
+        return torch_ops.moe_layer(x, w_r, w1, w2, cfg.k, cfg.score, cfg.normalize, cfg.scale, cfg.n_group,
+                                   cfg.topk_group, cfg.group_topn, inp.get("sel_bias"), inp.get("logit_offset"))
+    return fn
+
+
+@pytest.mark.parametrize("case", ["ragged_sigmoid_groups", "zipf_offsets"])
+def test_autograd_layer_equals_the_direct_training_calls(case):
+    """moe_layer under autograd: y, the routing and every gradient (x with the router's
+    term, w_r, w1, w2) bit-identical to the same training step through the C ABI, which
+    the backward tests check against the oracle."""
+    from test_gpu_backward import CASES, _inputs, train_step
+    cfg = CASES[case]
+    inp = _inputs(cfg, seed=5)
+    y, idx, w, gx, gwr, g1, g2 = _layer_grads(_layer_fn(cfg, inp), inp)
+    out = train_step(inp, cfg, staged=False)
+    assert out["err"] == 0
+    assert torch.equal(idx, out["idx"]) and torch.equal(w, out["w"]) and torch.equal(y, out["y"])
+    assert torch.equal(gx, out["dx"]) and torch.equal(gwr, out["dwr"])
+    assert torch.equal(g1, out["dw1"]) and torch.equal(g2, out["dw2"])
+
+
+def test_compiled_autograd_layer_equals_eager():
+    """moe_layer compiled with AOTAutograd (forward and backward graphs traced through the
+    operators' shape functions, no graph break): the same y and gradients as eager."""
+    from test_gpu_backward import CASES, _inputs
+    cfg = CASES["ragged_sigmoid_groups"]
+    inp = _inputs(cfg, seed=6)
+    fn = _layer_fn(cfg, inp)
+    eager = _layer_grads(fn, inp)
+    compiled = _layer_grads(torch.compile(fn, fullgraph=True, backend="aot_eager"), inp)
+    for a, b in zip(eager, compiled):
+        assert torch.equal(a, b)

@@ -7,7 +7,7 @@ from moe_expert_router_gb300 import torch_ops  # noqa: F401  (registers the oper
 
 
 def test_operators_are_registered():
-    for name in ("router", "forward", "forward_mx"):
+    for name in ("router", "forward", "forward_mx", "layer_train", "layer_backward"):
         assert hasattr(torch.ops.moe_gb300, name)
 
 
@@ -29,3 +29,21 @@ def test_fake_shapes():
         s2 = torch.empty((I // 128, E, H, 4), dtype=torch.uint8, device="cuda")
         y = torch.ops.moe_gb300.forward_mx(x, idx, w, c1, s1, c2, s2)
         assert y.shape == (T, H) and y.dtype == torch.bfloat16
+
+
+def test_layer_autograd_shapes():
+    """moe_layer's forward and its registered backward on shape-only tensors: output
+    and gradient shapes and dtypes, the routing outputs without a gradient."""
+    T, H, I, E, k = 40, 256, 128, 8, 2
+    # meta tensors: the operators' shape functions run, and the autograd engine needs no device
+    x = torch.empty((T, H), dtype=torch.bfloat16, device="meta", requires_grad=True)
+    w_r = torch.empty((E, H), dtype=torch.float32, device="meta", requires_grad=True)
+    w1 = torch.empty((E, 2 * I, H), dtype=torch.bfloat16, device="meta", requires_grad=True)
+    w2 = torch.empty((E, H, I), dtype=torch.bfloat16, device="meta", requires_grad=True)
+    y, idx, w, aux = torch_ops.moe_layer(x, w_r, w1, w2, k, "sigmoid", True, 2.5, 4, 2, 2)
+    assert y.shape == (T, H) and y.dtype == torch.bfloat16 and y.requires_grad
+    assert idx.shape == (T, k) and not w.requires_grad and not aux.requires_grad
+    y.backward(torch.empty_like(y))
+    assert x.grad.shape == x.shape and x.grad.dtype == torch.bfloat16
+    assert w_r.grad.shape == w_r.shape and w_r.grad.dtype == torch.float32
+    assert w1.grad.shape == w1.shape and w2.grad.shape == w2.shape
