@@ -87,6 +87,13 @@ CONFIGS: dict[str, MoEConfig] = {
     "zipf_prefill_slice": MoEConfig("zipf_prefill_slice", T=4096, H=4096, I=1536, E=128, k=8,
                                     zipf_s=1.2,
                                     description="zipf_prefill shapes at T=4096 (profiling size)"),
+    # profiling size of large_group's router: its tokens, hidden size, 256 experts and
+    # group-limited sigmoid routing (the same router kernels and split) with I = 128, so
+    # that a full ncu capture holds about 3 GB on the device
+    "large_group_router": MoEConfig("large_group_router", T=8192, H=7168, I=128, E=256, k=8,
+                                    score="sigmoid", scale=2.5, n_group=8, topk_group=4,
+                                    group_topn=2, sel_bias=True,
+                                    description="large_group router geometry, I = 128 (profiling size)"),
     # profiling size of the training step: the train geometry per expert (H, I, k,
     # about 768 routed rows per expert) with 16 experts, about 1 GB on the device
     "train_slice": MoEConfig("train_slice", T=2048, H=4096, I=1536, E=16, k=6, backward=True,
