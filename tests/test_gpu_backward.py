@@ -123,6 +123,9 @@ CASES = {
     "top1_normalized_softmax": _cfg(150, 128, 128, 8, 1),
     "top1_normalized_sigmoid": _cfg(150, 128, 128, 8, 1, score="sigmoid", scale=2.5),
     "one_token": _cfg(1, 64, 64, 4, 2),
+    # many experts and a large k: a wide router backward (E = 512), 16 slots per token
+    "e512_k16_groups": _cfg(96, 128, 64, 512, 16, score="sigmoid", scale=2.5, n_group=16, topk_group=8,
+                            sel_bias=True),
 }
 
 

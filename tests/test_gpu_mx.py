@@ -121,6 +121,8 @@ CASES = {
     "one_token": _cfg(1, 128, 128, 4, 2),
     # T k = 999: the scale arrays' rows are padded to 1000 (k-block-major words)
     "odd_rows": _cfg(333, 384, 256, 5, 3),
+    # the largest E and k: 2048 slots over 1024 experts, most of them empty or one-row
+    "e1024_k32": _cfg(64, 128, 128, 1024, 32),
 }
 
 
@@ -318,6 +320,8 @@ TRAIN_CASES = {
     "ragged": (_cfg(320, 256, 384, 8, 2), [0, 1, 33, 128, 129, 300, 5, 44]),
     # 256 rows per expert: two full k-blocks
     "two_kblocks": (_cfg(512, 512, 256, 4, 2), None),
+    # 256 experts with about two rows each: 256 padded k-blocks, mostly zero rows
+    "many_experts": (_cfg(64, 128, 128, 256, 8), None),
 }
 
 
