@@ -9,6 +9,8 @@ same bookkeeping on the host: it calls the library's quantizer
 """
 from __future__ import annotations
 
+import weakref
+
 import torch
 
 from . import binding as B
@@ -28,8 +30,11 @@ class MxWeightCache:
 
     ``get(w)`` returns ``(codes, scales)`` for ``w`` and quantizes again when the
     tensor's version counter moved since the cached copy was made (an in-place
-    update through autograd-visible ops). ``invalidate()`` drops every entry:
-    call it once per optimizer step.
+    update through autograd-visible ops), or when ``w`` is not the tensor object
+    the entry was made for (a weight freed and another allocated at its address
+    starts again at version 0; a detached view is another object and is quantized
+    on its own). ``invalidate()`` drops every entry: call it once per optimizer
+    step.
     """
 
     def __init__(self, quantize=None):
@@ -46,11 +51,11 @@ class MxWeightCache:
             raise ValueError("MXFP8 weights are quantized from bf16 along a last dimension of 32k")
         key = self._key(w)
         hit = self._store.get(key)
-        if hit is not None and hit[0] == w._version:
-            return hit[1]
+        if hit is not None and hit[0]() is w and hit[1] == w._version:
+            return hit[2]
         q = self._quantize(w)
         self.quantizations += 1
-        self._store[key] = (w._version, q)
+        self._store[key] = (weakref.ref(w), w._version, q)
         return q
 
     def invalidate(self):

@@ -27,12 +27,17 @@ runs the router (keeping the fp32 logits), the routing metadata and both stages
 library's backward (dX with the router's term, dW_r, dW1, dW2); `register_autograd`
 joins them. Gradients reach the router through y only: topk_idx, topk_w and aux
 are returned without a gradient (the library does not differentiate aux).
+`moe_layer(..., precision="mxfp8")` runs the expert stages and the weight gradients
+in MXFP8 (`layer_train_mx` / `layer_backward_mx`; the data gradients stay bf16, as in
+the guide's section "Expert precision") on E4M3 copies of w1 and w2 from an
+`MxWeightCache`.
 """
 from typing import Optional, Tuple
 
 import torch
 
 from . import binding as B
+from .mx_cache import MxWeightCache
 
 _LIB = "moe_gb300"
 
@@ -195,11 +200,132 @@ def _layer_backward_rule(ctx, dy, *unused):
 layer_train.register_autograd(_layer_backward_rule, setup_context=_layer_setup_context)
 
 
+@torch.library.custom_op(f"{_LIB}::layer_train_mx", mutates_args=())
+def layer_train_mx(x: torch.Tensor, w_r: torch.Tensor, w1: torch.Tensor, w2: torch.Tensor, w1_codes: torch.Tensor,
+                   w1_scales: torch.Tensor, w2_codes: torch.Tensor, w2_scales: torch.Tensor, k: int,
+                   score: str = "softmax", normalize: bool = True, scale: float = 1.0, n_group: int = 1,
+                   topk_group: int = 1, group_topn: int = 2, sel_bias: Optional[torch.Tensor] = None,
+                   logit_offset: Optional[torch.Tensor] = None
+                   ) -> Tuple[torch.Tensor, torch.Tensor, torch.Tensor, torch.Tensor, torch.Tensor, torch.Tensor,
+                              torch.Tensor]:
+    """layer_train with the expert stages in MXFP8 (the guide's mxfp8 expert precision):
+    the router as in bf16, x quantized by the dispatch, stage 1 on the E4M3 copy of w1
+    (keeping h), stage 2 on that of w2. w1 and w2 themselves are only read by the
+    backward's data gradients."""
+    T, H = x.shape
+    E, two_i, _ = w1.shape
+    I = two_i // 2
+    shp = B.shape(T, H, I, E, k, training=True, mxfp8=True)
+    ws = _train_workspace(shp, x.device)
+    R = T * k
+    idx = torch.empty((T, k), dtype=torch.int32, device=x.device)
+    w = torch.empty((T, k), dtype=torch.float32, device=x.device)
+    aux = torch.zeros((1,), dtype=torch.float32, device=x.device)
+    logits = torch.empty((T, E), dtype=torch.float32, device=x.device)
+    aq = torch.empty((R, I), dtype=torch.uint8, device=x.device)
+    as_ = B.mx_scales_empty((R, I), x.device)
+    h = torch.empty((R, 2 * I), dtype=torch.bfloat16, device=x.device)
+    y = torch.empty((T, H), dtype=torch.bfloat16, device=x.device)
+    cfg = B.router_cfg(score, normalize, scale, n_group, topk_group, group_topn)
+    B.moe_router_train(x, w_r, shp, cfg, idx, w, logits, ws, aux=aux, logit_offset=logit_offset,
+                       sel_bias=sel_bias)
+    B.moe_routing_metadata(idx, shp, ws)
+    B.moe_mx_quantize_dispatch(x, shp, ws)
+    B.moe_dispatch_gemm1_mx_train(w1_codes, w1_scales, shp, aq, as_, h, ws)
+    B.moe_swiglu_gemm2_combine_mx(aq, as_, w, w2_codes, w2_scales, shp, y, ws)
+    return y, idx, w, aux, h, logits, ws
+
+
+@layer_train_mx.register_fake
+def _layer_train_mx_fake(x, w_r, w1, w2, w1_codes, w1_scales, w2_codes, w2_scales, k, score="softmax",
+                         normalize=True, scale=1.0, n_group=1, topk_group=1, group_topn=2, sel_bias=None,
+                         logit_offset=None):
+    T, H = x.shape
+    E, two_i, _ = w1.shape
+    n = B.moe_workspace_size(B.shape(int(T), int(H), int(two_i) // 2, int(E), k, training=True, mxfp8=True))
+    return (x.new_empty((T, H), dtype=torch.bfloat16), x.new_empty((T, k), dtype=torch.int32),
+            x.new_empty((T, k), dtype=torch.float32), x.new_empty((1,), dtype=torch.float32),
+            x.new_empty((T * k, two_i), dtype=torch.bfloat16), x.new_empty((T, E), dtype=torch.float32),
+            x.new_empty((n,), dtype=torch.uint8))
+
+
+@torch.library.custom_op(f"{_LIB}::layer_backward_mx", mutates_args=("ws",))
+def layer_backward_mx(dy: torch.Tensor, x: torch.Tensor, w_r: torch.Tensor, w1: torch.Tensor, w2: torch.Tensor,
+                      topk_idx: torch.Tensor, topk_w: torch.Tensor, h: torch.Tensor, logits: torch.Tensor,
+                      ws: torch.Tensor, score: str = "softmax", normalize: bool = True, scale: float = 1.0,
+                      n_group: int = 1, topk_group: int = 1, group_topn: int = 2
+                      ) -> Tuple[torch.Tensor, torch.Tensor, torch.Tensor, torch.Tensor]:
+    """layer_backward of layer_train_mx: the data gradients in bf16 (on w1, w2 and the
+    saved h), dW2 and dW1 in MXFP8 (both operands quantized along the routed rows), the
+    router's gradients as in bf16. Returns (dX, dW_r, dW1, dW2)."""
+    T, H = x.shape
+    E, two_i, _ = w1.shape
+    k = topk_idx.shape[1]
+    shp = B.shape(T, H, two_i // 2, E, k, training=True, mxfp8=True)
+    dy = dy.contiguous()
+    dx = torch.empty((T, H), dtype=torch.bfloat16, device=x.device)
+    dw_r = torch.empty((E, H), dtype=torch.float32, device=x.device)
+    dw1 = torch.empty_like(w1)
+    dw2 = torch.empty_like(w2)
+    dtw = torch.empty((T, k), dtype=torch.float32, device=x.device)
+    cfg = B.router_cfg(score, normalize, scale, n_group, topk_group, group_topn)
+    B.moe_backward_stage2_data(dy, topk_w, w2, h, shp, ws, dtopk_w=dtw)
+    B.moe_backward_stage2_weight_mx(dy, shp, dw2, ws)
+    B.moe_router_backward(x, logits, topk_idx, topk_w, dtw, shp, cfg, dw_r, ws)
+    B.moe_backward_stage1_data(w1, shp, dx, ws, w_r=w_r, topk_idx=topk_idx, cfg=cfg)
+    B.moe_backward_stage1_weight_mx(x, shp, dw1, ws)
+    return dx, dw_r, dw1, dw2
+
+
+@layer_backward_mx.register_fake
+def _layer_backward_mx_fake(dy, x, w_r, w1, w2, topk_idx, topk_w, h, logits, ws, score="softmax",
+                            normalize=True, scale=1.0, n_group=1, topk_group=1, group_topn=2):
+    return (x.new_empty(x.shape, dtype=torch.bfloat16), w_r.new_empty(w_r.shape, dtype=torch.float32),
+            w1.new_empty(w1.shape), w2.new_empty(w2.shape))
+
+
+def _layer_mx_setup_context(ctx, inputs, output):
+    x, w_r, w1, w2 = inputs[:4]
+    score, normalize, scale, n_group, topk_group, group_topn = inputs[9:15]
+    _, idx, w, _, h, logits, ws = output
+    ctx.save_for_backward(x, w_r, w1, w2, idx, w, h, logits, ws)
+    ctx.cfg = (score, normalize, scale, n_group, topk_group, group_topn)
+    ctx.mark_non_differentiable(*output[1:])
+
+
+def _layer_mx_backward_rule(ctx, dy, *unused):
+    x, w_r, w1, w2, idx, w, h, logits, ws = ctx.saved_tensors
+    dx, dw_r, dw1, dw2 = layer_backward_mx(dy, x, w_r, w1, w2, idx, w, h, logits, ws, *ctx.cfg)
+    return (dx, dw_r, dw1, dw2) + (None,) * 13
+
+
+layer_train_mx.register_autograd(_layer_mx_backward_rule, setup_context=_layer_mx_setup_context)
+
+# the E4M3 copies of the expert weights that moe_layer(..., precision="mxfp8") uses when
+# no cache is passed; call .invalidate() once per optimizer step
+DEFAULT_MX_WEIGHT_CACHE = MxWeightCache()
+
+
 def moe_layer(x, w_r, w1, w2, k, score="softmax", normalize=True, scale=1.0, n_group=1, topk_group=1,
-              group_topn=2, sel_bias=None, logit_offset=None):
+              group_topn=2, sel_bias=None, logit_offset=None, precision="bf16", weight_cache=None):
     """The MoE layer as one differentiable call: (y, topk_idx, topk_w, aux). x bf16 [T, H],
     w_r fp32 [E, H], w1 bf16 [E, 2I, H], w2 bf16 [E, H, I]; y.backward(dy) fills x.grad
-    (with the router's term), w_r.grad, w1.grad and w2.grad through the library."""
-    y, idx, w, aux, _, _, _ = layer_train(x, w_r, w1, w2, k, score, normalize, scale, n_group, topk_group,
-                                          group_topn, sel_bias, logit_offset)
+    (with the router's term), w_r.grad, w1.grad and w2.grad through the library.
+
+    precision="mxfp8" runs the expert stages and the weight gradients in MXFP8 (H and I
+    multiples of 128): w1 and w2 stay the bf16 parameters, and their E4M3 copies come
+    from `weight_cache` (an MxWeightCache; DEFAULT_MX_WEIGHT_CACHE if None), which
+    quantizes again when a weight's version counter moves and must be invalidated once
+    per optimizer step."""
+    if precision == "bf16":
+        y, idx, w, aux, _, _, _ = layer_train(x, w_r, w1, w2, k, score, normalize, scale, n_group, topk_group,
+                                              group_topn, sel_bias, logit_offset)
+    elif precision == "mxfp8":
+        cache = DEFAULT_MX_WEIGHT_CACHE if weight_cache is None else weight_cache
+        w1c, w1s = cache.get(w1)
+        w2c, w2s = cache.get(w2)
+        y, idx, w, aux, _, _, _ = layer_train_mx(x, w_r, w1, w2, w1c, w1s, w2c, w2s, k, score, normalize, scale,
+                                                 n_group, topk_group, group_topn, sel_bias, logit_offset)
+    else:
+        raise ValueError(f"precision must be 'bf16' or 'mxfp8', not {precision!r}")
     return y, idx, w, aux

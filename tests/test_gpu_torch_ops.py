@@ -89,3 +89,82 @@ def test_compiled_autograd_layer_equals_eager():
     compiled = _layer_grads(torch.compile(fn, fullgraph=True, backend="aot_eager"), inp)
     for a, b in zip(eager, compiled):
         assert torch.equal(a, b)
+
+
+def test_autograd_mx_layer_equals_the_direct_training_calls():
+    """moe_layer(precision="mxfp8") under autograd: y, the routing and every gradient
+    bit-identical to the MXFP8 training step through the C ABI (router with logits,
+    the MXFP8 forward, bf16 data gradients, MXFP8 weight gradients), whose parts the
+    MXFP8 tests check against the oracle; the weight cache quantizes each weight once
+    and again after an in-place update."""
+    from test_gpu_backward import _inputs
+    from moe_expert_router_gb300.mx_cache import MxWeightCache
+    cfg = MoEConfig("case", T=300, H=256, I=384, E=16, k=4, score="sigmoid", scale=2.5, n_group=4, topk_group=2,
+                    group_topn=2, sel_bias=True, backward=True)
+    inp = _inputs(cfg, seed=8)
+    cache = MxWeightCache()
+
+    def fn(x, w_r, w1, w2):
+        return torch_ops.moe_layer(x, w_r, w1, w2, cfg.k, cfg.score, cfg.normalize, cfg.scale, cfg.n_group,
+                                   cfg.topk_group, cfg.group_topn, inp["sel_bias"], None, precision="mxfp8",
+                                   weight_cache=cache)
+
+    y, idx, w, gx, gwr, g1, g2 = _layer_grads(fn, inp)
+    assert cache.quantizations == 2
+
+    T, H, I, E, k = cfg.T, cfg.H, cfg.I, cfg.E, cfg.k
+    R = T * k
+    shp = B.shape(T, H, I, E, k, training=True, mxfp8=True)
+    ws = B.new_workspace(shp, "cuda")
+    rc = router_cfg_of(cfg)
+    idx_d = torch.empty((T, k), dtype=torch.int32, device="cuda")
+    w_d = torch.empty((T, k), dtype=torch.float32, device="cuda")
+    logits = torch.empty((T, E), dtype=torch.float32, device="cuda")
+    B.moe_router_train(inp["x"], inp["w_r"], shp, rc, idx_d, w_d, logits, ws, sel_bias=inp["sel_bias"])
+    w1c = torch.empty(inp["w1"].shape, dtype=torch.uint8, device="cuda")
+    w1s = B.mx_scales_empty(inp["w1"].shape, "cuda")
+    w2c = torch.empty(inp["w2"].shape, dtype=torch.uint8, device="cuda")
+    w2s = B.mx_scales_empty(inp["w2"].shape, "cuda")
+    B.moe_mx_quantize(inp["w1"], w1c, w1s)
+    B.moe_mx_quantize(inp["w2"], w2c, w2s)
+    aq = torch.empty((R, I), dtype=torch.uint8, device="cuda")
+    as_ = B.mx_scales_empty((R, I), "cuda")
+    h = torch.empty((R, 2 * I), dtype=torch.bfloat16, device="cuda")
+    y_d = torch.empty((T, H), dtype=torch.bfloat16, device="cuda")
+    B.moe_routing_metadata(idx_d, shp, ws)
+    B.moe_mx_quantize_dispatch(inp["x"], shp, ws)
+    B.moe_dispatch_gemm1_mx_train(w1c, w1s, shp, aq, as_, h, ws)
+    B.moe_swiglu_gemm2_combine_mx(aq, as_, w_d, w2c, w2s, shp, y_d, ws)
+    dtw = torch.empty((T, k), dtype=torch.float32, device="cuda")
+    dx = torch.empty((T, H), dtype=torch.bfloat16, device="cuda")
+    dwr = torch.empty((E, H), dtype=torch.float32, device="cuda")
+    dw1 = torch.empty_like(inp["w1"])
+    dw2 = torch.empty_like(inp["w2"])
+    B.moe_backward_stage2_data(inp["dy"], w_d, inp["w2"], h, shp, ws, dtopk_w=dtw)
+    B.moe_backward_stage2_weight_mx(inp["dy"], shp, dw2, ws)
+    B.moe_router_backward(inp["x"], logits, idx_d, w_d, dtw, shp, rc, dwr, ws)
+    B.moe_backward_stage1_data(inp["w1"], shp, dx, ws, w_r=inp["w_r"], topk_idx=idx_d, cfg=rc)
+    B.moe_backward_stage1_weight_mx(inp["x"], shp, dw1, ws)
+    assert B.moe_get_device_error(ws) == 0
+    assert torch.equal(idx, idx_d) and torch.equal(w, w_d) and torch.equal(y, y_d)
+    assert torch.equal(gx, dx) and torch.equal(gwr, dwr) and torch.equal(g1, dw1) and torch.equal(g2, dw2)
+
+    # the same parameters again: cache hits; an in-place update of w1 moves its
+    # version counter, and the next call quantizes w1 again
+    cache2 = MxWeightCache()
+    w1p = inp["w1"].clone().requires_grad_(True)
+    w2p = inp["w2"].clone().requires_grad_(True)
+
+    def call():
+        return torch_ops.moe_layer(inp["x"], inp["w_r"], w1p, w2p, cfg.k, cfg.score, cfg.normalize, cfg.scale,
+                                   cfg.n_group, cfg.topk_group, cfg.group_topn, inp["sel_bias"], None,
+                                   precision="mxfp8", weight_cache=cache2)[0]
+
+    y1 = call()
+    assert cache2.quantizations == 2 and torch.equal(y1, y)
+    call()
+    assert cache2.quantizations == 2
+    with torch.no_grad():
+        w1p.mul_(0.5)
+    y3 = call()
+    assert cache2.quantizations == 3 and not torch.equal(y3, y)

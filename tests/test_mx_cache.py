@@ -44,3 +44,18 @@ def test_separate_tensors_have_separate_entries():
         pass
     else:
         raise AssertionError("a last dimension that is not a multiple of 32 must be rejected")
+
+
+def test_another_tensor_at_the_same_address_is_not_a_hit():
+    """An entry belongs to one tensor object: a detached view (same storage, shape,
+    dtype and version) is quantized on its own, and so would be a new weight that
+    the allocator placed where a freed one was."""
+    c = MxWeightCache(quantize=_fake_quantize)
+    w = torch.zeros((2, 4, 64), dtype=torch.bfloat16)
+    c.get(w)
+    v = w.detach()
+    assert v.data_ptr() == w.data_ptr() and v._version == w._version
+    c.get(v)
+    assert c.quantizations == 2
+    c.get(v)
+    assert c.quantizations == 2

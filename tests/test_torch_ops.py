@@ -7,7 +7,8 @@ from moe_expert_router_gb300 import torch_ops  # noqa: F401  (registers the oper
 
 
 def test_operators_are_registered():
-    for name in ("router", "forward", "forward_mx", "layer_train", "layer_backward"):
+    for name in ("router", "forward", "forward_mx", "layer_train", "layer_backward", "layer_train_mx",
+                 "layer_backward_mx"):
         assert hasattr(torch.ops.moe_gb300, name)
 
 
@@ -46,4 +47,26 @@ def test_layer_autograd_shapes():
     y.backward(torch.empty_like(y))
     assert x.grad.shape == x.shape and x.grad.dtype == torch.bfloat16
     assert w_r.grad.shape == w_r.shape and w_r.grad.dtype == torch.float32
+    assert w1.grad.shape == w1.shape and w2.grad.shape == w2.shape
+
+
+def test_mx_layer_autograd_shapes():
+    """moe_layer(precision="mxfp8") on meta tensors, with a cache whose quantizer only
+    allocates: the MXFP8 operators' shapes and the registered backward's gradients."""
+    from moe_expert_router_gb300 import binding as B
+    from moe_expert_router_gb300.mx_cache import MxWeightCache
+
+    def shapes_only(w):
+        return torch.empty(w.shape, dtype=torch.uint8, device=w.device), B.mx_scales_empty(w.shape, w.device)
+
+    T, H, I, E, k = 40, 256, 128, 8, 2
+    x = torch.empty((T, H), dtype=torch.bfloat16, device="meta", requires_grad=True)
+    w_r = torch.empty((E, H), dtype=torch.float32, device="meta", requires_grad=True)
+    w1 = torch.empty((E, 2 * I, H), dtype=torch.bfloat16, device="meta", requires_grad=True)
+    w2 = torch.empty((E, H, I), dtype=torch.bfloat16, device="meta", requires_grad=True)
+    cache = MxWeightCache(quantize=shapes_only)
+    y, idx, w, aux = torch_ops.moe_layer(x, w_r, w1, w2, k, precision="mxfp8", weight_cache=cache)
+    assert y.shape == (T, H) and y.requires_grad and len(cache) == 2
+    y.backward(torch.empty_like(y))
+    assert x.grad.shape == x.shape and w_r.grad.shape == w_r.shape
     assert w1.grad.shape == w1.shape and w2.grad.shape == w2.shape
