@@ -33,8 +33,8 @@ class MxWeightCache:
     update through autograd-visible ops), or when ``w`` is not the tensor object
     the entry was made for (a weight freed and another allocated at its address
     starts again at version 0; a detached view is another object and is quantized
-    on its own). ``invalidate()`` drops every entry: call it once per optimizer
-    step.
+    on its own). An entry is dropped when its weight is freed. ``invalidate()``
+    drops every entry: call it once per optimizer step.
     """
 
     def __init__(self, quantize=None):
@@ -55,8 +55,19 @@ class MxWeightCache:
             return hit[2]
         q = self._quantize(w)
         self.quantizations += 1
-        self._store[key] = (weakref.ref(w), w._version, q)
+        self._store[key] = (weakref.ref(w, self._dropper(key)), w._version, q)
         return q
+
+    def _dropper(self, key):
+        # when the weight is freed its entry (and the device memory of its copy) goes
+        # too, unless the key already holds a newer entry
+        store = self._store
+
+        def drop(ref):
+            entry = store.get(key)
+            if entry is not None and entry[0] is ref:
+                del store[key]
+        return drop
 
     def invalidate(self):
         """Drop every cached quantization (once per optimizer step)."""

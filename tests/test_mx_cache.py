@@ -59,3 +59,16 @@ def test_another_tensor_at_the_same_address_is_not_a_hit():
     assert c.quantizations == 2
     c.get(v)
     assert c.quantizations == 2
+
+
+def test_a_freed_weight_drops_its_entry():
+    import gc
+    c = MxWeightCache(quantize=_fake_quantize)
+    w = torch.zeros((2, 4, 64), dtype=torch.bfloat16)
+    keep = torch.ones((2, 4, 64), dtype=torch.bfloat16)
+    c.get(w)
+    c.get(keep)
+    assert len(c) == 2
+    del w
+    gc.collect()
+    assert len(c) == 1 and c.get(keep) is not None and c.quantizations == 2
