@@ -42,11 +42,92 @@ from .mx_cache import MxWeightCache
 _LIB = "moe_gb300"
 
 
+def _expect(t: torch.Tensor, name: str, dtype: torch.dtype, shape) -> None:
+    """The library reads raw pointers: a tensor of another type or size would be
+    misread, so each operator checks its arguments here (also in its shape function)."""
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, not {t.dtype}")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, not {tuple(t.shape)}")
+
+
+def _check_router_args(x, w_r, k, sel_bias, logit_offset):
+    if x.dim() != 2 or w_r.dim() != 2:
+        raise ValueError("x must be [T, H] and w_r [E, H]")
+    T, H = x.shape
+    E = w_r.shape[0]
+    _expect(x, "x", torch.bfloat16, (T, H))
+    _expect(w_r, "w_r", torch.float32, (E, H))
+    if not 1 <= k <= E:
+        raise ValueError(f"k must be in [1, E = {E}], not {k}")
+    for name, t in (("sel_bias", sel_bias), ("logit_offset", logit_offset)):
+        if t is not None:
+            _expect(t, name, torch.float32, (E,))
+
+
+def _check_expert_weights(x, w1, w2):
+    if w1.dim() != 3 or w1.shape[1] % 2:
+        raise ValueError("w1 must be [E, 2I, H]")
+    E, two_i, H = w1.shape
+    if x.shape[1] != H:
+        raise ValueError(f"x has {x.shape[1]} columns, w1 {H}")
+    _expect(w1, "w1", torch.bfloat16, (E, two_i, H))
+    _expect(w2, "w2", torch.bfloat16, (E, H, two_i // 2))
+
+
+def _check_mx_weights(w1, w2, w1_codes, w1_scales, w2_codes, w2_scales):
+    E, two_i, H = w1.shape
+    I = two_i // 2
+    if H % 128 or I % 128:
+        raise ValueError("MXFP8 needs H and I multiples of 128")
+    _expect(w1_codes, "w1_codes", torch.uint8, (E, two_i, H))
+    _expect(w1_scales, "w1_scales", torch.uint8, (H // 128, E, two_i, 4))
+    _expect(w2_codes, "w2_codes", torch.uint8, (E, H, I))
+    _expect(w2_scales, "w2_scales", torch.uint8, (I // 128, E, H, 4))
+
+
+def _check_routing(x, topk_idx, topk_w, E):
+    T = x.shape[0]
+    if topk_idx.dim() != 2:
+        raise ValueError("topk_idx must be [T, k]")
+    k = topk_idx.shape[1]
+    _expect(topk_idx, "topk_idx", torch.int32, (T, k))
+    _expect(topk_w, "topk_w", torch.float32, (T, k))
+    if not 1 <= k <= E:
+        raise ValueError(f"k must be in [1, E = {E}], not {k}")
+
+
+def _check_forward_args(x, topk_idx, topk_w, w1, w2):
+    if x.dim() != 2:
+        raise ValueError("x must be [T, H]")
+    _expect(x, "x", torch.bfloat16, tuple(x.shape))
+    _check_expert_weights(x, w1, w2)
+    _check_routing(x, topk_idx, topk_w, w1.shape[0])
+
+
+def _check_forward_mx_args(x, topk_idx, topk_w, w1_codes, w1_scales, w2_codes, w2_scales):
+    if x.dim() != 2 or w1_codes.dim() != 3:
+        raise ValueError("x must be [T, H] and w1_codes [E, 2I, H]")
+    _expect(x, "x", torch.bfloat16, tuple(x.shape))
+    E, two_i, H = w1_codes.shape
+    if x.shape[1] != H or two_i % 2:
+        raise ValueError("w1_codes must be [E, 2I, H] with H = x.shape[1]")
+    I = two_i // 2
+    if H % 128 or I % 128:
+        raise ValueError("MXFP8 needs H and I multiples of 128")
+    _expect(w1_codes, "w1_codes", torch.uint8, (E, two_i, H))
+    _expect(w1_scales, "w1_scales", torch.uint8, (H // 128, E, two_i, 4))
+    _expect(w2_codes, "w2_codes", torch.uint8, (E, H, I))
+    _expect(w2_scales, "w2_scales", torch.uint8, (I // 128, E, H, 4))
+    _check_routing(x, topk_idx, topk_w, E)
+
+
 @torch.library.custom_op(f"{_LIB}::router", mutates_args=())
 def router(x: torch.Tensor, w_r: torch.Tensor, k: int, score: str = "softmax", normalize: bool = True,
            scale: float = 1.0, n_group: int = 1, topk_group: int = 1, group_topn: int = 2,
            sel_bias: Optional[torch.Tensor] = None,
            logit_offset: Optional[torch.Tensor] = None) -> Tuple[torch.Tensor, torch.Tensor, torch.Tensor]:
+    _check_router_args(x, w_r, k, sel_bias, logit_offset)
     T, H = x.shape
     E = w_r.shape[0]
     shp = B.shape(T, H, 8, E, k)                    # I is not used by the router
@@ -62,6 +143,7 @@ def router(x: torch.Tensor, w_r: torch.Tensor, k: int, score: str = "softmax", n
 @router.register_fake
 def _router_fake(x, w_r, k, score="softmax", normalize=True, scale=1.0, n_group=1, topk_group=1, group_topn=2,
                  sel_bias=None, logit_offset=None):
+    _check_router_args(x, w_r, k, sel_bias, logit_offset)
     T = x.shape[0]
     return (x.new_empty((T, k), dtype=torch.int32), x.new_empty((T, k), dtype=torch.float32),
             x.new_empty((1,), dtype=torch.float32))
@@ -70,6 +152,7 @@ def _router_fake(x, w_r, k, score="softmax", normalize=True, scale=1.0, n_group=
 @torch.library.custom_op(f"{_LIB}::forward", mutates_args=())
 def forward(x: torch.Tensor, topk_idx: torch.Tensor, topk_w: torch.Tensor, w1: torch.Tensor,
             w2: torch.Tensor) -> torch.Tensor:
+    _check_forward_args(x, topk_idx, topk_w, w1, w2)
     T, H = x.shape
     E, two_i, _ = w1.shape
     shp = B.shape(T, H, two_i // 2, E, topk_idx.shape[1])
@@ -81,12 +164,14 @@ def forward(x: torch.Tensor, topk_idx: torch.Tensor, topk_w: torch.Tensor, w1: t
 
 @forward.register_fake
 def _forward_fake(x, topk_idx, topk_w, w1, w2):
+    _check_forward_args(x, topk_idx, topk_w, w1, w2)
     return x.new_empty(x.shape, dtype=torch.bfloat16)
 
 
 @torch.library.custom_op(f"{_LIB}::forward_mx", mutates_args=())
 def forward_mx(x: torch.Tensor, topk_idx: torch.Tensor, topk_w: torch.Tensor, w1_codes: torch.Tensor,
                w1_scales: torch.Tensor, w2_codes: torch.Tensor, w2_scales: torch.Tensor) -> torch.Tensor:
+    _check_forward_mx_args(x, topk_idx, topk_w, w1_codes, w1_scales, w2_codes, w2_scales)
     T, H = x.shape
     E, two_i, _ = w1_codes.shape
     shp = B.shape(T, H, two_i // 2, E, topk_idx.shape[1], mxfp8=True)
@@ -98,6 +183,7 @@ def forward_mx(x: torch.Tensor, topk_idx: torch.Tensor, topk_w: torch.Tensor, w1
 
 @forward_mx.register_fake
 def _forward_mx_fake(x, topk_idx, topk_w, w1_codes, w1_scales, w2_codes, w2_scales):
+    _check_forward_mx_args(x, topk_idx, topk_w, w1_codes, w1_scales, w2_codes, w2_scales)
     return x.new_empty(x.shape, dtype=torch.bfloat16)
 
 
@@ -120,6 +206,8 @@ def layer_train(x: torch.Tensor, w_r: torch.Tensor, w1: torch.Tensor, w2: torch.
                            torch.Tensor]:
     """The layer's training forward: (y, topk_idx, topk_w, aux, h, logits, ws); the last
     three are what layer_backward reads."""
+    _check_router_args(x, w_r, k, sel_bias, logit_offset)
+    _check_expert_weights(x, w1, w2)
     T, H = x.shape
     E, two_i, _ = w1.shape
     I = two_i // 2
@@ -144,6 +232,8 @@ def layer_train(x: torch.Tensor, w_r: torch.Tensor, w1: torch.Tensor, w2: torch.
 @layer_train.register_fake
 def _layer_train_fake(x, w_r, w1, w2, k, score="softmax", normalize=True, scale=1.0, n_group=1, topk_group=1,
                       group_topn=2, sel_bias=None, logit_offset=None):
+    _check_router_args(x, w_r, k, sel_bias, logit_offset)
+    _check_expert_weights(x, w1, w2)
     T, H = x.shape
     E, two_i, _ = w1.shape
     n = B.moe_workspace_size(B.shape(int(T), int(H), int(two_i) // 2, int(E), k, training=True))
@@ -161,6 +251,7 @@ def layer_backward(dy: torch.Tensor, x: torch.Tensor, w_r: torch.Tensor, w1: tor
                    ) -> Tuple[torch.Tensor, torch.Tensor, torch.Tensor, torch.Tensor]:
     """The layer's backward from dY: (dX, dW_r, dW1, dW2). ws is layer_train's workspace
     (its routing metadata and dispatched rows; the backward also uses it as scratch)."""
+    _expect(dy, "dy", torch.bfloat16, tuple(x.shape))
     T, H = x.shape
     E, two_i, _ = w1.shape
     k = topk_idx.shape[1]
@@ -212,6 +303,9 @@ def layer_train_mx(x: torch.Tensor, w_r: torch.Tensor, w1: torch.Tensor, w2: tor
     the router as in bf16, x quantized by the dispatch, stage 1 on the E4M3 copy of w1
     (keeping h), stage 2 on that of w2. w1 and w2 themselves are only read by the
     backward's data gradients."""
+    _check_router_args(x, w_r, k, sel_bias, logit_offset)
+    _check_expert_weights(x, w1, w2)
+    _check_mx_weights(w1, w2, w1_codes, w1_scales, w2_codes, w2_scales)
     T, H = x.shape
     E, two_i, _ = w1.shape
     I = two_i // 2
@@ -240,6 +334,9 @@ def layer_train_mx(x: torch.Tensor, w_r: torch.Tensor, w1: torch.Tensor, w2: tor
 def _layer_train_mx_fake(x, w_r, w1, w2, w1_codes, w1_scales, w2_codes, w2_scales, k, score="softmax",
                          normalize=True, scale=1.0, n_group=1, topk_group=1, group_topn=2, sel_bias=None,
                          logit_offset=None):
+    _check_router_args(x, w_r, k, sel_bias, logit_offset)
+    _check_expert_weights(x, w1, w2)
+    _check_mx_weights(w1, w2, w1_codes, w1_scales, w2_codes, w2_scales)
     T, H = x.shape
     E, two_i, _ = w1.shape
     n = B.moe_workspace_size(B.shape(int(T), int(H), int(two_i) // 2, int(E), k, training=True, mxfp8=True))
@@ -258,6 +355,7 @@ def layer_backward_mx(dy: torch.Tensor, x: torch.Tensor, w_r: torch.Tensor, w1: 
     """layer_backward of layer_train_mx: the data gradients in bf16 (on w1, w2 and the
     saved h), dW2 and dW1 in MXFP8 (both operands quantized along the routed rows), the
     router's gradients as in bf16. Returns (dX, dW_r, dW1, dW2)."""
+    _expect(dy, "dy", torch.bfloat16, tuple(x.shape))
     T, H = x.shape
     E, two_i, _ = w1.shape
     k = topk_idx.shape[1]

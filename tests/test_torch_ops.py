@@ -70,3 +70,40 @@ def test_mx_layer_autograd_shapes():
     y.backward(torch.empty_like(y))
     assert x.grad.shape == x.shape and w_r.grad.shape == w_r.shape
     assert w1.grad.shape == w1.shape and w2.grad.shape == w2.shape
+
+
+def test_operators_refuse_wrong_types_and_shapes():
+    """The library reads raw pointers, so the operators check every argument's type and
+    shape first (in their shape functions too, which run here on meta tensors)."""
+    import pytest
+    T, H, I, E, k = 16, 256, 128, 8, 2
+    m = dict(device="meta")
+    x = torch.empty((T, H), dtype=torch.bfloat16, **m)
+    w_r = torch.empty((E, H), dtype=torch.float32, **m)
+    w1 = torch.empty((E, 2 * I, H), dtype=torch.bfloat16, **m)
+    w2 = torch.empty((E, H, I), dtype=torch.bfloat16, **m)
+    idx = torch.empty((T, k), dtype=torch.int32, **m)
+    w = torch.empty((T, k), dtype=torch.float32, **m)
+    with pytest.raises(TypeError):
+        torch.ops.moe_gb300.router(x.float(), w_r, k)
+    with pytest.raises(TypeError):
+        torch.ops.moe_gb300.router(x, w_r.bfloat16(), k)
+    with pytest.raises(ValueError):
+        torch.ops.moe_gb300.router(x, w_r, E + 1)
+    with pytest.raises(ValueError):
+        torch.ops.moe_gb300.router(x, w_r, k, sel_bias=torch.empty((E + 1,), **m))
+    with pytest.raises(TypeError):
+        torch.ops.moe_gb300.forward(x, idx.long(), w, w1, w2)
+    with pytest.raises(ValueError):
+        torch.ops.moe_gb300.forward(x, idx, w, w1, torch.empty((E, H, I + 8), dtype=torch.bfloat16, **m))
+    with pytest.raises(ValueError):
+        torch.ops.moe_gb300.forward(x[:, :128], idx, w, w1, w2)
+    c1 = torch.empty((E, 2 * I, H), dtype=torch.uint8, **m)
+    s1 = torch.empty((H // 128, E, 2 * I, 4), dtype=torch.uint8, **m)
+    c2 = torch.empty((E, H, I), dtype=torch.uint8, **m)
+    with pytest.raises(ValueError):
+        torch.ops.moe_gb300.forward_mx(x, idx, w, c1, s1, c2, torch.empty((I // 128, E, H, 3), dtype=torch.uint8, **m))
+    with pytest.raises(TypeError):
+        torch_ops.moe_layer(x, w_r, w1.float(), w2, k)
+    with pytest.raises(ValueError):
+        torch_ops.moe_layer(x, w_r, w1, w2, k, precision="fp4")
