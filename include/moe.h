@@ -434,7 +434,10 @@ moe_status_t moe_backward_stage1_weight(const void *x, const moe_shape_t *shape,
 /*
  * The whole backward, in the guide's order: stage 2 (data, weight), the router
  * (skipped when w_r is NULL; then dw_r is not written and logits may be NULL),
- * stage 1 (data, weight). dtopk_w may be NULL when w_r is NULL.
+ * stage 1 (data, weight). With w_r, the arguments logits, cfg, dw_r, topk_idx and
+ * dtopk_w (fp32 [T,k]: the routing-weight gradient, written by stage 2 and read by
+ * the router backward) are all required, else MOE_ERR_INVALID_ARG; without w_r,
+ * dtopk_w may be NULL.
  */
 moe_status_t moe_backward(const void *x, const float *w_r, const float *logits,
                           const int32_t *topk_idx, const float *topk_w, const void *w1,
